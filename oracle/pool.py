@@ -1,0 +1,179 @@
+"""Pure-Python model of the paged-KV block pool.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  It restates the
+bookkeeping the pages describe, step by step, so the native pool can be checked
+against it operation by operation:
+
+* fixed-size physical blocks in one global pool with a free list; a finished
+  sequence returns its blocks to the free list ("vLLM: treating the KV cache as
+  virtual memory", section "碎片从哪里来"; "留书阁 / knowledge-20" page,
+  section "PagedAttention：虚实分离，按需取用");
+* lazy allocation: a physical block is taken only when generation reaches the
+  first slot of a new logical block (OS-lab appendix, section 3.3; same
+  page-3 section: "after the first 16 tokens are full, take the next block");
+* reference counts: sharing a block increments its count, finishing a holder
+  decrements it, the block goes back to the free list only at zero ("第 6 章
+  缓存管理", section "块表长什么样");
+* fork copies the block table, not the data, and bumps every refcount
+  (page 2, section "碎片从哪里来"; OS-lab appendix, section 4.3);
+* copy-on-write: appending into a block whose refcount is above one first
+  moves the writer onto a fresh private copy (source refcount - 1, copy
+  refcount 1); the last remaining holder writes in place (OS-lab appendix,
+  section 4.4; page 3, section "写时复制与前缀缓存");
+* prefix sharing: a new request's table starts with the first
+  ``ceil(n / block_size)`` entries of another request's table (page 4, section
+  "块表长什么样": a 200-token shared prefix gives 13 shared entries);
+* pinning: a prefix-cache block stays out of the free list even at refcount
+  zero (page 2, section "碎片从哪里来": hot prefixes are kept outside the free
+  list).
+
+Policy choices the pages leave open (both implementations follow them so their
+tables can be compared bit for bit):
+
+* the free list is a stack (LIFO); it starts as ``initial_order`` with
+  ``initial_order[0]`` handed out first;
+* freeing a sequence releases its blocks from the last logical block to the
+  first;
+* sequence ids count up from 0 and are never reused.
+"""
+
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+
+class NoBlocks(Exception):
+    """The pool has no free block left (page 4, "缓存放不下的时候": reject)."""
+
+
+@dataclass
+class _Seq:
+    table: list = field(default_factory=list)
+    ctx: int = 0
+
+
+class BlockPool:
+    def __init__(self, num_blocks: int, block_size: int = 16, initial_order=None):
+        if num_blocks <= 0 or block_size <= 0:
+            raise ValueError("num_blocks and block_size must be positive")
+        order = list(range(num_blocks)) if initial_order is None else [int(x) for x in initial_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise ValueError("initial_order must be a permutation of range(num_blocks)")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.free = list(reversed(order))          # top of the stack is the end
+        self.refcount = [0] * num_blocks
+        self.pinned = [False] * num_blocks
+        self.seqs: dict[int, _Seq] = {}
+        self.next_id = 0
+        self.cow_copies = 0
+
+    # -- internal -----------------------------------------------------------
+    def _alloc(self) -> int:
+        if not self.free:
+            raise NoBlocks()
+        block = self.free.pop()
+        self.refcount[block] = 1
+        return block
+
+    def _release(self, block: int) -> None:
+        self.refcount[block] -= 1
+        if self.refcount[block] == 0 and not self.pinned[block]:
+            self.free.append(block)
+
+    def _seq(self, seq_id: int) -> _Seq:
+        if seq_id not in self.seqs:
+            raise KeyError(seq_id)
+        return self.seqs[seq_id]
+
+    # -- operations ---------------------------------------------------------
+    def new_seq(self) -> int:
+        seq_id = self.next_id
+        self.next_id += 1
+        self.seqs[seq_id] = _Seq()
+        return seq_id
+
+    def append_slot(self, seq_id: int):
+        """Reserve the slot of the sequence's next token.
+
+        Returns ``(slot, cow)`` where ``slot = physical * block_size + offset``
+        and ``cow`` is ``(src, dst)`` when a copy-on-write happened, else None.
+        """
+        seq = self._seq(seq_id)
+        logical, offset = divmod(seq.ctx, self.block_size)
+        cow = None
+        if offset == 0:
+            block = self._alloc()
+            seq.table.append(block)
+        else:
+            block = seq.table[logical]
+            if self.refcount[block] > 1:
+                fresh = self._alloc()
+                self.refcount[block] -= 1
+                seq.table[logical] = fresh
+                cow = (block, fresh)
+                self.cow_copies += 1
+                block = fresh
+        seq.ctx += 1
+        return block * self.block_size + offset, cow
+
+    def fork(self, parent_id: int) -> int:
+        parent = self._seq(parent_id)
+        child_id = self.new_seq()
+        child = self.seqs[child_id]
+        child.table = list(parent.table)
+        child.ctx = parent.ctx
+        for block in child.table:
+            self.refcount[block] += 1
+        return child_id
+
+    def share_prefix(self, src_id: int, dst_id: int, num_tokens: int) -> None:
+        src, dst = self._seq(src_id), self._seq(dst_id)
+        if dst.ctx != 0 or dst.table:
+            raise ValueError("destination must be an empty sequence")
+        if num_tokens <= 0 or num_tokens > src.ctx:
+            raise ValueError("num_tokens must be in 1..src context length")
+        count = -(-num_tokens // self.block_size)
+        dst.table = list(src.table[:count])
+        dst.ctx = num_tokens
+        for block in dst.table:
+            self.refcount[block] += 1
+
+    def pin(self, seq_id: int, num_tokens: int) -> None:
+        seq = self._seq(seq_id)
+        if num_tokens < 0 or num_tokens > seq.ctx:
+            raise ValueError("num_tokens must be in 0..context length")
+        for block in seq.table[:-(-num_tokens // self.block_size)]:
+            self.pinned[block] = True
+
+    def unpin(self, block: int) -> None:
+        if not self.pinned[block]:
+            raise ValueError("block is not pinned")
+        self.pinned[block] = False
+        if self.refcount[block] == 0:
+            self.free.append(block)
+
+    def free_seq(self, seq_id: int) -> None:
+        seq = self._seq(seq_id)
+        for block in reversed(seq.table):
+            self._release(block)
+        del self.seqs[seq_id]
+
+    # -- queries ------------------------------------------------------------
+    def block_table(self, seq_id: int):
+        seq = self._seq(seq_id)
+        return list(seq.table), seq.ctx
+
+    def stats(self) -> dict:
+        live = self.seqs.values()
+        return {
+            "num_blocks": self.num_blocks,
+            "free_blocks": len(self.free),
+            "used_blocks": sum(1 for rc in self.refcount if rc > 0),
+            "pinned_blocks": sum(1 for p in self.pinned if p),
+            "shared_blocks": sum(1 for rc in self.refcount if rc > 1),
+            "cow_copies": self.cow_copies,
+            "live_seqs": len(self.seqs),
+            "tokens": sum(s.ctx for s in live),
+            "internal_frag_slots": sum(len(s.table) * self.block_size - s.ctx for s in live),
+        }
