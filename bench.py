@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode hot path on GB300.
+
+One step = one decode step of the whole hot path over one batch: for every
+layer, kv_append of the batch's new K/V rows into their paged slots, then
+paged decode attention over the block tables (copy-on-write block copies are
+part of the path but the default workload never forks, so none are due).
+
+Default workload: 7B-shaped MHA decode -- batch 64, 32 query / 32 KV heads,
+head_dim 128, fp16, block size 16, context lengths log-uniform in [16, 2048],
+block tables as random disjoint draws from a pool of the needed blocks + 10 %,
+32 layers with separate caches (timed as 32 calls each of append and
+attention).  ``--workload gqa_8b`` runs the 8B-shaped GQA batch (128 sequences,
+32 / 8 heads, bf16, lengths log-uniform in [128, 8192] plus 4 x 8192, one layer).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
+reference arm of this method: there is no other implementation) on bounded
+samples of the same workload.
+"""
+
+from __future__ import annotations
+
+import os
+
+# The oracle baseline is timed single-threaded; pin BLAS before numpy loads.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import math  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import time  # noqa: E402
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from pagedattention_decode_attention_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged decode attention tokens/s and KV-read GB/s (% of GB300 HBM peak), 1 GPU"
+DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+ELEM = {"f16": 2, "bf16": 2, "f32": 4}
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b"], default="mha_7b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def make_batch(name: str, rank: int) -> wl.DecodeBatch:
+    # each rank decodes its own independent batch (replicas; no exchange)
+    if name == "mha_7b":
+        return wl.mha_7b(seed=wl.SEED_BASE + 2 + 100 * rank)
+    return wl.gqa_8b(seed=wl.SEED_BASE + 3 + 100 * rank)
+
+
+def algorithmic_bytes(batch: wl.DecodeBatch) -> dict:
+    """Bytes one attention call must move at minimum: the K and V rows of every
+    attended token, the queries, the outputs, the used table entries and the
+    context lengths."""
+    e = ELEM[batch.dtype]
+    toks = int(batch.context_lens.astype(np.int64).sum())
+    kv = toks * 2 * batch.num_kv_heads * batch.head_dim * e
+    qo = 2 * batch.num_seqs * batch.num_q_heads * batch.head_dim * e
+    tables = int(wl.num_blocks_for(batch.context_lens).sum()) * 4 + batch.num_seqs * 4
+    return {"kv": kv, "total": kv + qo + tables, "tokens": toks}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "pagedattention_decode_attention_gb300", "csrc")
+    for name in ("decode.cu", "decode.cuh", "device_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"decode_attention_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != kernel_source_hash():
+        return None
+    return float(val.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- ours
+class Replica:
+    """Device-resident inputs of one decode step of the workload."""
+
+    def __init__(self, batch: wl.DecodeBatch, device):
+        import pagedattention_decode_attention_gb300 as pa
+        self.pa = pa
+        self.batch = batch
+        self.device = device
+        dt = DTYPES[batch.dtype]
+        b, hq, hkv, d, nb = (batch.num_seqs, batch.num_q_heads, batch.num_kv_heads,
+                             batch.head_dim, batch.num_blocks)
+        L = batch.num_layers
+        s = batch.seed * 1000
+        self.k_cache = [wl.normal((nb, hkv, 16, d), dt, s + 4 * i, device) for i in range(L)]
+        self.v_cache = [wl.normal((nb, hkv, 16, d), dt, s + 4 * i + 1, device) for i in range(L)]
+        self.q = wl.normal((L, b, hq, d), dt, s + 7, device)
+        self.k_new = wl.normal((L, b, hkv, d), dt, s + 8, device)
+        self.v_new = wl.normal((L, b, hkv, d), dt, s + 9, device)
+        self.out = torch.empty((L, b, hq, d), dtype=dt, device=device)
+        self.tables = torch.from_numpy(batch.block_tables).to(device)
+        self.lens = torch.from_numpy(batch.context_lens).to(device)
+        self.slots = torch.from_numpy(batch.new_token_slots()).to(device)
+        self.ws = pa.alloc_workspace(b, hq, hkv, d, batch.max_blocks, device)
+        self.scale = batch.scale
+        self.launches_per_step = 3 * L       # kv_append + plan + attention per layer
+
+    def step(self, ev=None):
+        pa, L = self.pa, self.batch.num_layers
+        for layer in range(L):
+            pa.kv_append(self.k_new[layer], self.v_new[layer], self.k_cache[layer],
+                         self.v_cache[layer], self.slots)
+            if ev is not None:
+                ev[layer][0].record()
+            pa.paged_attention_decode(self.q[layer], self.k_cache[layer], self.v_cache[layer],
+                                      self.tables, self.lens, self.scale, out=self.out[layer],
+                                      workspace=self.ws)
+            if ev is not None:
+                ev[layer][1].record()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_steps(rep: Replica, steps: int, world: int, events: bool):
+    """Times `steps` steps between two barriers; returns (seconds, per-launch
+    attention durations in ms)."""
+    L = rep.batch.num_layers
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in range(L)] for _ in range(steps)] if events else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(steps):
+        rep.step(ev[i] if ev else None)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    secs = start.elapsed_time(end) / 1e3
+    per = [a.elapsed_time(b) for step_ev in ev for a, b in step_ev] if ev else []
+    return secs, per
+
+
+def time_e2e(rep: Replica, steps: int, world: int):
+    """Same steps with every step's inputs copied in from pinned host memory and
+    the outputs read back, inside the timed region."""
+    host_q = rep.q.cpu().pin_memory()
+    host_k = rep.k_new.cpu().pin_memory()
+    host_v = rep.v_new.cpu().pin_memory()
+    host_tab = rep.tables.cpu().pin_memory()
+    host_len = rep.lens.cpu().pin_memory()
+    host_slot = rep.slots.cpu().pin_memory()
+    host_out = torch.empty(rep.out.shape, dtype=rep.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v, host_tab, host_len, host_slot))
+    d2h = host_out.numel() * host_out.element_size()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record()
+    for _ in range(steps):
+        rep.q.copy_(host_q, non_blocking=True)
+        rep.k_new.copy_(host_k, non_blocking=True)
+        rep.v_new.copy_(host_v, non_blocking=True)
+        rep.tables.copy_(host_tab, non_blocking=True)
+        rep.lens.copy_(host_len, non_blocking=True)
+        rep.slots.copy_(host_slot, non_blocking=True)
+        rep.step()
+        host_out.copy_(rep.out, non_blocking=True)
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    return start.elapsed_time(end) / 1e3, h2d, d2h
+
+
+def cpu_oracle_sample(batch: wl.DecodeBatch, rep: Replica | None, seconds: float, step_units=None):
+    """Times the oracle on (sequence, layer) units of the workload.  A unit is one
+    sequence's attention over all query heads for one layer; 32 units of the
+    7B workload (its layer count) make one decoded token.  Returns
+    (tokens/s, units done, elapsed s, sequences used)."""
+    import oracle.attention as oa
+    if rep is not None:
+        kc = rep.k_cache[0].float().cpu().numpy()
+        vc = rep.v_cache[0].float().cpu().numpy()
+        q = rep.q[0].float().cpu().numpy()
+    else:
+        shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
+        gen = np.random.default_rng(batch.seed)
+        kc = gen.standard_normal(shape, dtype=np.float32)
+        vc = gen.standard_normal(shape, dtype=np.float32)
+        q = gen.standard_normal((batch.num_seqs, batch.num_q_heads, batch.head_dim), dtype=np.float32)
+    order = np.random.default_rng(7).permutation(batch.num_seqs)
+    units, t0, i = 0, time.perf_counter(), 0
+    while True:
+        b = int(order[i % batch.num_seqs])
+        oa.paged_attention_decode(q, kc, vc, batch.block_tables, batch.context_lens, batch.scale,
+                                  seqs=[b])
+        units += 1
+        i += 1
+        el = time.perf_counter() - t0
+        if (step_units is not None and units >= step_units) or (step_units is None and el >= seconds):
+            break
+    return units / batch.num_layers / el, units, el
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    batch = make_batch(args.workload, rank)
+    rep = Replica(batch, device)
+    for _ in range(max(args.warmup, 3)):
+        rep.step()
+    rep.pa.check_status()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    secs, per_launch = time_steps(rep, args.steps, world, events=True)
+    clk = clocks.stop()
+    rep.pa.check_status()
+    secs = max_over_ranks(secs, world)
+    tokens_per_step = batch.num_seqs * world
+    value = tokens_per_step * args.steps / secs
+
+    ab = algorithmic_bytes(batch)
+    avg_ms = statistics.mean(per_launch)
+    achieved = ab["total"] / (avg_ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    traffic = profiled_traffic(args.workload)
+
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            rep.step()
+        e_secs, h2d, d2h = time_e2e(rep, args.steps, world)
+        e_secs = max_over_ranks(e_secs, world)
+        e2e = {"value": tokens_per_step * args.steps / e_secs, "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, units, el = cpu_oracle_sample(batch, rep, args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": (f"{units} (sequence, layer) attention units of layer 0, all "
+                          f"{batch.num_q_heads} query heads each, float64 numpy on 1 host "
+                          f"thread in {el:.1f} s; {batch.num_layers} units = 1 token")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
+            "data": "synthetic (seeded N(0,1) K/V/Q, seeded lengths and placements)",
+            "config": {
+                "workload": batch.name, "num_seqs": batch.num_seqs,
+                "num_q_heads": batch.num_q_heads, "num_kv_heads": batch.num_kv_heads,
+                "head_dim": batch.head_dim, "block_size": 16, "layers": batch.num_layers,
+                "context_tokens": ab["tokens"], "num_blocks_per_layer": batch.num_blocks,
+                "l2": (f"inputs larger than L2: {ab['kv'] * batch.num_layers / 1e9:.2f} GB of KV "
+                       f"read per step across {batch.num_layers} separate layer caches"),
+                "step": "per layer: kv_append of the new K/V rows, then paged decode attention",
+                "parallelism": f"replicas x{world} (independent batches, no collective)",
+            },
+            "kv_read_gbs": ab["kv"] / (avg_ms / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": "paged_attention_decode call (plan + attention kernels)",
+                         "algorithmic_bytes_per_launch": ab["total"],
+                         "avg_launch_ms": avg_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": rep.launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- reference
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    batch = make_batch(args.workload, 0)
+    per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
+    for _ in range(max(args.warmup, 3)):
+        cpu_oracle_sample(batch, None, 0.0, step_units=1)
+    t0 = time.perf_counter()
+    units = 0
+    for _ in range(args.steps):
+        _, u, _ = cpu_oracle_sample(batch, None, 0.0, step_units=per_step_units)
+        units += u
+    secs = time.perf_counter() - t0
+    value = units / batch.num_layers / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": batch.name, "num_seqs": batch.num_seqs,
+                   "num_q_heads": batch.num_q_heads, "num_kv_heads": batch.num_kv_heads,
+                   "head_dim": batch.head_dim, "block_size": 16, "layers": batch.num_layers},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": (f"each step: {per_step_units} (sequence, layer) units "
+                                    "(one token) of the workload, float64 numpy, 1 thread")},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

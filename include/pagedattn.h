@@ -1,0 +1,243 @@
+/*
+ * pagedattn.h -- C ABI of the GB300 paged-KV decode library.
+ *
+ * What it computes.  Decode-time scaled dot-product attention of each
+ * sequence's single new query against its key/value cache, where the cache is
+ * stored as fixed 16-token physical blocks and a per-sequence block table maps
+ * logical block i to a physical block ("vLLM: treating the KV cache as virtual
+ * memory", section 破除误解: the formula is unchanged, only the layout; the
+ * kernel follows the block table with one indirection per block).  Around it:
+ * writing each step's new K/V rows into their paged slots, copying whole
+ * blocks for copy-on-write, and a host-side block pool that produces the
+ * tables.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every function returns an int status (pa_status).  On a non-zero status
+ *   pa_last_error() returns a message for the calling thread.
+ * - Device pointers are raw CUDA device addresses owned by the caller.  The
+ *   library never allocates, frees or retains device memory, and keeps no
+ *   pointer after a call returns.  Host pointers are read (or written) during
+ *   the call only.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Device work is enqueued asynchronously on it; a PA_OK return means the
+ *   work was validated and launched, not that it finished.
+ * - Host-side validation (shapes, dtype, alignment, pointer presence) happens
+ *   before any launch; a failing check launches nothing.
+ * - Data-dependent checks (block ids, slots, context lengths read on the
+ *   device) never fault: an out-of-range value is clamped or skipped and a
+ *   device status word is set.  pa_check_status() reads and clears it.
+ *   Every device-side wait is bounded; a wait that runs out sets
+ *   PA_ERR_DEVICE_TIMEOUT in the same word instead of hanging.
+ * - Element types: PA_F32, PA_F16, PA_BF16.  Caches, queries, new K/V and the
+ *   output all share one dtype per call.  head_dim is 64 or 128.
+ *
+ * Layouts (row-major, contiguous)
+ * -------------------------------
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][16][head_dim]
+ *                      (one (block, head) tile = 16 * head_dim elements,
+ *                       contiguous; physical block p, token offset o of head h
+ *                       is element ((p * num_kv_heads + h) * 16 + o) * head_dim)
+ *   q, out           : [num_seqs][num_q_heads][head_dim]
+ *   k, v (new rows)  : [num_tokens][num_kv_heads][head_dim]
+ *   block_tables     : int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens     : int32 [num_seqs]
+ *   slot_mapping     : int64 [num_tokens], slot = physical_block * 16 + offset
+ *   src_dst_pairs    : int64 [num_pairs][2]
+ *
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads) (contiguous
+ * groups; GQA when the ratio exceeds one).
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#define PA_BLOCK_SIZE 16
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,    /* bad shape, pointer, alignment or workspace size */
+  PA_ERR_UNSUPPORTED = 2,    /* dtype, head_dim or head grouping not built */
+  PA_ERR_NO_BLOCKS = 3,      /* pool exhausted (reject / queue is the caller's policy) */
+  PA_ERR_CUDA = 4,           /* a CUDA runtime call failed; see pa_last_error() */
+  PA_ERR_DEVICE_BOUNDS = 5,  /* a kernel saw an out-of-range block id / slot / length */
+  PA_ERR_DEVICE_TIMEOUT = 6, /* a bounded device-side wait ran out */
+  PA_ERR_NOT_FOUND = 7       /* unknown sequence id or block (pool) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Message describing the last non-zero status returned on this thread. */
+PA_API const char* pa_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+PA_API int pa_version(void);
+
+/* ------------------------------------------------------------------------
+ * pa_kv_append -- write the new tokens' K/V rows into their paged slots.
+ *
+ * OS-lab appendix "Lazy Allocation 与 Copy-on-Write 在 LLM 推理系统中的应用",
+ * section 2.1 (each decode step appends the new token's key/value) and the
+ * "留书阁 / knowledge-20" page, section "PagedAttention：虚实分离，按需取用"
+ * (logical block -> physical block; a token's slot is physical * 16 + offset).
+ *
+ * For every i < num_tokens with slot_mapping[i] >= 0:
+ *   k_cache[slot / 16][h][slot % 16][:] = k[i][h][:]   for all h, likewise v.
+ * A negative slot is a padding token and is skipped.  A slot >= num_blocks*16
+ * is skipped and sets PA_ERR_DEVICE_BOUNDS.  Bit-exact copy.  Two tokens
+ * mapping to the same slot race (the pool never produces that).
+ * k, v, k_cache, v_cache must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
+                        const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                        int head_dim, int num_blocks, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_workspace_size -- bytes of device workspace that
+ * pa_paged_attention_decode needs for these sizes (split partial results,
+ * the work list and per-(sequence, KV head) arrival counters).
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_workspace_size(int num_seqs, int num_q_heads,
+                                                    int num_kv_heads, int head_dim,
+                                                    int max_blocks_per_seq, size_t* bytes);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_attention_decode -- one decode step of attention over paged K/V.
+ *
+ * "vLLM: treating the KV cache as virtual memory", sections 破除误解 and
+ * "KV 的体积从哪来，页表如何把它切开" (loop over blocks doing Q x K/V
+ * multiply-add, then reduce across blocks); "留书阁 / knowledge-20" page,
+ * section 注意力计算的改写 (the contiguous reference softmax(QK^T/sqrt(d))V).
+ *
+ * For each sequence b and query head h, with G = num_q_heads/num_kv_heads,
+ * g = h / G, n = context_lens[b] and phys(t) = block_tables[b][t / 16]:
+ *   s_t = scale * q[b][h] . k_cache[phys(t)][g][t % 16],  t < n
+ *   out[b][h] = sum_t softmax(s)_t * v_cache[phys(t)][g][t % 16]
+ * n == 0 gives a zero row.  Accumulation is fp32 (bf16/fp16 inputs use the
+ * tensor cores for the two contractions, the probabilities are rounded to the
+ * input type before the P.V product); fp32 inputs run on the CUDA cores.
+ * Results do not depend on where the blocks sit physically.
+ *
+ * Preconditions checked on the host: G in 1..8 for F16/BF16 (any G for F32),
+ * head_dim in {64, 128}, 16-byte aligned tensors, workspace_bytes at least
+ * the size pa_paged_attention_decode_workspace_size() reports.  Checked on
+ * the device: 0 <= n <= max_blocks_per_seq * 16 and every table entry read
+ * in [0, num_blocks) -- a violation is clamped and sets PA_ERR_DEVICE_BOUNDS.
+ *
+ * The workspace belongs to one call at a time: two calls sharing it must be
+ * ordered on the same stream.  It needs no initialisation.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int max_blocks_per_seq, int num_blocks,
+                                     float scale, int dtype, void* out, void* workspace,
+                                     size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * pa_block_copy -- copy-on-write block copies, all layers in one launch.
+ *
+ * OS-lab appendix, sections 4.3-4.4 (when the target block's refcount is
+ * above one, copy it for the writer first); "第 6 章 缓存管理", section
+ * 块表长什么样 (modify a copy, never the shared block).
+ *
+ * k_caches / v_caches: HOST arrays of num_layers device pointers, each a
+ * cache as laid out above.  src_dst_pairs: DEVICE int64 [num_pairs][2].
+ * For every pair and layer: k_caches[l][dst] = k_caches[l][src] (the whole
+ * num_kv_heads * 16 * head_dim block), likewise v.  Pairs run concurrently:
+ * no dst may repeat or appear as another pair's src (the pool's pairs for one
+ * step satisfy this).  Ids outside [0, num_blocks) skip that pair and set
+ * PA_ERR_DEVICE_BOUNDS.  num_layers <= 256.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_layers,
+                         const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads,
+                         int head_dim, int num_blocks, int dtype, void* stream);
+
+/* ------------------------------------------------------------------------
+ * pa_check_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device.  Returns PA_OK, PA_ERR_DEVICE_BOUNDS or
+ * PA_ERR_DEVICE_TIMEOUT (or PA_ERR_CUDA if the synchronisation failed).
+ * ---------------------------------------------------------------------- */
+PA_API int pa_check_status(void* stream);
+
+/* ========================================================================
+ * Host block pool.  Produces block tables, slots and copy-on-write pairs;
+ * touches no device memory.  Not thread-safe: one pool per thread or
+ * external locking.
+ *
+ * Semantics ("vLLM: treating the KV cache as virtual memory", section
+ * 碎片从哪里来; "第 6 章 缓存管理", section 块表长什么样; OS-lab appendix
+ * sections 3.3 and 4.3-4.4; "留书阁 / knowledge-20" page, section
+ * 写时复制与前缀缓存):
+ *  - free list is a stack; it starts as initial_order (initial_order[0] is
+ *    handed out first; NULL = 0, 1, 2, ...);
+ *  - a block is taken only when a sequence's next token starts a new logical
+ *    block (lazy allocation);
+ *  - fork and share_prefix copy table entries and raise refcounts;
+ *  - appending into a block whose refcount is above one moves the writer to
+ *    a fresh block and reports the (src, dst) pair to copy; the last holder
+ *    writes in place;
+ *  - a block returns to the free list when its refcount reaches zero, unless
+ *    pinned (prefix cache);
+ *  - freeing a sequence releases its blocks from the last logical block to
+ *    the first; sequence ids count up from 0 and are never reused.
+ * ====================================================================== */
+typedef struct pa_pool pa_pool;
+
+typedef struct pa_pool_stats_t {
+  int64_t num_blocks;
+  int64_t free_blocks;
+  int64_t used_blocks;         /* refcount > 0 */
+  int64_t pinned_blocks;
+  int64_t shared_blocks;       /* refcount > 1 */
+  int64_t cow_copies;          /* cumulative copy-on-write pairs produced */
+  int64_t live_seqs;
+  int64_t tokens;              /* sum of live context lengths */
+  int64_t internal_frag_slots; /* sum over live seqs of table slots minus tokens */
+} pa_pool_stats_t;
+
+/* block_size >= 1 (device kernels accept only 16; other sizes serve host
+ * bookkeeping).  initial_order: NULL or a permutation of 0..num_blocks-1. */
+PA_API int pa_pool_create(int num_blocks, int block_size, const int32_t* initial_order,
+                          pa_pool** pool);
+PA_API int pa_pool_destroy(pa_pool* pool);
+PA_API int pa_pool_new_seq(pa_pool* pool, int* seq_id);
+/* Reserve the slot of `seq`'s next token.  *cow_src / *cow_dst receive the
+ * block pair to copy before writing, or -1 / -1.  PA_ERR_NO_BLOCKS leaves the
+ * pool unchanged. */
+PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* cow_src,
+                               int64_t* cow_dst);
+/* Batched form: one slot per entry of seqs[0..n), written to slots[] and the
+ * copy pairs (if any) appended to pairs[] (int64 [*num_pairs][2], capacity
+ * pair_cap).  Stops at the first error; *done tells how many succeeded. */
+PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64_t* slots,
+                                int64_t* pairs, int pair_cap, int* num_pairs, int* done);
+PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child);
+PA_API int pa_pool_share_prefix(pa_pool* pool, int src_seq, int dst_seq, int num_tokens);
+PA_API int pa_pool_pin(pa_pool* pool, int seq, int num_tokens);
+PA_API int pa_pool_unpin(pa_pool* pool, int block);
+PA_API int pa_pool_free_seq(pa_pool* pool, int seq);
+/* Copies up to `cap` table entries to out[] (may be NULL when cap == 0);
+ * *n receives the full table length and *ctx_len the context length. */
+PA_API int pa_pool_block_table(pa_pool* pool, int seq, int32_t* out, int cap, int* n,
+                               int* ctx_len);
+PA_API int pa_pool_refcount(pa_pool* pool, int block, int* rc);
+PA_API int pa_pool_stats(pa_pool* pool, pa_pool_stats_t* stats);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

@@ -1,0 +1,21 @@
+"""GB300-native paged-KV decode attention.
+
+Device entry points (hand-written sm_103a kernels behind the C ABI in
+``include/pagedattn.h``):
+
+* :func:`kv_append` -- write new tokens' K/V rows into their paged slots;
+* :func:`paged_attention_decode` -- one decode step of attention over a block
+  table, MHA and GQA;
+* :func:`block_copy` -- copy-on-write block copies across all layers;
+
+and the native host :class:`BlockPool` that produces tables, slots and copy
+pairs.  The library is loaded on first use; if it has not been built the call
+raises -- there is no fallback implementation.
+"""
+
+from .capi import PagedAttnError  # noqa: F401
+from .ops import (alloc_workspace, block_copy, check_status, kv_append,  # noqa: F401
+                  paged_attention_decode, workspace_size)
+from .pool import BlockPool  # noqa: F401
+
+BLOCK_SIZE = 16

@@ -1,0 +1,192 @@
+// kv_append and block_copy: the two bit-copy paths around decode attention,
+// plus the per-device status word and pa_check_status.
+//
+// kv_append follows the OS-lab appendix "Lazy Allocation 与 Copy-on-Write 在
+// LLM 推理系统中的应用", section 2.1 (each decode step appends the new
+// token's K/V) with slots numbered physical * 16 + offset as in the
+// "留书阁 / knowledge-20" block-table example.  block_copy follows the same
+// appendix, section 4.4 (the writer gets a private copy of a shared block).
+//
+// Both are pure data movement: 16-byte vector loads/stores, one thread per
+// 16-byte chunk, consecutive threads on consecutive chunks of a row so every
+// warp moves whole 128-byte lines.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "pagedattn.h"
+#include "status.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned g_status_word;  // one per device; zero at module load
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxLayers = 256;
+constexpr int kBlockSize = 16;
+
+struct StatusSlot {
+  std::once_flag once;
+  unsigned* addr = nullptr;
+};
+StatusSlot g_slots[kMaxDevices];
+
+__global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                 uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                 const int64_t* __restrict__ slots, int64_t total_vecs,
+                                 int heads_vecs, int row_vecs, int64_t num_slots,
+                                 unsigned* status) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t t = i / heads_vecs;
+    const int rem = int(i - t * heads_vecs);
+    const int h = rem / row_vecs, c = rem - h * row_vecs;
+    const int64_t slot = slots[t];
+    if (slot < 0) continue;  // padding token
+    if (slot >= num_slots) {
+      dev::flag_status(status, kStatusBounds);
+      continue;
+    }
+    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+    const int64_t num_heads = heads_vecs / row_vecs;
+    const int64_t dst = ((blk * num_heads + h) * kBlockSize + off) * row_vecs + c;
+    k_cache[dst] = k[i];
+    v_cache[dst] = v[i];
+  }
+}
+
+struct LayerPtrs {
+  uint4* k[kMaxLayers];
+  uint4* v[kMaxLayers];
+};
+
+__global__ void block_copy_kernel(const __grid_constant__ LayerPtrs ptrs,
+                                  const int64_t* __restrict__ pairs, int block_vecs,
+                                  int64_t num_blocks, unsigned* status) {
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int64_t src = pairs[2 * int64_t(pair)], dst = pairs[2 * int64_t(pair) + 1];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0) dev::flag_status(status, kStatusBounds);
+    return;
+  }
+  if (src == dst) return;
+  uint4* base = blockIdx.z == 0 ? ptrs.k[layer] : ptrs.v[layer];
+  const uint4* from = base + src * block_vecs;
+  uint4* to = base + dst * block_vecs;
+  for (int i = threadIdx.x; i < block_vecs; i += blockDim.x) to[i] = from[i];
+}
+
+int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+
+int check_common(int dtype, int head_dim, int num_kv_heads, int num_blocks, const char* who) {
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "%s: unknown dtype %d", who, dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d (64 or 128)", who, head_dim);
+  if (num_kv_heads <= 0 || num_blocks <= 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: num_kv_heads and num_blocks must be positive", who);
+  return PA_OK;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
+
+}  // namespace
+
+unsigned* device_status_word() {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices) {
+    fail(PA_ERR_CUDA, "no current CUDA device");
+    return nullptr;
+  }
+  StatusSlot& slot = g_slots[device];
+  std::call_once(slot.once, [&] {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) == cudaSuccess)
+      slot.addr = static_cast<unsigned*>(addr);
+  });
+  if (!slot.addr) fail(PA_ERR_CUDA, "cudaGetSymbolAddress of the status word failed");
+  return slot.addr;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
+                        const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                        int head_dim, int num_blocks, int dtype, void* stream) {
+  int rc = check_common(dtype, head_dim, num_kv_heads, num_blocks, "kv_append");
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "kv_append: num_tokens < 0");
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "kv_append: NULL pointer");
+  if (misaligned(k) || misaligned(v) || misaligned(k_cache) || misaligned(v_cache))
+    return fail(PA_ERR_INVALID_ARG, "kv_append: tensors must be 16-byte aligned");
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const int row_vecs = head_dim * elem_bytes(dtype) / 16;
+  const int heads_vecs = num_kv_heads * row_vecs;
+  const int64_t total = int64_t(num_tokens) * heads_vecs;
+  const int threads = 256;
+  const int64_t want = (total + threads - 1) / threads;
+  const int blocks = int(want < 65535 * 16 ? want : 65535 * 16);
+  kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), slot_mapping, total, heads_vecs, row_vecs,
+      int64_t(num_blocks) * kBlockSize, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "kv_append: launch failed: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_layers,
+                         const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads,
+                         int head_dim, int num_blocks, int dtype, void* stream) {
+  int rc = check_common(dtype, head_dim, num_kv_heads, num_blocks, "block_copy");
+  if (rc != PA_OK) return rc;
+  if (num_pairs < 0 || num_layers < 0 || num_layers > kMaxLayers)
+    return fail(PA_ERR_INVALID_ARG, "block_copy: num_pairs < 0 or num_layers outside 0..%d",
+                kMaxLayers);
+  if (num_pairs == 0 || num_layers == 0) return PA_OK;
+  if (!k_caches || !v_caches || !src_dst_pairs)
+    return fail(PA_ERR_INVALID_ARG, "block_copy: NULL pointer");
+  LayerPtrs ptrs = {};
+  for (int l = 0; l < num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l] || misaligned(k_caches[l]) || misaligned(v_caches[l]))
+      return fail(PA_ERR_INVALID_ARG, "block_copy: layer %d cache pointer NULL or unaligned", l);
+    ptrs.k[l] = static_cast<uint4*>(k_caches[l]);
+    ptrs.v[l] = static_cast<uint4*>(v_caches[l]);
+  }
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const int block_vecs = num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype) / 16;
+  dim3 grid(num_pairs, num_layers, 2);
+  block_copy_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      ptrs, src_dst_pairs, block_vecs, num_blocks, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "block_copy: launch failed: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+PA_API int pa_check_status(void* stream) {
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  unsigned word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(&word, status, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "check_status: %s", cudaGetErrorString(e));
+  if (word & kStatusTimeout)
+    return fail(PA_ERR_DEVICE_TIMEOUT, "a device-side wait ran out (status word 0x%x)", word);
+  if (word & kStatusBounds)
+    return fail(PA_ERR_DEVICE_BOUNDS, "a kernel saw an out-of-range block id, slot or length");
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Shared definitions between the decode kernels and their host launcher.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace pa {
+namespace decode {
+
+constexpr int kBlockSize = 16;      // tokens per physical block (device kernels)
+constexpr int kSplitBlocks = 32;    // logical blocks per work item (512 tokens)
+constexpr int kConsumerWarps = 4;   // warps doing the attention math
+constexpr int kStages = 8;          // (K, V) tiles buffered per CTA
+constexpr int kQueue = 4;           // work items buffered per CTA
+constexpr int kMaxGroup = 8;        // query heads per KV head on the tensor-core path
+constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + TMA issuer warp + scheduler warp
+
+// Views into the caller's workspace (all offsets 256-byte aligned).
+struct Workspace {
+  int* header;       // [0] next work item, [1] number of work items
+  int* units;        // int4 per (sequence, split): b, split, context length, blocks
+  int* arrivals;     // [num_seqs * num_kv_heads] finished splits per (b, kv head)
+  float* part_lse;   // [num_seqs][max_splits][num_q_heads]  (log2 domain)
+  float* part_o;     // [num_seqs][max_splits][num_q_heads][head_dim]
+};
+
+struct Layout {
+  size_t header, units, arrivals, part_lse, part_o, total;
+  int max_splits;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                               int max_blocks_per_seq) {
+  Layout l;
+  l.max_splits = (max_blocks_per_seq + kSplitBlocks - 1) / kSplitBlocks;
+  if (l.max_splits < 1) l.max_splits = 1;
+  const size_t units = size_t(num_seqs) * l.max_splits;
+  l.header = 0;
+  l.units = align256(l.header + 256);
+  l.arrivals = align256(l.units + units * 16);
+  l.part_lse = align256(l.arrivals + size_t(num_seqs) * num_kv_heads * 4);
+  l.part_o = align256(l.part_lse + units * num_q_heads * 4);
+  l.total = align256(l.part_o + units * num_q_heads * size_t(head_dim) * 4);
+  return l;
+}
+
+struct Params {
+  const void* q;
+  const void* k_cache;  // raw cache pointers (the fp32 path reads them directly;
+  const void* v_cache;  // the tensor-core path goes through tensor maps)
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  int num_seqs, num_q_heads, num_kv_heads, group, head_dim;
+  int max_blocks, num_blocks, max_splits;
+  float scale;       // softmax scale (fp32 path)
+  float scale_log2;  // scale * log2(e) (tensor-core path works in base 2)
+  Workspace ws;
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+}  // namespace decode
+}  // namespace pa

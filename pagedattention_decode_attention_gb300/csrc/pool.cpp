@@ -1,0 +1,266 @@
+// Host block pool: free list, refcounts, lazy allocation, fork, copy-on-write,
+// prefix sharing and pinning.  It produces block tables, slots and copy pairs
+// for the device kernels and never touches device memory.
+//
+// Sources: "vLLM: treating the KV cache as virtual memory", section
+// 碎片从哪里来 (fixed blocks, free list, refcounts, fork copies the table,
+// copy-on-write, prefix blocks kept outside the free list); "第 6 章 缓存管理",
+// section 块表长什么样 (refcount 1 -> 2 on sharing, -1 when a request ends,
+// free at 0); OS-lab appendix sections 3.3 (allocate a physical page only when
+// generation reaches it) and 4.4 (copy a shared partly-filled block on write;
+// the last holder writes in place).
+#include <algorithm>
+#include <cstdint>
+#include <unordered_map>
+#include <vector>
+
+#include "pagedattn.h"
+#include "status.h"
+
+namespace {
+
+struct Seq {
+  std::vector<int32_t> table;
+  int64_t ctx = 0;
+};
+
+}  // namespace
+
+struct pa_pool {
+  int num_blocks = 0;
+  int block_size = 16;
+  std::vector<int32_t> free_stack;  // top = back()
+  std::vector<int32_t> refcount;
+  std::vector<uint8_t> pinned;
+  std::vector<uint8_t> on_free;     // mirrors membership of free_stack
+  std::unordered_map<int, Seq> seqs;
+  int next_id = 0;
+  int64_t cow_copies = 0;
+
+  int32_t alloc() {
+    int32_t b = free_stack.back();
+    free_stack.pop_back();
+    on_free[b] = 0;
+    refcount[b] = 1;
+    return b;
+  }
+  void release(int32_t b) {
+    if (--refcount[b] == 0 && !pinned[b]) {
+      free_stack.push_back(b);
+      on_free[b] = 1;
+    }
+  }
+  Seq* find(int id) {
+    auto it = seqs.find(id);
+    return it == seqs.end() ? nullptr : &it->second;
+  }
+};
+
+extern "C" {
+
+PA_API int pa_pool_create(int num_blocks, int block_size, const int32_t* initial_order,
+                          pa_pool** pool) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: pool is NULL");
+  *pool = nullptr;
+  if (num_blocks <= 0 || block_size <= 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: num_blocks and block_size must be > 0");
+  auto* p = new pa_pool();
+  p->num_blocks = num_blocks;
+  p->block_size = block_size;
+  p->refcount.assign(num_blocks, 0);
+  p->pinned.assign(num_blocks, 0);
+  p->on_free.assign(num_blocks, 0);
+  p->free_stack.resize(num_blocks);
+  for (int i = 0; i < num_blocks; ++i) {
+    int32_t b = initial_order ? initial_order[i] : i;
+    if (b < 0 || b >= num_blocks || p->on_free[b]) {
+      delete p;
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: initial_order is not a permutation");
+    }
+    p->on_free[b] = 1;
+    p->free_stack[num_blocks - 1 - i] = b;  // initial_order[0] ends on top
+  }
+  *pool = p;
+  return PA_OK;
+}
+
+PA_API int pa_pool_destroy(pa_pool* pool) {
+  delete pool;
+  return PA_OK;
+}
+
+PA_API int pa_pool_new_seq(pa_pool* pool, int* seq_id) {
+  if (!pool || !seq_id) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_new_seq: NULL argument");
+  *seq_id = pool->next_id;
+  pool->seqs.emplace(pool->next_id, Seq());
+  pool->next_id++;
+  return PA_OK;
+}
+
+PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* cow_src,
+                               int64_t* cow_dst) {
+  if (!pool || !slot || !cow_src || !cow_dst)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slot: NULL argument");
+  Seq* s = pool->find(seq);
+  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_append_slot: unknown sequence");
+  const int64_t logical = s->ctx / pool->block_size;
+  const int64_t offset = s->ctx % pool->block_size;
+  int64_t src = -1, dst = -1;
+  int32_t block;
+  if (offset == 0) {
+    if (pool->free_stack.empty()) return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_append_slot: pool exhausted");
+    block = pool->alloc();
+    s->table.push_back(block);
+  } else {
+    block = s->table[logical];
+    if (pool->refcount[block] > 1) {
+      if (pool->free_stack.empty())
+        return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_append_slot: pool exhausted (copy-on-write)");
+      int32_t fresh = pool->alloc();
+      pool->refcount[block] -= 1;  // stays >= 1: another holder remains
+      s->table[logical] = fresh;
+      src = block;
+      dst = fresh;
+      pool->cow_copies++;
+      block = fresh;
+    }
+  }
+  s->ctx += 1;
+  *slot = static_cast<int64_t>(block) * pool->block_size + offset;
+  *cow_src = src;
+  *cow_dst = dst;
+  return PA_OK;
+}
+
+PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64_t* slots,
+                                int64_t* pairs, int pair_cap, int* num_pairs, int* done) {
+  if (!pool || (n > 0 && (!seqs || !slots)) || !num_pairs || !done || n < 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slots: bad argument");
+  *num_pairs = 0;
+  *done = 0;
+  for (int i = 0; i < n; ++i) {
+    int64_t src, dst;
+    // A copy pair needs room before the slot is taken, so a full pair buffer
+    // never leaves a copy unreported.
+    Seq* s = pool->find(seqs[i]);
+    if (s && s->ctx % pool->block_size != 0 &&
+        pool->refcount[s->table[s->ctx / pool->block_size]] > 1 && *num_pairs >= pair_cap)
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slots: pair buffer full");
+    int rc = pa_pool_append_slot(pool, seqs[i], &slots[i], &src, &dst);
+    if (rc != PA_OK) return rc;
+    if (src >= 0) {
+      pairs[2 * *num_pairs] = src;
+      pairs[2 * *num_pairs + 1] = dst;
+      (*num_pairs)++;
+    }
+    (*done)++;
+  }
+  return PA_OK;
+}
+
+PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child) {
+  if (!pool || !child) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_fork: NULL argument");
+  Seq* p = pool->find(parent);
+  if (!p) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_fork: unknown sequence");
+  Seq c;
+  c.table = p->table;
+  c.ctx = p->ctx;
+  for (int32_t b : c.table) pool->refcount[b] += 1;
+  *child = pool->next_id;
+  pool->seqs.emplace(pool->next_id, std::move(c));
+  pool->next_id++;
+  return PA_OK;
+}
+
+PA_API int pa_pool_share_prefix(pa_pool* pool, int src_seq, int dst_seq, int num_tokens) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_share_prefix: NULL pool");
+  Seq* src = pool->find(src_seq);
+  Seq* dst = pool->find(dst_seq);
+  if (!src || !dst) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_share_prefix: unknown sequence");
+  if (dst->ctx != 0 || !dst->table.empty())
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_share_prefix: destination must be empty");
+  if (num_tokens <= 0 || num_tokens > src->ctx)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_share_prefix: num_tokens out of range");
+  const int64_t count = (num_tokens + pool->block_size - 1) / pool->block_size;
+  dst->table.assign(src->table.begin(), src->table.begin() + count);
+  dst->ctx = num_tokens;
+  for (int32_t b : dst->table) pool->refcount[b] += 1;
+  return PA_OK;
+}
+
+PA_API int pa_pool_pin(pa_pool* pool, int seq, int num_tokens) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_pin: NULL pool");
+  Seq* s = pool->find(seq);
+  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_pin: unknown sequence");
+  if (num_tokens < 0 || num_tokens > s->ctx)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_pin: num_tokens out of range");
+  const int64_t count = (num_tokens + pool->block_size - 1) / pool->block_size;
+  for (int64_t i = 0; i < count; ++i) pool->pinned[s->table[i]] = 1;
+  return PA_OK;
+}
+
+PA_API int pa_pool_unpin(pa_pool* pool, int block) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_unpin: NULL pool");
+  if (block < 0 || block >= pool->num_blocks || !pool->pinned[block])
+    return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_unpin: block is not pinned");
+  pool->pinned[block] = 0;
+  if (pool->refcount[block] == 0) {
+    pool->free_stack.push_back(block);
+    pool->on_free[block] = 1;
+  }
+  return PA_OK;
+}
+
+PA_API int pa_pool_free_seq(pa_pool* pool, int seq) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_free_seq: NULL pool");
+  auto it = pool->seqs.find(seq);
+  if (it == pool->seqs.end()) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_free_seq: unknown sequence");
+  const auto& table = it->second.table;
+  for (auto b = table.rbegin(); b != table.rend(); ++b) pool->release(*b);
+  pool->seqs.erase(it);
+  return PA_OK;
+}
+
+PA_API int pa_pool_block_table(pa_pool* pool, int seq, int32_t* out, int cap, int* n,
+                               int* ctx_len) {
+  if (!pool || !n || !ctx_len || cap < 0 || (cap > 0 && !out))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_block_table: bad argument");
+  Seq* s = pool->find(seq);
+  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_block_table: unknown sequence");
+  const int len = static_cast<int>(s->table.size());
+  std::copy(s->table.begin(), s->table.begin() + std::min(len, cap), out);
+  *n = len;
+  *ctx_len = static_cast<int>(s->ctx);
+  return PA_OK;
+}
+
+PA_API int pa_pool_refcount(pa_pool* pool, int block, int* rc) {
+  if (!pool || !rc) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_refcount: NULL argument");
+  if (block < 0 || block >= pool->num_blocks)
+    return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_refcount: block out of range");
+  *rc = pool->refcount[block];
+  return PA_OK;
+}
+
+PA_API int pa_pool_stats(pa_pool* pool, pa_pool_stats_t* st) {
+  if (!pool || !st) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_stats: NULL argument");
+  st->num_blocks = pool->num_blocks;
+  st->free_blocks = static_cast<int64_t>(pool->free_stack.size());
+  st->used_blocks = st->pinned_blocks = st->shared_blocks = 0;
+  for (int b = 0; b < pool->num_blocks; ++b) {
+    st->used_blocks += pool->refcount[b] > 0;
+    st->shared_blocks += pool->refcount[b] > 1;
+    st->pinned_blocks += pool->pinned[b] != 0;
+  }
+  st->cow_copies = pool->cow_copies;
+  st->live_seqs = static_cast<int64_t>(pool->seqs.size());
+  st->tokens = st->internal_frag_slots = 0;
+  for (const auto& kv : pool->seqs) {
+    st->tokens += kv.second.ctx;
+    st->internal_frag_slots +=
+        static_cast<int64_t>(kv.second.table.size()) * pool->block_size - kv.second.ctx;
+  }
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,142 @@
+"""Torch-facing binding of the device entry points.
+
+Argument marshalling only: each function checks shapes / dtypes / devices of
+the torch tensors, passes their raw pointers and the current CUDA stream to the
+C ABI, and raises ``PagedAttnError`` on a non-zero status.  All computation
+happens in the library's kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import capi
+
+_DTYPES = {torch.float32: capi.PA_F32, torch.float16: capi.PA_F16, torch.bfloat16: capi.PA_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32, float16 or bfloat16)")
+    return _DTYPES[t.dtype]
+
+
+def _stream(device: torch.device, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _require(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(name: str, t: torch.Tensor, device: torch.device) -> None:
+    _require(t.is_cuda and t.device == device, f"{name} must be on {device}")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   max_blocks_per_seq: int) -> int:
+    out = C.c_size_t(0)
+    capi.check(capi.lib().pa_paged_attention_decode_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, C.byref(out)))
+    return out.value
+
+
+def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                    device) -> torch.Tensor:
+    n = workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+              slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write ``k[i]`` / ``v[i]`` (``[T, Hkv, d]``) into slot ``slot_mapping[i]``
+    of the paged caches (``[NB, Hkv, 16, d]``); negative slots are skipped."""
+    dev = k_cache.device
+    for name, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("slot_mapping", slot_mapping)):
+        _cuda_contig(name, t, dev)
+    _require(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    _require(k.dtype == v.dtype == k_cache.dtype == v_cache.dtype, "dtypes must match")
+    _require(k_cache.dim() == 4 and k_cache.shape == v_cache.shape and k_cache.shape[2] == 16,
+             "caches must be [num_blocks, num_kv_heads, 16, head_dim]")
+    nb, hkv, _, d = k_cache.shape
+    _require(k.shape == v.shape and k.dim() == 3 and tuple(k.shape[1:]) == (hkv, d),
+             "k, v must be [num_tokens, num_kv_heads, head_dim]")
+    _require(slot_mapping.shape == (k.shape[0],), "slot_mapping must be [num_tokens]")
+    capi.check(capi.lib().pa_kv_append(
+        k.data_ptr(), v.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        slot_mapping.data_ptr(), k.shape[0], hkv, d, nb, _dtype_code(k), _stream(dev, stream)))
+
+
+def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Decode attention of ``q`` (``[B, Hq, d]``) over paged ``k_cache`` /
+    ``v_cache`` (``[NB, Hkv, 16, d]``) through ``block_tables`` (int32
+    ``[B, max_blocks]``) for ``context_lens`` (int32 ``[B]``) tokens."""
+    dev = q.device
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda_contig(name, t, dev)
+    _require(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+             "block_tables and context_lens must be int32")
+    _require(q.dtype == k_cache.dtype == v_cache.dtype, "q and caches must share a dtype")
+    _require(k_cache.dim() == 4 and k_cache.shape == v_cache.shape and k_cache.shape[2] == 16,
+             "caches must be [num_blocks, num_kv_heads, 16, head_dim]")
+    nb, hkv, _, d = k_cache.shape
+    _require(q.dim() == 3 and q.shape[2] == d, "q must be [num_seqs, num_q_heads, head_dim]")
+    b, hq, _ = q.shape
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == b,
+             "block_tables must be [num_seqs, max_blocks_per_seq]")
+    _require(context_lens.shape == (b,), "context_lens must be [num_seqs]")
+    mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = alloc_workspace(b, hq, hkv, d, mb, dev)
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(dev, stream)))
+    return out
+
+
+def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks ``src -> dst`` (int64 ``[P, 2]`` on the device) in every
+    layer's caches."""
+    k_caches, v_caches = list(k_caches), list(v_caches)
+    _require(len(k_caches) == len(v_caches) and len(k_caches) > 0, "need one k/v cache per layer")
+    dev = k_caches[0].device
+    ref = k_caches[0]
+    for kc, vc in zip(k_caches, v_caches):
+        _cuda_contig("k_cache", kc, dev)
+        _cuda_contig("v_cache", vc, dev)
+        _require(kc.shape == ref.shape == vc.shape and kc.dtype == vc.dtype == ref.dtype,
+                 "all layer caches must share shape and dtype")
+    _cuda_contig("src_dst_pairs", src_dst_pairs, dev)
+    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.dim() == 2
+             and src_dst_pairs.shape[1] == 2, "src_dst_pairs must be int64 [P, 2]")
+    nb, hkv, _, d = ref.shape
+    n = len(k_caches)
+    kp = (C.c_void_p * n)(*[t.data_ptr() for t in k_caches])
+    vp = (C.c_void_p * n)(*[t.data_ptr() for t in v_caches])
+    capi.check(capi.lib().pa_block_copy(
+        kp, vp, n, src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], hkv, d, nb,
+        _dtype_code(ref), _stream(dev, stream)))
+
+
+def check_status(stream=None, device=None) -> None:
+    """Synchronise the stream and raise if a kernel flagged an out-of-range
+    index or a timed-out wait since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    capi.check(capi.lib().pa_check_status(_stream(dev, stream)))

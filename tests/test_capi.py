@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every symbol the public header declares, and
+rejects bad arguments on the host before touching a GPU (CPU only)."""
+
+import ctypes as C
+import glob
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from pagedattention_decode_attention_gb300 import build, capi
+    if not os.path.exists(capi.LIB_PATH):
+        build.build()
+    return capi.lib()
+
+
+def declared_symbols():
+    names = set()
+    for header in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(header).read()
+        names |= set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for required in ("pa_kv_append", "pa_paged_attention_decode", "pa_block_copy",
+                     "pa_paged_attention_decode_workspace_size", "pa_pool_create",
+                     "pa_pool_append_slot", "pa_pool_fork", "pa_pool_share_prefix",
+                     "pa_pool_free_seq", "pa_pool_block_table", "pa_check_status"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in sorted(declared_symbols()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_declares_exactly_the_header(lib):
+    from pagedattention_decode_attention_gb300 import capi
+    assert set(capi.SIGNATURES) == declared_symbols()
+
+
+def test_version(lib):
+    assert lib.pa_version() >= 100
+
+
+def test_workspace_size_is_host_only(lib):
+    out = C.c_size_t(0)
+    assert lib.pa_paged_attention_decode_workspace_size(128, 32, 8, 128, 512, C.byref(out)) == 0
+    # header + units + arrivals + partial (lse, o) for 16 splits of 128 seqs
+    assert out.value >= 128 * 16 * 32 * 128 * 4
+    assert lib.pa_paged_attention_decode_workspace_size(1, 0, 1, 64, 1, C.byref(out)) == 1
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(dtype=7), 2),                          # unknown dtype -> unsupported
+    (dict(head_dim=96), 2),                      # head_dim not built
+    (dict(num_q_heads=6, num_kv_heads=4), 1),    # ragged grouping
+    (dict(num_q_heads=32, num_kv_heads=2), 2),   # 16 heads per KV head > 8 (16-bit path)
+    (dict(workspace_bytes=16), 1),               # workspace too small
+])
+def test_decode_rejects_on_host(lib, kwargs, status):
+    a = dict(q=256, k=256, v=256, bt=256, cl=256, num_seqs=2, num_q_heads=4, num_kv_heads=4,
+             head_dim=64, max_blocks=4, num_blocks=8, scale=0.125, dtype=2, out=256,
+             ws=256, workspace_bytes=1 << 20)
+    a.update(kwargs)
+    rc = lib.pa_paged_attention_decode(a["q"], a["k"], a["v"], a["bt"], a["cl"], a["num_seqs"],
+                                       a["num_q_heads"], a["num_kv_heads"], a["head_dim"],
+                                       a["max_blocks"], a["num_blocks"], a["scale"], a["dtype"],
+                                       a["out"], a["ws"], a["workspace_bytes"], None)
+    assert rc == status
+    assert lib.pa_last_error()
+
+
+def test_empty_batches_are_noops(lib):
+    assert lib.pa_kv_append(None, None, None, None, None, 0, 8, 128, 16, 2, None) == 0
+    assert lib.pa_block_copy(None, None, 1, None, 0, 8, 128, 16, 2, None) == 0
+    assert lib.pa_paged_attention_decode(None, None, None, None, None, 0, 4, 4, 64, 4, 8,
+                                         0.1, 1, None, None, 0, None) == 0
+
+
+def test_copy_paths_reject_on_host(lib):
+    # misaligned pointer, bad dtype, too many layers
+    assert lib.pa_kv_append(8, 16, 16, 16, 16, 1, 8, 128, 16, 2, None) == 1
+    assert lib.pa_kv_append(16, 16, 16, 16, 16, 1, 8, 128, 16, 5, None) == 2
+    ptrs = (C.c_void_p * 1)(256)
+    assert lib.pa_block_copy(ptrs, ptrs, 300, 256, 1, 8, 128, 16, 2, None) == 1

@@ -1,0 +1,187 @@
+"""The native (C++) block pool against the Python pool model and the pages'
+worked examples (CPU only: the pool touches no device memory)."""
+
+import os
+
+import numpy as np
+import pytest
+
+from oracle.pool import BlockPool as ModelPool, NoBlocks
+from tests.conftest import golden
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from pagedattention_decode_attention_gb300 import build, capi
+    if not os.path.exists(capi.LIB_PATH):
+        build.build()
+
+
+def native(num_blocks, block_size=16, initial_order=None):
+    from pagedattention_decode_attention_gb300 import BlockPool
+    return BlockPool(num_blocks, block_size, initial_order)
+
+
+def is_no_blocks(exc):
+    from pagedattention_decode_attention_gb300.capi import PA_ERR_NO_BLOCKS, PagedAttnError
+    return isinstance(exc, PagedAttnError) and exc.status == PA_ERR_NO_BLOCKS
+
+
+def replay(pool, ops, is_native):
+    """Apply an op script; return every observable result."""
+    out = []
+    for op in ops:
+        kind = op[0]
+        try:
+            if kind == "new":
+                out.append(("new", pool.new_seq()))
+            elif kind == "append":
+                slot, cow = pool.append_slot(op[1])
+                out.append(("append", slot, None if cow is None else tuple(int(x) for x in cow)))
+            elif kind == "fork":
+                out.append(("fork", pool.fork(op[1])))
+            elif kind == "share":
+                pool.share_prefix(op[1], op[2], op[3])
+                out.append(("share",))
+            elif kind == "free":
+                pool.free_seq(op[1])
+                out.append(("free",))
+            elif kind == "pin":
+                pool.pin(op[1], op[2])
+                out.append(("pin",))
+        except Exception as e:  # noqa: BLE001
+            if isinstance(e, NoBlocks) or (is_native and is_no_blocks(e)):
+                out.append(("noblocks",))
+            else:
+                raise
+    return out
+
+
+def random_script(gen, n_ops, model):
+    """Random op script, generated against the model pool so every op is legal."""
+    ops, live = [], []
+    for _ in range(n_ops):
+        r = gen.integers(0, 20)
+        if r < 3 or not live:
+            ops.append(("new",))
+            live.append(model.new_seq())
+            continue
+        s = live[gen.integers(len(live))]
+        if r < 14:
+            ops.append(("append", s))
+            try:
+                model.append_slot(s)
+            except NoBlocks:
+                pass
+        elif r < 16:
+            ops.append(("fork", s))
+            live.append(model.fork(s))
+        elif r < 17:
+            ctx = model.block_table(s)[1]
+            if ctx:
+                d = model.new_seq()
+                live.append(d)
+                n = int(gen.integers(1, ctx + 1))
+                ops += [("new",), ("share", s, d, n)]
+                model.share_prefix(s, d, n)
+        elif r < 18:
+            ctx = model.block_table(s)[1]
+            n = int(gen.integers(0, ctx + 1))
+            ops.append(("pin", s, n))
+            model.pin(s, n)
+        else:
+            live.remove(s)
+            ops.append(("free", s))
+            model.free_seq(s)
+    return ops
+
+
+@pytest.mark.parametrize("seed,num_blocks,block_size", [(1, 48, 16), (2, 30, 4), (3, 200, 16)])
+def test_native_matches_model_on_random_scripts(seed, num_blocks, block_size):
+    gen = np.random.default_rng(seed)
+    order = gen.permutation(num_blocks)
+    script = random_script(gen, 3000, ModelPool(num_blocks, block_size, order))
+    model = ModelPool(num_blocks, block_size, order)
+    nat = native(num_blocks, block_size, order)
+    assert replay(nat, script, True) == replay(model, script, False)
+    for s in model.seqs:
+        assert nat.block_table(s) == model.block_table(s)
+    for b in range(num_blocks):
+        assert nat.refcount(b) == model.refcount[b]
+    assert nat.stats() == model.stats()
+
+
+def test_batched_append_matches_single():
+    gen = np.random.default_rng(9)
+    a, b = native(64), native(64)
+    seqs = [a.new_seq() for _ in range(4)]
+    [b.new_seq() for _ in range(4)]
+    for _ in range(21):
+        for s in seqs:
+            a.append_slot(s)
+            b.append_slot(s)
+    kids_a = [a.fork(s) for s in seqs]
+    kids_b = [b.fork(s) for s in seqs]
+    order = np.array(seqs + kids_a, dtype=np.int32)[gen.permutation(8)]
+    slots, pairs = a.append_slots(order)
+    single = [b.append_slot(int(s)) for s in order]
+    assert slots.tolist() == [s for s, _ in single]
+    assert [tuple(p) for p in pairs.tolist()] == [c for _, c in single if c is not None]
+    assert kids_a == kids_b
+
+
+def test_native_oslab_cow_example():
+    g = golden("cow_examples.json")["oslab_block4"]
+    pool = native(8, block_size=4)
+    a1 = pool.new_seq()
+    for _ in g["prefix_tokens"]:
+        pool.append_slot(a1)
+    a2 = pool.fork(a1)
+    table, _ = pool.block_table(a1)
+    assert pool.refcount(table[1]) == g["block1_refcount_after_fork"]
+    _, cow = pool.append_slot(a1)
+    assert cow[0] == table[1]
+    assert pool.refcount(table[1]) == g["block1_refcount_after_a1_write"]
+    slot, cow = pool.append_slot(a2)
+    assert cow is None and slot // 4 == table[1]
+    assert pool.stats()["cow_copies"] == g["a1_copies"] + g["a2_copies"]
+
+
+def test_native_share_example():
+    g = golden("cow_examples.json")["share_200_of_500"]
+    pool = native(128)
+    r1 = pool.new_seq()
+    for _ in range(g["first_tokens"]):
+        pool.append_slot(r1)
+    assert len(pool.block_table(r1)[0]) == g["first_blocks"]
+    r2 = pool.new_seq()
+    pool.share_prefix(r1, r2, g["shared_tokens"])
+    t2, _ = pool.block_table(r2)
+    assert len(t2) == g["shared_entries"]
+    assert all(pool.refcount(b) == g["refcount_shared"] for b in t2)
+    pool.free_seq(r1)
+    assert all(pool.refcount(b) == g["refcount_after_one_ends"] for b in t2)
+    pool.free_seq(r2)
+    assert pool.stats()["free_blocks"] == 128
+
+
+def test_native_errors():
+    from pagedattention_decode_attention_gb300.capi import (PA_ERR_INVALID_ARG, PA_ERR_NO_BLOCKS,
+                                                            PA_ERR_NOT_FOUND, PagedAttnError)
+    with pytest.raises(PagedAttnError) as e:
+        native(4, initial_order=[0, 1, 1, 2])
+    assert e.value.status == PA_ERR_INVALID_ARG
+    pool = native(1)
+    s = pool.new_seq()
+    for _ in range(16):
+        pool.append_slot(s)
+    with pytest.raises(PagedAttnError) as e:
+        pool.append_slot(s)
+    assert e.value.status == PA_ERR_NO_BLOCKS
+    with pytest.raises(PagedAttnError) as e:
+        pool.free_seq(99)
+    assert e.value.status == PA_ERR_NOT_FOUND
+    pool.free_seq(s)
+    with pytest.raises(PagedAttnError) as e:
+        pool.free_seq(s)                    # double free of a sequence
+    assert e.value.status == PA_ERR_NOT_FOUND
