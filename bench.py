@@ -53,13 +53,17 @@ L2_BYTES = 126 * 1024 * 1024
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["mha_7b", "gqa_8b"], default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the workload's layer count (profiling at a small footprint)")
+    ap.add_argument("--warmup-seconds", type=float, default=1.0,
+                    help="keep warming up until this much wall time has passed")
     return ap.parse_args()
 
 
@@ -122,51 +126,103 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons sampled during the timed
+    region, read through NVML (ctypes on libnvidia-ml; reading only).  Falls
+    back to ``nvidia-smi`` polling when NVML cannot be loaded."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, device: torch.device, period_s: float = 0.002):
+        self.device = device
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = None
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        self._smi = None
+        self._open()
+
+    def _open(self):
+        import ctypes as C
+        try:
+            nvml = C.CDLL("libnvidia-ml.so.1")
+            if nvml.nvmlInit_v2() != 0:
+                return
+            handle = C.c_void_p()
+            props = torch.cuda.get_device_properties(self.device)
+            bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0),
+                                        getattr(props, "pci_bus_id", 0),
+                                        getattr(props, "pci_device_id", 0))
+            if nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), C.byref(handle)) != 0:
+                if nvml.nvmlDeviceGetHandleByIndex_v2(self.device.index or 0, C.byref(handle)) != 0:
+                    return
+            mx = C.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(handle, 1, C.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self._nvml, self._handle = nvml, handle
+        except OSError:
+            self._nvml = None
+
+    def _poll(self):
+        import ctypes as C
+        clk, rs = C.c_uint(), C.c_ulonglong()
+        getr = getattr(self._nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._handle, 1, C.byref(clk)) == 0:
+                self.samples.append(float(clk.value))
+            if getr(self._handle, C.byref(rs)) == 0:
+                for bit, name in self.REASONS.items():
+                    if rs.value & bit:
+                        self.reasons.add(name)
+            self._stop.wait(self.period)
 
     def start(self):
+        import threading
+        if self._nvml is not None:
+            self._stop = threading.Event()
+            self._thread = threading.Thread(target=self._poll, daemon=True)
+            self._thread.start()
+            return
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device.index or 0),
+                 "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap", "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
-            self.proc = None
+            self._smi = None
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+    def stop(self) -> dict:
+        source = "nvml"
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join()
+        elif self._smi is not None:
+            source = "nvidia-smi"
+            self._smi.terminate()
+            out, _ = self._smi.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except (ValueError, IndexError):
+                    continue
+                for name, val in zip(names, f[2:6]):
+                    if val.lower() == "active":
+                        self.reasons.add(name)
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock source"], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": source}
 
 
 # --------------------------------------------------------------------- ours
@@ -194,20 +250,41 @@ class Replica:
         self.slots = torch.from_numpy(batch.new_token_slots()).to(device)
         self.ws = pa.alloc_workspace(b, hq, hkv, d, batch.max_blocks, device)
         self.scale = batch.scale
-        self.launches_per_step = 3 * L       # kv_append + plan + attention per layer
+        self.launches_per_step = 1 + 2 * L   # one plan, then kv_append + attention per layer
+        # Calls bound to this replica's buffers (validated once; each step only
+        # re-issues the C calls).
+        self.plan_call = pa.prepare_decode_plan(self.lens, hq, hkv, d, batch.max_blocks, self.ws)
+        self.append_calls = [pa.prepare_kv_append(self.k_new[i], self.v_new[i], self.k_cache[i],
+                                                  self.v_cache[i], self.slots) for i in range(L)]
+        self.run_calls = [pa.prepare_decode_run(self.q[i], self.k_cache[i], self.v_cache[i],
+                                                self.tables, self.lens, self.scale, self.ws,
+                                                self.out[i]) for i in range(L)]
 
     def step(self, ev=None):
-        pa, L = self.pa, self.batch.num_layers
-        for layer in range(L):
-            pa.kv_append(self.k_new[layer], self.v_new[layer], self.k_cache[layer],
-                         self.v_cache[layer], self.slots)
+        """One decode step: the work list is planned once from the context
+        lengths (the same for every layer), then each layer appends its new
+        K/V rows and runs attention."""
+        self.plan_call()
+        for layer in range(self.batch.num_layers):
+            self.append_calls[layer]()
             if ev is not None:
                 ev[layer][0].record()
-            pa.paged_attention_decode(self.q[layer], self.k_cache[layer], self.v_cache[layer],
-                                      self.tables, self.lens, self.scale, out=self.out[layer],
-                                      workspace=self.ws)
+            self.run_calls[layer]()
             if ev is not None:
                 ev[layer][1].record()
+
+    def kernel_only_ms(self, reps: int = 64) -> float:
+        """Mean device time of back-to-back attention runs on layer 0 (no host
+        gaps between them): a check on the per-launch event timings."""
+        self.plan_call()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.run_calls[0]()
+        start.record()
+        for _ in range(reps):
+            self.run_calls[0]()
+        end.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / reps
 
 
 def barrier(world):
@@ -276,30 +353,38 @@ def time_e2e(rep: Replica, steps: int, world: int):
     return start.elapsed_time(end) / 1e3, h2d, d2h
 
 
-def cpu_oracle_sample(batch: wl.DecodeBatch, rep: Replica | None, seconds: float, step_units=None):
+class OracleInputs:
+    """Host float32 copies of layer 0 of the workload for the oracle: from the
+    device replica when there is one, else drawn on the host."""
+
+    def __init__(self, batch: wl.DecodeBatch, rep: "Replica | None"):
+        if rep is not None:
+            self.kc = rep.k_cache[0].float().cpu().numpy()
+            self.vc = rep.v_cache[0].float().cpu().numpy()
+            self.q = rep.q[0].float().cpu().numpy()
+        else:
+            shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
+            gen = np.random.default_rng(batch.seed)
+            self.kc = gen.standard_normal(shape, dtype=np.float32)
+            self.vc = gen.standard_normal(shape, dtype=np.float32)
+            self.q = gen.standard_normal((batch.num_seqs, batch.num_q_heads, batch.head_dim),
+                                         dtype=np.float32)
+        self.order = np.random.default_rng(7).permutation(batch.num_seqs)
+        self.next = 0
+
+
+def cpu_oracle_sample(batch: wl.DecodeBatch, inp: OracleInputs, seconds: float, step_units=None):
     """Times the oracle on (sequence, layer) units of the workload.  A unit is one
-    sequence's attention over all query heads for one layer; 32 units of the
-    7B workload (its layer count) make one decoded token.  Returns
-    (tokens/s, units done, elapsed s, sequences used)."""
+    sequence's attention over all query heads for one layer; ``num_layers``
+    units make one decoded token.  Returns (tokens/s, units, elapsed s)."""
     import oracle.attention as oa
-    if rep is not None:
-        kc = rep.k_cache[0].float().cpu().numpy()
-        vc = rep.v_cache[0].float().cpu().numpy()
-        q = rep.q[0].float().cpu().numpy()
-    else:
-        shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
-        gen = np.random.default_rng(batch.seed)
-        kc = gen.standard_normal(shape, dtype=np.float32)
-        vc = gen.standard_normal(shape, dtype=np.float32)
-        q = gen.standard_normal((batch.num_seqs, batch.num_q_heads, batch.head_dim), dtype=np.float32)
-    order = np.random.default_rng(7).permutation(batch.num_seqs)
-    units, t0, i = 0, time.perf_counter(), 0
+    units, t0 = 0, time.perf_counter()
     while True:
-        b = int(order[i % batch.num_seqs])
-        oa.paged_attention_decode(q, kc, vc, batch.block_tables, batch.context_lens, batch.scale,
-                                  seqs=[b])
+        b = int(inp.order[inp.next % batch.num_seqs])
+        inp.next += 1
+        oa.paged_attention_decode(inp.q, inp.kc, inp.vc, batch.block_tables, batch.context_lens,
+                                  batch.scale, seqs=[b])
         units += 1
-        i += 1
         el = time.perf_counter() - t0
         if (step_units is not None and units >= step_units) or (step_units is None and el >= seconds):
             break
@@ -315,17 +400,27 @@ def run_ours(args):
     device = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(device)
     batch = make_batch(args.workload, rank)
+    if args.layers > 0:
+        batch.num_layers = args.layers
     rep = Replica(batch, device)
-    for _ in range(max(args.warmup, 3)):
+    # Warm-up: at least max(W, 3) steps and at least 1 s, so clocks have ramped.
+    warm, t0 = 0, time.perf_counter()
+    while warm < max(args.warmup, 3) or time.perf_counter() - t0 < args.warmup_seconds:
         rep.step()
+        warm += 1
+        if warm % 8 == 0:
+            torch.cuda.synchronize()
     rep.pa.check_status()
     torch.cuda.synchronize()
 
-    clocks = ClockSampler(device.index)
+    clocks = ClockSampler(device)
     clocks.start()
+    h0 = time.perf_counter()
     secs, per_launch = time_steps(rep, args.steps, world, events=True)
+    host_secs = time.perf_counter() - h0
     clk = clocks.stop()
     rep.pa.check_status()
+    kernel_ms = rep.kernel_only_ms()
     secs = max_over_ranks(secs, world)
     tokens_per_step = batch.num_seqs * world
     value = tokens_per_step * args.steps / secs
@@ -347,7 +442,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, units, el = cpu_oracle_sample(batch, rep, args.cpu_seconds)
+        v, units, el = cpu_oracle_sample(batch, OracleInputs(batch, rep), args.cpu_seconds)
         cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": (f"{units} (sequence, layer) attention units of layer 0, all "
                           f"{batch.num_q_heads} query heads each, float64 numpy on 1 host "
@@ -356,7 +451,7 @@ def run_ours(args):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": max(args.warmup, 3),
+            "steps": args.steps, "warmup": warm,
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
             "data": "synthetic (seeded N(0,1) K/V/Q, seeded lengths and placements)",
@@ -367,19 +462,21 @@ def run_ours(args):
                 "context_tokens": ab["tokens"], "num_blocks_per_layer": batch.num_blocks,
                 "l2": (f"inputs larger than L2: {ab['kv'] * batch.num_layers / 1e9:.2f} GB of KV "
                        f"read per step across {batch.num_layers} separate layer caches"),
-                "step": "per layer: kv_append of the new K/V rows, then paged decode attention",
+                "step": ("plan the work list once from the context lengths, then per layer: "
+                         "kv_append of the new K/V rows and paged decode attention"),
                 "parallelism": f"replicas x{world} (independent batches, no collective)",
             },
             "kv_read_gbs": ab["kv"] / (avg_ms / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs",
-                         "kernel": "paged_attention_decode call (plan + attention kernels)",
+                         "kernel": "paged_attention_decode_run (persistent attention kernel)",
                          "algorithmic_bytes_per_launch": ab["total"],
-                         "avg_launch_ms": avg_ms},
+                         "avg_launch_ms": avg_ms, "back_to_back_launch_ms": kernel_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": rep.launches_per_step * args.steps,
+            "host_ms_per_step": host_secs / args.steps * 1e3,
             "clocks": clk,
         }
         print(json.dumps(line))
@@ -395,12 +492,13 @@ def run_reference(args):
         return
     batch = make_batch(args.workload, 0)
     per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
+    inp = OracleInputs(batch, None)
     for _ in range(max(args.warmup, 3)):
-        cpu_oracle_sample(batch, None, 0.0, step_units=1)
+        cpu_oracle_sample(batch, inp, 0.0, step_units=1)
     t0 = time.perf_counter()
     units = 0
     for _ in range(args.steps):
-        _, u, _ = cpu_oracle_sample(batch, None, 0.0, step_units=per_step_units)
+        _, u, _ = cpu_oracle_sample(batch, inp, 0.0, step_units=per_step_units)
         units += u
     secs = time.perf_counter() - t0
     value = units / batch.num_layers / secs

@@ -136,6 +136,9 @@ PA_API int pa_paged_attention_decode_workspace_size(int num_seqs, int num_q_head
  * the device: 0 <= n <= max_blocks_per_seq * 16 and every table entry read
  * in [0, num_blocks) -- a violation is clamped and sets PA_ERR_DEVICE_BOUNDS.
  *
+ * Slots of the last block past the context are never read into the result,
+ * whatever they hold (NaN included).
+ *
  * The workspace belongs to one call at a time: two calls sharing it must be
  * ordered on the same stream.  It needs no initialisation.
  * ---------------------------------------------------------------------- */
@@ -145,6 +148,34 @@ PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const v
                                      int head_dim, int max_blocks_per_seq, int num_blocks,
                                      float scale, int dtype, void* out, void* workspace,
                                      size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_plan / pa_paged_attention_decode_run -- the same
+ * computation as pa_paged_attention_decode, split so that one plan serves
+ * every layer of a decode step.
+ *
+ * The plan (a one-block kernel) turns context_lens into the work list of the
+ * attention kernel and stores it in the workspace; it depends only on the
+ * context lengths and the shapes, which are the same for every layer of a
+ * step ("vLLM: treating the KV cache as virtual memory", section
+ * 调度：词一级的进入与退出: one scheduling decision per generated token).
+ * Any number of runs may follow one plan, in stream order, with the same
+ * context_lens values, num_seqs, head counts, head_dim, max_blocks_per_seq and
+ * workspace; each run leaves the workspace ready for the next.  A run whose
+ * workspace holds no plan for its shapes does nothing and sets the status
+ * word (pa_check_status returns PA_ERR_INVALID_ARG).  After a run that timed
+ * out, plan again.  F32 runs do not use the plan.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_plan(const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int max_blocks_per_seq, int num_blocks,
+                                         float scale, int dtype, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * pa_block_copy -- copy-on-write block copies, all layers in one launch.
@@ -167,8 +198,9 @@ PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_l
 
 /* ------------------------------------------------------------------------
  * pa_check_status -- synchronise `stream`, then read and clear the device
- * status word of the current device.  Returns PA_OK, PA_ERR_DEVICE_BOUNDS or
- * PA_ERR_DEVICE_TIMEOUT (or PA_ERR_CUDA if the synchronisation failed).
+ * status word of the current device.  Returns PA_OK, PA_ERR_DEVICE_BOUNDS,
+ * PA_ERR_DEVICE_TIMEOUT, PA_ERR_INVALID_ARG (a decode run found no plan in
+ * its workspace), or PA_ERR_CUDA if the synchronisation failed.
  * ---------------------------------------------------------------------- */
 PA_API int pa_check_status(void* stream);
 

@@ -5,7 +5,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
 
 * :func:`kv_append` -- write new tokens' K/V rows into their paged slots;
 * :func:`paged_attention_decode` -- one decode step of attention over a block
-  table, MHA and GQA;
+  table, MHA and GQA (:func:`paged_attention_decode_plan` +
+  :func:`paged_attention_decode_run` split it so one plan serves every layer);
 * :func:`block_copy` -- copy-on-write block copies across all layers;
 
 and the native host :class:`BlockPool` that produces tables, slots and copy
@@ -14,8 +15,10 @@ raises -- there is no fallback implementation.
 """
 
 from .capi import PagedAttnError  # noqa: F401
-from .ops import (alloc_workspace, block_copy, check_status, kv_append,  # noqa: F401
-                  paged_attention_decode, workspace_size)
+from .ops import (Prepared, alloc_workspace, block_copy, check_status, kv_append,  # noqa: F401
+                  paged_attention_decode, paged_attention_decode_plan,
+                  paged_attention_decode_run, prepare_decode_plan, prepare_decode_run,
+                  prepare_kv_append, workspace_size)
 from .pool import BlockPool  # noqa: F401
 
 BLOCK_SIZE = 16

@@ -184,6 +184,9 @@ PA_API int pa_check_status(void* stream) {
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "check_status: %s", cudaGetErrorString(e));
   if (word & kStatusTimeout)
     return fail(PA_ERR_DEVICE_TIMEOUT, "a device-side wait ran out (status word 0x%x)", word);
+  if (word & kStatusPlan)
+    return fail(PA_ERR_INVALID_ARG,
+                "a decode run found no plan for its shapes in the workspace (status 0x%x)", word);
   if (word & kStatusBounds)
     return fail(PA_ERR_DEVICE_BOUNDS, "a kernel saw an out-of-range block id, slot or length");
   return PA_OK;

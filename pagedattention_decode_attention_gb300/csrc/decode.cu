@@ -12,28 +12,36 @@
 //  * plan kernel (1 CTA): splits every sequence into work items of up to
 //    kSplitBlocks logical blocks (512 tokens), one item per (sequence, KV
 //    head, split); full items first, then partial ones by decreasing size, so
-//    the tail of the persistent kernel is made of the smallest items.
-//  * persistent attention kernel, one or two CTAs per SM, three warp roles:
-//      - scheduler warp: takes the next item from a global counter, reads the
-//        item's block-table entries (range-checked) and bulk-copies the G
-//        query rows of (b, g) into a shared-memory item queue;
-//      - TMA warp: for every block of the item issues 2-D tensor copies of the
-//        16 x head_dim K tile and V tile (each a contiguous 2 or 4 KiB run of
-//        the cache) into a ring of kStages shared-memory stages, 128-byte
-//        swizzled, with L2 evict-first hints (the cache is streamed once);
-//      - kConsumerWarps math warps: warp w takes blocks w, w+W, ... of the
-//        item.  Per 16-token block: S^T = K . Q^T on the tensor cores
-//        (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of the
-//        group, K = head_dim), online softmax in base 2 with per-head running
-//        max / sum, P rounded to the input type and transposed in registers
-//        (movmatrix), O^T += V^T . P^T (M = head_dim rows of V^T via
-//        ldmatrix.trans).  Each K/V tile is read from HBM once for the whole
-//        query group.
+//    the tail of the persistent kernel is made of the smallest items.  The
+//    plan depends only on the context lengths, so one plan serves every layer
+//    of a decode step.
+//  * persistent attention kernel, one CTA per SM, three warp roles:
+//      - scheduler warp: takes work items from a global counter (four at a
+//        time, so their dependent global reads overlap), reads each item's
+//        block-table entries (range-checked) and bulk-copies the G query rows
+//        of (b, g) into a shared-memory item queue;
+//      - finisher warp: publishes and counts finished splits (fence + atomic)
+//        so the math warps never wait on device-scope memory ordering;
+//      - W math warps: warp w takes blocks w, w+W, ... of every item and
+//        streams them through its own small ring: it issues the 2-D tensor
+//        copies (128-byte swizzled, L2 evict-first) of the K tile and V tile
+//        of a block NS blocks before it needs them.  Many independent issuers
+//        keep HBM busy; a single issuing thread per CTA could not (each copy
+//        instruction costs it hundreds of cycles).  Per 16-token block:
+//        S^T = K . Q^T on the tensor cores (m16n8k16, M = the 16 tokens,
+//        N = the G <= 8 query heads of the group, K = head_dim), online softmax
+//        in base 2 with per-head running max / sum, P rounded to the input
+//        type and transposed in registers (movmatrix), O^T += V^T . P^T
+//        (M = head_dim rows of V^T via ldmatrix.trans).  Each K/V tile is read
+//        from HBM once for the whole query group.  Slots past the context in
+//        the last block are zeroed in registers, so whatever bits they hold
+//        cannot reach the output.
 //    At the end of an item the math warps merge their partial (m, l, O)
 //    through shared memory.  A sequence with one split writes `out`
 //    directly; otherwise the item writes (o, lse) to the workspace and the
 //    CTA that finishes the last split of (b, g) merges all splits with
-//    log-sum-exp weights (an arrival counter, no spinning).
+//    log-sum-exp weights (an arrival counter, no spinning).  The work and
+//    arrival counters return to zero by the end of every run.
 //  * Every wait is an mbarrier wait with a time limit; running out sets the
 //    timeout bit of the device status word and the warp returns.
 //
@@ -44,10 +52,11 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
-#include <cfloat>
+#include <algorithm>
 #include <cmath>
-#include <cstring>
+#include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "decode.cuh"
 #include "device_common.cuh"
@@ -60,261 +69,420 @@ namespace decode {
 using dev::mbar_arrive;
 using dev::mbar_wait_bounded;
 
+// Optional cycle accounting per CTA and warp role, compiled in only with
+// -DPA_PROFILE (a separate build used to see where a persistent CTA spends its
+// time; the default build has none of it).
+#ifdef PA_PROFILE
+constexpr int kProfSlots = 16;
+__device__ unsigned long long g_prof[2048 * kProfSlots];
+#define PROF_T(var) const long long var = clock64()
+#define PROF_ADD(slot, t0)                                                                  \
+  do {                                                                                      \
+    if ((threadIdx.x & 31) == 0)                                                            \
+      atomicAdd(&g_prof[blockIdx.x * kProfSlots + (slot)],                                  \
+                static_cast<unsigned long long>(clock64() - (t0)));                         \
+  } while (0)
+#define PROF_INC(slot, v)                                                                   \
+  do {                                                                                      \
+    if ((threadIdx.x & 31) == 0)                                                            \
+      atomicAdd(&g_prof[blockIdx.x * kProfSlots + (slot)], static_cast<unsigned long long>(v)); \
+  } while (0)
+#else
+#define PROF_T(var)
+#define PROF_ADD(slot, t0)
+#define PROF_INC(slot, v)
+#endif
+
 template <int D>
 struct alignas(128) ItemSlot {
-  int b, g, s, ctx, nblk, nsplit, pad0, pad1;
+  int b, g, s, ctx, nblk, nsplit, first, pad0;
   int blocks[kSplitBlocks];
   alignas(16) uint16_t q[kMaxGroup * D];
 };
 
-template <int D>
+template <int D, int W>
 struct Smem {
   static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, head) tile
   static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
-  static constexpr size_t kRing = size_t(kStages) * kStageBytes;
   static constexpr size_t kItems = size_t(kQueue) * sizeof(ItemSlot<D>);
   static constexpr int kOPitch = D + 4;                  // floats; breaks bank conflicts
-  __host__ __device__ static size_t merge_o_floats(int group) { return size_t(2) * kConsumerWarps * group * kOPitch; }
-  static constexpr size_t kMergeMl = size_t(2) * kConsumerWarps * kMaxGroup * 2;  // floats
-  static constexpr size_t kBars = 2 * kStages + 2 * kQueue + 3;                   // uint64
-  static size_t bytes(int group) {
-    return 1024 /* alignment slack */ + kRing + kItems + merge_o_floats(group) * 4 +
-           kMergeMl * 4 + kBars * 8 + 16;
+  __host__ __device__ static size_t merge_o_floats(int group) {
+    return size_t(W) * group * kOPitch;
+  }
+  static constexpr size_t kMergeMl = size_t(W) * kMaxGroup * 2;  // floats
+  // barriers (uint64) + fin_info (int4 = 2 slots each) + verdicts
+  static constexpr size_t kBars = size_t(W) * kWarpStages + 2 * kQueue + 2 + 2 * kFinRing +
+                                  2 * kFinRing + kFinRing + 2;
+  static size_t fixed_bytes(int group) {
+    return 1024 /* alignment slack */ + kItems + merge_o_floats(group) * 4 + kMergeMl * 4 +
+           kBars * 8 + 16;
+  }
+  // `stages` is per math warp
+  static size_t bytes(int group, int stages) {
+    return fixed_bytes(group) + size_t(W) * stages * kStageBytes;
+  }
+  static int stages_for(int group, size_t budget) {
+    const long avail = long(budget) - long(fixed_bytes(group));
+    long s = avail / (long(W) * kStageBytes);
+    if (s > kWarpStages) s = kWarpStages;
+    return int(s);
   }
 };
 
 // ------------------------------------------------------------------ plan
-__global__ void __launch_bounds__(1024) plan_kernel(const Params p, int out_row_vecs) {
-  __shared__ int hist[kSplitBlocks];
-  __shared__ int bucket[kSplitBlocks];
-  __shared__ int warp_tot[32];
-  __shared__ int carry;
+// Splits of one sequence are balanced: nsplit = ceil(blocks / 32) splits whose
+// sizes differ by at most one block.  Units are then counting-sorted by size,
+// largest first, and a sequence's splits stay adjacent in the order.
+__device__ __forceinline__ void split_shape(int nblk, int& nsplit, int& base, int& big) {
+  nsplit = (nblk + kSplitBlocks - 1) / kSplitBlocks;
+  base = nsplit ? nblk / nsplit : 0;
+  big = nsplit ? nblk - base * nsplit : 0;  // the first `big` splits hold base + 1 blocks
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
+  __shared__ int hist[kSplitBlocks + 2];
+  __shared__ int bucket[kSplitBlocks + 2];
   dev::grid_launch_dependents();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid < kSplitBlocks) hist[tid] = 0;
-  if (tid == 0) carry = 0;
+  const int tid = threadIdx.x;
+  if (tid < kSplitBlocks + 2) hist[tid] = 0;
   __syncthreads();
   const int cap = p.max_blocks * kBlockSize;
   int4* units = reinterpret_cast<int4*>(p.ws.units);
 
-  for (int base = 0; base < p.num_seqs; base += 1024) {
-    const int b = base + tid;
-    int nfull = 0, ctx = 0;
-    if (b < p.num_seqs) {
-      ctx = p.context_lens[b];
-      if (ctx < 0 || ctx > cap) {
-        dev::flag_status(p.status, kStatusBounds);
-        ctx = ctx < 0 ? 0 : cap;
-      }
-      const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
-      nfull = nblk / kSplitBlocks;
-      const int rem = nblk % kSplitBlocks;
-      if (rem) atomicAdd(&hist[rem], 1);
-      for (int g = 0; g < p.num_kv_heads; ++g) p.ws.arrivals[size_t(b) * p.num_kv_heads + g] = 0;
-      if (ctx == 0) {  // empty context: zero output row
-        uint4* row = reinterpret_cast<uint4*>(p.out) + size_t(b) * out_row_vecs;
-        for (int i = 0; i < out_row_vecs; ++i) row[i] = make_uint4(0, 0, 0, 0);
-      }
+  for (int b = tid; b < p.num_seqs; b += 1024) {
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > cap) {
+      dev::flag_status(p.status, kStatusBounds);
+      ctx = ctx < 0 ? 0 : cap;
     }
-    // block-wide exclusive scan of nfull
-    int incl = nfull;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-      int t = warp_tot[lane], ti = t;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, ti, o);
-        if (lane >= o) ti += y;
-      }
-      warp_tot[lane] = ti - t;
-    }
-    __syncthreads();
-    const int excl = carry + warp_tot[warp] + incl - nfull;
-    for (int k = 0; k < nfull; ++k) units[excl + k] = make_int4(b, k, ctx, kSplitBlocks);
-    __syncthreads();
-    if (tid == 1023) carry = excl + nfull;
-    __syncthreads();
+    int nsplit, base, big;
+    split_shape((ctx + kBlockSize - 1) / kBlockSize, nsplit, base, big);
+    if (big) atomicAdd(&hist[base + 1], big);
+    if (nsplit - big) atomicAdd(&hist[base], nsplit - big);
+    for (int g = 0; g < p.num_kv_heads; ++g) p.ws.arrivals[size_t(b) * p.num_kv_heads + g] = 0;
   }
+  __syncthreads();
   if (tid == 0) {
-    int pos = carry;
-    for (int r = kSplitBlocks - 1; r >= 1; --r) {
+    int pos = 0;
+    for (int r = kSplitBlocks; r >= 1; --r) {
       bucket[r] = pos;
       pos += hist[r];
     }
-    p.ws.header[1] = pos * p.num_kv_heads;
-    p.ws.header[0] = 0;
+    p.ws.header[kHdrTotal] = pos * p.num_kv_heads;
+    p.ws.header[kHdrNext] = 0;
+    p.ws.header[kHdrDone] = 0;
+    p.ws.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
   for (int b = tid; b < p.num_seqs; b += 1024) {
     int ctx = p.context_lens[b];
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
-    const int nblk = (ctx + kBlockSize - 1) / kBlockSize;
-    const int rem = nblk % kSplitBlocks;
-    if (rem) {
-      const int pos = atomicAdd(&bucket[rem], 1);
-      units[pos] = make_int4(b, nblk / kSplitBlocks, ctx, rem);
+    int nsplit, base, big;
+    split_shape((ctx + kBlockSize - 1) / kBlockSize, nsplit, base, big);
+    const int at_big = big ? atomicAdd(&bucket[base + 1], big) : 0;
+    const int at_small = nsplit - big ? atomicAdd(&bucket[base], nsplit - big) : 0;
+    int first = 0;
+    for (int s = 0; s < nsplit; ++s) {
+      const int n = s < big ? base + 1 : base;
+      const int pos = s < big ? at_big + s : at_small + (s - big);
+      units[pos] = make_int4(b, (s << 8) | n, first, ctx);
+      first += n;
     }
   }
 }
 
 // --------------------------------------------------------- tensor-core path
-template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                          const __grid_constant__ CUtensorMap tmap_v,
-                                                          const Params p) {
-  using S = Smem<D>;
+template <typename T, int D, int W>
+__global__ void __launch_bounds__((W + 2) * 32)
+    decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  using S = Smem<D, W>;
   using M = dev::Mma<T>;
-  constexpr int W = kConsumerWarps;
-  constexpr int KT = D / 16;  // 16-wide steps along head_dim
+  constexpr int KT = D / 16;        // 16-wide steps along head_dim
+  constexpr int HALVES = D / 64;    // 128-byte TMA boxes per tile row
+  constexpr int R = kFinRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int G = p.group;
-  uint8_t* ring = smem;
-  ItemSlot<D>* items = reinterpret_cast<ItemSlot<D>*>(ring + S::kRing);
+  const int NS = p.stages;  // ring stages per math warp
+  uint8_t* rings = smem;
+  ItemSlot<D>* items =
+      reinterpret_cast<ItemSlot<D>*>(rings + size_t(W) * NS * S::kStageBytes);
   float* merge_o = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(items) + S::kItems);
   float* merge_ml = merge_o + S::merge_o_floats(G);
-  uint64_t* full = reinterpret_cast<uint64_t*>(merge_ml + S::kMergeMl);
-  uint64_t* empty = full + kStages;
-  uint64_t* item_full = empty + kStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(merge_ml + S::kMergeMl);  // [W][kWarpStages]
+  uint64_t* item_full = full + W * kWarpStages;
   uint64_t* item_empty = item_full + kQueue;
-  uint64_t* mb_merge = item_empty + kQueue;
-  uint64_t* mb_fence = mb_merge + 1;
-  uint64_t* mb_flag = mb_fence + 1;
-  volatile int* last_flag = reinterpret_cast<volatile int*>(mb_flag + 1);
+  uint64_t* mb_merge = item_empty + kQueue;  // all math threads wrote their partial state
+  uint64_t* mb_read = mb_merge + 1;          // all math threads finished reading it
+  uint64_t* mb_done = mb_read + 1;           // [R] an item's outputs are written
+  uint64_t* mb_verdict = mb_done + R;        // [R] the finisher's verdict is published
+  int4* fin_info = reinterpret_cast<int4*>(                   // [R] b, g, nsplit, -
+      (reinterpret_cast<uintptr_t>(mb_verdict + R) + 15) & ~uintptr_t(15));
+  volatile int* verdict = reinterpret_cast<volatile int*>(fin_info + R);  // [R]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      dev::mbar_init(&full[i], 1);
-      dev::mbar_init(&empty[i], 1);
-    }
+    for (int i = 0; i < W * kWarpStages; ++i) dev::mbar_init(&full[i], 1);
     for (int i = 0; i < kQueue; ++i) {
-      dev::mbar_init(&item_full[i], 32);
-      dev::mbar_init(&item_empty[i], W + 1);
+      dev::mbar_init(&item_full[i], 8);  // the lanes of one scheduler group
+      dev::mbar_init(&item_empty[i], W);
     }
     dev::mbar_init(mb_merge, W * 32);
-    dev::mbar_init(mb_fence, W * 32);
-    dev::mbar_init(mb_flag, 1);
+    dev::mbar_init(mb_read, W * 32);
+    for (int i = 0; i < R; ++i) {
+      dev::mbar_init(&mb_done[i], W * 32);
+      dev::mbar_init(&mb_verdict[i], 1);
+    }
     dev::mbar_fence_init();
   }
-  if (warp == W) {
+  if (warp < W && lane == 0) {
     dev::prefetch_tensormap(&tmap_k);
     dev::prefetch_tensormap(&tmap_v);
   }
   __syncthreads();
-  dev::grid_dependency_wait();  // the plan kernel's work list is complete
+  dev::grid_dependency_wait();  // a plan launched just before has completed
 
+  PROF_T(t_kernel);
   const unsigned long long tmo = p.timeout_ns;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
+  const bool planned =
+      *reinterpret_cast<volatile int*>(&p.ws.header[kHdrSignature]) == p.signature;
 
-  if (warp == W + 1) {
+  if (warp == W) {
     // ------------------------------------------------------------ scheduler
-    const int total = *reinterpret_cast<volatile int*>(&p.ws.header[1]);
-    const int4* units = reinterpret_cast<const int4*>(p.ws.units);
-    for (int it = 0;; ++it) {
-      int idx = 0;
-      if (lane == 0) idx = atomicAdd(&p.ws.header[0], 1);
-      idx = __shfl_sync(0xffffffffu, idx, 0);
-      const int qs = it % kQueue;
-      if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
-      ItemSlot<D>& sl = items[qs];
-      if (idx >= total) {
-        if (lane == 0) sl.b = -1;
-        mbar_arrive(&item_full[qs]);
-        return;
-      }
-      const int4 u = units[idx / Hkv];
-      const int g = idx % Hkv;
-      const int b = u.x, s = u.y, ctx = u.z, nblk = u.w;
-      int phys = 0;
-      if (lane < nblk) {
-        phys = p.block_tables[size_t(b) * p.max_blocks + s * kSplitBlocks + lane];
-        if (phys < 0 || phys >= p.num_blocks) {
-          dev::flag_status(p.status, kStatusBounds);
-          phys = 0;
+    // Four lane groups of 8 fetch four work items at once, so the dependent
+    // global round trips of an item (counter -> unit -> table entries) overlap.
+    if (!planned) {
+      if (lane == 0 && blockIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+    } else {
+      // rows of empty sequences are zero
+      for (int b = blockIdx.x * 32 + lane; b < p.num_seqs; b += gridDim.x * 32) {
+        if (p.context_lens[b] <= 0) {
+          uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
+          for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
         }
-      }
-      sl.blocks[lane] = phys;
-      if (lane == 0) {
-        const int nblk_all = (ctx + kBlockSize - 1) / kBlockSize;
-        sl.b = b;
-        sl.g = g;
-        sl.s = s;
-        sl.ctx = ctx;
-        sl.nblk = nblk;
-        sl.nsplit = (nblk_all + kSplitBlocks - 1) / kSplitBlocks;
-        const uint32_t qbytes = uint32_t(G) * D * 2;
-        dev::mbar_arrive_expect_tx(&item_full[qs], qbytes);
-        dev::bulk_load(sl.q,
-                       static_cast<const uint8_t*>(p.q) + (size_t(b) * Hq + size_t(g) * G) * D * 2,
-                       qbytes, &item_full[qs]);
-      } else {
-        mbar_arrive(&item_full[qs]);
       }
     }
-  } else if (warp == W) {
-    // ---------------------------------------------------------- TMA issuer
-    const uint64_t policy = dev::l2_policy_evict_first();
-    int n = 0;
-    for (int it = 0;; ++it) {
-      const int qs = it % kQueue;
-      if (!mbar_wait_bounded(&item_full[qs], (it / kQueue) & 1, tmo, p.status)) return;
-      const ItemSlot<D>& sl = items[qs];
-      const int b = sl.b;
-      const int nblk = b < 0 ? 0 : sl.nblk;
-      const int g = sl.g;
-      const int my_phys = sl.blocks[lane];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&item_empty[qs]);
-      if (b < 0) return;
-      for (int j = 0; j < nblk; ++j, ++n) {
-        const int phys = __shfl_sync(0xffffffffu, my_phys, j);
-        if (lane == 0) {
-          const int st = n % kStages;
-          if (!mbar_wait_bounded(&empty[st], ((n / kStages) & 1) ^ 1, tmo, p.status)) {
-            // Let the copies already issued land before the CTA exits.
-            for (int k = 1; k <= kStages && n - k >= 0; ++k) {
-              const int m = n - k;
-              mbar_wait_bounded(&full[m % kStages], (m / kStages) & 1, tmo, p.status);
-            }
-            n = -1;
-          } else {
-            dev::mbar_arrive_expect_tx(&full[st], S::kStageBytes);
-            uint8_t* stage = ring + size_t(st) * S::kStageBytes;
-            const int y = (phys * Hkv + g) * kBlockSize;
+    const int total = planned ? *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]) : 0;
+    const int4* units = reinterpret_cast<const int4*>(p.ws.units);
+    const int grp = lane >> 3, gl = lane & 7;
+    int it = 0;
+    for (bool more = true; more;) {
+      PROF_T(t_fetch);
+      int idx = total;
+      if (planned && gl == 0) idx = atomicAdd(&p.ws.header[kHdrNext], 1);
+      idx = __shfl_sync(0xffffffffu, idx, grp * 8);
+      const bool valid = idx < total;
+      int4 u = make_int4(0, 0, 0, 0);
+      if (valid) u = units[idx / Hkv];
+      const int g = valid ? idx % Hkv : 0;
+      const int b = u.x, s = u.y >> 8, nblk = u.y & 0xff, first = u.z, ctx = u.w;
+      int phys[kSplitBlocks / 8];
 #pragma unroll
-            for (int h = 0; h < D / 64; ++h) {
-              dev::tma_load_2d(stage + h * 2048, &tmap_k, h * 64, y, &full[st], policy);
-              dev::tma_load_2d(stage + S::kTileBytes + h * 2048, &tmap_v, h * 64, y, &full[st],
-                               policy);
-            }
+      for (int e = 0; e < kSplitBlocks / 8; ++e) {
+        const int j = gl + 8 * e;
+        phys[e] = 0;
+        if (valid && j < nblk) {
+          phys[e] = p.block_tables[size_t(b) * p.max_blocks + first + j];
+          if (phys[e] < 0 || phys[e] >= p.num_blocks) {
+            dev::flag_status(p.status, kStatusBounds);
+            phys[e] = 0;
           }
         }
-        n = __shfl_sync(0xffffffffu, n, 0);
-        if (n < 0) return;
+      }
+      more = __all_sync(0xffffffffu, valid);
+      PROF_ADD(7, t_fetch);
+      // push the valid items of this round in group order
+      for (int q = 0; q < 4; ++q) {
+        if (!__shfl_sync(0xffffffffu, valid, q * 8)) continue;
+        const int qs = it % kQueue;
+        PROF_T(t_slot);
+        if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
+        PROF_ADD(8, t_slot);
+        if (grp == q) {
+          ItemSlot<D>& sl = items[qs];
+#pragma unroll
+          for (int e = 0; e < kSplitBlocks / 8; ++e) sl.blocks[gl + 8 * e] = phys[e];
+          if (gl == 0) {
+            const int nblk_all = (ctx + kBlockSize - 1) / kBlockSize;
+            sl.b = b;
+            sl.g = g;
+            sl.s = s;
+            sl.ctx = ctx;
+            sl.nblk = nblk;
+            sl.nsplit = (nblk_all + kSplitBlocks - 1) / kSplitBlocks;
+            sl.first = first;
+            const uint32_t qbytes = uint32_t(G) * D * 2;
+            dev::mbar_arrive_expect_tx(&item_full[qs], qbytes);
+            dev::bulk_load(sl.q,
+                           static_cast<const uint8_t*>(p.q) +
+                               (size_t(b) * Hq + size_t(g) * G) * D * 2,
+                           qbytes, &item_full[qs]);
+          } else {
+            mbar_arrive(&item_full[qs]);
+          }
+        }
+        ++it;
+      }
+    }
+    // no more work: queue the end marker
+    const int qs = it % kQueue;
+    if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
+    if (grp == 0) {
+      if (gl == 0) items[qs].b = -1;
+      mbar_arrive(&item_full[qs]);
+    }
+    if (planned && lane == 0) {
+      // The last scheduler to finish returns the work counters to zero, so the
+      // next run on this plan starts clean.
+      __threadfence();
+      if (atomicAdd(&p.ws.header[kHdrDone], 1) == int(gridDim.x) - 1) {
+        atomicExch(&p.ws.header[kHdrNext], 0);
+        atomicExch(&p.ws.header[kHdrDone], 0);
+      }
+    }
+  } else if (warp == W + 1) {
+    // ------------------------------------------------------------- finisher
+    // Split bookkeeping off the math warps' path: after the math threads have
+    // written an item's partial result, publish it device-wide and count the
+    // split; tell the math warps (R items later) whether this CTA finished the
+    // last split of (b, g).
+    for (int k = 0;; ++k) {
+      const int slot = k % R;
+      if (!mbar_wait_bounded(&mb_done[slot], (k / R) & 1, tmo, p.status)) return;
+      const int4 info = fin_info[slot];
+      if (info.x < 0) return;
+      int last = 0;
+      if (info.z > 1) {
+        __threadfence();  // the item's partials (released to us at CTA scope) go device-wide
+        if (lane == 0) {
+          last = atomicAdd(&p.ws.arrivals[size_t(info.x) * Hkv + info.y], 1) == info.z - 1;
+          __threadfence();  // and the other CTAs' partials are visible before we say so
+        }
+      }
+      if (lane == 0) {
+        verdict[slot] = last;
+        mbar_arrive(&mb_verdict[slot]);
       }
     }
   } else {
     // -------------------------------------------------------- math warps
+    // Each math warp streams its own blocks (w, w+W, ... of every item) through
+    // a private ring of NS stages, issuing the copies of a block NS blocks before
+    // it needs it: many independent issuers keep HBM busy where one issuer per
+    // CTA could not.
     const int w = warp;
     const int tid = threadIdx.x;  // 0 .. W*32-1
     const int n0 = 2 * (lane & 3), n1 = n0 + 1;
-    uint32_t merge_phase = 0, fence_phase = 0, flag_phase = 0;
-    int n_base = 0;
+    const uint64_t policy = dev::l2_policy_evict_first();
+    uint8_t* ring = rings + size_t(w) * NS * S::kStageBytes;
+    uint64_t* my_full = full + w * kWarpStages;
+
+    // issue cursor: item ii, block ij of it, ik blocks issued so far
+    int ii = 0, ij = w, ik = 0, inblk = -1, ig = 0;
+    const ItemSlot<D>* isl = nullptr;
+    bool idone = false;
+    // Issues this warp's next blocks until NS are in flight.  It never waits
+    // for an item whose queue slot this CTA still holds (it_c + kQueue on).
+    auto top_up = [&](int it_c, int kc) -> bool {
+      while (!idone && ik < kc + NS) {
+        if (inblk < 0) {
+          if (ii >= it_c + kQueue) return true;
+          if (!mbar_wait_bounded(&item_full[ii % kQueue], (ii / kQueue) & 1, tmo, p.status))
+            return false;
+          isl = &items[ii % kQueue];
+          if (isl->b < 0) {
+            idone = true;
+            return true;
+          }
+          inblk = isl->nblk;
+          ig = isl->g;
+        }
+        if (ij >= inblk) {
+          ++ii;
+          ij = w;
+          inblk = -1;
+          continue;
+        }
+        const int phys = isl->blocks[ij];
+        const int st = ik % NS;
+        if (lane == 0) dev::mbar_arrive_expect_tx(&my_full[st], S::kStageBytes);
+        __syncwarp();
+        if (lane < 2 * HALVES) {  // lanes 0..3 (d = 128) issue the K and V boxes
+          const int which = lane / HALVES, h = lane % HALVES;
+          uint8_t* dst = ring + size_t(st) * S::kStageBytes + which * S::kTileBytes + h * 2048;
+          const int y = (phys * Hkv + ig) * kBlockSize;
+          dev::tma_load_2d(dst, which ? static_cast<const void*>(&tmap_v) : &tmap_k, h * 64, y,
+                           &my_full[st], policy);
+        }
+        ++ik;
+        ij += W;
+      }
+      return true;
+    };
+    // On a timeout: let this warp's copies in flight land, then give up.
+    auto drain = [&](int kc) {
+      if (lane == 0)
+        for (int k = kc; k < ik; ++k) mbar_wait_bounded(&my_full[k % NS], (k / NS) & 1, tmo, p.status);
+      __syncwarp();
+    };
+
+    // Merges all splits of (b, g) once the finisher says this CTA completed the
+    // last one (all math threads, one output element each).
+    auto merge_splits = [&](const int4 info) {
+      const int b = info.x, g = info.y, nsplit = info.z;
+      const size_t head0 = size_t(b) * Hq + size_t(g) * G;
+      const size_t pbase = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+      for (int e = tid; e < G * D; e += W * 32) {
+        const int hh = e / D, dd = e - hh * D;
+        float mrun = -INFINITY, lrun = 0.f, acc = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const size_t r = pbase + size_t(sp) * Hq + hh;
+          const float lse = __ldcg(&p.ws.part_lse[r]);
+          const float ov = __ldcg(&p.ws.part_o[r * D + dd]);
+          const float mn = fmaxf(mrun, lse);
+          const float a = dev::fast_exp2(mrun - mn), wv = dev::fast_exp2(lse - mn);
+          acc = acc * a + wv * ov;
+          lrun = lrun * a + wv;
+          mrun = mn;
+        }
+        static_cast<T*>(p.out)[(head0 + hh) * D + dd] = M::from_float(acc / lrun);
+      }
+      if (tid == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+    };
+    // Collects the finisher's verdict on item k (and merges if this CTA was last).
+    auto settle = [&](int k) -> bool {
+      const int slot = k % R;
+      if (!mbar_wait_bounded(&mb_verdict[slot], (k / R) & 1, tmo, p.status)) return false;
+      if (verdict[slot]) merge_splits(fin_info[slot]);
+      return true;
+    };
+
+    int kc = 0;  // blocks consumed so far
     for (int it = 0;; ++it) {
       const int qs = it % kQueue;
-      if (!mbar_wait_bounded(&item_full[qs], (it / kQueue) & 1, tmo, p.status)) return;
+      PROF_T(t_item);
+      if (!mbar_wait_bounded(&item_full[qs], (it / kQueue) & 1, tmo, p.status)) {
+        drain(kc);
+        return;
+      }
+      PROF_ADD(3, t_item);
       const ItemSlot<D>& sl = items[qs];
       const int b = sl.b;
-      if (b < 0) return;
+      if (b < 0) {
+        PROF_ADD(11, t_kernel);
+        // drain: settle the items still in the finisher's hands, then stop it
+        for (int k = it - R; k < it; ++k)
+          if (k >= 0 && !settle(k)) return;
+        const int slot = it % R;
+        if (tid == 0) fin_info[slot] = make_int4(-1, 0, 0, 0);
+        mbar_arrive(&mb_done[slot]);
+        return;
+      }
       const int g = sl.g, s = sl.s, ctx = sl.ctx, nblk = sl.nblk, nsplit = sl.nsplit;
+      const int first = sl.first;
       // B fragments of Q^T (k = head_dim, n = query head of the group)
       uint32_t qb0[KT], qb1[KT];
       {
@@ -326,8 +494,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
           qb1[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&item_empty[qs]);
+      if (!top_up(it, kc)) {
+        drain(kc);
+        return;
+      }
 
       float o[KT][4];
 #pragma unroll
@@ -336,9 +506,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
       const float sl2 = p.scale_log2;
 
       for (int j = w; j < nblk; j += W) {
-        const int nn = n_base + j;
-        const int st = nn % kStages;
-        if (!mbar_wait_bounded(&full[st], (nn / kStages) & 1, tmo, p.status)) return;
+        const int st = kc % NS;
+        PROF_T(t_full);
+        if (!mbar_wait_bounded(&my_full[st], (kc / NS) & 1, tmo, p.status)) {
+          drain(kc);
+          return;
+        }
+        PROF_ADD(0, t_full);
+        PROF_T(t_blk);
         const uint32_t kt = dev::smem_u32(ring + size_t(st) * S::kStageBytes);
         const uint32_t vt = kt + S::kTileBytes;
         // ---- S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8)
@@ -359,8 +534,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
           }
         }
         // ---- mask, scale to base 2, online softmax per head column
-        const int tok0 = (s * kSplitBlocks + j) * kBlockSize + (lane >> 2);
-        const bool v0 = tok0 < ctx, v1 = tok0 + 8 < ctx;
+        const int valid = ctx - (first + j) * kBlockSize;  // tokens of the block in context
+        const int r0 = lane >> 2;
+        const bool v0 = r0 < valid, v1 = r0 + 8 < valid;
         const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
         const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
         const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
@@ -392,6 +568,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         // ---- P^T as the B operand: transpose the two 8x8 halves in registers
         const uint32_t pb0 = dev::movmatrix_trans(p01);
         const uint32_t pb1 = dev::movmatrix_trans(p23);
+        // V^T fragments hold tokens 2(lane%4)+{0,1} (a0, a1) and +8 (a2, a3):
+        // zero the ones past the context so their bits never meet P = 0.
+        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+        if (valid < kBlockSize) {
+          const int t = 2 * (lane & 3);
+          vm_lo = (t < valid ? 0x0000ffffu : 0u) | (t + 1 < valid ? 0xffff0000u : 0u);
+          vm_hi = (t + 8 < valid ? 0x0000ffffu : 0u) | (t + 9 < valid ? 0xffff0000u : 0u);
+        }
         // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8)
         {
           const int tok = (lane & 7) + ((lane >> 4) << 3);
@@ -402,13 +586,22 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
                 vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
             uint32_t a0, a1, a2, a3;
             dev::ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-            M::run(o[mt], a0, a1, a2, a3, pb0, pb1);
+            M::run(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
           }
         }
+        // the stage is read; order those reads before the copy that reuses it
+        dev::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
+        ++kc;
+        PROF_ADD(1, t_blk);
+        PROF_INC(9, 1);
+        if (!top_up(it, kc)) {
+          drain(kc);
+          return;
+        }
       }
-      n_base += nblk;
+      PROF_T(t_end);
+      PROF_INC(10, 1);
 
       // ---- merge the W warps' partial states through shared memory
 #pragma unroll
@@ -416,9 +609,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
       }
-      const int pb = it & 1;
-      float* ow = merge_o + (size_t(pb) * W + w) * G * S::kOPitch;
-      float* mlw = merge_ml + (size_t(pb) * W + w) * kMaxGroup * 2;
+      // the previous item's readers are done with the scratch
+      if (it > 0 && !mbar_wait_bounded(mb_read, (it - 1) & 1, tmo, p.status)) {
+        drain(kc);
+        return;
+      }
+      float* ow = merge_o + size_t(w) * G * S::kOPitch;
+      float* mlw = merge_ml + size_t(w) * kMaxGroup * 2;
       if (lane < 4) {
         if (n0 < G) {
           mlw[n0 * 2] = m0;
@@ -442,24 +639,28 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         }
       }
       mbar_arrive(mb_merge);
-      if (!mbar_wait_bounded(mb_merge, merge_phase, tmo, p.status)) return;
-      merge_phase ^= 1;
+      PROF_T(t_merge);
+      if (!mbar_wait_bounded(mb_merge, it & 1, tmo, p.status)) {
+        drain(kc);
+        return;
+      }
+      PROF_ADD(13, t_merge);
+      // every warp has read this item's descriptor and query: release the slot
+      if (lane == 0) mbar_arrive(&item_empty[qs]);
 
-      const float* obuf = merge_o + size_t(pb) * W * G * S::kOPitch;
-      const float* mlbuf = merge_ml + size_t(pb) * W * kMaxGroup * 2;
       const size_t head0 = size_t(b) * Hq + size_t(g) * G;
       const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
       for (int e = tid; e < G * D; e += W * 32) {
         const int hh = e / D, dd = e - hh * D;
         float mf = -INFINITY;
 #pragma unroll
-        for (int ww = 0; ww < W; ++ww) mf = fmaxf(mf, mlbuf[ww * kMaxGroup * 2 + hh * 2]);
+        for (int ww = 0; ww < W; ++ww) mf = fmaxf(mf, merge_ml[ww * kMaxGroup * 2 + hh * 2]);
         float acc = 0.f, ls = 0.f;
 #pragma unroll
         for (int ww = 0; ww < W; ++ww) {
-          const float wt = dev::fast_exp2(mlbuf[ww * kMaxGroup * 2 + hh * 2] - mf);
-          acc += wt * obuf[(ww * G + hh) * S::kOPitch + dd];
-          ls += wt * mlbuf[ww * kMaxGroup * 2 + hh * 2 + 1];
+          const float wt = dev::fast_exp2(merge_ml[ww * kMaxGroup * 2 + hh * 2] - mf);
+          acc += wt * merge_o[(ww * G + hh) * S::kOPitch + dd];
+          ls += wt * merge_ml[ww * kMaxGroup * 2 + hh * 2 + 1];
         }
         const float val = acc / ls;
         if (nsplit == 1) {
@@ -469,40 +670,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
           if (dd == 0) p.ws.part_lse[part0 + hh] = mf + log2f(ls);
         }
       }
-      if (nsplit > 1) {
-        // ---- the CTA finishing the last split of (b, g) merges all splits
-        __threadfence();
-        mbar_arrive(mb_fence);
-        if (!mbar_wait_bounded(mb_fence, fence_phase, tmo, p.status)) return;
-        fence_phase ^= 1;
-        if (tid == 0) {
-          const int old = atomicAdd(&p.ws.arrivals[size_t(b) * Hkv + g], 1);
-          *last_flag = (old == nsplit - 1);
-          __threadfence();
-          mbar_arrive(mb_flag);
-        }
-        if (!mbar_wait_bounded(mb_flag, flag_phase, tmo, p.status)) return;
-        flag_phase ^= 1;
-        if (*last_flag) {
-          __threadfence();
-          const size_t pbase = size_t(b) * p.max_splits * Hq + size_t(g) * G;
-          for (int e = tid; e < G * D; e += W * 32) {
-            const int hh = e / D, dd = e - hh * D;
-            float mrun = -INFINITY, lrun = 0.f, acc = 0.f;
-            for (int sp = 0; sp < nsplit; ++sp) {
-              const size_t r = pbase + size_t(sp) * Hq + hh;
-              const float lse = __ldcg(&p.ws.part_lse[r]);
-              const float ov = __ldcg(&p.ws.part_o[r * D + dd]);
-              const float mn = fmaxf(mrun, lse);
-              const float a = dev::fast_exp2(mrun - mn), wv = dev::fast_exp2(lse - mn);
-              acc = acc * a + wv * ov;
-              lrun = lrun * a + wv;
-              mrun = mn;
-            }
-            static_cast<T*>(p.out)[(head0 + hh) * D + dd] = M::from_float(acc / lrun);
-          }
-        }
+      mbar_arrive(mb_read);
+      // settle the item that last used this finisher slot (merging its splits
+      // if this CTA finished the last one), then hand this item over
+      PROF_T(t_settle);
+      if (it >= R && !settle(it - R)) {
+        drain(kc);
+        return;
       }
+      PROF_ADD(12, t_settle);
+      const int slot = it % R;
+      if (tid == 0) fin_info[slot] = make_int4(b, g, nsplit, 0);
+      mbar_arrive(&mb_done[slot]);
+      PROF_ADD(2, t_end);
     }
   }
 }
@@ -569,40 +749,89 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+struct KernelConfig {
+  int stages = 0;
+  int ctas_per_sm = 0;
+  size_t smem = 0;
+};
+
+// Tuning knobs read once per process: math warps per CTA (4 or 8), CTAs per
+// SM, and a cap on the ring stages per math warp.  Defaults are the measured
+// best.
+struct Tuning {
+  int warps = kConsumerWarps;
+  int ctas_per_sm = 1;
+  int max_stages = kWarpStages;
+};
+Tuning read_tuning() {
+  Tuning t;
+  if (const char* v = std::getenv("PA_DECODE_WARPS")) t.warps = std::atoi(v) == 4 ? 4 : 8;
+  if (const char* v = std::getenv("PA_DECODE_CTAS_PER_SM")) t.ctas_per_sm = std::max(1, std::min(4, std::atoi(v)));
+  if (const char* v = std::getenv("PA_DECODE_MAX_STAGES")) t.max_stages = std::max(1, std::min(kWarpStages, std::atoi(v)));
+  return t;
+}
+
 struct DeviceState {
   std::once_flag once;
   int error = 0;  // PA_OK or the status the set-up failed with
   int sms = 0;
-  int ctas_per_sm[2][2][kMaxGroup + 1] = {};  // [bf16?][head_dim 128?][group]
+  Tuning tuning;
+  KernelConfig cfg[2][2][kMaxGroup + 1];  // [bf16?][head_dim 128?][group]
 };
 DeviceState g_dev[kMaxDevices];
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-template <typename T, int D>
-cudaError_t configure_kernel(int* ctas) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       int(Smem<D>::bytes(kMaxGroup)));
-  for (int g = 1; g <= kMaxGroup && e == cudaSuccess; ++g)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas[g], decode_kernel<T, D>, kThreads,
-                                                      Smem<D>::bytes(g));
+template <typename T, int D, int W>
+cudaError_t configure_kernel(KernelConfig* cfg, const Tuning& t, size_t optin, size_t per_sm) {
+  // shared memory per CTA when `ctas_per_sm` CTAs share an SM (1 KiB reserved each)
+  size_t budget = per_sm / t.ctas_per_sm - 1024;
+  if (budget > optin) budget = optin;
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, W>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(budget));
+  for (int g = 1; g <= kMaxGroup && e == cudaSuccess; ++g) {
+    int stages = Smem<D, W>::stages_for(g, budget);  // per math warp
+    if (stages > t.max_stages) stages = t.max_stages;
+    cfg[g].stages = stages;
+    cfg[g].smem = Smem<D, W>::bytes(g, stages);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg[g].ctas_per_sm, decode_kernel<T, D, W>,
+                                                      (W + 2) * 32, cfg[g].smem);
+    if (cfg[g].ctas_per_sm > t.ctas_per_sm) cfg[g].ctas_per_sm = t.ctas_per_sm;
+  }
+  return e;
+}
+
+template <int W>
+cudaError_t configure_all(DeviceState& st, size_t optin, size_t per_sm) {
+  cudaError_t e = configure_kernel<__nv_bfloat16, 128, W>(st.cfg[1][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__nv_bfloat16, 64, W>(st.cfg[1][0], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 128, W>(st.cfg[0][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 64, W>(st.cfg[0][0], st.tuning, optin, per_sm);
   return e;
 }
 
 int device_setup(int device) {
   DeviceState& st = g_dev[device];
   std::call_once(st.once, [&] {
-    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+    int optin = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) !=
+            cudaSuccess) {
       st.error = PA_ERR_CUDA;
       return;
     }
-    cudaError_t e = configure_kernel<__nv_bfloat16, 128>(st.ctas_per_sm[1][1]);
-    if (e == cudaSuccess) e = configure_kernel<__nv_bfloat16, 64>(st.ctas_per_sm[1][0]);
-    if (e == cudaSuccess) e = configure_kernel<__half, 128>(st.ctas_per_sm[0][1]);
-    if (e == cudaSuccess) e = configure_kernel<__half, 64>(st.ctas_per_sm[0][0]);
+    st.tuning = read_tuning();
+    cudaError_t e = st.tuning.warps == 4 ? configure_all<4>(st, optin, per_sm)
+                                         : configure_all<8>(st, optin, per_sm);
     st.error = e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    for (int a = 0; a < 2 && st.error == PA_OK; ++a)
+      for (int d = 0; d < 2; ++d)
+        for (int g = 1; g <= kMaxGroup; ++g)
+          if (st.cfg[a][d][g].stages < 1 || st.cfg[a][d][g].ctas_per_sm < 1)
+            st.error = PA_ERR_UNSUPPORTED;
   });
   if (st.error != PA_OK) return fail(st.error, "decode: per-device set-up failed on device %d", device);
   return PA_OK;
@@ -624,7 +853,7 @@ int get_encoder() {
 // 2-D view of a cache: rows = num_blocks * num_kv_heads * 16 token rows of
 // head_dim elements; one copy box = 16 rows x 64 elements (128 bytes wide,
 // 128-byte swizzle).
-int encode_cache_map(CUtensorMap* map, const void* cache, int dtype, int num_blocks,
+int encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, int num_blocks,
                      int num_kv_heads, int head_dim) {
   const cuuint64_t dims[2] = {cuuint64_t(head_dim),
                               cuuint64_t(num_blocks) * num_kv_heads * kBlockSize};
@@ -632,7 +861,7 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int dtype, int num_blo
   const cuuint32_t box[2] = {64, kBlockSize};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapDataType dt =
-      dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUresult r = g_encode(map, dt, 2, const_cast<void*>(cache), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -640,26 +869,199 @@ int encode_cache_map(CUtensorMap* map, const void* cache, int dtype, int num_blo
   return PA_OK;
 }
 
-template <typename T, int D>
-int launch_tc(const Params& prm, const void* k_cache, const void* v_cache, int dtype,
-              cudaStream_t stream, int grid) {
+// Per-thread cache of encoded tensor maps: a decode step reuses the same layer
+// caches every step, and encoding is a host-side driver call.
+struct MapKey {
+  const void* ptr;
+  int num_blocks, num_kv_heads, head_dim;
+  bool bf16;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && num_blocks == o.num_blocks && num_kv_heads == o.num_kv_heads &&
+           head_dim == o.head_dim && bf16 == o.bf16;
+  }
+};
+struct MapEntry {
+  MapKey key{nullptr, 0, 0, 0, false};
+  alignas(64) CUtensorMap map;
+};
+constexpr int kMapCache = 256;
+thread_local MapEntry t_maps[kMapCache];
+
+int cached_cache_map(CUtensorMap* out, const void* cache, bool bf16, int num_blocks,
+                     int num_kv_heads, int head_dim) {
+  const MapKey key{cache, num_blocks, num_kv_heads, head_dim, bf16};
+  uint64_t h = reinterpret_cast<uintptr_t>(cache) >> 8;
+  h ^= uint64_t(num_blocks) * 0x9E3779B97F4A7C15ull ^ uint64_t(num_kv_heads * 131 + head_dim);
+  MapEntry& e = t_maps[(h ^ (h >> 17)) % kMapCache];
+  if (!(e.key == key)) {
+    int rc = encode_cache_map(&e.map, cache, bf16, num_blocks, num_kv_heads, head_dim);
+    if (rc != PA_OK) {
+      e.key = MapKey{nullptr, 0, 0, 0, false};
+      return rc;
+    }
+    e.key = key;
+  }
+  *out = e.map;
+  return PA_OK;
+}
+
+template <typename T, int D, int W>
+int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) {
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   alignas(64) CUtensorMap mk, mv;
-  int rc = encode_cache_map(&mk, k_cache, dtype, prm.num_blocks, prm.num_kv_heads, D);
-  if (rc == PA_OK) rc = encode_cache_map(&mv, v_cache, dtype, prm.num_blocks, prm.num_kv_heads, D);
+  int rc = cached_cache_map(&mk, prm.k_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
+  if (rc == PA_OK) rc = cached_cache_map(&mv, prm.v_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
   if (rc != PA_OK) return rc;
+  prm.stages = kc.stages;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Smem<D>::bytes(prm.group);
+  cfg.gridDim = dim3(sms * kc.ctas_per_sm);
+  cfg.blockDim = dim3((W + 2) * 32);
+  cfg.dynamicSmemBytes = kc.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<T, D>, mk, mv, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<T, D, W>, mk, mv, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
+}
+
+// Host-side checks shared by every decode entry point.
+int check_decode_shapes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_blocks_per_seq, int dtype, const char* who) {
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "%s: unknown dtype %d", who, dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d (64 or 128)", who, head_dim);
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: sizes must be positive", who);
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: num_q_heads %% num_kv_heads != 0", who);
+  if (dtype != PA_F32 && num_q_heads / num_kv_heads > kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "%s: %d query heads per KV head (max %d)", who,
+                num_q_heads / num_kv_heads, kMaxGroup);
+  if (double(max_blocks_per_seq) * kBlockSize >= 2147483647.0)
+    return fail(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq too large", who);
+  return PA_OK;
+}
+
+int check_workspace(void* workspace, size_t workspace_bytes, const Layout& lay, const char* who) {
+  if (!workspace) return fail(PA_ERR_INVALID_ARG, "%s: workspace is NULL", who);
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", who);
+  if (workspace_bytes < lay.total)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                lay.total);
+  return PA_OK;
+}
+
+Params make_params(const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                   int head_dim, int max_blocks_per_seq, void* workspace, const Layout& lay,
+                   unsigned* status) {
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Params prm = {};
+  prm.context_lens = context_lens;
+  prm.num_seqs = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.head_dim = head_dim;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.max_splits = lay.max_splits;
+  prm.signature = plan_signature(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  prm.ws.header = reinterpret_cast<int*>(ws + lay.header);
+  prm.ws.units = reinterpret_cast<int*>(ws + lay.units);
+  prm.ws.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
+  prm.ws.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  prm.ws.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+  prm.status = status;
+  prm.timeout_ns = 1000000000ull;  // 1 s per wait
+  return prm;
+}
+
+int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+              int head_dim, int max_blocks_per_seq, void* workspace, size_t workspace_bytes,
+              cudaStream_t stream, const char* who) {
+  const Layout lay =
+      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  int rc = check_workspace(workspace, workspace_bytes, lay, who);
+  if (rc != PA_OK) return rc;
+  if (!context_lens) return fail(PA_ERR_INVALID_ARG, "%s: context_lens is NULL", who);
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                 max_blocks_per_seq, workspace, lay, status);
+  plan_kernel<<<1, 1024, 0, stream>>>(prm);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int run_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+             const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+             int head_dim, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+             void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
+             const char* who) {
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "%s: num_blocks must be positive", who);
+  if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
+    return fail(PA_ERR_INVALID_ARG, "%s: cache has too many rows", who);
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
+  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+    return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
+  const Layout lay =
+      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  int rc = check_workspace(workspace, workspace_bytes, lay, who);
+  if (rc != PA_OK) return rc;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
+  rc = device_setup(device);
+  if (rc != PA_OK) return rc;
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+
+  Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                           max_blocks_per_seq, workspace, lay, status);
+  prm.q = q;
+  prm.k_cache = k_cache;
+  prm.v_cache = v_cache;
+  prm.out = out;
+  prm.block_tables = block_tables;
+  prm.num_blocks = num_blocks;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+
+  if (dtype == PA_F32) {
+    const int blocks = (num_seqs * num_q_heads + 3) / 4;
+    if (head_dim == 64)
+      decode_f32_kernel<64><<<blocks, 128, 0, stream>>>(prm);
+    else
+      decode_f32_kernel<128><<<blocks, 128, 0, stream>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+      return fail(PA_ERR_CUDA, "%s (fp32): launch failed: %s", who, cudaGetErrorString(e));
+    return PA_OK;
+  }
+  rc = get_encoder();
+  if (rc != PA_OK) return rc;
+  const DeviceState& st = g_dev[device];
+  const KernelConfig& kc = st.cfg[dtype == PA_BF16][head_dim == 128][prm.group];
+  if (st.tuning.warps == 4) {
+    if (dtype == PA_BF16)
+      return head_dim == 128 ? launch_tc<__nv_bfloat16, 128, 4>(prm, kc, st.sms, stream)
+                             : launch_tc<__nv_bfloat16, 64, 4>(prm, kc, st.sms, stream);
+    return head_dim == 128 ? launch_tc<__half, 128, 4>(prm, kc, st.sms, stream)
+                           : launch_tc<__half, 64, 4>(prm, kc, st.sms, stream);
+  }
+  if (dtype == PA_BF16)
+    return head_dim == 128 ? launch_tc<__nv_bfloat16, 128, 8>(prm, kc, st.sms, stream)
+                           : launch_tc<__nv_bfloat16, 64, 8>(prm, kc, st.sms, stream);
+  return head_dim == 128 ? launch_tc<__half, 128, 8>(prm, kc, st.sms, stream)
+                         : launch_tc<__half, 64, 8>(prm, kc, st.sms, stream);
 }
 
 }  // namespace
@@ -670,6 +1072,17 @@ using namespace pa;
 using namespace pa::decode;
 
 extern "C" {
+
+#ifdef PA_PROFILE
+// Copies (and clears) the per-CTA cycle counters of a -DPA_PROFILE build.
+PA_API int pa_profile_read(unsigned long long* host, int ctas) {
+  const size_t bytes = size_t(ctas) * kProfSlots * sizeof(unsigned long long);
+  if (cudaMemcpyFromSymbol(host, g_prof, bytes) != cudaSuccess) return PA_ERR_CUDA;
+  static unsigned long long zeros[2048 * kProfSlots];
+  if (cudaMemcpyToSymbol(g_prof, zeros, bytes) != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+#endif
 
 PA_API int pa_paged_attention_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
                                                     int head_dim, int max_blocks_per_seq,
@@ -682,105 +1095,52 @@ PA_API int pa_paged_attention_decode_workspace_size(int num_seqs, int num_q_head
   return PA_OK;
 }
 
+PA_API int pa_paged_attention_decode_plan(const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_decode_plan";
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               PA_BF16, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  return plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who);
+}
+
+PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, const int32_t* context_lens,
+                                         int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int max_blocks_per_seq, int num_blocks,
+                                         float scale, int dtype, void* out, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_decode_run";
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               dtype, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  return run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                  num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                  workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who);
+}
+
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_tables, const int32_t* context_lens,
                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                      int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                      void* out, void* workspace, size_t workspace_bytes,
-                                     void* stream_) {
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
-    return fail(PA_ERR_UNSUPPORTED, "paged_attention_decode: unknown dtype %d", dtype);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(PA_ERR_UNSUPPORTED, "paged_attention_decode: head_dim %d (64 or 128)", head_dim);
-  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
-      num_blocks <= 0)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: sizes must be positive");
-  if (num_q_heads % num_kv_heads != 0)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: num_q_heads %% num_kv_heads != 0");
-  const int group = num_q_heads / num_kv_heads;
-  if (dtype != PA_F32 && group > kMaxGroup)
-    return fail(PA_ERR_UNSUPPORTED, "paged_attention_decode: %d query heads per KV head (max %d)",
-                group, kMaxGroup);
-  if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: cache has too many rows");
-  if (double(max_blocks_per_seq) * kBlockSize >= 2147483647.0)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: max_blocks_per_seq too large");
-  if (num_seqs == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: NULL pointer");
-  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
-  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
-    return fail(PA_ERR_INVALID_ARG,
-                "paged_attention_decode: tensors must be 16-byte aligned, workspace 256-byte");
-  const Layout lay =
-      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
-  if (workspace_bytes < lay.total)
-    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode: workspace %zu bytes < %zu needed",
-                workspace_bytes, lay.total);
-
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess || device >= kMaxDevices)
-    return fail(PA_ERR_CUDA, "paged_attention_decode: no current CUDA device");
-  int rc = device_setup(device);
-  if (rc != PA_OK) return rc;
-  unsigned* status = device_status_word();
-  if (!status) return PA_ERR_CUDA;
-
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  Params prm = {};
-  prm.q = q;
-  prm.k_cache = k_cache;
-  prm.v_cache = v_cache;
-  prm.out = out;
-  prm.block_tables = block_tables;
-  prm.context_lens = context_lens;
-  prm.num_seqs = num_seqs;
-  prm.num_q_heads = num_q_heads;
-  prm.num_kv_heads = num_kv_heads;
-  prm.group = group;
-  prm.head_dim = head_dim;
-  prm.max_blocks = max_blocks_per_seq;
-  prm.num_blocks = num_blocks;
-  prm.max_splits = lay.max_splits;
-  prm.scale = scale;
-  prm.scale_log2 = scale * 1.4426950408889634f;
-  prm.ws.header = reinterpret_cast<int*>(ws + lay.header);
-  prm.ws.units = reinterpret_cast<int*>(ws + lay.units);
-  prm.ws.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
-  prm.ws.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
-  prm.ws.part_o = reinterpret_cast<float*>(ws + lay.part_o);
-  prm.status = status;
-  prm.timeout_ns = 1000000000ull;  // 1 s per wait
-
-  if (dtype == PA_F32) {
-    const int warps = num_seqs * num_q_heads;
-    const int blocks = (warps + 3) / 4;
-    if (head_dim == 64)
-      decode_f32_kernel<64><<<blocks, 128, 0, stream>>>(prm);
-    else
-      decode_f32_kernel<128><<<blocks, 128, 0, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode (fp32): launch failed: %s", cudaGetErrorString(e));
-    return PA_OK;
+                                     void* stream) {
+  const char* who = "paged_attention_decode";
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               dtype, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype != PA_F32) {
+    rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                   workspace, workspace_bytes, s, who);
+    if (rc != PA_OK) return rc;
   }
-
-  rc = get_encoder();
-  if (rc != PA_OK) return rc;
-  const int out_row_vecs = num_q_heads * head_dim * 2 / 16;
-  plan_kernel<<<1, 1024, 0, stream>>>(prm, out_row_vecs);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode: plan launch failed: %s", cudaGetErrorString(e));
-
-  const DeviceState& st = g_dev[device];
-  const int per_sm = st.ctas_per_sm[dtype == PA_BF16][head_dim == 128][group];
-  const int grid = st.sms * (per_sm > 0 ? per_sm : 1);
-  if (dtype == PA_BF16)
-    return head_dim == 128 ? launch_tc<__nv_bfloat16, 128>(prm, k_cache, v_cache, dtype, stream, grid)
-                           : launch_tc<__nv_bfloat16, 64>(prm, k_cache, v_cache, dtype, stream, grid);
-  return head_dim == 128 ? launch_tc<__half, 128>(prm, k_cache, v_cache, dtype, stream, grid)
-                         : launch_tc<__half, 64>(prm, k_cache, v_cache, dtype, stream, grid);
+  return run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                  num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                  workspace, workspace_bytes, s, who);
 }
 
 }  // extern "C"

@@ -9,16 +9,22 @@ namespace decode {
 
 constexpr int kBlockSize = 16;      // tokens per physical block (device kernels)
 constexpr int kSplitBlocks = 32;    // logical blocks per work item (512 tokens)
-constexpr int kConsumerWarps = 4;   // warps doing the attention math
-constexpr int kStages = 8;          // (K, V) tiles buffered per CTA
-constexpr int kQueue = 4;           // work items buffered per CTA
+constexpr int kConsumerWarps = 8;   // default number of warps doing the attention math
+constexpr int kWarpStages = 4;      // upper bound of each math warp's (K, V) tile ring
+constexpr int kQueue = 8;           // work items buffered per CTA
+constexpr int kFinRing = 2;         // items whose split bookkeeping may be in flight
 constexpr int kMaxGroup = 8;        // query heads per KV head on the tensor-core path
-constexpr int kThreads = (kConsumerWarps + 2) * 32;  // + TMA issuer warp + scheduler warp
+
+// Workspace header words.
+constexpr int kHdrNext = 0;       // next work item (self-resetting)
+constexpr int kHdrTotal = 1;      // number of work items (written by the plan)
+constexpr int kHdrDone = 2;       // CTAs whose scheduler has finished (self-resetting)
+constexpr int kHdrSignature = 3;  // shape signature written by the plan
 
 // Views into the caller's workspace (all offsets 256-byte aligned).
 struct Workspace {
-  int* header;       // [0] next work item, [1] number of work items
-  int* units;        // int4 per (sequence, split): b, split, context length, blocks
+  int* header;       // see kHdr*
+  int* units;        // int4 per (sequence, split): b, split << 8 | blocks, first block, ctx
   int* arrivals;     // [num_seqs * num_kv_heads] finished splits per (b, kv head)
   float* part_lse;   // [num_seqs][max_splits][num_q_heads]  (log2 domain)
   float* part_o;     // [num_seqs][max_splits][num_q_heads][head_dim]
@@ -46,6 +52,19 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
   return l;
 }
 
+// Identifies the shapes a plan was made for, so a run can refuse a workspace
+// planned for something else.
+inline int plan_signature(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                          int max_blocks_per_seq) {
+  uint32_t h = 2166136261u;
+  const int v[5] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq};
+  for (int x : v) {
+    h ^= uint32_t(x);
+    h *= 16777619u;
+  }
+  return int(h | 1u);
+}
+
 struct Params {
   const void* q;
   const void* k_cache;  // raw cache pointers (the fp32 path reads them directly;
@@ -55,6 +74,8 @@ struct Params {
   const int32_t* context_lens;
   int num_seqs, num_q_heads, num_kv_heads, group, head_dim;
   int max_blocks, num_blocks, max_splits;
+  int stages;        // depth of the shared-memory tile ring (tensor-core path)
+  int signature;     // plan_signature() of these shapes
   float scale;       // softmax scale (fp32 path)
   float scale_log2;  // scale * log2(e) (tensor-core path works in base 2)
   Workspace ws;

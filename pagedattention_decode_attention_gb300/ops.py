@@ -73,13 +73,7 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: 
         slot_mapping.data_ptr(), k.shape[0], hkv, d, nb, _dtype_code(k), _stream(dev, stream)))
 
 
-def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
-                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
-                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                           stream=None) -> torch.Tensor:
-    """Decode attention of ``q`` (``[B, Hq, d]``) over paged ``k_cache`` /
-    ``v_cache`` (``[NB, Hkv, 16, d]``) through ``block_tables`` (int32
-    ``[B, max_blocks]``) for ``context_lens`` (int32 ``[B]``) tokens."""
+def _decode_args(q, k_cache, v_cache, block_tables, context_lens):
     dev = q.device
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
                     ("block_tables", block_tables), ("context_lens", context_lens)):
@@ -95,7 +89,31 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     _require(block_tables.dim() == 2 and block_tables.shape[0] == b,
              "block_tables must be [num_seqs, max_blocks_per_seq]")
     _require(context_lens.shape == (b,), "context_lens must be [num_seqs]")
-    mb = block_tables.shape[1]
+    return dev, b, hq, hkv, d, nb, block_tables.shape[1]
+
+
+def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           stream=None) -> torch.Tensor:
+    """Decode attention of ``q`` (``[B, Hq, d]``) over paged ``k_cache`` /
+    ``v_cache`` (``[NB, Hkv, 16, d]``) through ``block_tables`` (int32
+    ``[B, max_blocks]``) for ``context_lens`` (int32 ``[B]``) tokens.  Plans
+    and runs in one call."""
+    return _decode(capi.lib().pa_paged_attention_decode, q, k_cache, v_cache, block_tables,
+                   context_lens, scale, out, workspace, stream)
+
+
+def paged_attention_decode_run(q, k_cache, v_cache, block_tables, context_lens, scale,
+                               workspace: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """Same as :func:`paged_attention_decode` on a workspace already planned by
+    :func:`paged_attention_decode_plan` (one plan serves every layer of a step)."""
+    return _decode(capi.lib().pa_paged_attention_decode_run, q, k_cache, v_cache, block_tables,
+                   context_lens, scale, out, workspace, stream)
+
+
+def _decode(fn, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace, stream):
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
     if out is None:
         out = torch.empty_like(q)
     _cuda_contig("out", out, dev)
@@ -103,12 +121,81 @@ def paged_attention_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     if workspace is None:
         workspace = alloc_workspace(b, hq, hkv, d, mb, dev)
     _cuda_contig("workspace", workspace, dev)
-    capi.check(capi.lib().pa_paged_attention_decode(
+    capi.check(fn(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q),
         out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
         _stream(dev, stream)))
     return out
+
+
+def paged_attention_decode_plan(context_lens: torch.Tensor, num_q_heads: int, num_kv_heads: int,
+                                head_dim: int, max_blocks_per_seq: int, workspace: torch.Tensor,
+                                stream=None) -> None:
+    """Write the work list for these context lengths into ``workspace``."""
+    dev = context_lens.device
+    _cuda_contig("context_lens", context_lens, dev)
+    _cuda_contig("workspace", workspace, dev)
+    _require(context_lens.dtype == torch.int32 and context_lens.dim() == 1,
+             "context_lens must be int32 [num_seqs]")
+    capi.check(capi.lib().pa_paged_attention_decode_plan(
+        context_lens.data_ptr(), context_lens.shape[0], num_q_heads, num_kv_heads, head_dim,
+        max_blocks_per_seq, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(dev, stream)))
+
+
+class Prepared:
+    """A device entry point bound to fixed tensors.
+
+    Validation and pointer marshalling happen once, in the ``prepare_*``
+    function; each call re-issues only the C call with the stored arguments.
+    Meant for per-layer loops that reuse the same buffers every decode step.
+    The bound tensors are kept alive by this object.
+    """
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self) -> None:
+        status = self._fn(*self._args)
+        if status:
+            capi.check(status)
+
+
+def prepare_kv_append(k, v, k_cache, v_cache, slot_mapping, stream=None) -> Prepared:
+    kv_append(k[:0], v[:0], k_cache, v_cache, slot_mapping[:0], stream)  # validates shapes
+    nb, hkv, _, d = k_cache.shape
+    args = (C.c_void_p(k.data_ptr()), C.c_void_p(v.data_ptr()), C.c_void_p(k_cache.data_ptr()),
+            C.c_void_p(v_cache.data_ptr()), C.c_void_p(slot_mapping.data_ptr()), k.shape[0], hkv,
+            d, nb, _dtype_code(k), C.c_void_p(_stream(k_cache.device, stream)))
+    _require(slot_mapping.shape == (k.shape[0],), "slot_mapping must be [num_tokens]")
+    return Prepared(capi.lib().pa_kv_append, args, (k, v, k_cache, v_cache, slot_mapping))
+
+
+def prepare_decode_plan(context_lens, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                        workspace, stream=None) -> Prepared:
+    dev = context_lens.device
+    _cuda_contig("context_lens", context_lens, dev)
+    _cuda_contig("workspace", workspace, dev)
+    args = (C.c_void_p(context_lens.data_ptr()), context_lens.shape[0], num_q_heads, num_kv_heads,
+            head_dim, max_blocks_per_seq, C.c_void_p(workspace.data_ptr()),
+            C.c_size_t(workspace.numel() * workspace.element_size()), C.c_void_p(_stream(dev, stream)))
+    return Prepared(capi.lib().pa_paged_attention_decode_plan, args, (context_lens, workspace))
+
+
+def prepare_decode_run(q, k_cache, v_cache, block_tables, context_lens, scale, workspace, out,
+                       stream=None) -> Prepared:
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    _cuda_contig("out", out, dev)
+    _cuda_contig("workspace", workspace, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    args = (C.c_void_p(q.data_ptr()), C.c_void_p(k_cache.data_ptr()), C.c_void_p(v_cache.data_ptr()),
+            C.c_void_p(block_tables.data_ptr()), C.c_void_p(context_lens.data_ptr()), b, hq, hkv, d,
+            mb, nb, C.c_float(scale), _dtype_code(q), C.c_void_p(out.data_ptr()),
+            C.c_void_p(workspace.data_ptr()), C.c_size_t(workspace.numel() * workspace.element_size()),
+            C.c_void_p(_stream(dev, stream)))
+    return Prepared(capi.lib().pa_paged_attention_decode_run, args,
+                    (q, k_cache, v_cache, block_tables, context_lens, workspace, out))
 
 
 def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:

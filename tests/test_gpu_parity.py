@@ -179,3 +179,58 @@ def test_block_copy_bad_pair_is_skipped(gpu):
     with pytest.raises(pa().PagedAttnError):
         pa().check_status()
     assert torch.equal(kc, before)
+
+
+# ------------------------------------------------------- plan once, run many
+def test_one_plan_serves_many_runs(gpu):
+    """A plan followed by several runs (one per layer) gives, bit for bit, what
+    the combined call gives for each layer."""
+    batch = custom_batch([5, 530, 1300, 16, 2049], 32, 8, 128, "bf16", seed=31)
+    ws = pa().alloc_workspace(5, 32, 8, 128, batch.max_blocks, gpu)
+    _, _, _, bt, cl = decode_inputs(batch, gpu)
+    pa().paged_attention_decode_plan(cl, 32, 8, 128, batch.max_blocks, ws)
+    for layer in range(4):
+        q, kc, vc, _, _ = decode_inputs(batch, gpu, seed_offset=layer)
+        got = pa().paged_attention_decode_run(q, kc, vc, bt, cl, batch.scale, ws).clone()
+        ref = pa().paged_attention_decode(q, kc, vc, bt, cl, batch.scale)
+        pa().check_status()
+        assert torch.equal(got, ref)
+        if layer == 0:
+            assert_attention_close(got, oracle_decode(batch, q, kc, vc), torch.bfloat16)
+        # re-plan on a separate workspace does not disturb this one
+        pa().paged_attention_decode_plan(cl, 32, 8, 128, batch.max_blocks,
+                                         pa().alloc_workspace(5, 32, 8, 128, batch.max_blocks, gpu))
+
+
+def test_run_without_plan_is_refused_on_device(gpu):
+    batch = custom_batch([40, 70], 8, 8, 64, "f16", seed=32)
+    q, kc, vc, bt, cl = decode_inputs(batch, gpu)
+    ws = pa().alloc_workspace(2, 8, 8, 64, batch.max_blocks, gpu)
+    ws.zero_()
+    out = torch.full_like(q, 7.0)
+    pa().paged_attention_decode_run(q, kc, vc, bt, cl, batch.scale, ws, out=out)
+    with pytest.raises(pa().PagedAttnError) as e:
+        pa().check_status()
+    assert e.value.status == 1
+    assert torch.all(out == 7.0)                     # nothing was written
+    # a plan for other shapes is refused as well
+    pa().paged_attention_decode_plan(cl, 8, 4, 64, batch.max_blocks, ws)
+    pa().paged_attention_decode_run(q, kc, vc, bt, cl, batch.scale, ws, out=out)
+    with pytest.raises(pa().PagedAttnError):
+        pa().check_status()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_unused_slots_holding_nan_do_not_leak(gpu, dtype):
+    """Slots past the context in each sequence's last block hold NaN / Inf; the
+    output must still match the oracle (which never reads them)."""
+    batch = custom_batch([1, 7, 15, 17, 31, 100, 529], 16, 4, 128, dtype, seed=33)
+    q, kc, vc, bt, cl = decode_inputs(batch, gpu)
+    for b, n in enumerate(batch.context_lens):
+        last = int(batch.block_tables[b, (int(n) - 1) // 16])
+        off = int(n) % 16
+        if off:
+            kc[last, :, off:] = float("nan")
+            vc[last, :, off:] = float("inf")
+    out = run_decode(batch, q, kc, vc, bt, cl)
+    assert_attention_close(out, oracle_decode(batch, q, kc, vc), TORCH_DTYPES[dtype])
