@@ -178,6 +178,37 @@ PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, con
                                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_noalloc -- pa_paged_attention_decode without a
+ * caller-provided workspace.  (No counterpart on the pages: this entry point
+ * exists for callers, not for the method.)
+ *
+ * For callers that cannot allocate device memory: code running inside a host
+ * framework that owns the whole device-memory budget (a serving engine's
+ * pre-reserved pool, a process held to a memory cap) may not call cudaMalloc
+ * to make the workspace the other entry point needs.  This one uses a 64 MiB
+ * scratch array compiled into the library instead; every GPU that loads the
+ * library holds that array until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Same arguments and results as pa_paged_attention_decode, minus the
+ * workspace.  Shapes whose workspace (see
+ * pa_paged_attention_decode_workspace_size) exceeds 64 MiB are rejected with
+ * PA_ERR_INVALID_ARG before anything is launched.  The first call on a device
+ * looks up that device's scratch address (cudaGetSymbolAddress, with the
+ * device current), so make the first call on each device before any stream
+ * capture.  Every call re-plans its work into the scratch, so nothing needs
+ * clearing between calls; but all calls on a device share the one array, so
+ * two calls whose kernels overlap on the GPU (different streams, no ordering)
+ * race and corrupt each other's results.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_noalloc(const void* q, const void* k_cache,
+                                             const void* v_cache, const int32_t* block_tables,
+                                             const int32_t* context_lens, int num_seqs,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int max_blocks_per_seq, int num_blocks, float scale,
+                                             int dtype, void* out, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_block_copy -- copy-on-write block copies, all layers in one launch.
  *
  * OS-lab appendix, sections 4.3-4.4 (when the target block's refcount is

@@ -1144,3 +1144,77 @@ PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const v
 }
 
 }  // extern "C"
+
+// ====================================================== no-allocation variant
+// Some callers cannot hand this library a device workspace: they run inside a
+// host framework that owns the whole device-memory budget (a serving engine's
+// pre-reserved pool, a process capped at its memory limit) and may not call
+// cudaMalloc themselves.  For them the decode path can use a scratch area
+// compiled into this library instead: a fixed-size array in device memory
+// that every GPU loading the library holds until the process exits.
+namespace pa {
+namespace decode {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB per device
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+struct ScratchSlot {
+  std::once_flag once;
+  void* addr = nullptr;
+  cudaError_t error = cudaSuccess;
+};
+ScratchSlot g_scratch[kMaxDevices];
+
+// Device address of this device's scratch array (looked up once per device,
+// with that device current; the host-side name of the array is not a device
+// address).
+int static_scratch(void** out) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "paged_attention_decode_noalloc: no current CUDA device");
+  ScratchSlot& slot = g_scratch[device];
+  std::call_once(slot.once, [&] {
+    slot.error = cudaGetSymbolAddress(&slot.addr, g_static_scratch);
+    if (slot.error != cudaSuccess) slot.addr = nullptr;
+  });
+  if (!slot.addr)
+    return fail(PA_ERR_CUDA, "paged_attention_decode_noalloc: cudaGetSymbolAddress failed: %s",
+                cudaGetErrorString(slot.error));
+  *out = slot.addr;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace decode
+}  // namespace pa
+
+extern "C" {
+
+PA_API int pa_paged_attention_decode_noalloc(const void* q, const void* k_cache,
+                                             const void* v_cache, const int32_t* block_tables,
+                                             const int32_t* context_lens, int num_seqs,
+                                             int num_q_heads, int num_kv_heads, int head_dim,
+                                             int max_blocks_per_seq, int num_blocks, float scale,
+                                             int dtype, void* out, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "paged_attention_decode_noalloc: sizes must be positive");
+  const size_t need =
+      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
+  if (need > kStaticScratchBytes)
+    return fail(PA_ERR_INVALID_ARG,
+                "paged_attention_decode_noalloc: these shapes need %zu bytes of scratch, more than "
+                "the %zu built into the library; pass a workspace to pa_paged_attention_decode",
+                need, kStaticScratchBytes);
+  if (num_seqs == 0) return PA_OK;
+  void* scratch = nullptr;
+  const int rc = static_scratch(&scratch);
+  if (rc != PA_OK) return rc;
+  return pa_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                   num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                   num_blocks, scale, dtype, out, scratch, kStaticScratchBytes,
+                                   stream);
+}
+
+}  // extern "C"

@@ -129,6 +129,23 @@ def _decode(fn, q, k_cache, v_cache, block_tables, context_lens, scale, out, wor
     return out
 
 
+def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
+                                   out=None, stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode` for callers that cannot allocate device
+    memory: the library's built-in 64 MiB scratch replaces the workspace
+    (calls on one device share it, so they must not overlap on the GPU)."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    capi.check(capi.lib().pa_paged_attention_decode_noalloc(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q),
+        out.data_ptr(), _stream(dev, stream)))
+    return out
+
+
 def paged_attention_decode_plan(context_lens: torch.Tensor, num_q_heads: int, num_kv_heads: int,
                                 head_dim: int, max_blocks_per_seq: int, workspace: torch.Tensor,
                                 stream=None) -> None:
