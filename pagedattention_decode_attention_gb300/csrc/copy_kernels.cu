@@ -38,6 +38,10 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
                                  const int64_t* __restrict__ slots, int64_t total_vecs,
                                  int heads_vecs, int row_vecs, int64_t num_slots,
                                  unsigned* status) {
+  // Let the next kernel of the stream start its prologue now; touch memory only
+  // once the kernel before this one has finished.
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int64_t t = i / heads_vecs;
@@ -65,6 +69,8 @@ struct LayerPtrs {
 __global__ void block_copy_kernel(const __grid_constant__ LayerPtrs ptrs,
                                   const int64_t* __restrict__ pairs, int block_vecs,
                                   int64_t num_blocks, unsigned* status) {
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();
   const int pair = blockIdx.x, layer = blockIdx.y;
   const int64_t src = pairs[2 * int64_t(pair)], dst = pairs[2 * int64_t(pair) + 1];
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
@@ -91,6 +97,19 @@ int check_common(int dtype, int head_dim, int num_kv_heads, int num_blocks, cons
 }
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
+
+// These copies use no shared memory; asking for the largest shared-memory
+// split anyway keeps the SM configured as the attention kernel that follows
+// them in a decode step wants it, so no reconfiguration sits between them.
+void prefer_max_shared() {
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaFuncSetAttribute(kv_append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(block_copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+  });
+}
 
 }  // namespace
 
@@ -129,17 +148,26 @@ PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cac
     return fail(PA_ERR_INVALID_ARG, "kv_append: tensors must be 16-byte aligned");
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
+  prefer_max_shared();
   const int row_vecs = head_dim * elem_bytes(dtype) / 16;
   const int heads_vecs = num_kv_heads * row_vecs;
   const int64_t total = int64_t(num_tokens) * heads_vecs;
   const int threads = 256;
   const int64_t want = (total + threads - 1) / threads;
   const int blocks = int(want < 65535 * 16 ? want : 65535 * 16);
-  kv_append_kernel<<<blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-      static_cast<uint4*>(v_cache), slot_mapping, total, heads_vecs, row_vecs,
-      int64_t(num_blocks) * kBlockSize, status);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<const uint4*>(k),
+                                     static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
+                                     static_cast<uint4*>(v_cache), slot_mapping, total, heads_vecs,
+                                     row_vecs, int64_t(num_blocks) * kBlockSize, status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "kv_append: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
 }
@@ -164,11 +192,19 @@ PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_l
   }
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
+  prefer_max_shared();
   const int block_vecs = num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype) / 16;
-  dim3 grid(num_pairs, num_layers, 2);
-  block_copy_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      ptrs, src_dst_pairs, block_vecs, num_blocks, status);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_pairs, num_layers, 2);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, block_copy_kernel, ptrs, src_dst_pairs, block_vecs,
+                                     int64_t(num_blocks), status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "block_copy: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
 }

@@ -15,33 +15,31 @@
 //    the tail of the persistent kernel is made of the smallest items.  The
 //    plan depends only on the context lengths, so one plan serves every layer
 //    of a decode step.
-//  * persistent attention kernel, one CTA per SM, three warp roles:
+//  * persistent attention kernel, one CTA per SM, two warp roles:
 //      - scheduler warp: takes work items from a global counter (four at a
 //        time, so their dependent global reads overlap), reads each item's
 //        block-table entries (range-checked) and bulk-copies the G query rows
 //        of (b, g) into a shared-memory item queue;
-//      - finisher warp: publishes and counts finished splits (fence + atomic)
-//        so the math warps never wait on device-scope memory ordering;
-//      - W math warps: warp w takes blocks w, w+W, ... of every item and
-//        streams them through its own small ring: it issues the 2-D tensor
-//        copies (128-byte swizzled, L2 evict-first) of the K tile and V tile
-//        of a block NS blocks before it needs them.  Many independent issuers
+//      - W math warps: each takes whole items from the queue and streams all
+//        their blocks through its own small ring, issuing the 2-D tensor
+//        copies (128-byte swizzled, L2 evict-first) of a block's K and V
+//        tiles a few blocks before it needs them.  Many independent issuers
 //        keep HBM busy; a single issuing thread per CTA could not (each copy
-//        instruction costs it hundreds of cycles).  Per 16-token block:
-//        S^T = K . Q^T on the tensor cores (m16n8k16, M = the 16 tokens,
-//        N = the G <= 8 query heads of the group, K = head_dim), online softmax
-//        in base 2 with per-head running max / sum, P rounded to the input
-//        type and transposed in registers (movmatrix), O^T += V^T . P^T
-//        (M = head_dim rows of V^T via ldmatrix.trans).  Each K/V tile is read
-//        from HBM once for the whole query group.  Slots past the context in
-//        the last block are zeroed in registers, so whatever bits they hold
-//        cannot reach the output.
-//    At the end of an item the math warps merge their partial (m, l, O)
-//    through shared memory.  A sequence with one split writes `out`
-//    directly; otherwise the item writes (o, lse) to the workspace and the
-//    CTA that finishes the last split of (b, g) merges all splits with
-//    log-sum-exp weights (an arrival counter, no spinning).  The work and
-//    arrival counters return to zero by the end of every run.
+//        instruction costs it hundreds of cycles), and no CTA-wide barrier is
+//        needed.  Per 16-token block: S^T = K . Q^T on the tensor cores
+//        (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of the
+//        group, K = head_dim), online softmax in base 2 with per-head running
+//        max / sum, P rounded to the input type and transposed in registers
+//        (movmatrix), O^T += V^T . P^T (M = head_dim rows of V^T via
+//        ldmatrix.trans).  Each K/V tile is read from HBM once for the whole
+//        query group.  Slots past the context in the last block are zeroed in
+//        registers, so whatever bits they hold cannot reach the output.
+//    A sequence with one split is written to `out` straight from the
+//    warp's registers; otherwise the warp writes (o, lse) to the workspace,
+//    publishes it (fence) and counts it (atomic), and the warp that completes
+//    the last split of (b, g) merges all splits with log-sum-exp weights (no
+//    spinning).  The work and arrival counters return to zero by the end of
+//    every run.
 //  * Every wait is an mbarrier wait with a time limit; running out sets the
 //    timeout bit of the device status word and the warp returns.
 //
@@ -72,6 +70,18 @@ using dev::mbar_wait_bounded;
 // Optional cycle accounting per CTA and warp role, compiled in only with
 // -DPA_PROFILE (a separate build used to see where a persistent CTA spends its
 // time; the default build has none of it).
+#ifdef PA_PROFILE_TIMES
+// per (CTA, warp): globaltimer at start of work, at end, blocks consumed
+__device__ unsigned long long g_times[2048 * 16 * 3];
+#define TIME_MARK(i, v)                                                                     \
+  do {                                                                                      \
+    if ((threadIdx.x & 31) == 0)                                                            \
+      g_times[(blockIdx.x * 16 + (threadIdx.x >> 5)) * 3 + (i)] = (v);                      \
+  } while (0)
+#else
+#define TIME_MARK(i, v)
+#endif
+
 #ifdef PA_PROFILE
 constexpr int kProfSlots = 16;
 __device__ unsigned long long g_prof[2048 * kProfSlots];
@@ -105,17 +115,10 @@ struct Smem {
   static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, head) tile
   static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
   static constexpr size_t kItems = size_t(kQueue) * sizeof(ItemSlot<D>);
-  static constexpr int kOPitch = D + 4;                  // floats; breaks bank conflicts
-  __host__ __device__ static size_t merge_o_floats(int group) {
-    return size_t(W) * group * kOPitch;
-  }
-  static constexpr size_t kMergeMl = size_t(W) * kMaxGroup * 2;  // floats
-  // barriers (uint64) + fin_info (int4 = 2 slots each) + verdicts
-  static constexpr size_t kBars = size_t(W) * kWarpStages + 2 * kQueue + 2 + 2 * kFinRing +
-                                  2 * kFinRing + kFinRing + 2;
-  static size_t fixed_bytes(int group) {
-    return 1024 /* alignment slack */ + kItems + merge_o_floats(group) * 4 + kMergeMl * 4 +
-           kBars * 8 + 16;
+  // barriers (uint64) + the claim and pushed counters
+  static constexpr size_t kBars = size_t(W) * kWarpStages + 2 * kQueue + 1;
+  static size_t fixed_bytes(int /*group*/) {
+    return 1024 /* alignment slack */ + kItems + kBars * 8 + 16;
   }
   // `stages` is per math warp
   static size_t bytes(int group, int stages) {
@@ -133,8 +136,9 @@ struct Smem {
 // Splits of one sequence are balanced: nsplit = ceil(blocks / 32) splits whose
 // sizes differ by at most one block.  Units are then counting-sorted by size,
 // largest first, and a sequence's splits stay adjacent in the order.
-__device__ __forceinline__ void split_shape(int nblk, int& nsplit, int& base, int& big) {
-  nsplit = (nblk + kSplitBlocks - 1) / kSplitBlocks;
+__device__ __forceinline__ void split_shape(int nblk, int split, int& nsplit, int& base,
+                                            int& big) {
+  nsplit = (nblk + split - 1) / split;
   base = nsplit ? nblk / nsplit : 0;
   big = nsplit ? nblk - base * nsplit : 0;  // the first `big` splits hold base + 1 blocks
 }
@@ -156,7 +160,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
       ctx = ctx < 0 ? 0 : cap;
     }
     int nsplit, base, big;
-    split_shape((ctx + kBlockSize - 1) / kBlockSize, nsplit, base, big);
+    split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
     if (big) atomicAdd(&hist[base + 1], big);
     if (nsplit - big) atomicAdd(&hist[base], nsplit - big);
     for (int g = 0; g < p.num_kv_heads; ++g) p.ws.arrivals[size_t(b) * p.num_kv_heads + g] = 0;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
     int ctx = p.context_lens[b];
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
-    split_shape((ctx + kBlockSize - 1) / kBlockSize, nsplit, base, big);
+    split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
     const int at_big = big ? atomicAdd(&bucket[base + 1], big) : 0;
     const int at_small = nsplit - big ? atomicAdd(&bucket[base], nsplit - big) : 0;
     int first = 0;
@@ -193,14 +197,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
 
 // --------------------------------------------------------- tensor-core path
 template <typename T, int D, int W>
-__global__ void __launch_bounds__((W + 2) * 32)
+__global__ void __launch_bounds__((W + 1) * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
   using S = Smem<D, W>;
   using M = dev::Mma<T>;
   constexpr int KT = D / 16;        // 16-wide steps along head_dim
   constexpr int HALVES = D / 64;    // 128-byte TMA boxes per tile row
-  constexpr int R = kFinRing;
+  constexpr int FIFO = 2;           // items a math warp may hold (1 in work + 1 lookahead)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -209,32 +213,25 @@ __global__ void __launch_bounds__((W + 2) * 32)
   uint8_t* rings = smem;
   ItemSlot<D>* items =
       reinterpret_cast<ItemSlot<D>*>(rings + size_t(W) * NS * S::kStageBytes);
-  float* merge_o = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(items) + S::kItems);
-  float* merge_ml = merge_o + S::merge_o_floats(G);
-  uint64_t* full = reinterpret_cast<uint64_t*>(merge_ml + S::kMergeMl);  // [W][kWarpStages]
-  uint64_t* item_full = full + W * kWarpStages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(items) + S::kItems);
+  uint64_t* item_full = full + W * kWarpStages;  // [W][kWarpStages] before it
   uint64_t* item_empty = item_full + kQueue;
-  uint64_t* mb_merge = item_empty + kQueue;  // all math threads wrote their partial state
-  uint64_t* mb_read = mb_merge + 1;          // all math threads finished reading it
-  uint64_t* mb_done = mb_read + 1;           // [R] an item's outputs are written
-  uint64_t* mb_verdict = mb_done + R;        // [R] the finisher's verdict is published
-  int4* fin_info = reinterpret_cast<int4*>(                   // [R] b, g, nsplit, -
-      (reinterpret_cast<uintptr_t>(mb_verdict + R) + 15) & ~uintptr_t(15));
-  volatile int* verdict = reinterpret_cast<volatile int*>(fin_info + R);  // [R]
+  int* claim_ctr = reinterpret_cast<int*>(item_empty + kQueue);
+  // items the scheduler has written to the queue so far (only it writes)
+  volatile int* pushed = claim_ctr + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#ifdef PA_PROFILE_TIMES
+  if (threadIdx.x == 0) g_times[(blockIdx.x * 16 + 15) * 3 + 0] = dev::global_timer_ns();
+#endif
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * kWarpStages; ++i) dev::mbar_init(&full[i], 1);
     for (int i = 0; i < kQueue; ++i) {
       dev::mbar_init(&item_full[i], 8);  // the lanes of one scheduler group
-      dev::mbar_init(&item_empty[i], W);
+      dev::mbar_init(&item_empty[i], 1);  // the one math warp that took the item
     }
-    dev::mbar_init(mb_merge, W * 32);
-    dev::mbar_init(mb_read, W * 32);
-    for (int i = 0; i < R; ++i) {
-      dev::mbar_init(&mb_done[i], W * 32);
-      dev::mbar_init(&mb_verdict[i], 1);
-    }
+    *claim_ctr = 0;
+    *pushed = 0;
     dev::mbar_fence_init();
   }
   if (warp < W && lane == 0) {
@@ -245,6 +242,9 @@ __global__ void __launch_bounds__((W + 2) * 32)
   dev::grid_dependency_wait();  // a plan launched just before has completed
 
   PROF_T(t_kernel);
+#ifdef PA_PROFILE_TIMES
+  if (threadIdx.x == 0) g_times[(blockIdx.x * 16 + 15) * 3 + 1] = dev::global_timer_ns();
+#endif
   const unsigned long long tmo = p.timeout_ns;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
   const bool planned =
@@ -269,10 +269,29 @@ __global__ void __launch_bounds__((W + 2) * 32)
     const int4* units = reinterpret_cast<const int4*>(p.ws.units);
     const int grp = lane >> 3, gl = lane & 7;
     int it = 0;
+    bool first_round = true;
     for (bool more = true; more;) {
+      // Keep only a few unclaimed items queued: work left in the global list
+      // can still go to whichever CTA frees up first, which keeps the tail short.
+      if (planned) {
+        const uint64_t t0 = dev::global_timer_ns();
+        while (it - *reinterpret_cast<volatile int*>(claim_ctr) > kSchedAhead) {
+          if (dev::global_timer_ns() - t0 > tmo) {
+            dev::flag_status(p.status, kStatusTimeout);
+            return;
+          }
+          __nanosleep(128);
+        }
+      }
       PROF_T(t_fetch);
+      // The first round is dealt statically (the largest items, one per group
+      // and CTA), which saves the counter's round trip at the start; later
+      // rounds take the next items from the global counter.
       int idx = total;
-      if (planned && gl == 0) idx = atomicAdd(&p.ws.header[kHdrNext], 1);
+      if (planned && gl == 0)
+        idx = first_round ? grp * int(gridDim.x) + int(blockIdx.x)
+                          : 4 * int(gridDim.x) + atomicAdd(&p.ws.header[kHdrNext], 1);
+      first_round = false;
       idx = __shfl_sync(0xffffffffu, idx, grp * 8);
       const bool valid = idx < total;
       int4 u = make_int4(0, 0, 0, 0);
@@ -312,7 +331,7 @@ __global__ void __launch_bounds__((W + 2) * 32)
             sl.s = s;
             sl.ctx = ctx;
             sl.nblk = nblk;
-            sl.nsplit = (nblk_all + kSplitBlocks - 1) / kSplitBlocks;
+            sl.nsplit = (nblk_all + p.split_blocks - 1) / p.split_blocks;
             sl.first = first;
             const uint32_t qbytes = uint32_t(G) * D * 2;
             dev::mbar_arrive_expect_tx(&item_full[qs], qbytes);
@@ -325,14 +344,20 @@ __global__ void __launch_bounds__((W + 2) * 32)
           }
         }
         ++it;
+        __syncwarp();
+        if (lane == 0) dev::st_release_cta(pushed, it);
       }
     }
-    // no more work: queue the end marker
-    const int qs = it % kQueue;
-    if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
-    if (grp == 0) {
-      if (gl == 0) items[qs].b = -1;
-      mbar_arrive(&item_full[qs]);
+    // no more work: one end marker for each math warp (each takes exactly one)
+    for (int e = 0; e < W; ++e, ++it) {
+      const int qs = it % kQueue;
+      if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
+      if (grp == 0) {
+        if (gl == 0) items[qs].b = -1;
+        mbar_arrive(&item_full[qs]);
+      }
+      __syncwarp();
+      if (lane == 0) dev::st_release_cta(pushed, it + 1);
     }
     if (planned && lane == 0) {
       // The last scheduler to finish returns the work counters to zero, so the
@@ -343,56 +368,71 @@ __global__ void __launch_bounds__((W + 2) * 32)
         atomicExch(&p.ws.header[kHdrDone], 0);
       }
     }
-  } else if (warp == W + 1) {
-    // ------------------------------------------------------------- finisher
-    // Split bookkeeping off the math warps' path: after the math threads have
-    // written an item's partial result, publish it device-wide and count the
-    // split; tell the math warps (R items later) whether this CTA finished the
-    // last split of (b, g).
-    for (int k = 0;; ++k) {
-      const int slot = k % R;
-      if (!mbar_wait_bounded(&mb_done[slot], (k / R) & 1, tmo, p.status)) return;
-      const int4 info = fin_info[slot];
-      if (info.x < 0) return;
-      int last = 0;
-      if (info.z > 1) {
-        __threadfence();  // the item's partials (released to us at CTA scope) go device-wide
-        if (lane == 0) {
-          last = atomicAdd(&p.ws.arrivals[size_t(info.x) * Hkv + info.y], 1) == info.z - 1;
-          __threadfence();  // and the other CTAs' partials are visible before we say so
-        }
-      }
-      if (lane == 0) {
-        verdict[slot] = last;
-        mbar_arrive(&mb_verdict[slot]);
-      }
-    }
   } else {
     // -------------------------------------------------------- math warps
-    // Each math warp streams its own blocks (w, w+W, ... of every item) through
-    // a private ring of NS stages, issuing the copies of a block NS blocks before
-    // it needs it: many independent issuers keep HBM busy where one issuer per
-    // CTA could not.
+    // Each math warp takes whole work items from the queue (in order, one at a
+    // time) and streams every block of them through its own small ring,
+    // issuing the 2-D tensor copies (128-byte swizzled, L2 evict-first) of a
+    // block's K and V tiles NS blocks before it needs them.  Many independent
+    // issuers keep HBM busy, and no CTA-wide synchronisation is needed.
     const int w = warp;
-    const int tid = threadIdx.x;  // 0 .. W*32-1
     const int n0 = 2 * (lane & 3), n1 = n0 + 1;
     const uint64_t policy = dev::l2_policy_evict_first();
     uint8_t* ring = rings + size_t(w) * NS * S::kStageBytes;
     uint64_t* my_full = full + w * kWarpStages;
 
-    // issue cursor: item ii, block ij of it, ik blocks issued so far
-    int ii = 0, ij = w, ik = 0, inblk = -1, ig = 0;
+    // Waits for item x to be in the queue.  The pushed count goes first: the
+    // parity of a queue slot's barrier only tells laps apart once the slot's
+    // previous item (x - kQueue) has been pushed, which pushed > x implies.
+    auto wait_item = [&](int x) -> bool {
+      if (dev::ld_acquire_cta(pushed) <= x) {
+        const uint64_t t0 = dev::global_timer_ns();
+        while (dev::ld_acquire_cta(pushed) <= x) {
+          if (dev::global_timer_ns() - t0 > tmo) {
+            dev::flag_status(p.status, kStatusTimeout);
+            return false;
+          }
+          __nanosleep(64);
+        }
+      }
+      return mbar_wait_bounded(&item_full[x % kQueue], (x / kQueue) & 1, tmo, p.status);
+    };
+    auto claim = [&]() -> int {
+      int x = 0;
+      if (lane == 0) x = atomicAdd(claim_ctr, 1);
+      return __shfl_sync(0xffffffffu, x, 0);
+    };
+    // items held by this warp, oldest (the one being worked on) first; kept in
+    // four registers (h0 is the item in work)
+    int h0 = claim(), h1 = 0, h2 = 0, h3 = 0;
+    int nheld = 1;
+    auto held = [&](int i) { return i == 0 ? h0 : i == 1 ? h1 : i == 2 ? h2 : h3; };
+    auto hold = [&](int i, int v) {
+      if (i == 1) h1 = v;
+      else if (i == 2) h2 = v;
+      else if (i == 3) h3 = v;
+      else h0 = v;
+    };
+    // issue cursor: held[ipos], block ij of it; ik blocks issued so far
+    int ipos = 0, ij = 0, ik = 0, inblk = -1, ig = 0;
     const ItemSlot<D>* isl = nullptr;
     bool idone = false;
     // Issues this warp's next blocks until NS are in flight.  It never waits
-    // for an item whose queue slot this CTA still holds (it_c + kQueue on).
-    auto top_up = [&](int it_c, int kc) -> bool {
+    // for an item whose queue slot this warp itself still holds.
+    auto top_up = [&](int kc) -> bool {
       while (!idone && ik < kc + NS) {
         if (inblk < 0) {
-          if (ii >= it_c + kQueue) return true;
-          if (!mbar_wait_bounded(&item_full[ii % kQueue], (ii / kQueue) & 1, tmo, p.status))
-            return false;
-          isl = &items[ii % kQueue];
+          if (ipos == nheld) {
+            if (nheld == FIFO) return true;
+            hold(nheld++, claim());
+          }
+          const int x = held(ipos);
+          // Lookahead never blocks: an item not in the queue yet is tried again
+          // after the next block.  Its block list is readable as soon as it is
+          // pushed (release / acquire on the count); only the math needs the
+          // query copy to have landed.
+          if (x >= h0 + kQueue || dev::ld_acquire_cta(pushed) <= x) return true;
+          isl = &items[x % kQueue];
           if (isl->b < 0) {
             idone = true;
             return true;
@@ -401,8 +441,8 @@ __global__ void __launch_bounds__((W + 2) * 32)
           ig = isl->g;
         }
         if (ij >= inblk) {
-          ++ii;
-          ij = w;
+          ++ipos;
+          ij = 0;
           inblk = -1;
           continue;
         }
@@ -410,75 +450,47 @@ __global__ void __launch_bounds__((W + 2) * 32)
         const int st = ik % NS;
         if (lane == 0) dev::mbar_arrive_expect_tx(&my_full[st], S::kStageBytes);
         __syncwarp();
-        if (lane < 2 * HALVES) {  // lanes 0..3 (d = 128) issue the K and V boxes
-          const int which = lane / HALVES, h = lane % HALVES;
-          uint8_t* dst = ring + size_t(st) * S::kStageBytes + which * S::kTileBytes + h * 2048;
+        // lanes 0..HALVES-1 each issue one 128-byte-wide box of the K tile,
+        // then of the V tile (one tensor map per instruction)
+        if (lane < HALVES) {
+          uint8_t* dst = ring + size_t(st) * S::kStageBytes + lane * 2048;
           const int y = (phys * Hkv + ig) * kBlockSize;
-          dev::tma_load_2d(dst, which ? static_cast<const void*>(&tmap_v) : &tmap_k, h * 64, y,
-                           &my_full[st], policy);
+          dev::tma_load_2d(dst, &tmap_k, lane * 64, y, &my_full[st], policy);
+          dev::tma_load_2d(dst + S::kTileBytes, &tmap_v, lane * 64, y, &my_full[st], policy);
         }
         ++ik;
-        ij += W;
+        ++ij;
       }
       return true;
     };
+    int kc = 0;  // blocks consumed so far
+    TIME_MARK(0, dev::global_timer_ns());
     // On a timeout: let this warp's copies in flight land, then give up.
-    auto drain = [&](int kc) {
+    auto drain = [&]() {
       if (lane == 0)
         for (int k = kc; k < ik; ++k) mbar_wait_bounded(&my_full[k % NS], (k / NS) & 1, tmo, p.status);
       __syncwarp();
     };
 
-    // Merges all splits of (b, g) once the finisher says this CTA completed the
-    // last one (all math threads, one output element each).
-    auto merge_splits = [&](const int4 info) {
-      const int b = info.x, g = info.y, nsplit = info.z;
-      const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-      const size_t pbase = size_t(b) * p.max_splits * Hq + size_t(g) * G;
-      for (int e = tid; e < G * D; e += W * 32) {
-        const int hh = e / D, dd = e - hh * D;
-        float mrun = -INFINITY, lrun = 0.f, acc = 0.f;
-        for (int sp = 0; sp < nsplit; ++sp) {
-          const size_t r = pbase + size_t(sp) * Hq + hh;
-          const float lse = __ldcg(&p.ws.part_lse[r]);
-          const float ov = __ldcg(&p.ws.part_o[r * D + dd]);
-          const float mn = fmaxf(mrun, lse);
-          const float a = dev::fast_exp2(mrun - mn), wv = dev::fast_exp2(lse - mn);
-          acc = acc * a + wv * ov;
-          lrun = lrun * a + wv;
-          mrun = mn;
-        }
-        static_cast<T*>(p.out)[(head0 + hh) * D + dd] = M::from_float(acc / lrun);
-      }
-      if (tid == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
-    };
-    // Collects the finisher's verdict on item k (and merges if this CTA was last).
-    auto settle = [&](int k) -> bool {
-      const int slot = k % R;
-      if (!mbar_wait_bounded(&mb_verdict[slot], (k / R) & 1, tmo, p.status)) return false;
-      if (verdict[slot]) merge_splits(fin_info[slot]);
-      return true;
-    };
-
-    int kc = 0;  // blocks consumed so far
-    for (int it = 0;; ++it) {
-      const int qs = it % kQueue;
+    for (;;) {
+      const int x = h0;
+      const int qs = x % kQueue;
       PROF_T(t_item);
-      if (!mbar_wait_bounded(&item_full[qs], (it / kQueue) & 1, tmo, p.status)) {
-        drain(kc);
+      if (!wait_item(x)) {
+        drain();
         return;
       }
       PROF_ADD(3, t_item);
+#ifdef PA_PROFILE_TIMES
+      if (kc == 0 && (threadIdx.x & 31) == 0 && blockIdx.x * 16 + 15 >= 0)
+        g_times[(blockIdx.x * 16 + 14) * 3 + 0 + (warp & 1)] = dev::global_timer_ns();
+#endif
       const ItemSlot<D>& sl = items[qs];
       const int b = sl.b;
-      if (b < 0) {
+      if (b < 0) {  // end marker: every block this warp issued has been consumed
         PROF_ADD(11, t_kernel);
-        // drain: settle the items still in the finisher's hands, then stop it
-        for (int k = it - R; k < it; ++k)
-          if (k >= 0 && !settle(k)) return;
-        const int slot = it % R;
-        if (tid == 0) fin_info[slot] = make_int4(-1, 0, 0, 0);
-        mbar_arrive(&mb_done[slot]);
+        TIME_MARK(1, dev::global_timer_ns());
+        TIME_MARK(2, static_cast<unsigned long long>(kc));
         return;
       }
       const int g = sl.g, s = sl.s, ctx = sl.ctx, nblk = sl.nblk, nsplit = sl.nsplit;
@@ -494,8 +506,8 @@ __global__ void __launch_bounds__((W + 2) * 32)
           qb1[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
         }
       }
-      if (!top_up(it, kc)) {
-        drain(kc);
+      if (!top_up(kc)) {
+        drain();
         return;
       }
 
@@ -505,11 +517,11 @@ __global__ void __launch_bounds__((W + 2) * 32)
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
       const float sl2 = p.scale_log2;
 
-      for (int j = w; j < nblk; j += W) {
+      for (int j = 0; j < nblk; ++j) {
         const int st = kc % NS;
         PROF_T(t_full);
         if (!mbar_wait_bounded(&my_full[st], (kc / NS) & 1, tmo, p.status)) {
-          drain(kc);
+          drain();
           return;
         }
         PROF_ADD(0, t_full);
@@ -595,93 +607,108 @@ __global__ void __launch_bounds__((W + 2) * 32)
         ++kc;
         PROF_ADD(1, t_blk);
         PROF_INC(9, 1);
-        if (!top_up(it, kc)) {
-          drain(kc);
+        PROF_T(t_issue);
+        if (!top_up(kc)) {
+          drain();
           return;
         }
+        PROF_ADD(4, t_issue);
       }
       PROF_T(t_end);
       PROF_INC(10, 1);
 
-      // ---- merge the W warps' partial states through shared memory
+      // ---- end of the item: this warp holds the whole (m, l, O) of its split
 #pragma unroll
       for (int o_ = 4; o_ < 32; o_ <<= 1) {
         l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
         l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
       }
-      // the previous item's readers are done with the scratch
-      if (it > 0 && !mbar_wait_bounded(mb_read, (it - 1) & 1, tmo, p.status)) {
-        drain(kc);
-        return;
-      }
-      float* ow = merge_o + size_t(w) * G * S::kOPitch;
-      float* mlw = merge_ml + size_t(w) * kMaxGroup * 2;
-      if (lane < 4) {
-        if (n0 < G) {
-          mlw[n0 * 2] = m0;
-          mlw[n0 * 2 + 1] = l0;
-        }
-        if (n1 < G) {
-          mlw[n1 * 2] = m1;
-          mlw[n1 * 2 + 1] = l1;
-        }
-      }
-#pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        const int d0 = 16 * mt + (lane >> 2);
-        if (n0 < G) {
-          ow[n0 * S::kOPitch + d0] = o[mt][0];
-          ow[n0 * S::kOPitch + d0 + 8] = o[mt][2];
-        }
-        if (n1 < G) {
-          ow[n1 * S::kOPitch + d0] = o[mt][1];
-          ow[n1 * S::kOPitch + d0 + 8] = o[mt][3];
-        }
-      }
-      mbar_arrive(mb_merge);
-      PROF_T(t_merge);
-      if (!mbar_wait_bounded(mb_merge, it & 1, tmo, p.status)) {
-        drain(kc);
-        return;
-      }
-      PROF_ADD(13, t_merge);
-      // every warp has read this item's descriptor and query: release the slot
-      if (lane == 0) mbar_arrive(&item_empty[qs]);
-
+      const float inv0 = 1.f / l0, inv1 = 1.f / l1;
       const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-      const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
-      for (int e = tid; e < G * D; e += W * 32) {
-        const int hh = e / D, dd = e - hh * D;
-        float mf = -INFINITY;
+      if (nsplit == 1) {
+        T* orow = static_cast<T*>(p.out) + head0 * D;
 #pragma unroll
-        for (int ww = 0; ww < W; ++ww) mf = fmaxf(mf, merge_ml[ww * kMaxGroup * 2 + hh * 2]);
-        float acc = 0.f, ls = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < W; ++ww) {
-          const float wt = dev::fast_exp2(merge_ml[ww * kMaxGroup * 2 + hh * 2] - mf);
-          acc += wt * merge_o[(ww * G + hh) * S::kOPitch + dd];
-          ls += wt * merge_ml[ww * kMaxGroup * 2 + hh * 2 + 1];
+        for (int mt = 0; mt < KT; ++mt) {
+          const int d0 = 16 * mt + (lane >> 2);
+          if (n0 < G) {
+            orow[n0 * D + d0] = M::from_float(o[mt][0] * inv0);
+            orow[n0 * D + d0 + 8] = M::from_float(o[mt][2] * inv0);
+          }
+          if (n1 < G) {
+            orow[n1 * D + d0] = M::from_float(o[mt][1] * inv1);
+            orow[n1 * D + d0 + 8] = M::from_float(o[mt][3] * inv1);
+          }
         }
-        const float val = acc / ls;
-        if (nsplit == 1) {
-          static_cast<T*>(p.out)[(head0 + hh) * D + dd] = M::from_float(val);
-        } else {
-          p.ws.part_o[(part0 + hh) * D + dd] = val;
-          if (dd == 0) p.ws.part_lse[part0 + hh] = mf + log2f(ls);
+      } else {
+        const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
+        float* prow = p.ws.part_o + part0 * D;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          const int d0 = 16 * mt + (lane >> 2);
+          if (n0 < G) {
+            prow[n0 * D + d0] = o[mt][0] * inv0;
+            prow[n0 * D + d0 + 8] = o[mt][2] * inv0;
+          }
+          if (n1 < G) {
+            prow[n1 * D + d0] = o[mt][1] * inv1;
+            prow[n1 * D + d0 + 8] = o[mt][3] * inv1;
+          }
+        }
+        if (lane < 4) {
+          if (n0 < G) p.ws.part_lse[part0 + n0] = m0 + log2f(l0);
+          if (n1 < G) p.ws.part_lse[part0 + n1] = m1 + log2f(l1);
+        }
+        // publish this split, count it; the warp that completes (b, g) merges
+        __threadfence();
+        int last = 0;
+        if (lane == 0)
+          last = atomicAdd(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const size_t pbase = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+          T* orow = static_cast<T*>(p.out) + head0 * D;
+          // each lane owns 4 consecutive outputs per pass (one float4 per split)
+          for (int c = lane; c < G * D / 4; c += 32) {
+            const int hh = (c * 4) / D, dd = (c * 4) % D;
+            float mrun = -INFINITY, lrun = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int sp = 0; sp < nsplit; ++sp) {
+              const size_t r = pbase + size_t(sp) * Hq + hh;
+              const float lse = __ldcg(&p.ws.part_lse[r]);
+              const float4 ov = __ldcg(reinterpret_cast<const float4*>(&p.ws.part_o[r * D + dd]));
+              const float mn = fmaxf(mrun, lse);
+              const float a = dev::fast_exp2(mrun - mn), wv = dev::fast_exp2(lse - mn);
+              acc.x = acc.x * a + wv * ov.x;
+              acc.y = acc.y * a + wv * ov.y;
+              acc.z = acc.z * a + wv * ov.z;
+              acc.w = acc.w * a + wv * ov.w;
+              lrun = lrun * a + wv;
+              mrun = mn;
+            }
+            const float inv = 1.f / lrun;
+            orow[hh * D + dd + 0] = M::from_float(acc.x * inv);
+            orow[hh * D + dd + 1] = M::from_float(acc.y * inv);
+            orow[hh * D + dd + 2] = M::from_float(acc.z * inv);
+            orow[hh * D + dd + 3] = M::from_float(acc.w * inv);
+          }
+          if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
         }
       }
-      mbar_arrive(mb_read);
-      // settle the item that last used this finisher slot (merging its splits
-      // if this CTA finished the last one), then hand this item over
-      PROF_T(t_settle);
-      if (it >= R && !settle(it - R)) {
-        drain(kc);
-        return;
+      // done with this item: free its queue slot, move to the next one
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[qs]);
+      h0 = h1;
+      h1 = h2;
+      h2 = h3;
+      --nheld;
+      --ipos;
+      if (nheld == 0) {
+        h0 = claim();
+        nheld = 1;
+        ipos = 0;
       }
-      PROF_ADD(12, t_settle);
-      const int slot = it % R;
-      if (tid == 0) fin_info[slot] = make_int4(b, g, nsplit, 0);
-      mbar_arrive(&mb_done[slot]);
       PROF_ADD(2, t_end);
     }
   }
@@ -759,15 +786,23 @@ struct KernelConfig {
 // SM, and a cap on the ring stages per math warp.  Defaults are the measured
 // best.
 struct Tuning {
+  int split_blocks = 0;  // 0: by group size (16 blocks for G == 1, 32 otherwise)
   int warps = kConsumerWarps;
   int ctas_per_sm = 1;
   int max_stages = kWarpStages;
 };
-Tuning read_tuning() {
+Tuning read_tuning_env() {
   Tuning t;
   if (const char* v = std::getenv("PA_DECODE_WARPS")) t.warps = std::atoi(v) == 4 ? 4 : 8;
+  if (const char* v = std::getenv("PA_DECODE_SPLIT_BLOCKS"))
+    t.split_blocks = std::max(kMinSplitBlocks, std::min(kSplitBlocks, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_CTAS_PER_SM")) t.ctas_per_sm = std::max(1, std::min(4, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_MAX_STAGES")) t.max_stages = std::max(1, std::min(kWarpStages, std::atoi(v)));
+  return t;
+}
+// Read once per process.
+const Tuning& tuning() {
+  static const Tuning t = read_tuning_env();
   return t;
 }
 
@@ -796,7 +831,7 @@ cudaError_t configure_kernel(KernelConfig* cfg, const Tuning& t, size_t optin, s
     cfg[g].stages = stages;
     cfg[g].smem = Smem<D, W>::bytes(g, stages);
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg[g].ctas_per_sm, decode_kernel<T, D, W>,
-                                                      (W + 2) * 32, cfg[g].smem);
+                                                      (W + 1) * 32, cfg[g].smem);
     if (cfg[g].ctas_per_sm > t.ctas_per_sm) cfg[g].ctas_per_sm = t.ctas_per_sm;
   }
   return e;
@@ -823,7 +858,7 @@ int device_setup(int device) {
       st.error = PA_ERR_CUDA;
       return;
     }
-    st.tuning = read_tuning();
+    st.tuning = tuning();
     cudaError_t e = st.tuning.warps == 4 ? configure_all<4>(st, optin, per_sm)
                                          : configure_all<8>(st, optin, per_sm);
     st.error = e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -852,7 +887,9 @@ int get_encoder() {
 
 // 2-D view of a cache: rows = num_blocks * num_kv_heads * 16 token rows of
 // head_dim elements; one copy box = 16 rows x 64 elements (128 bytes wide,
-// 128-byte swizzle).
+// 128-byte swizzle), so a (block, head) tile is head_dim / 64 boxes.  In
+// shared memory, box h of a tile sits at h * 2048, row r at r * 128, with its
+// 16-byte chunks XOR-swizzled by r % 8.
 int encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, int num_blocks,
                      int num_kv_heads, int head_dim) {
   const cuuint64_t dims[2] = {cuuint64_t(head_dim),
@@ -915,7 +952,7 @@ int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) 
   prm.stages = kc.stages;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms * kc.ctas_per_sm);
-  cfg.blockDim = dim3((W + 2) * 32);
+  cfg.blockDim = dim3((W + 1) * 32);
   cfg.dynamicSmemBytes = kc.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -970,7 +1007,11 @@ Params make_params(const int32_t* context_lens, int num_seqs, int num_q_heads, i
   prm.head_dim = head_dim;
   prm.max_blocks = max_blocks_per_seq;
   prm.max_splits = lay.max_splits;
-  prm.signature = plan_signature(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  prm.split_blocks = tuning().split_blocks
+                         ? tuning().split_blocks
+                         : (num_q_heads == num_kv_heads ? kMinSplitBlocks : kSplitBlocks);
+  prm.signature = plan_signature(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                 prm.split_blocks);
   prm.ws.header = reinterpret_cast<int*>(ws + lay.header);
   prm.ws.units = reinterpret_cast<int*>(ws + lay.units);
   prm.ws.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
@@ -993,6 +1034,13 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   if (!status) return PA_ERR_CUDA;
   const Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                  max_blocks_per_seq, workspace, lay, status);
+  static std::once_flag carveout_once;
+  std::call_once(carveout_once, [] {
+    // keep the SM's shared-memory split the attention kernel wants, so no
+    // reconfiguration happens between the plan and the attention kernel
+    cudaFuncSetAttribute(plan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+  });
   plan_kernel<<<1, 1024, 0, stream>>>(prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
@@ -1081,6 +1129,15 @@ PA_API int pa_profile_read(unsigned long long* host, int ctas) {
   static unsigned long long zeros[2048 * kProfSlots];
   if (cudaMemcpyToSymbol(g_prof, zeros, bytes) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
+}
+#endif
+
+#ifdef PA_PROFILE_TIMES
+PA_API int pa_profile_times(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, g_times, size_t(n) * sizeof(unsigned long long)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
 }
 #endif
 

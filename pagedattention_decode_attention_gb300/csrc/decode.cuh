@@ -8,11 +8,12 @@ namespace pa {
 namespace decode {
 
 constexpr int kBlockSize = 16;      // tokens per physical block (device kernels)
-constexpr int kSplitBlocks = 32;    // logical blocks per work item (512 tokens)
+constexpr int kSplitBlocks = 32;    // most logical blocks per work item (512 tokens)
+constexpr int kMinSplitBlocks = 16; // fewest blocks a split may be planned with
 constexpr int kConsumerWarps = 8;   // default number of warps doing the attention math
 constexpr int kWarpStages = 4;      // upper bound of each math warp's (K, V) tile ring
-constexpr int kQueue = 8;           // work items buffered per CTA
-constexpr int kFinRing = 2;         // items whose split bookkeeping may be in flight
+constexpr int kQueue = 16;          // work-item slots per CTA
+constexpr int kSchedAhead = 2;      // pushed-but-unclaimed items the scheduler keeps
 constexpr int kMaxGroup = 8;        // query heads per KV head on the tensor-core path
 
 // Workspace header words.
@@ -40,7 +41,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                int max_blocks_per_seq) {
   Layout l;
-  l.max_splits = (max_blocks_per_seq + kSplitBlocks - 1) / kSplitBlocks;
+  // sized for the smallest split the plan may choose
+  l.max_splits = (max_blocks_per_seq + kMinSplitBlocks - 1) / kMinSplitBlocks;
   if (l.max_splits < 1) l.max_splits = 1;
   const size_t units = size_t(num_seqs) * l.max_splits;
   l.header = 0;
@@ -55,9 +57,10 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
 // Identifies the shapes a plan was made for, so a run can refuse a workspace
 // planned for something else.
 inline int plan_signature(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                          int max_blocks_per_seq) {
+                          int max_blocks_per_seq, int split_blocks) {
   uint32_t h = 2166136261u;
-  const int v[5] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq};
+  const int v[6] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                    split_blocks};
   for (int x : v) {
     h ^= uint32_t(x);
     h *= 16777619u;
@@ -75,6 +78,7 @@ struct Params {
   int num_seqs, num_q_heads, num_kv_heads, group, head_dim;
   int max_blocks, num_blocks, max_splits;
   int stages;        // depth of the shared-memory tile ring (tensor-core path)
+  int split_blocks;  // blocks per split, kMinSplitBlocks .. kSplitBlocks
   int signature;     // plan_signature() of these shapes
   float scale;       // softmax scale (fp32 path)
   float scale_log2;  // scale * log2(e) (tensor-core path works in base 2)
