@@ -178,6 +178,38 @@ PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, con
                                          size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_append_run -- pa_kv_append of one new token per
+ * sequence followed by pa_paged_attention_decode_run, in one launch.
+ *
+ * The two steps of a decode step the OS-lab appendix, section 2.1, describes
+ * for every layer (append the new token's K/V, then attend over the whole
+ * context including it), fused: the pages do not fuse them, the result is the
+ * same bit for bit.
+ *
+ * Row b of k_new / v_new ([num_seqs][num_kv_heads][head_dim], q's dtype) is
+ * sequence b's new token.  It is stored at slot_mapping[b] (int64, device)
+ * exactly as pa_kv_append stores token b, and sequence b attends over its
+ * context_lens[b] tokens, the last of which is the new one: slot_mapping[b]
+ * must be block_tables[b][(L - 1) / 16] * 16 + (L - 1) % 16 with
+ * L = context_lens[b] > 0, or negative (no new token: the row is not stored
+ * and the cache is attended as it is).  A slot >= num_blocks * 16, or one that
+ * is not that position, sets PA_ERR_DEVICE_BOUNDS (an out-of-range slot is
+ * not stored; for the other, sequence b's output is unspecified).  The block
+ * holding the new token must not be read by another sequence of the batch
+ * (copy-on-write guarantees this).  For context_lens[b] == 0 the row is
+ * stored and the output row is zero.  Needs a plan in the workspace like
+ * pa_paged_attention_decode_run.  F32 runs the two steps as two launches.
+ * Arguments otherwise as pa_paged_attention_decode_run; k_cache / v_cache
+ * are written.  k_new and v_new must be 16-byte aligned.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    int num_blocks, float scale, int dtype, void* out, void* workspace, size_t workspace_bytes,
+    void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_decode_noalloc -- pa_paged_attention_decode without a
  * caller-provided workspace.  (No counterpart on the pages: this entry point
  * exists for callers, not for the method.)
@@ -185,14 +217,14 @@ PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, con
  * For callers that cannot allocate device memory: code running inside a host
  * framework that owns the whole device-memory budget (a serving engine's
  * pre-reserved pool, a process held to a memory cap) may not call cudaMalloc
- * to make the workspace the other entry point needs.  This one uses a 64 MiB
+ * to make the workspace the other entry point needs.  This one uses a 128 MiB
  * scratch array compiled into the library instead; every GPU that loads the
  * library holds that array until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
  *
  * Same arguments and results as pa_paged_attention_decode, minus the
  * workspace.  Shapes whose workspace (see
- * pa_paged_attention_decode_workspace_size) exceeds 64 MiB are rejected with
+ * pa_paged_attention_decode_workspace_size) exceeds 128 MiB are rejected with
  * PA_ERR_INVALID_ARG before anything is launched.  The first call on a device
  * looks up that device's scratch address (cudaGetSymbolAddress, with the
  * device current), so make the first call on each device before any stream

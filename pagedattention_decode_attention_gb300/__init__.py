@@ -6,7 +6,9 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
 * :func:`kv_append` -- write new tokens' K/V rows into their paged slots;
 * :func:`paged_attention_decode` -- one decode step of attention over a block
   table, MHA and GQA (:func:`paged_attention_decode_plan` +
-  :func:`paged_attention_decode_run` split it so one plan serves every layer);
+  :func:`paged_attention_decode_run` split it so one plan serves every layer;
+  :func:`paged_attention_decode_append_run` also appends each sequence's new
+  token in the same launch);
 * :func:`block_copy` -- copy-on-write block copies across all layers;
 
 and the native host :class:`BlockPool` that produces tables, slots and copy
@@ -16,8 +18,9 @@ raises -- there is no fallback implementation.
 
 from .capi import PagedAttnError  # noqa: F401
 from .ops import (Prepared, alloc_workspace, block_copy, check_status, kv_append,  # noqa: F401
-                  paged_attention_decode, paged_attention_decode_plan,
-                  paged_attention_decode_run, prepare_decode_plan, prepare_decode_run,
+                  paged_attention_decode, paged_attention_decode_append_run,
+                  paged_attention_decode_plan, paged_attention_decode_run,
+                  prepare_decode_append_run, prepare_decode_plan, prepare_decode_run,
                   prepare_kv_append, workspace_size)
 from .pool import BlockPool  # noqa: F401
 

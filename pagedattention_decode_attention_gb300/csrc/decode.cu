@@ -15,25 +15,26 @@
 //    the tail of the persistent kernel is made of the smallest items.  The
 //    plan depends only on the context lengths, so one plan serves every layer
 //    of a decode step.
-//  * persistent attention kernel, one CTA per SM, two warp roles:
-//      - scheduler warp: takes work items from a global counter (four at a
-//        time, so their dependent global reads overlap), reads each item's
-//        block-table entries (range-checked) and bulk-copies the G query rows
-//        of (b, g) into a shared-memory item queue;
-//      - W math warps: each takes whole items from the queue and streams all
-//        their blocks through its own small ring, issuing the 2-D tensor
-//        copies (128-byte swizzled, L2 evict-first) of a block's K and V
-//        tiles a few blocks before it needs them.  Many independent issuers
-//        keep HBM busy; a single issuing thread per CTA could not (each copy
-//        instruction costs it hundreds of cycles), and no CTA-wide barrier is
-//        needed.  Per 16-token block: S^T = K . Q^T on the tensor cores
-//        (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of the
-//        group, K = head_dim), online softmax in base 2 with per-head running
-//        max / sum, P rounded to the input type and transposed in registers
-//        (movmatrix), O^T += V^T . P^T (M = head_dim rows of V^T via
-//        ldmatrix.trans).  Each K/V tile is read from HBM once for the whole
-//        query group.  Slots past the context in the last block are zeroed in
-//        registers, so whatever bits they hold cannot reach the output.
+//  * persistent attention kernel, one CTA of W math warps per SM.  Each warp
+//    works alone: it claims whole work items from a global counter (its first
+//    item is dealt statically), and streams every block of them through its
+//    own small ring, issuing the 2-D tensor copies (128-byte swizzled, L2
+//    evict-first) of a block's K and V tiles a few blocks before it needs
+//    them.  The claim of the next item is pipelined over the last blocks of
+//    the current one (counter reply, work unit, block-table entries with one
+//    entry per lane, then a bulk copy of the G query rows), so a warp commits
+//    to an item only shortly before it starts it and the work left in the
+//    list goes to whichever warp frees up first.  Many independent issuers
+//    keep HBM busy; a single issuing thread per CTA could not (each copy
+//    instruction costs it hundreds of cycles), and no CTA-wide barrier is
+//    needed.  Per 16-token block: S^T = K . Q^T on the tensor cores
+//    (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of the group,
+//    K = head_dim), online softmax in base 2 with per-head running max / sum,
+//    P rounded to the input type and transposed in registers (movmatrix),
+//    O^T += V^T . P^T (M = head_dim rows of V^T via ldmatrix.trans).  Each K/V
+//    tile is read from HBM once for the whole query group.  Slots past the
+//    context in the last block are zeroed in registers, so whatever bits they
+//    hold cannot reach the output.
 //    A sequence with one split is written to `out` straight from the
 //    warp's registers; otherwise the warp writes (o, lse) to the workspace,
 //    publishes it (fence) and counts it (atomic), and the warp that completes
@@ -67,9 +68,9 @@ namespace decode {
 using dev::mbar_arrive;
 using dev::mbar_wait_bounded;
 
-// Optional cycle accounting per CTA and warp role, compiled in only with
-// -DPA_PROFILE (a separate build used to see where a persistent CTA spends its
-// time; the default build has none of it).
+// Optional timestamps per warp and per item, compiled in only with
+// -DPA_PROFILE_TIMES (a separate build used to see where a persistent warp
+// spends its time; the default build has none of it).
 #ifdef PA_PROFILE_TIMES
 // per (CTA, warp): globaltimer at start of work, at end, blocks consumed
 __device__ unsigned long long g_times[2048 * 16 * 3];
@@ -78,64 +79,48 @@ __device__ unsigned long long g_times[2048 * 16 * 3];
     if ((threadIdx.x & 31) == 0)                                                            \
       g_times[(blockIdx.x * 16 + (threadIdx.x >> 5)) * 3 + (i)] = (v);                      \
   } while (0)
+// per (CTA, warp): its last 16 items as (start, end, blocks << 32 | splits,
+// ns spent merging << 32 | ns waiting for the query rows)
+__device__ unsigned long long g_item_trace[2048 * 16 * 16 * 4];
+#define ITEM_TRACE(n, start, blocks, splits, merge_ns, qwait_ns)                            \
+  do {                                                                                      \
+    if ((threadIdx.x & 31) == 0) {                                                          \
+      unsigned long long* r_ =                                                              \
+          &g_item_trace[((blockIdx.x * 16 + (threadIdx.x >> 5)) * 16 + ((n) & 15)) * 4];    \
+      r_[0] = (start);                                                                      \
+      r_[1] = dev::global_timer_ns();                                                       \
+      r_[2] = (static_cast<unsigned long long>(blocks) << 32) | unsigned(splits);           \
+      r_[3] = (static_cast<unsigned long long>(merge_ns) << 32) | unsigned(qwait_ns);       \
+    }                                                                                       \
+  } while (0)
 #else
 #define TIME_MARK(i, v)
+#define ITEM_TRACE(n, start, blocks, splits, merge_ns, qwait_ns)
 #endif
-
-#ifdef PA_PROFILE
-constexpr int kProfSlots = 16;
-__device__ unsigned long long g_prof[2048 * kProfSlots];
-#define PROF_T(var) const long long var = clock64()
-#define PROF_ADD(slot, t0)                                                                  \
-  do {                                                                                      \
-    if ((threadIdx.x & 31) == 0)                                                            \
-      atomicAdd(&g_prof[blockIdx.x * kProfSlots + (slot)],                                  \
-                static_cast<unsigned long long>(clock64() - (t0)));                         \
-  } while (0)
-#define PROF_INC(slot, v)                                                                   \
-  do {                                                                                      \
-    if ((threadIdx.x & 31) == 0)                                                            \
-      atomicAdd(&g_prof[blockIdx.x * kProfSlots + (slot)], static_cast<unsigned long long>(v)); \
-  } while (0)
-#else
-#define PROF_T(var)
-#define PROF_ADD(slot, t0)
-#define PROF_INC(slot, v)
-#endif
-
-template <int D>
-struct alignas(128) ItemSlot {
-  int b, g, s, ctx, nblk, nsplit, first, pad0;
-  int blocks[kSplitBlocks];
-  alignas(16) uint16_t q[kMaxGroup * D];
-};
 
 template <int D, int W>
 struct Smem {
   static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, head) tile
   static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
-  static constexpr size_t kItems = size_t(kQueue) * sizeof(ItemSlot<D>);
-  // barriers (uint64) + the claim and pushed counters
-  static constexpr size_t kBars = size_t(W) * kWarpStages + 2 * kQueue + 1;
-  static size_t fixed_bytes(int /*group*/) {
-    return 1024 /* alignment slack */ + kItems + kBars * 8 + 16;
-  }
-  // `stages` is per math warp
-  static size_t bytes(int group, int stages) {
-    return fixed_bytes(group) + size_t(W) * stages * kStageBytes;
-  }
-  static int stages_for(int group, size_t budget) {
-    const long avail = long(budget) - long(fixed_bytes(group));
-    long s = avail / (long(W) * kStageBytes);
-    if (s > kWarpStages) s = kWarpStages;
-    return int(s);
+  // one warp's staging buffer: its item's query rows, then the new token's
+  // K row and V row when the item carries the append
+  static constexpr int kQBytes = kMaxGroup * D * 2 + 2 * D * 2;
+  // layout: rings [W][stages][stage] | query buffers [W] | barriers [W][stages + 1]
+  static constexpr size_t kFixedBytes =
+      1024 /* alignment slack */ + size_t(W) * kQBytes + size_t(W) * (kWarpStages + 1) * 8;
+  static size_t bytes(int stages) { return kFixedBytes + size_t(W) * stages * kStageBytes; }
+  // deepest ring (stages per warp) that fits in `budget` bytes
+  static int stages_for(size_t budget) {
+    const long avail = long(budget) - long(kFixedBytes);
+    long st = avail / (long(W) * kStageBytes);
+    if (st > kWarpStages) st = kWarpStages;
+    return int(st);
   }
 };
 
 // ------------------------------------------------------------------ plan
-// Splits of one sequence are balanced: nsplit = ceil(blocks / 32) splits whose
-// sizes differ by at most one block.  Units are then counting-sorted by size,
-// largest first, and a sequence's splits stay adjacent in the order.
+// Splits of one sequence are balanced: nsplit = ceil(blocks / split) splits
+// whose sizes differ by at most one block.
 __device__ __forceinline__ void split_shape(int nblk, int split, int& nsplit, int& base,
                                             int& big) {
   nsplit = (nblk + split - 1) / split;
@@ -143,9 +128,22 @@ __device__ __forceinline__ void split_shape(int nblk, int split, int& nsplit, in
   big = nsplit ? nblk - base * nsplit : 0;  // the first `big` splits hold base + 1 blocks
 }
 
+// Units a split of n blocks becomes: itself, or balanced pieces of at most
+// kPieceBlocks blocks when n <= cut.
+__device__ __forceinline__ int pieces_of(int n, int cut) {
+  return n <= cut ? (n + kPieceBlocks - 1) / kPieceBlocks : 1;
+}
+
+// The work list is sorted by size, largest first, so the last items the
+// persistent kernel hands out are the smallest (longest-processing-time-first
+// order).  Its tail is made finer still: the smallest splits, whose work adds
+// up to about kTailWaves pieces per math warp, are cut into pieces of at most
+// kPieceBlocks blocks, so the warps run out of work at nearly the same time.
+// A sequence is cut only while its units fit the workspace's max_splits.
 __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   __shared__ int hist[kSplitBlocks + 2];
   __shared__ int bucket[kSplitBlocks + 2];
+  __shared__ int cut_s;
   dev::grid_launch_dependents();
   const int tid = threadIdx.x;
   if (tid < kSplitBlocks + 2) hist[tid] = 0;
@@ -153,6 +151,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   const int cap = p.max_blocks * kBlockSize;
   int4* units = reinterpret_cast<int4*>(p.ws.units);
 
+  // pass 1: split sizes before any cut
   for (int b = tid; b < p.num_seqs; b += 1024) {
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > cap) {
@@ -167,6 +166,45 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   }
   __syncthreads();
   if (tid == 0) {
+    // largest size `cut` such that all splits of at most `cut` blocks hold no
+    // more than the tail's share of the work
+    const long long budget = p.tail_blocks / p.num_kv_heads;
+    long long acc = 0;
+    int cut = 0;
+    while (cut < kSplitBlocks && acc + (long long)hist[cut + 1] * (cut + 1) <= budget) {
+      ++cut;
+      acc += (long long)hist[cut] * cut;
+    }
+    cut_s = cut;
+  }
+  __syncthreads();
+  const int cut_all = cut_s;
+  if (tid < kSplitBlocks + 2) hist[tid] = 0;
+  __syncthreads();
+
+  // pass 2: sizes of the final units (splits and pieces)
+  for (int b = tid; b < p.num_seqs; b += 1024) {
+    int ctx = p.context_lens[b];
+    ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
+    int nsplit, base, big;
+    split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
+    int cut = cut_all;
+    if (big * pieces_of(base + 1, cut) + (nsplit - big) * pieces_of(base, cut) > p.max_splits)
+      cut = 0;
+    int count = 0;
+    for (int k = 0; k < 2; ++k) {  // the two split sizes
+      const int n = base + 1 - k, m = k ? nsplit - big : big;
+      if (m == 0 || n == 0) continue;
+      const int np = pieces_of(n, cut);
+      count += m * np;
+      const int pb = n / np, pr = n - pb * np;  // pr pieces of pb + 1, the rest of pb
+      if (pr) atomicAdd(&hist[pb + 1], m * pr);
+      if (np - pr) atomicAdd(&hist[pb], m * (np - pr));
+    }
+    p.ws.nsplits[b] = count;
+  }
+  __syncthreads();
+  if (tid == 0) {
     int pos = 0;
     for (int r = kSplitBlocks; r >= 1; --r) {
       bucket[r] = pos;
@@ -178,541 +216,653 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
     p.ws.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
+
+  // pass 3: place every unit of a sequence, in block order, into its size's
+  // bucket: (b, first block, split index << 8 | blocks, context length)
   for (int b = tid; b < p.num_seqs; b += 1024) {
     int ctx = p.context_lens[b];
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
     split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
-    const int at_big = big ? atomicAdd(&bucket[base + 1], big) : 0;
-    const int at_small = nsplit - big ? atomicAdd(&bucket[base], nsplit - big) : 0;
-    int first = 0;
+    int cut = cut_all;
+    if (big * pieces_of(base + 1, cut) + (nsplit - big) * pieces_of(base, cut) > p.max_splits)
+      cut = 0;
+    // reserve this sequence's slots in each bucket it uses
+    int at[2][2];  // [split size k][piece size pb + 1 / pb]
+    for (int k = 0; k < 2; ++k) {
+      const int n = base + 1 - k, m = k ? nsplit - big : big;
+      at[k][0] = at[k][1] = 0;
+      if (m == 0 || n == 0) continue;
+      const int np = pieces_of(n, cut);
+      const int pb = n / np, pr = n - pb * np;
+      if (pr) at[k][0] = atomicAdd(&bucket[pb + 1], m * pr);
+      if (np - pr) at[k][1] = atomicAdd(&bucket[pb], m * (np - pr));
+    }
+    int first = 0, si = 0;
     for (int s = 0; s < nsplit; ++s) {
-      const int n = s < big ? base + 1 : base;
-      const int pos = s < big ? at_big + s : at_small + (s - big);
-      units[pos] = make_int4(b, (s << 8) | n, first, ctx);
-      first += n;
+      const int k = s < big ? 0 : 1;
+      const int n = base + 1 - k;
+      const int np = pieces_of(n, cut);
+      const int pb = n / np, pr = n - pb * np;
+      for (int j = 0; j < np; ++j) {
+        const int sz = j < pr ? pb + 1 : pb;
+        const int pos = j < pr ? at[k][0]++ : at[k][1]++;
+        units[pos] = make_int4(b, first, (si << 8) | sz, ctx);
+        first += sz;
+        ++si;
+      }
     }
   }
 }
 
 // --------------------------------------------------------- tensor-core path
+// Merges the nsplit partial results (o, lse) of the query heads of (b, g)
+// into out: out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M), M the largest
+// lse_s (a log-sum-exp merge; the partial o_s are already normalised).  One
+// warp does it, latency-bound on L2 reads of data other SMs just wrote (hence
+// .cg loads), so the reads are batched: first every (split, head) lse in one
+// round, then lane l owns the float4 columns c = l + 32 k (k < NK) of the
+// group's G x D outputs and issues the loads of U splits at once.
+// Where the partial results of one (b, g) live and where its merge goes.
+struct MergeArgs {
+  const float* lse;   // part_lse at (b, split 0, head g G); split stride Hq
+  const float4* po;   // part_o at the same row, as float4
+  void* out;          // out row of head g G of sequence b
+  int G, Hq, nsplit;
+};
+
+template <typename T, int D, int NK>
+__device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
+  using M = dev::Mma<T>;
+  constexpr int U = NK >= 6 ? 2 : 16 / NK;
+  const int G = a.G, Hq = a.Hq, nsplit = a.nsplit;
+  const int C = G * D / 4;  // float4 columns of the group's outputs
+  const float* lse = a.lse;
+  const float4* po = a.po;
+  const size_t split4 = size_t(Hq) * D / 4;  // float4s between two splits
+
+  // ---- per head: the largest lse and the sum of 2^(lse - largest)
+  float hm[kMaxGroup], hl[kMaxGroup];
+#pragma unroll
+  for (int hh = 0; hh < kMaxGroup; ++hh) {
+    hm[hh] = -INFINITY;
+    hl[hh] = 0.f;
+  }
+  for (int sp = lane; sp < nsplit; sp += 32) {
+    float x[kMaxGroup];
+#pragma unroll
+    for (int hh = 0; hh < kMaxGroup; ++hh)
+      x[hh] = hh < G ? __ldcg(lse + size_t(sp) * Hq + hh) : -INFINITY;
+#pragma unroll
+    for (int hh = 0; hh < kMaxGroup; ++hh) {
+      if (hh < G) {
+        const float mn = fmaxf(hm[hh], x[hh]);
+        hl[hh] = hl[hh] * dev::fast_exp2(hm[hh] - mn) + dev::fast_exp2(x[hh] - mn);
+        hm[hh] = mn;
+      }
+    }
+  }
+#pragma unroll
+  for (int hh = 0; hh < kMaxGroup; ++hh) {
+    if (hh < G) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, hm[hh], off);
+        const float ol = __shfl_xor_sync(0xffffffffu, hl[hh], off);
+        const float mn = fmaxf(hm[hh], om);
+        const float a = hm[hh] == -INFINITY ? 0.f : dev::fast_exp2(hm[hh] - mn);
+        const float c = om == -INFINITY ? 0.f : dev::fast_exp2(om - mn);
+        hl[hh] = hl[hh] * a + ol * c;
+        hm[hh] = mn;
+      }
+    }
+  }
+  // head of column k of this lane: 4 c / D, c = lane + 32 k
+  auto head_max = [&](int k) -> float {
+    if (D == 128) return hm[k < kMaxGroup ? k : 0];
+    const int h0 = 2 * k < kMaxGroup ? 2 * k : 0, h1 = 2 * k + 1 < kMaxGroup ? 2 * k + 1 : 0;
+    return (lane >> 4) ? hm[h1] : hm[h0];
+  };
+  auto head_sum = [&](int k) -> float {
+    if (D == 128) return hl[k < kMaxGroup ? k : 0];
+    const int h0 = 2 * k < kMaxGroup ? 2 * k : 0, h1 = 2 * k + 1 < kMaxGroup ? 2 * k + 1 : 0;
+    return (lane >> 4) ? hl[h1] : hl[h0];
+  };
+
+  // ---- weighted sum of the partial outputs
+  float4 acc[NK];
+#pragma unroll
+  for (int k = 0; k < NK; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int sp0 = 0; sp0 < nsplit; sp0 += U) {
+    float4 v[U][NK];
+    float w[U][NK];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int k = 0; k < NK; ++k) {
+        const int sp = sp0 + u, c = lane + 32 * k;
+        const bool on = sp < nsplit && c < C;
+        v[u][k] = on ? __ldcg(po + size_t(sp) * split4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[u][k] = on ? __ldcg(lse + size_t(sp) * Hq + (4 * c) / D) : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int k = 0; k < NK; ++k) {
+        const float e = w[u][k] == -INFINITY ? 0.f : dev::fast_exp2(w[u][k] - head_max(k));
+        acc[k].x += e * v[u][k].x;
+        acc[k].y += e * v[u][k].y;
+        acc[k].z += e * v[u][k].z;
+        acc[k].w += e * v[u][k].w;
+      }
+    }
+  }
+  T* orow = static_cast<T*>(a.out);
+#pragma unroll
+  for (int k = 0; k < NK; ++k) {
+    const int c = lane + 32 * k;
+    if (c < C) {
+      const float inv = 1.f / head_sum(k);
+      uint2 pk;
+      pk.x = M::pack(acc[k].x * inv, acc[k].y * inv);
+      pk.y = M::pack(acc[k].z * inv, acc[k].w * inv);
+      *reinterpret_cast<uint2*>(orow + 4 * c) = pk;
+    }
+  }
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
+  const int nk = (a.G * D / 4 + 31) / 32;
+  switch (nk) {
+    case 1: merge_splits<T, D, 1>(a, lane); break;
+    case 2: merge_splits<T, D, 2>(a, lane); break;
+    case 3: merge_splits<T, D, 3>(a, lane); break;
+    case 4: merge_splits<T, D, 4>(a, lane); break;
+    default:
+      if constexpr (D == 128) {
+        switch (nk) {
+          case 5: merge_splits<T, D, 5>(a, lane); break;
+          case 6: merge_splits<T, D, 6>(a, lane); break;
+          case 7: merge_splits<T, D, 7>(a, lane); break;
+          default: merge_splits<T, D, 8>(a, lane); break;
+        }
+      }
+  }
+}
+
+// A work item as a math warp holds it: registers only.  Lane j keeps the
+// physical block of the item's logical block j (an item has at most 32).
+struct Item {
+  int b;  // sequence, or -1 once the work list is exhausted
+  int g, s, nblk, first, ctx, nsplit;
+  int phys;
+  int slot;  // fused append: the new token's slot, or -1 (none / not this item)
+  bool patch;  // the new token is this item's last attended token
+};
+
 template <typename T, int D, int W>
-__global__ void __launch_bounds__((W + 1) * 32)
+__global__ void __launch_bounds__(W * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
   using S = Smem<D, W>;
   using M = dev::Mma<T>;
-  constexpr int KT = D / 16;        // 16-wide steps along head_dim
-  constexpr int HALVES = D / 64;    // 128-byte TMA boxes per tile row
-  constexpr int FIFO = 2;           // items a math warp may hold (1 in work + 1 lookahead)
+  constexpr int KT = D / 16;      // 16-wide steps along head_dim
+  constexpr int HALVES = D / 64;  // 128-byte TMA boxes per tile row
+  // The next item is claimed when this many blocks of the current one are
+  // still to be issued: its claim takes one pipeline step per block (counter,
+  // unit, table entries, query copy), so it is ready when the ring wants it.
+  constexpr int kLead = 3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int G = p.group;
-  const int NS = p.stages;  // ring stages per math warp
-  uint8_t* rings = smem;
-  ItemSlot<D>* items =
-      reinterpret_cast<ItemSlot<D>*>(rings + size_t(W) * NS * S::kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(items) + S::kItems);
-  uint64_t* item_full = full + W * kWarpStages;  // [W][kWarpStages] before it
-  uint64_t* item_empty = item_full + kQueue;
-  int* claim_ctr = reinterpret_cast<int*>(item_empty + kQueue);
-  // items the scheduler has written to the queue so far (only it writes)
-  volatile int* pushed = claim_ctr + 1;
-
+  const int NS = p.stages;  // ring stages of each warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#ifdef PA_PROFILE_TIMES
-  if (threadIdx.x == 0) g_times[(blockIdx.x * 16 + 15) * 3 + 0] = dev::global_timer_ns();
-#endif
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < W * kWarpStages; ++i) dev::mbar_init(&full[i], 1);
-    for (int i = 0; i < kQueue; ++i) {
-      dev::mbar_init(&item_full[i], 8);  // the lanes of one scheduler group
-      dev::mbar_init(&item_empty[i], 1);  // the one math warp that took the item
-    }
-    *claim_ctr = 0;
-    *pushed = 0;
+  uint8_t* ring = smem + size_t(warp) * NS * S::kStageBytes;
+  uint16_t* qbuf = reinterpret_cast<uint16_t*>(smem + size_t(W) * NS * S::kStageBytes +
+                                               size_t(warp) * S::kQBytes);
+  uint64_t* my_full = reinterpret_cast<uint64_t*>(smem + size_t(W) * NS * S::kStageBytes +
+                                                  size_t(W) * S::kQBytes) +
+                      warp * (kWarpStages + 1);
+  uint64_t* my_q = my_full + kWarpStages;
+
+  // Every warp owns its barriers, so no CTA-wide synchronisation is needed.
+  if (lane == 0) {
+    for (int i = 0; i < kWarpStages; ++i) dev::mbar_init(&my_full[i], 1);
+    dev::mbar_init(my_q, 1);
     dev::mbar_fence_init();
-  }
-  if (warp < W && lane == 0) {
     dev::prefetch_tensormap(&tmap_k);
     dev::prefetch_tensormap(&tmap_v);
   }
-  __syncthreads();
+  __syncwarp();
+  // The next kernel of the stream may start launching; it waits for this
+  // one's completion before it touches memory.
+  dev::grid_launch_dependents();
   dev::grid_dependency_wait();  // a plan launched just before has completed
+  TIME_MARK(0, dev::global_timer_ns());
 
-  PROF_T(t_kernel);
-#ifdef PA_PROFILE_TIMES
-  if (threadIdx.x == 0) g_times[(blockIdx.x * 16 + 15) * 3 + 1] = dev::global_timer_ns();
-#endif
   const unsigned long long tmo = p.timeout_ns;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
   const bool planned =
       *reinterpret_cast<volatile int*>(&p.ws.header[kHdrSignature]) == p.signature;
+  if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+  const int total = planned ? *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]) : 0;
+  const int4* units = reinterpret_cast<const int4*>(p.ws.units);
+  const int nwarps = int(gridDim.x) * W;
 
-  if (warp == W) {
-    // ------------------------------------------------------------ scheduler
-    // Four lane groups of 8 fetch four work items at once, so the dependent
-    // global round trips of an item (counter -> unit -> table entries) overlap.
-    if (!planned) {
-      if (lane == 0 && blockIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
-    } else {
-      // rows of empty sequences are zero
-      for (int b = blockIdx.x * 32 + lane; b < p.num_seqs; b += gridDim.x * 32) {
-        if (p.context_lens[b] <= 0) {
-          uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
-          for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-    const int total = planned ? *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]) : 0;
-    const int4* units = reinterpret_cast<const int4*>(p.ws.units);
-    const int grp = lane >> 3, gl = lane & 7;
-    int it = 0;
-    bool first_round = true;
-    for (bool more = true; more;) {
-      // Keep only a few unclaimed items queued: work left in the global list
-      // can still go to whichever CTA frees up first, which keeps the tail short.
-      if (planned) {
-        const uint64_t t0 = dev::global_timer_ns();
-        while (it - *reinterpret_cast<volatile int*>(claim_ctr) > kSchedAhead) {
-          if (dev::global_timer_ns() - t0 > tmo) {
-            dev::flag_status(p.status, kStatusTimeout);
-            return;
-          }
-          __nanosleep(128);
-        }
-      }
-      PROF_T(t_fetch);
-      // The first round is dealt statically (the largest items, one per group
-      // and CTA), which saves the counter's round trip at the start; later
-      // rounds take the next items from the global counter.
-      int idx = total;
-      if (planned && gl == 0)
-        idx = first_round ? grp * int(gridDim.x) + int(blockIdx.x)
-                          : 4 * int(gridDim.x) + atomicAdd(&p.ws.header[kHdrNext], 1);
-      first_round = false;
-      idx = __shfl_sync(0xffffffffu, idx, grp * 8);
-      const bool valid = idx < total;
-      int4 u = make_int4(0, 0, 0, 0);
-      if (valid) u = units[idx / Hkv];
-      const int g = valid ? idx % Hkv : 0;
-      const int b = u.x, s = u.y >> 8, nblk = u.y & 0xff, first = u.z, ctx = u.w;
-      int phys[kSplitBlocks / 8];
-#pragma unroll
-      for (int e = 0; e < kSplitBlocks / 8; ++e) {
-        const int j = gl + 8 * e;
-        phys[e] = 0;
-        if (valid && j < nblk) {
-          phys[e] = p.block_tables[size_t(b) * p.max_blocks + first + j];
-          if (phys[e] < 0 || phys[e] >= p.num_blocks) {
-            dev::flag_status(p.status, kStatusBounds);
-            phys[e] = 0;
+  const bool fused = p.slot_mapping != nullptr;
+  const long long num_slots = (long long)p.num_blocks * kBlockSize;
+  if (planned && warp == W - 1) {
+    // rows of empty sequences are zero; a new token of such a sequence is
+    // still stored (it attends nothing)
+    for (int b = blockIdx.x * 32 + lane; b < p.num_seqs; b += gridDim.x * 32) {
+      if (p.context_lens[b] <= 0) {
+        uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
+        for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
+        const long long slot = fused ? p.slot_mapping[b] : -1;
+        if (slot >= num_slots) dev::flag_status(p.status, kStatusBounds);
+        if (slot >= 0 && slot < num_slots) {
+          for (int h = 0; h < Hkv; ++h) {
+            const size_t src = (size_t(b) * Hkv + h) * D / 8;
+            const size_t dst = ((size_t(slot / kBlockSize) * Hkv + h) * kBlockSize +
+                                size_t(slot % kBlockSize)) * D / 8;
+            for (int c = 0; c < D / 8; ++c) {
+              static_cast<uint4*>(const_cast<void*>(p.k_cache))[dst + c] =
+                  static_cast<const uint4*>(p.k_new)[src + c];
+              static_cast<uint4*>(const_cast<void*>(p.v_cache))[dst + c] =
+                  static_cast<const uint4*>(p.v_new)[src + c];
+            }
           }
         }
       }
-      more = __all_sync(0xffffffffu, valid);
-      PROF_ADD(7, t_fetch);
-      // push the valid items of this round in group order
-      for (int q = 0; q < 4; ++q) {
-        if (!__shfl_sync(0xffffffffu, valid, q * 8)) continue;
-        const int qs = it % kQueue;
-        PROF_T(t_slot);
-        if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
-        PROF_ADD(8, t_slot);
-        if (grp == q) {
-          ItemSlot<D>& sl = items[qs];
-#pragma unroll
-          for (int e = 0; e < kSplitBlocks / 8; ++e) sl.blocks[gl + 8 * e] = phys[e];
-          if (gl == 0) {
-            const int nblk_all = (ctx + kBlockSize - 1) / kBlockSize;
-            sl.b = b;
-            sl.g = g;
-            sl.s = s;
-            sl.ctx = ctx;
-            sl.nblk = nblk;
-            sl.nsplit = (nblk_all + p.split_blocks - 1) / p.split_blocks;
-            sl.first = first;
-            const uint32_t qbytes = uint32_t(G) * D * 2;
-            dev::mbar_arrive_expect_tx(&item_full[qs], qbytes);
-            dev::bulk_load(sl.q,
-                           static_cast<const uint8_t*>(p.q) +
-                               (size_t(b) * Hq + size_t(g) * G) * D * 2,
-                           qbytes, &item_full[qs]);
-          } else {
-            mbar_arrive(&item_full[qs]);
-          }
-        }
-        ++it;
-        __syncwarp();
-        if (lane == 0) dev::st_release_cta(pushed, it);
-      }
     }
-    // no more work: one end marker for each math warp (each takes exactly one)
-    for (int e = 0; e < W; ++e, ++it) {
-      const int qs = it % kQueue;
-      if (!mbar_wait_bounded(&item_empty[qs], ((it / kQueue) & 1) ^ 1, tmo, p.status)) return;
-      if (grp == 0) {
-        if (gl == 0) items[qs].b = -1;
-        mbar_arrive(&item_full[qs]);
-      }
-      __syncwarp();
-      if (lane == 0) dev::st_release_cta(pushed, it + 1);
-    }
-    if (planned && lane == 0) {
-      // The last scheduler to finish returns the work counters to zero, so the
-      // next run on this plan starts clean.
+  }
+
+  // ---- claim pipeline for the next item (one step per call of advance())
+  //   1: the work counter's reply is awaited    2: the unit is being read
+  //   3: the table entries are being read       4: `nxt` is complete
+  Item cur, nxt;
+  cur.b = nxt.b = -1;
+  cur.g = cur.s = cur.nblk = cur.first = cur.ctx = cur.nsplit = cur.phys = 0;
+  nxt.g = nxt.s = nxt.nblk = nxt.first = nxt.ctx = nxt.nsplit = nxt.phys = 0;
+  cur.slot = nxt.slot = -1;
+  cur.patch = nxt.patch = false;
+  long long cslot = -1;  // slot_mapping[b] of the item being claimed
+  int cstage = 1;
+  int cx = blockIdx.x * W + warp;  // first item of every warp: dealt statically
+  int4 cu = make_int4(0, 0, 0, 0);
+  int q_issued = 0, q_taken = 0;  // query copies issued into / read from qbuf
+  auto finished = [&]() {
+    // This warp takes no more items.  The last warp to get here returns the
+    // counters to zero, so the next run on this plan starts clean.
+    if (lane == 0 && planned) {
       __threadfence();
-      if (atomicAdd(&p.ws.header[kHdrDone], 1) == int(gridDim.x) - 1) {
+      if (atomicAdd(&p.ws.header[kHdrDone], 1) == nwarps - 1) {
         atomicExch(&p.ws.header[kHdrNext], 0);
         atomicExch(&p.ws.header[kHdrDone], 0);
       }
     }
-  } else {
-    // -------------------------------------------------------- math warps
-    // Each math warp takes whole work items from the queue (in order, one at a
-    // time) and streams every block of them through its own small ring,
-    // issuing the 2-D tensor copies (128-byte swizzled, L2 evict-first) of a
-    // block's K and V tiles NS blocks before it needs them.  Many independent
-    // issuers keep HBM busy, and no CTA-wide synchronisation is needed.
-    const int w = warp;
-    const int n0 = 2 * (lane & 3), n1 = n0 + 1;
-    const uint64_t policy = dev::l2_policy_evict_first();
-    uint8_t* ring = rings + size_t(w) * NS * S::kStageBytes;
-    uint64_t* my_full = full + w * kWarpStages;
+  };
+  auto advance = [&]() {
+    if (cstage == 1) {
+      const int x = __shfl_sync(0xffffffffu, cx, 0);
+      if (x >= total) {
+        nxt.b = -1;
+        nxt.nblk = 0;
+        cstage = 4;
+        finished();
+      } else {
+        cu = __ldg(&units[x / Hkv]);
+        nxt.g = x % Hkv;
+        cstage = 2;
+      }
+    } else if (cstage == 2) {
+      nxt.b = cu.x;
+      nxt.first = cu.y;
+      nxt.s = cu.z >> 8;
+      nxt.nblk = cu.z & 0xff;
+      nxt.ctx = cu.w;
+      nxt.nsplit = __ldg(&p.ws.nsplits[nxt.b]);
+      cslot = fused ? __ldg(&p.slot_mapping[nxt.b]) : -1;
+      nxt.phys = lane < nxt.nblk
+                     ? __ldg(&p.block_tables[size_t(nxt.b) * p.max_blocks + nxt.first + lane])
+                     : 0;
+      cstage = 3;
+    } else if (cstage == 3) {
+      if (lane < nxt.nblk && (nxt.phys < 0 || nxt.phys >= p.num_blocks)) {
+        dev::flag_status(p.status, kStatusBounds);
+        nxt.phys = 0;
+      }
+      // Fused append: the item holding the sequence's last block stores the
+      // new token's K/V row of its KV head and uses it as its last token.
+      nxt.slot = -1;
+      nxt.patch = false;
+      if (fused && nxt.s == nxt.nsplit - 1 && cslot >= 0) {
+        if (cslot >= num_slots) {
+          dev::flag_status(p.status, kStatusBounds);
+        } else {
+          nxt.slot = int(cslot);
+          const int last_phys = __shfl_sync(0xffffffffu, nxt.phys, nxt.nblk - 1);
+          const long long at = (long long)last_phys * kBlockSize + (nxt.ctx - 1) % kBlockSize;
+          nxt.patch = at == cslot;
+          // a slot that is not the position of the sequence's last token
+          if (!nxt.patch) dev::flag_status(p.status, kStatusBounds);
+        }
+      }
+      // the G query rows of (b, g) (and the new K/V row) go to this warp's
+      // staging buffer, which the current item no longer reads: its rows are
+      // in registers
+      if (lane == 0) {
+        const uint32_t qbytes = uint32_t(G) * D * 2;
+        const uint32_t rbytes = nxt.slot >= 0 ? 2u * D * 2 : 0u;
+        dev::mbar_arrive_expect_tx(my_q, qbytes + rbytes);
+        dev::bulk_load(qbuf,
+                       static_cast<const uint8_t*>(p.q) +
+                           (size_t(nxt.b) * Hq + size_t(nxt.g) * G) * D * 2,
+                       qbytes, my_q);
+        if (rbytes) {
+          const size_t row = (size_t(nxt.b) * Hkv + nxt.g) * D * 2;
+          dev::bulk_load(qbuf + kMaxGroup * D, static_cast<const uint8_t*>(p.k_new) + row, D * 2,
+                         my_q);
+          dev::bulk_load(qbuf + kMaxGroup * D + D, static_cast<const uint8_t*>(p.v_new) + row,
+                         D * 2, my_q);
+        }
+      }
+      ++q_issued;
+      cstage = 4;
+    }
+  };
+  auto request = [&]() {  // starts the claim of the next item
+    if (lane == 0) cx = nwarps + atomicAdd(&p.ws.header[kHdrNext], 1);
+    cstage = 1;
+  };
 
-    // Waits for item x to be in the queue.  The pushed count goes first: the
-    // parity of a queue slot's barrier only tells laps apart once the slot's
-    // previous item (x - kQueue) has been pushed, which pushed > x implies.
-    auto wait_item = [&](int x) -> bool {
-      if (dev::ld_acquire_cta(pushed) <= x) {
-        const uint64_t t0 = dev::global_timer_ns();
-        while (dev::ld_acquire_cta(pushed) <= x) {
-          if (dev::global_timer_ns() - t0 > tmo) {
-            dev::flag_status(p.status, kStatusTimeout);
-            return false;
-          }
-          __nanosleep(64);
-        }
-      }
-      return mbar_wait_bounded(&item_full[x % kQueue], (x / kQueue) & 1, tmo, p.status);
-    };
-    auto claim = [&]() -> int {
-      int x = 0;
-      if (lane == 0) x = atomicAdd(claim_ctr, 1);
-      return __shfl_sync(0xffffffffu, x, 0);
-    };
-    // items held by this warp, oldest (the one being worked on) first; kept in
-    // four registers (h0 is the item in work)
-    int h0 = claim(), h1 = 0, h2 = 0, h3 = 0;
-    int nheld = 1;
-    auto held = [&](int i) { return i == 0 ? h0 : i == 1 ? h1 : i == 2 ? h2 : h3; };
-    auto hold = [&](int i, int v) {
-      if (i == 1) h1 = v;
-      else if (i == 2) h2 = v;
-      else if (i == 3) h3 = v;
-      else h0 = v;
-    };
-    // issue cursor: held[ipos], block ij of it; ik blocks issued so far
-    int ipos = 0, ij = 0, ik = 0, inblk = -1, ig = 0;
-    const ItemSlot<D>* isl = nullptr;
-    bool idone = false;
-    // Issues this warp's next blocks until NS are in flight.  It never waits
-    // for an item whose queue slot this warp itself still holds.
-    auto top_up = [&](int kc) -> bool {
-      while (!idone && ik < kc + NS) {
-        if (inblk < 0) {
-          if (ipos == nheld) {
-            if (nheld == FIFO) return true;
-            hold(nheld++, claim());
-          }
-          const int x = held(ipos);
-          // Lookahead never blocks: an item not in the queue yet is tried again
-          // after the next block.  Its block list is readable as soon as it is
-          // pushed (release / acquire on the count); only the math needs the
-          // query copy to have landed.
-          if (x >= h0 + kQueue || dev::ld_acquire_cta(pushed) <= x) return true;
-          isl = &items[x % kQueue];
-          if (isl->b < 0) {
-            idone = true;
-            return true;
-          }
-          inblk = isl->nblk;
-          ig = isl->g;
-        }
-        if (ij >= inblk) {
-          ++ipos;
-          ij = 0;
-          inblk = -1;
-          continue;
-        }
-        const int phys = isl->blocks[ij];
-        const int st = ik % NS;
-        if (lane == 0) dev::mbar_arrive_expect_tx(&my_full[st], S::kStageBytes);
-        __syncwarp();
-        // lanes 0..HALVES-1 each issue one 128-byte-wide box of the K tile,
-        // then of the V tile (one tensor map per instruction)
-        if (lane < HALVES) {
-          uint8_t* dst = ring + size_t(st) * S::kStageBytes + lane * 2048;
-          const int y = (phys * Hkv + ig) * kBlockSize;
-          dev::tma_load_2d(dst, &tmap_k, lane * 64, y, &my_full[st], policy);
-          dev::tma_load_2d(dst + S::kTileBytes, &tmap_v, lane * 64, y, &my_full[st], policy);
-        }
-        ++ik;
-        ++ij;
-      }
-      return true;
-    };
-    int kc = 0;  // blocks consumed so far
-    TIME_MARK(0, dev::global_timer_ns());
-    // On a timeout: let this warp's copies in flight land, then give up.
-    auto drain = [&]() {
-      if (lane == 0)
-        for (int k = kc; k < ik; ++k) mbar_wait_bounded(&my_full[k % NS], (k / NS) & 1, tmo, p.status);
+  // ---- issue cursor: blocks of `cur`, then of `nxt` once it is complete
+  int cur_issued = 0, nxt_issued = 0;
+  int ik = 0;  // blocks issued into the ring so far
+  const uint64_t policy = dev::l2_policy_evict_first();
+  auto top_up = [&](int kc) {
+    while (ik < kc + NS) {
+      bool from_cur = cur_issued < cur.nblk;
+      if (!from_cur && !(cstage == 4 && nxt_issued < nxt.nblk)) break;
+      const int j = from_cur ? cur_issued++ : nxt_issued++;
+      const int phys = __shfl_sync(0xffffffffu, from_cur ? cur.phys : nxt.phys, j);
+      const int gg = from_cur ? cur.g : nxt.g;
+      const int st = ik % NS;
+      if (lane == 0) dev::mbar_arrive_expect_tx(&my_full[st], S::kStageBytes);
       __syncwarp();
-    };
+      // lanes 0..HALVES-1 each issue one 128-byte-wide box of the K tile,
+      // then of the V tile (one tensor map per instruction)
+      if (lane < HALVES) {
+        uint8_t* dst = ring + size_t(st) * S::kStageBytes + lane * 2048;
+        const int y = (phys * Hkv + gg) * kBlockSize;
+        dev::tma_load_2d(dst, &tmap_k, lane * 64, y, &my_full[st], policy);
+        dev::tma_load_2d(dst + S::kTileBytes, &tmap_v, lane * 64, y, &my_full[st], policy);
+      }
+      ++ik;
+    }
+  };
+  int kc = 0;  // blocks consumed so far
+  // On a timeout: let this warp's copies in flight land, then give up.
+  auto drain = [&]() {
+    if (lane == 0) {
+      for (int k = kc; k < ik; ++k)
+        mbar_wait_bounded(&my_full[k % NS], (k / NS) & 1, tmo, p.status);
+      if (q_issued > q_taken) mbar_wait_bounded(my_q, q_taken & 1, tmo, p.status);
+    }
+    __syncwarp();
+  };
 
-    for (;;) {
-      const int x = h0;
-      const int qs = x % kQueue;
-      PROF_T(t_item);
-      if (!wait_item(x)) {
+  // the first item, claimed in full before anything else
+  while (cstage != 4) advance();
+#ifdef PA_PROFILE_TIMES
+  int n_items = 0;
+#endif
+  for (;;) {
+    // ---- move on to the next item
+    cur = nxt;
+    cur_issued = nxt_issued;
+    nxt_issued = 0;
+    nxt.b = -1;
+    nxt.nblk = 0;
+    cstage = 0;
+    if (cur.b < 0) break;
+#ifdef PA_PROFILE_TIMES
+    const unsigned long long item_t0 = dev::global_timer_ns();
+#endif
+    const int b = cur.b, g = cur.g, s = cur.s, ctx = cur.ctx, nblk = cur.nblk, first = cur.first;
+    const int nsplit = cur.nsplit;
+    // B fragments of Q^T (k = head_dim, n = query head of the group)
+    if (!mbar_wait_bounded(my_q, q_taken & 1, tmo, p.status)) {
+      drain();
+      return;
+    }
+    ++q_taken;
+#ifdef PA_PROFILE_TIMES
+    const unsigned long long qwait_ns = dev::global_timer_ns() - item_t0;
+    unsigned long long merge_ns = 0;
+#endif
+    uint32_t qb0[KT], qb1[KT];
+    {
+      const int hq = lane >> 2;
+      const int n0 = 2 * (lane & 3);
+      const uint16_t* qrow = qbuf + hq * D + n0;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        qb0[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk) : 0u;
+        qb1[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
+      }
+    }
+    // fused append: lane l < D/4 holds 16 bytes of the new K row (l < D/8)
+    // or V row; they go to the cache slot now and into the tile at the last block
+    uint4 nkv = make_uint4(0, 0, 0, 0);
+    if (cur.slot >= 0 && lane < D / 4) {
+      nkv = *reinterpret_cast<const uint4*>(qbuf + kMaxGroup * D + lane * 8);
+      const bool isv = lane >= D / 8;
+      const int c = isv ? lane - D / 8 : lane;
+      const size_t dst = ((size_t(cur.slot / kBlockSize) * Hkv + g) * kBlockSize +
+                          size_t(cur.slot % kBlockSize)) * (D / 8) + c;
+      static_cast<uint4*>(const_cast<void*>(isv ? p.v_cache : p.k_cache))[dst] = nkv;
+    }
+    // qbuf is read: order those reads before the copy that refills it
+    dev::fence_proxy_async_smem();
+    __syncwarp();
+    if (nblk - cur_issued <= kLead) request();
+    top_up(kc);
+
+    float o[KT][4];
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const float sl2 = p.scale_log2;
+
+    for (int j = 0; j < nblk; ++j) {
+      const int st = kc % NS;
+      if (!mbar_wait_bounded(&my_full[st], (kc / NS) & 1, tmo, p.status)) {
         drain();
         return;
       }
-      PROF_ADD(3, t_item);
-#ifdef PA_PROFILE_TIMES
-      if (kc == 0 && (threadIdx.x & 31) == 0 && blockIdx.x * 16 + 15 >= 0)
-        g_times[(blockIdx.x * 16 + 14) * 3 + 0 + (warp & 1)] = dev::global_timer_ns();
-#endif
-      const ItemSlot<D>& sl = items[qs];
-      const int b = sl.b;
-      if (b < 0) {  // end marker: every block this warp issued has been consumed
-        PROF_ADD(11, t_kernel);
-        TIME_MARK(1, dev::global_timer_ns());
-        TIME_MARK(2, static_cast<unsigned long long>(kc));
-        return;
+      const uint32_t kt = dev::smem_u32(ring + size_t(st) * S::kStageBytes);
+      const uint32_t vt = kt + S::kTileBytes;
+      if (cur.patch && j == nblk - 1) {
+        // the new token's row replaces whatever the cache held at its slot
+        const int r = (ctx - 1) % kBlockSize;
+        if (lane < D / 4) {
+          const bool isv = lane >= D / 8;
+          const int c = isv ? lane - D / 8 : lane;
+          const uint32_t addr =
+              (isv ? vt : kt) + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(nkv.x),
+                       "r"(nkv.y), "r"(nkv.z), "r"(nkv.w)
+                       : "memory");
+        }
+        __syncwarp();
       }
-      const int g = sl.g, s = sl.s, ctx = sl.ctx, nblk = sl.nblk, nsplit = sl.nsplit;
-      const int first = sl.first;
-      // B fragments of Q^T (k = head_dim, n = query head of the group)
-      uint32_t qb0[KT], qb1[KT];
+      // ---- S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8)
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
       {
-        const int hq = lane >> 2;
-        const uint16_t* qrow = sl.q + hq * D + n0;
+        const int row = lane & 15;
 #pragma unroll
         for (int kk = 0; kk < KT; ++kk) {
-          qb0[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk) : 0u;
-          qb1[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
+          const int gc = 2 * kk + (lane >> 4);  // 16-byte chunk along head_dim
+          const uint32_t addr =
+              kt + (gc >> 3) * 2048 + row * 128 + ((((gc & 7) ^ (row & 7))) << 4);
+          uint32_t a0, a1, a2, a3;
+          dev::ldmatrix_x4(addr, a0, a1, a2, a3);
+          if (kk & 1)
+            M::run(sb, a0, a1, a2, a3, qb0[kk], qb1[kk]);
+          else
+            M::run(sa, a0, a1, a2, a3, qb0[kk], qb1[kk]);
         }
       }
-      if (!top_up(kc)) {
-        drain();
-        return;
-      }
-
-      float o[KT][4];
-#pragma unroll
-      for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      const float sl2 = p.scale_log2;
-
-      for (int j = 0; j < nblk; ++j) {
-        const int st = kc % NS;
-        PROF_T(t_full);
-        if (!mbar_wait_bounded(&my_full[st], (kc / NS) & 1, tmo, p.status)) {
-          drain();
-          return;
-        }
-        PROF_ADD(0, t_full);
-        PROF_T(t_blk);
-        const uint32_t kt = dev::smem_u32(ring + size_t(st) * S::kStageBytes);
-        const uint32_t vt = kt + S::kTileBytes;
-        // ---- S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8)
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int row = lane & 15;
-#pragma unroll
-          for (int kk = 0; kk < KT; ++kk) {
-            const int gc = 2 * kk + (lane >> 4);  // 16-byte chunk along head_dim
-            const uint32_t addr =
-                kt + (gc >> 3) * 2048 + row * 128 + ((((gc & 7) ^ (row & 7))) << 4);
-            uint32_t a0, a1, a2, a3;
-            dev::ldmatrix_x4(addr, a0, a1, a2, a3);
-            if (kk & 1)
-              M::run(sb, a0, a1, a2, a3, qb0[kk], qb1[kk]);
-            else
-              M::run(sa, a0, a1, a2, a3, qb0[kk], qb1[kk]);
-          }
-        }
-        // ---- mask, scale to base 2, online softmax per head column
-        const int valid = ctx - (first + j) * kBlockSize;  // tokens of the block in context
-        const int r0 = lane >> 2;
-        const bool v0 = r0 < valid, v1 = r0 + 8 < valid;
-        const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-        const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-        const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-        const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
-        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int o_ = 4; o_ < 32; o_ <<= 1) {
-          bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o_));
-          bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o_));
-        }
-        const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-        const float al0 = dev::fast_exp2(m0 - mn0), al1 = dev::fast_exp2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
-        const uint32_t p01 = M::pack(dev::fast_exp2(x0 - mn0), dev::fast_exp2(x1 - mn1));
-        const uint32_t p23 = M::pack(dev::fast_exp2(x2 - mn0), dev::fast_exp2(x3 - mn1));
-        {
-          const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
-          l0 = l0 * al0 + f01.x + f23.x;
-          l1 = l1 * al1 + f01.y + f23.y;
-        }
-#pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-          o[mt][0] *= al0;
-          o[mt][1] *= al1;
-          o[mt][2] *= al0;
-          o[mt][3] *= al1;
-        }
-        // ---- P^T as the B operand: transpose the two 8x8 halves in registers
-        const uint32_t pb0 = dev::movmatrix_trans(p01);
-        const uint32_t pb1 = dev::movmatrix_trans(p23);
-        // V^T fragments hold tokens 2(lane%4)+{0,1} (a0, a1) and +8 (a2, a3):
-        // zero the ones past the context so their bits never meet P = 0.
-        uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
-        if (valid < kBlockSize) {
-          const int t = 2 * (lane & 3);
-          vm_lo = (t < valid ? 0x0000ffffu : 0u) | (t + 1 < valid ? 0xffff0000u : 0u);
-          vm_hi = (t + 8 < valid ? 0x0000ffffu : 0u) | (t + 9 < valid ? 0xffff0000u : 0u);
-        }
-        // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8)
-        {
-          const int tok = (lane & 7) + ((lane >> 4) << 3);
-#pragma unroll
-          for (int mt = 0; mt < KT; ++mt) {
-            const int gc = 2 * mt + ((lane >> 3) & 1);
-            const uint32_t addr =
-                vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
-            uint32_t a0, a1, a2, a3;
-            dev::ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-            M::run(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
-          }
-        }
-        // the stage is read; order those reads before the copy that reuses it
-        dev::fence_proxy_async_smem();
-        __syncwarp();
-        ++kc;
-        PROF_ADD(1, t_blk);
-        PROF_INC(9, 1);
-        PROF_T(t_issue);
-        if (!top_up(kc)) {
-          drain();
-          return;
-        }
-        PROF_ADD(4, t_issue);
-      }
-      PROF_T(t_end);
-      PROF_INC(10, 1);
-
-      // ---- end of the item: this warp holds the whole (m, l, O) of its split
+      // ---- mask, scale to base 2, online softmax per head column
+      const int valid = ctx - (first + j) * kBlockSize;  // tokens of the block in context
+      const int r0 = lane >> 2;
+      const bool v0 = r0 < valid, v1 = r0 + 8 < valid;
+      const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
+      const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
+      const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
+      const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
+      float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
       for (int o_ = 4; o_ < 32; o_ <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o_));
+        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o_));
       }
-      const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-      const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-      if (nsplit == 1) {
-        T* orow = static_cast<T*>(p.out) + head0 * D;
+      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+      const float al0 = dev::fast_exp2(m0 - mn0), al1 = dev::fast_exp2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      const uint32_t p01 = M::pack(dev::fast_exp2(x0 - mn0), dev::fast_exp2(x1 - mn1));
+      const uint32_t p23 = M::pack(dev::fast_exp2(x2 - mn0), dev::fast_exp2(x3 - mn1));
+      {
+        const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
+        l0 = l0 * al0 + f01.x + f23.x;
+        l1 = l1 * al1 + f01.y + f23.y;
+      }
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+      // ---- P^T as the B operand: transpose the two 8x8 halves in registers
+      const uint32_t pb0 = dev::movmatrix_trans(p01);
+      const uint32_t pb1 = dev::movmatrix_trans(p23);
+      // V^T fragments hold tokens 2(lane%4)+{0,1} (a0, a1) and +8 (a2, a3):
+      // zero the ones past the context so their bits never meet P = 0.
+      uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
+      if (valid < kBlockSize) {
+        const int t = 2 * (lane & 3);
+        vm_lo = (t < valid ? 0x0000ffffu : 0u) | (t + 1 < valid ? 0xffff0000u : 0u);
+        vm_hi = (t + 8 < valid ? 0x0000ffffu : 0u) | (t + 9 < valid ? 0xffff0000u : 0u);
+      }
+      // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8)
+      {
+        const int tok = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
-          const int d0 = 16 * mt + (lane >> 2);
-          if (n0 < G) {
-            orow[n0 * D + d0] = M::from_float(o[mt][0] * inv0);
-            orow[n0 * D + d0 + 8] = M::from_float(o[mt][2] * inv0);
-          }
-          if (n1 < G) {
-            orow[n1 * D + d0] = M::from_float(o[mt][1] * inv1);
-            orow[n1 * D + d0 + 8] = M::from_float(o[mt][3] * inv1);
-          }
-        }
-      } else {
-        const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
-        float* prow = p.ws.part_o + part0 * D;
-#pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-          const int d0 = 16 * mt + (lane >> 2);
-          if (n0 < G) {
-            prow[n0 * D + d0] = o[mt][0] * inv0;
-            prow[n0 * D + d0 + 8] = o[mt][2] * inv0;
-          }
-          if (n1 < G) {
-            prow[n1 * D + d0] = o[mt][1] * inv1;
-            prow[n1 * D + d0 + 8] = o[mt][3] * inv1;
-          }
-        }
-        if (lane < 4) {
-          if (n0 < G) p.ws.part_lse[part0 + n0] = m0 + log2f(l0);
-          if (n1 < G) p.ws.part_lse[part0 + n1] = m1 + log2f(l1);
-        }
-        // publish this split, count it; the warp that completes (b, g) merges
-        __threadfence();
-        int last = 0;
-        if (lane == 0)
-          last = atomicAdd(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          const size_t pbase = size_t(b) * p.max_splits * Hq + size_t(g) * G;
-          T* orow = static_cast<T*>(p.out) + head0 * D;
-          // each lane owns 4 consecutive outputs per pass (one float4 per split)
-          for (int c = lane; c < G * D / 4; c += 32) {
-            const int hh = (c * 4) / D, dd = (c * 4) % D;
-            float mrun = -INFINITY, lrun = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int sp = 0; sp < nsplit; ++sp) {
-              const size_t r = pbase + size_t(sp) * Hq + hh;
-              const float lse = __ldcg(&p.ws.part_lse[r]);
-              const float4 ov = __ldcg(reinterpret_cast<const float4*>(&p.ws.part_o[r * D + dd]));
-              const float mn = fmaxf(mrun, lse);
-              const float a = dev::fast_exp2(mrun - mn), wv = dev::fast_exp2(lse - mn);
-              acc.x = acc.x * a + wv * ov.x;
-              acc.y = acc.y * a + wv * ov.y;
-              acc.z = acc.z * a + wv * ov.z;
-              acc.w = acc.w * a + wv * ov.w;
-              lrun = lrun * a + wv;
-              mrun = mn;
-            }
-            const float inv = 1.f / lrun;
-            orow[hh * D + dd + 0] = M::from_float(acc.x * inv);
-            orow[hh * D + dd + 1] = M::from_float(acc.y * inv);
-            orow[hh * D + dd + 2] = M::from_float(acc.z * inv);
-            orow[hh * D + dd + 3] = M::from_float(acc.w * inv);
-          }
-          if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+          const int gc = 2 * mt + ((lane >> 3) & 1);
+          const uint32_t addr =
+              vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
+          uint32_t a0, a1, a2, a3;
+          dev::ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+          M::run(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
         }
       }
-      // done with this item: free its queue slot, move to the next one
+      // the stage is read; order those reads before the copy that reuses it
+      dev::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&item_empty[qs]);
-      h0 = h1;
-      h1 = h2;
-      h2 = h3;
-      --nheld;
-      --ipos;
-      if (nheld == 0) {
-        h0 = claim();
-        nheld = 1;
-        ipos = 0;
-      }
-      PROF_ADD(2, t_end);
+      ++kc;
+      advance();
+      if (cstage == 0 && nblk - cur_issued <= kLead) request();
+      top_up(kc);
     }
+
+    // ---- end of the item: this warp holds the whole (m, l, O) of its split
+#pragma unroll
+    for (int o_ = 4; o_ < 32; o_ <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
+    }
+    const int n0 = 2 * (lane & 3), n1 = n0 + 1;
+    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+    const size_t head0 = size_t(b) * Hq + size_t(g) * G;
+    if (nsplit == 1) {
+      T* orow = static_cast<T*>(p.out) + head0 * D;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d0 = 16 * mt + (lane >> 2);
+        if (n0 < G) {
+          orow[n0 * D + d0] = M::from_float(o[mt][0] * inv0);
+          orow[n0 * D + d0 + 8] = M::from_float(o[mt][2] * inv0);
+        }
+        if (n1 < G) {
+          orow[n1 * D + d0] = M::from_float(o[mt][1] * inv1);
+          orow[n1 * D + d0 + 8] = M::from_float(o[mt][3] * inv1);
+        }
+      }
+    } else {
+      const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
+      float* prow = p.ws.part_o + part0 * D;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d0 = 16 * mt + (lane >> 2);
+        if (n0 < G) {
+          prow[n0 * D + d0] = o[mt][0] * inv0;
+          prow[n0 * D + d0 + 8] = o[mt][2] * inv0;
+        }
+        if (n1 < G) {
+          prow[n1 * D + d0] = o[mt][1] * inv1;
+          prow[n1 * D + d0 + 8] = o[mt][3] * inv1;
+        }
+      }
+      if (lane < 4) {
+        if (n0 < G) p.ws.part_lse[part0 + n0] = m0 + log2f(l0);
+        if (n1 < G) p.ws.part_lse[part0 + n1] = m1 + log2f(l1);
+      }
+      // Publish this split and count it (release); the warp that completes
+      // (b, g) sees every other split's results (acquire) and merges them.
+      __syncwarp();
+      int last = 0;
+      if (lane == 0)
+        last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+#ifdef PA_PROFILE_TIMES
+        const unsigned long long merge_t0 = dev::global_timer_ns();
+#endif
+        __syncwarp();
+        const size_t row0 = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+        MergeArgs ma;
+        ma.lse = p.ws.part_lse + row0;
+        ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
+        ma.out = static_cast<T*>(p.out) + head0 * D;
+        ma.G = G;
+        ma.Hq = Hq;
+        ma.nsplit = nsplit;
+        merge_dispatch<T, D>(ma, lane);
+        if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+#ifdef PA_PROFILE_TIMES
+        merge_ns = dev::global_timer_ns() - merge_t0;
+#endif
+      }
+    }
+#ifdef PA_PROFILE_TIMES
+    ITEM_TRACE(n_items, item_t0, nblk, nsplit, merge_ns, qwait_ns);
+    ++n_items;
+#endif
+    // the next item must be complete before it becomes the current one
+    if (cstage == 0) request();
+    while (cstage != 4) advance();
   }
+  TIME_MARK(1, dev::global_timer_ns());
+  TIME_MARK(2, static_cast<unsigned long long>(kc));
 }
+
 
 // --------------------------------------------------------------- fp32 path
 template <int D>
@@ -790,6 +940,7 @@ struct Tuning {
   int warps = kConsumerWarps;
   int ctas_per_sm = 1;
   int max_stages = kWarpStages;
+  int tail_waves = kTailWaves;
 };
 Tuning read_tuning_env() {
   Tuning t;
@@ -798,6 +949,7 @@ Tuning read_tuning_env() {
     t.split_blocks = std::max(kMinSplitBlocks, std::min(kSplitBlocks, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_CTAS_PER_SM")) t.ctas_per_sm = std::max(1, std::min(4, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_MAX_STAGES")) t.max_stages = std::max(1, std::min(kWarpStages, std::atoi(v)));
+  if (const char* v = std::getenv("PA_DECODE_TAIL_WAVES")) t.tail_waves = std::max(0, std::min(16, std::atoi(v)));
   return t;
 }
 // Read once per process.
@@ -811,7 +963,7 @@ struct DeviceState {
   int error = 0;  // PA_OK or the status the set-up failed with
   int sms = 0;
   Tuning tuning;
-  KernelConfig cfg[2][2][kMaxGroup + 1];  // [bf16?][head_dim 128?][group]
+  KernelConfig cfg[2][2];  // [bf16?][head_dim 128?]
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -825,24 +977,23 @@ cudaError_t configure_kernel(KernelConfig* cfg, const Tuning& t, size_t optin, s
   if (budget > optin) budget = optin;
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, W>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(budget));
-  for (int g = 1; g <= kMaxGroup && e == cudaSuccess; ++g) {
-    int stages = Smem<D, W>::stages_for(g, budget);  // per math warp
-    if (stages > t.max_stages) stages = t.max_stages;
-    cfg[g].stages = stages;
-    cfg[g].smem = Smem<D, W>::bytes(g, stages);
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg[g].ctas_per_sm, decode_kernel<T, D, W>,
-                                                      (W + 1) * 32, cfg[g].smem);
-    if (cfg[g].ctas_per_sm > t.ctas_per_sm) cfg[g].ctas_per_sm = t.ctas_per_sm;
-  }
+  if (e != cudaSuccess) return e;
+  int stages = Smem<D, W>::stages_for(budget);  // per math warp
+  if (stages > t.max_stages) stages = t.max_stages;
+  cfg->stages = stages;
+  cfg->smem = Smem<D, W>::bytes(stages);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg->ctas_per_sm, decode_kernel<T, D, W>,
+                                                    W * 32, cfg->smem);
+  if (cfg->ctas_per_sm > t.ctas_per_sm) cfg->ctas_per_sm = t.ctas_per_sm;
   return e;
 }
 
 template <int W>
 cudaError_t configure_all(DeviceState& st, size_t optin, size_t per_sm) {
-  cudaError_t e = configure_kernel<__nv_bfloat16, 128, W>(st.cfg[1][1], st.tuning, optin, per_sm);
-  if (e == cudaSuccess) e = configure_kernel<__nv_bfloat16, 64, W>(st.cfg[1][0], st.tuning, optin, per_sm);
-  if (e == cudaSuccess) e = configure_kernel<__half, 128, W>(st.cfg[0][1], st.tuning, optin, per_sm);
-  if (e == cudaSuccess) e = configure_kernel<__half, 64, W>(st.cfg[0][0], st.tuning, optin, per_sm);
+  cudaError_t e = configure_kernel<__nv_bfloat16, 128, W>(&st.cfg[1][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__nv_bfloat16, 64, W>(&st.cfg[1][0], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 128, W>(&st.cfg[0][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 64, W>(&st.cfg[0][0], st.tuning, optin, per_sm);
   return e;
 }
 
@@ -864,9 +1015,7 @@ int device_setup(int device) {
     st.error = e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     for (int a = 0; a < 2 && st.error == PA_OK; ++a)
       for (int d = 0; d < 2; ++d)
-        for (int g = 1; g <= kMaxGroup; ++g)
-          if (st.cfg[a][d][g].stages < 1 || st.cfg[a][d][g].ctas_per_sm < 1)
-            st.error = PA_ERR_UNSUPPORTED;
+        if (st.cfg[a][d].stages < 1 || st.cfg[a][d].ctas_per_sm < 1) st.error = PA_ERR_UNSUPPORTED;
   });
   if (st.error != PA_OK) return fail(st.error, "decode: per-device set-up failed on device %d", device);
   return PA_OK;
@@ -919,7 +1068,7 @@ struct MapKey {
 };
 struct MapEntry {
   MapKey key{nullptr, 0, 0, 0, false};
-  alignas(64) CUtensorMap map;
+  CUtensorMap map;  // 64-byte aligned by its own declaration
 };
 constexpr int kMapCache = 256;
 thread_local MapEntry t_maps[kMapCache];
@@ -952,7 +1101,7 @@ int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) 
   prm.stages = kc.stages;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms * kc.ctas_per_sm);
-  cfg.blockDim = dim3((W + 1) * 32);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = kc.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1015,6 +1164,7 @@ Params make_params(const int32_t* context_lens, int num_seqs, int num_q_heads, i
   prm.ws.header = reinterpret_cast<int*>(ws + lay.header);
   prm.ws.units = reinterpret_cast<int*>(ws + lay.units);
   prm.ws.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
+  prm.ws.nsplits = reinterpret_cast<int*>(ws + lay.nsplits);
   prm.ws.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   prm.ws.part_o = reinterpret_cast<float*>(ws + lay.part_o);
   prm.status = status;
@@ -1032,8 +1182,17 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   if (!context_lens) return fail(PA_ERR_INVALID_ARG, "%s: context_lens is NULL", who);
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
-  const Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                 max_blocks_per_seq, workspace, lay, status);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
+  rc = device_setup(device);
+  if (rc != PA_OK) return rc;
+  Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                           max_blocks_per_seq, workspace, lay, status);
+  // the tail is sized for the math warps the attention kernel will launch
+  const DeviceState& st = g_dev[device];
+  const int nwarps = st.sms * st.cfg[1][head_dim == 128].ctas_per_sm * st.tuning.warps;
+  prm.tail_blocks = st.tuning.tail_waves * nwarps * kPieceBlocks;
   static std::once_flag carveout_once;
   std::call_once(carveout_once, [] {
     // keep the SM's shared-memory split the attention kernel wants, so no
@@ -1047,11 +1206,18 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   return PA_OK;
 }
 
+// The new tokens a fused call appends (all null: plain attention).
+struct AppendArgs {
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  const int64_t* slot_mapping = nullptr;
+};
+
 int run_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
              int head_dim, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
              void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-             const char* who) {
+             const char* who, const AppendArgs& app = AppendArgs()) {
   if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "%s: num_blocks must be positive", who);
   if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
     return fail(PA_ERR_INVALID_ARG, "%s: cache has too many rows", who);
@@ -1083,6 +1249,17 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
 
+  if (app.slot_mapping && dtype == PA_F32) {
+    // the fp32 path is not fused: append first, then attend
+    rc = pa_kv_append(app.k_new, app.v_new, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                      app.slot_mapping, num_seqs, num_kv_heads, head_dim, num_blocks, dtype,
+                      stream);
+    if (rc != PA_OK) return rc;
+  } else if (app.slot_mapping) {
+    prm.k_new = app.k_new;
+    prm.v_new = app.v_new;
+    prm.slot_mapping = app.slot_mapping;
+  }
   if (dtype == PA_F32) {
     const int blocks = (num_seqs * num_q_heads + 3) / 4;
     if (head_dim == 64)
@@ -1097,7 +1274,7 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
   rc = get_encoder();
   if (rc != PA_OK) return rc;
   const DeviceState& st = g_dev[device];
-  const KernelConfig& kc = st.cfg[dtype == PA_BF16][head_dim == 128][prm.group];
+  const KernelConfig& kc = st.cfg[dtype == PA_BF16][head_dim == 128];
   if (st.tuning.warps == 4) {
     if (dtype == PA_BF16)
       return head_dim == 128 ? launch_tc<__nv_bfloat16, 128, 4>(prm, kc, st.sms, stream)
@@ -1121,18 +1298,13 @@ using namespace pa::decode;
 
 extern "C" {
 
-#ifdef PA_PROFILE
-// Copies (and clears) the per-CTA cycle counters of a -DPA_PROFILE build.
-PA_API int pa_profile_read(unsigned long long* host, int ctas) {
-  const size_t bytes = size_t(ctas) * kProfSlots * sizeof(unsigned long long);
-  if (cudaMemcpyFromSymbol(host, g_prof, bytes) != cudaSuccess) return PA_ERR_CUDA;
-  static unsigned long long zeros[2048 * kProfSlots];
-  if (cudaMemcpyToSymbol(g_prof, zeros, bytes) != cudaSuccess) return PA_ERR_CUDA;
-  return PA_OK;
-}
-#endif
-
 #ifdef PA_PROFILE_TIMES
+PA_API int pa_profile_item_trace(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, g_item_trace, size_t(n) * sizeof(unsigned long long)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
 PA_API int pa_profile_times(unsigned long long* host, int n) {
   return cudaMemcpyFromSymbol(host, g_times, size_t(n) * sizeof(unsigned long long)) ==
                  cudaSuccess
@@ -1179,6 +1351,29 @@ PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, con
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who);
 }
 
+PA_API int pa_paged_attention_decode_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    int num_blocks, float scale, int dtype, void* out, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  const char* who = "paged_attention_decode_append_run";
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               dtype, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (!k_new || !v_new || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "%s: k_new, v_new and slot_mapping are required", who);
+  if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15))
+    return fail(PA_ERR_INVALID_ARG, "%s: k_new and v_new must be 16-byte aligned", who);
+  AppendArgs app;
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.slot_mapping = slot_mapping;
+  return run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                  num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                  workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who, app);
+}
+
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_tables, const int32_t* context_lens,
                                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -1213,7 +1408,7 @@ namespace pa {
 namespace decode {
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB per device
+constexpr size_t kStaticScratchBytes = size_t(128) << 20;  // 128 MiB per device
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 struct ScratchSlot {

@@ -10,29 +10,30 @@ namespace decode {
 constexpr int kBlockSize = 16;      // tokens per physical block (device kernels)
 constexpr int kSplitBlocks = 32;    // most logical blocks per work item (512 tokens)
 constexpr int kMinSplitBlocks = 16; // fewest blocks a split may be planned with
-constexpr int kConsumerWarps = 8;   // default number of warps doing the attention math
+constexpr int kPieceBlocks = 8;     // most blocks of a piece at the end of the work list
+constexpr int kTailWaves = 2;       // pieces at the end: about this many per math warp
+constexpr int kConsumerWarps = 8;   // default number of math warps per CTA
 constexpr int kWarpStages = 4;      // upper bound of each math warp's (K, V) tile ring
-constexpr int kQueue = 16;          // work-item slots per CTA
-constexpr int kSchedAhead = 2;      // pushed-but-unclaimed items the scheduler keeps
 constexpr int kMaxGroup = 8;        // query heads per KV head on the tensor-core path
 
 // Workspace header words.
 constexpr int kHdrNext = 0;       // next work item (self-resetting)
 constexpr int kHdrTotal = 1;      // number of work items (written by the plan)
-constexpr int kHdrDone = 2;       // CTAs whose scheduler has finished (self-resetting)
+constexpr int kHdrDone = 2;       // warps that have taken their last item (self-resetting)
 constexpr int kHdrSignature = 3;  // shape signature written by the plan
 
 // Views into the caller's workspace (all offsets 256-byte aligned).
 struct Workspace {
   int* header;       // see kHdr*
-  int* units;        // int4 per (sequence, split): b, split << 8 | blocks, first block, ctx
+  int* units;        // int4 per unit: b, first block, split index << 8 | blocks, ctx
   int* arrivals;     // [num_seqs * num_kv_heads] finished splits per (b, kv head)
+  int* nsplits;      // [num_seqs] splits the plan made of each sequence
   float* part_lse;   // [num_seqs][max_splits][num_q_heads]  (log2 domain)
   float* part_o;     // [num_seqs][max_splits][num_q_heads][head_dim]
 };
 
 struct Layout {
-  size_t header, units, arrivals, part_lse, part_o, total;
+  size_t header, units, arrivals, nsplits, part_lse, part_o, total;
   int max_splits;
 };
 
@@ -48,7 +49,8 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
   l.header = 0;
   l.units = align256(l.header + 256);
   l.arrivals = align256(l.units + units * 16);
-  l.part_lse = align256(l.arrivals + size_t(num_seqs) * num_kv_heads * 4);
+  l.nsplits = align256(l.arrivals + size_t(num_seqs) * num_kv_heads * 4);
+  l.part_lse = align256(l.nsplits + size_t(num_seqs) * 4);
   l.part_o = align256(l.part_lse + units * num_q_heads * 4);
   l.total = align256(l.part_o + units * num_q_heads * size_t(head_dim) * 4);
   return l;
@@ -75,10 +77,17 @@ struct Params {
   void* out;
   const int32_t* block_tables;
   const int32_t* context_lens;
+  // Fused append (all three null: none).  Row b of k_new / v_new
+  // ([num_seqs][num_kv_heads][head_dim]) is sequence b's new token, stored at
+  // slot_mapping[b] and attended as its token context_lens[b] - 1.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
   int num_seqs, num_q_heads, num_kv_heads, group, head_dim;
   int max_blocks, num_blocks, max_splits;
   int stages;        // depth of the shared-memory tile ring (tensor-core path)
   int split_blocks;  // blocks per split, kMinSplitBlocks .. kSplitBlocks
+  int tail_blocks;   // plan: work (in blocks) at the end of the list cut into pieces
   int signature;     // plan_signature() of these shapes
   float scale;       // softmax scale (fp32 path)
   float scale_log2;  // scale * log2(e) (tensor-core path works in base 2)

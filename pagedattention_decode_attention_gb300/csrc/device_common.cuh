@@ -42,6 +42,16 @@ __device__ __forceinline__ int ld_acquire_cta(volatile int* p) {
   return v;
 }
 
+// Atomic add at GPU scope with acquire-release semantics: the caller's earlier
+// writes (and those ordered before it, e.g. by a warp barrier) are visible to
+// whoever later acquires this location, and the caller sees all writes
+// released by earlier adds.  Returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -112,6 +112,40 @@ def paged_attention_decode_run(q, k_cache, v_cache, block_tables, context_lens, 
                    context_lens, scale, out, workspace, stream)
 
 
+def _append_args(q, k_new, v_new, slot_mapping, hkv, d):
+    dev, b = q.device, q.shape[0]
+    for name, t in (("k_new", k_new), ("v_new", v_new), ("slot_mapping", slot_mapping)):
+        _cuda_contig(name, t, dev)
+    _require(slot_mapping.dtype == torch.int64 and slot_mapping.shape == (b,),
+             "slot_mapping must be int64 [num_seqs]")
+    _require(k_new.dtype == v_new.dtype == q.dtype, "k_new / v_new must have q's dtype")
+    _require(k_new.shape == v_new.shape == (b, hkv, d),
+             "k_new, v_new must be [num_seqs, num_kv_heads, head_dim]")
+
+
+def paged_attention_decode_append_run(q, k_new, v_new, slot_mapping, k_cache, v_cache,
+                                      block_tables, context_lens, scale,
+                                      workspace: torch.Tensor, out=None,
+                                      stream=None) -> torch.Tensor:
+    """:func:`kv_append` of one new token per sequence (row ``b`` of ``k_new`` /
+    ``v_new`` to ``slot_mapping[b]``, the slot of the sequence's last token)
+    followed by :func:`paged_attention_decode_run`, in one launch.  The
+    workspace must hold a plan for these context lengths."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    _append_args(q, k_new, v_new, slot_mapping, hkv, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_append_run(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+        b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return out
+
+
 def _decode(fn, q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace, stream):
     dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
     if out is None:
@@ -132,7 +166,7 @@ def _decode(fn, q, k_cache, v_cache, block_tables, context_lens, scale, out, wor
 def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale,
                                    out=None, stream=None) -> torch.Tensor:
     """:func:`paged_attention_decode` for callers that cannot allocate device
-    memory: the library's built-in 64 MiB scratch replaces the workspace
+    memory: the library's built-in 128 MiB scratch replaces the workspace
     (calls on one device share it, so they must not overlap on the GPU)."""
     dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
     if out is None:
@@ -213,6 +247,25 @@ def prepare_decode_run(q, k_cache, v_cache, block_tables, context_lens, scale, w
             C.c_void_p(_stream(dev, stream)))
     return Prepared(capi.lib().pa_paged_attention_decode_run, args,
                     (q, k_cache, v_cache, block_tables, context_lens, workspace, out))
+
+
+def prepare_decode_append_run(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables,
+                              context_lens, scale, workspace, out, stream=None) -> Prepared:
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    _append_args(q, k_new, v_new, slot_mapping, hkv, d)
+    _cuda_contig("out", out, dev)
+    _cuda_contig("workspace", workspace, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    args = (C.c_void_p(q.data_ptr()), C.c_void_p(k_new.data_ptr()), C.c_void_p(v_new.data_ptr()),
+            C.c_void_p(slot_mapping.data_ptr()), C.c_void_p(k_cache.data_ptr()),
+            C.c_void_p(v_cache.data_ptr()), C.c_void_p(block_tables.data_ptr()),
+            C.c_void_p(context_lens.data_ptr()), b, hq, hkv, d, mb, nb, C.c_float(scale),
+            _dtype_code(q), C.c_void_p(out.data_ptr()), C.c_void_p(workspace.data_ptr()),
+            C.c_size_t(workspace.numel() * workspace.element_size()),
+            C.c_void_p(_stream(dev, stream)))
+    return Prepared(capi.lib().pa_paged_attention_decode_append_run, args,
+                    (q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                     workspace, out))
 
 
 def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:

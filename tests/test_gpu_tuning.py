@@ -1,0 +1,30 @@
+"""The attention kernel under non-default tuning (fewer warps, shallow rings,
+two CTAs per SM, no fine-grained tail, other split sizes), each in a child
+process because the tuning variables are read once per process."""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CONFIGS = {
+    "4warps_2stages_2ctas": {"PA_DECODE_WARPS": "4", "PA_DECODE_MAX_STAGES": "2",
+                             "PA_DECODE_CTAS_PER_SM": "2"},
+    "1stage": {"PA_DECODE_MAX_STAGES": "1"},
+    "no_tail_split16": {"PA_DECODE_TAIL_WAVES": "0", "PA_DECODE_SPLIT_BLOCKS": "16"},
+    "wide_tail_split24": {"PA_DECODE_TAIL_WAVES": "6", "PA_DECODE_SPLIT_BLOCKS": "24"},
+}
+
+
+@pytest.mark.parametrize("name", sorted(CONFIGS))
+def test_parity_under_tuning(gpu, name):
+    env = dict(os.environ)
+    env.update(CONFIGS[name])
+    r = subprocess.run([sys.executable, "-m", "tests.tuned_child"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]

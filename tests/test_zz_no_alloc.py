@@ -44,7 +44,7 @@ def test_noalloc_matches_workspace_entry_point_twice(gpu):
 def test_noalloc_rejects_shapes_beyond_its_scratch(gpu):
     from pagedattention_decode_attention_gb300 import capi
     lib = capi.lib()
-    # 4096 sequences x 256 blocks each: far more partial results than 64 MiB
+    # 4096 sequences x 256 blocks each: far more partial results than 128 MiB
     rc = lib.pa_paged_attention_decode_noalloc(256, 256, 256, 256, 256, 4096, 32, 8, 128, 4096,
                                                100000, C.c_float(0.1), capi.PA_BF16, 256, None)
     assert rc == capi.PA_ERR_INVALID_ARG
