@@ -140,11 +140,15 @@ __device__ __forceinline__ int pieces_of(int n, int cut) {
 // up to about kTailWaves pieces per math warp, are cut into pieces of at most
 // kPieceBlocks blocks, so the warps run out of work at nearly the same time.
 // A sequence is cut only while its units fit the workspace's max_splits.
-__global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
+constexpr int kPlanThreads = 256;  // small enough to sit beside an attention CTA
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
   __shared__ int hist[kSplitBlocks + 2];
   __shared__ int bucket[kSplitBlocks + 2];
   __shared__ int cut_s;
   dev::grid_launch_dependents();
+  // the previous kernel may still read the workspace (or write context_lens)
+  dev::grid_dependency_wait();
   const int tid = threadIdx.x;
   if (tid < kSplitBlocks + 2) hist[tid] = 0;
   __syncthreads();
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   int4* units = reinterpret_cast<int4*>(p.ws.units);
 
   // pass 1: split sizes before any cut
-  for (int b = tid; b < p.num_seqs; b += 1024) {
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > cap) {
       dev::flag_status(p.status, kStatusBounds);
@@ -183,7 +187,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
   __syncthreads();
 
   // pass 2: sizes of the final units (splits and pieces)
-  for (int b = tid; b < p.num_seqs; b += 1024) {
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx = p.context_lens[b];
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const Params p) {
 
   // pass 3: place every unit of a sequence, in block order, into its size's
   // bucket: (b, first block, split index << 8 | blocks, context length)
-  for (int b = tid; b < p.num_seqs; b += 1024) {
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx = p.context_lens[b];
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
@@ -440,7 +444,38 @@ __global__ void __launch_bounds__(W * 32)
   // The next kernel of the stream may start launching; it waits for this
   // one's completion before it touches memory.
   dev::grid_launch_dependents();
-  dev::grid_dependency_wait();  // a plan launched just before has completed
+  // While the kernel before this one finishes: warm L2 with the first blocks
+  // of this warp's statically dealt first item.  The work list and tables may
+  // still be changing (the previous kernel may be the plan), so this is only
+  // a hint: every value is range-checked before it becomes an address, and
+  // the real claim reads them again after the wait below.
+  {
+    const int x0 = blockIdx.x * W + warp;
+    const long long cap = (long long)p.num_seqs * p.max_splits * p.num_kv_heads;
+    const int total0 = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]);
+    if (x0 < total0 && x0 < cap) {
+      const int4 u = reinterpret_cast<const int4*>(p.ws.units)[x0 / p.num_kv_heads];
+      const int hg = x0 % p.num_kv_heads, n = u.z & 0xff;
+      constexpr int kWarmBlocks = 4;
+      if (u.x >= 0 && u.x < p.num_seqs && u.y >= 0 && n >= 1 && n <= kSplitBlocks &&
+          u.y + n <= p.max_blocks) {
+        const int nb = n < kWarmBlocks ? n : kWarmBlocks;
+        int phys = -1;
+        if (lane < nb) phys = p.block_tables[size_t(u.x) * p.max_blocks + u.y + lane];
+        for (int j = 0; j < nb; ++j) {
+          const int pj = __shfl_sync(0xffffffffu, phys, j);
+          if (pj < 0 || pj >= p.num_blocks) continue;
+          // a (block, head) tile is 16 * D * 2 bytes: D / 4 lines of 128 bytes
+          const size_t tile = (size_t(pj) * p.num_kv_heads + hg) * kBlockSize * D * 2;
+          for (int l = lane; l < D / 4; l += 32) {
+            dev::prefetch_l2(static_cast<const uint8_t*>(p.k_cache) + tile + size_t(l) * 128);
+            dev::prefetch_l2(static_cast<const uint8_t*>(p.v_cache) + tile + size_t(l) * 128);
+          }
+        }
+      }
+    }
+  }
+  dev::grid_dependency_wait();  // the kernel before this one has completed
   TIME_MARK(0, dev::global_timer_ns());
 
   const unsigned long long tmo = p.timeout_ns;
@@ -1200,8 +1235,16 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
     cudaFuncSetAttribute(plan_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                          cudaSharedmemCarveoutMaxShared);
   });
-  plan_kernel<<<1, 1024, 0, stream>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(kPlanThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, plan_kernel, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
 }
