@@ -254,12 +254,30 @@ class Replica:
         self.ws = pa.alloc_workspace(b, hq, hkv, d, batch.max_blocks, device)
         self.scale = batch.scale
         self.launches_per_step = 1 + L   # one plan, then one fused launch per layer
-        # Calls bound to this replica's buffers (validated once; each step only
-        # re-issues the C calls).
-        self.plan_call = pa.prepare_decode_plan(self.lens, hq, hkv, d, batch.max_blocks, self.ws)
-        self.layer_calls = [pa.prepare_decode_append_run(
-            self.q[i], self.k_new[i], self.v_new[i], self.slots, self.k_cache[i], self.v_cache[i],
-            self.tables, self.lens, self.scale, self.ws, self.out[i]) for i in range(L)]
+        self.plan_call, self.layer_calls = self.bind(self.inputs())
+
+    # the per-step inputs and the output of a step (the caches and the
+    # workspace are the replica's own)
+    INPUT_NAMES = ("q", "k_new", "v_new", "tables", "lens", "slots")
+
+    def inputs(self) -> dict:
+        return {n: getattr(self, n) for n in self.INPUT_NAMES + ("out",)}
+
+    def spare_inputs(self) -> dict:
+        """A second set of step buffers on the device (for double buffering)."""
+        return {n: torch.empty_like(t) for n, t in self.inputs().items()}
+
+    def bind(self, io: dict):
+        """Calls bound to one set of step buffers (validated once; each step
+        only re-issues the C calls)."""
+        pa, batch = self.pa, self.batch
+        hq, hkv, d = batch.num_q_heads, batch.num_kv_heads, batch.head_dim
+        plan = pa.prepare_decode_plan(io["lens"], hq, hkv, d, batch.max_blocks, self.ws)
+        layers = [pa.prepare_decode_append_run(
+            io["q"][i], io["k_new"][i], io["v_new"][i], io["slots"], self.k_cache[i],
+            self.v_cache[i], io["tables"], io["lens"], self.scale, self.ws, io["out"][i])
+            for i in range(batch.num_layers)]
+        return plan, layers
 
     def step(self, ev=None):
         """One decode step: the work list is planned once from the context
@@ -294,12 +312,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest x over the ranks (the slowest rank's time).  NCCL reduces a
+    device tensor; any other backend (gloo, in the CPU tests) a host one."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank_step: int, world: int, steps: int, secs: float) -> float:
+    """Whole-job tokens/s: every rank decodes its own batch each step, and
+    the job takes as long as its slowest rank (``secs``, max over ranks)."""
+    return tokens_per_rank_step * world * steps / secs
 
 
 def time_steps(rep: Replica, steps: int, world: int, events: bool):
@@ -323,31 +350,56 @@ def time_steps(rep: Replica, steps: int, world: int, events: bool):
 
 
 def time_e2e(rep: Replica, steps: int, world: int):
-    """Same steps with every step's inputs copied in from pinned host memory and
-    the outputs read back, inside the timed region."""
-    host_q = rep.q.cpu().pin_memory()
-    host_k = rep.k_new.cpu().pin_memory()
-    host_v = rep.v_new.cpu().pin_memory()
-    host_tab = rep.tables.cpu().pin_memory()
-    host_len = rep.lens.cpu().pin_memory()
-    host_slot = rep.slots.cpu().pin_memory()
-    host_out = torch.empty(rep.out.shape, dtype=rep.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (host_q, host_k, host_v, host_tab, host_len, host_slot))
-    d2h = host_out.numel() * host_out.element_size()
+    """Same steps, end to end: every step's inputs (q, new K/V rows, tables,
+    lengths, slots) are copied in from pinned host memory and its outputs read
+    back to pinned host memory, inside the timed region.  Two sets of step
+    buffers and two copy streams pipeline it: step i+1's inputs load and step
+    i-1's outputs drain while step i's kernels run."""
+    dev = rep.device
+    host_in = {n: t.cpu().pin_memory() for n, t in rep.inputs().items() if n != "out"}
+    host_out = [torch.empty(rep.out.shape, dtype=rep.out.dtype).pin_memory() for _ in range(2)]
+    sets = [rep.inputs(), rep.spare_inputs()]
+    calls = [(rep.plan_call, rep.layer_calls), rep.bind(sets[1])]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    main = torch.cuda.current_stream(dev)
+    load_s, drain_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def load(i):
+        j = i % 2
+        with torch.cuda.stream(load_s):
+            if i >= 2:
+                load_s.wait_event(computed[j])    # step i-2 no longer reads set j
+            for n, t in host_in.items():
+                sets[j][n].copy_(t, non_blocking=True)
+            loaded[j].record(load_s)
+
     barrier(world)
     torch.cuda.synchronize()
-    start.record()
-    for _ in range(steps):
-        rep.q.copy_(host_q, non_blocking=True)
-        rep.k_new.copy_(host_k, non_blocking=True)
-        rep.v_new.copy_(host_v, non_blocking=True)
-        rep.tables.copy_(host_tab, non_blocking=True)
-        rep.lens.copy_(host_len, non_blocking=True)
-        rep.slots.copy_(host_slot, non_blocking=True)
-        rep.step()
-        host_out.copy_(rep.out, non_blocking=True)
-    end.record()
+    start.record(main)
+    load(0)
+    for i in range(steps):
+        j = i % 2
+        if i + 1 < steps:
+            load(i + 1)
+        main.wait_event(loaded[j])
+        if i >= 2:
+            main.wait_event(drained[j])           # step i-2's outputs have been read back
+        plan, layers = calls[j]
+        plan()
+        for call in layers:
+            call()
+        computed[j].record(main)
+        with torch.cuda.stream(drain_s):
+            drain_s.wait_event(computed[j])
+            host_out[j].copy_(sets[j]["out"], non_blocking=True)
+            drained[j].record(drain_s)
+    main.wait_stream(drain_s)
+    end.record(main)
     torch.cuda.synchronize()
     barrier(world)
     return start.elapsed_time(end) / 1e3, h2d, d2h
@@ -430,7 +482,7 @@ def run_ours(args):
     kernel_ms = rep.kernel_only_ms()
     secs = max_over_ranks(secs, world)
     tokens_per_step = batch.num_seqs * world
-    value = tokens_per_step * args.steps / secs
+    value = weak_scaling_value(batch.num_seqs, world, args.steps, secs)
 
     ab = algorithmic_bytes(batch)
     # Average attention launch duration over the timed region: its event-timed
@@ -449,7 +501,9 @@ def run_ours(args):
         e_secs, h2d, d2h = time_e2e(rep, args.steps, world)
         e_secs = max_over_ranks(e_secs, world)
         e2e = {"value": tokens_per_step * args.steps / e_secs, "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "pipelining": ("two sets of step buffers: step i+1's host-to-device copies and "
+                              "step i-1's device-to-host copies overlap step i's kernels")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -482,6 +536,7 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs",
+                         "frac_of_nominal_7900": achieved / 7900.0,
                          "kernel": ("paged_attention_decode_append_run (persistent fused "
                                     "append + attention kernel)"),
                          "algorithmic_bytes_per_launch": ab["total"],

@@ -1,0 +1,71 @@
+"""The benchmark's multi-rank path on CPU: two gloo ranks (no GPU).
+
+Each rank is an independent replica (its own batch, no data-path exchange);
+the only cross-rank steps are the barrier around the timed region and the
+max over ranks of its length.  The reference arm runs on rank 0 alone.
+"""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        r, w, _ = bench.dist_env()
+        assert (r, w) == (rank, world)
+        batch = bench.make_batch("gqa_8b", rank)
+        bench.barrier(world)
+        slowest = bench.max_over_ranks(1.0 + rank, world)   # rank r "took" 1 + r seconds
+        value = bench.weak_scaling_value(batch.num_seqs, world, 10, slowest)
+        with open(os.path.join(out_dir, f"rank{rank}.json"), "w") as f:
+            json.dump({"slowest": slowest, "value": value, "seed": batch.seed,
+                       "lens_sum": int(batch.context_lens.sum()),
+                       "tables0": batch.block_tables[0, :4].tolist()}, f)
+        bench.barrier(world)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_are_independent_replicas(tmp_path):
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    r = [json.load(open(tmp_path / f"rank{i}.json")) for i in range(world)]
+    assert r[0]["slowest"] == r[1]["slowest"] == 2.0        # max over ranks
+    assert r[0]["value"] == r[1]["value"] == 128 * 2 * 10 / 2.0
+    assert r[0]["seed"] != r[1]["seed"]                      # independent batches
+    assert (r[0]["lens_sum"], r[0]["tables0"]) != (r[1]["lens_sum"], r[1]["tables0"])
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """``torchrun --nproc-per-node 2 bench.py --impl reference``: rank 0 prints
+    one JSON line, rank 1 exits 0 without work."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "1"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
