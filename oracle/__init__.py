@@ -9,7 +9,8 @@ it, and it never imports the product package: the two share no code.
 
 Modules
 -------
-attention : gather-through-block-table + softmax attention in float64,
+attention : gather-through-block-table + softmax attention in float64 (decode
+            and causal chunked prefill),
             kv_append and block_copy as plain element copies.
 pool      : a pure-Python model of the block pool (free list, refcounts,
             lazy allocation, fork, copy-on-write, prefix sharing, pinning).

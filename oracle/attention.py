@@ -114,6 +114,70 @@ def paged_attention_decode(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarr
     return out
 
 
+def chunk_positions(context_len: int, query_len: int) -> range:
+    """Token positions of a sequence's newest ``query_len`` tokens.
+
+    A prefill chunk is the last ``query_len`` tokens of the sequence's
+    ``context_len`` (their K/V already stored in the cache): positions
+    ``context_len - query_len .. context_len - 1``.
+    """
+    return range(context_len - query_len, context_len)
+
+
+def causal_prefix(buf: np.ndarray, position: int) -> np.ndarray:
+    """The tokens a query at ``position`` attends: 0 .. position inclusive."""
+    return buf[:position + 1]
+
+
+def paged_attention_prefill(q: np.ndarray, k_cache: np.ndarray, v_cache: np.ndarray,
+                            block_tables, context_lens, query_start, scale: float,
+                            rows=None) -> np.ndarray:
+    """Chunked-prefill attention over the paged cache.
+
+    OS-lab appendix, section 2.1: prefill writes the K/V of every prompt token
+    into the cache; "vLLM: treating the KV cache as virtual memory", section
+    "KV 的体积从哪来，页表如何把它切开": chunked prefill cuts a long prompt's
+    computation into pieces run between decode steps.  Each query attends, as
+    in any causal Transformer, over itself and the tokens before it.
+
+    ``q``: ``[total_q, num_q_heads, d]``; the query rows of sequence ``b`` are
+    ``query_start[b] .. query_start[b + 1] - 1`` (``T_b`` rows), the queries of
+    its newest ``T_b`` tokens (``chunk_positions``), whose K/V are in the cache
+    already, so ``T_b <= context_lens[b]``.  Query row ``i`` of sequence ``b``
+    at position ``p`` attends over tokens ``0 .. p`` of the sequence
+    (``causal_prefix``).  ``T_b = 1`` for every sequence is decode.  Returns
+    float64 ``[total_q, num_q_heads, d]``; ``rows`` restricts the work to a
+    sample of query rows (the others stay NaN).
+    """
+    total_q, num_q_heads, head_dim = q.shape
+    num_kv_heads = k_cache.shape[1]
+    group = num_q_heads // num_kv_heads
+    out = np.full((total_q, num_q_heads, head_dim), np.nan, dtype=np.float64)
+    wanted = None if rows is None else set(int(r) for r in rows)
+    for b in range(len(context_lens)):
+        first, last = int(query_start[b]), int(query_start[b + 1])
+        ctx, query_len = int(context_lens[b]), last - first
+        if query_len <= 0:
+            continue
+        if query_len > ctx:
+            raise ValueError(f"sequence {b}: {query_len} queries but only {ctx} tokens")
+        if wanted is not None and not any(first <= r < last for r in wanted):
+            continue
+        keys = gather_sequence(k_cache, block_tables[b], ctx)
+        values = gather_sequence(v_cache, block_tables[b], ctx)
+        for i, position in enumerate(chunk_positions(ctx, query_len)):
+            row = first + i
+            if wanted is not None and row not in wanted:
+                continue
+            k_seen = causal_prefix(keys, position)
+            v_seen = causal_prefix(values, position)
+            for h in range(num_q_heads):
+                kv_head = h // group
+                out[row, h] = attention_one(q[row, h].astype(np.float64),
+                                            k_seen[:, kv_head, :], v_seen[:, kv_head, :], scale)
+    return out
+
+
 def attention_lse(q: np.ndarray, keys: np.ndarray, scale: float) -> float:
     """Natural-log sum-exp of the scores of one query (used by split tests)."""
     if keys.shape[0] == 0:
