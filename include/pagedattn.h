@@ -210,6 +210,45 @@ PA_API int pa_paged_attention_decode_append_run(
     void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_prefill -- chunked-prefill attention over the paged cache.
+ *
+ * OS-lab appendix, section 2.1 (prefill writes the K/V of every prompt token
+ * into the cache) and "vLLM: treating the KV cache as virtual memory",
+ * section "KV 的体积从哪来，页表如何把它切开" (chunked prefill: a long prompt's
+ * computation is cut into pieces run between decode steps).
+ *
+ * Sequence b holds context_lens[b] tokens; its newest T_b tokens are a chunk
+ * whose K/V are already in the cache (pa_kv_append) and whose queries are
+ * rows query_start[b] .. query_start[b + 1] - 1 of q ([total_q][num_q_heads]
+ * [head_dim]); query_start (int32, device, num_seqs + 1 entries) is
+ * non-decreasing, query_start[0] >= 0, query_start[num_seqs] <= total_q.
+ * Query row i of sequence b is token p = context_lens[b] - T_b + i and, for
+ * query head h, attends over tokens 0 .. p with KV head h / (num_q_heads /
+ * num_kv_heads):
+ *   out[row][h] = softmax_t(scale * q[row][h] . K_t) V_t,  t <= p.
+ * T_b = 1 everywhere is decode; T_b = 0 skips the sequence.  out has q's
+ * shape and dtype; rows of no sequence are not written.  A sequence with
+ * T_b > context_lens[b], context_lens[b] > max_blocks_per_seq * 16 or rows
+ * outside [0, total_q) is skipped and sets PA_ERR_DEVICE_BOUNDS, as does a
+ * table entry outside [0, num_blocks) (read as block 0).
+ *
+ * Workspace: pa_paged_attention_prefill_workspace_size bytes, 256-byte
+ * aligned, owned by one call at a time, no initialisation needed.  Two
+ * launches (a one-CTA plan, then the attention kernel) on `stream`.  Same
+ * dtypes, head_dim and grouping limits as pa_paged_attention_decode.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_prefill_workspace_size(int num_seqs, int total_q, int num_q_heads,
+                                                     int num_kv_heads, int head_dim,
+                                                     size_t* bytes);
+PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      const int32_t* query_start, int num_seqs, int total_q,
+                                      int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int num_blocks, float scale,
+                                      int dtype, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_decode_noalloc -- pa_paged_attention_decode without a
  * caller-provided workspace.  (No counterpart on the pages: this entry point
  * exists for callers, not for the method.)

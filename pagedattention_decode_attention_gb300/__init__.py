@@ -9,6 +9,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
   :func:`paged_attention_decode_run` split it so one plan serves every layer;
   :func:`paged_attention_decode_append_run` also appends each sequence's new
   token in the same launch);
+* :func:`paged_attention_prefill` -- chunked-prefill attention: each
+  sequence's newest tokens attend causally over the paged cache;
 * :func:`block_copy` -- copy-on-write block copies across all layers;
 
 and the native host :class:`BlockPool` that produces tables, slots and copy
@@ -17,8 +19,10 @@ raises -- there is no fallback implementation.
 """
 
 from .capi import PagedAttnError  # noqa: F401
-from .ops import (Prepared, alloc_workspace, block_copy, check_status, kv_append,  # noqa: F401
-                  paged_attention_decode, paged_attention_decode_append_run,
+from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
+                  check_status, kv_append, paged_attention_decode,
+                  paged_attention_decode_append_run, paged_attention_prefill,
+                  prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,
                   prepare_decode_append_run, prepare_decode_plan, prepare_decode_run,
                   prepare_kv_append, workspace_size)

@@ -26,7 +26,7 @@ LIB_NAME = "libpagedattn.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["status.cpp", "pool.cpp", "copy_kernels.cu", "decode.cu"]
+SOURCES = ["status.cpp", "pool.cpp", "tensor_map.cpp", "copy_kernels.cu", "decode.cu", "prefill.cu"]
 
 
 def nvcc() -> str:

@@ -61,6 +61,7 @@
 #include "device_common.cuh"
 #include "pagedattn.h"
 #include "status.h"
+#include "tensor_map.h"
 
 namespace pa {
 namespace decode {
@@ -1002,8 +1003,6 @@ struct DeviceState {
 };
 DeviceState g_dev[kMaxDevices];
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
 
 template <typename T, int D, int W>
 cudaError_t configure_kernel(KernelConfig* cfg, const Tuning& t, size_t optin, size_t per_sm) {
@@ -1056,82 +1055,12 @@ int device_setup(int device) {
   return PA_OK;
 }
 
-int get_encoder() {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!g_encode) return fail(PA_ERR_CUDA, "decode: cuTensorMapEncodeTiled is unavailable");
-  return PA_OK;
-}
-
-// 2-D view of a cache: rows = num_blocks * num_kv_heads * 16 token rows of
-// head_dim elements; one copy box = 16 rows x 64 elements (128 bytes wide,
-// 128-byte swizzle), so a (block, head) tile is head_dim / 64 boxes.  In
-// shared memory, box h of a tile sits at h * 2048, row r at r * 128, with its
-// 16-byte chunks XOR-swizzled by r % 8.
-int encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, int num_blocks,
-                     int num_kv_heads, int head_dim) {
-  const cuuint64_t dims[2] = {cuuint64_t(head_dim),
-                              cuuint64_t(num_blocks) * num_kv_heads * kBlockSize};
-  const cuuint64_t strides[1] = {cuuint64_t(head_dim) * 2};
-  const cuuint32_t box[2] = {64, kBlockSize};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapDataType dt =
-      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUresult r = g_encode(map, dt, 2, const_cast<void*>(cache), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "decode: cuTensorMapEncodeTiled failed (%d)", int(r));
-  return PA_OK;
-}
-
-// Per-thread cache of encoded tensor maps: a decode step reuses the same layer
-// caches every step, and encoding is a host-side driver call.
-struct MapKey {
-  const void* ptr;
-  int num_blocks, num_kv_heads, head_dim;
-  bool bf16;
-  bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && num_blocks == o.num_blocks && num_kv_heads == o.num_kv_heads &&
-           head_dim == o.head_dim && bf16 == o.bf16;
-  }
-};
-struct MapEntry {
-  MapKey key{nullptr, 0, 0, 0, false};
-  CUtensorMap map;  // 64-byte aligned by its own declaration
-};
-constexpr int kMapCache = 256;
-thread_local MapEntry t_maps[kMapCache];
-
-int cached_cache_map(CUtensorMap* out, const void* cache, bool bf16, int num_blocks,
-                     int num_kv_heads, int head_dim) {
-  const MapKey key{cache, num_blocks, num_kv_heads, head_dim, bf16};
-  uint64_t h = reinterpret_cast<uintptr_t>(cache) >> 8;
-  h ^= uint64_t(num_blocks) * 0x9E3779B97F4A7C15ull ^ uint64_t(num_kv_heads * 131 + head_dim);
-  MapEntry& e = t_maps[(h ^ (h >> 17)) % kMapCache];
-  if (!(e.key == key)) {
-    int rc = encode_cache_map(&e.map, cache, bf16, num_blocks, num_kv_heads, head_dim);
-    if (rc != PA_OK) {
-      e.key = MapKey{nullptr, 0, 0, 0, false};
-      return rc;
-    }
-    e.key = key;
-  }
-  *out = e.map;
-  return PA_OK;
-}
-
 template <typename T, int D, int W>
 int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   alignas(64) CUtensorMap mk, mv;
-  int rc = cached_cache_map(&mk, prm.k_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
-  if (rc == PA_OK) rc = cached_cache_map(&mv, prm.v_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
+  int rc = cache_tensor_map(&mk, prm.k_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
+  if (rc == PA_OK) rc = cache_tensor_map(&mv, prm.v_cache, kBf16, prm.num_blocks, prm.num_kv_heads, D);
   if (rc != PA_OK) return rc;
   prm.stages = kc.stages;
   cudaLaunchConfig_t cfg = {};
@@ -1314,8 +1243,6 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
       return fail(PA_ERR_CUDA, "%s (fp32): launch failed: %s", who, cudaGetErrorString(e));
     return PA_OK;
   }
-  rc = get_encoder();
-  if (rc != PA_OK) return rc;
   const DeviceState& st = g_dev[device];
   const KernelConfig& kc = st.cfg[dtype == PA_BF16][head_dim == 128];
   if (st.tuning.warps == 4) {

@@ -1,0 +1,886 @@
+// Chunked-prefill attention over the paged KV cache, for sm_103a.
+//
+// What it computes: sequence b holds context_lens[b] tokens; its newest T_b of
+// them (a prefill chunk, K/V already stored in the cache) have query rows
+// query_start[b] .. query_start[b + 1] - 1.  Query row i (token position
+// p = context_lens[b] - T_b + i) of query head h attends over tokens 0 .. p:
+//   out[row][h] = softmax_t(scale * q[row][h] . K_t) . V_t,   t <= p,
+// K_t / V_t read through the block table (KV head h / G).  OS-lab appendix
+// "Lazy Allocation 与 Copy-on-Write 在 LLM 推理系统中的应用", section 2.1
+// (prefill writes the K/V of every prompt token to the cache); "vLLM: treating
+// the KV cache as virtual memory", section "KV 的体积从哪来，页表如何把它切开"
+// (chunked prefill cuts a long prompt into pieces run between decode steps).
+// Decode is the case T_b = 1.
+//
+// Design (ours; the pages give no kernel):
+//  * A work item is (sequence, KV head, block of 64 query rows, KV split).  A
+//    query row is one (token, query head of the group) pair, so one item's
+//    rows are up to 64 / G tokens of the chunk times the G heads that share
+//    the KV head: every K/V tile is read once for all of them.
+//  * plan kernel (1 CTA): query blocks per sequence, the KV range each needs
+//    (causal: up to its last token), KV splits only when the query blocks
+//    alone cannot fill the GPU, units ordered by size (largest first).
+//  * attention kernel: persistent CTAs of 4 warps, 16 query rows each, sharing
+//    a TMA-fed ring of 16-token K/V blocks (one issuing thread; a stage is
+//    refilled once all 4 warps have released it).  Per block and warp:
+//    S = Q K^T (16 rows x 16 tokens, m16n8k16 on the tensor cores), causal
+//    and context masks, online softmax in base 2, P reused in registers as
+//    the A operand of O += P V (V^T fragments via ldmatrix.trans).  Splits of
+//    a query block are merged with log-sum-exp weights by the CTA that
+//    finishes the last one.
+//  * fp32 caches take a plain CUDA-core path (one warp per (row, head)).
+//  * Every wait is an mbarrier or spin wait with a time limit; running out
+//    sets the timeout bit of the device status word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <type_traits>
+
+#include "device_common.cuh"
+#include "pagedattn.h"
+#include "status.h"
+#include "tensor_map.h"
+
+namespace pa {
+namespace prefill {
+
+constexpr int kBlockSize = 16;       // tokens per physical block
+constexpr int kWarps = 4;            // math warps per CTA
+constexpr int kRows = kWarps * 16;   // query rows per work item
+constexpr int kStages = 4;           // depth of the CTA's K/V ring
+constexpr int kMaxGroup = 8;         // query heads per KV head
+constexpr int kMinSplitBlocks = 16;  // smallest KV split
+constexpr int kPartialItems = 1024;  // (split unit, KV head) partial results, at most
+constexpr int kSizeBuckets = 32;     // work-list order: floor(log2(blocks)) buckets
+
+// Workspace header words.
+constexpr int kHdrNext = 0, kHdrTotal = 1, kHdrDone = 2, kHdrSignature = 3;
+
+struct Params {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  void* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;
+  int num_seqs, total_q, num_q_heads, num_kv_heads, group, head_dim;
+  int max_blocks, num_blocks;
+  int ncta;          // CTAs the attention kernel runs with (plan: how much to split)
+  int units_cap;     // unit slots in the workspace
+  int partial_cap;   // partial-result units in the workspace (per KV head)
+  int signature;
+  float scale, scale_log2;
+  int* header;
+  int4* units;       // 2 x int4 per unit (see plan)
+  int* arrivals;     // [partial_cap][num_kv_heads]
+  float* part_lse;   // [partial_cap][num_kv_heads][kRows]
+  float* part_o;     // [partial_cap][num_kv_heads][kRows][head_dim]
+  unsigned* status;
+  unsigned long long timeout_ns;
+};
+
+struct Layout {
+  size_t header, units, arrivals, part_lse, part_o, total;
+  int units_cap, partial_cap;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+inline Layout workspace_layout(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                               int head_dim) {
+  Layout l;
+  const int group = num_q_heads / num_kv_heads;
+  // query blocks: sum over sequences of ceil(T_b G / 64) <= total_q G / 64 + num_seqs
+  const long long qblocks = (long long)total_q * group / kRows + num_seqs + 1;
+  l.partial_cap = std::max(1, kPartialItems / num_kv_heads);
+  l.units_cap = int(std::min<long long>(qblocks + l.partial_cap, 1ll << 30));
+  l.header = 0;
+  l.units = align256(256);
+  l.arrivals = align256(l.units + size_t(l.units_cap) * 32);
+  l.part_lse = align256(l.arrivals + size_t(l.partial_cap) * num_kv_heads * 4);
+  l.part_o = align256(l.part_lse + size_t(l.partial_cap) * num_kv_heads * kRows * 4);
+  l.total = align256(l.part_o + size_t(l.partial_cap) * num_kv_heads * kRows * head_dim * 4);
+  return l;
+}
+
+inline int signature_of(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                        int head_dim, int max_blocks) {
+  uint32_t h = 2166136261u;
+  const int v[7] = {num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_blocks, 0x5EED};
+  for (int x : v) {
+    h ^= uint32_t(x);
+    h *= 16777619u;
+  }
+  return int(h | 1u);
+}
+
+// ------------------------------------------------------------------ plan
+// A query block qb of sequence b covers rows qb*64 .. of the sequence's
+// T_b * G rows; its last row's token sits at position ctx - T_b + i_last,
+// so it needs KV blocks 0 .. that position / 16.
+__device__ __forceinline__ int qblock_blocks(int ctx, int qlen, int group, int qb) {
+  const int rows = qlen * group;
+  const int last_row = min((qb + 1) * kRows, rows) - 1;
+  const int pos = ctx - qlen + last_row / group;
+  return pos / kBlockSize + 1;
+}
+
+__device__ __forceinline__ int size_bucket(int n) { return 31 - __clz(n); }  // floor(log2 n)
+
+constexpr int kPlanThreads = 256;
+
+__global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params p) {
+  __shared__ unsigned long long s_blocks;
+  __shared__ int s_qblocks, s_split_units, s_split, s_slot, s_group;
+  __shared__ int hist[kSizeBuckets];
+  __shared__ int bucket[kSizeBuckets];
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();  // the previous kernel may still read the workspace
+  const int tid = threadIdx.x;
+  const int G = p.group;
+  const int cap = p.max_blocks * kBlockSize;
+  if (tid == 0) {
+    s_blocks = 0;
+    s_qblocks = 0;
+    s_slot = 0;
+    s_group = 0;
+  }
+  if (tid < kSizeBuckets) hist[tid] = 0;
+  __syncthreads();
+
+  // a sequence's chunk: (ctx, qlen), or qlen = 0 when its lengths are invalid
+  auto chunk = [&](int b, int& ctx, int& qlen) {
+    ctx = p.context_lens[b];
+    const int q0 = p.query_start[b], q1 = p.query_start[b + 1];
+    qlen = q1 - q0;
+    if (ctx < 0 || ctx > cap || qlen < 0 || qlen > ctx || q0 < 0 || q1 > p.total_q) {
+      dev::flag_status(p.status, kStatusBounds);
+      qlen = 0;
+    }
+  };
+
+  // pass 1: query blocks and KV blocks in all
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    int ctx, qlen;
+    chunk(b, ctx, qlen);
+    const int nq = (qlen * G + kRows - 1) / kRows;
+    unsigned long long blocks = 0;
+    for (int qb = 0; qb < nq; ++qb) blocks += qblock_blocks(ctx, qlen, G, qb);
+    if (nq) {
+      atomicAdd(&s_qblocks, nq);
+      atomicAdd(&s_blocks, blocks);
+    }
+  }
+  __syncthreads();
+  // Split size: none while the query blocks alone give every CTA two items;
+  // otherwise aim at three items per CTA, never below kMinSplitBlocks, and
+  // double it until the split units fit the workspace's partial results.
+  if (tid == 0 && s_qblocks > p.units_cap - p.partial_cap) {
+    // inconsistent query_start (overlapping chunks): more query blocks than
+    // total_q can give; refuse the whole batch
+    dev::flag_status(p.status, kStatusBounds);
+    s_qblocks = 0;
+  }
+  __syncthreads();
+  if (s_qblocks == 0) {
+    if (tid == 0) {
+      p.header[kHdrTotal] = 0;
+      p.header[kHdrNext] = 0;
+      p.header[kHdrDone] = 0;
+      p.header[kHdrSignature] = p.signature;
+    }
+    return;
+  }
+  if (tid == 0) {
+    const long long items = (long long)s_qblocks * p.num_kv_heads;
+    int split = 0;
+    if (items < 2ll * p.ncta && s_qblocks > 0) {
+      const long long want = (long long)s_blocks * p.num_kv_heads / (3ll * p.ncta) + 1;
+      split = int(std::max<long long>(kMinSplitBlocks, want));
+    }
+    s_split = split;
+  }
+  __syncthreads();
+  for (int round = 0; round < 24 && s_split > 0; ++round) {
+    if (tid == 0) s_split_units = 0;
+    __syncthreads();
+    const int split = s_split;
+    for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+      int ctx, qlen;
+      chunk(b, ctx, qlen);
+      const int nq = (qlen * G + kRows - 1) / kRows;
+      int units = 0;
+      for (int qb = 0; qb < nq; ++qb) {
+        const int ns = (qblock_blocks(ctx, qlen, G, qb) + split - 1) / split;
+        if (ns > 1) units += ns;
+      }
+      if (units) atomicAdd(&s_split_units, units);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      if (s_split_units > p.partial_cap) s_split = s_split > (1 << 24) ? 0 : s_split * 2;
+      else s_split = -s_split;  // fits: stop (sign marks "done")
+    }
+    __syncthreads();
+    if (s_split <= 0) break;
+  }
+  __syncthreads();
+  const int split = s_split < 0 ? -s_split : 0;  // 0: no splitting
+
+  // pass 2: sizes of the units (a query block's splits are balanced)
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    int ctx, qlen;
+    chunk(b, ctx, qlen);
+    const int nq = (qlen * G + kRows - 1) / kRows;
+    for (int qb = 0; qb < nq; ++qb) {
+      const int nb = qblock_blocks(ctx, qlen, G, qb);
+      const int ns = split ? (nb + split - 1) / split : 1;
+      const int base = nb / ns, big = nb - base * ns;
+      if (big) atomicAdd(&hist[size_bucket(base + 1)], big);
+      if (ns - big) atomicAdd(&hist[size_bucket(base)], ns - big);
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int pos = 0;
+    for (int r = kSizeBuckets - 1; r >= 0; --r) {
+      bucket[r] = pos;
+      pos += hist[r];
+    }
+    p.header[kHdrTotal] = pos * p.num_kv_heads;
+    p.header[kHdrNext] = 0;
+    p.header[kHdrDone] = 0;
+    p.header[kHdrSignature] = p.signature;
+  }
+  __syncthreads();
+  // pass 3: place the units, claim partial slots and arrival counters for
+  // the split ones.  Unit = {b, qb, first block, blocks} {split << 16 | nsplit,
+  // first partial slot, arrival group, ctx}.
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    int ctx, qlen;
+    chunk(b, ctx, qlen);
+    const int nq = (qlen * G + kRows - 1) / kRows;
+    for (int qb = 0; qb < nq; ++qb) {
+      const int nb = qblock_blocks(ctx, qlen, G, qb);
+      const int ns = split ? (nb + split - 1) / split : 1;
+      const int base = nb / ns, big = nb - base * ns;
+      int slot = -1, grp = -1;
+      if (ns > 1) {
+        slot = atomicAdd(&s_slot, ns);
+        grp = atomicAdd(&s_group, 1);
+        for (int g = 0; g < p.num_kv_heads; ++g) p.arrivals[size_t(grp) * p.num_kv_heads + g] = 0;
+      }
+      int first = 0;
+      for (int s = 0; s < ns; ++s) {
+        const int n = s < big ? base + 1 : base;
+        const int pos = atomicAdd(&bucket[size_bucket(n)], 1);
+        p.units[2 * pos] = make_int4(b, qb, first, n);
+        p.units[2 * pos + 1] = make_int4((s << 16) | ns, slot, grp, ctx);
+        first += n;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------- tensor-core path
+template <int D>
+struct Smem {
+  static constexpr int kTileBytes = kBlockSize * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr size_t kBytes =
+      1024 /* alignment slack */ + size_t(kStages) * kStageBytes + 2 * kStages * 8 + 64;
+};
+
+// One work item as every thread of the CTA holds it.
+struct Item {
+  int b, qb, first, nblk, s, ns, slot, grp, ctx, g;
+  int q_first, qlen;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  using S = Smem<D>;
+  using M = dev::Mma<T>;
+  constexpr int KT = D / 16;      // 16-wide steps along head_dim
+  constexpr int ND = D / 8;       // 8-wide output column tiles
+  constexpr int HALVES = D / 64;  // 128-byte TMA boxes per tile row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + size_t(kStages) * S::kStageBytes);
+  uint64_t* empty = full + kStages;
+  int* s_claim = reinterpret_cast<int*>(empty + kStages);
+  int* s_last = s_claim + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row group / column pair
+  const bool producer = threadIdx.x == 0;
+  if (producer) {
+    for (int i = 0; i < kStages; ++i) {
+      dev::mbar_init(&full[i], 1);
+      dev::mbar_init(&empty[i], kWarps);
+    }
+    dev::mbar_fence_init();
+    dev::prefetch_tensormap(&tmap_k);
+    dev::prefetch_tensormap(&tmap_v);
+  }
+  __syncthreads();
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();
+
+  const unsigned long long tmo = p.timeout_ns;
+  const int G = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
+  if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+  const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
+  const uint64_t policy = dev::l2_policy_evict_first();
+  int kc = 0;  // blocks consumed by this warp so far (same for every warp)
+  int ik = 0;  // blocks issued so far (producer only)
+  bool ok = true;
+
+  // Issues block k (the item's block j) into the ring, once the stage's
+  // previous block has been released by every warp.
+  auto issue = [&](const Item& it, int j, int k) -> bool {
+    const int st = k % kStages;
+    if (k >= kStages && !dev::mbar_wait_bounded(&empty[st], ((k / kStages) - 1) & 1, tmo, p.status))
+      return false;
+    int phys = p.block_tables[size_t(it.b) * p.max_blocks + it.first + j];
+    if (phys < 0 || phys >= p.num_blocks) {
+      dev::flag_status(p.status, kStatusBounds);
+      phys = 0;
+    }
+    dev::mbar_arrive_expect_tx(&full[st], S::kStageBytes);
+    uint8_t* dst = ring + size_t(st) * S::kStageBytes;
+    const int y = (phys * Hkv + it.g) * kBlockSize;
+#pragma unroll
+    for (int h = 0; h < HALVES; ++h) {
+      dev::tma_load_2d(dst + h * 2048, &tmap_k, h * 64, y, &full[st], policy);
+      dev::tma_load_2d(dst + S::kTileBytes + h * 2048, &tmap_v, h * 64, y, &full[st], policy);
+    }
+    return true;
+  };
+
+  bool first_claim = true;
+  for (;;) {
+    if (producer) {
+      // the first item of every CTA is dealt statically, the rest come from
+      // the counter
+      *s_claim = first_claim ? int(blockIdx.x)
+                             : int(gridDim.x) + atomicAdd(&p.header[kHdrNext], 1);
+    }
+    first_claim = false;
+    __syncthreads();
+    const int x = *s_claim;
+    __syncthreads();
+    if (x >= total) break;
+    Item it;
+    {
+      const int4 u0 = p.units[2 * (x / Hkv)], u1 = p.units[2 * (x / Hkv) + 1];
+      it.g = x % Hkv;
+      it.b = u0.x;
+      it.qb = u0.y;
+      it.first = u0.z;
+      it.nblk = u0.w;
+      it.s = u1.x >> 16;
+      it.ns = u1.x & 0xffff;
+      it.slot = u1.y;
+      it.grp = u1.z;
+      it.ctx = u1.w;
+      it.q_first = p.query_start[it.b];
+      it.qlen = p.query_start[it.b + 1] - it.q_first;
+    }
+    // the ring's first blocks of this item
+    if (producer) {
+      for (int j = 0; j < it.nblk && j < kStages; ++j, ++ik)
+        if (!issue(it, j, ik)) ok = false;
+    }
+
+    // ---- this warp's 16 query rows: ra = gq, rb = gq + 8 (of the warp's 16)
+    const int row0 = it.qb * kRows + warp * 16;  // first row among (b, g)'s T * G rows
+    const int nrows = it.qlen * G;
+    const int ra = row0 + gq, rb = ra + 8;
+    const bool va = ra < nrows, vb = rb < nrows;
+    const int pos_a = va ? it.ctx - it.qlen + ra / G : -1;
+    const int pos_b = vb ? it.ctx - it.qlen + rb / G : -1;
+    const T* qa = static_cast<const T*>(p.q) +
+                  (size_t(it.q_first + (va ? ra / G : 0)) * Hq + it.g * G + (va ? ra % G : 0)) * D;
+    const T* qbp = static_cast<const T*>(p.q) +
+                   (size_t(it.q_first + (vb ? rb / G : 0)) * Hq + it.g * G + (vb ? rb % G : 0)) * D;
+    uint32_t qf[KT][4];
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      const int c = 16 * kk + 2 * tq;
+      qf[kk][0] = va ? *reinterpret_cast<const uint32_t*>(qa + c) : 0u;
+      qf[kk][1] = vb ? *reinterpret_cast<const uint32_t*>(qbp + c) : 0u;
+      qf[kk][2] = va ? *reinterpret_cast<const uint32_t*>(qa + c + 8) : 0u;
+      qf[kk][3] = vb ? *reinterpret_cast<const uint32_t*>(qbp + c + 8) : 0u;
+    }
+    float o[ND][4];
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
+    const float sl2 = p.scale_log2;
+
+    for (int j = 0; j < it.nblk; ++j, ++kc) {
+      const int st = kc % kStages;
+      if (!dev::mbar_wait_bounded(&full[st], (kc / kStages) & 1, tmo, p.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t kt = dev::smem_u32(ring + size_t(st) * S::kStageBytes);
+      const uint32_t vt = kt + S::kTileBytes;
+      const int t0 = (it.first + j) * kBlockSize;  // first token of the block
+      // ---- S = Q K^T: 16 rows x 16 tokens (two 8-token column tiles)
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3;
+        const int tok = ((mi >> 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+          const int gc = 2 * kk + (mi & 1);
+          const uint32_t addr =
+              kt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
+          uint32_t b0, b1, b2, b3;
+          dev::ldmatrix_x4(addr, b0, b1, b2, b3);
+          M::run(s0, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+          M::run(s1, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+        }
+      }
+      // ---- causal / context mask, base-2 scores
+      const int c0 = t0 + 2 * tq, c1 = c0 + 8;  // tokens of s0[0], s1[0]
+      float xa[4], xb[4];
+      xa[0] = c0 <= pos_a ? s0[0] * sl2 : -INFINITY;
+      xa[1] = c0 + 1 <= pos_a ? s0[1] * sl2 : -INFINITY;
+      xa[2] = c1 <= pos_a ? s1[0] * sl2 : -INFINITY;
+      xa[3] = c1 + 1 <= pos_a ? s1[1] * sl2 : -INFINITY;
+      xb[0] = c0 <= pos_b ? s0[2] * sl2 : -INFINITY;
+      xb[1] = c0 + 1 <= pos_b ? s0[3] * sl2 : -INFINITY;
+      xb[2] = c1 <= pos_b ? s1[2] * sl2 : -INFINITY;
+      xb[3] = c1 + 1 <= pos_b ? s1[3] * sl2 : -INFINITY;
+      float bma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+      float bmb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+      bma = fmaxf(bma, __shfl_xor_sync(0xffffffffu, bma, 1));
+      bma = fmaxf(bma, __shfl_xor_sync(0xffffffffu, bma, 2));
+      bmb = fmaxf(bmb, __shfl_xor_sync(0xffffffffu, bmb, 1));
+      bmb = fmaxf(bmb, __shfl_xor_sync(0xffffffffu, bmb, 2));
+      const float mna = fmaxf(ma, bma), mnb = fmaxf(mb, bmb);
+      // a row with nothing unmasked yet keeps m = -inf: use 0 as its reference
+      const float ra0 = mna == -INFINITY ? 0.f : mna, rb0 = mnb == -INFINITY ? 0.f : mnb;
+      const float ala = dev::fast_exp2(ma - ra0), alb = dev::fast_exp2(mb - rb0);
+      ma = mna;
+      mb = mnb;
+      const uint32_t pa01 = M::pack(dev::fast_exp2(xa[0] - ra0), dev::fast_exp2(xa[1] - ra0));
+      const uint32_t pb01 = M::pack(dev::fast_exp2(xb[0] - rb0), dev::fast_exp2(xb[1] - rb0));
+      const uint32_t pa23 = M::pack(dev::fast_exp2(xa[2] - ra0), dev::fast_exp2(xa[3] - ra0));
+      const uint32_t pb23 = M::pack(dev::fast_exp2(xb[2] - rb0), dev::fast_exp2(xb[3] - rb0));
+      {
+        const float2 f0 = M::unpack(pa01), f1 = M::unpack(pa23);
+        const float2 g0 = M::unpack(pb01), g1 = M::unpack(pb23);
+        la = la * ala + (f0.x + f0.y + f1.x + f1.y);
+        lb = lb * alb + (g0.x + g0.y + g1.x + g1.y);
+      }
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        o[nd][0] *= ala;
+        o[nd][1] *= ala;
+        o[nd][2] *= alb;
+        o[nd][3] *= alb;
+      }
+      // ---- O += P V: P (16 rows x 16 tokens) is the A operand as computed
+      {
+        const int mi = lane >> 3;
+        const int tok = ((mi & 1) << 3) + (lane & 7);
+#pragma unroll
+        for (int nd = 0; nd < ND; nd += 2) {
+          const int gc = nd + (mi >> 1);  // 16-byte chunk = 8 columns
+          const uint32_t addr =
+              vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
+          uint32_t b0, b1, b2, b3;
+          dev::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+          M::run(o[nd], pa01, pb01, pa23, pb23, b0, b1);
+          M::run(o[nd + 1], pa01, pb01, pa23, pb23, b2, b3);
+        }
+      }
+      // the stage is read: order those reads before the copy that reuses it
+      dev::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&empty[st]);
+      if (producer && j + kStages < it.nblk) {
+        if (!issue(it, j + kStages, ik)) ok = false;
+        ++ik;
+      }
+    }
+    // every thread agrees before anyone leaves the loop (no one may be left
+    // waiting at a CTA barrier)
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+
+    // ---- end of the item: row sums across the quad, then out or partials
+    la += __shfl_xor_sync(0xffffffffu, la, 1);
+    la += __shfl_xor_sync(0xffffffffu, la, 2);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+    lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+    const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
+    if (it.ns == 1) {
+      T* oa = static_cast<T*>(p.out) +
+              (size_t(it.q_first + (va ? ra / G : 0)) * Hq + it.g * G + (va ? ra % G : 0)) * D;
+      T* ob = static_cast<T*>(p.out) +
+              (size_t(it.q_first + (vb ? rb / G : 0)) * Hq + it.g * G + (vb ? rb % G : 0)) * D;
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int c = nd * 8 + 2 * tq;
+        if (va) *reinterpret_cast<uint32_t*>(oa + c) = M::pack(o[nd][0] * ia, o[nd][1] * ia);
+        if (vb) *reinterpret_cast<uint32_t*>(ob + c) = M::pack(o[nd][2] * ib, o[nd][3] * ib);
+      }
+    } else {
+      const size_t base = (size_t(it.slot + it.s) * Hkv + it.g) * kRows + warp * 16;
+      float* pa = p.part_o + (base + gq) * D;
+      float* pb = p.part_o + (base + gq + 8) * D;
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int c = nd * 8 + 2 * tq;
+        *reinterpret_cast<float2*>(pa + c) = make_float2(o[nd][0] * ia, o[nd][1] * ia);
+        *reinterpret_cast<float2*>(pb + c) = make_float2(o[nd][2] * ib, o[nd][3] * ib);
+      }
+      if (tq == 0) {
+        p.part_lse[base + gq] = la > 0.f ? ma + log2f(la) : -INFINITY;
+        p.part_lse[base + gq + 8] = lb > 0.f ? mb + log2f(lb) : -INFINITY;
+      }
+      // publish (every warp's rows), count; the CTA completing (group, g) merges
+      __syncthreads();
+      if (producer)
+        *s_last = dev::atom_add_acq_rel_gpu(&p.arrivals[size_t(it.grp) * Hkv + it.g], 1) ==
+                  it.ns - 1;
+      __syncthreads();
+      if (*s_last) {
+        // each warp merges its own 16 rows; lane l owns columns 4l .. 4l + 3
+        for (int r = 0; r < 16; ++r) {
+          const int row = row0 + r;
+          if (row >= nrows) break;
+          if (4 * lane < D) {
+            float mrun = -INFINITY, lrun = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < it.ns; ++sp) {
+              const size_t rr = (size_t(it.slot + sp) * Hkv + it.g) * kRows + warp * 16 + r;
+              const float lse = __ldcg(&p.part_lse[rr]);
+              if (lse == -INFINITY) continue;
+              const float4 ov = __ldcg(reinterpret_cast<const float4*>(&p.part_o[rr * D + 4 * lane]));
+              const float mn = fmaxf(mrun, lse);
+              const float a = mrun == -INFINITY ? 0.f : dev::fast_exp2(mrun - mn);
+              const float w = dev::fast_exp2(lse - mn);
+              acc.x = acc.x * a + w * ov.x;
+              acc.y = acc.y * a + w * ov.y;
+              acc.z = acc.z * a + w * ov.z;
+              acc.w = acc.w * a + w * ov.w;
+              lrun = lrun * a + w;
+              mrun = mn;
+            }
+            const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
+            T* orow = static_cast<T*>(p.out) +
+                      (size_t(it.q_first + row / G) * Hq + it.g * G + row % G) * D + 4 * lane;
+            uint2 pk;
+            pk.x = M::pack(acc.x * inv, acc.y * inv);
+            pk.y = M::pack(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2*>(orow) = pk;
+          }
+        }
+        if (producer) p.arrivals[size_t(it.grp) * Hkv + it.g] = 0;  // ready for the next run
+      }
+    }
+  }
+  if (!ok) {
+    // a wait ran out: let this CTA's copies in flight land, then give up
+    if (producer)
+      for (int k = kc; k < ik; ++k)
+        dev::mbar_wait_bounded(&full[k % kStages], (k / kStages) & 1, tmo, p.status);
+    return;
+  }
+  // the last CTA to finish returns the counters to zero
+  __syncthreads();
+  if (producer && planned) {
+    __threadfence();
+    if (atomicAdd(&p.header[kHdrDone], 1) == int(gridDim.x) - 1) {
+      atomicExch(&p.header[kHdrNext], 0);
+      atomicExch(&p.header[kHdrDone], 0);
+    }
+  }
+}
+
+// --------------------------------------------------------------- fp32 path
+// One warp per (query row, query head): a decode over the row's causal prefix.
+template <int D>
+__global__ void __launch_bounds__(128) prefill_f32_kernel(const Params p) {
+  constexpr int E = D / 32;
+  const long long unit = (long long)blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (unit >= (long long)p.total_q * p.num_q_heads) return;
+  const int row = int(unit / p.num_q_heads), h = int(unit % p.num_q_heads);
+  // the sequence of this row: query_start is sorted, binary search
+  int lo = 0, hi = p.num_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.query_start[mid] <= row) lo = mid;
+    else hi = mid - 1;
+  }
+  const int b = lo;
+  if (row < p.query_start[b] || row >= p.query_start[b + 1]) return;  // no sequence's row
+  const int qlen = p.query_start[b + 1] - p.query_start[b];
+  const int ctx = p.context_lens[b];
+  const int cap = p.max_blocks * kBlockSize;
+  if (ctx < 0 || ctx > cap || qlen > ctx) {
+    if (lane == 0) dev::flag_status(p.status, kStatusBounds);
+    return;
+  }
+  const int pos = ctx - qlen + (row - p.query_start[b]);
+  const int g = h / p.group;
+  const float* qv = static_cast<const float*>(p.q) + (size_t(row) * p.num_q_heads + h) * D + lane * E;
+  const float* k_cache = static_cast<const float*>(p.k_cache);
+  const float* v_cache = static_cast<const float*>(p.v_cache);
+  const int32_t* table = p.block_tables + size_t(b) * p.max_blocks;
+  float qr[E], acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    qr[e] = qv[e];
+    acc[e] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int t = 0; t <= pos; ++t) {
+    int phys = table[t / kBlockSize];
+    if (phys < 0 || phys >= p.num_blocks) {
+      if (lane == 0) dev::flag_status(p.status, kStatusBounds);
+      phys = 0;
+    }
+    const size_t r = ((size_t(phys) * p.num_kv_heads + g) * kBlockSize + t % kBlockSize) * D + lane * E;
+    float dot = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dot = fmaf(qr[e], k_cache[r + e], dot);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    const float sc = dot * p.scale;
+    const float mn = fmaxf(m, sc);
+    const float a = expf(m - mn), pw = expf(sc - mn);
+    l = l * a + pw;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = acc[e] * a + pw * v_cache[r + e];
+    m = mn;
+  }
+  float* out = static_cast<float*>(p.out) + (size_t(row) * p.num_q_heads + h) * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) out[e] = acc[e] / l;
+}
+
+}  // namespace prefill
+}  // namespace pa
+
+// ====================================================================== host
+namespace pa {
+namespace prefill {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int error = 0;
+  int sms = 0;
+  int ctas_per_sm[2][2] = {{0, 0}, {0, 0}};  // [bf16?][head_dim 128?]
+};
+DeviceState g_dev[kMaxDevices];
+
+template <typename T, int D>
+cudaError_t configure(int* ctas_per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       int(Smem<D>::kBytes));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, prefill_kernel<T, D>,
+                                                       kWarps * 32, Smem<D>::kBytes);
+}
+
+int device_setup(int device) {
+  DeviceState& st = g_dev[device];
+  std::call_once(st.once, [&] {
+    if (cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+      st.error = PA_ERR_CUDA;
+      return;
+    }
+    cudaError_t e = configure<__nv_bfloat16, 128>(&st.ctas_per_sm[1][1]);
+    if (e == cudaSuccess) e = configure<__nv_bfloat16, 64>(&st.ctas_per_sm[1][0]);
+    if (e == cudaSuccess) e = configure<__half, 128>(&st.ctas_per_sm[0][1]);
+    if (e == cudaSuccess) e = configure<__half, 64>(&st.ctas_per_sm[0][0]);
+    st.error = e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    for (int a = 0; a < 2; ++a)
+      for (int d = 0; d < 2; ++d)
+        if (st.error == PA_OK && st.ctas_per_sm[a][d] < 1) st.error = PA_ERR_UNSUPPORTED;
+  });
+  if (st.error != PA_OK) return fail(st.error, "prefill: per-device set-up failed on device %d", device);
+  return PA_OK;
+}
+
+int check_shapes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                 int max_blocks_per_seq, int dtype, const char* who) {
+  if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
+    return fail(PA_ERR_UNSUPPORTED, "%s: unknown dtype %d", who, dtype);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "%s: head_dim %d (64 or 128)", who, head_dim);
+  if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      max_blocks_per_seq <= 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: sizes must be positive", who);
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: num_q_heads %% num_kv_heads != 0", who);
+  if (num_q_heads / num_kv_heads > kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "%s: %d query heads per KV head (max %d)", who,
+                num_q_heads / num_kv_heads, kMaxGroup);
+  if (double(max_blocks_per_seq) * kBlockSize >= 2147483647.0 ||
+      double(total_q) * num_q_heads >= 2147483647.0)
+    return fail(PA_ERR_INVALID_ARG, "%s: sizes too large", who);
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace prefill
+}  // namespace pa
+
+using namespace pa;
+using namespace pa::prefill;
+
+extern "C" {
+
+PA_API int pa_paged_attention_prefill_workspace_size(int num_seqs, int total_q, int num_q_heads,
+                                                     int num_kv_heads, int head_dim,
+                                                     size_t* bytes) {
+  if (!bytes) return fail(PA_ERR_INVALID_ARG, "prefill_workspace_size: bytes is NULL");
+  if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "prefill_workspace_size: bad sizes");
+  *bytes = workspace_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim).total;
+  return PA_OK;
+}
+
+PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      const int32_t* query_start, int num_seqs, int total_q,
+                                      int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int num_blocks, float scale,
+                                      int dtype, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_prefill";
+  int rc = check_shapes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
+                        max_blocks_per_seq, dtype, who);
+  if (rc != PA_OK) return rc;
+  if (num_seqs == 0 || total_q == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) != 0; };
+  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+    return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
+  if (num_blocks <= 0 || double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
+    return fail(PA_ERR_INVALID_ARG, "%s: bad num_blocks", who);
+  const Layout lay = workspace_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace must be non-NULL and 256-byte aligned", who);
+  if (workspace_bytes < lay.total)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace %zu bytes < %zu needed", who, workspace_bytes,
+                lay.total);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
+  rc = device_setup(device);
+  if (rc != PA_OK) return rc;
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  Params prm = {};
+  prm.q = q;
+  prm.k_cache = k_cache;
+  prm.v_cache = v_cache;
+  prm.out = out;
+  prm.block_tables = block_tables;
+  prm.context_lens = context_lens;
+  prm.query_start = query_start;
+  prm.num_seqs = num_seqs;
+  prm.total_q = total_q;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.head_dim = head_dim;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_blocks = num_blocks;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.status = status;
+  prm.timeout_ns = 1000000000ull;
+
+  if (dtype == PA_F32) {
+    const long long units = (long long)total_q * num_q_heads;
+    const int blocks = int((units + 3) / 4);
+    if (head_dim == 64)
+      prefill_f32_kernel<64><<<blocks, 128, 0, s>>>(prm);
+    else
+      prefill_f32_kernel<128><<<blocks, 128, 0, s>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s (fp32): launch failed: %s", who, cudaGetErrorString(e));
+    return PA_OK;
+  }
+
+  const DeviceState& st = g_dev[device];
+  const bool bf16 = dtype == PA_BF16;
+  const int per_sm = st.ctas_per_sm[bf16][head_dim == 128];
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  prm.ncta = st.sms * per_sm;
+  prm.units_cap = lay.units_cap;
+  prm.partial_cap = lay.partial_cap;
+  prm.signature = signature_of(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
+                               max_blocks_per_seq);
+  prm.header = reinterpret_cast<int*>(ws + lay.header);
+  prm.units = reinterpret_cast<int4*>(ws + lay.units);
+  prm.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
+  prm.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  prm.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t pc = {};
+  pc.gridDim = dim3(1);
+  pc.blockDim = dim3(kPlanThreads);
+  pc.stream = s;
+  pc.attrs = attr;
+  pc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_plan_kernel, prm);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
+
+  alignas(64) CUtensorMap mk, mv;
+  rc = cache_tensor_map(&mk, k_cache, bf16, num_blocks, num_kv_heads, head_dim);
+  if (rc == PA_OK) rc = cache_tensor_map(&mv, v_cache, bf16, num_blocks, num_kv_heads, head_dim);
+  if (rc != PA_OK) return rc;
+  cudaLaunchConfig_t kc = {};
+  kc.gridDim = dim3(prm.ncta);
+  kc.blockDim = dim3(kWarps * 32);
+  kc.stream = s;
+  kc.attrs = attr;
+  kc.numAttrs = 1;
+  if (head_dim == 128) {
+    kc.dynamicSmemBytes = Smem<128>::kBytes;
+    e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 128>, mk, mv, prm)
+             : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 128>, mk, mv, prm);
+  } else {
+    kc.dynamicSmemBytes = Smem<64>::kBytes;
+    e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 64>, mk, mv, prm)
+             : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 64>, mk, mv, prm);
+  }
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
+}
+
+}  // extern "C"

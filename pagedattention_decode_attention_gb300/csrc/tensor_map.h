@@ -1,0 +1,19 @@
+// TMA tensor maps over a paged K or V cache, shared by the attention kernels.
+#pragma once
+
+#include <cuda.h>
+
+namespace pa {
+
+// Encodes (or takes from a per-thread cache) the 2-D tensor map of one cache
+// `[num_blocks][num_kv_heads][16][head_dim]` of 16-bit elements: rows =
+// num_blocks * num_kv_heads * 16 token rows of head_dim elements, one copy
+// box = 16 rows x 64 elements (128 bytes wide, 128-byte swizzle), so a
+// (block, head) tile is head_dim / 64 boxes.  In shared memory box h of a
+// tile sits at h * 2048, row r at r * 128, its 16-byte chunks XOR-swizzled by
+// r % 8.  A decode or prefill step reuses the same layer caches every step and
+// encoding is a host-side driver call, hence the cache.  Returns a pa_status.
+int cache_tensor_map(CUtensorMap* out, const void* cache, bool bf16, int num_blocks,
+                     int num_kv_heads, int head_dim);
+
+}  // namespace pa

@@ -268,6 +268,63 @@ def prepare_decode_append_run(q, k_new, v_new, slot_mapping, k_cache, v_cache, b
                      workspace, out))
 
 
+def prefill_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,
+                           head_dim: int) -> int:
+    n = C.c_size_t(0)
+    capi.check(capi.lib().pa_paged_attention_prefill_workspace_size(
+        num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, C.byref(n)))
+    return n.value
+
+
+def alloc_prefill_workspace(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
+                            device) -> torch.Tensor:
+    n = prefill_workspace_size(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            query_start: torch.Tensor, scale: float,
+                            out: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Chunked-prefill attention: the query rows ``query_start[b] ..
+    query_start[b+1]-1`` of ``q`` (``[total_q, Hq, d]``) are the newest tokens
+    of sequence ``b`` (K/V already in the cache); each attends causally over
+    the sequence's tokens up to itself."""
+    dev = q.device
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens),
+                    ("query_start", query_start)):
+        _cuda_contig(name, t, dev)
+    _require(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32
+             and query_start.dtype == torch.int32,
+             "block_tables, context_lens and query_start must be int32")
+    _require(q.dtype == k_cache.dtype == v_cache.dtype, "q and caches must share a dtype")
+    _require(k_cache.dim() == 4 and k_cache.shape == v_cache.shape and k_cache.shape[2] == 16,
+             "caches must be [num_blocks, num_kv_heads, 16, head_dim]")
+    nb, hkv, _, d = k_cache.shape
+    _require(q.dim() == 3 and q.shape[2] == d, "q must be [total_q, num_q_heads, head_dim]")
+    total_q, hq, _ = q.shape
+    b = context_lens.shape[0]
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == b,
+             "block_tables must be [num_seqs, max_blocks_per_seq]")
+    _require(query_start.shape == (b + 1,), "query_start must be [num_seqs + 1]")
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        workspace = alloc_prefill_workspace(b, total_q, hq, hkv, d, dev)
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_prefill(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), query_start.data_ptr(), b, total_q, hq, hkv, d,
+        block_tables.shape[1], nb, float(scale), _dtype_code(q), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(dev, stream)))
+    return out
+
+
 def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:
     """Copy whole blocks ``src -> dst`` (int64 ``[P, 2]`` on the device) in every
     layer's caches."""
