@@ -57,7 +57,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b"], default="mha_7b")
+    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b", "prefill_8b"], default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -79,7 +79,92 @@ def make_batch(name: str, rank: int) -> wl.DecodeBatch:
     # each rank decodes its own independent batch (replicas; no exchange)
     if name == "mha_7b":
         return wl.mha_7b(seed=wl.SEED_BASE + 2 + 100 * rank)
+    if name == "prefill_8b":
+        return wl.prefill_8b(seed=wl.SEED_BASE + 6 + 100 * rank)
     return wl.gqa_8b(seed=wl.SEED_BASE + 3 + 100 * rank)
+
+
+def prefill_flops(batch: wl.DecodeBatch) -> float:
+    """Flops of one chunked-prefill attention call: every query row (token x
+    query head) does 2 d flops for q.k and 2 d for p.v per attended token, and
+    the query at position p attends p + 1 tokens."""
+    total = 0.0
+    for ctx, qlen in zip(batch.context_lens.astype(np.int64), batch.extra["query_lens"]):
+        first = ctx - int(qlen)
+        attended = int(qlen) * (first + 1) + int(qlen) * (int(qlen) - 1) // 2
+        total += attended
+    return total * 4 * batch.head_dim * batch.num_q_heads
+
+
+def run_prefill_bench(args):
+    """Chunked-prefill attention: each step is one attention call (plan +
+    kernel) over the batch's chunks, rotating over the layer caches."""
+    import pagedattention_decode_attention_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    batch = make_batch("prefill_8b", 0)
+    if args.layers > 0:
+        batch.num_layers = args.layers
+    dt = DTYPES[batch.dtype]
+    hq, hkv, d, nb, L = (batch.num_q_heads, batch.num_kv_heads, batch.head_dim, batch.num_blocks,
+                         batch.num_layers)
+    qlens = batch.extra["query_lens"]
+    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    total_q = int(qs[-1])
+    s0 = batch.seed * 1000
+    kc = [wl.normal((nb, hkv, 16, d), dt, s0 + 4 * i, device) for i in range(L)]
+    vc = [wl.normal((nb, hkv, 16, d), dt, s0 + 4 * i + 1, device) for i in range(L)]
+    q = wl.normal((L, total_q, hq, d), dt, s0 + 7, device)
+    out = torch.empty_like(q)
+    bt = torch.from_numpy(batch.block_tables).to(device)
+    cl = torch.from_numpy(batch.context_lens).to(device)
+    qs_d = torch.from_numpy(qs).to(device)
+    ws = pa.alloc_prefill_workspace(batch.num_seqs, total_q, hq, hkv, d, device)
+
+    def step(i):
+        layer = i % L
+        pa.paged_attention_prefill(q[layer], kc[layer], vc[layer], bt, cl, qs_d, batch.scale,
+                                   out=out[layer], workspace=ws)
+
+    for i in range(max(args.warmup, 3) + L):
+        step(i)
+    torch.cuda.synchronize()
+    pa.check_status()
+    clocks = ClockSampler(device)
+    clocks.start()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for i in range(args.steps):
+        step(i)
+    end.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    pa.check_status()
+    secs = start.elapsed_time(end) / 1e3
+    per_call = secs / args.steps
+    flops = prefill_flops(batch)
+    kv_bytes = int(batch.context_lens.astype(np.int64).sum()) * 2 * hkv * d * ELEM[batch.dtype]
+    peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else 1900.0
+    line = {
+        "metric": "paged chunked-prefill attention query tokens/s per layer, 1 GPU",
+        "value": total_q / per_call, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3) + L, "ms_per_step": per_call * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
+        "data": "synthetic (seeded N(0,1) Q/K/V, seeded lengths and placements)",
+        "config": {"workload": batch.name, "num_seqs": batch.num_seqs,
+                   "num_q_heads": hq, "num_kv_heads": hkv, "head_dim": d, "block_size": 16,
+                   "query_tokens": total_q, "context_tokens": int(batch.context_lens.sum()),
+                   "layers_rotated": L,
+                   "step": "one chunked-prefill attention call (plan + kernel) on one layer"},
+        "roofline": {"bound": "tensor", "achieved": flops / per_call / 1e12, "peak": peak,
+                     "unit": "TFLOP/s", "frac": flops / per_call / 1e12 / peak,
+                     "flops_per_launch": flops, "peak_source": "measured bf16_tflops (burst)",
+                     "kv_read_gbs_unique": kv_bytes / per_call / 1e9},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
 
 
 def algorithmic_bytes(batch: wl.DecodeBatch) -> dict:
@@ -558,9 +643,50 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- reference
+def run_reference_prefill(args):
+    """Reference arm of the chunked-prefill workload: the prefill oracle on a
+    bounded sample of query rows per step, scaled to query tokens/s."""
+    import oracle.attention as oa
+    batch = make_batch("prefill_8b", 0)
+    qlens = batch.extra["query_lens"]
+    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int64)
+    total_q = int(qs[-1])
+    gen = np.random.default_rng(batch.seed)
+    shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
+    kc = gen.standard_normal(shape, dtype=np.float32)
+    vc = gen.standard_normal(shape, dtype=np.float32)
+    q = gen.standard_normal((total_q, batch.num_q_heads, batch.head_dim), dtype=np.float32)
+    rows_per_step = 8
+    order = np.random.default_rng(7).permutation(total_q)
+    for i in range(max(args.warmup, 3)):
+        oa.paged_attention_prefill(q, kc, vc, batch.block_tables, batch.context_lens, qs,
+                                   batch.scale, rows=order[i * rows_per_step:(i + 1) * rows_per_step])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        sel = order[(i * rows_per_step) % total_q:][:rows_per_step]
+        oa.paged_attention_prefill(q, kc, vc, batch.block_tables, batch.context_lens, qs,
+                                   batch.scale, rows=sel)
+    secs = time.perf_counter() - t0
+    value = rows_per_step * args.steps / secs
+    line = {
+        "impl": "reference", "metric": "paged chunked-prefill attention query tokens/s per layer, 1 GPU",
+        "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": batch.name, "num_seqs": batch.num_seqs},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: {rows_per_step} query rows (all heads), float64 numpy, 1 thread"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
+        return
+    if args.workload == "prefill_8b":
+        run_reference_prefill(args)
         return
     batch = make_batch(args.workload, 0)
     per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
@@ -595,6 +721,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "prefill_8b":
+        run_prefill_bench(args)
     else:
         run_ours(args)
 

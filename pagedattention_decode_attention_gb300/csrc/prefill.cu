@@ -302,7 +302,7 @@ struct Item {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     prefill_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v, const Params p) {
   using S = Smem<D>;
@@ -345,26 +345,42 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   int ik = 0;  // blocks issued so far (producer only)
   bool ok = true;
 
+  // Warp 0 issues the ring's copies; its lane l holds table entry tbl_base + l
+  // of the current item (refreshed every 32 blocks), so no copy waits on a
+  // dependent table read.
+  int tbl = 0, tbl_base = -32;
   // Issues block k (the item's block j) into the ring, once the stage's
-  // previous block has been released by every warp.
+  // previous block has been released by every warp.  Called by all of warp 0.
   auto issue = [&](const Item& it, int j, int k) -> bool {
+    if ((j & ~31) != tbl_base) {
+      tbl_base = j & ~31;
+      tbl = tbl_base + lane < it.nblk
+                ? p.block_tables[size_t(it.b) * p.max_blocks + it.first + tbl_base + lane]
+                : 0;
+      if (tbl < 0 || tbl >= p.num_blocks) {
+        dev::flag_status(p.status, kStatusBounds);
+        tbl = 0;
+      }
+    }
+    const int phys = __shfl_sync(0xffffffffu, tbl, j & 31);
     const int st = k % kStages;
-    if (k >= kStages && !dev::mbar_wait_bounded(&empty[st], ((k / kStages) - 1) & 1, tmo, p.status))
-      return false;
-    int phys = p.block_tables[size_t(it.b) * p.max_blocks + it.first + j];
-    if (phys < 0 || phys >= p.num_blocks) {
-      dev::flag_status(p.status, kStatusBounds);
-      phys = 0;
-    }
-    dev::mbar_arrive_expect_tx(&full[st], S::kStageBytes);
-    uint8_t* dst = ring + size_t(st) * S::kStageBytes;
-    const int y = (phys * Hkv + it.g) * kBlockSize;
+    bool ok_ = true;
+    if (lane == 0) {
+      if (k >= kStages &&
+          !dev::mbar_wait_bounded(&empty[st], ((k / kStages) - 1) & 1, tmo, p.status)) {
+        ok_ = false;
+      } else {
+        dev::mbar_arrive_expect_tx(&full[st], S::kStageBytes);
+        uint8_t* dst = ring + size_t(st) * S::kStageBytes;
+        const int y = (phys * Hkv + it.g) * kBlockSize;
 #pragma unroll
-    for (int h = 0; h < HALVES; ++h) {
-      dev::tma_load_2d(dst + h * 2048, &tmap_k, h * 64, y, &full[st], policy);
-      dev::tma_load_2d(dst + S::kTileBytes + h * 2048, &tmap_v, h * 64, y, &full[st], policy);
+        for (int h = 0; h < HALVES; ++h) {
+          dev::tma_load_2d(dst + h * 2048, &tmap_k, h * 64, y, &full[st], policy);
+          dev::tma_load_2d(dst + S::kTileBytes + h * 2048, &tmap_v, h * 64, y, &full[st], policy);
+        }
+      }
     }
-    return true;
+    return __shfl_sync(0xffffffffu, ok_, 0);
   };
 
   bool first_claim = true;
@@ -397,7 +413,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       it.qlen = p.query_start[it.b + 1] - it.q_first;
     }
     // the ring's first blocks of this item
-    if (producer) {
+    tbl_base = -32;
+    if (warp == 0) {
       for (int j = 0; j < it.nblk && j < kStages; ++j, ++ik)
         if (!issue(it, j, ik)) ok = false;
     }
@@ -438,8 +455,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       const uint32_t vt = kt + S::kTileBytes;
       const int t0 = (it.first + j) * kBlockSize;  // first token of the block
       // ---- S = Q K^T: 16 rows x 16 tokens (two 8-token column tiles)
+      // two accumulation chains per column tile (even / odd k-steps) halve
+      // the dependent MMA latency
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
       {
+        float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
         const int mi = lane >> 3;
         const int tok = ((mi >> 1) << 3) + (lane & 7);
 #pragma unroll
@@ -449,8 +469,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
               kt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
           uint32_t b0, b1, b2, b3;
           dev::ldmatrix_x4(addr, b0, b1, b2, b3);
-          M::run(s0, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
-          M::run(s1, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+          M::run(kk & 1 ? e0 : s0, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+          M::run(kk & 1 ? e1 : s1, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          s0[i] += e0[i];
+          s1[i] += e1[i];
         }
       }
       // ---- causal / context mask, base-2 scores
@@ -512,7 +537,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       dev::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(&empty[st]);
-      if (producer && j + kStages < it.nblk) {
+      if (warp == 0 && j + kStages < it.nblk) {
         if (!issue(it, j + kStages, ik)) ok = false;
         ++ik;
       }

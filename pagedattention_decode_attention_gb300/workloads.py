@@ -156,6 +156,23 @@ def gqa_8b(seed: int = SEED_BASE + 3, batch: int = 128, fixed_long: int = 4) -> 
     return DecodeBatch("gqa_8b_bf16", 32, 8, 128, "bf16", lens, tables, nb, seed=seed)
 
 
+def prefill_8b(seed: int = SEED_BASE + 6, batch: int = 16, chunk: int = 512,
+               layers: int = 8) -> DecodeBatch:
+    """Chunked prefill, 8B-shaped GQA (32/8 heads, d=128, bf16): ``batch``
+    sequences, each a ``chunk``-token piece of its prompt on top of a cached
+    prefix log-uniform in [16, 8192] tokens.  ``context_lens`` counts the chunk;
+    ``extra["query_lens"]`` holds the chunk lengths.  ``layers`` separate layer
+    caches."""
+    gen = rng(seed)
+    prefix = log_uniform_lengths(batch, 16, 8192, gen)
+    lens = (prefix + chunk).astype(np.int32)
+    nb = pool_size(lens)
+    tables = disjoint_tables(lens, nb, gen)
+    return DecodeBatch("prefill_8b_bf16", 32, 8, 128, "bf16", lens, tables, nb,
+                       num_layers=layers, seed=seed,
+                       extra={"query_lens": np.full(batch, chunk, dtype=np.int32)})
+
+
 @dataclass
 class SamplingScript:
     """Parallel sampling with copy-on-write: ``prompts`` prompts of
