@@ -57,7 +57,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b", "prefill_8b"], default="mha_7b")
+    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b", "prefill_8b", "swap_8b"],
+                    default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -643,6 +644,71 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- reference
+def run_swap_bench(args):
+    """Block swap (preemption / offload): a batch of 1024 blocks of every one
+    of 32 8B-shaped GQA layers goes to page-locked host memory and back, each
+    direction one launch.  The roofline is a plain pinned copy of the same
+    bytes in the same direction, measured in the same run."""
+    import pagedattention_decode_attention_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    layers = args.layers if args.layers > 0 else 32
+    nb, nblk, hkv, d, dt = 2048, 1024, 8, 128, torch.bfloat16
+    gen = np.random.default_rng(wl.SEED_BASE + 7)
+    dk = [wl.normal((nb, hkv, 16, d), dt, 4000 + 2 * i, device) for i in range(layers)]
+    dv = [wl.normal((nb, hkv, 16, d), dt, 4001 + 2 * i, device) for i in range(layers)]
+    hk = [torch.empty((nblk, hkv, 16, d), dtype=dt).pin_memory() for _ in range(layers)]
+    hv = [torch.empty((nblk, hkv, 16, d), dtype=dt).pin_memory() for _ in range(layers)]
+    out_pairs = torch.from_numpy(np.stack([gen.choice(nb, nblk, replace=False),
+                                           gen.permutation(nblk)], 1)).to(device)
+    in_pairs = torch.from_numpy(np.stack([gen.permutation(nblk),
+                                          gen.choice(nb, nblk, replace=False)], 1)).to(device)
+    block_bytes = 2 * hkv * 16 * d * 2                     # K + V of one block of one layer
+    moved = block_bytes * nblk * layers                    # payload of one direction
+    flat_dev = torch.empty(moved // 2, dtype=dt, device=device)
+    flat_host = torch.empty(moved // 2, dtype=dt).pin_memory()
+
+    def timed(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / reps
+
+    reps = max(args.steps, 3)
+    clocks = ClockSampler(device)
+    clocks.start()
+    t_out = timed(lambda: pa.block_swap(dk, dv, hk, hv, out_pairs, pa.PA_SWAP_OUT), reps)
+    t_in = timed(lambda: pa.block_swap(dk, dv, hk, hv, in_pairs, pa.PA_SWAP_IN), reps)
+    t_d2h = timed(lambda: flat_host.copy_(flat_dev, non_blocking=True), reps)
+    t_h2d = timed(lambda: flat_dev.copy_(flat_host, non_blocking=True), reps)
+    clk = clocks.stop()
+    pa.check_status()
+    gbs = lambda t: moved / t / 1e9  # noqa: E731
+    line = {
+        "metric": "paged KV block swap tokens/s (device <-> page-locked host), 1 GPU",
+        "value": nblk * 16 * 2 / (t_out + t_in), "unit": "tokens/s (out + in, all layers)",
+        "n_gpus": 1, "steps": reps, "warmup": 1, "ms_per_step": (t_out + t_in) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) caches, random block placement)",
+        "config": {"workload": "swap_8b_bf16", "layers": layers, "blocks_per_swap": nblk,
+                   "num_kv_heads": hkv, "head_dim": d, "block_size": 16,
+                   "bytes_per_direction": moved,
+                   "step": "pa_block_swap out (1024 blocks x all layers), then back in"},
+        "roofline": {"bound": "link", "unit": "GB/s",
+                     "out": {"achieved": gbs(t_out), "peak": gbs(t_d2h), "frac": t_d2h / t_out},
+                     "in": {"achieved": gbs(t_in), "peak": gbs(t_h2d), "frac": t_h2d / t_in},
+                     "peak_source": "pinned cudaMemcpyAsync of the same bytes, same run"},
+        "gpu_launches": 2 * reps,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def run_reference_prefill(args):
     """Reference arm of the chunked-prefill workload: the prefill oracle on a
     bounded sample of query rows per step, scaled to query tokens/s."""
@@ -723,6 +789,8 @@ def main():
         run_reference(args)
     elif args.workload == "prefill_8b":
         run_prefill_bench(args)
+    elif args.workload == "swap_8b":
+        run_swap_bench(args)
     else:
         run_ours(args)
 

@@ -299,6 +299,35 @@ PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_l
                          int head_dim, int num_blocks, int dtype, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_block_swap -- copy whole blocks between the device caches and caches in
+ * page-locked host memory, every layer, in one launch.
+ *
+ * "vLLM: treating the KV cache as virtual memory", section
+ * 调度：词一级的进入与退出 (a preempted sequence's KV is offloaded to host
+ * memory and loaded back later, block by block) and "第 6 章 缓存管理",
+ * section 缓存放不下的时候 (spill cold cache to CPU memory; a CPU with a fast
+ * link to the GPU reaches hundreds of GB/s).
+ *
+ * direction PA_SWAP_OUT: pairs[i] = (device block, host block) and
+ *   host_k[l][host block] = dev_k[l][device block] (likewise v) for every l;
+ * direction PA_SWAP_IN: pairs[i] = (host block, device block), the reverse.
+ * These are the pairs pa_pool_swap_out / pa_pool_swap_in produce (copied to
+ * the device).  Host caches are [num_host_blocks][num_kv_heads][16][head_dim]
+ * per layer in page-locked host memory (cudaHostAlloc / cudaHostRegister;
+ * anything else is PA_ERR_INVALID_ARG); dev/host cache pointer arrays are
+ * host arrays of num_layers (<= 256) pointers; pairs is device memory.
+ * Bit-exact.  A block id out of range skips the pair and sets
+ * PA_ERR_DEVICE_BOUNDS.  Destinations must be distinct.
+ * ---------------------------------------------------------------------- */
+#define PA_SWAP_OUT 0
+#define PA_SWAP_IN 1
+PA_API int pa_block_swap(void* const* dev_k_caches, void* const* dev_v_caches,
+                         void* const* host_k_caches, void* const* host_v_caches, int num_layers,
+                         const int64_t* pairs, int num_pairs, int direction, int num_kv_heads,
+                         int head_dim, int num_dev_blocks, int num_host_blocks, int dtype,
+                         void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_check_status -- synchronise `stream`, then read and clear the device
  * status word of the current device.  Returns PA_OK, PA_ERR_DEVICE_BOUNDS,
  * PA_ERR_DEVICE_TIMEOUT, PA_ERR_INVALID_ARG (a decode run found no plan in
@@ -340,6 +369,9 @@ typedef struct pa_pool_stats_t {
   int64_t live_seqs;
   int64_t tokens;              /* sum of live context lengths */
   int64_t internal_frag_slots; /* sum over live seqs of table slots minus tokens */
+  int64_t host_blocks;         /* size of the host tier (pa_pool_set_host_blocks) */
+  int64_t host_free_blocks;
+  int64_t swapped_seqs;        /* live sequences whose blocks are on the host tier */
 } pa_pool_stats_t;
 
 /* block_size >= 1 (device kernels accept only 16; other sizes serve host
@@ -369,6 +401,32 @@ PA_API int pa_pool_block_table(pa_pool* pool, int seq, int32_t* out, int cap, in
                                int* ctx_len);
 PA_API int pa_pool_refcount(pa_pool* pool, int block, int* rc);
 PA_API int pa_pool_stats(pa_pool* pool, pa_pool_stats_t* stats);
+
+/* Swapping ("vLLM: treating the KV cache as virtual memory", section
+ * 调度：词一级的进入与退出: a preempted sequence's KV goes to host memory and
+ * comes back later, block by block; "第 6 章 缓存管理", section
+ * 缓存放不下的时候: spill cold cache to CPU memory).
+ *
+ * pa_pool_set_host_blocks gives the pool a host tier of num_host_blocks
+ * blocks (a LIFO free list started from initial_order, NULL = identity); it
+ * fails while a sequence is swapped out.
+ *
+ * pa_pool_swap_out moves sequence seq to the host tier: for each logical
+ * block i in order it takes a host block and writes the copy pair
+ * (device block, host block) to pairs[2i], pairs[2i+1] (host int64 buffer of
+ * cap pairs), then releases the device blocks last to first.  *n = number of
+ * pairs.  Copy them (pa_block_swap) before the device blocks are written
+ * again.  Fails (nothing changed) when a block is shared (refcount > 1) or
+ * pinned (PA_ERR_INVALID_ARG), the host tier is short (PA_ERR_NO_BLOCKS) or
+ * cap is too small.  pa_pool_swap_in is the mirror image: pairs are
+ * (host block, device block), the device blocks come from the free list.
+ * A swapped sequence cannot append, fork, share or pin (PA_ERR_INVALID_ARG);
+ * its block table reports its host blocks; freeing it returns them. */
+PA_API int pa_pool_set_host_blocks(pa_pool* pool, int num_host_blocks,
+                                   const int32_t* initial_order);
+PA_API int pa_pool_swap_out(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n);
+PA_API int pa_pool_swap_in(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n);
+PA_API int pa_pool_is_swapped(pa_pool* pool, int seq, int* swapped);
 
 #ifdef __cplusplus
 }

@@ -219,3 +219,18 @@ def block_copy(k_caches, v_caches, src_dst_pairs) -> None:
         for k_cache, v_cache in zip(k_caches, v_caches):
             k_cache[dst] = k_cache[src]
             v_cache[dst] = v_cache[src]
+
+
+def block_swap(src_k_caches, src_v_caches, dst_k_caches, dst_v_caches, pairs) -> None:
+    """Copy whole blocks between two tiers, in every layer, in pair order.
+
+    "vLLM: treating the KV cache as virtual memory", section
+    "调度：词一级的进入与退出": a preempted sequence's KV moves to host memory
+    block by block and comes back later.  ``pairs[i] = (src, dst)``:
+    ``dst_cache[dst] = src_cache[src]`` for K and V of every layer.
+    """
+    for src, dst in pairs:
+        src, dst = int(src), int(dst)
+        for sk, sv, dk, dv in zip(src_k_caches, src_v_caches, dst_k_caches, dst_v_caches):
+            dk[dst] = sk[src]
+            dv[dst] = sv[src]

@@ -25,7 +25,11 @@ against it operation by operation:
   "块表长什么样": a 200-token shared prefix gives 13 shared entries);
 * pinning: a prefix-cache block stays out of the free list even at refcount
   zero (page 2, section "碎片从哪里来": hot prefixes are kept outside the free
-  list).
+  list);
+* swapping: a preempted sequence's KV moves to host memory block by block and
+  comes back later ("vLLM: treating the KV cache as virtual memory", section
+  "调度：词一级的进入与退出"; "第 6 章 缓存管理", section "缓存放不下的时候":
+  spill cold cache to CPU memory).  Host blocks have their own free list.
 
 Policy choices the pages leave open (both implementations follow them so their
 tables can be compared bit for bit):
@@ -34,7 +38,13 @@ tables can be compared bit for bit):
   ``initial_order[0]`` handed out first;
 * freeing a sequence releases its blocks from the last logical block to the
   first;
-* sequence ids count up from 0 and are never reused.
+* sequence ids count up from 0 and are never reused;
+* the host tier is a second LIFO stack (``host_initial_order[0]`` first); a
+  sequence swaps out only when none of its blocks is shared or pinned (a
+  shared block still has a reader on the device); swapping out takes a host
+  block per logical block in order, then releases the device blocks last to
+  first; swapping in is the mirror image; a swapped sequence cannot append,
+  fork, share or pin until it is swapped back in.
 """
 
 from __future__ import annotations
@@ -50,6 +60,7 @@ class NoBlocks(Exception):
 class _Seq:
     table: list = field(default_factory=list)
     ctx: int = 0
+    swapped: bool = False           # table holds host blocks
 
 
 class BlockPool:
@@ -67,6 +78,19 @@ class BlockPool:
         self.seqs: dict[int, _Seq] = {}
         self.next_id = 0
         self.cow_copies = 0
+        self.num_host_blocks = 0
+        self.host_free: list[int] = []
+
+    def set_host_blocks(self, num_host_blocks: int, initial_order=None) -> None:
+        """Give the pool a host tier of ``num_host_blocks`` blocks (swap space)."""
+        if num_host_blocks < 0 or any(s.swapped for s in self.seqs.values()):
+            raise ValueError("bad host block count, or sequences are swapped out")
+        order = (list(range(num_host_blocks)) if initial_order is None
+                 else [int(x) for x in initial_order])
+        if sorted(order) != list(range(num_host_blocks)):
+            raise ValueError("initial_order must be a permutation of range(num_host_blocks)")
+        self.num_host_blocks = num_host_blocks
+        self.host_free = list(reversed(order))
 
     # -- internal -----------------------------------------------------------
     def _alloc(self) -> int:
@@ -86,6 +110,12 @@ class BlockPool:
             raise KeyError(seq_id)
         return self.seqs[seq_id]
 
+    def _resident(self, seq_id: int) -> _Seq:
+        seq = self._seq(seq_id)
+        if seq.swapped:
+            raise ValueError("sequence is swapped out")
+        return seq
+
     # -- operations ---------------------------------------------------------
     def new_seq(self) -> int:
         seq_id = self.next_id
@@ -99,7 +129,7 @@ class BlockPool:
         Returns ``(slot, cow)`` where ``slot = physical * block_size + offset``
         and ``cow`` is ``(src, dst)`` when a copy-on-write happened, else None.
         """
-        seq = self._seq(seq_id)
+        seq = self._resident(seq_id)
         logical, offset = divmod(seq.ctx, self.block_size)
         cow = None
         if offset == 0:
@@ -118,7 +148,7 @@ class BlockPool:
         return block * self.block_size + offset, cow
 
     def fork(self, parent_id: int) -> int:
-        parent = self._seq(parent_id)
+        parent = self._resident(parent_id)
         child_id = self.new_seq()
         child = self.seqs[child_id]
         child.table = list(parent.table)
@@ -128,7 +158,7 @@ class BlockPool:
         return child_id
 
     def share_prefix(self, src_id: int, dst_id: int, num_tokens: int) -> None:
-        src, dst = self._seq(src_id), self._seq(dst_id)
+        src, dst = self._resident(src_id), self._resident(dst_id)
         if dst.ctx != 0 or dst.table:
             raise ValueError("destination must be an empty sequence")
         if num_tokens <= 0 or num_tokens > src.ctx:
@@ -140,7 +170,7 @@ class BlockPool:
             self.refcount[block] += 1
 
     def pin(self, seq_id: int, num_tokens: int) -> None:
-        seq = self._seq(seq_id)
+        seq = self._resident(seq_id)
         if num_tokens < 0 or num_tokens > seq.ctx:
             raise ValueError("num_tokens must be in 0..context length")
         for block in seq.table[:-(-num_tokens // self.block_size)]:
@@ -156,8 +186,47 @@ class BlockPool:
     def free_seq(self, seq_id: int) -> None:
         seq = self._seq(seq_id)
         for block in reversed(seq.table):
-            self._release(block)
+            if seq.swapped:
+                self.host_free.append(block)
+            else:
+                self._release(block)
         del self.seqs[seq_id]
+
+    def swap_out(self, seq_id: int):
+        """Move a sequence's blocks to the host tier.  Returns the copy pairs
+        ``(device_block, host_block)`` in logical order (copy them before the
+        device blocks are written again)."""
+        seq = self._resident(seq_id)
+        if any(self.refcount[b] != 1 or self.pinned[b] for b in seq.table):
+            raise ValueError("a shared or pinned block cannot be swapped out")
+        if len(seq.table) > len(self.host_free):
+            raise NoBlocks()
+        host = [self.host_free.pop() for _ in seq.table]
+        pairs = list(zip(seq.table, host))
+        for block in reversed(seq.table):
+            self._release(block)
+        seq.table = host
+        seq.swapped = True
+        return pairs
+
+    def swap_in(self, seq_id: int):
+        """Bring a swapped sequence back.  Returns the copy pairs
+        ``(host_block, device_block)`` in logical order."""
+        seq = self._seq(seq_id)
+        if not seq.swapped:
+            raise ValueError("sequence is not swapped out")
+        if len(seq.table) > len(self.free):
+            raise NoBlocks()
+        dev = [self._alloc() for _ in seq.table]
+        pairs = list(zip(seq.table, dev))
+        for block in reversed(seq.table):
+            self.host_free.append(block)
+        seq.table = dev
+        seq.swapped = False
+        return pairs
+
+    def is_swapped(self, seq_id: int) -> bool:
+        return self._seq(seq_id).swapped
 
     # -- queries ------------------------------------------------------------
     def block_table(self, seq_id: int):
@@ -176,4 +245,7 @@ class BlockPool:
             "live_seqs": len(self.seqs),
             "tokens": sum(s.ctx for s in live),
             "internal_frag_slots": sum(len(s.table) * self.block_size - s.ctx for s in live),
+            "host_blocks": self.num_host_blocks,
+            "host_free_blocks": len(self.host_free),
+            "swapped_seqs": sum(1 for s in live if s.swapped),
         }

@@ -12,6 +12,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
 * :func:`paged_attention_prefill` -- chunked-prefill attention: each
   sequence's newest tokens attend causally over the paged cache;
 * :func:`block_copy` -- copy-on-write block copies across all layers;
+* :func:`block_swap` -- whole blocks between the device caches and
+  page-locked host caches (preemption / offload), all layers in one launch;
 
 and the native host :class:`BlockPool` that produces tables, slots and copy
 pairs.  The library is loaded on first use; if it has not been built the call
@@ -19,8 +21,9 @@ raises -- there is no fallback implementation.
 """
 
 from .capi import PagedAttnError  # noqa: F401
+from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
 from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
-                  check_status, kv_append, paged_attention_decode,
+                  block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_prefill,
                   prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,

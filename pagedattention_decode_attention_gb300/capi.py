@@ -33,10 +33,14 @@ PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 BLOCK_SIZE = 16
 
 
+PA_SWAP_OUT, PA_SWAP_IN = 0, 1
+
+
 class PoolStats(C.Structure):
     _fields_ = [(name, C.c_int64) for name in (
         "num_blocks", "free_blocks", "used_blocks", "pinned_blocks", "shared_blocks",
-        "cow_copies", "live_seqs", "tokens", "internal_frag_slots")]
+        "cow_copies", "live_seqs", "tokens", "internal_frag_slots", "host_blocks",
+        "host_free_blocks", "swapped_seqs")]
 
 
 class PagedAttnError(RuntimeError):
@@ -66,6 +70,8 @@ SIGNATURES = {
     "pa_paged_attention_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                                C.c_float, _i, _vp, _vp]),
     "pa_block_copy": (_i, [C.POINTER(_vp), C.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_block_swap": (_i, [C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), _i,
+                           _vp, _i, _i, _i, _i, _i, _i, _i, _vp]),
     "pa_check_status": (_i, [_vp]),
     "pa_pool_create": (_i, [_i, _i, _i32p, C.POINTER(_vp)]),
     "pa_pool_destroy": (_i, [_vp]),
@@ -80,6 +86,10 @@ SIGNATURES = {
     "pa_pool_block_table": (_i, [_vp, _i, _i32p, _i, C.POINTER(_i), C.POINTER(_i)]),
     "pa_pool_refcount": (_i, [_vp, _i, C.POINTER(_i)]),
     "pa_pool_stats": (_i, [_vp, C.POINTER(PoolStats)]),
+    "pa_pool_set_host_blocks": (_i, [_vp, _i, _i32p]),
+    "pa_pool_swap_out": (_i, [_vp, _i, _i64p, _i, C.POINTER(_i)]),
+    "pa_pool_swap_in": (_i, [_vp, _i, _i64p, _i, C.POINTER(_i)]),
+    "pa_pool_is_swapped": (_i, [_vp, _i, C.POINTER(_i)]),
 }
 
 _lib = None

@@ -84,6 +84,41 @@ __global__ void block_copy_kernel(const __grid_constant__ LayerPtrs ptrs,
   for (int i = threadIdx.x; i < block_vecs; i += blockDim.x) to[i] = from[i];
 }
 
+// Whole-block copies between two caches of the same shape (one on the
+// device, one in page-locked host memory reached over the CPU-GPU link), all
+// layers in one launch: grid (pair, layer, K/V).  Each thread keeps eight
+// 16-byte loads in flight, so the link sees many outstanding requests.
+__global__ void block_swap_kernel(const __grid_constant__ LayerPtrs src,
+                                  const __grid_constant__ LayerPtrs dst,
+                                  const int64_t* __restrict__ pairs, int block_vecs,
+                                  int64_t num_src_blocks, int64_t num_dst_blocks,
+                                  unsigned* status) {
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int64_t s = pairs[2 * int64_t(pair)], d = pairs[2 * int64_t(pair) + 1];
+  if (s < 0 || s >= num_src_blocks || d < 0 || d >= num_dst_blocks) {
+    if (threadIdx.x == 0) dev::flag_status(status, kStatusBounds);
+    return;
+  }
+  const uint4* from = (blockIdx.z == 0 ? src.k[layer] : src.v[layer]) + s * block_vecs;
+  uint4* to = (blockIdx.z == 0 ? dst.k[layer] : dst.v[layer]) + d * block_vecs;
+  constexpr int kBatch = 8;
+  for (int base = 0; base < block_vecs; base += kBatch * blockDim.x) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < block_vecs) r[u] = from[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < block_vecs) to[i] = r[u];
+    }
+  }
+}
+
 int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
 
 int check_common(int dtype, int head_dim, int num_kv_heads, int num_blocks, const char* who) {
@@ -206,6 +241,58 @@ PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_l
   cudaError_t e = cudaLaunchKernelEx(&cfg, block_copy_kernel, ptrs, src_dst_pairs, block_vecs,
                                      int64_t(num_blocks), status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "block_copy: launch failed: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+PA_API int pa_block_swap(void* const* dev_k_caches, void* const* dev_v_caches,
+                         void* const* host_k_caches, void* const* host_v_caches, int num_layers,
+                         const int64_t* pairs, int num_pairs, int direction, int num_kv_heads,
+                         int head_dim, int num_dev_blocks, int num_host_blocks, int dtype,
+                         void* stream) {
+  int rc = check_common(dtype, head_dim, num_kv_heads, num_dev_blocks, "block_swap");
+  if (rc != PA_OK) return rc;
+  if (num_host_blocks <= 0 || num_pairs < 0 || num_layers < 0 || num_layers > kMaxLayers ||
+      (direction != PA_SWAP_OUT && direction != PA_SWAP_IN))
+    return fail(PA_ERR_INVALID_ARG, "block_swap: bad num_host_blocks, num_pairs, num_layers or direction");
+  if (num_pairs == 0 || num_layers == 0) return PA_OK;
+  if (!dev_k_caches || !dev_v_caches || !host_k_caches || !host_v_caches || !pairs)
+    return fail(PA_ERR_INVALID_ARG, "block_swap: NULL pointer");
+  LayerPtrs dev = {}, host = {};
+  for (int l = 0; l < num_layers; ++l) {
+    void* hp[2] = {host_k_caches[l], host_v_caches[l]};
+    void* dp[2] = {dev_k_caches[l], dev_v_caches[l]};
+    for (int kv = 0; kv < 2; ++kv) {
+      if (!dp[kv] || !hp[kv] || misaligned(dp[kv]) || misaligned(hp[kv]))
+        return fail(PA_ERR_INVALID_ARG, "block_swap: layer %d pointer NULL or unaligned", l);
+      // the host side must be page-locked memory the device can address
+      cudaPointerAttributes a;
+      if (cudaPointerGetAttributes(&a, hp[kv]) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+          !a.devicePointer) {
+        cudaGetLastError();
+        return fail(PA_ERR_INVALID_ARG, "block_swap: layer %d host cache is not page-locked host memory", l);
+      }
+      (kv ? host.v : host.k)[l] = static_cast<uint4*>(a.devicePointer);
+      (kv ? dev.v : dev.k)[l] = static_cast<uint4*>(dp[kv]);
+    }
+  }
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const int block_vecs = num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype) / 16;
+  const bool out = direction == PA_SWAP_OUT;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_pairs, num_layers, 2);
+  cfg.blockDim = dim3(256);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, block_swap_kernel, out ? dev : host, out ? host : dev,
+                                     pairs, block_vecs,
+                                     int64_t(out ? num_dev_blocks : num_host_blocks),
+                                     int64_t(out ? num_host_blocks : num_dev_blocks), status);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "block_swap: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
 }
 

@@ -1,6 +1,7 @@
 // Host block pool: free list, refcounts, lazy allocation, fork, copy-on-write,
-// prefix sharing and pinning.  It produces block tables, slots and copy pairs
-// for the device kernels and never touches device memory.
+// prefix sharing, pinning and swapping to a host tier.  It produces block
+// tables, slots and copy pairs for the device kernels and never touches
+// device memory.
 //
 // Sources: "vLLM: treating the KV cache as virtual memory", section
 // 碎片从哪里来 (fixed blocks, free list, refcounts, fork copies the table,
@@ -8,7 +9,10 @@
 // section 块表长什么样 (refcount 1 -> 2 on sharing, -1 when a request ends,
 // free at 0); OS-lab appendix sections 3.3 (allocate a physical page only when
 // generation reaches it) and 4.4 (copy a shared partly-filled block on write;
-// the last holder writes in place).
+// the last holder writes in place); "vLLM: treating the KV cache as virtual
+// memory", section 调度：词一级的进入与退出 (a preempted sequence's KV goes to
+// host memory block by block and comes back later) and "第 6 章 缓存管理",
+// section 缓存放不下的时候 (spill cold cache to CPU memory).
 #include <algorithm>
 #include <cstdint>
 #include <unordered_map>
@@ -20,8 +24,9 @@
 namespace {
 
 struct Seq {
-  std::vector<int32_t> table;
+  std::vector<int32_t> table;  // device blocks, or host blocks while swapped
   int64_t ctx = 0;
+  bool swapped = false;
 };
 
 }  // namespace
@@ -36,6 +41,8 @@ struct pa_pool {
   std::unordered_map<int, Seq> seqs;
   int next_id = 0;
   int64_t cow_copies = 0;
+  int num_host_blocks = 0;
+  std::vector<int32_t> host_free;   // top = back()
 
   int32_t alloc() {
     int32_t b = free_stack.back();
@@ -55,6 +62,23 @@ struct pa_pool {
     return it == seqs.end() ? nullptr : &it->second;
   }
 };
+
+namespace {
+// A live sequence whose blocks are on the device, or null with the error set.
+Seq* resident(pa_pool* pool, int id, const char* who, int* rc) {
+  Seq* s = pool->find(id);
+  if (!s) {
+    *rc = pa::fail(PA_ERR_NOT_FOUND, "%s: unknown sequence", who);
+    return nullptr;
+  }
+  if (s->swapped) {
+    *rc = pa::fail(PA_ERR_INVALID_ARG, "%s: sequence is swapped out", who);
+    return nullptr;
+  }
+  *rc = PA_OK;
+  return s;
+}
+}  // namespace
 
 extern "C" {
 
@@ -101,8 +125,9 @@ PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* c
                                int64_t* cow_dst) {
   if (!pool || !slot || !cow_src || !cow_dst)
     return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slot: NULL argument");
-  Seq* s = pool->find(seq);
-  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_append_slot: unknown sequence");
+  int rc = PA_OK;
+  Seq* s = resident(pool, seq, "pa_pool_append_slot", &rc);
+  if (!s) return rc;
   const int64_t logical = s->ctx / pool->block_size;
   const int64_t offset = s->ctx % pool->block_size;
   int64_t src = -1, dst = -1;
@@ -143,7 +168,7 @@ PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64
     // A copy pair needs room before the slot is taken, so a full pair buffer
     // never leaves a copy unreported.
     Seq* s = pool->find(seqs[i]);
-    if (s && s->ctx % pool->block_size != 0 &&
+    if (s && !s->swapped && s->ctx % pool->block_size != 0 &&
         pool->refcount[s->table[s->ctx / pool->block_size]] > 1 && *num_pairs >= pair_cap)
       return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slots: pair buffer full");
     int rc = pa_pool_append_slot(pool, seqs[i], &slots[i], &src, &dst);
@@ -160,8 +185,9 @@ PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64
 
 PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child) {
   if (!pool || !child) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_fork: NULL argument");
-  Seq* p = pool->find(parent);
-  if (!p) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_fork: unknown sequence");
+  int rc = PA_OK;
+  Seq* p = resident(pool, parent, "pa_pool_fork", &rc);
+  if (!p) return rc;
   Seq c;
   c.table = p->table;
   c.ctx = p->ctx;
@@ -174,9 +200,11 @@ PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child) {
 
 PA_API int pa_pool_share_prefix(pa_pool* pool, int src_seq, int dst_seq, int num_tokens) {
   if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_share_prefix: NULL pool");
-  Seq* src = pool->find(src_seq);
-  Seq* dst = pool->find(dst_seq);
-  if (!src || !dst) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_share_prefix: unknown sequence");
+  int rc = PA_OK;
+  Seq* src = resident(pool, src_seq, "pa_pool_share_prefix", &rc);
+  if (!src) return rc;
+  Seq* dst = resident(pool, dst_seq, "pa_pool_share_prefix", &rc);
+  if (!dst) return rc;
   if (dst->ctx != 0 || !dst->table.empty())
     return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_share_prefix: destination must be empty");
   if (num_tokens <= 0 || num_tokens > src->ctx)
@@ -190,8 +218,9 @@ PA_API int pa_pool_share_prefix(pa_pool* pool, int src_seq, int dst_seq, int num
 
 PA_API int pa_pool_pin(pa_pool* pool, int seq, int num_tokens) {
   if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_pin: NULL pool");
-  Seq* s = pool->find(seq);
-  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_pin: unknown sequence");
+  int rc = PA_OK;
+  Seq* s = resident(pool, seq, "pa_pool_pin", &rc);
+  if (!s) return rc;
   if (num_tokens < 0 || num_tokens > s->ctx)
     return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_pin: num_tokens out of range");
   const int64_t count = (num_tokens + pool->block_size - 1) / pool->block_size;
@@ -216,8 +245,92 @@ PA_API int pa_pool_free_seq(pa_pool* pool, int seq) {
   auto it = pool->seqs.find(seq);
   if (it == pool->seqs.end()) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_free_seq: unknown sequence");
   const auto& table = it->second.table;
-  for (auto b = table.rbegin(); b != table.rend(); ++b) pool->release(*b);
+  for (auto b = table.rbegin(); b != table.rend(); ++b) {
+    if (it->second.swapped)
+      pool->host_free.push_back(*b);
+    else
+      pool->release(*b);
+  }
   pool->seqs.erase(it);
+  return PA_OK;
+}
+
+PA_API int pa_pool_set_host_blocks(pa_pool* pool, int num_host_blocks,
+                                   const int32_t* initial_order) {
+  if (!pool || num_host_blocks < 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_set_host_blocks: bad argument");
+  for (const auto& kv : pool->seqs)
+    if (kv.second.swapped)
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_set_host_blocks: sequences are swapped out");
+  std::vector<uint8_t> seen(num_host_blocks, 0);
+  std::vector<int32_t> stack(num_host_blocks);
+  for (int i = 0; i < num_host_blocks; ++i) {
+    const int32_t b = initial_order ? initial_order[i] : i;
+    if (b < 0 || b >= num_host_blocks || seen[b])
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_set_host_blocks: initial_order is not a permutation");
+    seen[b] = 1;
+    stack[num_host_blocks - 1 - i] = b;  // initial_order[0] ends on top
+  }
+  pool->num_host_blocks = num_host_blocks;
+  pool->host_free.swap(stack);
+  return PA_OK;
+}
+
+PA_API int pa_pool_swap_out(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n) {
+  if (!pool || !n || cap < 0 || (cap > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_out: bad argument");
+  int rc = PA_OK;
+  Seq* s = resident(pool, seq, "pa_pool_swap_out", &rc);
+  if (!s) return rc;
+  const int len = static_cast<int>(s->table.size());
+  for (int32_t b : s->table)
+    if (pool->refcount[b] != 1 || pool->pinned[b])
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_out: a shared or pinned block cannot leave");
+  if (len > cap) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_out: pair buffer too small");
+  if (len > static_cast<int>(pool->host_free.size()))
+    return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_swap_out: host tier exhausted");
+  std::vector<int32_t> host(len);
+  for (int i = 0; i < len; ++i) {
+    host[i] = pool->host_free.back();
+    pool->host_free.pop_back();
+    pairs[2 * i] = s->table[i];
+    pairs[2 * i + 1] = host[i];
+  }
+  for (int i = len - 1; i >= 0; --i) pool->release(s->table[i]);
+  s->table.swap(host);
+  s->swapped = true;
+  *n = len;
+  return PA_OK;
+}
+
+PA_API int pa_pool_swap_in(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n) {
+  if (!pool || !n || cap < 0 || (cap > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_in: bad argument");
+  Seq* s = pool->find(seq);
+  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_swap_in: unknown sequence");
+  if (!s->swapped) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_in: sequence is not swapped out");
+  const int len = static_cast<int>(s->table.size());
+  if (len > cap) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_in: pair buffer too small");
+  if (len > static_cast<int>(pool->free_stack.size()))
+    return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_swap_in: pool exhausted");
+  std::vector<int32_t> dev(len);
+  for (int i = 0; i < len; ++i) {
+    dev[i] = pool->alloc();
+    pairs[2 * i] = s->table[i];
+    pairs[2 * i + 1] = dev[i];
+  }
+  for (int i = len - 1; i >= 0; --i) pool->host_free.push_back(s->table[i]);
+  s->table.swap(dev);
+  s->swapped = false;
+  *n = len;
+  return PA_OK;
+}
+
+PA_API int pa_pool_is_swapped(pa_pool* pool, int seq, int* swapped) {
+  if (!pool || !swapped) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_is_swapped: NULL argument");
+  Seq* s = pool->find(seq);
+  if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_is_swapped: unknown sequence");
+  *swapped = s->swapped ? 1 : 0;
   return PA_OK;
 }
 
@@ -255,7 +368,11 @@ PA_API int pa_pool_stats(pa_pool* pool, pa_pool_stats_t* st) {
   st->cow_copies = pool->cow_copies;
   st->live_seqs = static_cast<int64_t>(pool->seqs.size());
   st->tokens = st->internal_frag_slots = 0;
+  st->host_blocks = pool->num_host_blocks;
+  st->host_free_blocks = static_cast<int64_t>(pool->host_free.size());
+  st->swapped_seqs = 0;
   for (const auto& kv : pool->seqs) {
+    st->swapped_seqs += kv.second.swapped;
     st->tokens += kv.second.ctx;
     st->internal_frag_slots +=
         static_cast<int64_t>(kv.second.table.size()) * pool->block_size - kv.second.ctx;

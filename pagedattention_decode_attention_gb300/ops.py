@@ -325,6 +325,37 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     return out
 
 
+def block_swap(dev_k_caches, dev_v_caches, host_k_caches, host_v_caches,
+               pairs: torch.Tensor, direction: int, stream=None) -> None:
+    """Copy whole blocks between the device caches and page-locked host caches
+    (``[num_host_blocks, Hkv, 16, d]`` per layer), every layer in one launch:
+    ``direction`` ``PA_SWAP_OUT`` copies device block ``pairs[i, 0]`` to host
+    block ``pairs[i, 1]``; ``PA_SWAP_IN`` copies host ``pairs[i, 0]`` to device
+    ``pairs[i, 1]`` (the pairs the pool's swap_out / swap_in return)."""
+    dk, dv, hk, hv = (list(x) for x in (dev_k_caches, dev_v_caches, host_k_caches, host_v_caches))
+    _require(len(dk) == len(dv) == len(hk) == len(hv) and len(dk) > 0,
+             "need one device and one host K/V cache per layer")
+    dev = dk[0].device
+    ref, href = dk[0], hk[0]
+    for t in dk + dv:
+        _cuda_contig("device cache", t, dev)
+        _require(t.shape == ref.shape and t.dtype == ref.dtype, "device caches must match")
+    for t in hk + hv:
+        _require(not t.is_cuda and t.is_pinned() and t.is_contiguous(),
+                 "host caches must be contiguous page-locked CPU tensors")
+        _require(t.shape[1:] == ref.shape[1:] and t.dtype == ref.dtype and t.shape == href.shape,
+                 "host caches must be [num_host_blocks, num_kv_heads, 16, head_dim] of q's dtype")
+    _cuda_contig("pairs", pairs, dev)
+    _require(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2,
+             "pairs must be int64 [n, 2] on the device")
+    n = len(dk)
+    arr = lambda ts: (C.c_void_p * n)(*[t.data_ptr() for t in ts])  # noqa: E731
+    nb, hkv, _, d = ref.shape
+    capi.check(capi.lib().pa_block_swap(arr(dk), arr(dv), arr(hk), arr(hv), n, pairs.data_ptr(),
+                                        pairs.shape[0], int(direction), hkv, d, nb,
+                                        href.shape[0], _dtype_code(ref), _stream(dev, stream)))
+
+
 def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:
     """Copy whole blocks ``src -> dst`` (int64 ``[P, 2]`` on the device) in every
     layer's caches."""

@@ -86,6 +86,41 @@ class BlockPool:
                                                  n.value, C.byref(n), C.byref(ctx)))
         return buf[:n.value].tolist(), ctx.value
 
+    def set_host_blocks(self, num_host_blocks: int, initial_order=None) -> None:
+        """Give the pool a host tier (swap space) of ``num_host_blocks`` blocks."""
+        order = None
+        if initial_order is not None:
+            order = np.ascontiguousarray(initial_order, dtype=np.int32)
+            if order.shape != (num_host_blocks,):
+                raise ValueError("initial_order must have num_host_blocks entries")
+        capi.check(self._lib.pa_pool_set_host_blocks(
+            self._h, num_host_blocks,
+            None if order is None else order.ctypes.data_as(C.POINTER(C.c_int32))))
+        self._host_order = order
+
+    def _swap(self, fn, seq: int) -> np.ndarray:
+        table, _ = self.block_table(seq)
+        buf = np.empty((max(len(table), 1), 2), dtype=np.int64)
+        n = C.c_int()
+        capi.check(fn(self._h, seq, buf.ctypes.data_as(C.POINTER(C.c_int64)), len(table),
+                      C.byref(n)))
+        return buf[:n.value]
+
+    def swap_out(self, seq: int) -> np.ndarray:
+        """Move ``seq`` to the host tier; returns int64 ``[n, 2]`` copy pairs
+        (device block, host block) in logical order."""
+        return self._swap(self._lib.pa_pool_swap_out, seq)
+
+    def swap_in(self, seq: int) -> np.ndarray:
+        """Bring ``seq`` back; returns int64 ``[n, 2]`` copy pairs (host block,
+        device block) in logical order."""
+        return self._swap(self._lib.pa_pool_swap_in, seq)
+
+    def is_swapped(self, seq: int) -> bool:
+        out = C.c_int()
+        capi.check(self._lib.pa_pool_is_swapped(self._h, seq, C.byref(out)))
+        return bool(out.value)
+
     def refcount(self, block: int) -> int:
         out = C.c_int()
         capi.check(self._lib.pa_pool_refcount(self._h, block, C.byref(out)))

@@ -234,3 +234,52 @@ def test_write_never_lands_in_shared_block():
         s = seqs[gen.integers(len(seqs))]
         slot, _ = pool.append_slot(s)
         assert pool.refcount[slot // 16] == 1
+
+
+def test_swap_out_and_in_keep_the_sequence():
+    """Swapping (vLLM-VM, section "调度：词一级的进入与退出"): the device blocks
+    go back to the free list, the sequence keeps its length and its logical
+    order, and coming back it gets device blocks again."""
+    pool = BlockPool(10, 16, list(range(10)))
+    pool.set_host_blocks(6, list(range(6)))
+    a = pool.new_seq()
+    for _ in range(40):
+        pool.append_slot(a)
+    dev_table, ctx = pool.block_table(a)
+    pairs = pool.swap_out(a)
+    assert [d for d, _ in pairs] == dev_table
+    assert all(pool.refcount[b] == 0 for b in dev_table)
+    assert pool.stats()["free_blocks"] == 10 and pool.stats()["host_free_blocks"] == 3
+    assert pool.block_table(a) == ([h for _, h in pairs], ctx) and pool.is_swapped(a)
+    back = pool.swap_in(a)
+    assert [h for h, _ in back] == [h for _, h in pairs]
+    table, ctx2 = pool.block_table(a)
+    assert ctx2 == ctx and len(table) == len(dev_table) and not pool.is_swapped(a)
+    assert all(pool.refcount[b] == 1 for b in table)
+    assert pool.stats()["host_free_blocks"] == 6
+    pool.append_slot(a)                          # resident again: appends work
+    assert pool.block_table(a)[1] == ctx + 1
+
+
+def test_swap_refuses_shared_and_pinned_blocks():
+    import pytest
+    pool = BlockPool(10, 16)
+    pool.set_host_blocks(10)
+    a = pool.new_seq()
+    for _ in range(20):
+        pool.append_slot(a)
+    b = pool.fork(a)
+    with pytest.raises(ValueError):
+        pool.swap_out(a)                         # a reader remains on the device
+    pool.free_seq(b)
+    pool.pin(a, 16)
+    with pytest.raises(ValueError):
+        pool.swap_out(a)
+    c = pool.new_seq()
+    pool.append_slot(c)
+    pool.swap_out(c)
+    for op in (lambda: pool.append_slot(c), lambda: pool.fork(c), lambda: pool.pin(c, 0)):
+        with pytest.raises(ValueError):
+            op()
+    pool.free_seq(c)                             # host block goes back
+    assert pool.stats()["host_free_blocks"] == 10

@@ -49,6 +49,9 @@ def replay(pool, ops, is_native):
             elif kind == "pin":
                 pool.pin(op[1], op[2])
                 out.append(("pin",))
+            elif kind in ("swapout", "swapin"):
+                pairs = pool.swap_out(op[1]) if kind == "swapout" else pool.swap_in(op[1])
+                out.append((kind, [tuple(int(x) for x in p) for p in pairs]))
         except Exception as e:  # noqa: BLE001
             if isinstance(e, NoBlocks) or (is_native and is_no_blocks(e)):
                 out.append(("noblocks",))
@@ -57,16 +60,37 @@ def replay(pool, ops, is_native):
     return out
 
 
-def random_script(gen, n_ops, model):
-    """Random op script, generated against the model pool so every op is legal."""
+def _can_swap_out(model, s):
+    table, _ = model.block_table(s)
+    return (all(model.refcount[b] == 1 and not model.pinned[b] for b in table)
+            and len(table) <= len(model.host_free))
+
+
+def random_script(gen, n_ops, model, swaps=False):
+    """Random op script, generated against the model pool so every op is legal
+    (with ``swaps``, sequences also move to and from the host tier)."""
     ops, live = [], []
     for _ in range(n_ops):
-        r = gen.integers(0, 20)
+        r = gen.integers(0, 22 if swaps else 20)
         if r < 3 or not live:
             ops.append(("new",))
             live.append(model.new_seq())
             continue
         s = live[gen.integers(len(live))]
+        if model.is_swapped(s):
+            if r < 20 and len(model.block_table(s)[0]) <= len(model.free):
+                ops.append(("swapin", s))
+                model.swap_in(s)
+            elif r >= 20:
+                live.remove(s)
+                ops.append(("free", s))
+                model.free_seq(s)
+            continue
+        if r >= 20:
+            if _can_swap_out(model, s):
+                ops.append(("swapout", s))
+                model.swap_out(s)
+            continue
         if r < 14:
             ops.append(("append", s))
             try:
@@ -109,6 +133,56 @@ def test_native_matches_model_on_random_scripts(seed, num_blocks, block_size):
     for b in range(num_blocks):
         assert nat.refcount(b) == model.refcount[b]
     assert nat.stats() == model.stats()
+
+
+@pytest.mark.parametrize("seed,num_blocks,host_blocks", [(4, 64, 40), (5, 120, 300)])
+def test_native_matches_model_with_swapping(seed, num_blocks, host_blocks):
+    gen = np.random.default_rng(seed)
+    order = gen.permutation(num_blocks)
+    horder = gen.permutation(host_blocks)
+    m0 = ModelPool(num_blocks, 16, order)
+    m0.set_host_blocks(host_blocks, horder)
+    script = random_script(gen, 3000, m0, swaps=True)
+    assert any(op[0] == "swapout" for op in script) and any(op[0] == "swapin" for op in script)
+    model = ModelPool(num_blocks, 16, order)
+    model.set_host_blocks(host_blocks, horder)
+    nat = native(num_blocks, 16, order)
+    nat.set_host_blocks(host_blocks, horder)
+    assert replay(nat, script, True) == replay(model, script, False)
+    for s in model.seqs:
+        assert nat.block_table(s) == model.block_table(s)
+        assert nat.is_swapped(s) == model.is_swapped(s)
+    for b in range(num_blocks):
+        assert nat.refcount(b) == model.refcount[b]
+    assert nat.stats() == model.stats()
+
+
+def test_native_swap_refusals():
+    from pagedattention_decode_attention_gb300.capi import (PA_ERR_INVALID_ARG, PA_ERR_NO_BLOCKS,
+                                                            PagedAttnError)
+    pool = native(8)
+    pool.set_host_blocks(2)
+    a = pool.new_seq()
+    for _ in range(40):                      # 3 blocks
+        pool.append_slot(a)
+    with pytest.raises(PagedAttnError) as e:
+        pool.swap_out(a)                     # 3 blocks, 2 host blocks
+    assert e.value.status == PA_ERR_NO_BLOCKS
+    b = pool.fork(a)
+    pool.set_host_blocks(8)
+    with pytest.raises(PagedAttnError) as e:
+        pool.swap_out(a)                     # shared with the fork
+    assert e.value.status == PA_ERR_INVALID_ARG
+    pool.free_seq(b)
+    pairs = pool.swap_out(a)
+    assert pairs.shape == (3, 2) and pool.stats()["free_blocks"] == 8
+    for op in (lambda: pool.append_slot(a), lambda: pool.fork(a), lambda: pool.pin(a, 1)):
+        with pytest.raises(PagedAttnError) as e:
+            op()
+        assert e.value.status == PA_ERR_INVALID_ARG
+    back = pool.swap_in(a)
+    assert [tuple(p) for p in back[:, ::-1].tolist()] != [] and pool.block_table(a)[1] == 40
+    assert back[:, 0].tolist() == pairs[:, 1].tolist()     # the same host blocks come back
 
 
 def test_batched_append_matches_single():
