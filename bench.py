@@ -57,7 +57,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["mha_7b", "gqa_8b", "prefill_8b", "swap_8b"],
+    ap.add_argument("--workload",
+                    choices=["mha_7b", "gqa_8b", "prefill_8b", "swap_8b", "pool_churn"],
                     default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -709,6 +710,87 @@ def run_swap_bench(args):
     print(json.dumps(line))
 
 
+def pool_churn_stream(seed: int, n: int):
+    """Prefix-mix request stream: three 1024-token system prompts shared by
+    all requests, suffixes lognormal (median 128, clipped to [1, 4096]), 8 to
+    64 new tokens each, 0-3 arrivals per step."""
+    gen = np.random.default_rng(seed)
+    systems = [list(range(100_000 * (k + 1), 100_000 * (k + 1) + 1024)) for k in range(3)]
+    reqs = []
+    for _ in range(n):
+        sfx = int(np.clip(round(np.exp(gen.normal(np.log(128), 1.0))), 1, 4096))
+        reqs.append((systems[int(gen.integers(3))] + [int(x) for x in gen.integers(0, 50_000, sfx)],
+                     int(gen.integers(8, 65))))
+    return reqs, gen.integers(0, 4, size=1_000_000)
+
+
+def drive_pool(pool, no_blocks, reqs, arrivals):
+    """Runs the continuous-batching driver until every request retired;
+    returns (pool operations, steps, seconds)."""
+    from pagedattention_decode_attention_gb300.batching import ContinuousBatcher
+    b = ContinuousBatcher(pool, 16, no_blocks, max_running=128)
+    pending = list(reqs)
+    ops = steps = 0
+    tok = lambda r: (r.rid * 7919 + r.generated * 104729) % 50_000  # noqa: E731
+    t0 = time.perf_counter()
+    while pending or not b.idle:
+        for _ in range(int(arrivals[steps])):
+            if pending:
+                b.submit(*pending.pop(0))
+        rep = b.step(tok)
+        ops += (len(rep.slots) + len(rep.admitted) + len(rep.retired) + len(rep.swap_out)
+                + len(rep.swap_in))
+        steps += 1
+    return ops, steps, time.perf_counter() - t0
+
+
+def run_pool_bench(args):
+    """Host block pool under continuous-batching churn (no GPU work): pool
+    operations per second through the public API."""
+    import pagedattention_decode_attention_gb300 as pa
+    from pagedattention_decode_attention_gb300.capi import PA_ERR_NO_BLOCKS, PagedAttnError
+    reqs, arrivals = pool_churn_stream(wl.SEED_BASE + 8, 200)
+    pool = pa.BlockPool(4096, 16, np.random.default_rng(1).permutation(4096))
+    pool.enable_prefix_cache()
+    pool.set_host_blocks(1024)
+    no_blocks = lambda e: isinstance(e, PagedAttnError) and e.status == PA_ERR_NO_BLOCKS  # noqa: E731
+    ops, steps, secs = drive_pool(pool, no_blocks, reqs, arrivals)
+    st = pool.stats()
+    print(json.dumps(pool_line(ops, steps, secs, st, impl=None)))
+
+
+def pool_line(ops, steps, secs, st, impl):
+    line = {
+        "metric": "host block pool operations/s under continuous batching (prefix cache, swap)",
+        "value": ops / secs, "unit": "ops/s", "n_gpus": 1, "steps": steps, "warmup": 0,
+        "ms_per_step": secs / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic prefix-mix request stream",
+        "config": {"workload": "pool_churn", "requests": 200, "num_blocks": 4096,
+                   "host_blocks": 1024, "system_prompts": "3 x 1024 tokens",
+                   "prefix_hit_tokens": st["prefix_hit_tokens"], "evictions": st["evictions"],
+                   "ops": "one per appended token, admission, retirement, swap"},
+    }
+    if impl:
+        line["impl"] = impl
+    return line
+
+
+def run_reference_pool(args):
+    """Reference arm of the pool workload: the pool model driven the same way."""
+    from oracle.pool import BlockPool as ModelPool, NoBlocks
+    reqs, arrivals = pool_churn_stream(wl.SEED_BASE + 8, 200)
+    pool = ModelPool(4096, 16, np.random.default_rng(1).permutation(4096))
+    pool.enable_prefix_cache()
+    pool.set_host_blocks(1024)
+    ops, steps, secs = drive_pool(pool, NoBlocks, reqs, arrivals)
+    line = pool_line(ops, steps, secs, pool.stats(), impl="reference")
+    line["cpu_baseline"] = {"value": line["value"], "unit": "ops/s", "cores": 1, "kind": "oracle",
+                            "sample": "the whole stream through the Python pool model"}
+    line["e2e"] = {"value": line["value"], "unit": "ops/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}
+    print(json.dumps(line))
+
+
 def run_reference_prefill(args):
     """Reference arm of the chunked-prefill workload: the prefill oracle on a
     bounded sample of query rows per step, scaled to query tokens/s."""
@@ -754,6 +836,9 @@ def run_reference(args):
     if args.workload == "prefill_8b":
         run_reference_prefill(args)
         return
+    if args.workload == "pool_churn":
+        run_reference_pool(args)
+        return
     batch = make_batch(args.workload, 0)
     per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
     inp = OracleInputs(batch, None)
@@ -791,6 +876,8 @@ def main():
         run_prefill_bench(args)
     elif args.workload == "swap_8b":
         run_swap_bench(args)
+    elif args.workload == "pool_churn":
+        run_pool_bench(args)
     else:
         run_ours(args)
 

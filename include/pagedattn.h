@@ -372,6 +372,10 @@ typedef struct pa_pool_stats_t {
   int64_t host_blocks;         /* size of the host tier (pa_pool_set_host_blocks) */
   int64_t host_free_blocks;
   int64_t swapped_seqs;        /* live sequences whose blocks are on the host tier */
+  int64_t cached_blocks;       /* blocks keyed in the prefix cache */
+  int64_t evictable_blocks;    /* keyed blocks nobody holds (LRU list) */
+  int64_t prefix_hit_tokens;   /* cumulative prompt tokens served from the cache */
+  int64_t evictions;           /* cumulative cached blocks evicted for reuse */
 } pa_pool_stats_t;
 
 /* block_size >= 1 (device kernels accept only 16; other sizes serve host
@@ -427,6 +431,33 @@ PA_API int pa_pool_set_host_blocks(pa_pool* pool, int num_host_blocks,
 PA_API int pa_pool_swap_out(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n);
 PA_API int pa_pool_swap_in(pa_pool* pool, int seq, int64_t* pairs, int cap, int* n);
 PA_API int pa_pool_is_swapped(pa_pool* pool, int seq, int* swapped);
+
+/* Prefix cache ("vLLM: treating the KV cache as virtual memory", section
+ * 碎片从哪里来: hot prefixes stay outside the free list so the next request
+ * with the same system prompt hits them; "第 6 章 缓存管理", section
+ * 缓存放不下的时候: evict in least-recently-used order, recompute next time).
+ *
+ * pa_pool_enable_prefix_cache must come before the first sequence.  A full
+ * block is keyed by 64-bit FNV-1a over its parent block's key (8 bytes LE, 0
+ * for a first block) and its block_size token ids (int32 LE); lookups also
+ * compare the parent block and the ids, so equal hashes never alias.
+ * pa_pool_new_seq_with_prompt creates a sequence for a prompt of n token ids
+ * and gives it the longest run of leading full cached blocks (refcount + 1),
+ * leaving at least one token to compute: *hit_tokens (a multiple of
+ * block_size) tokens are already in the cache, the caller appends the rest.
+ * pa_pool_append_token is pa_pool_append_slot for a sequence whose token ids
+ * are tracked (made by new_seq_with_prompt, or forked / shared from one): a
+ * block it fills is keyed unless that key is already cached.  (A plain
+ * pa_pool_append_slot stops the tracking for that sequence.)  A keyed block
+ * whose refcount reaches zero joins the LRU list instead of the free list;
+ * allocations take the free list first and evict the least recently used
+ * cached block only when it is empty.  Stats report cached and evictable
+ * blocks, hit tokens and evictions. */
+PA_API int pa_pool_enable_prefix_cache(pa_pool* pool, int on);
+PA_API int pa_pool_new_seq_with_prompt(pa_pool* pool, const int32_t* tokens, int n, int* seq_id,
+                                       int* hit_tokens);
+PA_API int pa_pool_append_token(pa_pool* pool, int seq, int32_t token, int64_t* slot,
+                                int64_t* cow_src, int64_t* cow_dst);
 
 #ifdef __cplusplus
 }

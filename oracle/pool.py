@@ -26,6 +26,13 @@ against it operation by operation:
 * pinning: a prefix-cache block stays out of the free list even at refcount
   zero (page 2, section "碎片从哪里来": hot prefixes are kept outside the free
   list);
+* prefix caching: a full block is keyed by its content -- the key of the block
+  before it and its 16 token ids -- so a later request whose prompt starts
+  with the same blocks reuses them instead of recomputing them (page 2,
+  section "碎片从哪里来": the prefix cache keeps hot prefixes outside the free
+  list so the next request with the same system prompt hits them; page 4,
+  section "缓存放不下的时候": when memory is full, evict in least-recently-used
+  order and recompute on the next use);
 * swapping: a preempted sequence's KV moves to host memory block by block and
   comes back later ("vLLM: treating the KV cache as virtual memory", section
   "调度：词一级的进入与退出"; "第 6 章 缓存管理", section "缓存放不下的时候":
@@ -44,12 +51,46 @@ tables can be compared bit for bit):
   shared block still has a reader on the device); swapping out takes a host
   block per logical block in order, then releases the device blocks last to
   first; swapping in is the mirror image; a swapped sequence cannot append,
-  fork, share or pin until it is swapped back in.
+  fork, share or pin until it is swapped back in;
+* prefix cache: the key hash is 64-bit FNV-1a over the parent key (8 bytes,
+  little-endian; 0 for a sequence's first block) then the 16 token ids (int32,
+  little-endian); a lookup also compares the parent block and the token ids,
+  so equal hashes never alias different content.  A prompt reuses its longest
+  run of leading full cached blocks, but leaves at least one token to compute
+  (whose logits the caller needs).  A block is keyed when an append fills it,
+  unless its key is already cached.  A keyed block whose refcount drops to
+  zero goes to the back of an LRU list instead of the free list; allocation
+  takes the free list first and evicts the front of the LRU list (dropping its
+  key) only when the free list is empty; a hit on an LRU block takes it back
+  out.
 """
 
 from __future__ import annotations
 
+from collections import OrderedDict
 from dataclasses import dataclass, field
+
+_FNV_OFFSET = 0xCBF29CE484222325
+_FNV_PRIME = 0x100000001B3
+_MASK64 = (1 << 64) - 1
+
+
+def fnv1a64(data: bytes) -> int:
+    """64-bit FNV-1a (Fowler-Noll-Vo): start from the offset basis, for each
+    byte xor it in, then multiply by the FNV prime modulo 2^64."""
+    h = _FNV_OFFSET
+    for byte in data:
+        h ^= byte
+        h = (h * _FNV_PRIME) & _MASK64
+    return h
+
+
+def block_key_hash(parent_hash: int, tokens) -> int:
+    """Prefix-cache key hash of a full block: FNV-1a over the parent hash
+    (8 bytes LE) and the token ids (int32 LE each)."""
+    data = int(parent_hash & _MASK64).to_bytes(8, "little")
+    data += b"".join(int(t & 0xFFFFFFFF).to_bytes(4, "little") for t in tokens)
+    return fnv1a64(data)
 
 
 class NoBlocks(Exception):
@@ -61,6 +102,8 @@ class _Seq:
     table: list = field(default_factory=list)
     ctx: int = 0
     swapped: bool = False           # table holds host blocks
+    tokens: list | None = None      # token ids, when known (prefix cache)
+    hashes: list = field(default_factory=list)   # key hash of each keyed-or-full block
 
 
 class BlockPool:
@@ -80,6 +123,17 @@ class BlockPool:
         self.cow_copies = 0
         self.num_host_blocks = 0
         self.host_free: list[int] = []
+        self.prefix_cache = False
+        self.cache: dict[int, int] = {}            # key hash -> block
+        self.key = [None] * num_blocks             # block -> (hash, parent block, tokens)
+        self.lru: OrderedDict[int, None] = OrderedDict()   # evictable keyed blocks, oldest first
+        self.hit_tokens = 0
+        self.evictions = 0
+
+    def enable_prefix_cache(self, on: bool = True) -> None:
+        if self.seqs:
+            raise ValueError("enable the prefix cache before the first sequence")
+        self.prefix_cache = bool(on)
 
     def set_host_blocks(self, num_host_blocks: int, initial_order=None) -> None:
         """Give the pool a host tier of ``num_host_blocks`` blocks (swap space)."""
@@ -93,17 +147,33 @@ class BlockPool:
         self.host_free = list(reversed(order))
 
     # -- internal -----------------------------------------------------------
+    def _available(self) -> int:
+        return len(self.free) + len(self.lru)
+
     def _alloc(self) -> int:
-        if not self.free:
+        if self.free:
+            block = self.free.pop()
+        elif self.lru:
+            block, _ = self.lru.popitem(last=False)      # least recently used
+            del self.cache[self.key[block][0]]
+            self.key[block] = None
+            self.evictions += 1
+        else:
             raise NoBlocks()
-        block = self.free.pop()
         self.refcount[block] = 1
         return block
+
+    def _to_idle(self, block: int) -> None:
+        """A block nobody holds: evictable when keyed, else free."""
+        if self.key[block] is not None:
+            self.lru[block] = None
+        else:
+            self.free.append(block)
 
     def _release(self, block: int) -> None:
         self.refcount[block] -= 1
         if self.refcount[block] == 0 and not self.pinned[block]:
-            self.free.append(block)
+            self._to_idle(block)
 
     def _seq(self, seq_id: int) -> _Seq:
         if seq_id not in self.seqs:
@@ -145,7 +215,64 @@ class BlockPool:
                 self.cow_copies += 1
                 block = fresh
         seq.ctx += 1
+        if seq.tokens is not None:
+            seq.tokens = None          # the content of the new slot is unknown
         return block * self.block_size + offset, cow
+
+    def new_seq_with_prompt(self, tokens):
+        """A new sequence for a prompt: its longest run of leading full blocks
+        found in the prefix cache is reused (refcount + 1).  Returns
+        ``(seq_id, hit_tokens)``; the caller appends the remaining prompt tokens
+        with ``append_token``."""
+        tokens = [int(t) for t in tokens]
+        seq_id = self.new_seq()
+        seq = self.seqs[seq_id]
+        seq.tokens = []
+        if not self.prefix_cache:
+            return seq_id, 0
+        bs = self.block_size
+        limit = (len(tokens) - 1) // bs if tokens else 0
+        parent_hash, parent_block = 0, -1
+        for i in range(limit):
+            chunk = tokens[i * bs:(i + 1) * bs]
+            h = block_key_hash(parent_hash, chunk)
+            block = self.cache.get(h)
+            if block is None or self.key[block][1] != parent_block or self.key[block][2] != tuple(chunk):
+                break
+            if self.refcount[block] == 0 and block in self.lru:
+                del self.lru[block]
+            self.refcount[block] += 1
+            seq.table.append(block)
+            seq.hashes.append(h)
+            seq.tokens += chunk
+            seq.ctx += bs
+            parent_hash, parent_block = h, block
+        self.hit_tokens += seq.ctx
+        return seq_id, seq.ctx
+
+    def append_token(self, seq_id: int, token: int):
+        """``append_slot`` for a token whose id is known: a block it fills is
+        keyed into the prefix cache.  Returns ``(slot, cow)``."""
+        seq = self._resident(seq_id)
+        known = seq.tokens
+        slot, cow = self.append_slot(seq_id)
+        if known is None:
+            return slot, cow
+        known.append(int(token))
+        seq.tokens = known
+        bs = self.block_size
+        if self.prefix_cache and seq.ctx % bs == 0:
+            i = seq.ctx // bs - 1
+            parent_hash = seq.hashes[i - 1] if i > 0 else 0
+            parent_block = seq.table[i - 1] if i > 0 else -1
+            chunk = tuple(known[i * bs:(i + 1) * bs])
+            h = block_key_hash(parent_hash, chunk)
+            seq.hashes.append(h)
+            block = seq.table[i]
+            if h not in self.cache and self.key[block] is None:
+                self.cache[h] = block
+                self.key[block] = (h, parent_block, chunk)
+        return slot, cow
 
     def fork(self, parent_id: int) -> int:
         parent = self._resident(parent_id)
@@ -153,6 +280,8 @@ class BlockPool:
         child = self.seqs[child_id]
         child.table = list(parent.table)
         child.ctx = parent.ctx
+        child.tokens = None if parent.tokens is None else list(parent.tokens)
+        child.hashes = list(parent.hashes)
         for block in child.table:
             self.refcount[block] += 1
         return child_id
@@ -166,6 +295,8 @@ class BlockPool:
         count = -(-num_tokens // self.block_size)
         dst.table = list(src.table[:count])
         dst.ctx = num_tokens
+        dst.tokens = None if src.tokens is None else list(src.tokens[:num_tokens])
+        dst.hashes = list(src.hashes[:num_tokens // self.block_size])
         for block in dst.table:
             self.refcount[block] += 1
 
@@ -181,7 +312,7 @@ class BlockPool:
             raise ValueError("block is not pinned")
         self.pinned[block] = False
         if self.refcount[block] == 0:
-            self.free.append(block)
+            self._to_idle(block)
 
     def free_seq(self, seq_id: int) -> None:
         seq = self._seq(seq_id)
@@ -215,7 +346,7 @@ class BlockPool:
         seq = self._seq(seq_id)
         if not seq.swapped:
             raise ValueError("sequence is not swapped out")
-        if len(seq.table) > len(self.free):
+        if len(seq.table) > self._available():
             raise NoBlocks()
         dev = [self._alloc() for _ in seq.table]
         pairs = list(zip(seq.table, dev))
@@ -248,4 +379,8 @@ class BlockPool:
             "host_blocks": self.num_host_blocks,
             "host_free_blocks": len(self.host_free),
             "swapped_seqs": sum(1 for s in live if s.swapped),
+            "cached_blocks": len(self.cache),
+            "evictable_blocks": len(self.lru),
+            "prefix_hit_tokens": self.hit_tokens,
+            "evictions": self.evictions,
         }

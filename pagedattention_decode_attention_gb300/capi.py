@@ -40,7 +40,8 @@ class PoolStats(C.Structure):
     _fields_ = [(name, C.c_int64) for name in (
         "num_blocks", "free_blocks", "used_blocks", "pinned_blocks", "shared_blocks",
         "cow_copies", "live_seqs", "tokens", "internal_frag_slots", "host_blocks",
-        "host_free_blocks", "swapped_seqs")]
+        "host_free_blocks", "swapped_seqs", "cached_blocks", "evictable_blocks",
+        "prefix_hit_tokens", "evictions")]
 
 
 class PagedAttnError(RuntimeError):
@@ -90,6 +91,9 @@ SIGNATURES = {
     "pa_pool_swap_out": (_i, [_vp, _i, _i64p, _i, C.POINTER(_i)]),
     "pa_pool_swap_in": (_i, [_vp, _i, _i64p, _i, C.POINTER(_i)]),
     "pa_pool_is_swapped": (_i, [_vp, _i, C.POINTER(_i)]),
+    "pa_pool_enable_prefix_cache": (_i, [_vp, _i]),
+    "pa_pool_new_seq_with_prompt": (_i, [_vp, _i32p, _i, C.POINTER(_i), C.POINTER(_i)]),
+    "pa_pool_append_token": (_i, [_vp, _i, C.c_int32, _i64p, _i64p, _i64p]),
 }
 
 _lib = None

@@ -11,8 +11,10 @@
 // generation reaches it) and 4.4 (copy a shared partly-filled block on write;
 // the last holder writes in place); "vLLM: treating the KV cache as virtual
 // memory", section 调度：词一级的进入与退出 (a preempted sequence's KV goes to
-// host memory block by block and comes back later) and "第 6 章 缓存管理",
-// section 缓存放不下的时候 (spill cold cache to CPU memory).
+// host memory block by block and comes back later; section 碎片从哪里来: the
+// prefix cache keeps hot prefixes outside the free list) and "第 6 章 缓存管理",
+// section 缓存放不下的时候 (spill cold cache to CPU memory; evict in
+// least-recently-used order and recompute on the next use).
 #include <algorithm>
 #include <cstdint>
 #include <unordered_map>
@@ -27,7 +29,26 @@ struct Seq {
   std::vector<int32_t> table;  // device blocks, or host blocks while swapped
   int64_t ctx = 0;
   bool swapped = false;
+  bool tokens_known = false;     // prefix cache: the token ids are tracked
+  std::vector<int32_t> tokens;
+  std::vector<uint64_t> hashes;  // key hash of each full block
 };
+
+// 64-bit FNV-1a over the parent hash (8 bytes, little-endian) and the token
+// ids (int32, little-endian): the prefix-cache key of a full block.
+uint64_t block_key_hash(uint64_t parent, const int32_t* tokens, int n) {
+  uint64_t h = 0xCBF29CE484222325ull;
+  auto mix = [&](uint8_t byte) {
+    h ^= byte;
+    h *= 0x100000001B3ull;
+  };
+  for (int i = 0; i < 8; ++i) mix(static_cast<uint8_t>(parent >> (8 * i)));
+  for (int t = 0; t < n; ++t) {
+    const uint32_t v = static_cast<uint32_t>(tokens[t]);
+    for (int i = 0; i < 4; ++i) mix(static_cast<uint8_t>(v >> (8 * i)));
+  }
+  return h;
+}
 
 }  // namespace
 
@@ -43,19 +64,64 @@ struct pa_pool {
   int64_t cow_copies = 0;
   int num_host_blocks = 0;
   std::vector<int32_t> host_free;   // top = back()
+  // prefix cache
+  bool prefix_cache = false;
+  std::unordered_map<uint64_t, int32_t> cache;  // key hash -> block
+  std::vector<uint8_t> keyed;
+  std::vector<uint64_t> key_hash;
+  std::vector<int32_t> key_parent;
+  std::vector<int32_t> key_tokens;              // block_size ids per block
+  // evictable keyed blocks, least recently used at the head
+  std::vector<int32_t> lru_prev, lru_next;
+  std::vector<uint8_t> in_lru;
+  int32_t lru_head = -1, lru_tail = -1;
+  int64_t lru_size = 0, hit_tokens = 0, evictions = 0;
 
+  int64_t available() const { return static_cast<int64_t>(free_stack.size()) + lru_size; }
+  void lru_push(int32_t b) {
+    lru_prev[b] = lru_tail;
+    lru_next[b] = -1;
+    if (lru_tail >= 0) lru_next[lru_tail] = b;
+    else lru_head = b;
+    lru_tail = b;
+    in_lru[b] = 1;
+    ++lru_size;
+  }
+  void lru_remove(int32_t b) {
+    if (lru_prev[b] >= 0) lru_next[lru_prev[b]] = lru_next[b];
+    else lru_head = lru_next[b];
+    if (lru_next[b] >= 0) lru_prev[lru_next[b]] = lru_prev[b];
+    else lru_tail = lru_prev[b];
+    in_lru[b] = 0;
+    --lru_size;
+  }
+  // caller checks available() > 0 first
   int32_t alloc() {
-    int32_t b = free_stack.back();
-    free_stack.pop_back();
-    on_free[b] = 0;
+    int32_t b;
+    if (!free_stack.empty()) {
+      b = free_stack.back();
+      free_stack.pop_back();
+      on_free[b] = 0;
+    } else {
+      b = lru_head;  // least recently used cached block: drop its key
+      lru_remove(b);
+      cache.erase(key_hash[b]);
+      keyed[b] = 0;
+      ++evictions;
+    }
     refcount[b] = 1;
     return b;
   }
-  void release(int32_t b) {
-    if (--refcount[b] == 0 && !pinned[b]) {
+  void to_idle(int32_t b) {
+    if (keyed[b]) {
+      lru_push(b);
+    } else {
       free_stack.push_back(b);
       on_free[b] = 1;
     }
+  }
+  void release(int32_t b) {
+    if (--refcount[b] == 0 && !pinned[b]) to_idle(b);
   }
   Seq* find(int id) {
     auto it = seqs.find(id);
@@ -94,6 +160,13 @@ PA_API int pa_pool_create(int num_blocks, int block_size, const int32_t* initial
   p->refcount.assign(num_blocks, 0);
   p->pinned.assign(num_blocks, 0);
   p->on_free.assign(num_blocks, 0);
+  p->keyed.assign(num_blocks, 0);
+  p->key_hash.assign(num_blocks, 0);
+  p->key_parent.assign(num_blocks, -1);
+  p->key_tokens.assign(size_t(num_blocks) * block_size, 0);
+  p->lru_prev.assign(num_blocks, -1);
+  p->lru_next.assign(num_blocks, -1);
+  p->in_lru.assign(num_blocks, 0);
   p->free_stack.resize(num_blocks);
   for (int i = 0; i < num_blocks; ++i) {
     int32_t b = initial_order ? initial_order[i] : i;
@@ -133,13 +206,13 @@ PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* c
   int64_t src = -1, dst = -1;
   int32_t block;
   if (offset == 0) {
-    if (pool->free_stack.empty()) return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_append_slot: pool exhausted");
+    if (pool->available() == 0) return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_append_slot: pool exhausted");
     block = pool->alloc();
     s->table.push_back(block);
   } else {
     block = s->table[logical];
     if (pool->refcount[block] > 1) {
-      if (pool->free_stack.empty())
+      if (pool->available() == 0)
         return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_append_slot: pool exhausted (copy-on-write)");
       int32_t fresh = pool->alloc();
       pool->refcount[block] -= 1;  // stays >= 1: another holder remains
@@ -151,9 +224,87 @@ PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* c
     }
   }
   s->ctx += 1;
+  s->tokens_known = false;  // the content of the new slot is unknown
   *slot = static_cast<int64_t>(block) * pool->block_size + offset;
   *cow_src = src;
   *cow_dst = dst;
+  return PA_OK;
+}
+
+PA_API int pa_pool_enable_prefix_cache(pa_pool* pool, int on) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_enable_prefix_cache: NULL pool");
+  if (!pool->seqs.empty() || pool->next_id != 0)
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_enable_prefix_cache: enable before the first sequence");
+  pool->prefix_cache = on != 0;
+  return PA_OK;
+}
+
+PA_API int pa_pool_new_seq_with_prompt(pa_pool* pool, const int32_t* tokens, int n, int* seq_id,
+                                       int* hit_tokens) {
+  if (!pool || !seq_id || !hit_tokens || n < 0 || (n > 0 && !tokens))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_new_seq_with_prompt: bad argument");
+  Seq s;
+  s.tokens_known = true;
+  const int bs = pool->block_size;
+  if (pool->prefix_cache && n > 0) {
+    const int limit = (n - 1) / bs;  // leave at least one token to compute
+    uint64_t parent_hash = 0;
+    int32_t parent_block = -1;
+    for (int i = 0; i < limit; ++i) {
+      const int32_t* chunk = tokens + size_t(i) * bs;
+      const uint64_t h = block_key_hash(parent_hash, chunk, bs);
+      auto it = pool->cache.find(h);
+      if (it == pool->cache.end()) break;
+      const int32_t b = it->second;
+      if (pool->key_parent[b] != parent_block ||
+          !std::equal(chunk, chunk + bs, pool->key_tokens.begin() + size_t(b) * bs))
+        break;
+      if (pool->refcount[b] == 0 && pool->in_lru[b]) pool->lru_remove(b);
+      pool->refcount[b] += 1;
+      s.table.push_back(b);
+      s.hashes.push_back(h);
+      s.tokens.insert(s.tokens.end(), chunk, chunk + bs);
+      s.ctx += bs;
+      parent_hash = h;
+      parent_block = b;
+    }
+  }
+  pool->hit_tokens += s.ctx;
+  *hit_tokens = static_cast<int>(s.ctx);
+  *seq_id = pool->next_id;
+  pool->seqs.emplace(pool->next_id, std::move(s));
+  pool->next_id++;
+  return PA_OK;
+}
+
+PA_API int pa_pool_append_token(pa_pool* pool, int seq, int32_t token, int64_t* slot,
+                                int64_t* cow_src, int64_t* cow_dst) {
+  if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_token: NULL pool");
+  int rc = PA_OK;
+  Seq* s = resident(pool, seq, "pa_pool_append_token", &rc);
+  if (!s) return rc;
+  const bool known = s->tokens_known;
+  rc = pa_pool_append_slot(pool, seq, slot, cow_src, cow_dst);
+  if (rc != PA_OK || !known) return rc;
+  s->tokens_known = true;
+  s->tokens.push_back(token);
+  const int bs = pool->block_size;
+  if (pool->prefix_cache && s->ctx % bs == 0) {
+    const int64_t i = s->ctx / bs - 1;
+    const uint64_t parent_hash = i > 0 ? s->hashes[i - 1] : 0;
+    const int32_t parent_block = i > 0 ? s->table[i - 1] : -1;
+    const int32_t* chunk = s->tokens.data() + size_t(i) * bs;
+    const uint64_t h = block_key_hash(parent_hash, chunk, bs);
+    s->hashes.push_back(h);
+    const int32_t b = s->table[i];
+    if (!pool->cache.count(h) && !pool->keyed[b]) {
+      pool->cache.emplace(h, b);
+      pool->keyed[b] = 1;
+      pool->key_hash[b] = h;
+      pool->key_parent[b] = parent_block;
+      std::copy(chunk, chunk + bs, pool->key_tokens.begin() + size_t(b) * bs);
+    }
+  }
   return PA_OK;
 }
 
@@ -191,6 +342,9 @@ PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child) {
   Seq c;
   c.table = p->table;
   c.ctx = p->ctx;
+  c.tokens_known = p->tokens_known;
+  c.tokens = p->tokens;
+  c.hashes = p->hashes;
   for (int32_t b : c.table) pool->refcount[b] += 1;
   *child = pool->next_id;
   pool->seqs.emplace(pool->next_id, std::move(c));
@@ -212,6 +366,11 @@ PA_API int pa_pool_share_prefix(pa_pool* pool, int src_seq, int dst_seq, int num
   const int64_t count = (num_tokens + pool->block_size - 1) / pool->block_size;
   dst->table.assign(src->table.begin(), src->table.begin() + count);
   dst->ctx = num_tokens;
+  dst->tokens_known = src->tokens_known;
+  const size_t nt = src->tokens_known ? std::min(src->tokens.size(), size_t(num_tokens)) : 0;
+  dst->tokens.assign(src->tokens.begin(), src->tokens.begin() + nt);
+  const size_t nh = std::min(src->hashes.size(), size_t(num_tokens / pool->block_size));
+  dst->hashes.assign(src->hashes.begin(), src->hashes.begin() + nh);
   for (int32_t b : dst->table) pool->refcount[b] += 1;
   return PA_OK;
 }
@@ -233,10 +392,7 @@ PA_API int pa_pool_unpin(pa_pool* pool, int block) {
   if (block < 0 || block >= pool->num_blocks || !pool->pinned[block])
     return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_unpin: block is not pinned");
   pool->pinned[block] = 0;
-  if (pool->refcount[block] == 0) {
-    pool->free_stack.push_back(block);
-    pool->on_free[block] = 1;
-  }
+  if (pool->refcount[block] == 0) pool->to_idle(block);
   return PA_OK;
 }
 
@@ -311,7 +467,7 @@ PA_API int pa_pool_swap_in(pa_pool* pool, int seq, int64_t* pairs, int cap, int*
   if (!s->swapped) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_in: sequence is not swapped out");
   const int len = static_cast<int>(s->table.size());
   if (len > cap) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_swap_in: pair buffer too small");
-  if (len > static_cast<int>(pool->free_stack.size()))
+  if (len > pool->available())
     return pa::fail(PA_ERR_NO_BLOCKS, "pa_pool_swap_in: pool exhausted");
   std::vector<int32_t> dev(len);
   for (int i = 0; i < len; ++i) {
@@ -368,6 +524,10 @@ PA_API int pa_pool_stats(pa_pool* pool, pa_pool_stats_t* st) {
   st->cow_copies = pool->cow_copies;
   st->live_seqs = static_cast<int64_t>(pool->seqs.size());
   st->tokens = st->internal_frag_slots = 0;
+  st->cached_blocks = static_cast<int64_t>(pool->cache.size());
+  st->evictable_blocks = pool->lru_size;
+  st->prefix_hit_tokens = pool->hit_tokens;
+  st->evictions = pool->evictions;
   st->host_blocks = pool->num_host_blocks;
   st->host_free_blocks = static_cast<int64_t>(pool->host_free.size());
   st->swapped_seqs = 0;

@@ -86,6 +86,29 @@ class BlockPool:
                                                  n.value, C.byref(n), C.byref(ctx)))
         return buf[:n.value].tolist(), ctx.value
 
+    def enable_prefix_cache(self, on: bool = True) -> None:
+        """Key full blocks by content so later prompts reuse them (before the
+        first sequence)."""
+        capi.check(self._lib.pa_pool_enable_prefix_cache(self._h, int(bool(on))))
+
+    def new_seq_with_prompt(self, tokens) -> tuple[int, int]:
+        """New sequence for a prompt: returns ``(seq, hit_tokens)``; the first
+        ``hit_tokens`` tokens are served by cached blocks, the caller appends
+        the rest with :meth:`append_token`."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        seq, hit = C.c_int(), C.c_int()
+        capi.check(self._lib.pa_pool_new_seq_with_prompt(
+            self._h, toks.ctypes.data_as(C.POINTER(C.c_int32)), toks.shape[0], C.byref(seq),
+            C.byref(hit)))
+        return seq.value, hit.value
+
+    def append_token(self, seq: int, token: int):
+        """:meth:`append_slot` for a known token id (keys the block it fills)."""
+        slot, src, dst = C.c_int64(), C.c_int64(), C.c_int64()
+        capi.check(self._lib.pa_pool_append_token(self._h, seq, int(token), C.byref(slot),
+                                                  C.byref(src), C.byref(dst)))
+        return slot.value, (None if src.value < 0 else (src.value, dst.value))
+
     def set_host_blocks(self, num_host_blocks: int, initial_order=None) -> None:
         """Give the pool a host tier (swap space) of ``num_host_blocks`` blocks."""
         order = None

@@ -283,3 +283,100 @@ def test_swap_refuses_shared_and_pinned_blocks():
             op()
     pool.free_seq(c)                             # host block goes back
     assert pool.stats()["host_free_blocks"] == 10
+
+
+# ------------------------------------------------------------- prefix cache
+def test_fnv1a64_published_vectors():
+    """The hash the prefix cache keys blocks with, against the FNV-1a 64-bit
+    test vectors of its authors."""
+    from oracle.pool import fnv1a64
+    assert fnv1a64(b"") == 0xCBF29CE484222325
+    assert fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert fnv1a64(b"foobar") == 0x85944171F73967E8
+
+
+def _prompt_pool(num_blocks=64):
+    pool = BlockPool(num_blocks, 16)
+    pool.enable_prefix_cache()
+    return pool
+
+
+def _run_prompt(pool, tokens):
+    seq, hit = pool.new_seq_with_prompt(tokens)
+    for t in tokens[hit:]:
+        pool.append_token(seq, t)
+    return seq, hit
+
+
+def test_prefix_cache_share_200_of_500():
+    """Page 4, section "块表长什么样": a 500-token request, then one whose first
+    200 tokens are the same.  Content-keyed caching serves the 12 full shared
+    blocks (192 tokens); the 13th, partly shared block is recomputed (sharing
+    it as a partial block is what share_prefix does instead)."""
+    pool = _prompt_pool()
+    system = list(range(1000, 1200))
+    first = system + list(range(300))
+    s1, hit1 = _run_prompt(pool, first)
+    assert hit1 == 0 and len(pool.block_table(s1)[0]) == 32
+    second = system + list(range(5000, 5100))
+    s2, hit2 = _run_prompt(pool, second)
+    assert hit2 == 192
+    t1, t2 = pool.block_table(s1)[0], pool.block_table(s2)[0]
+    assert t2[:12] == t1[:12] and t2[12] != t1[12]
+    assert all(pool.refcount[b] == 2 for b in t1[:12])
+    assert pool.stats()["prefix_hit_tokens"] == 192
+
+
+def test_prefix_cache_hot_system_prompt_survives_its_request():
+    """Page 2, section "碎片从哪里来": the prefix cache keeps a hot prefix
+    outside the free list, so the next request with the same system prompt
+    hits it even after the first one finished."""
+    pool = _prompt_pool()
+    system = list(range(64))                     # 4 full blocks
+    a, _ = _run_prompt(pool, system + [7, 8, 9])
+    blocks = pool.block_table(a)[0][:4]
+    pool.free_seq(a)
+    assert all(pool.refcount[b] == 0 for b in blocks)
+    assert pool.stats()["evictable_blocks"] >= 4 and pool.stats()["cached_blocks"] >= 4
+    b, hit = _run_prompt(pool, system + [1, 2])
+    assert hit == 64 and pool.block_table(b)[0][:4] == blocks
+    # at least one token is always left to compute
+    c, hit_c = _run_prompt(pool, system)
+    assert hit_c == 48
+
+
+def test_prefix_cache_evicts_least_recently_used():
+    """Page 4, section "缓存放不下的时候": when memory is full, evict in
+    least-recently-used order."""
+    pool = _prompt_pool(num_blocks=9)
+    seqs = [_run_prompt(pool, [100 * p + i for i in range(33)])[0] for p in range(3)]
+    assert pool.stats()["free_blocks"] == 0 and pool.stats()["cached_blocks"] == 6
+    tables = [pool.block_table(s)[0] for s in seqs]
+    for s in (seqs[1], seqs[0], seqs[2]):        # each releases its blocks last to first
+        pool.free_seq(s)
+    # LRU order now: seq 1 block 1, seq 1 block 0, seq 0 block 1, ...; the
+    # three partial (unkeyed) blocks are on the free list
+    d = pool.new_seq()
+    for _ in range(4 * 16):                      # 3 free blocks, then one eviction
+        pool.append_slot(d)
+    assert pool.stats()["evictions"] == 1
+    assert tables[1][1] in pool.block_table(d)[0]
+    s0, hit0 = pool.new_seq_with_prompt([i for i in range(33)])
+    s1, hit1 = pool.new_seq_with_prompt([100 + i for i in range(33)])
+    assert hit0 == 32 and pool.block_table(s0)[0] == tables[0][:2]
+    assert hit1 == 16 and pool.block_table(s1)[0] == tables[1][:1]
+
+
+def test_prefix_cache_equal_hashes_do_not_alias(monkeypatch):
+    """Keys compare the parent block and the token ids as well as the hash, so
+    even a total hash collision never serves another prompt's blocks."""
+    import oracle.pool as op
+    monkeypatch.setattr(op, "block_key_hash", lambda parent, tokens: 42)
+    pool = _prompt_pool()
+    _run_prompt(pool, list(range(40)))
+    s, hit = _run_prompt(pool, list(range(500, 540)))
+    assert hit == 0
+    # only the first block could be keyed (a key is never duplicated), and it
+    # still serves the prompt that really owns it
+    s2, hit2 = _run_prompt(pool, list(range(40)))
+    assert hit2 == 16
