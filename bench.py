@@ -58,7 +58,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=["mha_7b", "gqa_8b", "prefill_8b", "swap_8b", "pool_churn"],
+                    choices=["mha_7b", "gqa_8b", "prefix_8b", "prefill_8b", "swap_8b",
+                             "pool_churn"],
                     default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,7 +84,43 @@ def make_batch(name: str, rank: int) -> wl.DecodeBatch:
         return wl.mha_7b(seed=wl.SEED_BASE + 2 + 100 * rank)
     if name == "prefill_8b":
         return wl.prefill_8b(seed=wl.SEED_BASE + 6 + 100 * rank)
+    if name == "prefix_8b":
+        return prefix_batch(wl.prefix_mix(seed=wl.SEED_BASE + 5 + 100 * rank))
     return wl.gqa_8b(seed=wl.SEED_BASE + 3 + 100 * rank)
+
+
+def prefix_batch(script) -> wl.DecodeBatch:
+    """The prefix-mix decode batch, tables from the native pool: one pinned
+    prefix sequence, then every request shares its blocks and appends its own
+    suffix (the request's newest token last)."""
+    import pagedattention_decode_attention_gb300 as pa
+    pool = pa.BlockPool(script.num_blocks, 16, script.initial_order)
+    root = pool.new_seq()
+    for _ in range(script.prefix_len):
+        pool.append_slot(root)
+    pool.pin(root, script.prefix_len)
+    seqs = []
+    for n in script.suffix_lens:
+        s = pool.new_seq()
+        pool.share_prefix(root, s, script.prefix_len)
+        for _ in range(int(n)):
+            pool.append_slot(s)
+        seqs.append(s)
+    max_blocks = max(len(pool.block_table(s)[0]) for s in seqs)
+    tables, lens = pool.tables(seqs, max_blocks)
+    return wl.DecodeBatch("prefix_8b_bf16", 32, 8, 128, "bf16", lens, tables, script.num_blocks,
+                          num_layers=script.num_layers, seed=script.seed)
+
+
+def unique_kv_bytes(batch: wl.DecodeBatch) -> int:
+    """K/V bytes of one call counting every physical block once (the tokens of
+    a block any sequence attends, at most 16)."""
+    used = {}
+    for b, ctx in enumerate(batch.context_lens):
+        for j in range((int(ctx) + 15) // 16):
+            blk = int(batch.block_tables[b, j])
+            used[blk] = max(used.get(blk, 0), min(16, int(ctx) - 16 * j))
+    return sum(used.values()) * 2 * batch.num_kv_heads * batch.head_dim * ELEM[batch.dtype]
 
 
 def prefill_flops(batch: wl.DecodeBatch) -> float:
@@ -620,6 +657,7 @@ def run_ours(args):
                 "parallelism": f"replicas x{world} (independent batches, no collective)",
             },
             "kv_read_gbs": ab["kv"] / (avg_ms / 1e3) / 1e9,
+            "kv_read_gbs_unique": unique_kv_bytes(batch) / (avg_ms / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_kind} hbm_gbs",
