@@ -210,6 +210,37 @@ PA_API int pa_paged_attention_decode_append_run(
     void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_shared_prefix -- pa_paged_attention_decode for a
+ * batch whose block tables all start with the same prefix_blocks blocks (a
+ * shared system prompt): the prefix's K/V are read once for all queries.
+ *
+ * "vLLM: treating the KV cache as virtual memory", section 碎片从哪里来 and
+ * "第 6 章 缓存管理", section 块表长什么样 (sequences sharing a prefix point
+ * their tables at the same physical blocks); the merge of the two parts is
+ * the same log-sum-exp reduction across blocks as the split merge ("KV
+ * 的体积从哪来，页表如何把它切开": reduce across blocks).  Reading the shared
+ * blocks once per batch instead of once per sequence is our extension.
+ *
+ * Same result and arguments as pa_paged_attention_decode, plus prefix_blocks
+ * (0 .. max_blocks_per_seq): every sequence's block_tables[b][0 ..
+ * prefix_blocks - 1] must equal row 0's and context_lens[b] >= prefix_blocks
+ * * 16 (a violation sets PA_ERR_DEVICE_BOUNDS; that sequence's output is then
+ * unspecified).  Three phases on `stream`: the prefix (all queries against
+ * the shared blocks, a CTA-shared K/V ring, tensor cores), each sequence's
+ * own blocks (the decode kernel), and a log-sum-exp merge.  Workspace:
+ * pa_paged_attention_decode_shared_prefix_workspace_size bytes.
+ * prefix_blocks == 0 or F32 runs a plain decode.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    size_t* bytes);
+PA_API int pa_paged_attention_decode_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_prefill -- chunked-prefill attention over the paged cache.
  *
  * OS-lab appendix, section 2.1 (prefill writes the K/V of every prompt token

@@ -8,7 +8,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
   table, MHA and GQA (:func:`paged_attention_decode_plan` +
   :func:`paged_attention_decode_run` split it so one plan serves every layer;
   :func:`paged_attention_decode_append_run` also appends each sequence's new
-  token in the same launch);
+  token in the same launch; :func:`paged_attention_decode_shared_prefix` reads
+  a prefix shared by the whole batch once);
 * :func:`paged_attention_prefill` -- chunked-prefill attention: each
   sequence's newest tokens attend causally over the paged cache;
 * :func:`block_copy` -- copy-on-write block copies across all layers;
@@ -24,7 +25,8 @@ from .capi import PagedAttnError  # noqa: F401
 from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
 from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
                   block_swap, check_status, kv_append, paged_attention_decode,
-                  paged_attention_decode_append_run, paged_attention_prefill,
+                  paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
+                  paged_attention_prefill, shared_prefix_workspace_size,
                   prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,
                   prepare_decode_append_run, prepare_decode_plan, prepare_decode_run,

@@ -60,6 +60,7 @@
 #include "decode.cuh"
 #include "device_common.cuh"
 #include "pagedattn.h"
+#include "prefill.h"
 #include "status.h"
 #include "tensor_map.h"
 
@@ -153,12 +154,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
   const int tid = threadIdx.x;
   if (tid < kSplitBlocks + 2) hist[tid] = 0;
   __syncthreads();
-  const int cap = p.max_blocks * kBlockSize;
+  const int cap = (p.max_blocks - p.table_offset) * kBlockSize;
   int4* units = reinterpret_cast<int4*>(p.ws.units);
 
   // pass 1: split sizes before any cut
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-    int ctx = p.context_lens[b];
+    int ctx = p.context_lens[b] - p.ctx_offset;
     if (ctx < 0 || ctx > cap) {
       dev::flag_status(p.status, kStatusBounds);
       ctx = ctx < 0 ? 0 : cap;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
 
   // pass 2: sizes of the final units (splits and pieces)
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-    int ctx = p.context_lens[b];
+    int ctx = p.context_lens[b] - p.ctx_offset;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
     split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
   // pass 3: place every unit of a sequence, in block order, into its size's
   // bucket: (b, first block, split index << 8 | blocks, context length)
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
-    int ctx = p.context_lens[b];
+    int ctx = p.context_lens[b] - p.ctx_offset;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
     int nsplit, base, big;
     split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
@@ -273,6 +274,8 @@ struct MergeArgs {
   const float* lse;   // part_lse at (b, split 0, head g G); split stride Hq
   const float4* po;   // part_o at the same row, as float4
   void* out;          // out row of head g G of sequence b
+  float* cas_o;       // suffix mode: fp32 o rows of head g G (else null)
+  float* cas_lse;     // suffix mode: base-2 log-sum-exp of head g G
   int G, Hq, nsplit;
 };
 
@@ -369,11 +372,27 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
     const int c = lane + 32 * k;
     if (c < C) {
       const float inv = 1.f / head_sum(k);
-      uint2 pk;
-      pk.x = M::pack(acc[k].x * inv, acc[k].y * inv);
-      pk.y = M::pack(acc[k].z * inv, acc[k].w * inv);
-      *reinterpret_cast<uint2*>(orow + 4 * c) = pk;
+      if (a.cas_o) {
+        *reinterpret_cast<float4*>(a.cas_o + 4 * c) =
+            make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
+      } else {
+        uint2 pk;
+        pk.x = M::pack(acc[k].x * inv, acc[k].y * inv);
+        pk.y = M::pack(acc[k].z * inv, acc[k].w * inv);
+        *reinterpret_cast<uint2*>(orow + 4 * c) = pk;
+      }
     }
+  }
+  if (a.cas_lse && lane < G) {
+    // lse of head `lane` = its largest lse plus log2 of its weight sum
+    float mh = hm[0], lh = hl[0];
+#pragma unroll
+    for (int hh = 1; hh < kMaxGroup; ++hh)
+      if (hh == lane) {
+        mh = hm[hh];
+        lh = hl[hh];
+      }
+    a.cas_lse[lane] = mh + log2f(lh);
   }
 }
 
@@ -459,10 +478,11 @@ __global__ void __launch_bounds__(W * 32)
       const int hg = x0 % p.num_kv_heads, n = u.z & 0xff;
       constexpr int kWarmBlocks = 4;
       if (u.x >= 0 && u.x < p.num_seqs && u.y >= 0 && n >= 1 && n <= kSplitBlocks &&
-          u.y + n <= p.max_blocks) {
+          p.table_offset + u.y + n <= p.max_blocks) {
         const int nb = n < kWarmBlocks ? n : kWarmBlocks;
         int phys = -1;
-        if (lane < nb) phys = p.block_tables[size_t(u.x) * p.max_blocks + u.y + lane];
+        if (lane < nb)
+          phys = p.block_tables[size_t(u.x) * p.max_blocks + p.table_offset + u.y + lane];
         for (int j = 0; j < nb; ++j) {
           const int pj = __shfl_sync(0xffffffffu, phys, j);
           if (pj < 0 || pj >= p.num_blocks) continue;
@@ -494,7 +514,11 @@ __global__ void __launch_bounds__(W * 32)
     // rows of empty sequences are zero; a new token of such a sequence is
     // still stored (it attends nothing)
     for (int b = blockIdx.x * 32 + lane; b < p.num_seqs; b += gridDim.x * 32) {
-      if (p.context_lens[b] <= 0) {
+      if (p.cas_o && p.context_lens[b] - p.ctx_offset <= 0) {
+        // suffix mode: nothing past the shared prefix (weight 0 in the merge)
+        for (int i = 0; i < Hq * D; ++i) p.cas_o[size_t(b) * Hq * D + i] = 0.f;
+        for (int h = 0; h < Hq; ++h) p.cas_lse[size_t(b) * Hq + h] = -INFINITY;
+      } else if (!p.cas_o && p.context_lens[b] <= 0) {
         uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
         for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
         const long long slot = fused ? p.slot_mapping[b] : -1;
@@ -563,7 +587,8 @@ __global__ void __launch_bounds__(W * 32)
       nxt.nsplit = __ldg(&p.ws.nsplits[nxt.b]);
       cslot = fused ? __ldg(&p.slot_mapping[nxt.b]) : -1;
       nxt.phys = lane < nxt.nblk
-                     ? __ldg(&p.block_tables[size_t(nxt.b) * p.max_blocks + nxt.first + lane])
+                     ? __ldg(&p.block_tables[size_t(nxt.b) * p.max_blocks + p.table_offset +
+                                             nxt.first + lane])
                      : 0;
       cstage = 3;
     } else if (cstage == 3) {
@@ -827,7 +852,25 @@ __global__ void __launch_bounds__(W * 32)
     const int n0 = 2 * (lane & 3), n1 = n0 + 1;
     const float inv0 = 1.f / l0, inv1 = 1.f / l1;
     const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-    if (nsplit == 1) {
+    if (nsplit == 1 && p.cas_o) {
+      float* crow = p.cas_o + head0 * D;
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) {
+        const int d0 = 16 * mt + (lane >> 2);
+        if (n0 < G) {
+          crow[n0 * D + d0] = o[mt][0] * inv0;
+          crow[n0 * D + d0 + 8] = o[mt][2] * inv0;
+        }
+        if (n1 < G) {
+          crow[n1 * D + d0] = o[mt][1] * inv1;
+          crow[n1 * D + d0 + 8] = o[mt][3] * inv1;
+        }
+      }
+      if (lane < 4) {
+        if (n0 < G) p.cas_lse[head0 + n0] = m0 + log2f(l0);
+        if (n1 < G) p.cas_lse[head0 + n1] = m1 + log2f(l1);
+      }
+    } else if (nsplit == 1) {
       T* orow = static_cast<T*>(p.out) + head0 * D;
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
@@ -877,6 +920,8 @@ __global__ void __launch_bounds__(W * 32)
         ma.lse = p.ws.part_lse + row0;
         ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
         ma.out = static_cast<T*>(p.out) + head0 * D;
+        ma.cas_o = p.cas_o ? p.cas_o + head0 * D : nullptr;
+        ma.cas_lse = p.cas_lse ? p.cas_lse + head0 : nullptr;
         ma.G = G;
         ma.Hq = Hq;
         ma.nsplit = nsplit;
@@ -950,6 +995,48 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const Params p) {
   float* out = static_cast<float*>(p.out) + (size_t(b) * p.num_q_heads + h) * D + lane * E;
 #pragma unroll
   for (int e = 0; e < E; ++e) out[e] = ctx > 0 ? acc[e] / l : 0.f;
+}
+
+}  // namespace decode
+}  // namespace pa
+
+namespace pa {
+namespace decode {
+
+// Last step of a shared-prefix decode: each (sequence, head) merges the
+// shared prefix's (o, lse) with its own suffix's by log-sum-exp weights
+// (base 2); a side empty of tokens has lse = -inf and weight 0.  Also checks
+// that every table starts with the shared prefix (row 0's entries).
+template <typename T, int D>
+__global__ void __launch_bounds__(256)
+    cascade_combine_kernel(const float* __restrict__ po, const float* __restrict__ plse,
+                           const float* __restrict__ so, const float* __restrict__ slse, T* out,
+                           int rows, const int32_t* __restrict__ block_tables, int prefix_blocks,
+                           int num_seqs, int max_blocks, unsigned* status) {
+  dev::grid_dependency_wait();
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  for (long long i = tid; i < (long long)num_seqs * prefix_blocks; i += nthreads) {
+    const long long b = i / prefix_blocks, j = i % prefix_blocks;
+    if (block_tables[b * max_blocks + j] != block_tables[j]) dev::flag_status(status, kStatusBounds);
+  }
+  using M = dev::Mma<T>;
+  const int lane = threadIdx.x & 31;
+  for (long long r = tid >> 5; r < rows; r += nthreads >> 5) {
+    const float lp = plse[r], ls = slse[r];
+    const float m = fmaxf(lp, ls);
+    const float wp = lp == -INFINITY ? 0.f : dev::fast_exp2(lp - m);
+    const float ws = ls == -INFINITY ? 0.f : dev::fast_exp2(ls - m);
+    const float inv = wp + ws > 0.f ? 1.f / (wp + ws) : 0.f;
+    for (int c = 4 * lane; c < D; c += 128) {
+      const float4 a = *reinterpret_cast<const float4*>(po + r * D + c);
+      const float4 b = *reinterpret_cast<const float4*>(so + r * D + c);
+      uint2 pk;
+      pk.x = M::pack((wp * a.x + ws * b.x) * inv, (wp * a.y + ws * b.y) * inv);
+      pk.y = M::pack((wp * a.z + ws * b.z) * inv, (wp * a.w + ws * b.w) * inv);
+      *reinterpret_cast<uint2*>(out + r * D + c) = pk;
+    }
+  }
 }
 
 }  // namespace decode
@@ -1136,9 +1223,25 @@ Params make_params(const int32_t* context_lens, int num_seqs, int num_q_heads, i
   return prm;
 }
 
+// Suffix mode of a shared-prefix decode (all zero / null: a plain decode).
+struct SuffixArgs {
+  int prefix_blocks = 0;
+  float* cas_o = nullptr;
+  float* cas_lse = nullptr;
+};
+
+void apply_suffix(Params& prm, const SuffixArgs& sfx) {
+  prm.table_offset = sfx.prefix_blocks;
+  prm.ctx_offset = sfx.prefix_blocks * kBlockSize;
+  prm.cas_o = sfx.cas_o;
+  prm.cas_lse = sfx.cas_lse;
+  prm.signature = plan_signature(prm.num_seqs, prm.num_q_heads, prm.num_kv_heads, prm.head_dim,
+                                 prm.max_blocks, prm.split_blocks, prm.table_offset);
+}
+
 int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
               int head_dim, int max_blocks_per_seq, void* workspace, size_t workspace_bytes,
-              cudaStream_t stream, const char* who) {
+              cudaStream_t stream, const char* who, const SuffixArgs& sfx = SuffixArgs()) {
   const Layout lay =
       workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
   int rc = check_workspace(workspace, workspace_bytes, lay, who);
@@ -1153,6 +1256,7 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   if (rc != PA_OK) return rc;
   Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                            max_blocks_per_seq, workspace, lay, status);
+  apply_suffix(prm, sfx);
   // the tail is sized for the math warps the attention kernel will launch
   const DeviceState& st = g_dev[device];
   const int nwarps = st.sms * st.cfg[1][head_dim == 128].ctas_per_sm * st.tuning.warps;
@@ -1189,7 +1293,8 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
              int head_dim, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
              void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
-             const char* who, const AppendArgs& app = AppendArgs()) {
+             const char* who, const AppendArgs& app = AppendArgs(),
+             const SuffixArgs& sfx = SuffixArgs()) {
   if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "%s: num_blocks must be positive", who);
   if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
     return fail(PA_ERR_INVALID_ARG, "%s: cache has too many rows", who);
@@ -1220,6 +1325,7 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
   prm.num_blocks = num_blocks;
   prm.scale = scale;
   prm.scale_log2 = scale * 1.4426950408889634f;
+  apply_suffix(prm, sfx);
 
   if (app.slot_mapping && dtype == PA_F32) {
     // the fp32 path is not fused: append first, then attend
@@ -1342,6 +1448,127 @@ PA_API int pa_paged_attention_decode_append_run(
   return run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                   num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who, app);
+}
+
+}  // extern "C"
+
+namespace {
+// Workspace of a shared-prefix decode: the suffix decode's, the prefix
+// phase's, then fp32 (o, lse) of both phases.
+struct SharedLayout {
+  size_t decode, prefix, po, plse, so, slse, total;
+};
+SharedLayout shared_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                           int max_blocks_per_seq) {
+  SharedLayout l;
+  const size_t rows = size_t(num_seqs) * num_q_heads;
+  l.decode = 0;
+  l.prefix = align256(
+      workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total);
+  l.po = align256(l.prefix + prefill::shared_prefix_workspace_bytes(num_seqs, num_q_heads,
+                                                                    num_kv_heads, head_dim));
+  l.plse = align256(l.po + rows * head_dim * 4);
+  l.so = align256(l.plse + rows * 4);
+  l.slse = align256(l.so + rows * head_dim * 4);
+  l.total = align256(l.slse + rows * 4);
+  return l;
+}
+}  // namespace
+
+extern "C" {
+
+PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    size_t* bytes) {
+  if (!bytes) return fail(PA_ERR_INVALID_ARG, "shared_prefix_workspace_size: bytes is NULL");
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_blocks_per_seq <= 0 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID_ARG, "shared_prefix_workspace_size: bad sizes");
+  *bytes = shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
+  return PA_OK;
+}
+
+PA_API int pa_paged_attention_decode_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_decode_shared_prefix";
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               dtype, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq)
+    return fail(PA_ERR_INVALID_ARG, "%s: prefix_blocks outside 0..max_blocks_per_seq", who);
+  const SharedLayout sl =
+      shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < sl.total)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace NULL, unaligned or < %zu bytes", who, sl.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (prefix_blocks == 0 || dtype == PA_F32) {
+    // nothing shared to exploit (or the fp32 path): a plain decode is exact
+    return pa_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
+                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                     num_blocks, scale, dtype, out, workspace, workspace_bytes,
+                                     stream);
+  }
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* po = reinterpret_cast<float*>(ws + sl.po);
+  float* plse = reinterpret_cast<float*>(ws + sl.plse);
+  float* so = reinterpret_cast<float*>(ws + sl.so);
+  float* slse = reinterpret_cast<float*>(ws + sl.slse);
+  // 1. the shared prefix, read once for all queries
+  rc = prefill::shared_prefix_phase(q, k_cache, v_cache, block_tables, prefix_blocks * kBlockSize,
+                                    num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                    max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
+                                    ws + sl.prefix, sl.po - sl.prefix, s);
+  if (rc != PA_OK) return rc;
+  // 2. every sequence's own blocks
+  SuffixArgs sfx;
+  sfx.prefix_blocks = prefix_blocks;
+  sfx.cas_o = so;
+  sfx.cas_lse = slse;
+  rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                 workspace, sl.prefix, s, who, sfx);
+  if (rc != PA_OK) return rc;
+  rc = run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                workspace, sl.prefix, s, who, AppendArgs(), sfx);
+  if (rc != PA_OK) return rc;
+  // 3. merge
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const int rows = num_seqs * num_q_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (dtype == PA_BF16)
+    e = head_dim == 128
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, po, plse, so,
+                                 slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
+                                 prefix_blocks, num_seqs, max_blocks_per_seq, status)
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, po, plse, so,
+                                 slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
+                                 prefix_blocks, num_seqs, max_blocks_per_seq, status);
+  else
+    e = head_dim == 128
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 128>, po, plse, so, slse,
+                                 static_cast<__half*>(out), rows, block_tables, prefix_blocks,
+                                 num_seqs, max_blocks_per_seq, status)
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 64>, po, plse, so, slse,
+                                 static_cast<__half*>(out), rows, block_tables, prefix_blocks,
+                                 num_seqs, max_blocks_per_seq, status);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
 }
 
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,

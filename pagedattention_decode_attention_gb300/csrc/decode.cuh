@@ -59,10 +59,10 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
 // Identifies the shapes a plan was made for, so a run can refuse a workspace
 // planned for something else.
 inline int plan_signature(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                          int max_blocks_per_seq, int split_blocks) {
+                          int max_blocks_per_seq, int split_blocks, int table_offset = 0) {
   uint32_t h = 2166136261u;
-  const int v[6] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                    split_blocks};
+  const int v[7] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                    split_blocks, table_offset};
   for (int x : v) {
     h ^= uint32_t(x);
     h *= 16777619u;
@@ -83,6 +83,13 @@ struct Params {
   const void* k_new;
   const void* v_new;
   const int64_t* slot_mapping;
+  // Suffix mode (cas_o non-null): each sequence attends only its tokens from
+  // ctx_offset on (table entries from table_offset on), and the results go
+  // to cas_o / cas_lse (fp32 o and base-2 log-sum-exp per (sequence, head))
+  // for a later merge with the shared prefix's, instead of out.
+  int table_offset, ctx_offset;
+  float* cas_o;      // [num_seqs * num_q_heads][head_dim]
+  float* cas_lse;    // [num_seqs * num_q_heads]
   int num_seqs, num_q_heads, num_kv_heads, group, head_dim;
   int max_blocks, num_blocks, max_splits;
   int stages;        // depth of the shared-memory tile ring (tensor-core path)

@@ -41,6 +41,7 @@
 
 #include "device_common.cuh"
 #include "pagedattn.h"
+#include "prefill.h"
 #include "status.h"
 #include "tensor_map.h"
 
@@ -55,6 +56,14 @@ constexpr int kMaxGroup = 8;         // query heads per KV head
 constexpr int kMinSplitBlocks = 16;  // smallest KV split
 constexpr int kPartialItems = 1024;  // (split unit, KV head) partial results, at most
 constexpr int kSizeBuckets = 32;     // work-list order: floor(log2(blocks)) buckets
+constexpr int kMaxSplits = 64;       // splits of one query block (the merge's weights fit the ring)
+
+// Splits of a query block of nb KV blocks at split size `split` (0: none).
+__host__ __device__ __forceinline__ int nsplits_of(int nb, int split) {
+  if (!split) return 1;
+  const int ns = (nb + split - 1) / split;
+  return ns < kMaxSplits ? ns : kMaxSplits;
+}
 
 // Workspace header words.
 constexpr int kHdrNext = 0, kHdrTotal = 1, kHdrDone = 2, kHdrSignature = 3;
@@ -73,6 +82,14 @@ struct Params {
   int units_cap;     // unit slots in the workspace
   int partial_cap;   // partial-result units in the workspace (per KV head)
   int signature;
+  // Shared-prefix mode (shared_ctx > 0): the batch's decode queries are the
+  // total_q "tokens" of one sequence (num_seqs = 1) whose K/V are the
+  // shared_ctx tokens of the shared prefix (block_tables row 0); every row
+  // attends all of them (no causal mask), and the results go to cas_o /
+  // cas_lse (fp32 o and base-2 log-sum-exp per (row, head)) instead of out.
+  int shared_ctx;
+  float* cas_o;      // [total_q * num_q_heads][head_dim]
+  float* cas_lse;    // [total_q * num_q_heads]
   float scale, scale_log2;
   int* header;
   int4* units;       // 2 x int4 per unit (see plan)
@@ -122,7 +139,9 @@ inline int signature_of(int num_seqs, int total_q, int num_q_heads, int num_kv_h
 // A query block qb of sequence b covers rows qb*64 .. of the sequence's
 // T_b * G rows; its last row's token sits at position ctx - T_b + i_last,
 // so it needs KV blocks 0 .. that position / 16.
-__device__ __forceinline__ int qblock_blocks(int ctx, int qlen, int group, int qb) {
+__device__ __forceinline__ int qblock_blocks(int ctx, int qlen, int group, int qb,
+                                             bool all_tokens = false) {
+  if (all_tokens) return (ctx + kBlockSize - 1) / kBlockSize;
   const int rows = qlen * group;
   const int last_row = min((qb + 1) * kRows, rows) - 1;
   const int pos = ctx - qlen + last_row / group;
@@ -153,7 +172,13 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   __syncthreads();
 
   // a sequence's chunk: (ctx, qlen), or qlen = 0 when its lengths are invalid
+  const bool shared = p.shared_ctx > 0;
   auto chunk = [&](int b, int& ctx, int& qlen) {
+    if (shared) {
+      ctx = p.shared_ctx <= cap ? p.shared_ctx : 0;
+      qlen = ctx > 0 ? p.total_q : 0;
+      return;
+    }
     ctx = p.context_lens[b];
     const int q0 = p.query_start[b], q1 = p.query_start[b + 1];
     qlen = q1 - q0;
@@ -169,7 +194,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + kRows - 1) / kRows;
     unsigned long long blocks = 0;
-    for (int qb = 0; qb < nq; ++qb) blocks += qblock_blocks(ctx, qlen, G, qb);
+    for (int qb = 0; qb < nq; ++qb) blocks += qblock_blocks(ctx, qlen, G, qb, shared);
     if (nq) {
       atomicAdd(&s_qblocks, nq);
       atomicAdd(&s_blocks, blocks);
@@ -200,7 +225,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     int split = 0;
     if (items < 2ll * p.ncta && s_qblocks > 0) {
       const long long want = (long long)s_blocks * p.num_kv_heads / (3ll * p.ncta) + 1;
-      split = int(std::max<long long>(kMinSplitBlocks, want));
+      // the shared-prefix phase has few, short rows: allow shorter splits
+      split = int(std::max<long long>(shared ? kMinSplitBlocks / 2 : kMinSplitBlocks, want));
     }
     s_split = split;
   }
@@ -215,7 +241,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       const int nq = (qlen * G + kRows - 1) / kRows;
       int units = 0;
       for (int qb = 0; qb < nq; ++qb) {
-        const int ns = (qblock_blocks(ctx, qlen, G, qb) + split - 1) / split;
+        const int ns = nsplits_of(qblock_blocks(ctx, qlen, G, qb, shared), split);
         if (ns > 1) units += ns;
       }
       if (units) atomicAdd(&s_split_units, units);
@@ -237,8 +263,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + kRows - 1) / kRows;
     for (int qb = 0; qb < nq; ++qb) {
-      const int nb = qblock_blocks(ctx, qlen, G, qb);
-      const int ns = split ? (nb + split - 1) / split : 1;
+      const int nb = qblock_blocks(ctx, qlen, G, qb, shared);
+      const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
       if (big) atomicAdd(&hist[size_bucket(base + 1)], big);
       if (ns - big) atomicAdd(&hist[size_bucket(base)], ns - big);
@@ -265,8 +291,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + kRows - 1) / kRows;
     for (int qb = 0; qb < nq; ++qb) {
-      const int nb = qblock_blocks(ctx, qlen, G, qb);
-      const int ns = split ? (nb + split - 1) / split : 1;
+      const int nb = qblock_blocks(ctx, qlen, G, qb, shared);
+      const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
       int slot = -1, grp = -1;
       if (ns > 1) {
@@ -337,6 +363,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 
   const unsigned long long tmo = p.timeout_ns;
   const int G = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const bool shared = p.shared_ctx > 0;
   const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
@@ -409,8 +436,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       it.slot = u1.y;
       it.grp = u1.z;
       it.ctx = u1.w;
-      it.q_first = p.query_start[it.b];
-      it.qlen = p.query_start[it.b + 1] - it.q_first;
+      it.q_first = shared ? 0 : p.query_start[it.b];
+      it.qlen = shared ? p.total_q : p.query_start[it.b + 1] - it.q_first;
     }
     // the ring's first blocks of this item
     tbl_base = -32;
@@ -424,8 +451,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     const int nrows = it.qlen * G;
     const int ra = row0 + gq, rb = ra + 8;
     const bool va = ra < nrows, vb = rb < nrows;
-    const int pos_a = va ? it.ctx - it.qlen + ra / G : -1;
-    const int pos_b = vb ? it.ctx - it.qlen + rb / G : -1;
+    const int pos_a = va ? (shared ? it.ctx - 1 : it.ctx - it.qlen + ra / G) : -1;
+    const int pos_b = vb ? (shared ? it.ctx - 1 : it.ctx - it.qlen + rb / G) : -1;
     const T* qa = static_cast<const T*>(p.q) +
                   (size_t(it.q_first + (va ? ra / G : 0)) * Hq + it.g * G + (va ? ra % G : 0)) * D;
     const T* qbp = static_cast<const T*>(p.q) +
@@ -555,7 +582,21 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     lb += __shfl_xor_sync(0xffffffffu, lb, 1);
     lb += __shfl_xor_sync(0xffffffffu, lb, 2);
     const float ia = la > 0.f ? 1.f / la : 0.f, ib = lb > 0.f ? 1.f / lb : 0.f;
-    if (it.ns == 1) {
+    if (it.ns == 1 && shared) {
+      // (row, head) index of the rows: token ra / G is the batch's sequence
+      const size_t ha = size_t(it.q_first + (va ? ra / G : 0)) * Hq + it.g * G + (va ? ra % G : 0);
+      const size_t hb = size_t(it.q_first + (vb ? rb / G : 0)) * Hq + it.g * G + (vb ? rb % G : 0);
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int c = nd * 8 + 2 * tq;
+        if (va) *reinterpret_cast<float2*>(p.cas_o + ha * D + c) = make_float2(o[nd][0] * ia, o[nd][1] * ia);
+        if (vb) *reinterpret_cast<float2*>(p.cas_o + hb * D + c) = make_float2(o[nd][2] * ib, o[nd][3] * ib);
+      }
+      if (tq == 0) {
+        if (va) p.cas_lse[ha] = la > 0.f ? ma + log2f(la) : -INFINITY;
+        if (vb) p.cas_lse[hb] = lb > 0.f ? mb + log2f(lb) : -INFINITY;
+      }
+    } else if (it.ns == 1) {
       T* oa = static_cast<T*>(p.out) +
               (size_t(it.q_first + (va ? ra / G : 0)) * Hq + it.g * G + (va ? ra % G : 0)) * D;
       T* ob = static_cast<T*>(p.out) +
@@ -587,37 +628,68 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
                   it.ns - 1;
       __syncthreads();
       if (*s_last) {
-        // each warp merges its own 16 rows; lane l owns columns 4l .. 4l + 3
-        for (int r = 0; r < 16; ++r) {
-          const int row = row0 + r;
-          if (row >= nrows) break;
-          if (4 * lane < D) {
-            float mrun = -INFINITY, lrun = 0.f;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp = 0; sp < it.ns; ++sp) {
-              const size_t rr = (size_t(it.slot + sp) * Hkv + it.g) * kRows + warp * 16 + r;
-              const float lse = __ldcg(&p.part_lse[rr]);
-              if (lse == -INFINITY) continue;
-              const float4 ov = __ldcg(reinterpret_cast<const float4*>(&p.part_o[rr * D + 4 * lane]));
-              const float mn = fmaxf(mrun, lse);
-              const float a = mrun == -INFINITY ? 0.f : dev::fast_exp2(mrun - mn);
-              const float w = dev::fast_exp2(lse - mn);
-              acc.x = acc.x * a + w * ov.x;
-              acc.y = acc.y * a + w * ov.y;
-              acc.z = acc.z * a + w * ov.z;
-              acc.w = acc.w * a + w * ov.w;
-              lrun = lrun * a + w;
-              mrun = mn;
-            }
-            const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
-            T* orow = static_cast<T*>(p.out) +
-                      (size_t(it.q_first + row / G) * Hq + it.g * G + row % G) * D + 4 * lane;
-            uint2 pk;
-            pk.x = M::pack(acc.x * inv, acc.y * inv);
-            pk.y = M::pack(acc.z * inv, acc.w * inv);
-            *reinterpret_cast<uint2*>(orow) = pk;
+        // The whole CTA merges the item's 64 rows.  Pass 1: one thread per row
+        // turns the splits' lse into weights, kept in the (now idle) ring.
+        float* wsm = reinterpret_cast<float*>(ring);  // [ns][kRows]
+        const size_t sbase = (size_t(it.slot) * Hkv + it.g) * kRows;  // split s adds s*Hkv*kRows
+        const size_t sstride = size_t(Hkv) * kRows;
+        if (threadIdx.x < kRows) {
+          const int r = threadIdx.x;
+          float mx = -INFINITY;
+          for (int sp = 0; sp < it.ns; ++sp)
+            mx = fmaxf(mx, __ldcg(&p.part_lse[sbase + sp * sstride + r]));
+          float sum = 0.f;
+          for (int sp = 0; sp < it.ns; ++sp) {
+            const float x = __ldcg(&p.part_lse[sbase + sp * sstride + r]);
+            const float w = x == -INFINITY ? 0.f : dev::fast_exp2(x - mx);
+            wsm[sp * kRows + r] = w;
+            sum += w;
+          }
+          const float inv = sum > 0.f ? 1.f / sum : 0.f;
+          for (int sp = 0; sp < it.ns; ++sp) wsm[sp * kRows + r] *= inv;
+          const int row = it.qb * kRows + r;
+          if (shared && row < nrows)
+            p.cas_lse[size_t(it.q_first + row / G) * Hq + it.g * G + row % G] =
+                sum > 0.f ? mx + log2f(sum) : -INFINITY;
+        }
+        __syncthreads();
+        // Pass 2: thread t owns float4 column t % C4 of rows t / C4 + k * RS;
+        // every split's loads for all its rows are in flight together.
+        constexpr int C4 = D / 4, RS = kWarps * 32 / C4, NR = kRows / RS;
+        const int c4 = threadIdx.x % C4, r0 = threadIdx.x / C4;
+        float4 acc[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < it.ns; ++sp) {
+          const float4* src = reinterpret_cast<const float4*>(p.part_o + (sbase + sp * sstride) * D);
+#pragma unroll
+          for (int k = 0; k < NR; ++k) {
+            const int r = r0 + k * RS;
+            const float w = wsm[sp * kRows + r];
+            const float4 v = __ldcg(src + size_t(r) * C4 + c4);
+            acc[k].x += w * v.x;
+            acc[k].y += w * v.y;
+            acc[k].z += w * v.z;
+            acc[k].w += w * v.w;
           }
         }
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+          const int row = it.qb * kRows + r0 + k * RS;
+          if (row >= nrows) continue;
+          const size_t hrow = size_t(it.q_first + row / G) * Hq + it.g * G + row % G;
+          if (shared) {
+            reinterpret_cast<float4*>(p.cas_o + hrow * D)[c4] = acc[k];
+          } else {
+            uint2 pk;
+            pk.x = M::pack(acc[k].x, acc[k].y);
+            pk.y = M::pack(acc[k].z, acc[k].w);
+            reinterpret_cast<uint2*>(static_cast<T*>(p.out) + hrow * D)[c4] = pk;
+          }
+        }
+        // the ring is a copy target again after this
+        dev::fence_proxy_async_smem();
+        __syncthreads();
         if (producer) p.arrivals[size_t(it.grp) * Hkv + it.g] = 0;  // ready for the next run
       }
     }
@@ -751,6 +823,9 @@ int device_setup(int device) {
   return PA_OK;
 }
 
+int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
+              cudaStream_t s, const char* who);
+
 int check_shapes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads, int head_dim,
                  int max_blocks_per_seq, int dtype, const char* who) {
   if (dtype != PA_F32 && dtype != PA_F16 && dtype != PA_BF16)
@@ -858,6 +933,24 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
     return PA_OK;
   }
 
+  return launch_tc(prm, lay, device, dtype, workspace, s, who);
+}
+
+}  // extern "C"
+
+namespace pa {
+namespace prefill {
+namespace {
+
+// Plan + tensor-core attention kernel for a filled-in Params (16-bit dtypes).
+int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
+              cudaStream_t s, const char* who) {
+  const int num_seqs = prm.num_seqs, total_q = prm.total_q, num_q_heads = prm.num_q_heads;
+  const int num_kv_heads = prm.num_kv_heads, head_dim = prm.head_dim;
+  const int max_blocks_per_seq = prm.max_blocks, num_blocks = prm.num_blocks;
+  const void* k_cache = prm.k_cache;
+  const void* v_cache = prm.v_cache;
+  int rc = PA_OK;
   const DeviceState& st = g_dev[device];
   const bool bf16 = dtype == PA_BF16;
   const int per_sm = st.ctas_per_sm[bf16][head_dim == 128];
@@ -866,7 +959,7 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
   prm.signature = signature_of(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
-                               max_blocks_per_seq);
+                               max_blocks_per_seq) ^ (prm.shared_ctx << 1);
   prm.header = reinterpret_cast<int*>(ws + lay.header);
   prm.units = reinterpret_cast<int4*>(ws + lay.units);
   prm.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
@@ -908,4 +1001,50 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
   return PA_OK;
 }
 
-}  // extern "C"
+}  // namespace
+
+size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim) {
+  return workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim).total;
+}
+
+int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int prefix_tokens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                        int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const char* who = "paged_attention_decode_shared_prefix (prefix)";
+  const Layout lay = workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim);
+  if (workspace_bytes < lay.total) return fail(PA_ERR_INVALID_ARG, "%s: workspace too small", who);
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
+  int rc = device_setup(device);
+  if (rc != PA_OK) return rc;
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  Params prm = {};
+  prm.q = q;
+  prm.k_cache = k_cache;
+  prm.v_cache = v_cache;
+  prm.block_tables = block_tables;
+  prm.num_seqs = 1;
+  prm.total_q = num_seqs;
+  prm.num_q_heads = num_q_heads;
+  prm.num_kv_heads = num_kv_heads;
+  prm.group = num_q_heads / num_kv_heads;
+  prm.head_dim = head_dim;
+  prm.max_blocks = max_blocks_per_seq;
+  prm.num_blocks = num_blocks;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  prm.status = status;
+  prm.timeout_ns = 1000000000ull;
+  prm.shared_ctx = prefix_tokens;
+  prm.cas_o = cas_o;
+  prm.cas_lse = cas_lse;
+  return launch_tc(prm, lay, device, dtype, workspace, stream, who);
+}
+
+}  // namespace prefill
+}  // namespace pa

@@ -1,0 +1,29 @@
+// Internal interface of the prefill engine used by other parts of the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace pa {
+namespace prefill {
+
+// Workspace bytes of the shared-prefix phase for a batch of num_seqs decode
+// queries.
+size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim);
+
+// Shared-prefix phase of a cascade decode: each of the num_seqs decode
+// queries q[b][h] attends all prefix_tokens tokens of the prefix whose blocks
+// are block_tables[0][0 ..] (no causal mask); writes fp32 o and the base-2
+// log-sum-exp per (sequence, head) to cas_o / cas_lse.  Two launches (plan +
+// kernel) on `stream`.  Returns a pa_status.  16-bit dtypes only.
+int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int prefix_tokens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                        int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace prefill
+}  // namespace pa

@@ -268,6 +268,38 @@ def prepare_decode_append_run(q, k_new, v_new, slot_mapping, k_cache, v_cache, b
                      workspace, out))
 
 
+def shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                 head_dim: int, max_blocks_per_seq: int) -> int:
+    n = C.c_size_t(0)
+    capi.check(capi.lib().pa_paged_attention_decode_shared_prefix_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, C.byref(n)))
+    return n.value
+
+
+def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens,
+                                         prefix_blocks: int, scale: float, out=None,
+                                         workspace=None, stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode` for a batch whose tables all start with
+    the same ``prefix_blocks`` blocks: the shared blocks are read once for all
+    queries, each sequence's own blocks by the decode kernel, then the two
+    parts are merged."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        n = shared_prefix_workspace_size(b, hq, hkv, d, mb)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_shared_prefix(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), int(prefix_blocks), b, hq, hkv, d, mb, nb, float(scale),
+        _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return out
+
+
 def prefill_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,
                            head_dim: int) -> int:
     n = C.c_size_t(0)
