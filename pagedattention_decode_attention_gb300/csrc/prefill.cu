@@ -36,12 +36,14 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 #include <type_traits>
 
 #include "device_common.cuh"
 #include "pagedattn.h"
 #include "prefill.h"
+#include "tc05.cuh"
 #include "status.h"
 #include "tensor_map.h"
 
@@ -88,6 +90,7 @@ struct Params {
   // attends all of them (no causal mask), and the results go to cas_o /
   // cas_lse (fp32 o and base-2 log-sum-exp per (row, head)) instead of out.
   int shared_ctx;
+  int no_split;      // plan: never split a unit's KV range (tcgen05 kernel)
   float* cas_o;      // [total_q * num_q_heads][head_dim]
   float* cas_lse;    // [total_q * num_q_heads]
   float scale, scale_log2;
@@ -139,11 +142,12 @@ inline int signature_of(int num_seqs, int total_q, int num_q_heads, int num_kv_h
 // A query block qb of sequence b covers rows qb*64 .. of the sequence's
 // T_b * G rows; its last row's token sits at position ctx - T_b + i_last,
 // so it needs KV blocks 0 .. that position / 16.
+template <int ROWS = kRows>
 __device__ __forceinline__ int qblock_blocks(int ctx, int qlen, int group, int qb,
                                              bool all_tokens = false) {
   if (all_tokens) return (ctx + kBlockSize - 1) / kBlockSize;
   const int rows = qlen * group;
-  const int last_row = min((qb + 1) * kRows, rows) - 1;
+  const int last_row = min((qb + 1) * ROWS, rows) - 1;
   const int pos = ctx - qlen + last_row / group;
   return pos / kBlockSize + 1;
 }
@@ -152,6 +156,9 @@ __device__ __forceinline__ int size_bucket(int n) { return 31 - __clz(n); }  // 
 
 constexpr int kPlanThreads = 256;
 
+// ROWS: query rows per unit (64 for the mma.sync kernel, 128 for the
+// tcgen05 one, which never splits: p.no_split).
+template <int ROWS>
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params p) {
   __shared__ unsigned long long s_blocks;
   __shared__ int s_qblocks, s_split_units, s_split, s_slot, s_group;
@@ -192,9 +199,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx, qlen;
     chunk(b, ctx, qlen);
-    const int nq = (qlen * G + kRows - 1) / kRows;
+    const int nq = (qlen * G + ROWS - 1) / ROWS;
     unsigned long long blocks = 0;
-    for (int qb = 0; qb < nq; ++qb) blocks += qblock_blocks(ctx, qlen, G, qb, shared);
+    for (int qb = 0; qb < nq; ++qb) blocks += qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
     if (nq) {
       atomicAdd(&s_qblocks, nq);
       atomicAdd(&s_blocks, blocks);
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   if (tid == 0) {
     const long long items = (long long)s_qblocks * p.num_kv_heads;
     int split = 0;
-    if (items < 2ll * p.ncta && s_qblocks > 0) {
+    if (!p.no_split && items < 2ll * p.ncta && s_qblocks > 0) {
       const long long want = (long long)s_blocks * p.num_kv_heads / (3ll * p.ncta) + 1;
       // the shared-prefix phase has few, short rows: allow shorter splits
       split = int(std::max<long long>(shared ? kMinSplitBlocks / 2 : kMinSplitBlocks, want));
@@ -238,10 +245,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
       int ctx, qlen;
       chunk(b, ctx, qlen);
-      const int nq = (qlen * G + kRows - 1) / kRows;
+      const int nq = (qlen * G + ROWS - 1) / ROWS;
       int units = 0;
       for (int qb = 0; qb < nq; ++qb) {
-        const int ns = nsplits_of(qblock_blocks(ctx, qlen, G, qb, shared), split);
+        const int ns = nsplits_of(qblock_blocks<ROWS>(ctx, qlen, G, qb, shared), split);
         if (ns > 1) units += ns;
       }
       if (units) atomicAdd(&s_split_units, units);
@@ -261,9 +268,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx, qlen;
     chunk(b, ctx, qlen);
-    const int nq = (qlen * G + kRows - 1) / kRows;
+    const int nq = (qlen * G + ROWS - 1) / ROWS;
     for (int qb = 0; qb < nq; ++qb) {
-      const int nb = qblock_blocks(ctx, qlen, G, qb, shared);
+      const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
       const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
       if (big) atomicAdd(&hist[size_bucket(base + 1)], big);
@@ -289,9 +296,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx, qlen;
     chunk(b, ctx, qlen);
-    const int nq = (qlen * G + kRows - 1) / kRows;
+    const int nq = (qlen * G + ROWS - 1) / ROWS;
     for (int qb = 0; qb < nq; ++qb) {
-      const int nb = qblock_blocks(ctx, qlen, G, qb, shared);
+      const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
       const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
       int slot = -1, grp = -1;
@@ -712,6 +719,380 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   }
 }
 
+// ------------------------------------------------------- tcgen05 path (d = 128)
+// A CTA takes 128-row query tiles (rows = tokens x the group's heads, as
+// above) and streams their causal KV range in tiles of 128 tokens (8 paged
+// blocks) through a 2-stage ring.  One thread of warp 4 issues the TMA copies
+// and the 5th-generation tensor-core MMAs:
+//   S  = Q K^T   (M 128 rows, N 128 tokens, K 128; fp32 accumulator in TMEM)
+//   O += P V     (M 128 rows, N 128 = head_dim, K 128 tokens; O in TMEM)
+// Warps 0-3 run the softmax, one thread per row (its TMEM lane): S is read
+// from TMEM, masked (causal, context), exponentiated in base 2 against a
+// reference that moves only when a row's maximum grows by more than 2^8 (the
+// O rescale then happens in TMEM; the result is exact either way), and P is
+// written to shared memory in the 128-byte-swizzled K-major layout the MMA
+// reads.  V is the MMA's N-contiguous B operand, straight from the TMA tile.
+constexpr int kTcRows = 128;       // query rows per tile (TMEM lanes)
+constexpr int kTcTokens = 128;     // tokens per KV tile
+constexpr int kTcBlocks = kTcTokens / kBlockSize;
+constexpr int kTcThreads = 160;    // 4 softmax warps + 1 issue warp
+constexpr uint32_t kTcCols = 256;  // TMEM columns: S at 0, O at 128
+constexpr float kTcRescale = 8.f;  // log2 of the growth that forces an O rescale
+
+struct TcSmem {  // head_dim 128, 16-bit: every chunk is [128 rows][128 bytes]
+  static constexpr int kChunk = kTcRows * 128;            // 16 KB
+  static constexpr int kQ = 0;                            // 2 chunks (d 0-63, 64-127)
+  static constexpr int kK = 2 * kChunk;                   // [2 stages][2 chunks]
+  static constexpr int kV = kK + 4 * kChunk;              // [2 stages][2 chunks]
+  static constexpr int kP = kV + 4 * kChunk;              // 2 chunks (tokens 0-63, 64-127)
+  static constexpr int kBars = kP + 2 * kChunk;           // mbarriers
+  static constexpr int kBytes = kBars + 128 + 1024;       // + scalars, alignment slack
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                      const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  constexpr int D = 128;
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  using M = dev::Mma<T>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcSmem::kBars);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_full = bars + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
+  int* s_claim = reinterpret_cast<int*>(bars + 9);
+  const uint32_t sbase = dev::smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool issuer = warp == 4 && lane == 0;
+  if (issuer) {
+    dev::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      dev::mbar_init(&kv_full[i], 1);
+      dev::mbar_init(&kv_empty[i], 1);
+    }
+    dev::mbar_init(s_full, 1);
+    dev::mbar_init(p_full, kTcRows);
+    dev::mbar_init(o_full, 1);
+    dev::mbar_fence_init();
+    dev::prefetch_tensormap(&tmap_q);
+    dev::prefetch_tensormap(&tmap_k);
+    dev::prefetch_tensormap(&tmap_v);
+  }
+  if (warp == 4) dev::tmem_alloc(tmem_slot, kTcCols);
+  dev::tc_fence_before_sync();
+  __syncthreads();
+  dev::tc_fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();
+
+  const unsigned long long tmo = p.timeout_ns;
+  const int G = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+  const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
+  if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+  const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
+  const uint64_t policy = dev::l2_policy_evict_first();
+  const uint32_t idesc_s = dev::mma_idesc_f16(kBf16, kTcRows, kTcTokens, false);
+  const uint32_t idesc_o = dev::mma_idesc_f16(kBf16, kTcRows, D, true);
+  // phase counters, the same in every thread that uses them
+  int kv_tiles = 0;  // KV tiles through the ring so far
+  int q_loads = 0, s_count = 0, p_count = 0, o_count = 0;
+  bool ok = true;
+  bool first_claim = true;
+
+  for (;;) {
+    if (threadIdx.x == 0)
+      *s_claim = first_claim ? int(blockIdx.x) : int(gridDim.x) + atomicAdd(&p.header[kHdrNext], 1);
+    first_claim = false;
+    __syncthreads();
+    const int x = *s_claim;
+    __syncthreads();
+    if (x >= total) break;
+    const int4 u0 = p.units[2 * (x / Hkv)], u1 = p.units[2 * (x / Hkv) + 1];
+    const int g = x % Hkv, b = u0.x, qt = u0.y, nblk = u0.w, ctx = u1.w;
+    const int q_first = p.query_start[b];
+    const int qlen = p.query_start[b + 1] - q_first;
+    const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
+    const int tok0 = qt * (kTcRows / G);  // first query token of the tile in the chunk
+
+    if (warp == 4) {
+      // ---------------------------------------------------- issue warp
+      // table entries, 32 at a time, one per lane
+      int tbl = 0, tbl_base = -32;
+      auto load_tile = [&](int j) -> bool {  // KV tile j into stage (kv_tiles + j) % 2
+        const int k = kv_tiles + j, st = k & 1;
+        const int nb = min(kTcBlocks, nblk - j * kTcBlocks);
+        bool good = true;
+        if (lane == 0 && k >= 2)
+          good = dev::mbar_wait_bounded(&kv_empty[st], ((k >> 1) - 1) & 1, tmo, p.status);
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) return false;
+        if (lane == 0) dev::mbar_arrive_expect_tx(&kv_full[st], uint32_t(nb) * 4 * 2048);
+        for (int jb = 0; jb < nb; ++jb) {
+          const int blk = j * kTcBlocks + jb;
+          if ((blk & ~31) != tbl_base) {
+            tbl_base = blk & ~31;
+            tbl = tbl_base + lane < nblk
+                      ? p.block_tables[size_t(b) * p.max_blocks + tbl_base + lane]
+                      : 0;
+            if (tbl < 0 || tbl >= p.num_blocks) {
+              dev::flag_status(p.status, kStatusBounds);
+              tbl = 0;
+            }
+          }
+          const int phys = __shfl_sync(0xffffffffu, tbl, blk & 31);
+          if (lane == 0) {
+            const int y = (phys * Hkv + g) * kBlockSize;
+            uint8_t* kd = smem + TcSmem::kK + st * 2 * TcSmem::kChunk + jb * 2048;
+            uint8_t* vd = smem + TcSmem::kV + st * 2 * TcSmem::kChunk + jb * 2048;
+            for (int h = 0; h < 2; ++h) {
+              dev::tma_load_2d(kd + h * TcSmem::kChunk, &tmap_k, h * 64, y, &kv_full[st], policy);
+              dev::tma_load_2d(vd + h * TcSmem::kChunk, &tmap_v, h * 64, y, &kv_full[st], policy);
+            }
+          }
+        }
+        return true;
+      };
+      // the query tile, then the first two KV tiles
+      if (lane == 0) {
+        dev::mbar_arrive_expect_tx(q_full, 2 * TcSmem::kChunk);
+        for (int h = 0; h < 2; ++h) {
+          const int zc = q_first + tok0;
+          asm volatile(
+              "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + TcSmem::kQ + h * TcSmem::kChunk),
+              "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(h * 64), "r"(g * G), "r"(zc),
+              "r"(dev::smem_u32(q_full))
+              : "memory");
+        }
+      }
+      for (int j = 0; j < ntiles && j < 2 && ok; ++j) ok = load_tile(j);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int k = kv_tiles + j, st = k & 1;
+        bool good = true;
+        if (lane == 0) {
+          good = dev::mbar_wait_bounded(&kv_full[st], (k >> 1) & 1, tmo, p.status);
+          if (good && j == 0) good = dev::mbar_wait_bounded(q_full, q_loads & 1, tmo, p.status);
+          if (good && j > 0) {
+            // P of the previous tile is ready: O += P V
+            good = dev::mbar_wait_bounded(p_full, (p_count + j - 1) & 1, tmo, p.status);
+            if (good) {
+              dev::tc_fence_after_sync();
+              const uint32_t vb = sbase + TcSmem::kV + ((k - 1) & 1) * 2 * TcSmem::kChunk;
+              for (int kk = 0; kk < kTcTokens / 16; ++kk) {
+                const uint64_t ad = dev::smem_desc_sw128(
+                    sbase + TcSmem::kP + (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = dev::smem_desc_sw128(vb + kk * 2048, TcSmem::kChunk, 1024);
+                dev::tc_mma_f16(tmem + 128, ad, bd, idesc_o, j > 1 || kk > 0);
+              }
+              dev::tc_commit(&kv_empty[(k - 1) & 1]);
+            }
+          }
+          if (good) {
+            // S = Q K^T for this tile
+            dev::tc_fence_after_sync();
+            const uint32_t kb = sbase + TcSmem::kK + st * 2 * TcSmem::kChunk;
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32;
+              const uint64_t ad = dev::smem_desc_sw128(sbase + TcSmem::kQ + off, 16, 1024);
+              const uint64_t bd = dev::smem_desc_sw128(kb + off, 16, 1024);
+              dev::tc_mma_f16(tmem + 0, ad, bd, idesc_s, kk > 0);
+            }
+            dev::tc_commit(s_full);
+          }
+        }
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) {
+          ok = false;
+          break;
+        }
+        // the stage of the previous tile is released by that tile's P V: refill it
+        if (j >= 1 && j + 1 < ntiles) ok = load_tile(j + 1);
+      }
+      if (ok && lane == 0) {
+        // the last tile's O += P V
+        const int k = kv_tiles + ntiles - 1;
+        bool good = dev::mbar_wait_bounded(p_full, (p_count + ntiles - 1) & 1, tmo, p.status);
+        if (good) {
+          dev::tc_fence_after_sync();
+          const uint32_t vb = sbase + TcSmem::kV + (k & 1) * 2 * TcSmem::kChunk;
+          for (int kk = 0; kk < kTcTokens / 16; ++kk) {
+            const uint64_t ad = dev::smem_desc_sw128(
+                sbase + TcSmem::kP + (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32, 16, 1024);
+            const uint64_t bd = dev::smem_desc_sw128(vb + kk * 2048, TcSmem::kChunk, 1024);
+            dev::tc_mma_f16(tmem + 128, ad, bd, idesc_o, ntiles > 1 || kk > 0);
+          }
+          dev::tc_commit(&kv_empty[k & 1]);
+          dev::tc_commit(o_full);
+        }
+        ok = good;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else {
+      // ---------------------------------------------------- softmax warps
+      const int r = threadIdx.x;  // row of the tile = TMEM lane
+      const int gr = qt * kTcRows + r;
+      const bool valid = gr < qlen * G;
+      const int pos = valid ? ctx - qlen + gr / G : -1;
+      const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+      const float sl2 = p.scale_log2;
+      float mref = -INFINITY, l = 0.f;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int k = kv_tiles + j, st = k & 1;
+        if (!dev::mbar_wait_bounded(s_full, (s_count + j) & 1, tmo, p.status)) {
+          ok = false;
+          break;
+        }
+        dev::tc_fence_after_sync();
+        const int t0 = j * kTcTokens;
+        // pass 1: the tile's row maximum
+        float mx = -INFINITY;
+        for (int c = 0; c < kTcTokens; c += 32) {
+          uint32_t v[32];
+          dev::tmem_ld32(trow + c, v);
+          dev::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (t0 + c + i <= pos) mx = fmaxf(mx, __uint_as_float(v[i]) * sl2);
+        }
+        float ref = mref;
+        if (mx > mref + kTcRescale || (mref == -INFINITY && mx != -INFINITY)) {
+          ref = mx;
+          if (mref != -INFINITY) {
+            // O (already holding every earlier tile: this tile's S was issued
+            // after the previous P V) is rescaled in TMEM
+            const float a = dev::fast_exp2(mref - ref);
+            l *= a;
+            for (int c = 0; c < D; c += 32) {
+              uint32_t v[32];
+              dev::tmem_ld32(trow + 128 + c, v);
+              dev::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+              dev::tmem_st32(trow + 128 + c, v);
+            }
+            dev::tmem_wait_st();
+          }
+          mref = ref;
+        }
+        // V rows past the context or past the loaded blocks are zeroed, so
+        // whatever bits they hold never meet a zero probability
+        if (!dev::mbar_wait_bounded(&kv_full[st], (k >> 1) & 1, tmo, p.status)) {
+          ok = false;
+          break;
+        }
+        {
+          const int tok = t0 + r;
+          const int bound = min(ctx, nblk * kBlockSize);
+          if (tok >= bound) {
+            uint8_t* vrow = smem + TcSmem::kV + st * 2 * TcSmem::kChunk + r * 128;
+            for (int h = 0; h < 2; ++h)
+              for (int q16 = 0; q16 < 8; ++q16)
+                *reinterpret_cast<uint4*>(vrow + h * TcSmem::kChunk + q16 * 16) =
+                    make_uint4(0, 0, 0, 0);
+          }
+        }
+        // pass 2: P = 2^(s - ref) in the input type, row sum, P to shared memory
+        for (int c = 0; c < kTcTokens; c += 32) {
+          uint32_t v[32];
+          dev::tmem_ld32(trow + c, v);
+          dev::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int ta = t0 + c + 2 * i;
+            const float x0 = ta <= pos && ref != -INFINITY ? __uint_as_float(v[2 * i]) * sl2 - ref : -INFINITY;
+            const float x1 = ta + 1 <= pos && ref != -INFINITY ? __uint_as_float(v[2 * i + 1]) * sl2 - ref : -INFINITY;
+            pk[i] = M::pack(dev::fast_exp2(x0), dev::fast_exp2(x1));
+            const float2 f = M::unpack(pk[i]);
+            l += f.x + f.y;
+          }
+          // 32 tokens = 4 chunks of 16 bytes; chunk index along the row
+          // (tokens / 8), swizzled by the row within its 8-row group
+#pragma unroll
+          for (int q16 = 0; q16 < 4; ++q16) {
+            const int chunk = (c >> 3) + q16;  // 0..15 over the 128 tokens
+            const int h = chunk >> 3, w = chunk & 7;
+            uint8_t* dst = smem + TcSmem::kP + h * TcSmem::kChunk + r * 128 + ((w ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(dst) =
+                make_uint4(pk[4 * q16], pk[4 * q16 + 1], pk[4 * q16 + 2], pk[4 * q16 + 3]);
+          }
+        }
+        dev::fence_proxy_async_smem();
+        dev::tc_fence_before_sync();
+        dev::mbar_arrive(p_full);
+      }
+      if (ok) {
+        // the tile's O is complete: normalise and write
+        if (!dev::mbar_wait_bounded(o_full, o_count & 1, tmo, p.status)) ok = false;
+        if (ok) {
+          dev::tc_fence_after_sync();
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          T* orow = static_cast<T*>(p.out) +
+                    (size_t(q_first + (valid ? gr / G : 0)) * Hq + g * G + (valid ? gr % G : 0)) * D;
+          for (int c = 0; c < D; c += 32) {
+            uint32_t v[32];
+            dev::tmem_ld32(trow + 128 + c, v);
+            dev::tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint4 w;
+                w.x = M::pack(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
+                w.y = M::pack(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
+                w.z = M::pack(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
+                w.w = M::pack(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
+                *reinterpret_cast<uint4*>(orow + c + 8 * i) = w;
+              }
+            }
+          }
+        }
+      }
+    }
+    // every thread agrees before the next item (the TMEM and the ring are reused)
+    dev::tc_fence_before_sync();
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    dev::tc_fence_after_sync();
+    kv_tiles += ntiles;
+    q_loads += 1;
+    s_count += ntiles;
+    p_count += ntiles;
+    o_count += 1;
+  }
+  if (!ok && issuer) {
+    // a wait ran out: let the copies and MMAs in flight finish before leaving
+    dev::tc_commit(o_full);
+    dev::mbar_wait_bounded(o_full, o_count & 1, tmo, p.status);
+    for (int k = kv_tiles; k < kv_tiles + 2; ++k)
+      dev::mbar_wait_bounded(&kv_full[k & 1], (k >> 1) & 1, tmo, p.status);
+  }
+  dev::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 4) {
+    dev::tc_fence_after_sync();
+    dev::tmem_dealloc(tmem, kTcCols);
+  }
+  if (threadIdx.x == 0 && planned && ok) {
+    __threadfence();
+    if (atomicAdd(&p.header[kHdrDone], 1) == int(gridDim.x) - 1) {
+      atomicExch(&p.header[kHdrNext], 0);
+      atomicExch(&p.header[kHdrDone], 0);
+    }
+  }
+}
+
 // --------------------------------------------------------------- fp32 path
 // One warp per (query row, query head): a decode over the row's causal prefix.
 template <int D>
@@ -790,7 +1171,19 @@ struct DeviceState {
   int error = 0;
   int sms = 0;
   int ctas_per_sm[2][2] = {{0, 0}, {0, 0}};  // [bf16?][head_dim 128?]
+  bool tc_ok = false;                        // tcgen05 kernel configured
 };
+
+// The tcgen05 kernel serves 16-bit, head_dim 128 and groups dividing its
+// 128-row tile (the mma.sync kernel the rest); PA_PREFILL_TC=0 turns it off
+// (read once per process).
+bool tc_wanted() {
+  static const bool on = [] {
+    const char* v = std::getenv("PA_PREFILL_TC");
+    return v ? std::atoi(v) != 0 : true;
+  }();
+  return on;
+}
 DeviceState g_dev[kMaxDevices];
 
 template <typename T, int D>
@@ -818,6 +1211,15 @@ int device_setup(int device) {
     for (int a = 0; a < 2; ++a)
       for (int d = 0; d < 2; ++d)
         if (st.error == PA_OK && st.ctas_per_sm[a][d] < 1) st.error = PA_ERR_UNSUPPORTED;
+    if (st.error == PA_OK) {
+      st.tc_ok = cudaFuncSetAttribute(prefill_tc_kernel<__nv_bfloat16>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      TcSmem::kBytes) == cudaSuccess &&
+                 cudaFuncSetAttribute(prefill_tc_kernel<__half>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      TcSmem::kBytes) == cudaSuccess;
+      cudaGetLastError();
+    }
   });
   if (st.error != PA_OK) return fail(st.error, "prefill: per-device set-up failed on device %d", device);
   return PA_OK;
@@ -955,11 +1357,16 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
   const bool bf16 = dtype == PA_BF16;
   const int per_sm = st.ctas_per_sm[bf16][head_dim == 128];
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  prm.ncta = st.sms * per_sm;
+  const int G = num_q_heads / num_kv_heads;
+  const bool use_tc = tc_wanted() && st.tc_ok && prm.shared_ctx == 0 && head_dim == 128 &&
+                      (G == 1 || G == 2 || G == 4 || G == 8);
+  prm.ncta = use_tc ? st.sms : st.sms * per_sm;
+  prm.no_split = use_tc ? 1 : 0;
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
   prm.signature = signature_of(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
-                               max_blocks_per_seq) ^ (prm.shared_ctx << 1);
+                               max_blocks_per_seq) ^ (prm.shared_ctx << 1) ^
+                  (use_tc ? 0x2A000000 : 0);
   prm.header = reinterpret_cast<int*>(ws + lay.header);
   prm.units = reinterpret_cast<int4*>(ws + lay.units);
   prm.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
@@ -975,8 +1382,27 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
   pc.stream = s;
   pc.attrs = attr;
   pc.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&pc, prefill_plan_kernel, prm);
+  cudaError_t e = use_tc ? cudaLaunchKernelEx(&pc, prefill_plan_kernel<kTcRows>, prm)
+                         : cudaLaunchKernelEx(&pc, prefill_plan_kernel<kRows>, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
+  if (use_tc) {
+    alignas(64) CUtensorMap mq, mk, mv;
+    rc = query_tensor_map(&mq, prm.q, bf16, total_q, num_q_heads, head_dim, G, kTcRows);
+    if (rc == PA_OK) rc = cache_tensor_map(&mk, k_cache, bf16, num_blocks, num_kv_heads, head_dim);
+    if (rc == PA_OK) rc = cache_tensor_map(&mv, v_cache, bf16, num_blocks, num_kv_heads, head_dim);
+    if (rc != PA_OK) return rc;
+    cudaLaunchConfig_t tc = {};
+    tc.gridDim = dim3(prm.ncta);
+    tc.blockDim = dim3(kTcThreads);
+    tc.dynamicSmemBytes = TcSmem::kBytes;
+    tc.stream = s;
+    tc.attrs = attr;
+    tc.numAttrs = 1;
+    e = bf16 ? cudaLaunchKernelEx(&tc, prefill_tc_kernel<__nv_bfloat16>, mq, mk, mv, prm)
+             : cudaLaunchKernelEx(&tc, prefill_tc_kernel<__half>, mq, mk, mv, prm);
+    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
+    return PA_OK;
+  }
 
   alignas(64) CUtensorMap mk, mv;
   rc = cache_tensor_map(&mk, k_cache, bf16, num_blocks, num_kv_heads, head_dim);

@@ -16,4 +16,12 @@ namespace pa {
 int cache_tensor_map(CUtensorMap* out, const void* cache, bool bf16, int num_blocks,
                      int num_kv_heads, int head_dim);
 
+// Encodes the 3-D tensor map of a query tensor `[total_q][num_q_heads][head_dim]`
+// (16-bit) whose copy box is 64 elements x `group` heads x (rows / group)
+// tokens with 128-byte swizzle: one box fills `rows` consecutive 128-byte
+// rows of a query tile, row = token * group + head within the group.
+// Returns a pa_status.
+int query_tensor_map(CUtensorMap* out, const void* q, bool bf16, int total_q, int num_q_heads,
+                     int head_dim, int group, int rows);
+
 }  // namespace pa

@@ -28,3 +28,12 @@ def test_parity_under_tuning(gpu, name):
     r = subprocess.run([sys.executable, "-m", "tests.tuned_child"], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+@pytest.mark.parametrize("tc", ["0", "1"], ids=["mma_sync", "tcgen05"])
+def test_prefill_parity_per_kernel(gpu, tc):
+    """Chunked prefill through each of its two tensor-core kernels."""
+    env = dict(os.environ, PA_PREFILL_TC=tc)
+    r = subprocess.run([sys.executable, "-m", "tests.prefill_child"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
