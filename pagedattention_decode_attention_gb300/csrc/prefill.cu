@@ -720,33 +720,44 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 }
 
 // ------------------------------------------------------- tcgen05 path (d = 128)
-// A CTA takes 128-row query tiles (rows = tokens x the group's heads, as
-// above) and streams their causal KV range in tiles of 128 tokens (8 paged
-// blocks) through a 2-stage ring.  One thread of warp 4 issues the TMA copies
-// and the 5th-generation tensor-core MMAs:
-//   S  = Q K^T   (M 128 rows, N 128 tokens, K 128; fp32 accumulator in TMEM)
-//   O += P V     (M 128 rows, N 128 = head_dim, K 128 tokens; O in TMEM)
-// Warps 0-3 run the softmax, one thread per row (its TMEM lane): S is read
-// from TMEM, masked (causal, context), exponentiated in base 2 against a
-// reference that moves only when a row's maximum grows by more than 2^8 (the
-// O rescale then happens in TMEM; the result is exact either way), and P is
-// written to shared memory in the 128-byte-swizzled K-major layout the MMA
-// reads.  V is the MMA's N-contiguous B operand, straight from the TMA tile.
+// A work item is 256 query rows (rows = tokens x the group's heads, as above)
+// of one (sequence, KV head): two 128-row query tiles that share every KV
+// tile of the item's causal range, streamed in tiles of 128 tokens (8 paged
+// blocks).  Warp roles:
+//   warp 8       producer: claims items (two-slot queue), TMA copies of the
+//                query tiles and the K / V tiles (separate 2-stage rings)
+//   warp 9       one thread issues the 5th-generation tensor-core MMAs
+//                  S_w  = Q_w K^T   (M 128, N 128 tokens, K 128; fp32 in TMEM)
+//                  O_w += P_w V     (M 128, N 128 = head_dim, K 128 tokens)
+//   warps 0-3, 4-7  softmax of query tile 0 / 1, one thread per row (its TMEM
+//                lane); while one group works on its scores the tensor core
+//                runs the other group's MMAs.
+// TMEM (512 columns): S_0 | S_1 | O_0 | O_1, 128 columns each.  P_w is written
+// in the input type over the first 64 columns of S_w and is the A operand of
+// O_w += P_w V straight from TMEM; V is the N-contiguous B operand, K the
+// K-major B operand of S, as the TMA tiles land.  The softmax exponentiates
+// in base 2 against a reference that moves only when a row's maximum grows by
+// more than 2^8 (O_w is then rescaled in TMEM; the result is the same either
+// way).
 constexpr int kTcRows = 128;       // query rows per tile (TMEM lanes)
+constexpr int kTcItemRows = 256;   // two query tiles per work item
 constexpr int kTcTokens = 128;     // tokens per KV tile
 constexpr int kTcBlocks = kTcTokens / kBlockSize;
-constexpr int kTcThreads = 160;    // 4 softmax warps + 1 issue warp
-constexpr uint32_t kTcCols = 256;  // TMEM columns: S at 0, O at 128
+constexpr int kTcThreads = 384;    // 8 softmax warps, producer warp, MMA warp, 2 idle
+// registers per thread after the split: launched with 65536 / 384 = 168 each,
+// the producer warpgroup gives back to 56 and the softmax warpgroups take
+// 224: (224 + 224 + 56) x 128 = 64512 = 168 x 384
+constexpr int kTcRegsSoftmax = 224, kTcRegsProducer = 56;
+constexpr uint32_t kTcCols = 512;  // TMEM columns: S_0, S_1, O_0, O_1
 constexpr float kTcRescale = 8.f;  // log2 of the growth that forces an O rescale
 
 struct TcSmem {  // head_dim 128, 16-bit: every chunk is [128 rows][128 bytes]
-  static constexpr int kChunk = kTcRows * 128;            // 16 KB
-  static constexpr int kQ = 0;                            // 2 chunks (d 0-63, 64-127)
-  static constexpr int kK = 2 * kChunk;                   // [2 stages][2 chunks]
-  static constexpr int kV = kK + 4 * kChunk;              // [2 stages][2 chunks]
-  static constexpr int kP = kV + 4 * kChunk;              // 2 chunks (tokens 0-63, 64-127)
-  static constexpr int kBars = kP + 2 * kChunk;           // mbarriers
-  static constexpr int kBytes = kBars + 128 + 1024;       // + scalars, alignment slack
+  static constexpr int kChunk = kTcRows * 128;  // 16 KB
+  static constexpr int kQ = 0;                  // [2 tiles][2 chunks (d 0-63, 64-127)]
+  static constexpr int kK = 4 * kChunk;         // [2 stages][2 chunks]
+  static constexpr int kV = kK + 4 * kChunk;    // [2 stages][2 chunks]
+  static constexpr int kBars = kV + 4 * kChunk; // mbarriers, item slots
+  static constexpr int kBytes = kBars + 256 + 1024;  // + alignment slack
 };
 
 template <typename T>
@@ -761,33 +772,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TcSmem::kBars);
-  uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_full = bars + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8);
-  int* s_claim = reinterpret_cast<int*>(bars + 9);
+  uint64_t* item_full = bars + 0;   // [2] the producer wrote the slot
+  uint64_t* item_empty = bars + 2;  // [2] every role has read it
+  uint64_t* q_full = bars + 4;
+  uint64_t* q_empty = bars + 5;     // the item's last S MMA finished with Q
+  uint64_t* k_full = bars + 6;      // [2]
+  uint64_t* k_empty = bars + 8;     // [2]
+  uint64_t* v_full = bars + 10;     // [2]
+  uint64_t* v_empty = bars + 12;    // [2]
+  uint64_t* s_full = bars + 14;     // [2] S_w is in TMEM
+  uint64_t* p_full = bars + 16;     // [2] P_w is in TMEM (128 arrivals)
+  uint64_t* pv_done = bars + 18;    // [2] O_w += P_w V finished
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  int* s_item = reinterpret_cast<int*>(bars + 21);  // [2]
+  uint64_t* drain = bars + 22;      // every MMA issued has finished (error exit)
   const uint32_t sbase = dev::smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool issuer = warp == 4 && lane == 0;
-  if (issuer) {
-    dev::mbar_init(q_full, 1);
+  if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      dev::mbar_init(&kv_full[i], 1);
-      dev::mbar_init(&kv_empty[i], 1);
+      dev::mbar_init(&item_full[i], 1);
+      dev::mbar_init(&item_empty[i], 9);  // 8 softmax warps + the MMA thread
+      dev::mbar_init(&k_full[i], 1);
+      dev::mbar_init(&k_empty[i], 1);
+      dev::mbar_init(&v_full[i], 1);
+      dev::mbar_init(&v_empty[i], 1);
+      dev::mbar_init(&s_full[i], 1);
+      dev::mbar_init(&p_full[i], kTcRows);
+      dev::mbar_init(&pv_done[i], 1);
     }
-    dev::mbar_init(s_full, 1);
-    dev::mbar_init(p_full, kTcRows);
-    dev::mbar_init(o_full, 1);
+    dev::mbar_init(q_full, 1);
+    dev::mbar_init(q_empty, 1);
+    dev::mbar_init(drain, 1);
     dev::mbar_fence_init();
     dev::prefetch_tensormap(&tmap_q);
     dev::prefetch_tensormap(&tmap_k);
     dev::prefetch_tensormap(&tmap_v);
   }
-  if (warp == 4) dev::tmem_alloc(tmem_slot, kTcCols);
+  if (warp == 9) dev::tmem_alloc(tmem_slot, kTcCols);
   dev::tc_fence_before_sync();
   __syncthreads();
   dev::tc_fence_after_sync();
@@ -800,291 +822,349 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
-  const uint64_t policy = dev::l2_policy_evict_first();
-  const uint32_t idesc_s = dev::mma_idesc_f16(kBf16, kTcRows, kTcTokens, false);
-  const uint32_t idesc_o = dev::mma_idesc_f16(kBf16, kTcRows, D, true);
-  // phase counters, the same in every thread that uses them
-  int kv_tiles = 0;  // KV tiles through the ring so far
-  int q_loads = 0, s_count = 0, p_count = 0, o_count = 0;
   bool ok = true;
-  bool first_claim = true;
 
-  for (;;) {
-    if (threadIdx.x == 0)
-      *s_claim = first_claim ? int(blockIdx.x) : int(gridDim.x) + atomicAdd(&p.header[kHdrNext], 1);
-    first_claim = false;
-    __syncthreads();
-    const int x = *s_claim;
-    __syncthreads();
-    if (x >= total) break;
+  // what every role decodes from a claimed item
+  struct Item {
+    int b, qt, nblk, ctx, q_first, qlen, g, ntiles;
+    bool two;  // the second query tile holds valid rows
+  };
+  auto decode = [&](int x) {
+    Item it;
     const int4 u0 = p.units[2 * (x / Hkv)], u1 = p.units[2 * (x / Hkv) + 1];
-    const int g = x % Hkv, b = u0.x, qt = u0.y, nblk = u0.w, ctx = u1.w;
-    const int q_first = p.query_start[b];
-    const int qlen = p.query_start[b + 1] - q_first;
-    const int ntiles = (nblk + kTcBlocks - 1) / kTcBlocks;
-    const int tok0 = qt * (kTcRows / G);  // first query token of the tile in the chunk
+    it.g = x % Hkv;
+    it.b = u0.x;
+    it.qt = u0.y;
+    it.nblk = u0.w;
+    it.ctx = u1.w;
+    it.q_first = p.query_start[it.b];
+    it.qlen = p.query_start[it.b + 1] - it.q_first;
+    it.ntiles = (it.nblk + kTcBlocks - 1) / kTcBlocks;
+    it.two = it.qt * kTcItemRows + kTcRows < it.qlen * G;
+    return it;
+  };
 
-    if (warp == 4) {
-      // ---------------------------------------------------- issue warp
-      // table entries, 32 at a time, one per lane
-      int tbl = 0, tbl_base = -32;
-      auto load_tile = [&](int j) -> bool {  // KV tile j into stage (kv_tiles + j) % 2
-        const int k = kv_tiles + j, st = k & 1;
-        const int nb = min(kTcBlocks, nblk - j * kTcBlocks);
-        bool good = true;
-        if (lane == 0 && k >= 2)
-          good = dev::mbar_wait_bounded(&kv_empty[st], ((k >> 1) - 1) & 1, tmo, p.status);
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) return false;
-        if (lane == 0) dev::mbar_arrive_expect_tx(&kv_full[st], uint32_t(nb) * 4 * 2048);
-        for (int jb = 0; jb < nb; ++jb) {
-          const int blk = j * kTcBlocks + jb;
-          if ((blk & ~31) != tbl_base) {
-            tbl_base = blk & ~31;
-            tbl = tbl_base + lane < nblk
-                      ? p.block_tables[size_t(b) * p.max_blocks + tbl_base + lane]
-                      : 0;
-            if (tbl < 0 || tbl >= p.num_blocks) {
-              dev::flag_status(p.status, kStatusBounds);
-              tbl = 0;
-            }
-          }
-          const int phys = __shfl_sync(0xffffffffu, tbl, blk & 31);
-          if (lane == 0) {
-            const int y = (phys * Hkv + g) * kBlockSize;
-            uint8_t* kd = smem + TcSmem::kK + st * 2 * TcSmem::kChunk + jb * 2048;
-            uint8_t* vd = smem + TcSmem::kV + st * 2 * TcSmem::kChunk + jb * 2048;
-            for (int h = 0; h < 2; ++h) {
-              dev::tma_load_2d(kd + h * TcSmem::kChunk, &tmap_k, h * 64, y, &kv_full[st], policy);
-              dev::tma_load_2d(vd + h * TcSmem::kChunk, &tmap_v, h * 64, y, &kv_full[st], policy);
-            }
-          }
-        }
-        return true;
-      };
-      // the query tile, then the first two KV tiles
+  if (warp >= 8) dev::setmaxnreg_dec<kTcRegsProducer>();
+  if (warp == 8) {
+    // ====================================================== producer warp
+    const uint64_t policy = dev::l2_policy_evict_first();
+    int kt = 0;  // K / V tiles loaded so far
+    int qn = 0;  // query-tile loads so far
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      int x = 0;
       if (lane == 0) {
-        dev::mbar_arrive_expect_tx(q_full, 2 * TcSmem::kChunk);
-        for (int h = 0; h < 2; ++h) {
-          const int zc = q_first + tok0;
-          asm volatile(
-              "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-              " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + TcSmem::kQ + h * TcSmem::kChunk),
-              "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(h * 64), "r"(g * G), "r"(zc),
-              "r"(dev::smem_u32(q_full))
-              : "memory");
+        if (n >= 2) ok = dev::mbar_wait_bounded(&item_empty[slot], ((n >> 1) - 1) & 1, tmo, p.status);
+        x = n == 0 ? int(blockIdx.x) : int(gridDim.x) + atomicAdd(&p.header[kHdrNext], 1);
+        if (!ok) x = total;  // stop every role
+        s_item[slot] = x;
+        dev::mbar_arrive(&item_full[slot]);
+      }
+      x = __shfl_sync(0xffffffffu, x, 0);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (x >= total) break;
+      const Item it = decode(x);
+      if (lane == 0) {
+        if (n >= 1) ok = dev::mbar_wait_bounded(q_empty, (n - 1) & 1, tmo, p.status);
+        if (ok) {
+          const int tiles = it.two ? 2 : 1;
+          ++qn;
+          dev::mbar_arrive_expect_tx(q_full, uint32_t(tiles) * 2 * TcSmem::kChunk);
+          for (int w = 0; w < tiles; ++w)
+            for (int h = 0; h < 2; ++h) {
+              const int zc = it.q_first + it.qt * (kTcItemRows / G) + w * (kTcRows / G);
+              asm volatile(
+                  "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sbase + TcSmem::kQ +
+                                                           (2 * w + h) * TcSmem::kChunk),
+                  "l"(reinterpret_cast<uint64_t>(&tmap_q)), "r"(h * 64), "r"(it.g * G), "r"(zc),
+                  "r"(dev::smem_u32(q_full))
+                  : "memory");
+            }
         }
       }
-      for (int j = 0; j < ntiles && j < 2 && ok; ++j) ok = load_tile(j);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int k = kv_tiles + j, st = k & 1;
-        bool good = true;
-        if (lane == 0) {
-          good = dev::mbar_wait_bounded(&kv_full[st], (k >> 1) & 1, tmo, p.status);
-          if (good && j == 0) good = dev::mbar_wait_bounded(q_full, q_loads & 1, tmo, p.status);
-          if (good && j > 0) {
-            // P of the previous tile is ready: O += P V
-            good = dev::mbar_wait_bounded(p_full, (p_count + j - 1) & 1, tmo, p.status);
-            if (good) {
-              dev::tc_fence_after_sync();
-              const uint32_t vb = sbase + TcSmem::kV + ((k - 1) & 1) * 2 * TcSmem::kChunk;
-              for (int kk = 0; kk < kTcTokens / 16; ++kk) {
-                const uint64_t ad = dev::smem_desc_sw128(
-                    sbase + TcSmem::kP + (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32, 16, 1024);
-                const uint64_t bd = dev::smem_desc_sw128(vb + kk * 2048, TcSmem::kChunk, 1024);
-                dev::tc_mma_f16(tmem + 128, ad, bd, idesc_o, j > 1 || kk > 0);
-              }
-              dev::tc_commit(&kv_empty[(k - 1) & 1]);
-            }
-          }
-          if (good) {
-            // S = Q K^T for this tile
-            dev::tc_fence_after_sync();
-            const uint32_t kb = sbase + TcSmem::kK + st * 2 * TcSmem::kChunk;
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32;
-              const uint64_t ad = dev::smem_desc_sw128(sbase + TcSmem::kQ + off, 16, 1024);
-              const uint64_t bd = dev::smem_desc_sw128(kb + off, 16, 1024);
-              dev::tc_mma_f16(tmem + 0, ad, bd, idesc_s, kk > 0);
-            }
-            dev::tc_commit(s_full);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // table entries, 32 at a time, one per lane
+      int tbl = 0, tbl_base = -32;
+      for (int j = 0; j < it.ntiles && ok; ++j, ++kt) {
+        const int st = kt & 1;
+        const int nb = min(kTcBlocks, it.nblk - j * kTcBlocks);
+        if ((j * kTcBlocks & ~31) != tbl_base) {
+          tbl_base = j * kTcBlocks & ~31;
+          tbl = tbl_base + lane < it.nblk
+                    ? p.block_tables[size_t(it.b) * p.max_blocks + tbl_base + lane]
+                    : 0;
+          if (tbl < 0 || tbl >= p.num_blocks) {
+            dev::flag_status(p.status, kStatusBounds);
+            tbl = 0;
           }
         }
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) {
+        const int phys = __shfl_sync(0xffffffffu, tbl, (j * kTcBlocks + lane) & 31);
+        for (int kind = 0; kind < 2 && ok; ++kind) {  // K, then V
+          uint64_t* full = kind == 0 ? &k_full[st] : &v_full[st];
+          uint64_t* empty = kind == 0 ? &k_empty[st] : &v_empty[st];
+          if (lane == 0) {
+            if (kt >= 2) ok = dev::mbar_wait_bounded(empty, ((kt >> 1) - 1) & 1, tmo, p.status);
+            if (ok) dev::mbar_arrive_expect_tx(full, uint32_t(nb) * 4 * 1024);
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          // lane jb < nb copies block jb of the tile (both 64-column halves)
+          if (lane < nb) {
+            const int y = (phys * Hkv + it.g) * kBlockSize;
+            uint8_t* dst = smem + (kind == 0 ? TcSmem::kK : TcSmem::kV) +
+                           st * 2 * TcSmem::kChunk + lane * 2048;
+            const CUtensorMap* map = kind == 0 ? &tmap_k : &tmap_v;
+            for (int h = 0; h < 2; ++h)
+              dev::tma_load_2d(dst + h * TcSmem::kChunk, map, h * 64, y, full, policy);
+          }
+        }
+      }
+      if (!ok) break;
+    }
+    if (lane == 0) {
+      // copies still in flight land before the CTA leaves
+      if (qn > 0) dev::mbar_wait_bounded(q_full, (qn - 1) & 1, tmo, p.status);
+      for (int k = max(0, kt - 2); k < kt; ++k) {
+        dev::mbar_wait_bounded(&k_full[k & 1], (k >> 1) & 1, tmo, p.status);
+        dev::mbar_wait_bounded(&v_full[k & 1], (k >> 1) & 1, tmo, p.status);
+      }
+    }
+  } else if (warp == 9) {
+    // ====================================================== MMA warp
+    if (lane == 0) {
+      const uint32_t idesc_s = dev::mma_idesc_f16(kBf16, kTcRows, kTcTokens, false);
+      const uint32_t idesc_o = dev::mma_idesc_f16(kBf16, kTcRows, D, true);
+      // operand descriptors of the tiles' first bytes; a step adds its byte
+      // offset / 16 to the address field (no carry: shared addresses < 256 KB)
+      const uint64_t desc_q = dev::smem_desc_sw128(sbase + TcSmem::kQ, 16, 1024);
+      const uint64_t desc_k = dev::smem_desc_sw128(sbase + TcSmem::kK, 16, 1024);
+      const uint64_t desc_v = dev::smem_desc_sw128(sbase + TcSmem::kV, TcSmem::kChunk, 1024);
+      int kt = 0;         // K / V tiles consumed
+      int pv[2] = {0, 0};  // P V products issued per query tile
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 1;
+        if (!dev::mbar_wait_bounded(&item_full[slot], (n >> 1) & 1, tmo, p.status)) {
           ok = false;
           break;
         }
-        // the stage of the previous tile is released by that tile's P V: refill it
-        if (j >= 1 && j + 1 < ntiles) ok = load_tile(j + 1);
-      }
-      if (ok && lane == 0) {
-        // the last tile's O += P V
-        const int k = kv_tiles + ntiles - 1;
-        bool good = dev::mbar_wait_bounded(p_full, (p_count + ntiles - 1) & 1, tmo, p.status);
-        if (good) {
+        const int x = *reinterpret_cast<volatile int*>(&s_item[slot]);
+        dev::mbar_arrive(&item_empty[slot]);
+        if (x >= total) break;
+        const Item it = decode(x);
+        const int tiles = it.two ? 2 : 1;
+        ok = dev::mbar_wait_bounded(q_full, n & 1, tmo, p.status);
+        // S_w = Q_w K_j^T once O_w += P_w V of the previous tile has finished
+        // (P_w sits in S_w's columns)
+        auto issue_s = [&](int w, int j, int st) -> bool {
+          if (pv[w] > 0 && !dev::mbar_wait_bounded(&pv_done[w], (pv[w] - 1) & 1, tmo, p.status))
+            return false;
           dev::tc_fence_after_sync();
-          const uint32_t vb = sbase + TcSmem::kV + (k & 1) * 2 * TcSmem::kChunk;
-          for (int kk = 0; kk < kTcTokens / 16; ++kk) {
-            const uint64_t ad = dev::smem_desc_sw128(
-                sbase + TcSmem::kP + (kk >> 2) * TcSmem::kChunk + (kk & 3) * 32, 16, 1024);
-            const uint64_t bd = dev::smem_desc_sw128(vb + kk * 2048, TcSmem::kChunk, 1024);
-            dev::tc_mma_f16(tmem + 128, ad, bd, idesc_o, ntiles > 1 || kk > 0);
+          const uint64_t a = desc_q + uint32_t((w * 2 * TcSmem::kChunk) >> 4);
+          const uint64_t bk = desc_k + uint32_t((st * 2 * TcSmem::kChunk) >> 4);
+#pragma unroll 1
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = uint32_t(((kk >> 2) * TcSmem::kChunk + (kk & 3) * 32) >> 4);
+            dev::tc_mma_f16(tmem + w * 128, a + off, bk + off, idesc_s, kk > 0);
           }
-          dev::tc_commit(&kv_empty[k & 1]);
-          dev::tc_commit(o_full);
+          dev::tc_commit(&s_full[w]);
+          return true;
+        };
+        auto issue_pv = [&](int w, int j, int st) -> bool {
+          if (!dev::mbar_wait_bounded(&p_full[w], pv[w] & 1, tmo, p.status)) return false;
+          dev::tc_fence_after_sync();
+          const uint64_t bv = desc_v + uint32_t((st * 2 * TcSmem::kChunk) >> 4);
+#pragma unroll 1
+          for (int kk = 0; kk < kTcTokens / 16; ++kk)
+            dev::tc_mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
+                               bv + uint32_t((kk * 2048) >> 4), idesc_o, j > 0 || kk > 0);
+          dev::tc_commit(&pv_done[w]);
+          ++pv[w];
+          return true;
+        };
+        // prologue: S of the first tile for both query tiles
+        if (ok) ok = dev::mbar_wait_bounded(&k_full[kt & 1], (kt >> 1) & 1, tmo, p.status);
+        for (int w = 0; w < tiles && ok; ++w) ok = issue_s(w, 0, kt & 1);
+        if (ok) {
+          dev::tc_commit(&k_empty[kt & 1]);
+          if (it.ntiles == 1) dev::tc_commit(q_empty);
         }
-        ok = good;
+        for (int j = 0; j < it.ntiles && ok; ++j) {
+          const int st = (kt + j) & 1, nst = (kt + j + 1) & 1;
+          const bool more = j + 1 < it.ntiles;
+          ok = dev::mbar_wait_bounded(&v_full[st], ((kt + j) >> 1) & 1, tmo, p.status);
+          if (ok) ok = issue_pv(0, j, st);
+          if (ok && more) {
+            ok = dev::mbar_wait_bounded(&k_full[nst], ((kt + j + 1) >> 1) & 1, tmo, p.status);
+            if (ok) ok = issue_s(0, j + 1, nst);
+          }
+          if (ok && tiles == 2) ok = issue_pv(1, j, st);
+          if (ok) dev::tc_commit(&v_empty[st]);
+          if (ok && more && tiles == 2) ok = issue_s(1, j + 1, nst);
+          if (ok && more) {
+            dev::tc_commit(&k_empty[nst]);
+            if (j + 2 == it.ntiles) dev::tc_commit(q_empty);
+          }
+        }
+        kt += it.ntiles;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-    } else {
-      // ---------------------------------------------------- softmax warps
-      const int r = threadIdx.x;  // row of the tile = TMEM lane
-      const int gr = qt * kTcRows + r;
-      const bool valid = gr < qlen * G;
-      const int pos = valid ? ctx - qlen + gr / G : -1;
-      const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-      const float sl2 = p.scale_log2;
+      if (!ok) {
+        // a wait ran out: let the MMAs in flight finish before TMEM is freed
+        dev::tc_commit(drain);
+        dev::mbar_wait_bounded(drain, 0, tmo, p.status);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ====================================================== softmax warps
+    dev::setmaxnreg_inc<kTcRegsSoftmax>();
+    const int w = warp >> 2;              // query tile of this group
+    const int r = threadIdx.x & 127;      // row of the tile = TMEM lane
+    const uint32_t lanes = uint32_t((warp & 3) * 32) << 16;
+    const uint32_t t_s = tmem + lanes + w * 128, t_o = tmem + lanes + 256 + w * 128;
+    const float sl2 = p.scale_log2;       // > 0 on this path
+    int cnt = 0;                          // tiles of this group so far
+    int kt = 0;                           // K / V tiles so far (group 0 sees them all)
+    for (int n = 0;; ++n) {
+      const int slot = n & 1;
+      if (!dev::mbar_wait_bounded(&item_full[slot], (n >> 1) & 1, tmo, p.status)) {
+        ok = false;
+        break;
+      }
+      const int x = *reinterpret_cast<volatile int*>(&s_item[slot]);
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(&item_empty[slot]);
+      if (x >= total) break;
+      const Item it = decode(x);
+      if (w == 1 && !it.two) continue;
+      const int gr = it.qt * kTcItemRows + w * kTcRows + r;
+      const bool valid = gr < it.qlen * G;
+      const int pos = valid ? it.ctx - it.qlen + gr / G : -1;
+      const int bound = min(it.ctx, it.nblk * kBlockSize);
       float mref = -INFINITY, l = 0.f;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int k = kv_tiles + j, st = k & 1;
-        if (!dev::mbar_wait_bounded(s_full, (s_count + j) & 1, tmo, p.status)) {
+      for (int j = 0; j < it.ntiles && ok; ++j, ++cnt) {
+        if (!dev::mbar_wait_bounded(&s_full[w], cnt & 1, tmo, p.status)) {
           ok = false;
           break;
         }
         dev::tc_fence_after_sync();
         const int t0 = j * kTcTokens;
-        // pass 1: the tile's row maximum
-        float mx = -INFINITY;
-        for (int c = 0; c < kTcTokens; c += 32) {
-          uint32_t v[32];
-          dev::tmem_ld32(trow + c, v);
-          dev::tmem_wait_ld();
+        uint32_t sv[4][32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (t0 + c + i <= pos) mx = fmaxf(mx, __uint_as_float(v[i]) * sl2);
+        for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + 32 * c, sv[c]);
+        dev::tmem_wait_ld();
+        const bool whole = t0 + kTcTokens - 1 <= pos;  // no masked column in this row
+        float mx = -INFINITY;
+        if (whole) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (t0 + 32 * c + i <= pos) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
         }
-        float ref = mref;
+        mx *= sl2;
         if (mx > mref + kTcRescale || (mref == -INFINITY && mx != -INFINITY)) {
-          ref = mx;
           if (mref != -INFINITY) {
-            // O (already holding every earlier tile: this tile's S was issued
-            // after the previous P V) is rescaled in TMEM
-            const float a = dev::fast_exp2(mref - ref);
+            // O_w holds every earlier tile (S_w of this tile was issued after
+            // the previous P V finished): rescale it in TMEM
+            const float a = dev::fast_exp2(mref - mx);
             l *= a;
-            for (int c = 0; c < D; c += 32) {
-              uint32_t v[32];
-              dev::tmem_ld32(trow + 128 + c, v);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t ov[32];
+              dev::tmem_ld32(t_o + 32 * c, ov);
               dev::tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
-              dev::tmem_st32(trow + 128 + c, v);
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+              dev::tmem_st32(t_o + 32 * c, ov);
             }
-            dev::tmem_wait_st();
           }
-          mref = ref;
+          mref = mx;
         }
-        // V rows past the context or past the loaded blocks are zeroed, so
-        // whatever bits they hold never meet a zero probability
-        if (!dev::mbar_wait_bounded(&kv_full[st], (k >> 1) & 1, tmo, p.status)) {
-          ok = false;
-          break;
+        // P = 2^(s scale log2 e - ref) in the input type, over S's first 64 columns
+        const float ref = mref;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int ta = t0 + 32 * c + 2 * i;
+            float e0, e1;
+            if (whole) {
+              e0 = dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -ref));
+              e1 = dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -ref));
+            } else {
+              e0 = ta <= pos ? dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -ref)) : 0.f;
+              e1 = ta + 1 <= pos ? dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -ref))
+                                 : 0.f;
+            }
+            l += e0 + e1;
+            sv[c >> 1][16 * (c & 1) + i] = M::pack(e0, e1);
+          }
         }
-        {
-          const int tok = t0 + r;
-          const int bound = min(ctx, nblk * kBlockSize);
-          if (tok >= bound) {
-            uint8_t* vrow = smem + TcSmem::kV + st * 2 * TcSmem::kChunk + r * 128;
+        dev::tmem_st32(t_s, sv[0]);
+        dev::tmem_st32(t_s + 32, sv[1]);
+        if (w == 0 && t0 + kTcTokens > bound) {
+          // rows of the last V tile past the context or past the loaded
+          // blocks are zeroed, so whatever bits they hold meet only p = 0
+          if (!dev::mbar_wait_bounded(&v_full[kt & 1], (kt >> 1) & 1, tmo, p.status)) ok = false;
+          if (ok && t0 + r >= bound) {
+            uint8_t* vrow = smem + TcSmem::kV + (kt & 1) * 2 * TcSmem::kChunk + r * 128;
             for (int h = 0; h < 2; ++h)
               for (int q16 = 0; q16 < 8; ++q16)
                 *reinterpret_cast<uint4*>(vrow + h * TcSmem::kChunk + q16 * 16) =
                     make_uint4(0, 0, 0, 0);
           }
+          dev::fence_proxy_async_smem();
         }
-        // pass 2: P = 2^(s - ref) in the input type, row sum, P to shared memory
-        for (int c = 0; c < kTcTokens; c += 32) {
-          uint32_t v[32];
-          dev::tmem_ld32(trow + c, v);
-          dev::tmem_wait_ld();
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int ta = t0 + c + 2 * i;
-            const float x0 = ta <= pos && ref != -INFINITY ? __uint_as_float(v[2 * i]) * sl2 - ref : -INFINITY;
-            const float x1 = ta + 1 <= pos && ref != -INFINITY ? __uint_as_float(v[2 * i + 1]) * sl2 - ref : -INFINITY;
-            pk[i] = M::pack(dev::fast_exp2(x0), dev::fast_exp2(x1));
-            const float2 f = M::unpack(pk[i]);
-            l += f.x + f.y;
-          }
-          // 32 tokens = 4 chunks of 16 bytes; chunk index along the row
-          // (tokens / 8), swizzled by the row within its 8-row group
-#pragma unroll
-          for (int q16 = 0; q16 < 4; ++q16) {
-            const int chunk = (c >> 3) + q16;  // 0..15 over the 128 tokens
-            const int h = chunk >> 3, w = chunk & 7;
-            uint8_t* dst = smem + TcSmem::kP + h * TcSmem::kChunk + r * 128 + ((w ^ (r & 7)) << 4);
-            *reinterpret_cast<uint4*>(dst) =
-                make_uint4(pk[4 * q16], pk[4 * q16 + 1], pk[4 * q16 + 2], pk[4 * q16 + 3]);
-          }
-        }
-        dev::fence_proxy_async_smem();
+        if (w == 0) ++kt;
+        dev::tmem_wait_st();
         dev::tc_fence_before_sync();
-        dev::mbar_arrive(p_full);
+        dev::mbar_arrive(&p_full[w]);
       }
-      if (ok) {
-        // the tile's O is complete: normalise and write
-        if (!dev::mbar_wait_bounded(o_full, o_count & 1, tmo, p.status)) ok = false;
-        if (ok) {
-          dev::tc_fence_after_sync();
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          T* orow = static_cast<T*>(p.out) +
-                    (size_t(q_first + (valid ? gr / G : 0)) * Hq + g * G + (valid ? gr % G : 0)) * D;
-          for (int c = 0; c < D; c += 32) {
-            uint32_t v[32];
-            dev::tmem_ld32(trow + 128 + c, v);
-            dev::tmem_wait_ld();
-            if (valid) {
+      if (!ok) break;
+      // O_w is complete once the last P V has finished: normalise and write
+      if (!dev::mbar_wait_bounded(&pv_done[w], (cnt - 1) & 1, tmo, p.status)) {
+        ok = false;
+        break;
+      }
+      dev::tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint32_t ov[4][32];
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint4 w;
-                w.x = M::pack(__uint_as_float(v[8 * i + 0]) * inv, __uint_as_float(v[8 * i + 1]) * inv);
-                w.y = M::pack(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv);
-                w.z = M::pack(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv);
-                w.w = M::pack(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv);
-                *reinterpret_cast<uint4*>(orow + c + 8 * i) = w;
-              }
-            }
+      for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_o + 32 * c, ov[c]);
+      dev::tmem_wait_ld();
+      if (valid) {
+        T* orow = static_cast<T*>(p.out) +
+                  (size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G) * D;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = M::pack(__uint_as_float(ov[c][8 * i + 0]) * inv, __uint_as_float(ov[c][8 * i + 1]) * inv);
+            v.y = M::pack(__uint_as_float(ov[c][8 * i + 2]) * inv, __uint_as_float(ov[c][8 * i + 3]) * inv);
+            v.z = M::pack(__uint_as_float(ov[c][8 * i + 4]) * inv, __uint_as_float(ov[c][8 * i + 5]) * inv);
+            v.w = M::pack(__uint_as_float(ov[c][8 * i + 6]) * inv, __uint_as_float(ov[c][8 * i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * i) = v;
           }
-        }
       }
+      // O_w is read: the next item's first P V may overwrite it
+      dev::tc_fence_before_sync();
     }
-    // every thread agrees before the next item (the TMEM and the ring are reused)
-    dev::tc_fence_before_sync();
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    dev::tc_fence_after_sync();
-    kv_tiles += ntiles;
-    q_loads += 1;
-    s_count += ntiles;
-    p_count += ntiles;
-    o_count += 1;
-  }
-  if (!ok && issuer) {
-    // a wait ran out: let the copies and MMAs in flight finish before leaving
-    dev::tc_commit(o_full);
-    dev::mbar_wait_bounded(o_full, o_count & 1, tmo, p.status);
-    for (int k = kv_tiles; k < kv_tiles + 2; ++k)
-      dev::mbar_wait_bounded(&kv_full[k & 1], (k >> 1) & 1, tmo, p.status);
   }
   dev::tc_fence_before_sync();
-  __syncthreads();
-  if (warp == 4) {
+  const bool all_ok = __syncthreads_and(ok);
+  if (warp == 9) {
     dev::tc_fence_after_sync();
     dev::tmem_dealloc(tmem, kTcCols);
   }
-  if (threadIdx.x == 0 && planned && ok) {
+  if (threadIdx.x == 0 && planned && all_ok) {
     __threadfence();
     if (atomicAdd(&p.header[kHdrDone], 1) == int(gridDim.x) - 1) {
       atomicExch(&p.header[kHdrNext], 0);
@@ -1359,6 +1439,7 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int G = num_q_heads / num_kv_heads;
   const bool use_tc = tc_wanted() && st.tc_ok && prm.shared_ctx == 0 && head_dim == 128 &&
+                      prm.scale_log2 > 0.f &&
                       (G == 1 || G == 2 || G == 4 || G == 8);
   prm.ncta = use_tc ? st.sms : st.sms * per_sm;
   prm.no_split = use_tc ? 1 : 0;
@@ -1382,7 +1463,7 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
   pc.stream = s;
   pc.attrs = attr;
   pc.numAttrs = 1;
-  cudaError_t e = use_tc ? cudaLaunchKernelEx(&pc, prefill_plan_kernel<kTcRows>, prm)
+  cudaError_t e = use_tc ? cudaLaunchKernelEx(&pc, prefill_plan_kernel<kTcItemRows>, prm)
                          : cudaLaunchKernelEx(&pc, prefill_plan_kernel<kRows>, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
   if (use_tc) {
