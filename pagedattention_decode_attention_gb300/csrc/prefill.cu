@@ -1054,22 +1054,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + 32 * c, sv[c]);
         dev::tmem_wait_ld();
-        const bool whole = t0 + kTcTokens - 1 <= pos;  // no masked column in this row
-        float mx = -INFINITY;
-        if (whole) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
-        } else {
+        if (t0 + kTcTokens - 1 > pos) {
+          // columns past the row's position (causal, context) do not count
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              if (t0 + 32 * c + i <= pos) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+              if (t0 + 32 * c + i > pos) sv[c][i] = __float_as_uint(-INFINITY);
         }
-        mx *= sl2;
-        if (mx > mref + kTcRescale || (mref == -INFINITY && mx != -INFINITY)) {
+        // row maximum: eight independent chains of three-input maxima
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t* v = &sv[k >> 1][16 * (k & 1)];
+          float m = dev::fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+#pragma unroll
+          for (int i = 3; i < 15; i += 2) m = dev::fmax3(m, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+          m8[k] = fmaxf(m, __uint_as_float(v[15]));
+        }
+        float mx = dev::fmax3(dev::fmax3(m8[0], m8[1], m8[2]), dev::fmax3(m8[3], m8[4], m8[5]),
+                              fmaxf(m8[6], m8[7])) * sl2;
+        if (mx > mref + kTcRescale) {  // also the row's first unmasked column
           if (mref != -INFINITY) {
             // O_w holds every earlier tile (S_w of this tile was issued after
             // the previous P V finished): rescale it in TMEM
@@ -1087,26 +1092,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           mref = mx;
         }
-        // P = 2^(s scale log2 e - ref) in the input type, over S's first 64 columns
-        const float ref = mref;
+        // P = 2^(s scale log2 e - ref) in the input type, over S's first 64
+        // columns; masked columns (-inf) give 0.  A row with nothing visible
+        // yet (ref -inf) uses 0 as its reference: every p is 0 then.
+        const float nref = mref == -INFINITY ? 0.f : -mref;
+        float acc[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int ta = t0 + 32 * c + 2 * i;
-            float e0, e1;
-            if (whole) {
-              e0 = dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -ref));
-              e1 = dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -ref));
-            } else {
-              e0 = ta <= pos ? dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -ref)) : 0.f;
-              e1 = ta + 1 <= pos ? dev::fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -ref))
-                                 : 0.f;
-            }
-            l += e0 + e1;
+            float x0, x1;
+            dev::fma2_scalar(x0, x1, __uint_as_float(sv[c][2 * i]), __uint_as_float(sv[c][2 * i + 1]),
+                             sl2, nref);
+            const float e0 = dev::fast_exp2(x0), e1 = dev::fast_exp2(x1);
+            dev::add2(acc[i & 3][0], acc[i & 3][1], e0, e1);
             sv[c >> 1][16 * (c & 1) + i] = M::pack(e0, e1);
           }
         }
+        l += ((acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1])) +
+             ((acc[2][0] + acc[2][1]) + (acc[3][0] + acc[3][1]));
         dev::tmem_st32(t_s, sv[0]);
         dev::tmem_st32(t_s + 32, sv[1]);
         if (w == 0 && t0 + kTcTokens > bound) {

@@ -91,6 +91,28 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// --------------------------------------------- packed / three-input fp32
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (x0, x1) * s + (r, r), both lanes in one instruction, round to nearest
+__device__ __forceinline__ void fma2_scalar(float& y0, float& y1, float x0, float x1, float s,
+                                            float r) {
+  asm("{\n\t.reg .b64 x, sc, rr, y;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 sc, {%4, %4};\n\t"
+      "mov.b64 rr, {%5, %5};\n\tfma.rn.f32x2 y, x, sc, rr;\n\tmov.b64 {%0, %1}, y;\n\t}"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(s), "f"(r));
+}
+// (a0, a1) += (b0, b1)
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, z, y;\n\tmov.b64 x, {%0, %1};\n\tmov.b64 z, {%2, %3};\n\t"
+      "add.rn.f32x2 y, x, z;\n\tmov.b64 {%0, %1}, y;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
 // Per-thread register budget of the executing warpgroup (every warp of the
 // warpgroup runs it): dec gives registers back to the CTA's pool, inc waits
 // until the pool holds enough.
