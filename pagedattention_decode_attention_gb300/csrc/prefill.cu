@@ -739,6 +739,38 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 // in base 2 against a reference that moves only when a row's maximum grows by
 // more than 2^8 (O_w is then rescaled in TMEM; the result is the same either
 // way).
+// Optional per-role wait counters (SM cycles), compiled in only with
+// -DPA_PROFILE_TIMES (a separate build; the default build has none of it).
+// Per CTA 32 slots of 8: MMA thread, softmax group 0 (its thread 0), group 1,
+// producer lane 0; the last slot of each is the role's total (the meaning of
+// each other slot is where it is added).
+#ifdef PA_PROFILE_TIMES
+__device__ unsigned long long g_pf_times[2048 * 32];
+#define PF_DECL long long pf_[8] = {0, 0, 0, 0, 0, 0, 0, 0}; const long long pf_start_ = clock64()
+#define PF_WAIT(slot, call)                    \
+  ([&]() {                                     \
+    const long long t_ = clock64();            \
+    const bool r_ = (call);                    \
+    pf_[slot] += clock64() - t_;               \
+    return r_;                                 \
+  }())
+#define PF_MARK(name) const long long name = clock64()
+#define PF_ADD(slot, since) pf_[slot] += clock64() - (since)
+#define PF_STORE(base, on)                                                             \
+  do {                                                                                 \
+    if (on) {                                                                          \
+      pf_[7] = clock64() - pf_start_;                                                  \
+      for (int i_ = 0; i_ < 8; ++i_) g_pf_times[blockIdx.x * 32 + (base) + i_] = pf_[i_]; \
+    }                                                                                  \
+  } while (0)
+#else
+#define PF_DECL
+#define PF_WAIT(slot, call) (call)
+#define PF_MARK(name)
+#define PF_ADD(slot, since)
+#define PF_STORE(base, on)
+#endif
+
 constexpr int kTcRows = 128;       // query rows per tile (TMEM lanes)
 constexpr int kTcItemRows = 256;   // two query tiles per work item
 constexpr int kTcTokens = 128;     // tokens per KV tile
@@ -848,13 +880,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 8) {
     // ====================================================== producer warp
     const uint64_t policy = dev::l2_policy_evict_first();
+    PF_DECL;
     int kt = 0;  // K / V tiles loaded so far
     int qn = 0;  // query-tile loads so far
     for (int n = 0;; ++n) {
       const int slot = n & 1;
       int x = 0;
       if (lane == 0) {
-        if (n >= 2) ok = dev::mbar_wait_bounded(&item_empty[slot], ((n >> 1) - 1) & 1, tmo, p.status);
+        if (n >= 2)
+          ok = PF_WAIT(0, dev::mbar_wait_bounded(&item_empty[slot], ((n >> 1) - 1) & 1, tmo, p.status));
         x = n == 0 ? int(blockIdx.x) : int(gridDim.x) + atomicAdd(&p.header[kHdrNext], 1);
         if (!ok) x = total;  // stop every role
         s_item[slot] = x;
@@ -865,7 +899,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (x >= total) break;
       const Item it = decode(x);
       if (lane == 0) {
-        if (n >= 1) ok = dev::mbar_wait_bounded(q_empty, (n - 1) & 1, tmo, p.status);
+        if (n >= 1) ok = PF_WAIT(1, dev::mbar_wait_bounded(q_empty, (n - 1) & 1, tmo, p.status));
         if (ok) {
           const int tiles = it.two ? 2 : 1;
           ++qn;
@@ -905,7 +939,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint64_t* full = kind == 0 ? &k_full[st] : &v_full[st];
           uint64_t* empty = kind == 0 ? &k_empty[st] : &v_empty[st];
           if (lane == 0) {
-            if (kt >= 2) ok = dev::mbar_wait_bounded(empty, ((kt >> 1) - 1) & 1, tmo, p.status);
+            if (kt >= 2)
+              ok = PF_WAIT(2 + kind, dev::mbar_wait_bounded(empty, ((kt >> 1) - 1) & 1, tmo, p.status));
             if (ok) dev::mbar_arrive_expect_tx(full, uint32_t(nb) * 4 * 1024);
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -923,6 +958,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (!ok) break;
     }
+    PF_STORE(24, lane == 0);
     if (lane == 0) {
       // copies still in flight land before the CTA leaves
       if (qn > 0) dev::mbar_wait_bounded(q_full, (qn - 1) & 1, tmo, p.status);
@@ -933,87 +969,96 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 9) {
     // ====================================================== MMA warp
-    if (lane == 0) {
-      const uint32_t idesc_s = dev::mma_idesc_f16(kBf16, kTcRows, kTcTokens, false);
-      const uint32_t idesc_o = dev::mma_idesc_f16(kBf16, kTcRows, D, true);
-      // operand descriptors of the tiles' first bytes; a step adds its byte
-      // offset / 16 to the address field (no carry: shared addresses < 256 KB)
-      const uint64_t desc_q = dev::smem_desc_sw128(sbase + TcSmem::kQ, 16, 1024);
-      const uint64_t desc_k = dev::smem_desc_sw128(sbase + TcSmem::kK, 16, 1024);
-      const uint64_t desc_v = dev::smem_desc_sw128(sbase + TcSmem::kV, TcSmem::kChunk, 1024);
-      int kt = 0;         // K / V tiles consumed
-      int pv[2] = {0, 0};  // P V products issued per query tile
-      for (int n = 0; ok; ++n) {
-        const int slot = n & 1;
-        if (!dev::mbar_wait_bounded(&item_full[slot], (n >> 1) & 1, tmo, p.status)) {
-          ok = false;
-          break;
-        }
-        const int x = *reinterpret_cast<volatile int*>(&s_item[slot]);
-        dev::mbar_arrive(&item_empty[slot]);
-        if (x >= total) break;
-        const Item it = decode(x);
-        const int tiles = it.two ? 2 : 1;
-        ok = dev::mbar_wait_bounded(q_full, n & 1, tmo, p.status);
-        // S_w = Q_w K_j^T once O_w += P_w V of the previous tile has finished
-        // (P_w sits in S_w's columns)
-        auto issue_s = [&](int w, int j, int st) -> bool {
-          if (pv[w] > 0 && !dev::mbar_wait_bounded(&pv_done[w], (pv[w] - 1) & 1, tmo, p.status))
-            return false;
-          dev::tc_fence_after_sync();
-          const uint64_t a = desc_q + uint32_t((w * 2 * TcSmem::kChunk) >> 4);
-          const uint64_t bk = desc_k + uint32_t((st * 2 * TcSmem::kChunk) >> 4);
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = uint32_t(((kk >> 2) * TcSmem::kChunk + (kk & 3) * 32) >> 4);
-            dev::tc_mma_f16(tmem + w * 128, a + off, bk + off, idesc_s, kk > 0);
-          }
-          dev::tc_commit(&s_full[w]);
-          return true;
-        };
-        auto issue_pv = [&](int w, int j, int st) -> bool {
-          if (!dev::mbar_wait_bounded(&p_full[w], pv[w] & 1, tmo, p.status)) return false;
-          dev::tc_fence_after_sync();
-          const uint64_t bv = desc_v + uint32_t((st * 2 * TcSmem::kChunk) >> 4);
-#pragma unroll 1
-          for (int kk = 0; kk < kTcTokens / 16; ++kk)
-            dev::tc_mma_f16_ts(tmem + 256 + w * 128, tmem + w * 128 + kk * 8,
-                               bv + uint32_t((kk * 2048) >> 4), idesc_o, j > 0 || kk > 0);
-          dev::tc_commit(&pv_done[w]);
-          ++pv[w];
-          return true;
-        };
-        // prologue: S of the first tile for both query tiles
-        if (ok) ok = dev::mbar_wait_bounded(&k_full[kt & 1], (kt >> 1) & 1, tmo, p.status);
-        for (int w = 0; w < tiles && ok; ++w) ok = issue_s(w, 0, kt & 1);
-        if (ok) {
-          dev::tc_commit(&k_empty[kt & 1]);
-          if (it.ntiles == 1) dev::tc_commit(q_empty);
-        }
-        for (int j = 0; j < it.ntiles && ok; ++j) {
-          const int st = (kt + j) & 1, nst = (kt + j + 1) & 1;
-          const bool more = j + 1 < it.ntiles;
-          ok = dev::mbar_wait_bounded(&v_full[st], ((kt + j) >> 1) & 1, tmo, p.status);
-          if (ok) ok = issue_pv(0, j, st);
-          if (ok && more) {
-            ok = dev::mbar_wait_bounded(&k_full[nst], ((kt + j + 1) >> 1) & 1, tmo, p.status);
-            if (ok) ok = issue_s(0, j + 1, nst);
-          }
-          if (ok && tiles == 2) ok = issue_pv(1, j, st);
-          if (ok) dev::tc_commit(&v_empty[st]);
-          if (ok && more && tiles == 2) ok = issue_s(1, j + 1, nst);
-          if (ok && more) {
-            dev::tc_commit(&k_empty[nst]);
-            if (j + 2 == it.ntiles) dev::tc_commit(q_empty);
-          }
-        }
-        kt += it.ntiles;
+    // The whole warp runs the loop (descriptors stay warp-uniform); the lane
+    // elected here issues every MMA and commit.
+    const uint32_t leader = dev::elect_one();
+    const uint32_t idesc_s = dev::mma_idesc_f16(kBf16, kTcRows, kTcTokens, false);
+    const uint32_t idesc_o = dev::mma_idesc_f16(kBf16, kTcRows, D, true);
+    // operand descriptors of the tiles' first bytes; a step adds its byte
+    // offset / 16 to the address field (the low 14 bits: below 256 KB of
+    // shared memory an offset never carries out of it)
+    const uint64_t desc_q = dev::smem_desc_sw128(sbase + TcSmem::kQ, 16, 1024);
+    const uint64_t desc_k = dev::smem_desc_sw128(sbase + TcSmem::kK, 16, 1024);
+    const uint64_t desc_v = dev::smem_desc_sw128(sbase + TcSmem::kV, TcSmem::kChunk, 1024);
+    // every lane waits; the warp goes on only if every lane saw the phase
+    auto wait = [&](uint64_t* bar, int parity) -> bool {
+      return __all_sync(0xffffffffu, dev::mbar_wait_bounded(bar, uint32_t(parity), tmo, p.status));
+    };
+    int kt = 0;          // K / V tiles consumed
+    int pv[2] = {0, 0};  // P V products issued per query tile
+    PF_DECL;
+    for (int n = 0; ok; ++n) {
+      const int slot = n & 1;
+      if (!PF_WAIT(0, wait(&item_full[slot], (n >> 1) & 1))) {
+        ok = false;
+        break;
       }
-      if (!ok) {
-        // a wait ran out: let the MMAs in flight finish before TMEM is freed
-        dev::tc_commit(drain);
-        dev::mbar_wait_bounded(drain, 0, tmo, p.status);
+      const int x = *reinterpret_cast<volatile int*>(&s_item[slot]);
+      __syncwarp();
+      if (leader) dev::mbar_arrive(&item_empty[slot]);
+      if (x >= total) break;
+      const Item it = decode(x);
+      const int tiles = it.two ? 2 : 1;
+      ok = PF_WAIT(1, wait(q_full, n & 1));
+      // S_w = Q_w K_j^T once O_w += P_w V of the previous tile has finished
+      // (P_w sits in S_w's columns)
+      auto issue_s = [&](int w, int st) -> bool {
+        if (pv[w] > 0 && !PF_WAIT(5, wait(&pv_done[w], (pv[w] - 1) & 1))) return false;
+        dev::tc_fence_after_sync();
+        const uint64_t a = desc_q + uint64_t((w * 2 * TcSmem::kChunk) >> 4);
+        const uint64_t bk = desc_k + uint64_t((st * 2 * TcSmem::kChunk) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = uint64_t(((kk >> 2) * TcSmem::kChunk + (kk & 3) * 32) >> 4);
+          dev::tc_mma_ss_leader(tmem + w * 128, a + off, bk + off, idesc_s, uint32_t(kk), leader);
+        }
+        dev::tc_commit_leader(&s_full[w], leader);
+        return true;
+      };
+      auto issue_pv = [&](int w, int j, int st) -> bool {
+        if (!PF_WAIT(4, wait(&p_full[w], pv[w] & 1))) return false;
+        dev::tc_fence_after_sync();
+        const uint64_t bv = desc_v + uint64_t((st * 2 * TcSmem::kChunk) >> 4);
+        const uint32_t d = tmem + 256 + w * 128, pa = tmem + w * 128;
+        dev::tc_mma_ts_leader(d, pa, bv, idesc_o, uint32_t(j), leader);
+#pragma unroll
+        for (int kk = 1; kk < kTcTokens / 16; ++kk)
+          dev::tc_mma_ts_leader(d, pa + kk * 8, bv + uint64_t((kk * 2048) >> 4), idesc_o, 1u, leader);
+        dev::tc_commit_leader(&pv_done[w], leader);
+        ++pv[w];
+        return true;
+      };
+      // prologue: S of the first tile for both query tiles
+      if (ok) ok = PF_WAIT(2, wait(&k_full[kt & 1], (kt >> 1) & 1));
+      for (int w = 0; w < tiles && ok; ++w) ok = issue_s(w, kt & 1);
+      if (ok) {
+        dev::tc_commit_leader(&k_empty[kt & 1], leader);
+        if (it.ntiles == 1) dev::tc_commit_leader(q_empty, leader);
       }
+      for (int j = 0; j < it.ntiles && ok; ++j) {
+        const int st = (kt + j) & 1, nst = (kt + j + 1) & 1;
+        const bool more = j + 1 < it.ntiles;
+        ok = PF_WAIT(3, wait(&v_full[st], ((kt + j) >> 1) & 1));
+        if (ok) ok = issue_pv(0, j, st);
+        if (ok && more) {
+          ok = PF_WAIT(2, wait(&k_full[nst], ((kt + j + 1) >> 1) & 1));
+          if (ok) ok = issue_s(0, nst);
+        }
+        if (ok && tiles == 2) ok = issue_pv(1, j, st);
+        if (ok) dev::tc_commit_leader(&v_empty[st], leader);
+        if (ok && more && tiles == 2) ok = issue_s(1, nst);
+        if (ok && more) {
+          dev::tc_commit_leader(&k_empty[nst], leader);
+          if (j + 2 == it.ntiles) dev::tc_commit_leader(q_empty, leader);
+        }
+      }
+      kt += it.ntiles;
+    }
+    PF_STORE(0, leader != 0);
+    if (!ok) {
+      // a wait ran out: let the MMAs in flight finish before TMEM is freed
+      dev::tc_commit_leader(drain, leader);
+      dev::mbar_wait_bounded(drain, 0, tmo, p.status);
     }
     __syncwarp();
   } else if (warp < 8) {
@@ -1026,9 +1071,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float sl2 = p.scale_log2;       // > 0 on this path
     int cnt = 0;                          // tiles of this group so far
     int kt = 0;                           // K / V tiles so far (group 0 sees them all)
+    PF_DECL;
     for (int n = 0;; ++n) {
       const int slot = n & 1;
-      if (!dev::mbar_wait_bounded(&item_full[slot], (n >> 1) & 1, tmo, p.status)) {
+      if (!PF_WAIT(0, dev::mbar_wait_bounded(&item_full[slot], (n >> 1) & 1, tmo, p.status))) {
         ok = false;
         break;
       }
@@ -1044,10 +1090,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int bound = min(it.ctx, it.nblk * kBlockSize);
       float mref = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ntiles && ok; ++j, ++cnt) {
-        if (!dev::mbar_wait_bounded(&s_full[w], cnt & 1, tmo, p.status)) {
+        if (!PF_WAIT(1, dev::mbar_wait_bounded(&s_full[w], cnt & 1, tmo, p.status))) {
           ok = false;
           break;
         }
+        PF_MARK(pf_tile);
         dev::tc_fence_after_sync();
         const int t0 = j * kTcTokens;
         uint32_t sv[4][32];
@@ -1130,13 +1177,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dev::tmem_wait_st();
         dev::tc_fence_before_sync();
         dev::mbar_arrive(&p_full[w]);
+        PF_ADD(2, pf_tile);
       }
       if (!ok) break;
       // O_w is complete once the last P V has finished: normalise and write
-      if (!dev::mbar_wait_bounded(&pv_done[w], (cnt - 1) & 1, tmo, p.status)) {
+      if (!PF_WAIT(3, dev::mbar_wait_bounded(&pv_done[w], (cnt - 1) & 1, tmo, p.status))) {
         ok = false;
         break;
       }
+      PF_MARK(pf_epi);
       dev::tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint32_t ov[4][32];
@@ -1160,7 +1209,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       // O_w is read: the next item's first P V may overwrite it
       dev::tc_fence_before_sync();
+      PF_ADD(4, pf_epi);
     }
+    PF_STORE(8 + 8 * w, r == 0);
   }
   dev::tc_fence_before_sync();
   const bool all_ok = __syncthreads_and(ok);
@@ -1340,6 +1391,16 @@ using namespace pa;
 using namespace pa::prefill;
 
 extern "C" {
+
+#ifdef PA_PROFILE_TIMES
+PA_API int pa_profile_prefill_times(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, pa::prefill::g_pf_times, size_t(n) * sizeof(unsigned long long)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+#endif
+
 
 PA_API int pa_paged_attention_prefill_workspace_size(int num_seqs, int total_q, int num_q_heads,
                                                      int num_kv_heads, int head_dim,
