@@ -280,6 +280,41 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
                                       size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_prefill_plan / pa_paged_attention_prefill_run -- the two
+ * launches of pa_paged_attention_prefill as separate calls, so that one plan
+ * serves every layer of a model step (the chunks, and so the work list, are
+ * the same in every layer).  (No counterpart on the pages: the split exists
+ * for callers, not for the method.)
+ *
+ * _plan reads only context_lens and query_start (device) and the sizes, and
+ * writes the work list into the workspace; scale and dtype pick the kernel
+ * the work list is cut for.  _run takes pa_paged_attention_prefill's
+ * arguments and launches only the attention kernel; it needs a plan made
+ * with the same sizes, dtype and sign of scale and with the same
+ * context_lens / query_start contents, in stream order on the same
+ * workspace.  A run whose workspace holds no plan for its sizes does nothing
+ * and sets the status word (pa_check_status returns PA_ERR_INVALID_ARG);
+ * changed lengths under the same sizes are not detected and give unspecified
+ * output.  Runs may follow one plan any number of times, on any caches,
+ * queries and outputs; each leaves the workspace ready for the next.  After
+ * a run that timed out, plan again.  For PA_F32 the plan does nothing and
+ * the run is the whole call.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_prefill_plan(const int32_t* context_lens,
+                                           const int32_t* query_start, int num_seqs,
+                                           int total_q, int num_q_heads, int num_kv_heads,
+                                           int head_dim, int max_blocks_per_seq, float scale,
+                                           int dtype, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+PA_API int pa_paged_attention_prefill_run(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, const int32_t* context_lens,
+                                          const int32_t* query_start, int num_seqs, int total_q,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq, int num_blocks, float scale,
+                                          int dtype, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_decode_noalloc -- pa_paged_attention_decode without a
  * caller-provided workspace.  (No counterpart on the pages: this entry point
  * exists for callers, not for the method.)

@@ -11,7 +11,9 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
   token in the same launch; :func:`paged_attention_decode_shared_prefix` reads
   a prefix shared by the whole batch once);
 * :func:`paged_attention_prefill` -- chunked-prefill attention: each
-  sequence's newest tokens attend causally over the paged cache;
+  sequence's newest tokens attend causally over the paged cache
+  (:func:`prefill_plan` + :func:`paged_attention_prefill_run` split it so one
+  plan serves every layer);
 * :func:`block_copy` -- copy-on-write block copies across all layers;
 * :func:`block_swap` -- whole blocks between the device caches and
   page-locked host caches (preemption / offload), all layers in one launch;
@@ -26,8 +28,8 @@ from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
 from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
                   block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
-                  paged_attention_prefill, shared_prefix_workspace_size,
-                  prefill_workspace_size,
+                  paged_attention_prefill, paged_attention_prefill_run, prefill_plan,
+                  shared_prefix_workspace_size, prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,
                   prepare_decode_append_run, prepare_decode_plan, prepare_decode_run,
                   prepare_kv_append, workspace_size)

@@ -72,6 +72,10 @@ SIGNATURES = {
     "pa_paged_attention_prefill_workspace_size": (_i, [_i, _i, _i, _i, _i, C.POINTER(_sz)]),
     "pa_paged_attention_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                         C.c_float, _i, _vp, _vp, _sz, _vp]),
+    "pa_paged_attention_prefill_plan": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _i, C.c_float, _i,
+                                             _vp, _sz, _vp]),
+    "pa_paged_attention_prefill_run": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                            _i, C.c_float, _i, _vp, _vp, _sz, _vp]),
     "pa_paged_attention_decode_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                                C.c_float, _i, _vp, _vp]),
     "pa_block_copy": (_i, [C.POINTER(_vp), C.POINTER(_vp), _i, _vp, _i, _i, _i, _i, _i, _vp]),

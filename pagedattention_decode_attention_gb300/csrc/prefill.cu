@@ -756,6 +756,11 @@ __device__ unsigned long long g_pf_times[2048 * 32];
   }())
 #define PF_MARK(name) const long long name = clock64()
 #define PF_ADD(slot, since) pf_[slot] += clock64() - (since)
+__device__ unsigned long long g_pf_stamps[2048 * 4];
+#define PF_STAMP(i)                                                                    \
+  do {                                                                                 \
+    if (threadIdx.x == 0) g_pf_stamps[blockIdx.x * 4 + (i)] = dev::global_timer_ns();  \
+  } while (0)
 #define PF_STORE(base, on)                                                             \
   do {                                                                                 \
     if (on) {                                                                          \
@@ -769,6 +774,7 @@ __device__ unsigned long long g_pf_times[2048 * 32];
 #define PF_MARK(name)
 #define PF_ADD(slot, since)
 #define PF_STORE(base, on)
+#define PF_STAMP(i)
 #endif
 
 constexpr int kTcRows = 128;       // query rows per tile (TMEM lanes)
@@ -821,6 +827,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t sbase = dev::smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  PF_STAMP(0);
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(&item_full[i], 1);
@@ -855,6 +862,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
   bool ok = true;
+  PF_STAMP(1);
 
   // what every role decodes from a claimed item
   struct Item {
@@ -1195,17 +1203,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (valid) {
         T* orow = static_cast<T*>(p.out) +
                   (size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G) * D;
+        // a row is 256 bytes: whole 32-byte sectors per store when the
+        // output is 32-byte aligned, 16-byte stores otherwise
+        const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31) == 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 v;
-            v.x = M::pack(__uint_as_float(ov[c][8 * i + 0]) * inv, __uint_as_float(ov[c][8 * i + 1]) * inv);
-            v.y = M::pack(__uint_as_float(ov[c][8 * i + 2]) * inv, __uint_as_float(ov[c][8 * i + 3]) * inv);
-            v.z = M::pack(__uint_as_float(ov[c][8 * i + 4]) * inv, __uint_as_float(ov[c][8 * i + 5]) * inv);
-            v.w = M::pack(__uint_as_float(ov[c][8 * i + 6]) * inv, __uint_as_float(ov[c][8 * i + 7]) * inv);
-            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * i) = v;
+          for (int i = 0; i < 16; ++i)
+            pk[i] = M::pack(__uint_as_float(ov[c][2 * i]) * inv, __uint_as_float(ov[c][2 * i + 1]) * inv);
+          if (wide) {
+            dev::st_global_v8(orow + 32 * c, pk);
+            dev::st_global_v8(orow + 32 * c + 16, pk + 8);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              *reinterpret_cast<uint4*>(orow + 32 * c + 8 * i) =
+                  make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
           }
+        }
       }
       // O_w is read: the next item's first P V may overwrite it
       dev::tc_fence_before_sync();
@@ -1213,12 +1229,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     PF_STORE(8 + 8 * w, r == 0);
   }
+  PF_STAMP(2);
   dev::tc_fence_before_sync();
   const bool all_ok = __syncthreads_and(ok);
   if (warp == 9) {
     dev::tc_fence_after_sync();
     dev::tmem_dealloc(tmem, kTcCols);
   }
+  PF_STAMP(3);
   if (threadIdx.x == 0 && planned && all_ok) {
     __threadfence();
     if (atomicAdd(&p.header[kHdrDone], 1) == int(gridDim.x) - 1) {
@@ -1362,6 +1380,9 @@ int device_setup(int device) {
 
 int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
               cudaStream_t s, const char* who);
+bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* workspace);
+int launch_plan(const Params& prm, bool use_tc, cudaStream_t s, const char* who);
+int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, const char* who);
 
 int check_shapes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads, int head_dim,
                  int max_blocks_per_seq, int dtype, const char* who) {
@@ -1393,6 +1414,12 @@ using namespace pa::prefill;
 extern "C" {
 
 #ifdef PA_PROFILE_TIMES
+PA_API int pa_profile_prefill_stamps(unsigned long long* host, int n) {
+  return cudaMemcpyFromSymbol(host, pa::prefill::g_pf_stamps, size_t(n) * sizeof(unsigned long long)) ==
+                 cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
 PA_API int pa_profile_prefill_times(unsigned long long* host, int n) {
   return cudaMemcpyFromSymbol(host, pa::prefill::g_pf_times, size_t(n) * sizeof(unsigned long long)) ==
                  cudaSuccess
@@ -1413,24 +1440,36 @@ PA_API int pa_paged_attention_prefill_workspace_size(int num_seqs, int total_q, 
   return PA_OK;
 }
 
-PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* block_tables, const int32_t* context_lens,
-                                      const int32_t* query_start, int num_seqs, int total_q,
-                                      int num_q_heads, int num_kv_heads, int head_dim,
-                                      int max_blocks_per_seq, int num_blocks, float scale,
-                                      int dtype, void* out, void* workspace,
-                                      size_t workspace_bytes, void* stream) {
-  const char* who = "paged_attention_prefill";
+}  // extern "C"
+
+namespace pa {
+namespace prefill {
+namespace {
+
+enum class Mode { kPlanAndRun, kPlanOnly, kRunOnly };
+
+// Validation, then the plan and / or the attention kernel.  The plan reads
+// only context_lens and query_start (and the sizes); q, the caches, the
+// tables and out may be NULL for Mode::kPlanOnly.
+int prefill_entry(Mode mode, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens,
+                  const int32_t* query_start, int num_seqs, int total_q, int num_q_heads,
+                  int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                  float scale, int dtype, void* out, void* workspace, size_t workspace_bytes,
+                  void* stream, const char* who) {
   int rc = check_shapes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
                         max_blocks_per_seq, dtype, who);
   if (rc != PA_OK) return rc;
   if (num_seqs == 0 || total_q == 0) return PA_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+  const bool runs = mode != Mode::kPlanOnly;
+  if (!context_lens || !query_start)
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
     return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
   auto misaligned = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15) != 0; };
-  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+  if (runs && (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out)))
     return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
-  if (num_blocks <= 0 || double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
+  if (runs && (num_blocks <= 0 || double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0))
     return fail(PA_ERR_INVALID_ARG, "%s: bad num_blocks", who);
   const Layout lay = workspace_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
@@ -1469,6 +1508,8 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
   prm.timeout_ns = 1000000000ull;
 
   if (dtype == PA_F32) {
+    // one warp per (row, head) needs no plan
+    if (!runs) return PA_OK;
     const long long units = (long long)total_q * num_q_heads;
     const int blocks = int((units + 3) / 4);
     if (head_dim == 64)
@@ -1479,8 +1520,59 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
     if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s (fp32): launch failed: %s", who, cudaGetErrorString(e));
     return PA_OK;
   }
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  if (mode != Mode::kRunOnly) {
+    rc = launch_plan(prm, use_tc, s, who);
+    if (rc != PA_OK) return rc;
+  }
+  return runs ? launch_attention(prm, use_tc, dtype, s, who) : PA_OK;
+}
 
-  return launch_tc(prm, lay, device, dtype, workspace, s, who);
+}  // namespace
+}  // namespace prefill
+}  // namespace pa
+
+extern "C" {
+
+PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, const int32_t* context_lens,
+                                      const int32_t* query_start, int num_seqs, int total_q,
+                                      int num_q_heads, int num_kv_heads, int head_dim,
+                                      int max_blocks_per_seq, int num_blocks, float scale,
+                                      int dtype, void* out, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  return pa::prefill::prefill_entry(pa::prefill::Mode::kPlanAndRun, q, k_cache, v_cache,
+                                    block_tables, context_lens, query_start, num_seqs, total_q,
+                                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                    num_blocks, scale, dtype, out, workspace, workspace_bytes,
+                                    stream, "paged_attention_prefill");
+}
+
+PA_API int pa_paged_attention_prefill_plan(const int32_t* context_lens,
+                                           const int32_t* query_start, int num_seqs,
+                                           int total_q, int num_q_heads, int num_kv_heads,
+                                           int head_dim, int max_blocks_per_seq, float scale,
+                                           int dtype, void* workspace, size_t workspace_bytes,
+                                           void* stream) {
+  return pa::prefill::prefill_entry(pa::prefill::Mode::kPlanOnly, nullptr, nullptr, nullptr,
+                                    nullptr, context_lens, query_start, num_seqs, total_q,
+                                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0,
+                                    scale, dtype, nullptr, workspace, workspace_bytes, stream,
+                                    "paged_attention_prefill_plan");
+}
+
+PA_API int pa_paged_attention_prefill_run(const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, const int32_t* context_lens,
+                                          const int32_t* query_start, int num_seqs, int total_q,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int max_blocks_per_seq, int num_blocks, float scale,
+                                          int dtype, void* out, void* workspace,
+                                          size_t workspace_bytes, void* stream) {
+  return pa::prefill::prefill_entry(pa::prefill::Mode::kRunOnly, q, k_cache, v_cache,
+                                    block_tables, context_lens, query_start, num_seqs, total_q,
+                                    num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                    num_blocks, scale, dtype, out, workspace, workspace_bytes,
+                                    stream, "paged_attention_prefill_run");
 }
 
 }  // extern "C"
@@ -1489,39 +1581,42 @@ namespace pa {
 namespace prefill {
 namespace {
 
-// Plan + tensor-core attention kernel for a filled-in Params (16-bit dtypes).
-int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
-              cudaStream_t s, const char* who) {
-  const int num_seqs = prm.num_seqs, total_q = prm.total_q, num_q_heads = prm.num_q_heads;
-  const int num_kv_heads = prm.num_kv_heads, head_dim = prm.head_dim;
-  const int max_blocks_per_seq = prm.max_blocks, num_blocks = prm.num_blocks;
-  const void* k_cache = prm.k_cache;
-  const void* v_cache = prm.v_cache;
-  int rc = PA_OK;
+// The plan-dependent fields of a filled-in Params (16-bit dtypes): which
+// kernel runs (its query-block size fixes the plan), the plan's signature and
+// the workspace's pieces.  Returns whether the tensor-core kernel runs.
+bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* workspace) {
   const DeviceState& st = g_dev[device];
   const bool bf16 = dtype == PA_BF16;
-  const int per_sm = st.ctas_per_sm[bf16][head_dim == 128];
+  const int per_sm = st.ctas_per_sm[bf16][prm.head_dim == 128];
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int G = num_q_heads / num_kv_heads;
-  const bool use_tc = tc_wanted() && st.tc_ok && prm.shared_ctx == 0 && head_dim == 128 &&
-                      prm.scale_log2 > 0.f &&
-                      (G == 1 || G == 2 || G == 4 || G == 8);
+  const int G = prm.num_q_heads / prm.num_kv_heads;
+  const bool use_tc = tc_wanted() && st.tc_ok && prm.shared_ctx == 0 && prm.head_dim == 128 &&
+                      prm.scale_log2 > 0.f && (G == 1 || G == 2 || G == 4 || G == 8);
   prm.ncta = use_tc ? st.sms : st.sms * per_sm;
   prm.no_split = use_tc ? 1 : 0;
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
-  prm.signature = signature_of(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
-                               max_blocks_per_seq) ^ (prm.shared_ctx << 1) ^
-                  (use_tc ? 0x2A000000 : 0);
+  prm.signature = signature_of(prm.num_seqs, prm.total_q, prm.num_q_heads, prm.num_kv_heads,
+                               prm.head_dim, prm.max_blocks) ^
+                  (prm.shared_ctx << 1) ^ (use_tc ? 0x2A000000 : 0);
   prm.header = reinterpret_cast<int*>(ws + lay.header);
   prm.units = reinterpret_cast<int4*>(ws + lay.units);
   prm.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
   prm.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   prm.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+  return use_tc;
+}
 
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+// The one-CTA plan kernel: the work list into the workspace.
+int launch_plan(const Params& prm, bool use_tc, cudaStream_t s, const char* who) {
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cudaLaunchConfig_t pc = {};
   pc.gridDim = dim3(1);
   pc.blockDim = dim3(kPlanThreads);
@@ -1531,11 +1626,22 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
   cudaError_t e = use_tc ? cudaLaunchKernelEx(&pc, prefill_plan_kernel<kTcItemRows>, prm)
                          : cudaLaunchKernelEx(&pc, prefill_plan_kernel<kRows>, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
+}
+
+// The attention kernel over a planned workspace.
+int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, const char* who) {
+  const bool bf16 = dtype == PA_BF16;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  alignas(64) CUtensorMap mq, mk, mv;
+  int rc = cache_tensor_map(&mk, prm.k_cache, bf16, prm.num_blocks, prm.num_kv_heads, prm.head_dim);
+  if (rc == PA_OK)
+    rc = cache_tensor_map(&mv, prm.v_cache, bf16, prm.num_blocks, prm.num_kv_heads, prm.head_dim);
+  if (rc != PA_OK) return rc;
+  cudaError_t e;
   if (use_tc) {
-    alignas(64) CUtensorMap mq, mk, mv;
-    rc = query_tensor_map(&mq, prm.q, bf16, total_q, num_q_heads, head_dim, G, kTcRows);
-    if (rc == PA_OK) rc = cache_tensor_map(&mk, k_cache, bf16, num_blocks, num_kv_heads, head_dim);
-    if (rc == PA_OK) rc = cache_tensor_map(&mv, v_cache, bf16, num_blocks, num_kv_heads, head_dim);
+    rc = query_tensor_map(&mq, prm.q, bf16, prm.total_q, prm.num_q_heads, prm.head_dim,
+                          prm.num_q_heads / prm.num_kv_heads, kTcRows);
     if (rc != PA_OK) return rc;
     cudaLaunchConfig_t tc = {};
     tc.gridDim = dim3(prm.ncta);
@@ -1546,31 +1652,33 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
     tc.numAttrs = 1;
     e = bf16 ? cudaLaunchKernelEx(&tc, prefill_tc_kernel<__nv_bfloat16>, mq, mk, mv, prm)
              : cudaLaunchKernelEx(&tc, prefill_tc_kernel<__half>, mq, mk, mv, prm);
-    if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
-    return PA_OK;
-  }
-
-  alignas(64) CUtensorMap mk, mv;
-  rc = cache_tensor_map(&mk, k_cache, bf16, num_blocks, num_kv_heads, head_dim);
-  if (rc == PA_OK) rc = cache_tensor_map(&mv, v_cache, bf16, num_blocks, num_kv_heads, head_dim);
-  if (rc != PA_OK) return rc;
-  cudaLaunchConfig_t kc = {};
-  kc.gridDim = dim3(prm.ncta);
-  kc.blockDim = dim3(kWarps * 32);
-  kc.stream = s;
-  kc.attrs = attr;
-  kc.numAttrs = 1;
-  if (head_dim == 128) {
-    kc.dynamicSmemBytes = Smem<128>::kBytes;
-    e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 128>, mk, mv, prm)
-             : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 128>, mk, mv, prm);
   } else {
-    kc.dynamicSmemBytes = Smem<64>::kBytes;
-    e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 64>, mk, mv, prm)
-             : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 64>, mk, mv, prm);
+    cudaLaunchConfig_t kc = {};
+    kc.gridDim = dim3(prm.ncta);
+    kc.blockDim = dim3(kWarps * 32);
+    kc.stream = s;
+    kc.attrs = attr;
+    kc.numAttrs = 1;
+    if (prm.head_dim == 128) {
+      kc.dynamicSmemBytes = Smem<128>::kBytes;
+      e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 128>, mk, mv, prm)
+               : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 128>, mk, mv, prm);
+    } else {
+      kc.dynamicSmemBytes = Smem<64>::kBytes;
+      e = bf16 ? cudaLaunchKernelEx(&kc, prefill_kernel<__nv_bfloat16, 64>, mk, mv, prm)
+               : cudaLaunchKernelEx(&kc, prefill_kernel<__half, 64>, mk, mv, prm);
+    }
   }
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
+}
+
+// Plan, then attention (16-bit dtypes).
+int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
+              cudaStream_t s, const char* who) {
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  const int rc = launch_plan(prm, use_tc, s, who);
+  return rc != PA_OK ? rc : launch_attention(prm, use_tc, dtype, s, who);
 }
 
 }  // namespace

@@ -30,37 +30,6 @@ __device__ __forceinline__ void tc_fence_before_sync() {
 __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
-// D (tmem) [+]= A (smem descriptor) x B (smem descriptor), one thread issues.
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-// The same with each descriptor given as its two 32-bit halves (a step along
-// a tile changes only the low half's address field).
-__device__ __forceinline__ void tc_mma_f16_lohi(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                                uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
-                                                uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\tsetp.ne.b32 p, %6, 0;\n\t"
-      "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void tc_mma_f16_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                                   uint32_t b_hi, uint32_t idesc,
-                                                   uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\tsetp.ne.b32 p, %5, 0;\n\t"
-      "mov.b64 b, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // ------------------------------------------- issue from a converged warp
 // The whole warp runs the issuing loop (its operands stay warp-uniform) and
 // only the lane chosen once by elect_one() issues: every lane executes the
@@ -72,6 +41,8 @@ __device__ __forceinline__ uint32_t elect_one() {
       : "=r"(leader));
   return leader;
 }
+// D (tmem) [+]= A (smem descriptor) x B (smem descriptor); `accumulate` 0
+// overwrites D.
 __device__ __forceinline__ void tc_mma_ss_leader(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate,
                                                  uint32_t leader) {
@@ -81,6 +52,8 @@ __device__ __forceinline__ void tc_mma_ss_leader(uint32_t d_tmem, uint64_t a_des
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
+// D (tmem) [+]= A (tmem) x B (smem descriptor): A's row i sits in TMEM lane
+// i, its K elements two to a 32-bit column (16 of them in 8 columns).
 __device__ __forceinline__ void tc_mma_ts_leader(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, uint32_t accumulate,
                                                  uint32_t leader) {
@@ -90,6 +63,8 @@ __device__ __forceinline__ void tc_mma_ts_leader(uint32_t d_tmem, uint32_t a_tme
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(leader)
       : "memory");
 }
+// The mbarrier gets one arrival once every tcgen05 operation the issuing
+// lane started before has completed.
 __device__ __forceinline__ void tc_commit_leader(uint64_t* bar, uint32_t leader) {
   asm volatile(
       "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %1, 0;\n\t"
@@ -99,24 +74,6 @@ __device__ __forceinline__ void tc_commit_leader(uint64_t* bar, uint32_t leader)
       : "memory");
 }
 
-// D (tmem) [+]= A (tmem) x B (smem descriptor): A's row i sits in TMEM lane
-// i, its K elements two to a 32-bit column (16 of them in 8 columns).
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-// The mbarrier gets one arrival once every tcgen05 operation this thread
-// issued before has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 // 32 consecutive 32-bit columns of this thread's TMEM lane (warp w of a
 // warpgroup reaches lanes 32 (w % 4) .. + 31).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -149,6 +106,13 @@ __device__ __forceinline__ void tmem_wait_ld() {
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 bytes to global memory in one instruction (address 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
 }
 
 // --------------------------------------------- packed / three-input fp32

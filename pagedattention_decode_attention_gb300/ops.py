@@ -314,11 +314,44 @@ def alloc_prefill_workspace(num_seqs, total_q, num_q_heads, num_kv_heads, head_d
     return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
 
 
+def prefill_plan(context_lens: torch.Tensor, query_start: torch.Tensor, total_q: int,
+                 num_q_heads: int, num_kv_heads: int, head_dim: int, max_blocks_per_seq: int,
+                 scale: float, dtype: torch.dtype, workspace: torch.Tensor, stream=None) -> None:
+    """The work list of a chunked-prefill batch, into ``workspace``: one plan
+    serves every ``paged_attention_prefill_run`` over the same chunks."""
+    dev = context_lens.device
+    for name, t in (("context_lens", context_lens), ("query_start", query_start),
+                    ("workspace", workspace)):
+        _cuda_contig(name, t, dev)
+    _require(context_lens.dtype == torch.int32 and query_start.dtype == torch.int32,
+             "context_lens and query_start must be int32")
+    b = context_lens.shape[0]
+    _require(query_start.shape == (b + 1,), "query_start must be [num_seqs + 1]")
+    _require(dtype in _DTYPES, "dtype must be float32, float16 or bfloat16")
+    capi.check(capi.lib().pa_paged_attention_prefill_plan(
+        context_lens.data_ptr(), query_start.data_ptr(), b, int(total_q), int(num_q_heads),
+        int(num_kv_heads), int(head_dim), int(max_blocks_per_seq), float(scale),
+        _DTYPES[dtype], workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(dev, stream)))
+
+
+def paged_attention_prefill_run(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                query_start: torch.Tensor, scale: float, workspace: torch.Tensor,
+                                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """``paged_attention_prefill`` over a workspace that ``prefill_plan``
+    filled for the same chunks: the attention kernel only."""
+    return paged_attention_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                                   scale, out=out, workspace=workspace, stream=stream,
+                                   _entry="pa_paged_attention_prefill_run")
+
+
 def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                             block_tables: torch.Tensor, context_lens: torch.Tensor,
                             query_start: torch.Tensor, scale: float,
                             out: torch.Tensor | None = None,
-                            workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                            workspace: torch.Tensor | None = None, stream=None,
+                            _entry: str = "pa_paged_attention_prefill") -> torch.Tensor:
     """Chunked-prefill attention: the query rows ``query_start[b] ..
     query_start[b+1]-1`` of ``q`` (``[total_q, Hq, d]``) are the newest tokens
     of sequence ``b`` (K/V already in the cache); each attends causally over
@@ -348,7 +381,7 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     if workspace is None:
         workspace = alloc_prefill_workspace(b, total_q, hq, hkv, d, dev)
     _cuda_contig("workspace", workspace, dev)
-    capi.check(capi.lib().pa_paged_attention_prefill(
+    capi.check(getattr(capi.lib(), _entry)(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), query_start.data_ptr(), b, total_q, hq, hkv, d,
         block_tables.shape[1], nb, float(scale), _dtype_code(q), out.data_ptr(),

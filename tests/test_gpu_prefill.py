@@ -146,3 +146,51 @@ def test_prefill_chunk_longer_than_context_sets_bounds_status(gpu):
     assert torch.count_nonzero(out[20:]) == 0                       # skipped sequence
     ref = oracle_prefill(batch, q[:20], kc, vc, np.array([0, 20, 20], dtype=np.int32))
     assert_attention_close(out[:20], ref[:20], torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype,head_dim", [("bf16", 128), ("f16", 128), ("bf16", 64), ("f32", 128)])
+def test_prefill_one_plan_serves_every_layer(gpu, dtype, head_dim):
+    """prefill_plan once, then paged_attention_prefill_run on three layers'
+    caches and queries: each is bit-identical to the one-shot call on that
+    layer and matches the oracle."""
+    dt = TORCH_DTYPES[dtype]
+    batch = custom_batch(LENS, 32, 8, head_dim, dtype, seed=95)
+    qs = np.concatenate([[0], np.cumsum(QLENS)]).astype(np.int32)
+    shape = (batch.num_blocks, 8, 16, head_dim)
+    layers = [(wl.normal((int(qs[-1]), 32, head_dim), dt, 950 + 3 * i, gpu),
+               wl.normal(shape, dt, 951 + 3 * i, gpu), wl.normal(shape, dt, 952 + 3 * i, gpu))
+              for i in range(3)]
+    bt = torch.from_numpy(batch.block_tables).to(gpu)
+    cl = torch.from_numpy(batch.context_lens).to(gpu)
+    qsd = torch.from_numpy(qs).to(gpu)
+    ws = pa().alloc_prefill_workspace(len(LENS), int(qs[-1]), 32, 8, head_dim, gpu)
+    pa().prefill_plan(cl, qsd, int(qs[-1]), 32, 8, head_dim, batch.max_blocks, batch.scale, dt, ws)
+    runs = [pa().paged_attention_prefill_run(q, kc, vc, bt, cl, qsd, batch.scale, ws).clone()
+            for q, kc, vc in layers]
+    pa().check_status()
+    for (q, kc, vc), got in zip(layers, runs):
+        whole = run_prefill(batch, q, kc, vc, qs, gpu)
+        assert torch.equal(got, whole)
+        assert_attention_close(got, oracle_prefill(batch, q, kc, vc, qs), dt)
+
+
+def test_prefill_run_without_plan_sets_status(gpu):
+    batch, q, kc, vc, qs = prefill_inputs([300, 90], [64, 90], 32, 8, 128, "bf16", seed=97,
+                                          dev=gpu)
+    ws = pa().alloc_prefill_workspace(2, int(qs[-1]), 32, 8, 128, gpu)
+    ws.zero_()
+    out = torch.zeros_like(q)
+    pa().paged_attention_prefill_run(q, kc, vc, torch.from_numpy(batch.block_tables).to(gpu),
+                                     torch.from_numpy(batch.context_lens).to(gpu),
+                                     torch.from_numpy(qs).to(gpu), batch.scale, ws, out=out)
+    with pytest.raises(pa().PagedAttnError):
+        pa().check_status()
+    assert torch.count_nonzero(out) == 0
+    # a plan makes the same workspace usable
+    pa().prefill_plan(torch.from_numpy(batch.context_lens).to(gpu), torch.from_numpy(qs).to(gpu),
+                      int(qs[-1]), 32, 8, 128, batch.max_blocks, batch.scale, torch.bfloat16, ws)
+    got = pa().paged_attention_prefill_run(q, kc, vc, torch.from_numpy(batch.block_tables).to(gpu),
+                                           torch.from_numpy(batch.context_lens).to(gpu),
+                                           torch.from_numpy(qs).to(gpu), batch.scale, ws)
+    pa().check_status()
+    assert_attention_close(got, oracle_prefill(batch, q, kc, vc, qs), torch.bfloat16)
