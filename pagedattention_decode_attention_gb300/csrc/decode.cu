@@ -1059,7 +1059,7 @@ struct KernelConfig {
 // SM, and a cap on the ring stages per math warp.  Defaults are the measured
 // best.
 struct Tuning {
-  int split_blocks = 0;  // 0: by group size (16 blocks for G == 1, 32 otherwise)
+  int split_blocks = 0;  // 0: kSplitBlocks (measured best for both MHA and GQA batches)
   int warps = kConsumerWarps;
   int ctas_per_sm = 1;
   int max_stages = kWarpStages;
@@ -1207,9 +1207,7 @@ Params make_params(const int32_t* context_lens, int num_seqs, int num_q_heads, i
   prm.head_dim = head_dim;
   prm.max_blocks = max_blocks_per_seq;
   prm.max_splits = lay.max_splits;
-  prm.split_blocks = tuning().split_blocks
-                         ? tuning().split_blocks
-                         : (num_q_heads == num_kv_heads ? kMinSplitBlocks : kSplitBlocks);
+  prm.split_blocks = tuning().split_blocks ? tuning().split_blocks : kSplitBlocks;
   prm.signature = plan_signature(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                  prm.split_blocks);
   prm.ws.header = reinterpret_cast<int*>(ws + lay.header);
