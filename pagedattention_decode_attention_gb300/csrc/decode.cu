@@ -131,16 +131,17 @@ __device__ __forceinline__ void split_shape(int nblk, int split, int& nsplit, in
 }
 
 // Units a split of n blocks becomes: itself, or balanced pieces of at most
-// kPieceBlocks blocks when n <= cut.
-__device__ __forceinline__ int pieces_of(int n, int cut) {
-  return n <= cut ? (n + kPieceBlocks - 1) / kPieceBlocks : 1;
+// `piece` blocks when n <= cut.
+__device__ __forceinline__ int pieces_of(int n, int cut, int piece) {
+  return n <= cut ? (n + piece - 1) / piece : 1;
 }
 
 // The work list is sorted by size, largest first, so the last items the
 // persistent kernel hands out are the smallest (longest-processing-time-first
 // order).  Its tail is made finer still: the smallest splits, whose work adds
 // up to about kTailWaves pieces per math warp, are cut into pieces of at most
-// kPieceBlocks blocks, so the warps run out of work at nearly the same time.
+// kPieceBlocks blocks (both tunable), so the warps run out of work at nearly
+// the same time.
 // A sequence is cut only while its units fit the workspace's max_splits.
 constexpr int kPlanThreads = 256;  // small enough to sit beside an attention CTA
 
@@ -195,13 +196,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
     int nsplit, base, big;
     split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
     int cut = cut_all;
-    if (big * pieces_of(base + 1, cut) + (nsplit - big) * pieces_of(base, cut) > p.max_splits)
+    if (big * pieces_of(base + 1, cut, p.piece_blocks) + (nsplit - big) * pieces_of(base, cut, p.piece_blocks) > p.max_splits)
       cut = 0;
     int count = 0;
     for (int k = 0; k < 2; ++k) {  // the two split sizes
       const int n = base + 1 - k, m = k ? nsplit - big : big;
       if (m == 0 || n == 0) continue;
-      const int np = pieces_of(n, cut);
+      const int np = pieces_of(n, cut, p.piece_blocks);
       count += m * np;
       const int pb = n / np, pr = n - pb * np;  // pr pieces of pb + 1, the rest of pb
       if (pr) atomicAdd(&hist[pb + 1], m * pr);
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
     int nsplit, base, big;
     split_shape((ctx + kBlockSize - 1) / kBlockSize, p.split_blocks, nsplit, base, big);
     int cut = cut_all;
-    if (big * pieces_of(base + 1, cut) + (nsplit - big) * pieces_of(base, cut) > p.max_splits)
+    if (big * pieces_of(base + 1, cut, p.piece_blocks) + (nsplit - big) * pieces_of(base, cut, p.piece_blocks) > p.max_splits)
       cut = 0;
     // reserve this sequence's slots in each bucket it uses
     int at[2][2];  // [split size k][piece size pb + 1 / pb]
@@ -239,7 +240,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
       const int n = base + 1 - k, m = k ? nsplit - big : big;
       at[k][0] = at[k][1] = 0;
       if (m == 0 || n == 0) continue;
-      const int np = pieces_of(n, cut);
+      const int np = pieces_of(n, cut, p.piece_blocks);
       const int pb = n / np, pr = n - pb * np;
       if (pr) at[k][0] = atomicAdd(&bucket[pb + 1], m * pr);
       if (np - pr) at[k][1] = atomicAdd(&bucket[pb], m * (np - pr));
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
     for (int s = 0; s < nsplit; ++s) {
       const int k = s < big ? 0 : 1;
       const int n = base + 1 - k;
-      const int np = pieces_of(n, cut);
+      const int np = pieces_of(n, cut, p.piece_blocks);
       const int pb = n / np, pr = n - pb * np;
       for (int j = 0; j < np; ++j) {
         const int sz = j < pr ? pb + 1 : pb;
@@ -1064,6 +1065,7 @@ struct Tuning {
   int ctas_per_sm = 1;
   int max_stages = kWarpStages;
   int tail_waves = kTailWaves;
+  int piece_blocks = kPieceBlocks;
 };
 Tuning read_tuning_env() {
   Tuning t;
@@ -1073,6 +1075,8 @@ Tuning read_tuning_env() {
   if (const char* v = std::getenv("PA_DECODE_CTAS_PER_SM")) t.ctas_per_sm = std::max(1, std::min(4, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_MAX_STAGES")) t.max_stages = std::max(1, std::min(kWarpStages, std::atoi(v)));
   if (const char* v = std::getenv("PA_DECODE_TAIL_WAVES")) t.tail_waves = std::max(0, std::min(16, std::atoi(v)));
+  if (const char* v = std::getenv("PA_DECODE_PIECE_BLOCKS"))
+    t.piece_blocks = std::max(1, std::min(16, std::atoi(v)));
   return t;
 }
 // Read once per process.
@@ -1258,7 +1262,8 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   // the tail is sized for the math warps the attention kernel will launch
   const DeviceState& st = g_dev[device];
   const int nwarps = st.sms * st.cfg[1][head_dim == 128].ctas_per_sm * st.tuning.warps;
-  prm.tail_blocks = st.tuning.tail_waves * nwarps * kPieceBlocks;
+  prm.piece_blocks = st.tuning.piece_blocks;
+  prm.tail_blocks = st.tuning.tail_waves * nwarps * prm.piece_blocks;
   static std::once_flag carveout_once;
   std::call_once(carveout_once, [] {
     // keep the SM's shared-memory split the attention kernel wants, so no

@@ -10,8 +10,8 @@ namespace decode {
 constexpr int kBlockSize = 16;      // tokens per physical block (device kernels)
 constexpr int kSplitBlocks = 32;    // most logical blocks per work item (512 tokens)
 constexpr int kMinSplitBlocks = 16; // fewest blocks a split may be planned with
-constexpr int kPieceBlocks = 8;     // most blocks of a piece at the end of the work list
-constexpr int kTailWaves = 2;       // pieces at the end: about this many per math warp
+constexpr int kPieceBlocks = 8;     // default: most blocks of a piece at the end of the work list
+constexpr int kTailWaves = 1;       // pieces at the end: about this many per math warp
 constexpr int kConsumerWarps = 8;   // default number of math warps per CTA
 constexpr int kWarpStages = 4;      // upper bound of each math warp's (K, V) tile ring
 constexpr int kMaxGroup = 8;        // query heads per KV head on the tensor-core path
@@ -95,6 +95,7 @@ struct Params {
   int stages;        // depth of the shared-memory tile ring (tensor-core path)
   int split_blocks;  // blocks per split, kMinSplitBlocks .. kSplitBlocks
   int tail_blocks;   // plan: work (in blocks) at the end of the list cut into pieces
+  int piece_blocks;  // plan: most blocks of such a piece
   int signature;     // plan_signature() of these shapes
   float scale;       // softmax scale (fp32 path)
   float scale_log2;  // scale * log2(e) (tensor-core path works in base 2)

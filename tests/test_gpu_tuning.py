@@ -1,5 +1,5 @@
 """The attention kernel under non-default tuning (fewer warps, shallow rings,
-two CTAs per SM, no fine-grained tail, other split sizes), each in a child
+two CTAs per SM, no fine-grained tail, other split and piece sizes), each in a child
 process because the tuning variables are read once per process."""
 
 import os
@@ -18,6 +18,7 @@ CONFIGS = {
     "1stage": {"PA_DECODE_MAX_STAGES": "1"},
     "no_tail_split16": {"PA_DECODE_TAIL_WAVES": "0", "PA_DECODE_SPLIT_BLOCKS": "16"},
     "wide_tail_split24": {"PA_DECODE_TAIL_WAVES": "6", "PA_DECODE_SPLIT_BLOCKS": "24"},
+    "tiny_pieces": {"PA_DECODE_TAIL_WAVES": "8", "PA_DECODE_PIECE_BLOCKS": "1"},
 }
 
 
