@@ -68,6 +68,8 @@ def parse_args():
                     help="override the workload's layer count (profiling at a small footprint)")
     ap.add_argument("--warmup-seconds", type=float, default=1.0,
                     help="keep warming up until this much wall time has passed")
+    ap.add_argument("--cascade", action="store_true",
+                    help="prefix_8b: time the shared-prefix (cascade) decode against the plain one")
     return ap.parse_args()
 
 
@@ -109,7 +111,8 @@ def prefix_batch(script) -> wl.DecodeBatch:
     max_blocks = max(len(pool.block_table(s)[0]) for s in seqs)
     tables, lens = pool.tables(seqs, max_blocks)
     return wl.DecodeBatch("prefix_8b_bf16", 32, 8, 128, "bf16", lens, tables, script.num_blocks,
-                          num_layers=script.num_layers, seed=script.seed)
+                          num_layers=script.num_layers, seed=script.seed,
+                          extra={"prefix_blocks": script.prefix_len // 16})
 
 
 def unique_kv_bytes(batch: wl.DecodeBatch) -> int:
@@ -690,6 +693,77 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- reference
+def run_cascade_bench(args):
+    """Shared-prefix (cascade) decode on the prefix-mix batch, beside the
+    plain decode of the same batch.  Both run as a model step would: one plan
+    from the lengths, then per layer the new tokens' K/V appended and
+    attention over the whole context (the plain path fuses the two into one
+    launch; the cascade path appends, then runs its prefix phase, suffix
+    decode and combine)."""
+    import pagedattention_decode_attention_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    batch = make_batch("prefix_8b", 0)
+    if args.layers > 0:
+        batch.num_layers = args.layers
+    rep = Replica(batch, device)
+    L, P = batch.num_layers, batch.extra["prefix_blocks"]
+    hq, hkv, d, mb = batch.num_q_heads, batch.num_kv_heads, batch.head_dim, batch.max_blocks
+    dt = DTYPES[batch.dtype]
+    ws = torch.empty(max(pa.shared_prefix_workspace_size(batch.num_seqs, hq, hkv, d, mb), 256),
+                     dtype=torch.uint8, device=device)
+    appends = [pa.prepare_kv_append(rep.k_new[i], rep.v_new[i], rep.k_cache[i], rep.v_cache[i],
+                                    rep.slots) for i in range(L)]
+
+    def cascade_step():
+        pa.shared_prefix_plan(rep.lens, P, hq, hkv, d, mb, batch.scale, dt, ws)
+        for i in range(L):
+            appends[i]()
+            pa.paged_attention_decode_shared_prefix_run(rep.q[i], rep.k_cache[i], rep.v_cache[i],
+                                                        rep.tables, rep.lens, P, batch.scale, ws,
+                                                        out=rep.out[i])
+
+    def timed(step):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        torch.cuda.synchronize()
+        pa.check_status()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            step()
+        end.record()
+        torch.cuda.synchronize()
+        pa.check_status()
+        return start.elapsed_time(end) / 1e3 / args.steps
+
+    clocks = ClockSampler(device)
+    clocks.start()
+    plain_s = timed(rep.step)
+    plain_out = rep.out.clone()
+    cascade_s = timed(cascade_step)
+    clk = clocks.stop()
+    # the same attention either way (within rounding of the two merges)
+    diff = (plain_out.float() - rep.out.float()).abs().max().item()
+    line = {
+        "metric": "decode tokens/s, shared-prefix (cascade) path, 1 GPU",
+        "value": batch.num_seqs / cascade_s, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": cascade_s * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
+        "data": "synthetic (seeded N(0,1) Q/K/V; prefix-mix lengths and pool tables)",
+        "config": {"workload": batch.name, "num_seqs": batch.num_seqs, "layers": L,
+                   "prefix_blocks": P, "context_tokens": int(batch.context_lens.sum()),
+                   "step": "one plan, then per layer: append the new tokens' K/V and attend"},
+        "cascade_us_per_layer": cascade_s / L * 1e6,
+        "plain_us_per_layer": plain_s / L * 1e6,
+        "plain_value": batch.num_seqs / plain_s,
+        "max_abs_diff_vs_plain": diff,
+        "gpu_launches": args.steps * (2 + 4 * L),
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def run_swap_bench(args):
     """Block swap (preemption / offload): a batch of 1024 blocks of every one
     of 32 8B-shaped GQA layers goes to page-locked host memory and back, each
@@ -919,6 +993,8 @@ def main():
         run_reference(args)
     elif args.workload == "prefill_8b":
         run_prefill_bench(args)
+    elif args.workload == "prefix_8b" and args.cascade:
+        run_cascade_bench(args)
     elif args.workload == "swap_8b":
         run_swap_bench(args)
     elif args.workload == "pool_churn":

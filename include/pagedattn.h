@@ -241,6 +241,37 @@ PA_API int pa_paged_attention_decode_shared_prefix(
     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_shared_prefix_plan / _run -- the plans and the
+ * compute launches of pa_paged_attention_decode_shared_prefix as separate
+ * calls, so that one plan serves every layer of a decode step.  (No
+ * counterpart on the pages: the split exists for callers, not for the
+ * method.)
+ *
+ * _plan reads only context_lens (device) and the sizes, and launches the two
+ * work-list plans (the prefix phase's and the suffix decode's) into the
+ * workspace; scale and dtype pick the kernels the lists are cut for.  _run
+ * takes pa_paged_attention_decode_shared_prefix's arguments and launches the
+ * prefix phase, the suffix decode and the combine.  It needs a plan made with
+ * the same sizes, prefix_blocks, dtype and sign of scale and the same
+ * context_lens contents, in stream order on the same workspace; a run whose
+ * workspace holds no plan for its sizes does nothing and sets the status
+ * word (pa_check_status returns PA_ERR_INVALID_ARG), changed lengths under
+ * the same sizes are not detected and give unspecified output.  Runs may
+ * follow one plan any number of times; each leaves the workspace ready for
+ * the next.  With prefix_blocks == 0 the pair is the plain decode's plan and
+ * run; for PA_F32 the plan does nothing.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_shared_prefix_plan(
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
+    void* workspace, size_t workspace_bytes, void* stream);
+PA_API int pa_paged_attention_decode_shared_prefix_run(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_prefill -- chunked-prefill attention over the paged cache.
  *
  * OS-lab appendix, section 2.1 (prefill writes the K/V of every prompt token

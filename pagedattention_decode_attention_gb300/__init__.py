@@ -28,6 +28,7 @@ from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
 from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
                   block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
+                  paged_attention_decode_shared_prefix_run, shared_prefix_plan,
                   paged_attention_prefill, paged_attention_prefill_run, prefill_plan,
                   shared_prefix_workspace_size, prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,

@@ -1491,12 +1491,21 @@ PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
   return PA_OK;
 }
 
-PA_API int pa_paged_attention_decode_shared_prefix(
-    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
-    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
-    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
-  const char* who = "paged_attention_decode_shared_prefix";
+}  // extern "C"
+
+namespace {
+
+enum class SharedMode { kPlanAndRun, kPlanOnly, kRunOnly };
+
+// The cascade decode: the prefix phase, each sequence's own blocks, the
+// combine.  kPlanOnly launches the two plans (they read only the lengths and
+// sizes; q, the caches, the tables and out may be NULL), kRunOnly the three
+// compute launches over a planned workspace.
+int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, int prefix_blocks,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out,
+                       void* workspace, size_t workspace_bytes, void* stream, const char* who) {
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
   if (rc != PA_OK || num_seqs == 0) return rc;
@@ -1508,34 +1517,48 @@ PA_API int pa_paged_attention_decode_shared_prefix(
       workspace_bytes < sl.total)
     return fail(PA_ERR_INVALID_ARG, "%s: workspace NULL, unaligned or < %zu bytes", who, sl.total);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
+  if (!context_lens) return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
   if (prefix_blocks == 0 || dtype == PA_F32) {
     // nothing shared to exploit (or the fp32 path): a plain decode is exact
-    return pa_paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, num_seqs,
-                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                                     num_blocks, scale, dtype, out, workspace, workspace_bytes,
-                                     stream);
+    if (plans && dtype != PA_F32) {
+      rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                     max_blocks_per_seq, workspace, workspace_bytes, s, who);
+      if (rc != PA_OK) return rc;
+    }
+    return runs ? run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
+                           num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
+                           out, workspace, workspace_bytes, s, who)
+                : PA_OK;
   }
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+  if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
     return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* po = reinterpret_cast<float*>(ws + sl.po);
   float* plse = reinterpret_cast<float*>(ws + sl.plse);
   float* so = reinterpret_cast<float*>(ws + sl.so);
   float* slse = reinterpret_cast<float*>(ws + sl.slse);
-  // 1. the shared prefix, read once for all queries
-  rc = prefill::shared_prefix_phase(q, k_cache, v_cache, block_tables, prefix_blocks * kBlockSize,
-                                    num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                    max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
-                                    ws + sl.prefix, sl.po - sl.prefix, s);
-  if (rc != PA_OK) return rc;
-  // 2. every sequence's own blocks
   SuffixArgs sfx;
   sfx.prefix_blocks = prefix_blocks;
   sfx.cas_o = so;
   sfx.cas_lse = slse;
-  rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                 workspace, sl.prefix, s, who, sfx);
+  if (plans) {
+    rc = prefill::shared_prefix_plan(prefix_blocks * kBlockSize, num_seqs, num_q_heads,
+                                     num_kv_heads, head_dim, max_blocks_per_seq, scale, dtype,
+                                     ws + sl.prefix, sl.po - sl.prefix, s);
+    if (rc != PA_OK) return rc;
+    rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                   workspace, sl.prefix, s, who, sfx);
+    if (rc != PA_OK) return rc;
+  }
+  if (!runs) return PA_OK;
+  // 1. the shared prefix, read once for all queries
+  rc = prefill::shared_prefix_run(q, k_cache, v_cache, block_tables, prefix_blocks * kBlockSize,
+                                  num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
+                                  ws + sl.prefix, sl.po - sl.prefix, s);
   if (rc != PA_OK) return rc;
+  // 2. every sequence's own blocks
   rc = run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                 num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
                 workspace, sl.prefix, s, who, AppendArgs(), sfx);
@@ -1572,6 +1595,44 @@ PA_API int pa_paged_attention_decode_shared_prefix(
                                  num_seqs, max_blocks_per_seq, status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API int pa_paged_attention_decode_shared_prefix(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return shared_prefix_impl(SharedMode::kPlanAndRun, q, k_cache, v_cache, block_tables,
+                            context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                            workspace, workspace_bytes, stream,
+                            "paged_attention_decode_shared_prefix");
+}
+
+PA_API int pa_paged_attention_decode_shared_prefix_plan(
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  return shared_prefix_impl(SharedMode::kPlanOnly, nullptr, nullptr, nullptr, nullptr,
+                            context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, max_blocks_per_seq, 0, scale, dtype, nullptr, workspace,
+                            workspace_bytes, stream, "paged_attention_decode_shared_prefix_plan");
+}
+
+PA_API int pa_paged_attention_decode_shared_prefix_run(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return shared_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables,
+                            context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                            workspace, workspace_bytes, stream,
+                            "paged_attention_decode_shared_prefix_run");
 }
 
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,

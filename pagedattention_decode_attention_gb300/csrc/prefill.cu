@@ -1688,22 +1688,24 @@ size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
   return workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim).total;
 }
 
-int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
-                        const int32_t* block_tables, int prefix_tokens, int num_seqs,
-                        int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
-                        int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
-                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  const char* who = "paged_attention_decode_shared_prefix (prefix)";
-  const Layout lay = workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim);
+namespace {
+
+// Params of the shared-prefix phase: the batch's decode queries are the rows
+// of one sequence over the prefix (no causal mask).
+int shared_params(Params& prm, Layout& lay, int& device, const void* q, const void* k_cache,
+                  const void* v_cache, const int32_t* block_tables, int prefix_tokens,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                  int max_blocks_per_seq, int num_blocks, float scale, float* cas_o,
+                  float* cas_lse, size_t workspace_bytes, const char* who) {
+  lay = workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim);
   if (workspace_bytes < lay.total) return fail(PA_ERR_INVALID_ARG, "%s: workspace too small", who);
-  int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
     return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
   int rc = device_setup(device);
   if (rc != PA_OK) return rc;
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
-  Params prm = {};
+  prm = Params{};
   prm.q = q;
   prm.k_cache = k_cache;
   prm.v_cache = v_cache;
@@ -1723,7 +1725,54 @@ int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
   prm.shared_ctx = prefix_tokens;
   prm.cas_o = cas_o;
   prm.cas_lse = cas_lse;
-  return launch_tc(prm, lay, device, dtype, workspace, stream, who);
+  return PA_OK;
+}
+
+}  // namespace
+
+int shared_prefix_plan(int prefix_tokens, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int head_dim, int max_blocks_per_seq, float scale, int dtype,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const char* who = "paged_attention_decode_shared_prefix (prefix plan)";
+  Params prm;
+  Layout lay;
+  int device = 0;
+  int rc = shared_params(prm, lay, device, nullptr, nullptr, nullptr, nullptr, prefix_tokens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0,
+                         scale, nullptr, nullptr, workspace_bytes, who);
+  if (rc != PA_OK) return rc;
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  return launch_plan(prm, use_tc, stream, who);
+}
+
+int shared_prefix_run(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int prefix_tokens, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                      int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const char* who = "paged_attention_decode_shared_prefix (prefix)";
+  Params prm;
+  Layout lay;
+  int device = 0;
+  int rc = shared_params(prm, lay, device, q, k_cache, v_cache, block_tables, prefix_tokens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                         num_blocks, scale, cas_o, cas_lse, workspace_bytes, who);
+  if (rc != PA_OK) return rc;
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  return launch_attention(prm, use_tc, dtype, stream, who);
+}
+
+int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int prefix_tokens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                        int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int rc = shared_prefix_plan(prefix_tokens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                              max_blocks_per_seq, scale, dtype, workspace, workspace_bytes, stream);
+  if (rc != PA_OK) return rc;
+  return shared_prefix_run(q, k_cache, v_cache, block_tables, prefix_tokens, num_seqs,
+                           num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
+                           scale, dtype, cas_o, cas_lse, workspace, workspace_bytes, stream);
 }
 
 }  // namespace prefill

@@ -25,5 +25,17 @@ int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
                         int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+// The two launches of shared_prefix_phase as separate calls: the plan depends
+// only on the sizes and prefix_tokens, so one serves every layer; the run
+// needs a plan for the same sizes and prefix_tokens in the workspace.
+int shared_prefix_plan(int prefix_tokens, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int head_dim, int max_blocks_per_seq, float scale, int dtype,
+                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+int shared_prefix_run(const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int prefix_tokens, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                      int num_blocks, float scale, int dtype, float* cas_o, float* cas_lse,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 }  // namespace prefill
 }  // namespace pa

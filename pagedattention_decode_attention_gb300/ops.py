@@ -276,9 +276,39 @@ def shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: 
     return n.value
 
 
+def shared_prefix_plan(context_lens: torch.Tensor, prefix_blocks: int, num_q_heads: int,
+                       num_kv_heads: int, head_dim: int, max_blocks_per_seq: int, scale: float,
+                       dtype: torch.dtype, workspace: torch.Tensor, stream=None) -> None:
+    """The work lists of a shared-prefix (cascade) decode batch, into
+    ``workspace``: one plan serves every
+    :func:`paged_attention_decode_shared_prefix_run` over the same lengths."""
+    dev = context_lens.device
+    _cuda_contig("context_lens", context_lens, dev)
+    _cuda_contig("workspace", workspace, dev)
+    _require(context_lens.dtype == torch.int32, "context_lens must be int32")
+    _require(dtype in _DTYPES, "dtype must be float32, float16 or bfloat16")
+    capi.check(capi.lib().pa_paged_attention_decode_shared_prefix_plan(
+        context_lens.data_ptr(), int(prefix_blocks), context_lens.shape[0], int(num_q_heads),
+        int(num_kv_heads), int(head_dim), int(max_blocks_per_seq), float(scale), _DTYPES[dtype],
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+
+
+def paged_attention_decode_shared_prefix_run(q, k_cache, v_cache, block_tables, context_lens,
+                                             prefix_blocks: int, scale: float, workspace,
+                                             out=None, stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode_shared_prefix` over a workspace that
+    :func:`shared_prefix_plan` filled for the same lengths: the compute
+    launches only."""
+    return paged_attention_decode_shared_prefix(
+        q, k_cache, v_cache, block_tables, context_lens, prefix_blocks, scale, out=out,
+        workspace=workspace, stream=stream, _entry="pa_paged_attention_decode_shared_prefix_run")
+
+
 def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, context_lens,
                                          prefix_blocks: int, scale: float, out=None,
-                                         workspace=None, stream=None) -> torch.Tensor:
+                                         workspace=None, stream=None,
+                                         _entry="pa_paged_attention_decode_shared_prefix"
+                                         ) -> torch.Tensor:
     """:func:`paged_attention_decode` for a batch whose tables all start with
     the same ``prefix_blocks`` blocks: the shared blocks are read once for all
     queries, each sequence's own blocks by the decode kernel, then the two
@@ -292,7 +322,7 @@ def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, cont
         n = shared_prefix_workspace_size(b, hq, hkv, d, mb)
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
     _cuda_contig("workspace", workspace, dev)
-    capi.check(capi.lib().pa_paged_attention_decode_shared_prefix(
+    capi.check(getattr(capi.lib(), _entry)(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), int(prefix_blocks), b, hq, hkv, d, mb, nb, float(scale),
         _dtype_code(q), out.data_ptr(), workspace.data_ptr(),

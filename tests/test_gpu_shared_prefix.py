@@ -83,3 +83,45 @@ def test_shared_prefix_mismatched_table_sets_bounds_status(gpu):
         q, kc, vc, torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu), 4, 0.125)
     with pytest.raises(pa().PagedAttnError):
         pa().check_status()
+
+
+@pytest.mark.parametrize("dtype,head_dim,prefix", [("bf16", 128, 1024), ("f16", 64, 1024),
+                                                   ("bf16", 128, 0), ("f32", 128, 1024)])
+def test_shared_prefix_one_plan_serves_every_layer(gpu, dtype, head_dim, prefix):
+    """shared_prefix_plan once, then the run on three layers' caches and
+    queries: each is bit-identical to the one-shot call on that layer and
+    matches the oracle (prefix 0 is the plain decode's plan and run)."""
+    dt = TORCH_DTYPES[dtype]
+    q0, kc0, vc0, tables, lens = shared_batch(1024, SUFFIXES, 32, 8, head_dim, dtype, seed=350,
+                                              dev=gpu)
+    layers = [(q0, kc0, vc0)] + [(wl.normal(q0.shape, dt, 360 + 3 * i, gpu),
+                                  wl.normal(kc0.shape, dt, 361 + 3 * i, gpu),
+                                  wl.normal(vc0.shape, dt, 362 + 3 * i, gpu)) for i in range(2)]
+    bt, cl = torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu)
+    mb = tables.shape[1]
+    scale = 1.0 / np.sqrt(head_dim)
+    n = pa().shared_prefix_workspace_size(len(SUFFIXES), 32, 8, head_dim, mb)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=gpu)
+    pa().shared_prefix_plan(cl, prefix // 16, 32, 8, head_dim, mb, scale, dt, ws)
+    runs = [pa().paged_attention_decode_shared_prefix_run(q, kc, vc, bt, cl, prefix // 16, scale,
+                                                          ws).clone()
+            for q, kc, vc in layers]
+    pa().check_status()
+    for (q, kc, vc), got in zip(layers, runs):
+        whole = pa().paged_attention_decode_shared_prefix(q, kc, vc, bt, cl, prefix // 16, scale)
+        pa().check_status()
+        assert torch.equal(got, whole)
+        ref = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc),
+                                        tables, lens, scale)
+        assert_attention_close(got, ref, dt)
+
+
+def test_shared_prefix_run_without_plan_sets_status(gpu):
+    q, kc, vc, tables, lens = shared_batch(256, [5, 40, 100], 32, 8, 128, "bf16", seed=45,
+                                           dev=gpu)
+    bt, cl = torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu)
+    n = pa().shared_prefix_workspace_size(3, 32, 8, 128, tables.shape[1])
+    ws = torch.zeros(max(n, 256), dtype=torch.uint8, device=gpu)
+    pa().paged_attention_decode_shared_prefix_run(q, kc, vc, bt, cl, 16, 1.0 / np.sqrt(128), ws)
+    with pytest.raises(pa().PagedAttnError):
+        pa().check_status()
