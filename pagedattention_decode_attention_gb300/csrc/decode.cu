@@ -1011,8 +1011,9 @@ namespace decode {
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
     cascade_combine_kernel(const float* __restrict__ po, const float* __restrict__ plse,
-                           const float* __restrict__ so, const float* __restrict__ slse, T* out,
-                           int rows, const int32_t* __restrict__ block_tables, int prefix_blocks,
+                           const int* __restrict__ prefix_parts, const float* __restrict__ so,
+                           const float* __restrict__ slse, T* out, int rows,
+                           const int32_t* __restrict__ block_tables, int prefix_blocks,
                            int num_seqs, int max_blocks, unsigned* status) {
   dev::grid_dependency_wait();
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1021,20 +1022,50 @@ __global__ void __launch_bounds__(256)
     const long long b = i / prefix_blocks, j = i % prefix_blocks;
     if (block_tables[b * max_blocks + j] != block_tables[j]) dev::flag_status(status, kStatusBounds);
   }
+  // the prefix phase's parts per row: 1 .. kSharedMaxSplits (part k of row r
+  // at po + (k * rows + r) * D, plse[k * rows + r])
+  int np = *prefix_parts;
+  if (np < 1 || np > prefill::kSharedMaxSplits) {
+    if (tid == 0) dev::flag_status(status, kStatusBounds);
+    np = np < 1 ? 1 : prefill::kSharedMaxSplits;
+  }
   using M = dev::Mma<T>;
   const int lane = threadIdx.x & 31;
   for (long long r = tid >> 5; r < rows; r += nthreads >> 5) {
-    const float lp = plse[r], ls = slse[r];
-    const float m = fmaxf(lp, ls);
-    const float wp = lp == -INFINITY ? 0.f : dev::fast_exp2(lp - m);
+    // weights of the prefix parts and of the suffix, by their log-sum-exp
+    float lp[prefill::kSharedMaxSplits];
+    const float ls = slse[r];
+    float m = ls;
+#pragma unroll
+    for (int k = 0; k < prefill::kSharedMaxSplits; ++k) {
+      lp[k] = k < np ? plse[size_t(k) * rows + r] : -INFINITY;
+      m = fmaxf(m, lp[k]);
+    }
+    float wp[prefill::kSharedMaxSplits], sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < prefill::kSharedMaxSplits; ++k) {
+      wp[k] = lp[k] == -INFINITY ? 0.f : dev::fast_exp2(lp[k] - m);
+      sum += wp[k];
+    }
     const float ws = ls == -INFINITY ? 0.f : dev::fast_exp2(ls - m);
-    const float inv = wp + ws > 0.f ? 1.f / (wp + ws) : 0.f;
+    sum += ws;
+    const float inv = sum > 0.f ? 1.f / sum : 0.f;
     for (int c = 4 * lane; c < D; c += 128) {
-      const float4 a = *reinterpret_cast<const float4*>(po + r * D + c);
       const float4 b = *reinterpret_cast<const float4*>(so + r * D + c);
+      float4 acc = make_float4(ws * b.x, ws * b.y, ws * b.z, ws * b.w);
+#pragma unroll
+      for (int k = 0; k < prefill::kSharedMaxSplits; ++k) {
+        if (k < np) {
+          const float4 a = *reinterpret_cast<const float4*>(po + (size_t(k) * rows + r) * D + c);
+          acc.x += wp[k] * a.x;
+          acc.y += wp[k] * a.y;
+          acc.z += wp[k] * a.z;
+          acc.w += wp[k] * a.w;
+        }
+      }
       uint2 pk;
-      pk.x = M::pack((wp * a.x + ws * b.x) * inv, (wp * a.y + ws * b.y) * inv);
-      pk.y = M::pack((wp * a.z + ws * b.z) * inv, (wp * a.w + ws * b.w) * inv);
+      pk.x = M::pack(acc.x * inv, acc.y * inv);
+      pk.y = M::pack(acc.z * inv, acc.w * inv);
       *reinterpret_cast<uint2*>(out + r * D + c) = pk;
     }
   }
@@ -1470,8 +1501,9 @@ SharedLayout shared_layout(int num_seqs, int num_q_heads, int num_kv_heads, int 
       workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total);
   l.po = align256(l.prefix + prefill::shared_prefix_workspace_bytes(num_seqs, num_q_heads,
                                                                     num_kv_heads, head_dim));
-  l.plse = align256(l.po + rows * head_dim * 4);
-  l.so = align256(l.plse + rows * 4);
+  // the prefix phase may leave up to kSharedMaxSplits parts per row
+  l.plse = align256(l.po + size_t(prefill::kSharedMaxSplits) * rows * head_dim * 4);
+  l.so = align256(l.plse + size_t(prefill::kSharedMaxSplits) * rows * 4);
   l.slse = align256(l.so + rows * head_dim * 4);
   l.total = align256(l.slse + rows * 4);
   return l;
@@ -1564,6 +1596,7 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
                 workspace, sl.prefix, s, who, AppendArgs(), sfx);
   if (rc != PA_OK) return rc;
   // 3. merge
+  const int* parts = prefill::shared_prefix_split_count(ws + sl.prefix);
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
   const int rows = num_seqs * num_q_heads;
@@ -1579,18 +1612,18 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
   cudaError_t e;
   if (dtype == PA_BF16)
     e = head_dim == 128
-            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, po, plse, so,
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, po, plse, parts, so,
                                  slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
                                  prefix_blocks, num_seqs, max_blocks_per_seq, status)
-            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, po, plse, so,
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, po, plse, parts, so,
                                  slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
                                  prefix_blocks, num_seqs, max_blocks_per_seq, status);
   else
     e = head_dim == 128
-            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 128>, po, plse, so, slse,
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 128>, po, plse, parts, so, slse,
                                  static_cast<__half*>(out), rows, block_tables, prefix_blocks,
                                  num_seqs, max_blocks_per_seq, status)
-            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 64>, po, plse, so, slse,
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 64>, po, plse, parts, so, slse,
                                  static_cast<__half*>(out), rows, block_tables, prefix_blocks,
                                  num_seqs, max_blocks_per_seq, status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));

@@ -69,6 +69,9 @@ __host__ __device__ __forceinline__ int nsplits_of(int nb, int split) {
 
 // Workspace header words.
 constexpr int kHdrNext = 0, kHdrTotal = 1, kHdrDone = 2, kHdrSignature = 3;
+// shared-prefix mode: how many (o, lse) parts per row the phase left in
+// cas_o / cas_lse for the caller to merge (1 when it merged them itself)
+constexpr int kHdrSplits = 4;
 
 struct Params {
   const void* q;
@@ -91,6 +94,10 @@ struct Params {
   // cas_lse (fp32 o and base-2 log-sum-exp per (row, head)) instead of out.
   int shared_ctx;
   int no_split;      // plan: never split a unit's KV range (tcgen05 kernel)
+  // shared-prefix mode on the tcgen05 kernel: split s of every row writes its
+  // own (o, lse) to slot s of cas_o / cas_lse ([kSharedMaxSplits][rows]...);
+  // the caller merges them (the split count is header word kHdrSplits)
+  int defer_merge;
   float* cas_o;      // [total_q * num_q_heads][head_dim]
   float* cas_lse;    // [total_q * num_q_heads]
   float scale, scale_log2;
@@ -223,6 +230,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       p.header[kHdrTotal] = 0;
       p.header[kHdrNext] = 0;
       p.header[kHdrDone] = 0;
+      p.header[kHdrSplits] = 1;
       p.header[kHdrSignature] = p.signature;
     }
     return;
@@ -234,6 +242,11 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       const long long want = (long long)s_blocks * p.num_kv_heads / (3ll * p.ncta) + 1;
       // the shared-prefix phase has few, short rows: allow shorter splits
       split = int(std::max<long long>(shared ? kMinSplitBlocks / 2 : kMinSplitBlocks, want));
+      // parts left for the caller: at most kSharedMaxSplits per row
+      if (p.defer_merge) {
+        const int nb = (p.shared_ctx + kBlockSize - 1) / kBlockSize;
+        split = std::max(split, (nb + kSharedMaxSplits - 1) / kSharedMaxSplits);
+      }
     }
     s_split = split;
   }
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       int units = 0;
       for (int qb = 0; qb < nq; ++qb) {
         const int ns = nsplits_of(qblock_blocks<ROWS>(ctx, qlen, G, qb, shared), split);
-        if (ns > 1) units += ns;
+        if (ns > 1 && !p.defer_merge) units += ns * (ROWS / kRows);  // partial slots of kRows rows
       }
       if (units) atomicAdd(&s_split_units, units);
     }
@@ -287,6 +300,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     p.header[kHdrTotal] = pos * p.num_kv_heads;
     p.header[kHdrNext] = 0;
     p.header[kHdrDone] = 0;
+    p.header[kHdrSplits] =
+        p.defer_merge && shared
+            ? nsplits_of((p.shared_ctx + kBlockSize - 1) / kBlockSize, split)
+            : 1;
     p.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
@@ -302,8 +319,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
       int slot = -1, grp = -1;
-      if (ns > 1) {
-        slot = atomicAdd(&s_slot, ns);
+      if (ns > 1 && !p.defer_merge) {
+        slot = atomicAdd(&s_slot, ns * (ROWS / kRows));
         grp = atomicAdd(&s_group, 1);
         for (int g = 0; g < p.num_kv_heads; ++g) p.arrivals[size_t(grp) * p.num_kv_heads + g] = 0;
       }
@@ -861,12 +878,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
+  const bool shared = p.shared_ctx > 0;
   bool ok = true;
   PF_STAMP(1);
 
   // what every role decodes from a claimed item
   struct Item {
-    int b, qt, nblk, ctx, q_first, qlen, g, ntiles;
+    int b, qt, first, nblk, ctx, q_first, qlen, g, ntiles, s;
     bool two;  // the second query tile holds valid rows
   };
   auto decode = [&](int x) {
@@ -875,10 +893,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     it.g = x % Hkv;
     it.b = u0.x;
     it.qt = u0.y;
+    it.first = u0.z;  // the item's KV range: blocks first .. first + nblk - 1
     it.nblk = u0.w;
+    it.s = u1.x >> 16;  // split index (0 unless the prefix phase splits)
     it.ctx = u1.w;
-    it.q_first = p.query_start[it.b];
-    it.qlen = p.query_start[it.b + 1] - it.q_first;
+    // shared-prefix mode: the batch's queries are the rows of one sequence
+    it.q_first = shared ? 0 : p.query_start[it.b];
+    it.qlen = shared ? p.total_q : p.query_start[it.b + 1] - it.q_first;
     it.ntiles = (it.nblk + kTcBlocks - 1) / kTcBlocks;
     it.two = it.qt * kTcItemRows + kTcRows < it.qlen * G;
     return it;
@@ -935,7 +956,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if ((j * kTcBlocks & ~31) != tbl_base) {
           tbl_base = j * kTcBlocks & ~31;
           tbl = tbl_base + lane < it.nblk
-                    ? p.block_tables[size_t(it.b) * p.max_blocks + tbl_base + lane]
+                    ? p.block_tables[size_t(it.b) * p.max_blocks + it.first + tbl_base + lane]
                     : 0;
           if (tbl < 0 || tbl >= p.num_blocks) {
             dev::flag_status(p.status, kStatusBounds);
@@ -1094,8 +1115,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (w == 1 && !it.two) continue;
       const int gr = it.qt * kTcItemRows + w * kTcRows + r;
       const bool valid = gr < it.qlen * G;
-      const int pos = valid ? it.ctx - it.qlen + gr / G : -1;
-      const int bound = min(it.ctx, it.nblk * kBlockSize);
+      // tokens past the context or past the item's blocks (a split's last
+      // tile) are never read into the result
+      const int bound = min(it.ctx, (it.first + it.nblk) * kBlockSize);
+      // the row's last visible token: causal within the chunk; in
+      // shared-prefix mode every row sees the (item's part of the) prefix
+      const int pos = valid ? min(shared ? it.ctx - 1 : it.ctx - it.qlen + gr / G, bound - 1) : -1;
       float mref = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ntiles && ok; ++j, ++cnt) {
         if (!PF_WAIT(1, dev::mbar_wait_bounded(&s_full[w], cnt & 1, tmo, p.status))) {
@@ -1104,7 +1129,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         PF_MARK(pf_tile);
         dev::tc_fence_after_sync();
-        const int t0 = j * kTcTokens;
+        const int t0 = it.first * kBlockSize + j * kTcTokens;  // first token of the tile
         uint32_t sv[4][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + 32 * c, sv[c]);
@@ -1200,7 +1225,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_o + 32 * c, ov[c]);
       dev::tmem_wait_ld();
-      if (valid) {
+      if (valid && shared) {
+        // fp32 o (normalised) and the base-2 log-sum-exp of the row
+        const size_t hrow = size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G;
+        const size_t rows = size_t(p.total_q) * Hq;  // split s writes part s
+        float* crow = p.cas_o + (size_t(it.s) * rows + hrow) * D;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __float_as_uint(__uint_as_float(ov[c][8 * i + e]) * inv);
+            dev::st_global_v8(crow + 32 * c + 8 * i, f);
+          }
+        p.cas_lse[size_t(it.s) * rows + hrow] = l > 0.f ? mref + log2f(l) : -INFINITY;
+      } else if (valid) {
         T* orow = static_cast<T*>(p.out) +
                   (size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G) * D;
         // a row is 256 bytes: whole 32-byte sectors per store when the
@@ -1590,10 +1630,13 @@ bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* worksp
   const int per_sm = st.ctas_per_sm[bf16][prm.head_dim == 128];
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const int G = prm.num_q_heads / prm.num_kv_heads;
-  const bool use_tc = tc_wanted() && st.tc_ok && prm.shared_ctx == 0 && prm.head_dim == 128 &&
-                      prm.scale_log2 > 0.f && (G == 1 || G == 2 || G == 4 || G == 8);
+  const bool use_tc = tc_wanted() && st.tc_ok && prm.head_dim == 128 && prm.scale_log2 > 0.f &&
+                      (G == 1 || G == 2 || G == 4 || G == 8);
   prm.ncta = use_tc ? st.sms : st.sms * per_sm;
-  prm.no_split = use_tc ? 1 : 0;
+  // the tcgen05 kernel does not merge splits itself: it splits only the
+  // shared-prefix phase, whose parts the cascade combine merges
+  prm.defer_merge = use_tc && prm.shared_ctx > 0 ? 1 : 0;
+  prm.no_split = use_tc && !prm.defer_merge ? 1 : 0;
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
   prm.signature = signature_of(prm.num_seqs, prm.total_q, prm.num_q_heads, prm.num_kv_heads,
@@ -1682,6 +1725,10 @@ int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* worksp
 }
 
 }  // namespace
+
+const int* shared_prefix_split_count(const void* workspace) {
+  return static_cast<const int*>(workspace) + kHdrSplits;  // the header is at offset 0
+}
 
 size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                      int head_dim) {

@@ -9,6 +9,14 @@
 namespace pa {
 namespace prefill {
 
+// Most (o, lse) parts per row the shared-prefix phase leaves for the caller
+// to merge (it splits the prefix into at most this many pieces).
+constexpr int kSharedMaxSplits = 8;
+
+// Device address of the word in a shared-prefix phase workspace holding how
+// many parts per row the last planned phase leaves (1 .. kSharedMaxSplits).
+const int* shared_prefix_split_count(const void* workspace);
+
 // Workspace bytes of the shared-prefix phase for a batch of num_seqs decode
 // queries.
 size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -17,7 +25,10 @@ size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_h
 // Shared-prefix phase of a cascade decode: each of the num_seqs decode
 // queries q[b][h] attends all prefix_tokens tokens of the prefix whose blocks
 // are block_tables[0][0 ..] (no causal mask); writes fp32 o and the base-2
-// log-sum-exp per (sequence, head) to cas_o / cas_lse.  Two launches (plan +
+// log-sum-exp per (sequence, head) to cas_o / cas_lse, as n parts (n the
+// word at shared_prefix_split_count, parts k at cas_o + k * rows * head_dim
+// and cas_lse + k * rows, rows = num_seqs * num_q_heads) whose log-sum-exp
+// merge is the result; cas_o / cas_lse hold kSharedMaxSplits parts.  Two launches (plan +
 // kernel) on `stream`.  Returns a pa_status.  16-bit dtypes only.
 int shared_prefix_phase(const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* block_tables, int prefix_tokens, int num_seqs,
