@@ -745,6 +745,9 @@ def run_cascade_bench(args):
     clk = clocks.stop()
     # the same attention either way (within rounding of the two merges)
     diff = (plain_out.float() - rep.out.float()).abs().max().item()
+    peak, peak_src = load_peaks()
+    qo = 2 * batch.num_seqs * hq * d * ELEM[batch.dtype]
+    uniq = unique_kv_bytes(batch) + qo
     line = {
         "metric": "decode tokens/s, shared-prefix (cascade) path, 1 GPU",
         "value": batch.num_seqs / cascade_s, "unit": "tokens/s", "n_gpus": 1,
@@ -754,6 +757,12 @@ def run_cascade_bench(args):
         "config": {"workload": batch.name, "num_seqs": batch.num_seqs, "layers": L,
                    "prefix_blocks": P, "context_tokens": int(batch.context_lens.sum()),
                    "step": "one plan, then per layer: append the new tokens' K/V and attend"},
+        "roofline": {"bound": "hbm", "achieved": uniq / (cascade_s / L) / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": uniq / (cascade_s / L) / 1e9 / peak,
+                     "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                     "bytes_per_layer": uniq,
+                     "bytes": "unique K/V (each physical block once: the prefix once, "
+                              "every suffix once), q, out"},
         "cascade_us_per_layer": cascade_s / L * 1e6,
         "plain_us_per_layer": plain_s / L * 1e6,
         "plain_value": batch.num_seqs / plain_s,
