@@ -1134,6 +1134,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + 32 * c, sv[c]);
         dev::tmem_wait_ld();
+        PF_ADD(5, pf_tile);
+        PF_MARK(pf_math);
         if (t0 + kTcTokens - 1 > pos) {
           // columns past the row's position (causal, context) do not count
 #pragma unroll
@@ -1191,6 +1193,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         l += ((acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1])) +
              ((acc[2][0] + acc[2][1]) + (acc[3][0] + acc[3][1]));
+        PF_ADD(6, pf_math);
         dev::tmem_st32(t_s, sv[0]);
         dev::tmem_st32(t_s + 32, sv[1]);
         if (w == 0 && t0 + kTcTokens > bound) {
