@@ -841,6 +841,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   int* s_item = reinterpret_cast<int*>(bars + 21);  // [2]
   uint64_t* drain = bars + 22;      // every MMA issued has finished (error exit)
+  // a split item's partial rows are written (8 warp arrivals), then the
+  // merge decision is out (1 arrival); the decision word follows
+  uint64_t* part_full = bars + 23;
+  uint64_t* merge_go = bars + 24;
+  int* s_merge = reinterpret_cast<int*>(bars + 25);
   const uint32_t sbase = dev::smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -860,6 +865,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dev::mbar_init(q_full, 1);
     dev::mbar_init(q_empty, 1);
     dev::mbar_init(drain, 1);
+    dev::mbar_init(part_full, 8);
+    dev::mbar_init(merge_go, 1);
     dev::mbar_fence_init();
     dev::prefetch_tensormap(&tmap_q);
     dev::prefetch_tensormap(&tmap_k);
@@ -884,7 +891,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // what every role decodes from a claimed item
   struct Item {
-    int b, qt, first, nblk, ctx, q_first, qlen, g, ntiles, s;
+    int b, qt, first, nblk, ctx, q_first, qlen, g, ntiles, s, ns, slot, grp;
     bool two;  // the second query tile holds valid rows
   };
   auto decode = [&](int x) {
@@ -895,7 +902,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     it.qt = u0.y;
     it.first = u0.z;  // the item's KV range: blocks first .. first + nblk - 1
     it.nblk = u0.w;
-    it.s = u1.x >> 16;  // split index (0 unless the prefix phase splits)
+    it.s = u1.x >> 16;  // split index and count
+    it.ns = u1.x & 0xffff;
+    it.slot = u1.y;     // first partial slot (kRows rows each) and arrival group
+    it.grp = u1.z;
     it.ctx = u1.w;
     // shared-prefix mode: the batch's queries are the rows of one sequence
     it.q_first = shared ? 0 : p.query_start[it.b];
@@ -1099,6 +1109,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t t_s = tmem + lanes + w * 128, t_o = tmem + lanes + 256 + w * 128;
     const float sl2 = p.scale_log2;       // > 0 on this path
     int cnt = 0;                          // tiles of this group so far
+    int merges = 0;                       // split items merged in-kernel so far
     int kt = 0;                           // K / V tiles so far (group 0 sees them all)
     PF_DECL;
     for (int n = 0;; ++n) {
@@ -1112,7 +1123,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) dev::mbar_arrive(&item_empty[slot]);
       if (x >= total) break;
       const Item it = decode(x);
-      if (w == 1 && !it.two) continue;
+      // a split item's rows are merged here unless the caller merges them
+      const bool merge_here = it.ns > 1 && !p.defer_merge;
+      if (w == 1 && !it.two) {
+        // no rows here; still pass this item's merge phase with group 0, so
+        // that no later wait can take an old phase for its own
+        if (merge_here) {
+          if (!dev::mbar_wait_bounded(merge_go, merges & 1, tmo, p.status)) {
+            ok = false;
+            break;
+          }
+          ++merges;
+        }
+        continue;
+      }
       const int gr = it.qt * kTcItemRows + w * kTcRows + r;
       const bool valid = gr < it.qlen * G;
       // tokens past the context or past the item's blocks (a split's last
@@ -1228,7 +1252,93 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_o + 32 * c, ov[c]);
       dev::tmem_wait_ld();
-      if (valid && shared) {
+      if (merge_here) {
+        // ---- one of ns splits of this (query block, KV head): its rows'
+        // normalised o and base-2 log-sum-exp go to the workspace; the CTA
+        // that completes the set merges every row of it.  Slots are counted
+        // in kRows-row units: this item's split s starts at row
+        // ((slot / (256 / kRows) + s) * Hkv + g) * 256.
+        const size_t pstride = size_t(Hkv) * kTcItemRows;
+        const size_t pbase =
+            (size_t(it.slot / (kTcItemRows / kRows)) * Hkv + it.g) * kTcItemRows + w * kTcRows + r;
+        if (valid) {  // rows past the chunk have no partial results (nor a merge)
+          float* prow = p.part_o + (pbase + it.s * pstride) * D;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint32_t f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __float_as_uint(__uint_as_float(ov[c][8 * i + e]) * inv);
+              dev::st_global_v8(prow + 32 * c + 8 * i, f);
+            }
+          p.part_lse[pbase + it.s * pstride] = l > 0.f ? mref + log2f(l) : -INFINITY;
+        }
+        // every participating warp's rows are written (a lone first tile
+        // arrives for the absent second one too); one thread counts the split
+        __syncwarp();
+        if (lane == 0) dev::mbar_arrive_count(part_full, it.two ? 1 : 2);
+        if (threadIdx.x == 0) {
+          int decision = -1;  // -1: a wait ran out
+          if (dev::mbar_wait_bounded(part_full, merges & 1, tmo, p.status))
+            decision = dev::atom_add_acq_rel_gpu(&p.arrivals[size_t(it.grp) * Hkv + it.g], 1) ==
+                               it.ns - 1
+                           ? 1
+                           : 0;
+          *reinterpret_cast<volatile int*>(s_merge) = decision;
+          dev::mbar_arrive(merge_go);
+        }
+        if (!dev::mbar_wait_bounded(merge_go, merges & 1, tmo, p.status)) ok = false;
+        ++merges;
+        const int decision = ok ? *reinterpret_cast<volatile int*>(s_merge) : -1;
+        if (decision < 0) {
+          ok = false;
+          break;
+        }
+        if (decision == 1 && valid) {
+          // the last split: merge this thread's row over the ns splits
+          float mx = -INFINITY;
+          for (int sp = 0; sp < it.ns; ++sp)
+            mx = fmaxf(mx, __ldcg(&p.part_lse[pbase + sp * pstride]));
+          float sum = 0.f;
+          for (int sp = 0; sp < it.ns; ++sp) {
+            const float x = __ldcg(&p.part_lse[pbase + sp * pstride]);
+            sum += x == -INFINITY ? 0.f : dev::fast_exp2(x - mx);
+          }
+          const float rs = sum > 0.f ? 1.f / sum : 0.f;
+          T* orow = static_cast<T*>(p.out) + (size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G) * D;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {  // 32 columns at a time
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            for (int sp = 0; sp < it.ns; ++sp) {
+              const float x = __ldcg(&p.part_lse[pbase + sp * pstride]);
+              const float wgt = x == -INFINITY ? 0.f : dev::fast_exp2(x - mx) * rs;
+              const float4* src =
+                  reinterpret_cast<const float4*>(p.part_o + (pbase + sp * pstride) * D + 32 * c);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = __ldcg(src + q4);
+                acc[4 * q4] += wgt * v.x;
+                acc[4 * q4 + 1] += wgt * v.y;
+                acc[4 * q4 + 2] += wgt * v.z;
+                acc[4 * q4 + 3] += wgt * v.w;
+              }
+            }
+            {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(orow + 32 * c + 8 * i) =
+                    make_uint4(M::pack(acc[8 * i], acc[8 * i + 1]), M::pack(acc[8 * i + 2], acc[8 * i + 3]),
+                               M::pack(acc[8 * i + 4], acc[8 * i + 5]),
+                               M::pack(acc[8 * i + 6], acc[8 * i + 7]));
+            }
+          }
+        }
+        // ready for the next run on this plan
+        if (decision == 1 && threadIdx.x == 0) p.arrivals[size_t(it.grp) * Hkv + it.g] = 0;
+      } else if (valid && shared) {
         // fp32 o (normalised) and the base-2 log-sum-exp of the row
         const size_t hrow = size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G;
         const size_t rows = size_t(p.total_q) * Hq;  // split s writes part s
@@ -1636,10 +1746,10 @@ bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* worksp
   const bool use_tc = tc_wanted() && st.tc_ok && prm.head_dim == 128 && prm.scale_log2 > 0.f &&
                       (G == 1 || G == 2 || G == 4 || G == 8);
   prm.ncta = use_tc ? st.sms : st.sms * per_sm;
-  // the tcgen05 kernel does not merge splits itself: it splits only the
-  // shared-prefix phase, whose parts the cascade combine merges
+  // the tcgen05 kernel merges its splits itself, except in the shared-prefix
+  // phase, whose parts the cascade combine merges
   prm.defer_merge = use_tc && prm.shared_ctx > 0 ? 1 : 0;
-  prm.no_split = use_tc && !prm.defer_merge ? 1 : 0;
+  prm.no_split = 0;
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
   prm.signature = signature_of(prm.num_seqs, prm.total_q, prm.num_q_heads, prm.num_kv_heads,

@@ -194,3 +194,16 @@ def test_prefill_run_without_plan_sets_status(gpu):
                                            torch.from_numpy(qs).to(gpu), batch.scale, ws)
     pa().check_status()
     assert_attention_close(got, oracle_prefill(batch, q, kc, vc, qs), torch.bfloat16)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_prefill_split_merge_with_mixed_tiles(gpu, dtype):
+    """Few query blocks over long contexts: the plan splits their KV ranges and
+    the kernel merges the splits; query blocks with one and with two 128-row
+    tiles interleave, which exercises the merge's phase bookkeeping."""
+    lens, qlens = [9000, 5000, 300, 4100], [300, 20, 290, 33]
+    batch, q, kc, vc, qs = prefill_inputs(lens, qlens, 32, 8, 128, dtype, seed=99, dev=gpu)
+    out = run_prefill(batch, q, kc, vc, qs, gpu)
+    again = run_prefill(batch, q, kc, vc, qs, gpu)
+    assert torch.equal(out, again)            # the counters reset between runs
+    assert_attention_close(out, oracle_prefill(batch, q, kc, vc, qs), TORCH_DTYPES[dtype])
