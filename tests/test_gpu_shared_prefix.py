@@ -125,3 +125,19 @@ def test_shared_prefix_run_without_plan_sets_status(gpu):
     pa().paged_attention_decode_shared_prefix_run(q, kc, vc, bt, cl, 16, 1.0 / np.sqrt(128), ws)
     with pytest.raises(pa().PagedAttnError):
         pa().check_status()
+
+
+@pytest.mark.parametrize("heads", [(8, 8), (32, 8), (16, 2)], ids=["g1", "g4", "g8"])
+def test_shared_prefix_split_with_partial_tiles(gpu, heads):
+    """A 63-block prefix: the prefix phase's splits are 7 or 8 blocks, so a
+    split's last 128-token tile is partial and the tokens past its last block
+    (the next split's) must not count."""
+    hq, hkv = heads
+    q, kc, vc, tables, lens = shared_batch(1008, SUFFIXES, hq, hkv, 128, "bf16", seed=47 + hq,
+                                           dev=gpu)
+    bt, cl = torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu)
+    out = pa().paged_attention_decode_shared_prefix(q, kc, vc, bt, cl, 63, 1.0 / np.sqrt(128))
+    pa().check_status()
+    ref = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc), tables,
+                                    lens, 1.0 / np.sqrt(128))
+    assert_attention_close(out, ref, torch.bfloat16)
