@@ -1531,8 +1531,6 @@ int device_setup(int device) {
   return PA_OK;
 }
 
-int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
-              cudaStream_t s, const char* who);
 bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* workspace);
 int launch_plan(const Params& prm, bool use_tc, cudaStream_t s, const char* who);
 int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, const char* who);
@@ -1827,14 +1825,6 @@ int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, 
   }
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
-}
-
-// Plan, then attention (16-bit dtypes).
-int launch_tc(Params prm, const Layout& lay, int device, int dtype, void* workspace,
-              cudaStream_t s, const char* who) {
-  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
-  const int rc = launch_plan(prm, use_tc, s, who);
-  return rc != PA_OK ? rc : launch_attention(prm, use_tc, dtype, s, who);
 }
 
 }  // namespace
