@@ -754,6 +754,13 @@ def run_ours(args):
                          "algorithmic_bytes_per_launch": ab["total"],
                          "avg_launch_ms": avg_ms, "back_to_back_launch_ms": kernel_ms,
                          "events_around_each_launch_ms": events_ms,
+                         # per-launch event times over every timed launch (at
+                         # least 20): median and best, and their GB/s
+                         "events_launches": len(per_launch),
+                         "events_median_ms": statistics.median(per_launch),
+                         "events_best_ms": min(per_launch),
+                         "events_median_gbs": ab["total"] / (statistics.median(per_launch) / 1e3) / 1e9,
+                         "events_best_gbs": ab["total"] / (min(per_launch) / 1e3) / 1e9,
                          "launch_timing": ("timed region / attention launches in it (plan "
                                            "included); events_around_each_launch_ms from a "
                                            "second pass with an event pair per launch")},
