@@ -13,6 +13,9 @@ block tables as random disjoint draws from a pool of the needed blocks + 10 %,
 32 layers with separate caches (timed as 32 fused append + attention
 launches).  ``--workload gqa_8b`` runs the 8B-shaped GQA batch (128 sequences,
 32 / 8 heads, bf16, lengths log-uniform in [128, 8192] plus 4 x 8192, one layer).
+Other workloads: ``prefill_8b`` (chunked prefill), ``prefix_8b`` [``--cascade``]
+(shared-prefix batch), ``block_copy_8b`` (copy-on-write at a 4-way fork),
+``swap_8b`` (device <-> host block swap) and ``pool_churn`` (host pool).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
 reference arm of this method: there is no other implementation) on bounded
@@ -59,7 +62,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
                     choices=["mha_7b", "gqa_8b", "prefix_8b", "prefill_8b", "swap_8b",
-                             "pool_churn"],
+                             "block_copy_8b", "pool_churn"],
                     default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -246,6 +249,29 @@ def kernel_source_hash() -> str:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def copy_kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "pagedattention_decode_attention_gb300", "csrc",
+                           "copy_kernels.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_copy_traffic():
+    """Steady-state DRAM bytes per block_copy launch of the block_copy_8b
+    workload from the committed ncu summary, if it was taken on the current
+    kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "block_copy_cow_divergence_8b.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not src or not val or src.group(1) != copy_kernel_source_hash():
+        return None
+    return float(val.group(1))
 
 
 def profiled_traffic(workload: str):
@@ -922,6 +948,178 @@ def run_swap_bench(args):
     print(json.dumps(line))
 
 
+def cow_divergence(pool, script):
+    """Drives a block pool (the native one or the oracle's model, same calls)
+    to the divergence point of parallel sampling: every prompt of
+    ``prompt_len + shared_extra`` tokens forked into ``branches`` branches,
+    then one append per branch.  Returns the copy-on-write pairs, int64
+    [P, 2]: every branch but the last holder of each shared partial block
+    gets its own copy."""
+    roots = []
+    for p in range(script.prompts):
+        s = pool.new_seq()
+        for _ in range(script.prompt_len + int(script.shared_extra[p])):
+            pool.append_slot(s)
+        roots.append(s)
+    branches = []
+    for s in roots:
+        branches.append(s)
+        branches.extend(pool.fork(s) for _ in range(script.branches - 1))
+    pairs = [cow for _, cow in (pool.append_slot(b) for b in branches) if cow is not None]
+    return np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+
+
+COPY_METRIC = "paged KV copy-on-write block copies/s (all layers, K and V), 1 GPU"
+
+
+def run_copy_bench(args):
+    """Copy-on-write at the divergence of parallel sampling: 32 prompts of
+    1024 + U{1..15} tokens forked 4 ways; the first divergent append of each
+    branch copies the shared partial block (96 pairs), in every one of 32
+    8B-shaped GQA layers (32 / 8 heads, head_dim 128, bf16), one launch per
+    step.  The pairs come from the native pool; consecutive steps use four
+    relabellings of the physical ids so each step copies other blocks.
+    Roofline: bytes read + written against the measured HBM copy."""
+    import pagedattention_decode_attention_gb300 as pa
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    layers = args.layers if args.layers > 0 else 32
+    hkv, d, dt = 8, 128, torch.bfloat16
+    script = wl.sampling_cow()
+    nb = script.num_blocks
+    pool = pa.BlockPool(nb, 16, script.initial_order)
+    base = cow_divergence(pool, script)
+    npairs = base.shape[0]
+    assert npairs == script.prompts * (script.branches - 1)
+    gen = np.random.default_rng(wl.SEED_BASE + 8)
+    relabel = [np.arange(nb)] + [gen.permutation(nb) for _ in range(3)]
+    pair_sets = [torch.from_numpy(r[base]).to(device) for r in relabel]
+    kc = [wl.normal((nb, hkv, 16, d), dt, 5000 + 2 * i, device) for i in range(layers)]
+    vc = [wl.normal((nb, hkv, 16, d), dt, 5001 + 2 * i, device) for i in range(layers)]
+    block_bytes = hkv * 16 * d * 2
+    moved = 2 * 2 * block_bytes * npairs * layers       # K and V, read + written, per pair
+    # The branches of one prompt copy the same shared block, so a source is
+    # read from DRAM once and from L2 after that: the DRAM minimum counts
+    # each distinct source once and every destination once.
+    n_src = len(np.unique(base[:, 0]))
+    unique = 2 * block_bytes * (n_src + npairs) * layers
+    caches = pa.LayerCaches(kc, vc)        # checked once; each copy is one C call
+    host_sets = [torch.from_numpy(r[base]).pin_memory() for r in relabel]
+    staging = torch.empty_like(pair_sets[0])
+
+    warm = max(args.warmup, 3)
+    for i in range(warm):
+        caches.block_copy(pair_sets[i % 4])
+    pa.check_status()
+    torch.cuda.synchronize()
+    steps = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    clocks = ClockSampler(device)
+    clocks.start()
+    ev[0].record()
+    for i in range(steps):
+        caches.block_copy(pair_sets[i % 4])
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    # end to end: the pool's pairs copied from page-locked host memory, the
+    # copy, and the status read back, every step
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        staging.copy_(host_sets[i % 4], non_blocking=True)
+        caches.block_copy(staging)
+        pa.check_status()
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    per = [ev[i].elapsed_time(ev[i + 1]) / 1e3 for i in range(steps)]
+    total = ev[0].elapsed_time(ev[steps]) / 1e3
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    # context: one contiguous device-to-device copy of the same bytes
+    flat_src = torch.empty(moved // 2, dtype=torch.uint8, device=device)   # read + written = moved
+    flat_dst = torch.empty_like(flat_src)
+    for _ in range(3):
+        flat_dst.copy_(flat_src)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record()
+    for _ in range(steps):
+        flat_dst.copy_(flat_src)
+    m1.record()
+    torch.cuda.synchronize()
+    memcpy_gbs = moved * steps / (m0.elapsed_time(m1) / 1e3) / 1e9
+    del flat_src, flat_dst
+
+    # every destination equals its source afterwards (a fresh destination)
+    probe = pair_sets[1]
+    for c in (kc[0], vc[-1]):
+        c.index_fill_(0, probe[:, 1], 0)
+    caches.block_copy(probe)
+    pa.check_status()
+    for c in (kc[0], vc[-1]):
+        assert torch.equal(c.index_select(0, probe[:, 1]), c.index_select(0, probe[:, 0]))
+
+    peak, peak_kind = load_peaks()
+    avg = total / steps
+    line = {
+        "metric": COPY_METRIC, "value": npairs / avg, "unit": "block copies/s",
+        "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": avg * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) caches; pairs from the native pool's forks)",
+        "config": {"workload": "block_copy_8b", "layers": layers, "pairs": npairs,
+                   "prompts": script.prompts, "branches": script.branches,
+                   "num_kv_heads": hkv, "head_dim": d, "block_size": 16, "num_blocks": nb,
+                   "bytes_per_step": moved, "distinct_sources": n_src,
+                   "unique_bytes_per_step": unique,
+                   "l2": "inputs larger than L2 (201 MB copied per step, four rotating pair sets)",
+                   "step": "pa_block_copy of the 96 divergence pairs in all layers"},
+        "roofline": {"bound": "hbm", "achieved": unique / avg / 1e9, "peak": peak,
+                     "unit": "GB/s", "frac": unique / avg / 1e9 / peak,
+                     "traffic": profiled_copy_traffic(),
+                     "bytes": "unique: each distinct source block read once, each destination "
+                              "written once (K and V, all layers)",
+                     "median_ms": statistics.median(per) * 1e3, "best_ms": min(per) * 1e3,
+                     "median_gbs": unique / statistics.median(per) / 1e9,
+                     "per_pair_gbs": moved / avg / 1e9,
+                     "same_bytes_contiguous_copy_gbs": memcpy_gbs,
+                     "peak_source": f"{peak_kind} hbm_gbs (read + written bytes of a copy)"},
+        "e2e": {"value": npairs * steps / e2e_s, "unit": "block copies/s",
+                "h2d_bytes_per_step": int(staging.numel() * 8), "d2h_bytes_per_step": 4},
+        "gpu_launches": steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_copy_sample(script, layers, hkv, d, args.cpu_seconds / 4)
+    print(json.dumps(line))
+
+
+def oracle_copy_sample(script, layers, hkv, d, seconds):
+    """The oracle's pool model and block copy on the same divergence, host
+    caches holding only the blocks the pairs touch (16-bit words standing in
+    for bf16: the copy moves bytes), repeated for about ``seconds``."""
+    import oracle.attention as oa
+    from oracle.pool import BlockPool as ModelPool
+    model = ModelPool(script.num_blocks, 16, script.initial_order)
+    pairs = cow_divergence(model, script)
+    ids, compact = np.unique(pairs, return_inverse=True)
+    compact = compact.reshape(pairs.shape)
+    gen = np.random.default_rng(wl.SEED_BASE + 9)
+    shape = (len(ids), hkv, 16, d)
+    kc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    vc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    oa.block_copy(kc, vc, compact)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oa.block_copy(kc, vc, compact)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    secs = time.perf_counter() - t0
+    return {"value": len(pairs) * reps / secs, "unit": "block copies/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"{reps} runs of the oracle's block copy of the {len(pairs)} divergence "
+                       f"pairs in all {layers} layers, 1 thread")}
+
+
 def pool_churn_stream(seed: int, n: int):
     """Prefix-mix request stream: three 1024-token system prompts shared by
     all requests, suffixes lognormal (median 128, clipped to [1, 4096]), 8 to
@@ -1041,6 +1239,89 @@ def run_reference_prefill(args):
     print(json.dumps(line))
 
 
+def run_reference_copy(args):
+    """Reference arm of the block_copy_8b workload: the oracle's pool model
+    and block copy, each step one copy of the 96 divergence pairs in every
+    layer (host caches holding only the blocks the pairs touch)."""
+    import oracle.attention as oa
+    from oracle.pool import BlockPool as ModelPool
+    script = wl.sampling_cow()
+    layers = args.layers if args.layers > 0 else 32
+    hkv, d = 8, 128
+    pairs = cow_divergence(ModelPool(script.num_blocks, 16, script.initial_order), script)
+    ids, compact = np.unique(pairs, return_inverse=True)
+    compact = compact.reshape(pairs.shape)
+    gen = np.random.default_rng(wl.SEED_BASE + 9)
+    shape = (len(ids), hkv, 16, d)
+    kc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    vc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    warm = max(args.warmup, 3)
+    for _ in range(warm):
+        oa.block_copy(kc, vc, compact)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oa.block_copy(kc, vc, compact)
+    secs = time.perf_counter() - t0
+    value = len(pairs) * args.steps / secs
+    line = {
+        "impl": "reference", "metric": COPY_METRIC, "value": value, "unit": "block copies/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": warm, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic", "config": {"workload": "block_copy_8b", "layers": layers,
+                                        "pairs": len(pairs)},
+        "cpu_baseline": {"value": value, "unit": "block copies/s", "cores": 1, "kind": "oracle",
+                         "sample": (f"each step: the {len(pairs)} divergence pairs in all "
+                                    f"{layers} layers, numpy, 1 thread")},
+        "e2e": {"value": value, "unit": "block copies/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_reference_swap(args):
+    """Reference arm of the swap_8b workload: the oracle's block swap, each
+    step 64 blocks of every layer out to a second set of host caches and back
+    (a bounded sample of the 1024-block batch)."""
+    import oracle.attention as oa
+    layers = args.layers if args.layers > 0 else 32
+    hkv, d, nblk, nb = 8, 128, 64, 128
+    gen = np.random.default_rng(wl.SEED_BASE + 7)
+    shape = (nb, hkv, 16, d)
+    dk = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    dv = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    hk = [np.empty((nblk, hkv, 16, d), dtype=np.uint16) for _ in range(layers)]
+    hv = [np.empty((nblk, hkv, 16, d), dtype=np.uint16) for _ in range(layers)]
+    out_pairs = np.stack([gen.choice(nb, nblk, replace=False), gen.permutation(nblk)], 1)
+    in_pairs = np.stack([gen.permutation(nblk), gen.choice(nb, nblk, replace=False)], 1)
+
+    def step():
+        oa.block_swap(dk, dv, hk, hv, out_pairs)
+        oa.block_swap(hk, hv, dk, dv, in_pairs)
+
+    warm = max(args.warmup, 3)
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    value = nblk * 16 * 2 * args.steps / secs
+    line = {
+        "impl": "reference", "metric": "paged KV block swap tokens/s (device <-> page-locked host), 1 GPU",
+        "value": value, "unit": "tokens/s (out + in, all layers)", "n_gpus": 1,
+        "steps": args.steps, "warmup": warm, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic", "config": {"workload": "swap_8b_bf16", "layers": layers},
+        "cpu_baseline": {"value": value, "unit": "tokens/s (out + in, all layers)", "cores": 1,
+                         "kind": "oracle",
+                         "sample": (f"each step: {nblk} blocks of all {layers} layers out and "
+                                    "back between host arrays, numpy, 1 thread")},
+        "e2e": {"value": value, "unit": "tokens/s (out + in, all layers)",
+                "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -1050,6 +1331,12 @@ def run_reference(args):
         return
     if args.workload == "pool_churn":
         run_reference_pool(args)
+        return
+    if args.workload == "block_copy_8b":
+        run_reference_copy(args)
+        return
+    if args.workload == "swap_8b":
+        run_reference_swap(args)
         return
     batch = make_batch(args.workload, 0)
     per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
@@ -1090,6 +1377,8 @@ def main():
         run_cascade_bench(args)
     elif args.workload == "swap_8b":
         run_swap_bench(args)
+    elif args.workload == "block_copy_8b":
+        run_copy_bench(args)
     elif args.workload == "pool_churn":
         run_pool_bench(args)
     else:

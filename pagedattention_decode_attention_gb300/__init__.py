@@ -17,6 +17,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
 * :func:`block_copy` -- copy-on-write block copies across all layers;
 * :func:`block_swap` -- whole blocks between the device caches and
   page-locked host caches (preemption / offload), all layers in one launch;
+* :class:`LayerCaches` -- every layer's caches checked once, for repeated
+  copies and swaps at one C call each;
 
 and the native host :class:`BlockPool` that produces tables, slots and copy
 pairs.  The library is loaded on first use; if it has not been built the call
@@ -25,8 +27,8 @@ raises -- there is no fallback implementation.
 
 from .capi import PagedAttnError  # noqa: F401
 from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
-from .ops import (Prepared, alloc_prefill_workspace, alloc_workspace, block_copy,  # noqa: F401
-                  block_swap, check_status, kv_append, paged_attention_decode,
+from .ops import (LayerCaches, Prepared, alloc_prefill_workspace, alloc_workspace,  # noqa: F401
+                  block_copy, block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
                   paged_attention_decode_shared_prefix_run, shared_prefix_plan,
                   paged_attention_prefill, paged_attention_prefill_run, prefill_plan,

@@ -7,9 +7,9 @@
 // "留书阁 / knowledge-20" block-table example.  block_copy follows the same
 // appendix, section 4.4 (the writer gets a private copy of a shared block).
 //
-// Both are pure data movement: 16-byte vector loads/stores, one thread per
-// 16-byte chunk, consecutive threads on consecutive chunks of a row so every
-// warp moves whole 128-byte lines.
+// Both are pure data movement in 16-byte vector loads/stores, consecutive
+// threads on consecutive chunks so every warp moves whole 128-byte lines:
+// kv_append one chunk per thread, the whole-block copies eight per thread.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -66,6 +66,28 @@ struct LayerPtrs {
   uint4* v[kMaxLayers];
 };
 
+// One block's `block_vecs` 16-byte chunks, from -> to, by the whole CTA.
+// Each thread issues eight loads before its eight stores, so an SM keeps
+// enough bytes in flight to cover HBM (or CPU-GPU link) latency.  The two
+// ranges must not overlap (a pair's source and destination are different
+// blocks).
+__device__ __forceinline__ void copy_block(const uint4* from, uint4* to, int block_vecs) {
+  constexpr int kBatch = 8;
+  for (int base = 0; base < block_vecs; base += kBatch * blockDim.x) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < block_vecs) r[u] = from[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + u * blockDim.x + threadIdx.x;
+      if (i < block_vecs) to[i] = r[u];
+    }
+  }
+}
+
 __global__ void block_copy_kernel(const __grid_constant__ LayerPtrs ptrs,
                                   const int64_t* __restrict__ pairs, int block_vecs,
                                   int64_t num_blocks, unsigned* status) {
@@ -79,9 +101,7 @@ __global__ void block_copy_kernel(const __grid_constant__ LayerPtrs ptrs,
   }
   if (src == dst) return;
   uint4* base = blockIdx.z == 0 ? ptrs.k[layer] : ptrs.v[layer];
-  const uint4* from = base + src * block_vecs;
-  uint4* to = base + dst * block_vecs;
-  for (int i = threadIdx.x; i < block_vecs; i += blockDim.x) to[i] = from[i];
+  copy_block(base + src * block_vecs, base + dst * block_vecs, block_vecs);
 }
 
 // Whole-block copies between two caches of the same shape (one on the
@@ -103,20 +123,7 @@ __global__ void block_swap_kernel(const __grid_constant__ LayerPtrs src,
   }
   const uint4* from = (blockIdx.z == 0 ? src.k[layer] : src.v[layer]) + s * block_vecs;
   uint4* to = (blockIdx.z == 0 ? dst.k[layer] : dst.v[layer]) + d * block_vecs;
-  constexpr int kBatch = 8;
-  for (int base = 0; base < block_vecs; base += kBatch * blockDim.x) {
-    uint4 r[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * blockDim.x + threadIdx.x;
-      if (i < block_vecs) r[u] = from[i];
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = base + u * blockDim.x + threadIdx.x;
-      if (i < block_vecs) to[i] = r[u];
-    }
-  }
+  copy_block(from, to, block_vecs);
 }
 
 int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
@@ -133,15 +140,16 @@ int check_common(int dtype, int head_dim, int num_kv_heads, int num_blocks, cons
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
 
-// These copies use no shared memory; asking for the largest shared-memory
-// split anyway keeps the SM configured as the attention kernel that follows
-// them in a decode step wants it, so no reconfiguration sits between them.
+// kv_append uses no shared memory and moves a few rows; asking for the
+// largest shared-memory split anyway keeps the SM configured as the attention
+// kernel that follows it in a decode step wants it, so no reconfiguration
+// sits between them.  block_copy keeps the default split: its loads in
+// flight need the L1 that a maximal shared-memory split takes away (16-18 %
+// slower copies with it).
 void prefer_max_shared() {
   static std::once_flag once;
   std::call_once(once, [] {
     cudaFuncSetAttribute(kv_append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    cudaFuncSetAttribute(block_copy_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                          cudaSharedmemCarveoutMaxShared);
   });
 }
@@ -227,7 +235,6 @@ PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_l
   }
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
-  prefer_max_shared();
   const int block_vecs = num_kv_heads * kBlockSize * head_dim * elem_bytes(dtype) / 16;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_pairs, num_layers, 2);

@@ -420,59 +420,88 @@ def paged_attention_prefill(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     return out
 
 
+class LayerCaches:
+    """Every layer's K and V cache (``[num_blocks, Hkv, 16, d]`` each), checked
+    once, with the per-layer pointer arrays the multi-layer copies pass
+    through the C ABI built once.  A copy-on-write step then costs one C call
+    instead of a pass over every layer's tensors.
+
+    ``host=False``: CUDA tensors on one device.  ``host=True``: contiguous
+    page-locked CPU tensors (the swap tier).  The object holds references to
+    the tensors; resizing or replacing their storage afterwards is not seen
+    (build a new object)."""
+
+    def __init__(self, k_caches, v_caches, host: bool = False):
+        k, v = list(k_caches), list(v_caches)
+        _require(len(k) == len(v) and len(k) > 0, "need one K and one V cache per layer")
+        ref = k[0]
+        _require(ref.dim() == 4 and ref.shape[2] == 16,
+                 "caches must be [num_blocks, num_kv_heads, 16, head_dim]")
+        self.device = None if host else ref.device
+        for t in k + v:
+            if host:
+                _require(not t.is_cuda and t.is_pinned() and t.is_contiguous(),
+                         "host caches must be contiguous page-locked CPU tensors")
+            else:
+                _cuda_contig("cache", t, self.device)
+            _require(t.shape == ref.shape and t.dtype == ref.dtype,
+                     "all layer caches must share shape and dtype")
+        self.k, self.v, self.host = k, v, host
+        self.num_layers = len(k)
+        self.num_blocks, self.num_kv_heads, _, self.head_dim = ref.shape
+        self.dtype = ref.dtype
+        self._code = _dtype_code(ref)
+        n = self.num_layers
+        self._kp = (C.c_void_p * n)(*[t.data_ptr() for t in k])
+        self._vp = (C.c_void_p * n)(*[t.data_ptr() for t in v])
+
+    def _pairs(self, pairs: torch.Tensor, name: str) -> None:
+        _require(pairs.is_cuda and pairs.device == self.device and pairs.is_contiguous(),
+                 f"{name} must be contiguous on {self.device}")
+        _require(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2,
+                 f"{name} must be int64 [n, 2]")
+
+    def block_copy(self, src_dst_pairs: torch.Tensor, stream=None) -> None:
+        """Copy whole blocks ``src -> dst`` (int64 ``[P, 2]`` on the device) in
+        every layer, one launch."""
+        _require(not self.host, "block_copy runs on device caches")
+        self._pairs(src_dst_pairs, "src_dst_pairs")
+        capi.check(capi.lib().pa_block_copy(
+            self._kp, self._vp, self.num_layers, src_dst_pairs.data_ptr(),
+            src_dst_pairs.shape[0], self.num_kv_heads, self.head_dim, self.num_blocks,
+            self._code, _stream(self.device, stream)))
+
+    def block_swap(self, host: "LayerCaches", pairs: torch.Tensor, direction: int,
+                   stream=None) -> None:
+        """Copy whole blocks between these device caches and the page-locked
+        ``host`` caches, every layer in one launch: ``PA_SWAP_OUT`` copies
+        device block ``pairs[i, 0]`` to host block ``pairs[i, 1]``,
+        ``PA_SWAP_IN`` host ``pairs[i, 0]`` to device ``pairs[i, 1]`` (the
+        pairs the pool's swap_out / swap_in return)."""
+        _require(not self.host and host.host, "block_swap goes between device and host caches")
+        _require(host.num_layers == self.num_layers and host.dtype == self.dtype
+                 and (host.num_kv_heads, host.head_dim) == (self.num_kv_heads, self.head_dim),
+                 "host caches must be [num_host_blocks, num_kv_heads, 16, head_dim] of the "
+                 "device caches' dtype, one per layer")
+        self._pairs(pairs, "pairs")
+        capi.check(capi.lib().pa_block_swap(
+            self._kp, self._vp, host._kp, host._vp, self.num_layers, pairs.data_ptr(),
+            pairs.shape[0], int(direction), self.num_kv_heads, self.head_dim, self.num_blocks,
+            host.num_blocks, self._code, _stream(self.device, stream)))
+
+
 def block_swap(dev_k_caches, dev_v_caches, host_k_caches, host_v_caches,
                pairs: torch.Tensor, direction: int, stream=None) -> None:
-    """Copy whole blocks between the device caches and page-locked host caches
-    (``[num_host_blocks, Hkv, 16, d]`` per layer), every layer in one launch:
-    ``direction`` ``PA_SWAP_OUT`` copies device block ``pairs[i, 0]`` to host
-    block ``pairs[i, 1]``; ``PA_SWAP_IN`` copies host ``pairs[i, 0]`` to device
-    ``pairs[i, 1]`` (the pairs the pool's swap_out / swap_in return)."""
-    dk, dv, hk, hv = (list(x) for x in (dev_k_caches, dev_v_caches, host_k_caches, host_v_caches))
-    _require(len(dk) == len(dv) == len(hk) == len(hv) and len(dk) > 0,
-             "need one device and one host K/V cache per layer")
-    dev = dk[0].device
-    ref, href = dk[0], hk[0]
-    for t in dk + dv:
-        _cuda_contig("device cache", t, dev)
-        _require(t.shape == ref.shape and t.dtype == ref.dtype, "device caches must match")
-    for t in hk + hv:
-        _require(not t.is_cuda and t.is_pinned() and t.is_contiguous(),
-                 "host caches must be contiguous page-locked CPU tensors")
-        _require(t.shape[1:] == ref.shape[1:] and t.dtype == ref.dtype and t.shape == href.shape,
-                 "host caches must be [num_host_blocks, num_kv_heads, 16, head_dim] of q's dtype")
-    _cuda_contig("pairs", pairs, dev)
-    _require(pairs.dtype == torch.int64 and pairs.dim() == 2 and pairs.shape[1] == 2,
-             "pairs must be int64 [n, 2] on the device")
-    n = len(dk)
-    arr = lambda ts: (C.c_void_p * n)(*[t.data_ptr() for t in ts])  # noqa: E731
-    nb, hkv, _, d = ref.shape
-    capi.check(capi.lib().pa_block_swap(arr(dk), arr(dv), arr(hk), arr(hv), n, pairs.data_ptr(),
-                                        pairs.shape[0], int(direction), hkv, d, nb,
-                                        href.shape[0], _dtype_code(ref), _stream(dev, stream)))
+    """:meth:`LayerCaches.block_swap` on caches given as per-layer lists
+    (checked on every call)."""
+    LayerCaches(dev_k_caches, dev_v_caches).block_swap(
+        LayerCaches(host_k_caches, host_v_caches, host=True), pairs, direction, stream)
 
 
 def block_copy(k_caches, v_caches, src_dst_pairs: torch.Tensor, stream=None) -> None:
-    """Copy whole blocks ``src -> dst`` (int64 ``[P, 2]`` on the device) in every
-    layer's caches."""
-    k_caches, v_caches = list(k_caches), list(v_caches)
-    _require(len(k_caches) == len(v_caches) and len(k_caches) > 0, "need one k/v cache per layer")
-    dev = k_caches[0].device
-    ref = k_caches[0]
-    for kc, vc in zip(k_caches, v_caches):
-        _cuda_contig("k_cache", kc, dev)
-        _cuda_contig("v_cache", vc, dev)
-        _require(kc.shape == ref.shape == vc.shape and kc.dtype == vc.dtype == ref.dtype,
-                 "all layer caches must share shape and dtype")
-    _cuda_contig("src_dst_pairs", src_dst_pairs, dev)
-    _require(src_dst_pairs.dtype == torch.int64 and src_dst_pairs.dim() == 2
-             and src_dst_pairs.shape[1] == 2, "src_dst_pairs must be int64 [P, 2]")
-    nb, hkv, _, d = ref.shape
-    n = len(k_caches)
-    kp = (C.c_void_p * n)(*[t.data_ptr() for t in k_caches])
-    vp = (C.c_void_p * n)(*[t.data_ptr() for t in v_caches])
-    capi.check(capi.lib().pa_block_copy(
-        kp, vp, n, src_dst_pairs.data_ptr(), src_dst_pairs.shape[0], hkv, d, nb,
-        _dtype_code(ref), _stream(dev, stream)))
+    """:meth:`LayerCaches.block_copy` on caches given as per-layer lists
+    (checked on every call)."""
+    LayerCaches(k_caches, v_caches).block_copy(src_dst_pairs, stream)
 
 
 def check_status(stream=None, device=None) -> None:

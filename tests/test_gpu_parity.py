@@ -154,12 +154,14 @@ def test_kv_append_out_of_range_slot(gpu):
 
 
 # ------------------------------------------------------------ block_copy
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_block_copy_bit_exact_all_layers(gpu, dtype):
+# A block is 2048 16-byte chunks in bf16 8 x 128 (one batch of eight per
+# thread), 4096 in f32 (two batches) and 384 in f16 3 x 64 (a ragged batch).
+@pytest.mark.parametrize("dtype,hkv,d", [("bf16", 8, 128), ("f32", 8, 128), ("f16", 3, 64)])
+def test_block_copy_bit_exact_all_layers(gpu, dtype, hkv, d):
     dt = TORCH_DTYPES[dtype]
     from pagedattention_decode_attention_gb300 import workloads as wl
-    layers = [(wl.normal((30, 8, 16, 128), dt, 10 + i, gpu),
-               wl.normal((30, 8, 16, 128), dt, 50 + i, gpu)) for i in range(5)]
+    layers = [(wl.normal((30, hkv, 16, d), dt, 10 + i, gpu),
+               wl.normal((30, hkv, 16, d), dt, 50 + i, gpu)) for i in range(5)]
     pairs = np.array([[1, 20], [2, 21], [7, 3], [29, 0]], dtype=np.int64)
     ref = [(k.cpu().clone(), v.cpu().clone()) for k, v in layers]
     as_np = (lambda t: t.numpy()) if dt == torch.float32 else (lambda t: t.view(torch.int16).numpy())

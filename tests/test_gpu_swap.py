@@ -117,3 +117,56 @@ def test_block_swap_rejects_pageable_host_memory_and_bad_ids(gpu):
     pa().block_swap(dk, dv, hk, hv, bad, pa().PA_SWAP_OUT)
     with pytest.raises(pa().PagedAttnError):
         pa().check_status()
+
+
+# ------------------------------------------------------- prepared caches
+def test_layer_caches_copy_and_swap_repeated(gpu):
+    """One LayerCaches object serves many copy-on-write copies and a swap
+    round trip; every result equals the oracle's, bit for bit."""
+    dt, nb, hkv, d, layers = torch.bfloat16, 40, 8, 128, 6
+    dk = [wl.normal((nb, hkv, 16, d), dt, 300 + i, gpu) for i in range(layers)]
+    dv = [wl.normal((nb, hkv, 16, d), dt, 400 + i, gpu) for i in range(layers)]
+    rk, rv = [as_bits(t).copy() for t in dk], [as_bits(t).copy() for t in dv]
+    caches = pa().LayerCaches(dk, dv)
+    assert (caches.num_layers, caches.num_blocks, caches.num_kv_heads, caches.head_dim) == \
+        (layers, nb, hkv, d)
+    steps = [np.array([[1, 20], [2, 21]]), np.array([[20, 30], [7, 3], [39, 0]]),
+             np.array([[5, 6]])]
+    for pairs in steps:
+        oa.block_copy(rk, rv, pairs)
+        caches.block_copy(torch.from_numpy(pairs.astype(np.int64)).to(gpu))
+    hk = [torch.zeros((8, hkv, 16, d), dtype=dt).pin_memory() for _ in range(layers)]
+    hv = [torch.zeros((8, hkv, 16, d), dtype=dt).pin_memory() for _ in range(layers)]
+    host = pa().LayerCaches(hk, hv, host=True)
+    hrk, hrv = [as_bits(t).copy() for t in hk], [as_bits(t).copy() for t in hv]
+    out = np.array([[20, 0], [3, 5], [39, 7]])
+    inn = np.array([[0, 11], [7, 12]])
+    oa.block_swap(rk, rv, hrk, hrv, out)
+    caches.block_swap(host, torch.from_numpy(out.astype(np.int64)).to(gpu), pa().PA_SWAP_OUT)
+    oa.block_swap(hrk, hrv, rk, rv, inn)
+    caches.block_swap(host, torch.from_numpy(inn.astype(np.int64)).to(gpu), pa().PA_SWAP_IN)
+    pa().check_status()
+    for got, want in zip(dk + dv + hk + hv, rk + rv + hrk + hrv):
+        assert np.array_equal(as_bits(got), want)
+
+
+def test_layer_caches_rejects_mismatches(gpu):
+    k = [torch.zeros((4, 2, 16, 64), dtype=torch.float16, device=gpu) for _ in range(2)]
+    with pytest.raises(ValueError):
+        pa().LayerCaches(k, k[:1])                                    # layer counts differ
+    with pytest.raises(ValueError):
+        pa().LayerCaches(k, [k[0], torch.zeros((4, 2, 16, 128), dtype=torch.float16,
+                                               device=gpu)])         # shapes differ
+    with pytest.raises(ValueError):
+        pa().LayerCaches([t.cpu() for t in k], [t.cpu() for t in k], host=True)   # pageable
+    caches = pa().LayerCaches(k, k)
+    with pytest.raises(ValueError):
+        caches.block_copy(torch.tensor([[0, 1]], dtype=torch.int32, device=gpu))
+    host = pa().LayerCaches([torch.zeros((4, 2, 16, 64), dtype=torch.float16).pin_memory()],
+                            [torch.zeros((4, 2, 16, 64), dtype=torch.float16).pin_memory()],
+                            host=True)
+    with pytest.raises(ValueError):                                   # one host layer, two device
+        caches.block_swap(host, torch.tensor([[0, 1]], dtype=torch.int64, device=gpu),
+                          pa().PA_SWAP_OUT)
+    with pytest.raises(ValueError):
+        host.block_copy(torch.tensor([[0, 1]], dtype=torch.int64, device=gpu))
