@@ -174,22 +174,47 @@ def run_prefill_bench(args):
             pa.paged_attention_prefill_run(q[layer], kc[layer], vc[layer], bt, cl, qs_d,
                                            batch.scale, ws, out=out[layer])
 
+    # The chunk's own K/V rows, appended to their paged slots in every layer
+    # before its attention (a model step does this; the attention-only pass
+    # above it is the kernel's roofline).
+    pos = np.concatenate([np.arange(c - n, c) for c, n in zip(batch.context_lens, qlens)])
+    seq = np.repeat(np.arange(batch.num_seqs), qlens)
+    slots = torch.from_numpy((batch.block_tables[seq, pos // 16].astype(np.int64) * 16
+                              + pos % 16)).to(device)
+    k_new = wl.normal((L, total_q, hkv, d), dt, s0 + 8, device)
+    v_new = wl.normal((L, total_q, hkv, d), dt, s0 + 9, device)
+    appends = [pa.prepare_kv_append(k_new[i], v_new[i], kc[i], vc[i], slots) for i in range(L)]
+
+    def step_with_append():
+        pa.prefill_plan(cl, qs_d, total_q, hq, hkv, d, batch.max_blocks, batch.scale, dt, ws)
+        for layer in range(L):
+            appends[layer]()
+            pa.paged_attention_prefill_run(q[layer], kc[layer], vc[layer], bt, cl, qs_d,
+                                           batch.scale, ws, out=out[layer])
+
+    def timed(fn):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            fn()
+        end.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / 1e3
+
     for _ in range(max(args.warmup, 3)):
         step()
+        step_with_append()
     torch.cuda.synchronize()
     pa.check_status()
     clocks = ClockSampler(device)
     clocks.start()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(args.steps):
-        step()
-    end.record()
-    torch.cuda.synchronize()
+    secs = timed(step)
+    secs_append = timed(step_with_append)
     clk = clocks.stop()
     pa.check_status()
-    secs = start.elapsed_time(end) / 1e3
     per_call = secs / (args.steps * L)     # one layer's share of a step
+    per_layer_append = secs_append / (args.steps * L)
+    append_bytes = 2 * 2 * total_q * hkv * d * ELEM[batch.dtype] + total_q * 8
     flops = prefill_flops(batch)
     kv_bytes = int(batch.context_lens.astype(np.int64).sum()) * 2 * hkv * d * ELEM[batch.dtype]
     peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"]) \
@@ -213,6 +238,12 @@ def run_prefill_bench(args):
                      "unit": "TFLOP/s", "frac": flops / per_call / 1e12 / peak,
                      "flops_per_launch": flops, "peak_source": "measured bf16_tflops (burst)",
                      "kv_read_gbs_unique": kv_bytes / per_call / 1e9},
+        "with_append": {"ms_per_layer": per_layer_append * 1e3,
+                        "tokens_per_s": total_q / per_layer_append,
+                        "append_ms_per_layer": (per_layer_append - per_call) * 1e3,
+                        "append_bytes": append_bytes,
+                        "append_gbs": append_bytes / max(per_layer_append - per_call, 1e-9) / 1e9,
+                        "step": "per layer: kv_append of the chunk's K/V, then attention"},
         "gpu_launches": (1 + L) * args.steps,
         "clocks": clk,
     }

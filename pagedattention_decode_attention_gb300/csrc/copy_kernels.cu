@@ -10,6 +10,10 @@
 // Both are pure data movement in 16-byte vector loads/stores, consecutive
 // threads on consecutive chunks so every warp moves whole 128-byte lines:
 // kv_append one chunk per thread, the whole-block copies eight per thread.
+// Both keep the default shared-memory / L1 split: their loads in flight need
+// the L1 that the largest shared-memory split takes away (block copies ran
+// 16-18 % slower with it, and a kernel that needs that split right after a
+// small append started no later without it).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -140,20 +144,6 @@ int check_common(int dtype, int head_dim, int num_kv_heads, int num_blocks, cons
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; }
 
-// kv_append uses no shared memory and moves a few rows; asking for the
-// largest shared-memory split anyway keeps the SM configured as the attention
-// kernel that follows it in a decode step wants it, so no reconfiguration
-// sits between them.  block_copy keeps the default split: its loads in
-// flight need the L1 that a maximal shared-memory split takes away (16-18 %
-// slower copies with it).
-void prefer_max_shared() {
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaFuncSetAttribute(kv_append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-  });
-}
-
 }  // namespace
 
 unsigned* device_status_word() {
@@ -191,7 +181,6 @@ PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cac
     return fail(PA_ERR_INVALID_ARG, "kv_append: tensors must be 16-byte aligned");
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
-  prefer_max_shared();
   const int row_vecs = head_dim * elem_bytes(dtype) / 16;
   const int heads_vecs = num_kv_heads * row_vecs;
   const int64_t total = int64_t(num_tokens) * heads_vecs;
