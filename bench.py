@@ -14,7 +14,8 @@ block tables as random disjoint draws from a pool of the needed blocks + 10 %,
 launches).  ``--workload gqa_8b`` runs the 8B-shaped GQA batch (128 sequences,
 32 / 8 heads, bf16, lengths log-uniform in [128, 8192] plus 4 x 8192, one layer).
 Other workloads: ``prefill_8b`` (chunked prefill), ``prefix_8b`` [``--cascade``]
-(shared-prefix batch), ``block_copy_8b`` (copy-on-write at a 4-way fork),
+(shared-prefix batch), ``sampling_8b`` (decode of 128 branches forked 4 ways
+from 32 prompts), ``block_copy_8b`` (copy-on-write at a 4-way fork),
 ``swap_8b`` (device <-> host block swap) and ``pool_churn`` (host pool).
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
@@ -61,8 +62,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=["mha_7b", "gqa_8b", "prefix_8b", "prefill_8b", "swap_8b",
-                             "block_copy_8b", "pool_churn"],
+                    choices=["mha_7b", "gqa_8b", "prefix_8b", "sampling_8b", "prefill_8b",
+                             "swap_8b", "block_copy_8b", "pool_churn"],
                     default="mha_7b")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,23 +84,57 @@ def dist_env():
     return rank, world, local
 
 
-def make_batch(name: str, rank: int) -> wl.DecodeBatch:
-    # each rank decodes its own independent batch (replicas; no exchange)
+def make_batch(name: str, rank: int, model_pool: bool = False) -> wl.DecodeBatch:
+    """The workload's batch; each rank decodes its own independent batch
+    (replicas; no exchange).  Tables of pool-built batches come from the
+    native pool, or with ``model_pool`` from the oracle's model of it (the
+    reference arm runs nothing of this library)."""
     if name == "mha_7b":
         return wl.mha_7b(seed=wl.SEED_BASE + 2 + 100 * rank)
     if name == "prefill_8b":
         return wl.prefill_8b(seed=wl.SEED_BASE + 6 + 100 * rank)
     if name == "prefix_8b":
-        return prefix_batch(wl.prefix_mix(seed=wl.SEED_BASE + 5 + 100 * rank))
+        return prefix_batch(wl.prefix_mix(seed=wl.SEED_BASE + 5 + 100 * rank), model_pool)
+    if name == "sampling_8b":
+        return sampling_batch(wl.sampling_cow(seed=wl.SEED_BASE + 4 + 100 * rank), model_pool)
     return wl.gqa_8b(seed=wl.SEED_BASE + 3 + 100 * rank)
 
 
-def prefix_batch(script) -> wl.DecodeBatch:
-    """The prefix-mix decode batch, tables from the native pool: one pinned
-    prefix sequence, then every request shares its blocks and appends its own
-    suffix (the request's newest token last)."""
+def make_pool(script, model_pool: bool):
+    if model_pool:
+        from oracle.pool import BlockPool as ModelPool
+        return ModelPool(script.num_blocks, 16, script.initial_order)
     import pagedattention_decode_attention_gb300 as pa
-    pool = pa.BlockPool(script.num_blocks, 16, script.initial_order)
+    return pa.BlockPool(script.num_blocks, 16, script.initial_order)
+
+
+def pool_tables(pool, seqs):
+    """Block tables (int32, -1 padded to the longest) and context lengths."""
+    rows = [pool.block_table(s) for s in seqs]
+    tab = np.full((len(rows), max(len(t) for t, _ in rows)), -1, dtype=np.int32)
+    for i, (t, _) in enumerate(rows):
+        tab[i, :len(t)] = t
+    return tab, np.array([c for _, c in rows], dtype=np.int32)
+
+
+def sampling_batch(script, model_pool: bool = False) -> wl.DecodeBatch:
+    """Parallel sampling after the divergence: the branches of every prompt,
+    sharing all of their prompt's blocks but the last (each branch's own
+    copy, or the block its last holder kept).  Eight layer caches rotate so
+    a step reads about 1.1 GB of distinct K/V (one layer's 138 MB would
+    nearly fit in L2)."""
+    pool = make_pool(script, model_pool)
+    branches, _ = cow_divergence(pool, script)
+    tables, lens = pool_tables(pool, branches)
+    return wl.DecodeBatch("sampling_8b_bf16", 32, 8, 128, "bf16", lens, tables, script.num_blocks,
+                          num_layers=8, seed=script.seed)
+
+
+def prefix_batch(script, model_pool: bool = False) -> wl.DecodeBatch:
+    """The prefix-mix decode batch, tables from the pool: one pinned prefix
+    sequence, then every request shares its blocks and appends its own
+    suffix (the request's newest token last)."""
+    pool = make_pool(script, model_pool)
     root = pool.new_seq()
     for _ in range(script.prefix_len):
         pool.append_slot(root)
@@ -111,8 +146,7 @@ def prefix_batch(script) -> wl.DecodeBatch:
         for _ in range(int(n)):
             pool.append_slot(s)
         seqs.append(s)
-    max_blocks = max(len(pool.block_table(s)[0]) for s in seqs)
-    tables, lens = pool.tables(seqs, max_blocks)
+    tables, lens = pool_tables(pool, seqs)
     return wl.DecodeBatch("prefix_8b_bf16", 32, 8, 128, "bf16", lens, tables, script.num_blocks,
                           num_layers=script.num_layers, seed=script.seed,
                           extra={"prefix_blocks": script.prefix_len // 16})
@@ -983,9 +1017,9 @@ def cow_divergence(pool, script):
     """Drives a block pool (the native one or the oracle's model, same calls)
     to the divergence point of parallel sampling: every prompt of
     ``prompt_len + shared_extra`` tokens forked into ``branches`` branches,
-    then one append per branch.  Returns the copy-on-write pairs, int64
-    [P, 2]: every branch but the last holder of each shared partial block
-    gets its own copy."""
+    then one append per branch.  Returns the branches and the copy-on-write
+    pairs, int64 [P, 2]: every branch but the last holder of each shared
+    partial block gets its own copy."""
     roots = []
     for p in range(script.prompts):
         s = pool.new_seq()
@@ -997,7 +1031,7 @@ def cow_divergence(pool, script):
         branches.append(s)
         branches.extend(pool.fork(s) for _ in range(script.branches - 1))
     pairs = [cow for _, cow in (pool.append_slot(b) for b in branches) if cow is not None]
-    return np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    return branches, np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
 
 
 COPY_METRIC = "paged KV copy-on-write block copies/s (all layers, K and V), 1 GPU"
@@ -1019,7 +1053,7 @@ def run_copy_bench(args):
     script = wl.sampling_cow()
     nb = script.num_blocks
     pool = pa.BlockPool(nb, 16, script.initial_order)
-    base = cow_divergence(pool, script)
+    _, base = cow_divergence(pool, script)
     npairs = base.shape[0]
     assert npairs == script.prompts * (script.branches - 1)
     gen = np.random.default_rng(wl.SEED_BASE + 8)
@@ -1130,7 +1164,7 @@ def oracle_copy_sample(script, layers, hkv, d, seconds):
     import oracle.attention as oa
     from oracle.pool import BlockPool as ModelPool
     model = ModelPool(script.num_blocks, 16, script.initial_order)
-    pairs = cow_divergence(model, script)
+    _, pairs = cow_divergence(model, script)
     ids, compact = np.unique(pairs, return_inverse=True)
     compact = compact.reshape(pairs.shape)
     gen = np.random.default_rng(wl.SEED_BASE + 9)
@@ -1279,7 +1313,7 @@ def run_reference_copy(args):
     script = wl.sampling_cow()
     layers = args.layers if args.layers > 0 else 32
     hkv, d = 8, 128
-    pairs = cow_divergence(ModelPool(script.num_blocks, 16, script.initial_order), script)
+    _, pairs = cow_divergence(ModelPool(script.num_blocks, 16, script.initial_order), script)
     ids, compact = np.unique(pairs, return_inverse=True)
     compact = compact.reshape(pairs.shape)
     gen = np.random.default_rng(wl.SEED_BASE + 9)
@@ -1369,7 +1403,7 @@ def run_reference(args):
     if args.workload == "swap_8b":
         run_reference_swap(args)
         return
-    batch = make_batch(args.workload, 0)
+    batch = make_batch(args.workload, 0, model_pool=True)
     per_step_units = batch.num_layers          # one token's worth of (sequence, layer) units
     inp = OracleInputs(batch, None)
     for _ in range(max(args.warmup, 3)):
