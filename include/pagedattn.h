@@ -272,6 +272,69 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_grouped_prefix -- pa_paged_attention_decode for
+ * a batch made of groups of sequences, each group sharing its own prefix
+ * (the branches of one prompt forked for parallel sampling, requests that
+ * share one of several system prompts): every group's prefix is read once
+ * for all of the group's queries.
+ *
+ * "第 6 章 缓存管理", section 块表长什么样, and the OS-lab appendix, section
+ * 4.3 (forked sequences point their tables at the same physical blocks until
+ * a write copies one); the merge is the log-sum-exp reduction across blocks
+ * of "KV 的体积从哪来，页表如何把它切开".  Reading a group's shared blocks
+ * once per group is our extension, as in the single-prefix form above.
+ *
+ * Same result and arguments as pa_paged_attention_decode, plus:
+ *   group_start          DEVICE int32 [num_groups + 1]: group g is sequences
+ *                        group_start[g] .. group_start[g + 1] - 1 (members
+ *                        of a group are contiguous in the batch);
+ *                        group_start[0] = 0, group_start[num_groups] =
+ *                        num_seqs, non-decreasing.
+ *   group_prefix_blocks  DEVICE int32 [num_groups]: how many leading table
+ *                        entries every member of group g shares with the
+ *                        group's first member (0 .. max_blocks_per_seq; 0:
+ *                        nothing shared).  A member's context must cover
+ *                        them (context_lens[b] >= 16 * group_prefix_blocks).
+ *   num_groups           1 .. num_seqs.
+ * A member whose table does not start with its group's prefix, or whose
+ * group data or length is out of range, sets the status word
+ * (PA_ERR_DEVICE_BOUNDS from pa_check_status); its output is then
+ * unspecified.  16-bit dtypes only (PA_F32 returns PA_ERR_UNSUPPORTED: the
+ * fp32 decode is exact without it).  The workspace holds
+ * pa_paged_attention_decode_grouped_prefix_workspace_size bytes (256-byte
+ * aligned).
+ *
+ * _plan (block_tables, context_lens and the group arrays; once per decode
+ * step) writes each sequence's table past its group's prefix and the plans
+ * of the prefix phase and the suffix decode into the workspace; _run (per
+ * layer, same sizes and arrays, same workspace, stream order) launches the
+ * prefix phase, the suffix decode and the combine.  A run whose workspace
+ * holds no plan for its sizes does nothing and sets the status word
+ * (PA_ERR_INVALID_ARG); tables or lengths changed after the plan are not
+ * detected and give unspecified output.  The one-shot entry is _plan then
+ * _run.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_grouped_prefix_workspace_size(
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    size_t* bytes);
+PA_API int pa_paged_attention_decode_grouped_prefix(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* group_start, const int32_t* group_prefix_blocks,
+    int num_groups, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
+    size_t workspace_bytes, void* stream);
+PA_API int pa_paged_attention_decode_grouped_prefix_plan(
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
+    void* workspace, size_t workspace_bytes, void* stream);
+PA_API int pa_paged_attention_decode_grouped_prefix_run(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* group_start, const int32_t* group_prefix_blocks, int num_groups, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+    float scale, int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_prefill -- chunked-prefill attention over the paged cache.
  *
  * OS-lab appendix, section 2.1 (prefill writes the K/V of every prompt token

@@ -9,7 +9,8 @@ Device entry points (hand-written sm_103a kernels behind the C ABI in
   :func:`paged_attention_decode_run` split it so one plan serves every layer;
   :func:`paged_attention_decode_append_run` also appends each sequence's new
   token in the same launch; :func:`paged_attention_decode_shared_prefix` reads
-  a prefix shared by the whole batch once);
+  a prefix shared by the whole batch once;
+  :func:`paged_attention_decode_grouped_prefix` each group's own prefix once);
 * :func:`paged_attention_prefill` -- chunked-prefill attention: each
   sequence's newest tokens attend causally over the paged cache
   (:func:`prefill_plan` + :func:`paged_attention_prefill_run` split it so one
@@ -30,6 +31,8 @@ from .capi import PA_SWAP_IN, PA_SWAP_OUT  # noqa: F401
 from .ops import (LayerCaches, Prepared, alloc_prefill_workspace, alloc_workspace,  # noqa: F401
                   block_copy, block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
+                  paged_attention_decode_grouped_prefix, paged_attention_decode_grouped_prefix_run,
+                  grouped_prefix_plan, grouped_prefix_workspace_size,
                   paged_attention_decode_shared_prefix_run, shared_prefix_plan,
                   paged_attention_prefill, paged_attention_prefill_run, prefill_plan,
                   shared_prefix_workspace_size, prefill_workspace_size,

@@ -74,6 +74,16 @@ SIGNATURES = {
     "pa_paged_attention_decode_shared_prefix_run": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
                                                          _i, _i, _i, C.c_float, _i, _vp, _vp, _sz,
                                                          _vp]),
+    "pa_paged_attention_decode_grouped_prefix_workspace_size": (_i, [_i, _i, _i, _i, _i,
+                                                                     C.POINTER(_sz)]),
+    "pa_paged_attention_decode_grouped_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
+                                                      _i, _i, _i, _i, _i, C.c_float, _i, _vp,
+                                                      _vp, _sz, _vp]),
+    "pa_paged_attention_decode_grouped_prefix_plan": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                                                           _i, _i, C.c_float, _i, _vp, _sz, _vp]),
+    "pa_paged_attention_decode_grouped_prefix_run": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
+                                                          _i, _i, _i, _i, _i, C.c_float, _i, _vp,
+                                                          _vp, _sz, _vp]),
     "pa_paged_attention_prefill_workspace_size": (_i, [_i, _i, _i, _i, _i, C.POINTER(_sz)]),
     "pa_paged_attention_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                         C.c_float, _i, _vp, _vp, _sz, _vp]),

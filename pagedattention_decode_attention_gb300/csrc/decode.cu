@@ -1007,14 +1007,19 @@ namespace decode {
 // Last step of a shared-prefix decode: each (sequence, head) merges the
 // shared prefix's (o, lse) with its own suffix's by log-sum-exp weights
 // (base 2); a side empty of tokens has lse = -inf and weight 0.  Also checks
-// that every table starts with the shared prefix (row 0's entries).
+// that every table starts with the shared prefix (row 0's entries; none with
+// prefix_blocks 0).  Grouped mode (seq_blocks non-null): the row's parts are
+// those of its own group's prefix (seq_blocks[b] blocks, split as the word
+// at split_blocks says); the tables were checked when the step was planned.
 template <typename T, int D>
 __global__ void __launch_bounds__(256)
     cascade_combine_kernel(const float* __restrict__ po, const float* __restrict__ plse,
                            const int* __restrict__ prefix_parts, const float* __restrict__ so,
                            const float* __restrict__ slse, T* out, int rows,
                            const int32_t* __restrict__ block_tables, int prefix_blocks,
-                           int num_seqs, int max_blocks, unsigned* status) {
+                           int num_seqs, int max_blocks, unsigned* status,
+                           const int* __restrict__ seq_blocks, const int* __restrict__ split_blocks,
+                           int num_q_heads) {
   dev::grid_dependency_wait();
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * blockDim.x;
@@ -1023,15 +1028,19 @@ __global__ void __launch_bounds__(256)
     if (block_tables[b * max_blocks + j] != block_tables[j]) dev::flag_status(status, kStatusBounds);
   }
   // the prefix phase's parts per row: 1 .. kSharedMaxSplits (part k of row r
-  // at po + (k * rows + r) * D, plse[k * rows + r])
-  int np = *prefix_parts;
-  if (np < 1 || np > prefill::kSharedMaxSplits) {
+  // at po + (k * rows + r) * D, plse[k * rows + r]); 0 in grouped mode for a
+  // group with no shared blocks
+  int np_all = seq_blocks ? 0 : *prefix_parts;
+  if (!seq_blocks && (np_all < 1 || np_all > prefill::kSharedMaxSplits)) {
     if (tid == 0) dev::flag_status(status, kStatusBounds);
-    np = np < 1 ? 1 : prefill::kSharedMaxSplits;
+    np_all = np_all < 1 ? 1 : prefill::kSharedMaxSplits;
   }
+  const int split = seq_blocks ? *split_blocks : 0;
   using M = dev::Mma<T>;
   const int lane = threadIdx.x & 31;
   for (long long r = tid >> 5; r < rows; r += nthreads >> 5) {
+    const int np = seq_blocks ? prefill::shared_prefix_parts(seq_blocks[r / num_q_heads], split)
+                              : np_all;
     // weights of the prefix parts and of the suffix, by their log-sum-exp
     float lp[prefill::kSharedMaxSplits];
     const float ls = slse[r];
@@ -1068,6 +1077,60 @@ __global__ void __launch_bounds__(256)
       pk.y = M::pack(acc.z * inv, acc.w * inv);
       *reinterpret_cast<uint2*>(out + r * D + c) = pk;
     }
+  }
+}
+
+// Grouped shared-prefix decode, once per step: CTA b finds sequence b's group
+// (the g with group_start[g] <= b < group_start[g + 1]), checks that its table
+// starts with the group's prefix (the first member's first group_blocks[g]
+// entries), and writes what the suffix decode and the combine read: the
+// table past the prefix (-1 padded), the context past it, and the prefix's
+// block count.  Bad groups or lengths set the status word (the sequence then
+// keeps no prefix).
+__global__ void __launch_bounds__(128)
+    grouped_suffix_kernel(const int32_t* __restrict__ block_tables,
+                          const int32_t* __restrict__ context_lens,
+                          const int32_t* __restrict__ group_start,
+                          const int32_t* __restrict__ group_blocks, int num_groups, int num_seqs,
+                          int max_blocks, int32_t* __restrict__ sfx_tables,
+                          int32_t* __restrict__ sfx_ctx, int32_t* __restrict__ seq_blocks,
+                          unsigned* status) {
+  __shared__ int s_nb, s_first;
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();  // the previous kernel may still read these arrays
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    if (b == 0) {
+      bool ok = group_start[0] == 0 && group_start[num_groups] == num_seqs;
+      for (int g = 0; g < num_groups && ok; ++g) ok = group_start[g] <= group_start[g + 1];
+      if (!ok) dev::flag_status(status, kStatusBounds);
+    }
+    int lo = 0, hi = num_groups - 1;  // the last g with group_start[g] <= b
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (group_start[mid] <= b) lo = mid;
+      else hi = mid - 1;
+    }
+    const int first = group_start[lo];
+    int nb = group_blocks[lo];
+    const int ctx = context_lens[b];
+    if (first > b || group_start[lo + 1] <= b || first < 0 || nb < 0 || nb > max_blocks ||
+        ctx < nb * kBlockSize || ctx > max_blocks * kBlockSize) {
+      dev::flag_status(status, kStatusBounds);
+      nb = 0;
+    }
+    s_nb = nb;
+    s_first = first < 0 || first >= num_seqs ? b : first;
+    sfx_ctx[b] = max(0, min(ctx, max_blocks * kBlockSize) - nb * kBlockSize);
+    seq_blocks[b] = nb;
+  }
+  __syncthreads();
+  const int nb = s_nb, first = s_first;
+  const int32_t* row = block_tables + size_t(b) * max_blocks;
+  for (int j = threadIdx.x; j < max_blocks; j += blockDim.x) {
+    if (j < nb && row[j] != block_tables[size_t(first) * max_blocks + j])
+      dev::flag_status(status, kStatusBounds);
+    sfx_tables[size_t(b) * max_blocks + j] = j + nb < max_blocks ? row[j + nb] : -1;
   }
 }
 
@@ -1508,6 +1571,23 @@ SharedLayout shared_layout(int num_seqs, int num_q_heads, int num_kv_heads, int 
   l.total = align256(l.slse + rows * 4);
   return l;
 }
+
+// The grouped cascade adds, per sequence, the table past its group's prefix,
+// the context past it and the prefix's block count (written once per step).
+struct GroupedLayout {
+  SharedLayout sh;
+  size_t sfx_tables, sfx_ctx, seq_blocks, total;
+};
+GroupedLayout grouped_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int max_blocks_per_seq) {
+  GroupedLayout l;
+  l.sh = shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  l.sfx_tables = l.sh.total;
+  l.sfx_ctx = align256(l.sfx_tables + size_t(num_seqs) * max_blocks_per_seq * 4);
+  l.seq_blocks = align256(l.sfx_ctx + size_t(num_seqs) * 4);
+  l.total = align256(l.seq_blocks + size_t(num_seqs) * 4);
+  return l;
+}
 }  // namespace
 
 extern "C" {
@@ -1614,18 +1694,132 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
     e = head_dim == 128
             ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, po, plse, parts, so,
                                  slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
-                                 prefix_blocks, num_seqs, max_blocks_per_seq, status)
+                                 prefix_blocks, num_seqs, max_blocks_per_seq, status,
+                                 nullptr, nullptr, num_q_heads)
             : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, po, plse, parts, so,
                                  slse, static_cast<__nv_bfloat16*>(out), rows, block_tables,
-                                 prefix_blocks, num_seqs, max_blocks_per_seq, status);
+                                 prefix_blocks, num_seqs, max_blocks_per_seq, status,
+                                 nullptr, nullptr, num_q_heads);
   else
     e = head_dim == 128
             ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 128>, po, plse, parts, so, slse,
                                  static_cast<__half*>(out), rows, block_tables, prefix_blocks,
-                                 num_seqs, max_blocks_per_seq, status)
+                                 num_seqs, max_blocks_per_seq, status, nullptr, nullptr,
+                                 num_q_heads)
             : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 64>, po, plse, parts, so, slse,
                                  static_cast<__half*>(out), rows, block_tables, prefix_blocks,
-                                 num_seqs, max_blocks_per_seq, status);
+                                 num_seqs, max_blocks_per_seq, status, nullptr, nullptr,
+                                 num_q_heads);
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
+}
+
+// The grouped cascade: plan (once per step) = the suffix tables and lengths,
+// the prefix phase's plan over the groups, the suffix decode's plan; run (per
+// layer) = the prefix phase, the suffix decode, the combine.
+int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, const int32_t* context_lens,
+                        const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out,
+                        void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               dtype, who);
+  if (rc != PA_OK || num_seqs == 0) return rc;
+  if (dtype == PA_F32)
+    return fail(PA_ERR_UNSUPPORTED, "%s: 16-bit dtypes only (fp32 decodes exactly without it)", who);
+  if (num_groups < 1 || num_groups > num_seqs)
+    return fail(PA_ERR_INVALID_ARG, "%s: num_groups outside 1..num_seqs", who);
+  const GroupedLayout gl =
+      grouped_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  const SharedLayout& sl = gl.sh;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < gl.total)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace NULL, unaligned or < %zu bytes", who, gl.total);
+  if (!group_start || !group_blocks) return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
+  if (plans && (!context_lens || !block_tables))
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* po = reinterpret_cast<float*>(ws + sl.po);
+  float* plse = reinterpret_cast<float*>(ws + sl.plse);
+  float* so = reinterpret_cast<float*>(ws + sl.so);
+  float* slse = reinterpret_cast<float*>(ws + sl.slse);
+  int32_t* sfx_tables = reinterpret_cast<int32_t*>(ws + gl.sfx_tables);
+  int32_t* sfx_ctx = reinterpret_cast<int32_t*>(ws + gl.sfx_ctx);
+  int32_t* seq_blocks = reinterpret_cast<int32_t*>(ws + gl.seq_blocks);
+  SuffixArgs sfx;  // no offsets: the suffix decode reads the suffix tables
+  sfx.cas_o = so;
+  sfx.cas_lse = slse;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (plans) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_seqs);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_suffix_kernel, block_tables, context_lens,
+                                       group_start, group_blocks, num_groups, num_seqs,
+                                       max_blocks_per_seq, sfx_tables, sfx_ctx, seq_blocks, status);
+    if (e != cudaSuccess)
+      return fail(PA_ERR_CUDA, "%s: suffix-table launch failed: %s", who, cudaGetErrorString(e));
+    rc = prefill::grouped_prefix_plan(group_start, group_blocks, num_groups, num_seqs, num_q_heads,
+                                      num_kv_heads, head_dim, max_blocks_per_seq, scale, dtype,
+                                      ws + sl.prefix, sl.po - sl.prefix, s);
+    if (rc != PA_OK) return rc;
+    rc = plan_impl(sfx_ctx, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                   workspace, sl.prefix, s, who, sfx);
+    if (rc != PA_OK) return rc;
+  }
+  if (!runs) return PA_OK;
+  // 1. every group's prefix, read once for the group's queries
+  rc = prefill::grouped_prefix_run(q, k_cache, v_cache, block_tables, group_start, group_blocks,
+                                   num_groups, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                   max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
+                                   ws + sl.prefix, sl.po - sl.prefix, s);
+  if (rc != PA_OK) return rc;
+  // 2. every sequence's own blocks
+  rc = run_impl(q, k_cache, v_cache, sfx_tables, sfx_ctx, num_seqs, num_q_heads, num_kv_heads,
+                head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out, workspace, sl.prefix,
+                s, who, AppendArgs(), sfx);
+  if (rc != PA_OK) return rc;
+  // 3. merge, each row with its own group's parts
+  const int* parts = prefill::shared_prefix_split_count(ws + sl.prefix);
+  const int* split = prefill::shared_prefix_split_blocks(ws + sl.prefix);
+  const int rows = num_seqs * num_q_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (dtype == PA_BF16)
+    e = head_dim == 128
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 128>, po, plse, parts,
+                                 so, slse, static_cast<__nv_bfloat16*>(out), rows, block_tables, 0,
+                                 num_seqs, max_blocks_per_seq, status, seq_blocks, split,
+                                 num_q_heads)
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__nv_bfloat16, 64>, po, plse, parts,
+                                 so, slse, static_cast<__nv_bfloat16*>(out), rows, block_tables, 0,
+                                 num_seqs, max_blocks_per_seq, status, seq_blocks, split,
+                                 num_q_heads);
+  else
+    e = head_dim == 128
+            ? cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 128>, po, plse, parts, so,
+                                 slse, static_cast<__half*>(out), rows, block_tables, 0, num_seqs,
+                                 max_blocks_per_seq, status, seq_blocks, split, num_q_heads)
+            : cudaLaunchKernelEx(&cfg, cascade_combine_kernel<__half, 64>, po, plse, parts, so,
+                                 slse, static_cast<__half*>(out), rows, block_tables, 0, num_seqs,
+                                 max_blocks_per_seq, status, seq_blocks, split, num_q_heads);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
 }
@@ -1666,6 +1860,54 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
                             head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
                             workspace, workspace_bytes, stream,
                             "paged_attention_decode_shared_prefix_run");
+}
+
+PA_API int pa_paged_attention_decode_grouped_prefix_workspace_size(
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+    size_t* bytes) {
+  int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                               PA_BF16, "paged_attention_decode_grouped_prefix_workspace_size");
+  if (rc != PA_OK) return rc;
+  if (!bytes) return fail(PA_ERR_INVALID_ARG, "grouped_prefix_workspace_size: bytes is NULL");
+  *bytes = grouped_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
+  return PA_OK;
+}
+
+PA_API int pa_paged_attention_decode_grouped_prefix(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* context_lens, const int32_t* group_start, const int32_t* group_prefix_blocks,
+    int num_groups, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  return grouped_prefix_impl(SharedMode::kPlanAndRun, q, k_cache, v_cache, block_tables,
+                             context_lens, group_start, group_prefix_blocks, num_groups, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
+                             scale, dtype, out, workspace, workspace_bytes, stream,
+                             "paged_attention_decode_grouped_prefix");
+}
+
+PA_API int pa_paged_attention_decode_grouped_prefix_plan(
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  return grouped_prefix_impl(SharedMode::kPlanOnly, nullptr, nullptr, nullptr, block_tables,
+                             context_lens, group_start, group_prefix_blocks, num_groups, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0, scale,
+                             dtype, nullptr, workspace, workspace_bytes, stream,
+                             "paged_attention_decode_grouped_prefix_plan");
+}
+
+PA_API int pa_paged_attention_decode_grouped_prefix_run(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    const int32_t* group_start, const int32_t* group_prefix_blocks, int num_groups, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+    float scale, int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  return grouped_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables, nullptr,
+                             group_start, group_prefix_blocks, num_groups, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
+                             out, workspace, workspace_bytes, stream,
+                             "paged_attention_decode_grouped_prefix_run");
 }
 
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -70,8 +70,10 @@ __host__ __device__ __forceinline__ int nsplits_of(int nb, int split) {
 // Workspace header words.
 constexpr int kHdrNext = 0, kHdrTotal = 1, kHdrDone = 2, kHdrSignature = 3;
 // shared-prefix mode: how many (o, lse) parts per row the phase left in
-// cas_o / cas_lse for the caller to merge (1 when it merged them itself)
-constexpr int kHdrSplits = 4;
+// cas_o / cas_lse for the caller to merge (1 when it merged them itself);
+// the split size in blocks behind it (0: none, or merged in-kernel), from
+// which the caller works out each group's count in grouped mode
+constexpr int kHdrSplits = 4, kHdrSplitBlocks = 5;
 
 struct Params {
   const void* q;
@@ -93,6 +95,12 @@ struct Params {
   // attends all of them (no causal mask), and the results go to cas_o /
   // cas_lse (fp32 o and base-2 log-sum-exp per (row, head)) instead of out.
   int shared_ctx;
+  // Grouped shared-prefix mode (shared_blocks non-null): num_seqs groups of
+  // decode queries, group g the rows query_start[g] .. query_start[g + 1] - 1
+  // (one per sequence, so the group's first member has table row
+  // query_start[g]), attending the group's own prefix of shared_blocks[g]
+  // blocks (no causal mask); results as in shared-prefix mode.
+  const int32_t* shared_blocks;
   int no_split;      // plan: never split a unit's KV range (tcgen05 kernel)
   // shared-prefix mode on the tcgen05 kernel: split s of every row writes its
   // own (o, lse) to slot s of cas_o / cas_lse ([kSharedMaxSplits][rows]...);
@@ -168,7 +176,7 @@ constexpr int kPlanThreads = 256;
 template <int ROWS>
 __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params p) {
   __shared__ unsigned long long s_blocks;
-  __shared__ int s_qblocks, s_split_units, s_split, s_slot, s_group;
+  __shared__ int s_qblocks, s_split_units, s_split, s_slot, s_group, s_maxnb;
   __shared__ int hist[kSizeBuckets];
   __shared__ int bucket[kSizeBuckets];
   dev::grid_launch_dependents();
@@ -181,13 +189,26 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     s_qblocks = 0;
     s_slot = 0;
     s_group = 0;
+    s_maxnb = 0;
   }
   if (tid < kSizeBuckets) hist[tid] = 0;
   __syncthreads();
 
   // a sequence's chunk: (ctx, qlen), or qlen = 0 when its lengths are invalid
-  const bool shared = p.shared_ctx > 0;
+  const bool shared = p.shared_ctx > 0 || p.shared_blocks;
   auto chunk = [&](int b, int& ctx, int& qlen) {
+    if (p.shared_blocks) {  // group b: its rows over its own prefix
+      const int nb = p.shared_blocks[b];
+      const int q0 = p.query_start[b], q1 = p.query_start[b + 1];
+      ctx = nb * kBlockSize;
+      qlen = q1 - q0;
+      if (nb < 0 || ctx > cap || qlen < 0 || q0 < 0 || q1 > p.total_q) {
+        dev::flag_status(p.status, kStatusBounds);
+        qlen = 0;
+      }
+      if (ctx <= 0) qlen = 0;
+      return;
+    }
     if (shared) {
       ctx = p.shared_ctx <= cap ? p.shared_ctx : 0;
       qlen = ctx > 0 ? p.total_q : 0;
@@ -212,6 +233,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     if (nq) {
       atomicAdd(&s_qblocks, nq);
       atomicAdd(&s_blocks, blocks);
+      if (shared) atomicMax(&s_maxnb, (ctx + kBlockSize - 1) / kBlockSize);
     }
   }
   __syncthreads();
@@ -231,6 +253,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       p.header[kHdrNext] = 0;
       p.header[kHdrDone] = 0;
       p.header[kHdrSplits] = 1;
+      p.header[kHdrSplitBlocks] = 0;
       p.header[kHdrSignature] = p.signature;
     }
     return;
@@ -242,11 +265,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       const long long want = (long long)s_blocks * p.num_kv_heads / (3ll * p.ncta) + 1;
       // the shared-prefix phase has few, short rows: allow shorter splits
       split = int(std::max<long long>(shared ? kMinSplitBlocks / 2 : kMinSplitBlocks, want));
-      // parts left for the caller: at most kSharedMaxSplits per row
-      if (p.defer_merge) {
-        const int nb = (p.shared_ctx + kBlockSize - 1) / kBlockSize;
-        split = std::max(split, (nb + kSharedMaxSplits - 1) / kSharedMaxSplits);
-      }
+      // parts left for the caller: at most kSharedMaxSplits per row (the
+      // longest prefix decides)
+      if (p.defer_merge) split = std::max(split, (s_maxnb + kSharedMaxSplits - 1) / kSharedMaxSplits);
     }
     s_split = split;
   }
@@ -300,10 +321,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     p.header[kHdrTotal] = pos * p.num_kv_heads;
     p.header[kHdrNext] = 0;
     p.header[kHdrDone] = 0;
-    p.header[kHdrSplits] =
-        p.defer_merge && shared
-            ? nsplits_of((p.shared_ctx + kBlockSize - 1) / kBlockSize, split)
-            : 1;
+    p.header[kHdrSplits] = p.defer_merge && shared ? nsplits_of(s_maxnb, split) : 1;
+    p.header[kHdrSplitBlocks] = p.defer_merge && shared ? split : 0;
     p.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
@@ -387,7 +406,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 
   const unsigned long long tmo = p.timeout_ns;
   const int G = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
-  const bool shared = p.shared_ctx > 0;
+  const bool shared = p.shared_ctx > 0 || p.shared_blocks;
   const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
@@ -406,7 +425,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     if ((j & ~31) != tbl_base) {
       tbl_base = j & ~31;
       tbl = tbl_base + lane < it.nblk
-                ? p.block_tables[size_t(it.b) * p.max_blocks + it.first + tbl_base + lane]
+                ? p.block_tables[size_t(shared ? it.q_first : it.b) * p.max_blocks + it.first +
+                                 tbl_base + lane]
                 : 0;
       if (tbl < 0 || tbl >= p.num_blocks) {
         dev::flag_status(p.status, kStatusBounds);
@@ -460,8 +480,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       it.slot = u1.y;
       it.grp = u1.z;
       it.ctx = u1.w;
-      it.q_first = shared ? 0 : p.query_start[it.b];
-      it.qlen = shared ? p.total_q : p.query_start[it.b + 1] - it.q_first;
+      // shared-prefix mode: the batch's queries are the rows of one sequence
+      // (grouped: the group's rows)
+      const bool starts = !shared || p.shared_blocks;
+      it.q_first = starts ? p.query_start[it.b] : 0;
+      it.qlen = starts ? p.query_start[it.b + 1] - it.q_first : p.total_q;
     }
     // the ring's first blocks of this item
     tbl_base = -32;
@@ -885,7 +908,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool planned = *reinterpret_cast<volatile int*>(&p.header[kHdrSignature]) == p.signature;
   if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.header[kHdrTotal]) : 0;
-  const bool shared = p.shared_ctx > 0;
+  const bool shared = p.shared_ctx > 0 || p.shared_blocks;
   bool ok = true;
   PF_STAMP(1);
 
@@ -908,8 +931,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     it.grp = u1.z;
     it.ctx = u1.w;
     // shared-prefix mode: the batch's queries are the rows of one sequence
-    it.q_first = shared ? 0 : p.query_start[it.b];
-    it.qlen = shared ? p.total_q : p.query_start[it.b + 1] - it.q_first;
+    // (grouped: the group's rows)
+    const bool starts = !shared || p.shared_blocks;
+    it.q_first = starts ? p.query_start[it.b] : 0;
+    it.qlen = starts ? p.query_start[it.b + 1] - it.q_first : p.total_q;
     it.ntiles = (it.nblk + kTcBlocks - 1) / kTcBlocks;
     it.two = it.qt * kTcItemRows + kTcRows < it.qlen * G;
     return it;
@@ -966,7 +991,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if ((j * kTcBlocks & ~31) != tbl_base) {
           tbl_base = j * kTcBlocks & ~31;
           tbl = tbl_base + lane < it.nblk
-                    ? p.block_tables[size_t(it.b) * p.max_blocks + it.first + tbl_base + lane]
+                    ? p.block_tables[size_t(shared ? it.q_first : it.b) * p.max_blocks + it.first +
+                                 tbl_base + lane]
                     : 0;
           if (tbl < 0 || tbl >= p.num_blocks) {
             dev::flag_status(p.status, kStatusBounds);
@@ -1746,13 +1772,14 @@ bool prepare(Params& prm, const Layout& lay, int device, int dtype, void* worksp
   prm.ncta = use_tc ? st.sms : st.sms * per_sm;
   // the tcgen05 kernel merges its splits itself, except in the shared-prefix
   // phase, whose parts the cascade combine merges
-  prm.defer_merge = use_tc && prm.shared_ctx > 0 ? 1 : 0;
+  prm.defer_merge = use_tc && (prm.shared_ctx > 0 || prm.shared_blocks) ? 1 : 0;
   prm.no_split = 0;
   prm.units_cap = lay.units_cap;
   prm.partial_cap = lay.partial_cap;
   prm.signature = signature_of(prm.num_seqs, prm.total_q, prm.num_q_heads, prm.num_kv_heads,
                                prm.head_dim, prm.max_blocks) ^
-                  (prm.shared_ctx << 1) ^ (use_tc ? 0x2A000000 : 0);
+                  (prm.shared_ctx << 1) ^ (use_tc ? 0x2A000000 : 0) ^
+                  (prm.shared_blocks ? 0x15000000 : 0);
   prm.header = reinterpret_cast<int*>(ws + lay.header);
   prm.units = reinterpret_cast<int4*>(ws + lay.units);
   prm.arrivals = reinterpret_cast<int*>(ws + lay.arrivals);
@@ -1833,9 +1860,13 @@ const int* shared_prefix_split_count(const void* workspace) {
   return static_cast<const int*>(workspace) + kHdrSplits;  // the header is at offset 0
 }
 
+const int* shared_prefix_split_blocks(const void* workspace) {
+  return static_cast<const int*>(workspace) + kHdrSplitBlocks;
+}
+
 size_t shared_prefix_workspace_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                      int head_dim) {
-  return workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim).total;
+  return workspace_layout(num_seqs, num_seqs, num_q_heads, num_kv_heads, head_dim).total;
 }
 
 namespace {
@@ -1847,7 +1878,9 @@ int shared_params(Params& prm, Layout& lay, int& device, const void* q, const vo
                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                   int max_blocks_per_seq, int num_blocks, float scale, float* cas_o,
                   float* cas_lse, size_t workspace_bytes, const char* who) {
-  lay = workspace_layout(1, num_seqs, num_q_heads, num_kv_heads, head_dim);
+  // sized for up to num_seqs groups (one group in the single-prefix mode),
+  // so both modes share one layout
+  lay = workspace_layout(num_seqs, num_seqs, num_q_heads, num_kv_heads, head_dim);
   if (workspace_bytes < lay.total) return fail(PA_ERR_INVALID_ARG, "%s: workspace too small", who);
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
     return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
@@ -1908,6 +1941,46 @@ int shared_prefix_run(const void* q, const void* k_cache, const void* v_cache,
                          num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                          num_blocks, scale, cas_o, cas_lse, workspace_bytes, who);
   if (rc != PA_OK) return rc;
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  return launch_attention(prm, use_tc, dtype, stream, who);
+}
+
+int grouped_prefix_plan(const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int max_blocks_per_seq, float scale, int dtype, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  const char* who = "paged_attention_decode_grouped_prefix (prefix plan)";
+  Params prm;
+  Layout lay;
+  int device = 0;
+  int rc = shared_params(prm, lay, device, nullptr, nullptr, nullptr, nullptr, 0, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0, scale,
+                         nullptr, nullptr, workspace_bytes, who);
+  if (rc != PA_OK) return rc;
+  prm.num_seqs = num_groups;
+  prm.query_start = group_start;
+  prm.shared_blocks = group_blocks;
+  const bool use_tc = prepare(prm, lay, device, dtype, workspace);
+  return launch_plan(prm, use_tc, stream, who);
+}
+
+int grouped_prefix_run(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* group_start,
+                       const int32_t* group_blocks, int num_groups, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
+                       float scale, int dtype, float* cas_o, float* cas_lse, void* workspace,
+                       size_t workspace_bytes, cudaStream_t stream) {
+  const char* who = "paged_attention_decode_grouped_prefix (prefix)";
+  Params prm;
+  Layout lay;
+  int device = 0;
+  int rc = shared_params(prm, lay, device, q, k_cache, v_cache, block_tables, 0, num_seqs,
+                         num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
+                         scale, cas_o, cas_lse, workspace_bytes, who);
+  if (rc != PA_OK) return rc;
+  prm.num_seqs = num_groups;
+  prm.query_start = group_start;
+  prm.shared_blocks = group_blocks;
   const bool use_tc = prepare(prm, lay, device, dtype, workspace);
   return launch_attention(prm, use_tc, dtype, stream, who);
 }

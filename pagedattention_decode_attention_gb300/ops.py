@@ -74,11 +74,15 @@ def kv_append(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: 
 
 
 def _decode_args(q, k_cache, v_cache, block_tables, context_lens):
+    """Checks the decode operands (context_lens None: not passed) and returns
+    (device, num_seqs, Hq, Hkv, d, num_blocks, max_blocks_per_seq)."""
     dev = q.device
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
                     ("block_tables", block_tables), ("context_lens", context_lens)):
-        _cuda_contig(name, t, dev)
-    _require(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+        if t is not None:
+            _cuda_contig(name, t, dev)
+    _require(block_tables.dtype == torch.int32 and
+             (context_lens is None or context_lens.dtype == torch.int32),
              "block_tables and context_lens must be int32")
     _require(q.dtype == k_cache.dtype == v_cache.dtype, "q and caches must share a dtype")
     _require(k_cache.dim() == 4 and k_cache.shape == v_cache.shape and k_cache.shape[2] == 16,
@@ -88,7 +92,7 @@ def _decode_args(q, k_cache, v_cache, block_tables, context_lens):
     b, hq, _ = q.shape
     _require(block_tables.dim() == 2 and block_tables.shape[0] == b,
              "block_tables must be [num_seqs, max_blocks_per_seq]")
-    _require(context_lens.shape == (b,), "context_lens must be [num_seqs]")
+    _require(context_lens is None or context_lens.shape == (b,), "context_lens must be [num_seqs]")
     return dev, b, hq, hkv, d, nb, block_tables.shape[1]
 
 
@@ -326,6 +330,96 @@ def paged_attention_decode_shared_prefix(q, k_cache, v_cache, block_tables, cont
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
         context_lens.data_ptr(), int(prefix_blocks), b, hq, hkv, d, mb, nb, float(scale),
         _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return out
+
+
+def grouped_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                                  head_dim: int, max_blocks_per_seq: int) -> int:
+    n = C.c_size_t(0)
+    capi.check(capi.lib().pa_paged_attention_decode_grouped_prefix_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, C.byref(n)))
+    return n.value
+
+
+def _group_args(group_start, group_prefix_blocks, num_seqs, dev):
+    for name, t in (("group_start", group_start), ("group_prefix_blocks", group_prefix_blocks)):
+        _cuda_contig(name, t, dev)
+        _require(t.dtype == torch.int32 and t.dim() == 1, f"{name} must be int32 [n]")
+    g = group_prefix_blocks.shape[0]
+    _require(group_start.shape[0] == g + 1, "group_start must have num_groups + 1 entries")
+    _require(1 <= g <= num_seqs, "num_groups must be 1 .. num_seqs")
+    return g
+
+
+def grouped_prefix_plan(block_tables: torch.Tensor, context_lens: torch.Tensor,
+                        group_start: torch.Tensor, group_prefix_blocks: torch.Tensor,
+                        num_q_heads: int, num_kv_heads: int, head_dim: int, scale: float,
+                        dtype: torch.dtype, workspace: torch.Tensor, stream=None) -> None:
+    """Once per decode step: every sequence's table past its group's prefix
+    and the work lists of a grouped shared-prefix (cascade) decode, into
+    ``workspace``; one plan serves every
+    :func:`paged_attention_decode_grouped_prefix_run` of the step."""
+    dev = context_lens.device
+    for name, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                    ("workspace", workspace)):
+        _cuda_contig(name, t, dev)
+    _require(block_tables.dtype == torch.int32 and context_lens.dtype == torch.int32,
+             "block_tables and context_lens must be int32")
+    _require(block_tables.dim() == 2 and block_tables.shape[0] == context_lens.shape[0],
+             "block_tables must be [num_seqs, max_blocks_per_seq]")
+    b = context_lens.shape[0]
+    g = _group_args(group_start, group_prefix_blocks, b, dev)
+    _require(dtype in _DTYPES, "dtype must be float32, float16 or bfloat16")
+    capi.check(capi.lib().pa_paged_attention_decode_grouped_prefix_plan(
+        block_tables.data_ptr(), context_lens.data_ptr(), group_start.data_ptr(),
+        group_prefix_blocks.data_ptr(), g, b, int(num_q_heads), int(num_kv_heads), int(head_dim),
+        block_tables.shape[1], float(scale), _DTYPES[dtype], workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+
+
+def paged_attention_decode_grouped_prefix_run(q, k_cache, v_cache, block_tables, group_start,
+                                              group_prefix_blocks, scale: float, workspace,
+                                              out=None, stream=None) -> torch.Tensor:
+    """Per layer, over a workspace :func:`grouped_prefix_plan` filled: every
+    group's prefix read once for its queries, each sequence's own blocks,
+    then the merge."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, None)
+    g = _group_args(group_start, group_prefix_blocks, b, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_grouped_prefix_run(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        group_start.data_ptr(), group_prefix_blocks.data_ptr(), g, b, hq, hkv, d, mb, nb,
+        float(scale), _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return out
+
+
+def paged_attention_decode_grouped_prefix(q, k_cache, v_cache, block_tables, context_lens,
+                                          group_start, group_prefix_blocks, scale: float,
+                                          out=None, workspace=None, stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode` for a batch of groups of sequences, each
+    group's tables starting with the same ``group_prefix_blocks[g]`` blocks
+    (group g: sequences ``group_start[g] .. group_start[g + 1] - 1``): each
+    group's shared blocks are read once for the group's queries."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    g = _group_args(group_start, group_prefix_blocks, b, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    if workspace is None:
+        n = grouped_prefix_workspace_size(b, hq, hkv, d, mb)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=dev)
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_grouped_prefix(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        context_lens.data_ptr(), group_start.data_ptr(), group_prefix_blocks.data_ptr(), g, b,
+        hq, hkv, d, mb, nb, float(scale), _dtype_code(q), out.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(dev, stream)))
     return out
 
