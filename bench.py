@@ -73,7 +73,8 @@ def parse_args():
     ap.add_argument("--warmup-seconds", type=float, default=1.0,
                     help="keep warming up until this much wall time has passed")
     ap.add_argument("--cascade", action="store_true",
-                    help="prefix_8b: time the shared-prefix (cascade) decode against the plain one")
+                    help="prefix_8b / sampling_8b: time the (grouped) shared-prefix decode "
+                         "against the plain one")
     return ap.parse_args()
 
 
@@ -126,8 +127,20 @@ def sampling_batch(script, model_pool: bool = False) -> wl.DecodeBatch:
     pool = make_pool(script, model_pool)
     branches, _ = cow_divergence(pool, script)
     tables, lens = pool_tables(pool, branches)
+    # each prompt's branches are one group: contiguous, sharing the prompt's
+    # whole blocks (the leading table entries all members agree on)
+    starts = np.arange(0, len(branches) + 1, script.branches, dtype=np.int32)
+    shared = []
+    for a, b in zip(starts[:-1], starts[1:]):
+        rows = tables[a:b]
+        n = 0
+        while n < rows.shape[1] and rows[0, n] >= 0 and (rows[:, n] == rows[0, n]).all():
+            n += 1
+        shared.append(n)
     return wl.DecodeBatch("sampling_8b_bf16", 32, 8, 128, "bf16", lens, tables, script.num_blocks,
-                          num_layers=8, seed=script.seed)
+                          num_layers=8, seed=script.seed,
+                          extra={"group_start": starts,
+                                 "group_blocks": np.array(shared, dtype=np.int32)})
 
 
 def prefix_batch(script, model_pool: bool = False) -> wl.DecodeBatch:
@@ -869,34 +882,51 @@ def run_ours(args):
 
 # ---------------------------------------------------------------- reference
 def run_cascade_bench(args):
-    """Shared-prefix (cascade) decode on the prefix-mix batch, beside the
-    plain decode of the same batch.  Both run as a model step would: one plan
-    from the lengths, then per layer the new tokens' K/V appended and
-    attention over the whole context (the plain path fuses the two into one
-    launch; the cascade path appends, then runs its prefix phase, suffix
-    decode and combine)."""
+    """Shared-prefix (cascade) decode beside the plain decode of the same
+    batch: the prefix-mix batch (one prefix for the whole batch) or the
+    parallel-sampling batch (grouped: each prompt's branches share their
+    prompt).  Both run as a model step would: one plan, then per layer the
+    new tokens' K/V appended and attention over the whole context (the plain
+    path fuses the two into one launch; the cascade path appends, then runs
+    its prefix phase, suffix decode and combine)."""
     import pagedattention_decode_attention_gb300 as pa
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    batch = make_batch("prefix_8b", 0)
+    batch = make_batch(args.workload, 0)
     if args.layers > 0:
         batch.num_layers = args.layers
     rep = Replica(batch, device)
-    L, P = batch.num_layers, batch.extra["prefix_blocks"]
+    grouped = "group_start" in batch.extra
+    L = batch.num_layers
     hq, hkv, d, mb = batch.num_q_heads, batch.num_kv_heads, batch.head_dim, batch.max_blocks
     dt = DTYPES[batch.dtype]
-    ws = torch.empty(max(pa.shared_prefix_workspace_size(batch.num_seqs, hq, hkv, d, mb), 256),
-                     dtype=torch.uint8, device=device)
+    size = (pa.grouped_prefix_workspace_size if grouped else pa.shared_prefix_workspace_size)(
+        batch.num_seqs, hq, hkv, d, mb)
+    ws = torch.empty(max(size, 256), dtype=torch.uint8, device=device)
     appends = [pa.prepare_kv_append(rep.k_new[i], rep.v_new[i], rep.k_cache[i], rep.v_cache[i],
                                     rep.slots) for i in range(L)]
+    if grouped:
+        gs = torch.from_numpy(batch.extra["group_start"]).to(device)
+        gb = torch.from_numpy(batch.extra["group_blocks"]).to(device)
+        P = int(batch.extra["group_blocks"].min())
 
-    def cascade_step():
-        pa.shared_prefix_plan(rep.lens, P, hq, hkv, d, mb, batch.scale, dt, ws)
-        for i in range(L):
-            appends[i]()
-            pa.paged_attention_decode_shared_prefix_run(rep.q[i], rep.k_cache[i], rep.v_cache[i],
-                                                        rep.tables, rep.lens, P, batch.scale, ws,
-                                                        out=rep.out[i])
+        def cascade_step():
+            pa.grouped_prefix_plan(rep.tables, rep.lens, gs, gb, hq, hkv, d, batch.scale, dt, ws)
+            for i in range(L):
+                appends[i]()
+                pa.paged_attention_decode_grouped_prefix_run(rep.q[i], rep.k_cache[i],
+                                                             rep.v_cache[i], rep.tables, gs, gb,
+                                                             batch.scale, ws, out=rep.out[i])
+    else:
+        P = batch.extra["prefix_blocks"]
+
+        def cascade_step():
+            pa.shared_prefix_plan(rep.lens, P, hq, hkv, d, mb, batch.scale, dt, ws)
+            for i in range(L):
+                appends[i]()
+                pa.paged_attention_decode_shared_prefix_run(rep.q[i], rep.k_cache[i],
+                                                            rep.v_cache[i], rep.tables, rep.lens,
+                                                            P, batch.scale, ws, out=rep.out[i])
 
     def timed(step):
         for _ in range(max(args.warmup, 3)):
@@ -924,13 +954,15 @@ def run_cascade_bench(args):
     qo = 2 * batch.num_seqs * hq * d * ELEM[batch.dtype]
     uniq = unique_kv_bytes(batch) + qo
     line = {
-        "metric": "decode tokens/s, shared-prefix (cascade) path, 1 GPU",
+        "metric": ("decode tokens/s, grouped shared-prefix (cascade) path, 1 GPU" if grouped
+                   else "decode tokens/s, shared-prefix (cascade) path, 1 GPU"),
         "value": batch.num_seqs / cascade_s, "unit": "tokens/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": cascade_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
-        "data": "synthetic (seeded N(0,1) Q/K/V; prefix-mix lengths and pool tables)",
+        "data": "synthetic (seeded N(0,1) Q/K/V; seeded lengths and pool tables)",
         "config": {"workload": batch.name, "num_seqs": batch.num_seqs, "layers": L,
                    "prefix_blocks": P, "context_tokens": int(batch.context_lens.sum()),
+                   "groups": len(batch.extra["group_start"]) - 1 if grouped else 1,
                    "step": "one plan, then per layer: append the new tokens' K/V and attend"},
         "roofline": {"bound": "hbm", "achieved": uniq / (cascade_s / L) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": uniq / (cascade_s / L) / 1e9 / peak,
@@ -942,7 +974,7 @@ def run_cascade_bench(args):
         "plain_us_per_layer": plain_s / L * 1e6,
         "plain_value": batch.num_seqs / plain_s,
         "max_abs_diff_vs_plain": diff,
-        "gpu_launches": args.steps * (2 + 4 * L),
+        "gpu_launches": args.steps * ((3 if grouped else 2) + 4 * L),
         "clocks": clk,
     }
     print(json.dumps(line))
@@ -1438,7 +1470,7 @@ def main():
         run_reference(args)
     elif args.workload == "prefill_8b":
         run_prefill_bench(args)
-    elif args.workload == "prefix_8b" and args.cascade:
+    elif args.workload in ("prefix_8b", "sampling_8b") and args.cascade:
         run_cascade_bench(args)
     elif args.workload == "swap_8b":
         run_swap_bench(args)

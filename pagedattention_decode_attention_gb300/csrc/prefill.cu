@@ -869,6 +869,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* part_full = bars + 23;
   uint64_t* merge_go = bars + 24;
   int* s_merge = reinterpret_cast<int*>(bars + 25);
+  // [2] an item with one query tile alternates its S between the two S
+  // buffers (group 1 has no rows then): S of buffer b is in TMEM
+  uint64_t* sb_full = bars + 26;
   const uint32_t sbase = dev::smem_u32(smem);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -890,6 +893,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dev::mbar_init(drain, 1);
     dev::mbar_init(part_full, 8);
     dev::mbar_init(merge_go, 1);
+    dev::mbar_init(&sb_full[0], 1);
+    dev::mbar_init(&sb_full[1], 1);
     dev::mbar_fence_init();
     dev::prefetch_tensormap(&tmap_q);
     dev::prefetch_tensormap(&tmap_k);
@@ -1080,11 +1085,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         dev::tc_commit_leader(&s_full[w], leader);
         return true;
       };
-      auto issue_pv = [&](int w, int j, int st) -> bool {
+      // O_w += P V, P read from S buffer `buf` (w, or the alternating buffer
+      // of a one-tile item)
+      auto issue_pv = [&](int w, int j, int st, int buf) -> bool {
         if (!PF_WAIT(4, wait(&p_full[w], pv[w] & 1))) return false;
         dev::tc_fence_after_sync();
         const uint64_t bv = desc_v + uint64_t((st * 2 * TcSmem::kChunk) >> 4);
-        const uint32_t d = tmem + 256 + w * 128, pa = tmem + w * 128;
+        const uint32_t d = tmem + 256 + w * 128, pa = tmem + buf * 128;
         dev::tc_mma_ts_leader(d, pa, bv, idesc_o, uint32_t(j), leader);
 #pragma unroll
         for (int kk = 1; kk < kTcTokens / 16; ++kk)
@@ -1093,28 +1100,76 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ++pv[w];
         return true;
       };
-      // prologue: S of the first tile for both query tiles
-      if (ok) ok = PF_WAIT(2, wait(&k_full[kt & 1], (kt >> 1) & 1));
-      for (int w = 0; w < tiles && ok; ++w) ok = issue_s(w, kt & 1);
-      if (ok) {
-        dev::tc_commit_leader(&k_empty[kt & 1], leader);
-        if (it.ntiles == 1) dev::tc_commit_leader(q_empty, leader);
-      }
-      for (int j = 0; j < it.ntiles && ok; ++j) {
-        const int st = (kt + j) & 1, nst = (kt + j + 1) & 1;
-        const bool more = j + 1 < it.ntiles;
-        ok = PF_WAIT(3, wait(&v_full[st], ((kt + j) >> 1) & 1));
-        if (ok) ok = issue_pv(0, j, st);
-        if (ok && more) {
-          ok = PF_WAIT(2, wait(&k_full[nst], ((kt + j + 1) >> 1) & 1));
-          if (ok) ok = issue_s(0, nst);
+      if (tiles == 2) {
+        // prologue: S of the first tile for both query tiles
+        if (ok) ok = PF_WAIT(2, wait(&k_full[kt & 1], (kt >> 1) & 1));
+        for (int w = 0; w < tiles && ok; ++w) ok = issue_s(w, kt & 1);
+        if (ok) {
+          dev::tc_commit_leader(&k_empty[kt & 1], leader);
+          if (it.ntiles == 1) dev::tc_commit_leader(q_empty, leader);
         }
-        if (ok && tiles == 2) ok = issue_pv(1, j, st);
-        if (ok) dev::tc_commit_leader(&v_empty[st], leader);
-        if (ok && more && tiles == 2) ok = issue_s(1, nst);
-        if (ok && more) {
-          dev::tc_commit_leader(&k_empty[nst], leader);
-          if (j + 2 == it.ntiles) dev::tc_commit_leader(q_empty, leader);
+        for (int j = 0; j < it.ntiles && ok; ++j) {
+          const int st = (kt + j) & 1, nst = (kt + j + 1) & 1;
+          const bool more = j + 1 < it.ntiles;
+          ok = PF_WAIT(3, wait(&v_full[st], ((kt + j) >> 1) & 1));
+          if (ok) ok = issue_pv(0, j, st, 0);
+          if (ok && more) {
+            ok = PF_WAIT(2, wait(&k_full[nst], ((kt + j + 1) >> 1) & 1));
+            if (ok) ok = issue_s(0, nst);
+          }
+          if (ok) ok = issue_pv(1, j, st, 1);
+          if (ok) dev::tc_commit_leader(&v_empty[st], leader);
+          if (ok && more) ok = issue_s(1, nst);
+          if (ok && more) {
+            dev::tc_commit_leader(&k_empty[nst], leader);
+            if (j + 2 == it.ntiles) dev::tc_commit_leader(q_empty, leader);
+          }
+        }
+      } else {
+        // One query tile: S of tile j goes to S buffer j & 1, so the next
+        // tile's S runs while the softmax works on this one.  The buffer's
+        // last P was read by the P V two tiles back (the item's tile j - 2,
+        // or for j < 2 the previous item's P V, all finished once the newest
+        // has); that P V is always the newest issued when S waits for it.
+        const int pv0 = pv[0];
+        auto issue_s1 = [&](int j, int st) -> bool {
+          const int need = j >= 2 ? pv0 + j - 2 : pv0 - 1;
+          if (need >= 0 && !PF_WAIT(5, wait(&pv_done[0], need & 1))) return false;
+          // buffer 1 last held group 1's P if a two-query-tile item came
+          // before: its newest P V came after group 0's
+          if (j < 2 && pv[1] > 0 && !PF_WAIT(5, wait(&pv_done[1], (pv[1] - 1) & 1))) return false;
+          dev::tc_fence_after_sync();
+          const uint64_t bk = desc_k + uint64_t((st * 2 * TcSmem::kChunk) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = uint64_t(((kk >> 2) * TcSmem::kChunk + (kk & 3) * 32) >> 4);
+            dev::tc_mma_ss_leader(tmem + (j & 1) * 128, desc_q + off, bk + off, idesc_s,
+                                  uint32_t(kk), leader);
+          }
+          dev::tc_commit_leader(&sb_full[j & 1], leader);
+          return true;
+        };
+        const int pro = it.ntiles < 2 ? it.ntiles : 2;
+        for (int j = 0; j < pro && ok; ++j) {
+          const int st = (kt + j) & 1;
+          ok = PF_WAIT(2, wait(&k_full[st], ((kt + j) >> 1) & 1));
+          if (ok) ok = issue_s1(j, st);
+          if (ok) dev::tc_commit_leader(&k_empty[st], leader);
+        }
+        if (ok && it.ntiles <= 2) dev::tc_commit_leader(q_empty, leader);
+        for (int j = 0; j < it.ntiles && ok; ++j) {
+          const int st = (kt + j) & 1;  // also the stage of tile j + 2
+          ok = PF_WAIT(3, wait(&v_full[st], ((kt + j) >> 1) & 1));
+          if (ok) ok = issue_pv(0, j, st, j & 1);
+          if (ok) dev::tc_commit_leader(&v_empty[st], leader);
+          if (ok && j + 2 < it.ntiles) {
+            ok = PF_WAIT(2, wait(&k_full[st], ((kt + j + 2) >> 1) & 1));
+            if (ok) ok = issue_s1(j + 2, st);
+            if (ok) {
+              dev::tc_commit_leader(&k_empty[st], leader);
+              if (j + 3 == it.ntiles) dev::tc_commit_leader(q_empty, leader);
+            }
+          }
         }
       }
       kt += it.ntiles;
@@ -1132,9 +1187,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int w = warp >> 2;              // query tile of this group
     const int r = threadIdx.x & 127;      // row of the tile = TMEM lane
     const uint32_t lanes = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t t_s = tmem + lanes + w * 128, t_o = tmem + lanes + 256 + w * 128;
+    const uint32_t t_o = tmem + lanes + 256 + w * 128;
     const float sl2 = p.scale_log2;       // > 0 on this path
     int cnt = 0;                          // tiles of this group so far
+    int sfw = 0;                          // waits on s_full[w] (two-tile items)
+    int sbw[2] = {0, 0};                  // waits on sb_full[b] (one-tile items, group 0)
     int merges = 0;                       // split items merged in-kernel so far
     int kt = 0;                           // K / V tiles so far (group 0 sees them all)
     PF_DECL;
@@ -1173,12 +1230,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int pos = valid ? min(shared ? it.ctx - 1 : it.ctx - it.qlen + gr / G, bound - 1) : -1;
       float mref = -INFINITY, l = 0.f;
       for (int j = 0; j < it.ntiles && ok; ++j, ++cnt) {
-        if (!PF_WAIT(1, dev::mbar_wait_bounded(&s_full[w], cnt & 1, tmo, p.status))) {
+        // this tile's S buffer: the group's own, or (one query tile) the
+        // buffer the tiles alternate over
+        const int buf = it.two ? w : (j & 1);
+        uint64_t* sbar = it.two ? &s_full[w] : &sb_full[buf];
+        const int spar = it.two ? (sfw++ & 1) : (sbw[buf]++ & 1);
+        if (!PF_WAIT(1, dev::mbar_wait_bounded(sbar, uint32_t(spar), tmo, p.status))) {
           ok = false;
           break;
         }
         PF_MARK(pf_tile);
         dev::tc_fence_after_sync();
+        const uint32_t t_s = tmem + lanes + buf * 128;
         const int t0 = it.first * kBlockSize + j * kTcTokens;  // first token of the tile
         uint32_t sv[4][32];
 #pragma unroll
@@ -1194,6 +1257,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (t0 + 32 * c + i > pos) sv[c][i] = __float_as_uint(-INFINITY);
         }
+        // One query tile: this tile's S did not wait for the previous P V.
+        // Wait for it before touching O_w or announcing P, so that at most
+        // one P V of this group is ever outstanding: the parity waits on
+        // pv_done (here and in the epilogue) and the MMA warp's wait on
+        // p_full then never see a barrier two phases ahead.
+        bool pv_waited = it.two || j == 0;
+        auto wait_prev_pv = [&]() -> bool {
+          if (pv_waited) return true;
+          pv_waited = true;
+          if (!PF_WAIT(3, dev::mbar_wait_bounded(&pv_done[w], (cnt - 1) & 1, tmo, p.status)))
+            return false;
+          dev::tc_fence_after_sync();
+          return true;
+        };
         // row maximum: eight independent chains of three-input maxima
         float m8[8];
 #pragma unroll
@@ -1208,8 +1285,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               fmaxf(m8[6], m8[7])) * sl2;
         if (mx > mref + kTcRescale) {  // also the row's first unmasked column
           if (mref != -INFINITY) {
-            // O_w holds every earlier tile (S_w of this tile was issued after
-            // the previous P V finished): rescale it in TMEM
+            // O_w holds every earlier tile once the previous P V has finished
+            // (with two query tiles S_w was issued only after it; one tile's
+            // S runs ahead, so wait for it): rescale it in TMEM
+            if (!wait_prev_pv()) {
+              ok = false;
+              break;
+            }
             const float a = dev::fast_exp2(mref - mx);
             l *= a;
 #pragma unroll 1
@@ -1244,6 +1326,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l += ((acc[0][0] + acc[0][1]) + (acc[1][0] + acc[1][1])) +
              ((acc[2][0] + acc[2][1]) + (acc[3][0] + acc[3][1]));
         PF_ADD(6, pf_math);
+        if (!wait_prev_pv()) {
+          ok = false;
+          break;
+        }
         dev::tmem_st32(t_s, sv[0]);
         dev::tmem_st32(t_s + 32, sv[1]);
         if (w == 0 && t0 + kTcTokens > bound) {

@@ -207,3 +207,23 @@ def test_prefill_split_merge_with_mixed_tiles(gpu, dtype):
     again = run_prefill(batch, q, kc, vc, qs, gpu)
     assert torch.equal(out, again)            # the counters reset between runs
     assert_attention_close(out, oracle_prefill(batch, q, kc, vc, qs), TORCH_DTYPES[dtype])
+
+
+@pytest.mark.parametrize("heads", [(32, 8), (8, 8)], ids=["g4", "g1"])
+def test_prefill_one_and_two_tile_items_alternate(gpu, heads):
+    """Enough query blocks not to split, with items of one 128-row query tile
+    (whose S alternates between the two S buffers) and of two tiles mixed in
+    the work list, over contexts of 3 to 24 KV tiles (odd and even counts):
+    the buffers change hands between the two kinds of item."""
+    hq, hkv = heads
+    g = hq // hkv
+    # rows = chunk * G: one tile (<= 128), two tiles, two with a partial second
+    chunks = [max(1, 100 // g), 256 // g, 132 // g, max(1, 20 // g), 360 // g, 64 // g,
+              max(1, 120 // g), 200 // g] * 2
+    rng = np.random.default_rng(123)
+    lens = [int(c + rng.integers(300, 3000)) for c in chunks]
+    batch, q, kc, vc, qs = prefill_inputs(lens, chunks, hq, hkv, 128, "bf16", seed=124, dev=gpu)
+    out = run_prefill(batch, q, kc, vc, qs, gpu)
+    again = run_prefill(batch, q, kc, vc, qs, gpu)
+    assert torch.equal(out, again)
+    assert_attention_close(out, oracle_prefill(batch, q, kc, vc, qs), torch.bfloat16)
