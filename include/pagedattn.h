@@ -253,10 +253,11 @@ PA_API int pa_paged_attention_decode_shared_prefix(
  * takes pa_paged_attention_decode_shared_prefix's arguments and launches the
  * prefix phase, the suffix decode and the combine.  It needs a plan made with
  * the same sizes, prefix_blocks, dtype and sign of scale and the same
- * context_lens contents, in stream order on the same workspace; a run whose
- * workspace holds no plan for its sizes does nothing and sets the status
- * word (pa_check_status returns PA_ERR_INVALID_ARG), changed lengths under
- * the same sizes are not detected and give unspecified output.  Runs may
+ * context_lens contents, in stream order on the same workspace; in a run
+ * whose workspace holds no plan for its sizes the attention kernels do
+ * nothing and set the status word (pa_check_status returns
+ * PA_ERR_INVALID_ARG), and out is unspecified; changed lengths under the
+ * same sizes are not detected and give unspecified output.  Runs may
  * follow one plan any number of times; each leaves the workspace ready for
  * the next.  With prefix_blocks == 0 the pair is the plain decode's plan and
  * run; for PA_F32 the plan does nothing.
@@ -308,10 +309,11 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
  * step) writes each sequence's table past its group's prefix and the plans
  * of the prefix phase and the suffix decode into the workspace; _run (per
  * layer, same sizes and arrays, same workspace, stream order) launches the
- * prefix phase, the suffix decode and the combine.  A run whose workspace
- * holds no plan for its sizes does nothing and sets the status word
- * (PA_ERR_INVALID_ARG); tables or lengths changed after the plan are not
- * detected and give unspecified output.  The one-shot entry is _plan then
+ * prefix phase, the suffix decode and the combine.  In a run whose
+ * workspace holds no plan for its sizes the attention kernels do nothing
+ * and set the status word (PA_ERR_INVALID_ARG), and out is unspecified;
+ * tables or lengths changed after the plan are not detected and give
+ * unspecified output.  The one-shot entry is _plan then
  * _run.
  * ---------------------------------------------------------------------- */
 PA_API int pa_paged_attention_decode_grouped_prefix_workspace_size(
