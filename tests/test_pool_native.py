@@ -259,3 +259,38 @@ def test_native_errors():
     with pytest.raises(PagedAttnError) as e:
         pool.free_seq(s)                    # double free of a sequence
     assert e.value.status == PA_ERR_NOT_FOUND
+
+
+# ------------------------------------------------- bench batches, both pools
+def test_bench_pool_batches_match_the_model():
+    """The bench's pool-built workloads (the prefix mix and the sampling
+    divergence) give the same tables, lengths and groups from the native pool
+    and from the oracle's model of it (the reference arm uses the model)."""
+    import bench
+    for name in ("prefix_8b", "sampling_8b"):
+        native, model = bench.make_batch(name, 0), bench.make_batch(name, 0, model_pool=True)
+        assert np.array_equal(native.block_tables, model.block_tables)
+        assert np.array_equal(native.context_lens, model.context_lens)
+        for key in ("group_start", "group_blocks"):
+            if key in native.extra:
+                assert np.array_equal(native.extra[key], model.extra[key])
+
+
+def test_sampling_divergence_pairs_and_groups():
+    """The divergence of 32 prompts forked 4 ways: 3 copy-on-write pairs per
+    prompt, distinct destinations, no destination another pair's source; each
+    group's members share exactly the prompt's whole blocks."""
+    import bench
+    from pagedattention_decode_attention_gb300 import workloads as wl
+    script = wl.sampling_cow()
+    pool = native(script.num_blocks, 16, script.initial_order)
+    branches, pairs = bench.cow_divergence(pool, script)
+    assert len(branches) == script.prompts * script.branches
+    assert pairs.shape == (script.prompts * (script.branches - 1), 2)
+    assert len(set(pairs[:, 1])) == len(pairs)
+    assert not set(pairs[:, 0]) & set(pairs[:, 1])
+    batch = bench.sampling_batch(script)
+    whole = (script.prompt_len + script.shared_extra) // 16
+    assert np.array_equal(batch.extra["group_blocks"], whole.astype(np.int32))
+    assert np.array_equal(batch.extra["group_start"],
+                          np.arange(0, len(branches) + 1, script.branches))
