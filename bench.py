@@ -887,8 +887,8 @@ def run_cascade_bench(args):
     parallel-sampling batch (grouped: each prompt's branches share their
     prompt).  Both run as a model step would: one plan, then per layer the
     new tokens' K/V appended and attention over the whole context (the plain
-    path fuses the two into one launch; the cascade path appends, then runs
-    its prefix phase, suffix decode and combine)."""
+    path in one launch; the cascade path as its prefix phase, the suffix
+    decode that also stores the new rows, and the combine)."""
     import pagedattention_decode_attention_gb300 as pa
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
@@ -903,8 +903,6 @@ def run_cascade_bench(args):
     size = (pa.grouped_prefix_workspace_size if grouped else pa.shared_prefix_workspace_size)(
         batch.num_seqs, hq, hkv, d, mb)
     ws = torch.empty(max(size, 256), dtype=torch.uint8, device=device)
-    appends = [pa.prepare_kv_append(rep.k_new[i], rep.v_new[i], rep.k_cache[i], rep.v_cache[i],
-                                    rep.slots) for i in range(L)]
     if grouped:
         gs = torch.from_numpy(batch.extra["group_start"]).to(device)
         gb = torch.from_numpy(batch.extra["group_blocks"]).to(device)
@@ -913,20 +911,18 @@ def run_cascade_bench(args):
         def cascade_step():
             pa.grouped_prefix_plan(rep.tables, rep.lens, gs, gb, hq, hkv, d, batch.scale, dt, ws)
             for i in range(L):
-                appends[i]()
-                pa.paged_attention_decode_grouped_prefix_run(rep.q[i], rep.k_cache[i],
-                                                             rep.v_cache[i], rep.tables, gs, gb,
-                                                             batch.scale, ws, out=rep.out[i])
+                pa.paged_attention_decode_grouped_prefix_append_run(
+                    rep.q[i], rep.k_new[i], rep.v_new[i], rep.slots, rep.k_cache[i],
+                    rep.v_cache[i], rep.tables, gs, gb, batch.scale, ws, out=rep.out[i])
     else:
         P = batch.extra["prefix_blocks"]
 
         def cascade_step():
             pa.shared_prefix_plan(rep.lens, P, hq, hkv, d, mb, batch.scale, dt, ws)
             for i in range(L):
-                appends[i]()
-                pa.paged_attention_decode_shared_prefix_run(rep.q[i], rep.k_cache[i],
-                                                            rep.v_cache[i], rep.tables, rep.lens,
-                                                            P, batch.scale, ws, out=rep.out[i])
+                pa.paged_attention_decode_shared_prefix_append_run(
+                    rep.q[i], rep.k_new[i], rep.v_new[i], rep.slots, rep.k_cache[i],
+                    rep.v_cache[i], rep.tables, rep.lens, P, batch.scale, ws, out=rep.out[i])
 
     def timed(step):
         for _ in range(max(args.warmup, 3)):
@@ -974,7 +970,7 @@ def run_cascade_bench(args):
         "plain_us_per_layer": plain_s / L * 1e6,
         "plain_value": batch.num_seqs / plain_s,
         "max_abs_diff_vs_plain": diff,
-        "gpu_launches": args.steps * ((3 if grouped else 2) + 4 * L),
+        "gpu_launches": args.steps * ((3 if grouped else 2) + 3 * L),
         "clocks": clk,
     }
     print(json.dumps(line))

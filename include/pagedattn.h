@@ -337,6 +337,37 @@ PA_API int pa_paged_attention_decode_grouped_prefix_run(
     float scale, int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * pa_paged_attention_decode_shared_prefix_append_run,
+ * pa_paged_attention_decode_grouped_prefix_append_run -- the _run of the
+ * single-prefix and grouped forms above with the step's new K/V rows stored
+ * and attended in the same launches, as pa_paged_attention_decode_append_run
+ * does for the plain decode (OS-lab appendix, section 2.1: each decode step
+ * appends the new token's key/value).
+ *
+ * k_new, v_new: [num_seqs][num_kv_heads][head_dim] (16-byte aligned);
+ * slot_mapping: DEVICE int64 [num_seqs], sequence b's new slot
+ * (physical * 16 + offset), < 0 for none.  Same result as pa_kv_append of
+ * the rows followed by the _run.  The new token of sequence b must be the last
+ * of its context and lie past the shared prefix, in a block of its own (the
+ * copy-on-write pool never appends into a shared block): the prefix phase
+ * does not see it.  A slot that is not the position of the sequence's last
+ * token, or a sequence with nothing past the prefix that has a slot, sets
+ * PA_ERR_DEVICE_BOUNDS.  The plan is the same _plan as above.
+ * ---------------------------------------------------------------------- */
+PA_API int pa_paged_attention_decode_shared_prefix_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    int prefix_blocks, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
+    size_t workspace_bytes, void* stream);
+PA_API int pa_paged_attention_decode_grouped_prefix_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * pa_paged_attention_prefill -- chunked-prefill attention over the paged cache.
  *
  * OS-lab appendix, section 2.1 (prefill writes the K/V of every prompt token

@@ -32,6 +32,8 @@ from .ops import (LayerCaches, Prepared, alloc_prefill_workspace, alloc_workspac
                   block_copy, block_swap, check_status, kv_append, paged_attention_decode,
                   paged_attention_decode_append_run, paged_attention_decode_shared_prefix,
                   paged_attention_decode_grouped_prefix, paged_attention_decode_grouped_prefix_run,
+                  paged_attention_decode_shared_prefix_append_run,
+                  paged_attention_decode_grouped_prefix_append_run,
                   grouped_prefix_plan, grouped_prefix_workspace_size,
                   paged_attention_decode_shared_prefix_run, shared_prefix_plan,
                   paged_attention_prefill, paged_attention_prefill_run, prefill_plan,

@@ -84,6 +84,14 @@ SIGNATURES = {
     "pa_paged_attention_decode_grouped_prefix_run": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i,
                                                           _i, _i, _i, _i, _i, C.c_float, _i, _vp,
                                                           _vp, _sz, _vp]),
+    "pa_paged_attention_decode_shared_prefix_append_run": (_i, [_vp, _vp, _vp, _vp, _vp, _vp,
+                                                                _vp, _vp, _i, _i, _i, _i, _i,
+                                                                _i, _i, C.c_float, _i, _vp,
+                                                                _vp, _sz, _vp]),
+    "pa_paged_attention_decode_grouped_prefix_append_run": (_i, [_vp, _vp, _vp, _vp, _vp, _vp,
+                                                                 _vp, _vp, _vp, _i, _i, _i, _i,
+                                                                 _i, _i, _i, C.c_float, _i, _vp,
+                                                                 _vp, _sz, _vp]),
     "pa_paged_attention_prefill_workspace_size": (_i, [_i, _i, _i, _i, _i, C.POINTER(_sz)]),
     "pa_paged_attention_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                                         C.c_float, _i, _vp, _vp, _sz, _vp]),

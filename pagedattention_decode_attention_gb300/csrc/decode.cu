@@ -516,9 +516,12 @@ __global__ void __launch_bounds__(W * 32)
     // still stored (it attends nothing)
     for (int b = blockIdx.x * 32 + lane; b < p.num_seqs; b += gridDim.x * 32) {
       if (p.cas_o && p.context_lens[b] - p.ctx_offset <= 0) {
-        // suffix mode: nothing past the shared prefix (weight 0 in the merge)
+        // suffix mode: nothing past the shared prefix (weight 0 in the merge).
+        // A new token would then sit inside the shared blocks, which a
+        // sequence never writes (copy-on-write gives it its own block first).
         for (int i = 0; i < Hq * D; ++i) p.cas_o[size_t(b) * Hq * D + i] = 0.f;
         for (int h = 0; h < Hq; ++h) p.cas_lse[size_t(b) * Hq + h] = -INFINITY;
+        if (fused && p.slot_mapping[b] >= 0) dev::flag_status(p.status, kStatusBounds);
       } else if (!p.cas_o && p.context_lens[b] <= 0) {
         uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
         for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
@@ -1386,6 +1389,19 @@ struct AppendArgs {
   const int64_t* slot_mapping = nullptr;
 };
 
+// Checks the new tokens' rows and slots of a fused append call.
+int append_args(const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                AppendArgs& app, const char* who) {
+  if (!k_new || !v_new || !slot_mapping)
+    return fail(PA_ERR_INVALID_ARG, "%s: k_new, v_new and slot_mapping are required", who);
+  if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15))
+    return fail(PA_ERR_INVALID_ARG, "%s: k_new and v_new must be 16-byte aligned", who);
+  app.k_new = k_new;
+  app.v_new = v_new;
+  app.slot_mapping = slot_mapping;
+  return PA_OK;
+}
+
 int run_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
              const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
              int head_dim, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
@@ -1534,14 +1550,9 @@ PA_API int pa_paged_attention_decode_append_run(
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
   if (rc != PA_OK || num_seqs == 0) return rc;
-  if (!k_new || !v_new || !slot_mapping)
-    return fail(PA_ERR_INVALID_ARG, "%s: k_new, v_new and slot_mapping are required", who);
-  if ((reinterpret_cast<uintptr_t>(k_new) & 15) || (reinterpret_cast<uintptr_t>(v_new) & 15))
-    return fail(PA_ERR_INVALID_ARG, "%s: k_new and v_new must be 16-byte aligned", who);
   AppendArgs app;
-  app.k_new = k_new;
-  app.v_new = v_new;
-  app.slot_mapping = slot_mapping;
+  rc = append_args(k_new, v_new, slot_mapping, app, who);
+  if (rc != PA_OK) return rc;
   return run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                   num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream), who, app);
@@ -1617,7 +1628,8 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
                        const int32_t* block_tables, const int32_t* context_lens, int prefix_blocks,
                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out,
-                       void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+                       void* workspace, size_t workspace_bytes, void* stream, const char* who,
+                       const AppendArgs& app = AppendArgs()) {
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
   if (rc != PA_OK || num_seqs == 0) return rc;
@@ -1640,7 +1652,7 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
     }
     return runs ? run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                            num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
-                           out, workspace, workspace_bytes, s, who)
+                           out, workspace, workspace_bytes, s, who, app)
                 : PA_OK;
   }
   if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
@@ -1670,10 +1682,11 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
                                   max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
                                   ws + sl.prefix, sl.po - sl.prefix, s);
   if (rc != PA_OK) return rc;
-  // 2. every sequence's own blocks
+  // 2. every sequence's own blocks (the new tokens, if any, are stored and
+  // attended here: they always lie past the shared prefix)
   rc = run_impl(q, k_cache, v_cache, block_tables, context_lens, num_seqs, num_q_heads,
                 num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
-                workspace, sl.prefix, s, who, AppendArgs(), sfx);
+                workspace, sl.prefix, s, who, app, sfx);
   if (rc != PA_OK) return rc;
   // 3. merge
   const int* parts = prefill::shared_prefix_split_count(ws + sl.prefix);
@@ -1722,7 +1735,8 @@ int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, con
                         const int32_t* group_start, const int32_t* group_blocks, int num_groups,
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                         int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out,
-                        void* workspace, size_t workspace_bytes, void* stream, const char* who) {
+                        void* workspace, size_t workspace_bytes, void* stream, const char* who,
+                        const AppendArgs& app = AppendArgs()) {
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
   if (rc != PA_OK || num_seqs == 0) return rc;
@@ -1786,10 +1800,10 @@ int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, con
                                    max_blocks_per_seq, num_blocks, scale, dtype, po, plse,
                                    ws + sl.prefix, sl.po - sl.prefix, s);
   if (rc != PA_OK) return rc;
-  // 2. every sequence's own blocks
+  // 2. every sequence's own blocks (and its new token, if any)
   rc = run_impl(q, k_cache, v_cache, sfx_tables, sfx_ctx, num_seqs, num_q_heads, num_kv_heads,
                 head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out, workspace, sl.prefix,
-                s, who, AppendArgs(), sfx);
+                s, who, app, sfx);
   if (rc != PA_OK) return rc;
   // 3. merge, each row with its own group's parts
   const int* parts = prefill::shared_prefix_split_count(ws + sl.prefix);
@@ -1908,6 +1922,38 @@ PA_API int pa_paged_attention_decode_grouped_prefix_run(
                              num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
                              out, workspace, workspace_bytes, stream,
                              "paged_attention_decode_grouped_prefix_run");
+}
+
+PA_API int pa_paged_attention_decode_shared_prefix_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    int prefix_blocks, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_decode_shared_prefix_append_run";
+  AppendArgs app;
+  int rc = append_args(k_new, v_new, slot_mapping, app, who);
+  if (rc != PA_OK) return rc;
+  return shared_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables,
+                            context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
+                            head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                            workspace, workspace_bytes, stream, who, app);
+}
+
+PA_API int pa_paged_attention_decode_grouped_prefix_append_run(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* group_start,
+    const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+    int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* who = "paged_attention_decode_grouped_prefix_append_run";
+  AppendArgs app;
+  int rc = append_args(k_new, v_new, slot_mapping, app, who);
+  if (rc != PA_OK) return rc;
+  return grouped_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables, nullptr,
+                             group_start, group_prefix_blocks, num_groups, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
+                             out, workspace, workspace_bytes, stream, who, app);
 }
 
 PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,

@@ -424,6 +424,53 @@ def paged_attention_decode_grouped_prefix(q, k_cache, v_cache, block_tables, con
     return out
 
 
+def paged_attention_decode_shared_prefix_append_run(q, k_new, v_new, slot_mapping, k_cache,
+                                                    v_cache, block_tables, context_lens,
+                                                    prefix_blocks: int, scale: float, workspace,
+                                                    out=None, stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode_shared_prefix_run` with the step's new
+    K/V rows (one per sequence, to ``slot_mapping[b]``, past the shared
+    prefix) stored and attended in the same launches."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, context_lens)
+    _append_args(q, k_new, v_new, slot_mapping, hkv, d)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_shared_prefix_append_run(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), context_lens.data_ptr(),
+        int(prefix_blocks), b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(dev, stream)))
+    return out
+
+
+def paged_attention_decode_grouped_prefix_append_run(q, k_new, v_new, slot_mapping, k_cache,
+                                                     v_cache, block_tables, group_start,
+                                                     group_prefix_blocks, scale: float,
+                                                     workspace, out=None,
+                                                     stream=None) -> torch.Tensor:
+    """:func:`paged_attention_decode_grouped_prefix_run` with the step's new
+    K/V rows (one per sequence, to ``slot_mapping[b]``, past its group's
+    prefix) stored and attended in the same launches."""
+    dev, b, hq, hkv, d, nb, mb = _decode_args(q, k_cache, v_cache, block_tables, None)
+    _append_args(q, k_new, v_new, slot_mapping, hkv, d)
+    g = _group_args(group_start, group_prefix_blocks, b, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _cuda_contig("out", out, dev)
+    _require(out.shape == q.shape and out.dtype == q.dtype, "out must match q")
+    _cuda_contig("workspace", workspace, dev)
+    capi.check(capi.lib().pa_paged_attention_decode_grouped_prefix_append_run(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(),
+        k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), group_start.data_ptr(),
+        group_prefix_blocks.data_ptr(), g, b, hq, hkv, d, mb, nb, float(scale), _dtype_code(q),
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        _stream(dev, stream)))
+    return out
+
+
 def prefill_workspace_size(num_seqs: int, total_q: int, num_q_heads: int, num_kv_heads: int,
                            head_dim: int) -> int:
     n = C.c_size_t(0)

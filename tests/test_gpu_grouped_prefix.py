@@ -193,3 +193,37 @@ def test_grouped_prefix_rejects_fp32_and_bad_group_count(gpu):
                                                    gs_d, gb_d, 0.125)
     with pytest.raises(ValueError):                  # group_start one entry short
         pa().paged_attention_decode_grouped_prefix(q, kc, vc, bt, cl, gs_d[:-1], gb_d, 0.125)
+
+
+@pytest.mark.parametrize("dtype,head_dim", [("bf16", 128), ("f16", 64)])
+def test_grouped_prefix_append_run_equals_append_then_run(gpu, dtype, head_dim):
+    """The fused grouped run stores each sequence's new row past its group's
+    prefix and attends it: caches and output bit-identical to kv_append
+    followed by the run; the oracle over the updated caches agrees."""
+    dt = TORCH_DTYPES[dtype]
+    q, kc, vc, tables, lens, gs, gb = grouped_batch(GROUPS, 32, 8, head_dim, dtype, seed=590,
+                                                    dev=gpu)
+    first_private = np.repeat(gb.astype(np.int64) * 16, np.diff(gs))
+    pos = lens.astype(np.int64) - 1
+    slots = tables[np.arange(len(lens)), pos // 16].astype(np.int64) * 16 + pos % 16
+    slots[pos < first_private] = -1          # nothing past the prefix: no new token there
+    slots_d = torch.from_numpy(slots).to(gpu)
+    k_new = wl.normal((len(lens), 8, head_dim), dt, 591, gpu)
+    v_new = wl.normal((len(lens), 8, head_dim), dt, 592, gpu)
+    bt, cl, gs_d, gb_d = on(gpu, tables, lens, gs, gb)
+    scale = 1.0 / np.sqrt(head_dim)
+    n = pa().grouped_prefix_workspace_size(len(lens), 32, 8, head_dim, tables.shape[1])
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=gpu)
+    kc2, vc2 = kc.clone(), vc.clone()
+    pa().grouped_prefix_plan(bt, cl, gs_d, gb_d, 32, 8, head_dim, scale, dt, ws)
+    pa().kv_append(k_new, v_new, kc, vc, slots_d)
+    ref = pa().paged_attention_decode_grouped_prefix_run(q, kc, vc, bt, gs_d, gb_d, scale,
+                                                         ws).clone()
+    got = pa().paged_attention_decode_grouped_prefix_append_run(q, k_new, v_new, slots_d, kc2,
+                                                                vc2, bt, gs_d, gb_d, scale, ws)
+    pa().check_status()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(got, ref)
+    want = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc), tables,
+                                     lens, scale)
+    assert_attention_close(got, want, dt)

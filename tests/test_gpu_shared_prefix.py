@@ -141,3 +141,59 @@ def test_shared_prefix_split_with_partial_tiles(gpu, heads):
     ref = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc), tables,
                                     lens, 1.0 / np.sqrt(128))
     assert_attention_close(out, ref, torch.bfloat16)
+
+
+def new_token_inputs(q, kc, tables, lens, first_private, seed, dev):
+    """Each sequence's newest token as the step's new row: its slot (-1 where
+    the token lies inside the shared blocks: copy-on-write never appends
+    there) and random K/V rows."""
+    pos = lens.astype(np.int64) - 1
+    slots = tables[np.arange(len(lens)), pos // 16].astype(np.int64) * 16 + pos % 16
+    slots[pos < first_private] = -1
+    hkv, d = kc.shape[1], kc.shape[3]
+    k_new = wl.normal((len(lens), hkv, d), kc.dtype, seed, dev)
+    v_new = wl.normal((len(lens), hkv, d), kc.dtype, seed + 1, dev)
+    return k_new, v_new, torch.from_numpy(slots).to(dev)
+
+
+@pytest.mark.parametrize("dtype,head_dim", [("bf16", 128), ("f16", 64)])
+def test_shared_prefix_append_run_equals_append_then_run(gpu, dtype, head_dim):
+    """The fused run stores the new rows and attends them: caches and output
+    bit-identical to kv_append followed by the run, and the oracle over the
+    updated caches agrees."""
+    dt = TORCH_DTYPES[dtype]
+    q, kc, vc, tables, lens = shared_batch(1024, SUFFIXES, 32, 8, head_dim, dtype, seed=370,
+                                           dev=gpu)
+    k_new, v_new, slots = new_token_inputs(q, kc, tables, lens, 1024, 380, gpu)
+    bt, cl = torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu)
+    mb, scale = tables.shape[1], 1.0 / np.sqrt(head_dim)
+    n = pa().shared_prefix_workspace_size(len(lens), 32, 8, head_dim, mb)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=gpu)
+    kc2, vc2 = kc.clone(), vc.clone()
+    pa().shared_prefix_plan(cl, 64, 32, 8, head_dim, mb, scale, dt, ws)
+    pa().kv_append(k_new, v_new, kc, vc, slots)
+    ref = pa().paged_attention_decode_shared_prefix_run(q, kc, vc, bt, cl, 64, scale, ws).clone()
+    got = pa().paged_attention_decode_shared_prefix_append_run(q, k_new, v_new, slots, kc2, vc2,
+                                                               bt, cl, 64, scale, ws)
+    pa().check_status()
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert torch.equal(got, ref)
+    want = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc), tables,
+                                     lens, scale)
+    assert_attention_close(got, want, dt)
+
+
+def test_shared_prefix_append_into_the_prefix_sets_bounds_status(gpu):
+    """A new token with nothing past the prefix would be written into a
+    shared block: refused through the status word."""
+    q, kc, vc, tables, lens = shared_batch(256, [0, 5, 40], 32, 8, 128, "bf16", seed=390,
+                                           dev=gpu)
+    k_new, v_new, slots = new_token_inputs(q, kc, tables, lens, 0, 391, gpu)  # every slot set
+    bt, cl = torch.from_numpy(tables).to(gpu), torch.from_numpy(lens).to(gpu)
+    n = pa().shared_prefix_workspace_size(3, 32, 8, 128, tables.shape[1])
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=gpu)
+    pa().shared_prefix_plan(cl, 16, 32, 8, 128, tables.shape[1], 0.125, torch.bfloat16, ws)
+    pa().paged_attention_decode_shared_prefix_append_run(q, k_new, v_new, slots, kc, vc, bt, cl,
+                                                         16, 0.125, ws)
+    with pytest.raises(pa().PagedAttnError):
+        pa().check_status()
