@@ -27,21 +27,6 @@ __device__ __forceinline__ void flag_status(unsigned* status, unsigned bits) {
   if (status) atomicOr(status, bits);
 }
 
-// ---------------------------------------------- shared-memory release/acquire
-__device__ __forceinline__ void st_release_cta(volatile int* p, int v) {
-  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(const_cast<int*>(p))),
-               "r"(v)
-               : "memory");
-}
-__device__ __forceinline__ int ld_acquire_cta(volatile int* p) {
-  int v;
-  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];"
-               : "=r"(v)
-               : "r"(smem_u32(const_cast<int*>(p)))
-               : "memory");
-  return v;
-}
-
 // Atomic add at GPU scope with acquire-release semantics: the caller's earlier
 // writes (and those ordered before it, e.g. by a warp barrier) are visible to
 // whoever later acquires this location, and the caller sees all writes
