@@ -91,3 +91,53 @@ def test_copy_paths_reject_on_host(lib):
     assert lib.pa_kv_append(16, 16, 16, 16, 16, 1, 8, 128, 16, 5, None) == 2
     ptrs = (C.c_void_p * 1)(256)
     assert lib.pa_block_copy(ptrs, ptrs, 300, 256, 1, 8, 128, 16, 2, None) == 1
+
+
+def _grouped(lib, **kw):
+    a = dict(q=256, k=256, v=256, bt=256, cl=256, gs=256, gb=256, num_groups=2, num_seqs=4,
+             num_q_heads=32, num_kv_heads=8, head_dim=128, max_blocks=8, num_blocks=64,
+             scale=0.125, dtype=2, out=256, ws=256, workspace_bytes=1 << 30)
+    a.update(kw)
+    return lib.pa_paged_attention_decode_grouped_prefix(
+        a["q"], a["k"], a["v"], a["bt"], a["cl"], a["gs"], a["gb"], a["num_groups"],
+        a["num_seqs"], a["num_q_heads"], a["num_kv_heads"], a["head_dim"], a["max_blocks"],
+        a["num_blocks"], a["scale"], a["dtype"], a["out"], a["ws"], a["workspace_bytes"], None)
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(num_groups=0), 1),              # no group
+    (dict(num_groups=5), 1),              # more groups than sequences
+    (dict(dtype=0), 2),                   # fp32 decodes exactly without the cascade
+    (dict(workspace_bytes=4096), 1),      # workspace too small
+    (dict(ws=264), 1),                    # workspace not 256-byte aligned
+    (dict(gs=None), 1),                   # group arrays required
+    (dict(bt=None), 1),                   # tables required by the plan
+])
+def test_grouped_prefix_rejects_on_host(lib, kwargs, status):
+    assert _grouped(lib, **kwargs) == status
+    assert lib.pa_last_error()
+
+
+def test_grouped_prefix_workspace_covers_the_shared_layout(lib):
+    g, s = C.c_size_t(0), C.c_size_t(0)
+    assert lib.pa_paged_attention_decode_grouped_prefix_workspace_size(
+        128, 32, 8, 128, 65, C.byref(g)) == 0
+    assert lib.pa_paged_attention_decode_shared_prefix_workspace_size(
+        128, 32, 8, 128, 65, C.byref(s)) == 0
+    # plus each sequence's suffix table, suffix length and prefix block count
+    assert g.value >= s.value + 128 * 65 * 4 + 2 * 128 * 4
+
+
+def test_fused_cascade_runs_reject_on_host(lib):
+    ptr = 256
+    # new K/V rows and slots are required, and 16-byte aligned
+    assert lib.pa_paged_attention_decode_shared_prefix_append_run(
+        ptr, None, ptr, ptr, ptr, ptr, ptr, ptr, 4, 4, 32, 8, 128, 8, 64, 0.125, 2, ptr, ptr,
+        1 << 30, None) == 1
+    assert lib.pa_paged_attention_decode_grouped_prefix_append_run(
+        ptr, ptr + 8, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 2, 4, 32, 8, 128, 8, 64, 0.125, 2, ptr,
+        ptr, 1 << 30, None) == 1
+    # a prefix longer than the table
+    assert lib.pa_paged_attention_decode_shared_prefix_append_run(
+        ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 9, 4, 32, 8, 128, 8, 64, 0.125, 2, ptr, ptr,
+        1 << 30, None) == 1
