@@ -1185,20 +1185,26 @@ def run_copy_bench(args):
     print(json.dumps(line))
 
 
-def oracle_copy_sample(script, layers, hkv, d, seconds):
-    """The oracle's pool model and block copy on the same divergence, host
-    caches holding only the blocks the pairs touch (16-bit words standing in
-    for bf16: the copy moves bytes), repeated for about ``seconds``."""
-    import oracle.attention as oa
+def oracle_copy_inputs(script, layers, hkv, d):
+    """The divergence's pairs from the oracle's pool model, renumbered onto
+    host caches that hold only the blocks the pairs touch (16-bit words
+    standing in for bf16: the copy moves bytes).  Returns (pair count,
+    per-layer K caches, V caches, renumbered pairs)."""
     from oracle.pool import BlockPool as ModelPool
-    model = ModelPool(script.num_blocks, 16, script.initial_order)
-    _, pairs = cow_divergence(model, script)
+    _, pairs = cow_divergence(ModelPool(script.num_blocks, 16, script.initial_order), script)
     ids, compact = np.unique(pairs, return_inverse=True)
-    compact = compact.reshape(pairs.shape)
     gen = np.random.default_rng(wl.SEED_BASE + 9)
     shape = (len(ids), hkv, 16, d)
     kc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
     vc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    return len(pairs), kc, vc, compact.reshape(pairs.shape)
+
+
+def oracle_copy_sample(script, layers, hkv, d, seconds):
+    """The oracle's block copy of the same divergence, repeated for about
+    ``seconds``."""
+    import oracle.attention as oa
+    npairs, kc, vc, compact = oracle_copy_inputs(script, layers, hkv, d)
     oa.block_copy(kc, vc, compact)
     reps, t0 = 0, time.perf_counter()
     while True:
@@ -1207,9 +1213,9 @@ def oracle_copy_sample(script, layers, hkv, d, seconds):
         if time.perf_counter() - t0 >= seconds:
             break
     secs = time.perf_counter() - t0
-    return {"value": len(pairs) * reps / secs, "unit": "block copies/s", "cores": 1,
+    return {"value": npairs * reps / secs, "unit": "block copies/s", "cores": 1,
             "kind": "oracle",
-            "sample": (f"{reps} runs of the oracle's block copy of the {len(pairs)} divergence "
+            "sample": (f"{reps} runs of the oracle's block copy of the {npairs} divergence "
                        f"pairs in all {layers} layers, 1 thread")}
 
 
@@ -1337,17 +1343,9 @@ def run_reference_copy(args):
     and block copy, each step one copy of the 96 divergence pairs in every
     layer (host caches holding only the blocks the pairs touch)."""
     import oracle.attention as oa
-    from oracle.pool import BlockPool as ModelPool
     script = wl.sampling_cow()
     layers = args.layers if args.layers > 0 else 32
-    hkv, d = 8, 128
-    _, pairs = cow_divergence(ModelPool(script.num_blocks, 16, script.initial_order), script)
-    ids, compact = np.unique(pairs, return_inverse=True)
-    compact = compact.reshape(pairs.shape)
-    gen = np.random.default_rng(wl.SEED_BASE + 9)
-    shape = (len(ids), hkv, 16, d)
-    kc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
-    vc = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
+    npairs, kc, vc, compact = oracle_copy_inputs(script, layers, 8, 128)
     warm = max(args.warmup, 3)
     for _ in range(warm):
         oa.block_copy(kc, vc, compact)
@@ -1355,15 +1353,15 @@ def run_reference_copy(args):
     for _ in range(args.steps):
         oa.block_copy(kc, vc, compact)
     secs = time.perf_counter() - t0
-    value = len(pairs) * args.steps / secs
+    value = npairs * args.steps / secs
     line = {
         "impl": "reference", "metric": COPY_METRIC, "value": value, "unit": "block copies/s",
         "n_gpus": 1, "steps": args.steps, "warmup": warm, "ms_per_step": secs / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
         "data": "synthetic", "config": {"workload": "block_copy_8b", "layers": layers,
-                                        "pairs": len(pairs)},
+                                        "pairs": npairs},
         "cpu_baseline": {"value": value, "unit": "block copies/s", "cores": 1, "kind": "oracle",
-                         "sample": (f"each step: the {len(pairs)} divergence pairs in all "
+                         "sample": (f"each step: the {npairs} divergence pairs in all "
                                     f"{layers} layers, numpy, 1 thread")},
         "e2e": {"value": value, "unit": "block copies/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
