@@ -11,6 +11,7 @@ import socket
 import subprocess
 import sys
 
+import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
@@ -69,3 +70,23 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+
+
+@pytest.mark.parametrize("workload", ["prefix_8b", "sampling_8b", "prefill_8b", "block_copy_8b",
+                                      "swap_8b", "pool_churn"])
+def test_reference_arm_prints_one_complete_line(workload):
+    """``bench.py --impl reference --workload W``: the oracle arm of every
+    bench workload prints one JSON line with the contract's keys, the
+    workload's name and a positive value (CPU only)."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           workload, "--steps", "1", "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["config"]["workload"].startswith(workload.split("_")[0])
