@@ -294,6 +294,8 @@ def run_prefill_bench(args):
         "gpu_launches": (1 + L) * args.steps,
         "clocks": clk,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_prefill_baseline(batch, args.cpu_seconds / 2)
     print(json.dumps(line))
 
 
@@ -973,6 +975,12 @@ def run_cascade_bench(args):
         "gpu_launches": args.steps * ((3 if grouped else 2) + 3 * L),
         "clocks": clk,
     }
+    if not args.no_cpu_baseline:
+        # the oracle computes the same attention (the cascade is exact)
+        v, units, _ = cpu_oracle_sample(batch, OracleInputs(batch, rep), args.cpu_seconds / 2)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": (f"{units} (sequence, layer) units of layer 0, float64 "
+                                           f"numpy, 1 thread; {L} units = 1 token")}
     print(json.dumps(line))
 
 
@@ -1038,6 +1046,8 @@ def run_swap_bench(args):
         "gpu_launches": 2 * reps,
         "clocks": clk,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_swap_baseline(layers, args.cpu_seconds / 4)
     print(json.dumps(line))
 
 
@@ -1300,21 +1310,45 @@ def run_reference_pool(args):
     print(json.dumps(line))
 
 
-def run_reference_prefill(args):
-    """Reference arm of the chunked-prefill workload: the prefill oracle on a
-    bounded sample of query rows per step, scaled to query tokens/s."""
-    import oracle.attention as oa
-    batch = make_batch("prefill_8b", 0)
-    qlens = batch.extra["query_lens"]
-    qs = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int64)
+def oracle_prefill_inputs(batch):
+    """Host inputs of the chunked-prefill oracle for the workload's shapes:
+    (q, k cache, v cache, query starts, row order)."""
+    qs = np.concatenate([[0], np.cumsum(batch.extra["query_lens"])]).astype(np.int64)
     total_q = int(qs[-1])
     gen = np.random.default_rng(batch.seed)
     shape = (batch.num_blocks, batch.num_kv_heads, 16, batch.head_dim)
     kc = gen.standard_normal(shape, dtype=np.float32)
     vc = gen.standard_normal(shape, dtype=np.float32)
     q = gen.standard_normal((total_q, batch.num_q_heads, batch.head_dim), dtype=np.float32)
+    return q, kc, vc, qs, np.random.default_rng(7).permutation(total_q)
+
+
+def oracle_prefill_baseline(batch, seconds: float) -> dict:
+    """The prefill oracle on 8 query rows at a time for about ``seconds``:
+    query tokens/s per layer on one host thread."""
+    import oracle.attention as oa
+    q, kc, vc, qs, order = oracle_prefill_inputs(batch)
+    oa.paged_attention_prefill(q, kc, vc, batch.block_tables, batch.context_lens, qs, batch.scale,
+                               rows=order[:8])  # untimed first call
+    rows, t0 = 0, time.perf_counter()
+    while rows == 0 or time.perf_counter() - t0 < seconds:
+        sel = order[rows % len(order):][:8]
+        oa.paged_attention_prefill(q, kc, vc, batch.block_tables, batch.context_lens, qs,
+                                   batch.scale, rows=sel)
+        rows += len(sel)
+    value = rows / (time.perf_counter() - t0)
+    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} query rows (all heads) of one layer, float64 numpy, 1 thread"}
+
+
+def run_reference_prefill(args):
+    """Reference arm of the chunked-prefill workload: the prefill oracle on a
+    bounded sample of query rows per step, scaled to query tokens/s."""
+    import oracle.attention as oa
+    batch = make_batch("prefill_8b", 0)
+    q, kc, vc, qs, order = oracle_prefill_inputs(batch)
+    total_q = len(order)
     rows_per_step = 8
-    order = np.random.default_rng(7).permutation(total_q)
     for i in range(max(args.warmup, 3)):
         oa.paged_attention_prefill(q, kc, vc, batch.block_tables, batch.context_lens, qs,
                                    batch.scale, rows=order[i * rows_per_step:(i + 1) * rows_per_step])
@@ -1369,13 +1403,12 @@ def run_reference_copy(args):
     print(json.dumps(line))
 
 
-def run_reference_swap(args):
-    """Reference arm of the swap_8b workload: the oracle's block swap, each
-    step 64 blocks of every layer out to a second set of host caches and back
-    (a bounded sample of the 1024-block batch)."""
+def oracle_swap_step(layers: int, nblk: int = 64):
+    """One step of the oracle's block swap: ``nblk`` blocks of every layer out
+    to a second set of host caches and back (16-bit words standing in for
+    bf16).  Returns (step function, blocks per direction)."""
     import oracle.attention as oa
-    layers = args.layers if args.layers > 0 else 32
-    hkv, d, nblk, nb = 8, 128, 64, 128
+    hkv, d, nb = 8, 128, 2 * nblk
     gen = np.random.default_rng(wl.SEED_BASE + 7)
     shape = (nb, hkv, 16, d)
     dk = [gen.integers(0, 1 << 16, size=shape, dtype=np.uint16) for _ in range(layers)]
@@ -1388,6 +1421,28 @@ def run_reference_swap(args):
     def step():
         oa.block_swap(dk, dv, hk, hv, out_pairs)
         oa.block_swap(hk, hv, dk, dv, in_pairs)
+    return step, nblk
+
+
+def oracle_swap_baseline(layers: int, seconds: float) -> dict:
+    step, nblk = oracle_swap_step(layers)
+    step()
+    n, t0 = 0, time.perf_counter()
+    while n == 0 or time.perf_counter() - t0 < seconds:
+        step()
+        n += 1
+    value = nblk * 16 * 2 * n / (time.perf_counter() - t0)
+    return {"value": value, "unit": "tokens/s (out + in, all layers)", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} steps of {nblk} blocks of all {layers} layers out and back, 1 thread"}
+
+
+def run_reference_swap(args):
+    """Reference arm of the swap_8b workload: the oracle's block swap, each
+    step 64 blocks of every layer out to a second set of host caches and back
+    (a bounded sample of the 1024-block batch)."""
+    layers = args.layers if args.layers > 0 else 32
+    step, nblk = oracle_swap_step(layers)
 
     warm = max(args.warmup, 3)
     for _ in range(warm):
