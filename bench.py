@@ -1243,11 +1243,11 @@ def pool_churn_stream(seed: int, n: int):
     return reqs, gen.integers(0, 4, size=1_000_000)
 
 
-def drive_pool(pool, no_blocks, reqs, arrivals):
+def drive_pool(pool, reqs, arrivals):
     """Runs the continuous-batching driver until every request retired;
     returns (pool operations, steps, seconds)."""
     from pagedattention_decode_attention_gb300.batching import ContinuousBatcher
-    b = ContinuousBatcher(pool, 16, no_blocks, max_running=128)
+    b = ContinuousBatcher(pool, 16, max_running=128)
     pending = list(reqs)
     ops = steps = 0
     tok = lambda r: (r.rid * 7919 + r.generated * 104729) % 50_000  # noqa: E731
@@ -1267,13 +1267,11 @@ def run_pool_bench(args):
     """Host block pool under continuous-batching churn (no GPU work): pool
     operations per second through the public API."""
     import pagedattention_decode_attention_gb300 as pa
-    from pagedattention_decode_attention_gb300.capi import PA_ERR_NO_BLOCKS, PagedAttnError
     reqs, arrivals = pool_churn_stream(wl.SEED_BASE + 8, 200)
     pool = pa.BlockPool(4096, 16, np.random.default_rng(1).permutation(4096))
     pool.enable_prefix_cache()
     pool.set_host_blocks(1024)
-    no_blocks = lambda e: isinstance(e, PagedAttnError) and e.status == PA_ERR_NO_BLOCKS  # noqa: E731
-    ops, steps, secs = drive_pool(pool, no_blocks, reqs, arrivals)
+    ops, steps, secs = drive_pool(pool, reqs, arrivals)
     st = pool.stats()
     print(json.dumps(pool_line(ops, steps, secs, st, impl=None)))
 
@@ -1296,12 +1294,12 @@ def pool_line(ops, steps, secs, st, impl):
 
 def run_reference_pool(args):
     """Reference arm of the pool workload: the pool model driven the same way."""
-    from oracle.pool import BlockPool as ModelPool, NoBlocks
+    from oracle.pool import BlockPool as ModelPool
     reqs, arrivals = pool_churn_stream(wl.SEED_BASE + 8, 200)
     pool = ModelPool(4096, 16, np.random.default_rng(1).permutation(4096))
     pool.enable_prefix_cache()
     pool.set_host_blocks(1024)
-    ops, steps, secs = drive_pool(pool, NoBlocks, reqs, arrivals)
+    ops, steps, secs = drive_pool(pool, reqs, arrivals)
     line = pool_line(ops, steps, secs, pool.stats(), impl="reference")
     line["cpu_baseline"] = {"value": line["value"], "unit": "ops/s", "cores": 1, "kind": "oracle",
                             "sample": "the whole stream through the Python pool model"}

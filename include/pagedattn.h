@@ -584,7 +584,8 @@ PA_API int pa_pool_append_slot(pa_pool* pool, int seq, int64_t* slot, int64_t* c
                                int64_t* cow_dst);
 /* Batched form: one slot per entry of seqs[0..n), written to slots[] and the
  * copy pairs (if any) appended to pairs[] (int64 [*num_pairs][2], capacity
- * pair_cap).  Stops at the first error; *done tells how many succeeded. */
+ * pair_cap; pairs may be NULL only when pair_cap == 0).  Stops at the first
+ * error; *done tells how many succeeded. */
 PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64_t* slots,
                                 int64_t* pairs, int pair_cap, int* num_pairs, int* done);
 PA_API int pa_pool_fork(pa_pool* pool, int parent, int* child);
@@ -651,6 +652,17 @@ PA_API int pa_pool_new_seq_with_prompt(pa_pool* pool, const int32_t* tokens, int
                                        int* hit_tokens);
 PA_API int pa_pool_append_token(pa_pool* pool, int seq, int32_t token, int64_t* slot,
                                 int64_t* cow_src, int64_t* cow_dst);
+/* Batched form of pa_pool_append_token: token tokens[i] appended to sequence
+ * seqs[i] for i = 0, 1, ... in order (a sequence may repeat: a prompt's
+ * tokens), slots to slots[], copy pairs appended to pairs[] (int64
+ * [*num_pairs][2], capacity pair_cap; NULL only when pair_cap == 0).  Stops
+ * at the first failing append and
+ * returns its status (PA_ERR_NO_BLOCKS when the pool ran out) with *done =
+ * the appends made; a full pair buffer returns PA_ERR_INVALID_ARG before the
+ * append that would need it. */
+PA_API int pa_pool_append_tokens(pa_pool* pool, const int32_t* seqs, const int32_t* tokens,
+                                 int n, int64_t* slots, int64_t* pairs, int pair_cap,
+                                 int* num_pairs, int* done);
 
 #ifdef __cplusplus
 }

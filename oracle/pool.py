@@ -274,6 +274,22 @@ class BlockPool:
                 self.key[block] = (h, parent_block, chunk)
         return slot, cow
 
+    def append_tokens(self, seqs, tokens):
+        """``append_token(seqs[i], tokens[i])`` for every i in order, stopping
+        where the pool runs out of blocks.  Returns (slots, copy pairs, number
+        of appends made), the native pool's batched form."""
+        slots, pairs, done = [], [], 0
+        for seq_id, token in zip(seqs, tokens):
+            try:
+                slot, cow = self.append_token(int(seq_id), int(token))
+            except NoBlocks:
+                break
+            slots.append(slot)
+            if cow is not None:
+                pairs.append(cow)
+            done += 1
+        return slots, pairs, done
+
     def fork(self, parent_id: int) -> int:
         parent = self._resident(parent_id)
         child_id = self.new_seq()

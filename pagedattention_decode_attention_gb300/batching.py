@@ -52,14 +52,12 @@ class StepReport:
 
 
 class ContinuousBatcher:
-    def __init__(self, pool, block_size: int, no_blocks, max_running: int = 256):
-        """``pool``: a block pool with the native pool's methods;
-        ``no_blocks``: the exception type (or predicate) its allocation raises
-        when it runs out of blocks."""
+    def __init__(self, pool, block_size: int, max_running: int = 256):
+        """``pool``: a block pool with the native pool's methods; its
+        ``append_tokens`` reports how many appends fit before it ran out of
+        blocks."""
         self.pool = pool
         self.bs = block_size
-        self.is_no_blocks = (no_blocks if callable(no_blocks) and not isinstance(no_blocks, type)
-                             else (lambda e, t=no_blocks: isinstance(e, t)))
         self.max_running = max_running
         self.waiting: deque[Request] = deque()
         self.swapped: deque[Request] = deque()
@@ -75,18 +73,6 @@ class ContinuousBatcher:
     def _free_blocks(self) -> int:
         st = self.pool.stats()
         return st["free_blocks"] + st.get("evictable_blocks", 0)
-
-    def _append(self, req: Request, token: int, rep: StepReport) -> bool:
-        try:
-            slot, cow = self.pool.append_token(req.seq, token)
-        except Exception as e:  # noqa: BLE001
-            if self.is_no_blocks(e):
-                return False
-            raise
-        rep.slots.append((req.seq, int(slot)))
-        if cow is not None:
-            rep.cow_pairs.append((int(cow[0]), int(cow[1])))
-        return True
 
     def _preempt(self, rep: StepReport) -> bool:
         """Preempt the most recently admitted running sequence."""
@@ -131,28 +117,34 @@ class ContinuousBatcher:
                 break
             seq, hit = self.pool.new_seq_with_prompt(req.prompt)
             req.seq, req.hit_tokens = seq, hit
-            ok = True
-            for t in req.prompt[hit:]:
-                if not self._append(req, t, rep):
-                    ok = False
-                    break
-            if not ok:                                   # cached blocks were evicted meanwhile
+            rest = req.prompt[hit:]
+            slots, pairs, done = self.pool.append_tokens([seq] * len(rest), rest)
+            rep.slots.extend((seq, int(s)) for s in slots)
+            rep.cow_pairs.extend((int(a), int(b)) for a, b in pairs)
+            if done < len(rest):                         # cached blocks were evicted meanwhile
                 self.pool.free_seq(seq)
                 req.seq = -1
                 break
             self.waiting.popleft()
             self.running.append(req)
             rep.admitted.append((req.rid, seq, hit))
-        # one new token for every running sequence
+        # one new token for every running sequence, in one pool call; where
+        # the pool runs out, preempt and go on from the sequence that failed
         i = 0
         while i < len(self.running):
-            req = self.running[i]
-            if self._append(req, next_token(req), rep):
-                req.generated += 1
-                i += 1
-            elif not self._preempt(rep) or req not in self.running:
-                if req in self.running:                  # nothing left to preempt
-                    raise RuntimeError("pool too small for one sequence")
+            batch = self.running[i:]
+            slots, pairs, done = self.pool.append_tokens([r.seq for r in batch],
+                                                         [next_token(r) for r in batch])
+            for r, s in zip(batch[:done], slots):
+                r.generated += 1
+                rep.slots.append((r.seq, int(s)))
+            rep.cow_pairs.extend((int(a), int(b)) for a, b in pairs)
+            i += done
+            if i < len(self.running):
+                req = self.running[i]
+                if not self._preempt(rep) or req not in self.running:
+                    if req in self.running:              # nothing left to preempt
+                        raise RuntimeError("pool too small for one sequence")
         # retire the finished
         for req in [r for r in self.running if r.generated >= r.max_new_tokens]:
             self.running.remove(req)

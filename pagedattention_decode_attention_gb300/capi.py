@@ -110,6 +110,8 @@ SIGNATURES = {
     "pa_pool_new_seq": (_i, [_vp, C.POINTER(_i)]),
     "pa_pool_append_slot": (_i, [_vp, _i, _i64p, _i64p, _i64p]),
     "pa_pool_append_slots": (_i, [_vp, _i32p, _i, _i64p, _i64p, _i, C.POINTER(_i), C.POINTER(_i)]),
+    "pa_pool_append_tokens": (_i, [_vp, _i32p, _i32p, _i, _i64p, _i64p, _i, C.POINTER(_i),
+                                   C.POINTER(_i)]),
     "pa_pool_fork": (_i, [_vp, _i, C.POINTER(_i)]),
     "pa_pool_share_prefix": (_i, [_vp, _i, _i, _i]),
     "pa_pool_pin": (_i, [_vp, _i, _i]),

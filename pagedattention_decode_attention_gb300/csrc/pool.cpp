@@ -308,9 +308,37 @@ PA_API int pa_pool_append_token(pa_pool* pool, int seq, int32_t token, int64_t* 
   return PA_OK;
 }
 
+PA_API int pa_pool_append_tokens(pa_pool* pool, const int32_t* seqs, const int32_t* tokens,
+                                 int n, int64_t* slots, int64_t* pairs, int pair_cap,
+                                 int* num_pairs, int* done) {
+  if (!pool || (n > 0 && (!seqs || !tokens || !slots)) || !num_pairs || !done || n < 0 ||
+      pair_cap < 0 || (pair_cap > 0 && !pairs))
+    return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_tokens: bad argument");
+  *num_pairs = 0;
+  *done = 0;
+  for (int i = 0; i < n; ++i) {
+    int64_t src, dst;
+    // as in pa_pool_append_slots: room for a copy pair before the slot is taken
+    Seq* s = pool->find(seqs[i]);
+    if (s && !s->swapped && s->ctx % pool->block_size != 0 &&
+        pool->refcount[s->table[s->ctx / pool->block_size]] > 1 && *num_pairs >= pair_cap)
+      return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_tokens: pair buffer full");
+    int rc = pa_pool_append_token(pool, seqs[i], tokens[i], &slots[i], &src, &dst);
+    if (rc != PA_OK) return rc;
+    if (src >= 0) {
+      pairs[2 * *num_pairs] = src;
+      pairs[2 * *num_pairs + 1] = dst;
+      (*num_pairs)++;
+    }
+    (*done)++;
+  }
+  return PA_OK;
+}
+
 PA_API int pa_pool_append_slots(pa_pool* pool, const int32_t* seqs, int n, int64_t* slots,
                                 int64_t* pairs, int pair_cap, int* num_pairs, int* done) {
-  if (!pool || (n > 0 && (!seqs || !slots)) || !num_pairs || !done || n < 0)
+  if (!pool || (n > 0 && (!seqs || !slots)) || !num_pairs || !done || n < 0 ||
+      pair_cap < 0 || (pair_cap > 0 && !pairs))
     return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_append_slots: bad argument");
   *num_pairs = 0;
   *done = 0;

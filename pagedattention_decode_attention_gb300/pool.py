@@ -109,6 +109,28 @@ class BlockPool:
                                                   C.byref(src), C.byref(dst)))
         return slot.value, (None if src.value < 0 else (src.value, dst.value))
 
+    def append_tokens(self, seqs, tokens):
+        """:meth:`append_token` of ``tokens[i]`` to ``seqs[i]`` for every i, in
+        order, in one call.  Stops where the pool runs out of blocks.  Returns
+        (int64 slots of the appends made, int64 copy pairs [p, 2], number of
+        appends made); other errors raise."""
+        seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        if seqs.shape != toks.shape or seqs.ndim != 1:
+            raise ValueError("seqs and tokens must be 1-D of one length")
+        n = seqs.shape[0]
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+        npairs, done = C.c_int(), C.c_int()
+        rc = self._lib.pa_pool_append_tokens(
+            self._h, seqs.ctypes.data_as(C.POINTER(C.c_int32)),
+            toks.ctypes.data_as(C.POINTER(C.c_int32)), n,
+            slots.ctypes.data_as(C.POINTER(C.c_int64)), pairs.ctypes.data_as(C.POINTER(C.c_int64)),
+            max(n, 1), C.byref(npairs), C.byref(done))
+        if rc != capi.PA_ERR_NO_BLOCKS:
+            capi.check(rc)
+        return slots[:done.value], pairs[:npairs.value], done.value
+
     def set_host_blocks(self, num_host_blocks: int, initial_order=None) -> None:
         """Give the pool a host tier (swap space) of ``num_host_blocks`` blocks."""
         order = None

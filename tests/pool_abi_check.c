@@ -2,7 +2,8 @@
  * the OS-lab appendix's copy-on-write walk-through at block size 4 (section
  * 4.4: after a fork both sequences share every block; the first writer into
  * the shared partial block gets a copy, the last holder writes in place),
- * refcounts through free, and the error statuses.  Exit status 0 when every
+ * refcounts through free, and the error statuses, the batched token append's
+ * short count among them.  Exit status 0 when every
  * check holds; the first failing check is printed. */
 #include <stdint.h>
 #include <stdio.h>
@@ -80,6 +81,22 @@ static int errors(void) {
   CHECK(pa_pool_free_seq(pool, s) == PA_ERR_NOT_FOUND);  /* no double free */
   CHECK(pa_pool_destroy(pool) == PA_OK);
   CHECK(pa_pool_create(4, 0, NULL, &pool) == PA_ERR_INVALID_ARG);
+
+  /* the batched token append: 6 tokens into a 1-block pool stop after 4 */
+  CHECK(pa_pool_create(1, 4, NULL, &pool) == PA_OK);
+  CHECK(pa_pool_new_seq(pool, &s) == PA_OK);
+  int32_t seqs[6], toks[6];
+  int64_t slots[6], pairs[12];
+  for (int t = 0; t < 6; ++t) { seqs[t] = s; toks[t] = 7 + t; }
+  int np = -1, done = -1;
+  CHECK(pa_pool_append_tokens(pool, seqs, toks, 6, slots, NULL, 6, &np, &done) ==
+        PA_ERR_INVALID_ARG);  /* pairs NULL with room claimed */
+  CHECK(pa_pool_append_tokens(pool, seqs, toks, 6, slots, pairs, 6, &np, &done) ==
+        PA_ERR_NO_BLOCKS);
+  CHECK(done == 4 && np == 0 && slots[0] == 0 && slots[3] == 3);
+  CHECK(pa_pool_append_tokens(pool, seqs, toks, 0, NULL, NULL, 0, &np, &done) == PA_OK &&
+        done == 0);
+  CHECK(pa_pool_destroy(pool) == PA_OK);
   return 0;
 }
 

@@ -8,7 +8,7 @@ import os
 import numpy as np
 import pytest
 
-from oracle.pool import BlockPool as ModelPool, NoBlocks
+from oracle.pool import BlockPool as ModelPool
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -16,11 +16,6 @@ def built():
     from pagedattention_decode_attention_gb300 import build, capi
     if not os.path.exists(capi.LIB_PATH):
         build.build()
-
-
-def _native_no_blocks(e):
-    from pagedattention_decode_attention_gb300.capi import PA_ERR_NO_BLOCKS, PagedAttnError
-    return isinstance(e, PagedAttnError) and e.status == PA_ERR_NO_BLOCKS
 
 
 def _stream(seed, n_requests):
@@ -38,9 +33,9 @@ def _stream(seed, n_requests):
     return reqs
 
 
-def _drive(pool, no_blocks, reqs, steps):
+def _drive(pool, reqs, steps):
     from pagedattention_decode_attention_gb300.batching import ContinuousBatcher
-    b = ContinuousBatcher(pool, 16, no_blocks, max_running=48)
+    b = ContinuousBatcher(pool, 16, max_running=48)
     reports, pending = [], list(reqs)
     arrivals = np.random.default_rng(len(reqs)).integers(0, 4, size=steps)
     tok = lambda r: (r.rid * 7919 + r.generated * 104729) % 50_000  # noqa: E731
@@ -72,8 +67,8 @@ def _pools(num_blocks, host_blocks, seed):
 def test_batcher_native_equals_model(seed, num_blocks, host_blocks):
     reqs = _stream(seed, 70)
     nat, mod = _pools(num_blocks, host_blocks, seed)
-    r_nat = _drive(nat, _native_no_blocks, reqs, 2000)
-    r_mod = _drive(mod, NoBlocks, reqs, 2000)
+    r_nat = _drive(nat, reqs, 2000)
+    r_mod = _drive(mod, reqs, 2000)
     assert r_nat == r_mod
     st = nat.stats()
     assert st == mod.stats()
@@ -84,7 +79,7 @@ def test_batcher_native_equals_model(seed, num_blocks, host_blocks):
 def test_batcher_under_pressure_preempts_and_evicts():
     reqs = _stream(4, 70)
     nat, mod = _pools(72, 48, 4)
-    reports = _drive(nat, _native_no_blocks, reqs, 4000)
+    reports = _drive(nat, reqs, 4000)
     assert any(r[3] for r in reports) and any(r[4] for r in reports)   # swaps out and in
     assert nat.stats()["evictions"] > 0
-    assert _drive(mod, NoBlocks, reqs, 4000) == reports
+    assert _drive(mod, reqs, 4000) == reports

@@ -204,6 +204,55 @@ def test_batched_append_matches_single():
     assert kids_a == kids_b
 
 
+
+def test_append_tokens_matches_model_through_exhaustion():
+    """The batched token append against the pool model, prefix cache on: a
+    prompt in one call, a fork, then alternating appends that copy the shared
+    partial block and run the pool dry part way through the batch.  Slots,
+    copy pairs, the count made, the tables and the cache keys agree; a second
+    prompt with the same tokens hits the blocks the appends keyed."""
+    order = np.random.default_rng(5).permutation(12)
+    nat, mod = native(12, 4, order), ModelPool(12, 4, order)
+    for pool in (nat, mod):
+        pool.enable_prefix_cache()
+    prompt = list(range(100, 110))                         # 2 full blocks + 2 tokens
+    out = []
+    for pool in (nat, mod):
+        a, _ = pool.new_seq_with_prompt(prompt)              # nothing cached yet
+        r0 = pool.append_tokens([a] * len(prompt), prompt)
+        b = pool.fork(a)
+        seqs = [a, b] * 20
+        toks = [200 + i for i in range(len(seqs))]
+        r1 = pool.append_tokens(seqs, toks)
+        tables = [pool.block_table(s) for s in (a, b)]
+        pool.free_seq(a)
+        pool.free_seq(b)
+        c, hit = pool.new_seq_with_prompt(prompt + [200, 202, 204])
+        out.append((r0, r1, tables, hit, pool.stats()))
+    (n0, n1, nt, nh, nst), (m0, m1, mt, mh, mst) = out
+    for n, m in ((n0, m0), (n1, m1)):
+        assert list(n[0]) == list(m[0])
+        assert [tuple(p) for p in n[1].tolist()] == [tuple(p) for p in m[1]]
+        assert n[2] == m[2]
+    assert n0[2] == len(prompt) and len(n0[1]) == 0
+    assert 0 < n1[2] < 40 and len(n1[1]) == 1                # ran dry part way; one copy
+    assert [(list(t), c) for t, c in nt] == [(list(t), c) for t, c in mt]
+    assert nh == mh == 12                                  # 3 keyed blocks of 4 (a's)
+    for k in ("free_blocks", "cached_blocks", "evictable_blocks", "cow_copies"):
+        assert nst[k] == mst[k], k
+
+
+def test_append_tokens_empty_and_bad_arguments():
+    pool = native(4, 4)
+    s = pool.new_seq()
+    slots, pairs, done = pool.append_tokens([], [])
+    assert (len(slots), len(pairs), done) == (0, 0, 0)
+    with pytest.raises(ValueError):
+        pool.append_tokens([s, s], [1])
+    from pagedattention_decode_attention_gb300.capi import PagedAttnError
+    with pytest.raises(PagedAttnError):
+        pool.append_tokens([s, 999], [1, 2])                # unknown sequence: not a short count
+
 def test_native_oslab_cow_example():
     g = golden("cow_examples.json")["oslab_block4"]
     pool = native(8, block_size=4)
