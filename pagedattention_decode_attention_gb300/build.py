@@ -3,7 +3,7 @@
 Each translation unit compiles in parallel, then one link step makes the shared
 library next to this file.  The CUDA runtime is linked statically, so the
 library loads on a machine without a GPU (the pool and symbol tests need that)
-and on the GPU machine alongside PyTorch's own runtime.
+and on a GPU machine alongside PyTorch's own runtime.
 
     python -m pagedattention_decode_attention_gb300.build [--force] [--verbose]
 """
