@@ -12,7 +12,8 @@ This driver exercises the pool the way a serving loop does -- admissions with
 prefix-cache hits, one token per running sequence per step, retirements,
 preemption by swapping out, resumption by swapping in -- and reports what the
 device kernels would need each step (slots, copy-on-write pairs, swap pairs).
-It only calls pool methods, so the native pool and a model pool with the same
+A prompt's appends, and a step's appends for all running sequences, each go
+to the pool in one ``append_tokens`` call.  It only calls pool methods, so the native pool and a model pool with the same
 methods can be driven by the same script and compared step by step.
 
 Policy (ours; the pages leave it to the product): first-come first-served

@@ -97,6 +97,22 @@ static int errors(void) {
   CHECK(pa_pool_append_tokens(pool, seqs, toks, 0, NULL, NULL, 0, &np, &done) == PA_OK &&
         done == 0);
   CHECK(pa_pool_destroy(pool) == PA_OK);
+
+  /* a copy pair with no room for it: refused before that append, the ones
+   * before it kept */
+  CHECK(pa_pool_create(4, 4, NULL, &pool) == PA_OK);
+  CHECK(pa_pool_new_seq(pool, &s) == PA_OK);
+  seqs[0] = seqs[1] = s;
+  CHECK(pa_pool_append_tokens(pool, seqs, toks, 2, slots, pairs, 0, &np, &done) == PA_OK &&
+        done == 2);
+  CHECK(pa_pool_fork(pool, s, &child) == PA_OK);
+  int32_t two[2] = {child, s};
+  CHECK(pa_pool_append_tokens(pool, two, toks, 2, slots, NULL, 0, &np, &done) ==
+        PA_ERR_INVALID_ARG);
+  CHECK(done == 0 && np == 0);
+  CHECK(pa_pool_append_tokens(pool, two, toks, 2, slots, pairs, 1, &np, &done) == PA_OK);
+  CHECK(done == 2 && np == 1);  /* the child copies; the parent then writes in place */
+  CHECK(pa_pool_destroy(pool) == PA_OK);
   return 0;
 }
 
