@@ -40,7 +40,22 @@ from .ops import (LayerCaches, Prepared, alloc_prefill_workspace, alloc_workspac
                   shared_prefix_workspace_size, prefill_workspace_size,
                   paged_attention_decode_plan, paged_attention_decode_run,
                   prepare_decode_append_run, prepare_decode_plan, prepare_decode_run,
-                  prepare_kv_append, workspace_size)
+                  paged_attention_decode_noalloc, prepare_kv_append, workspace_size)
 from .pool import BlockPool  # noqa: F401
+
+# the C entry points' own names for the calls above whose Python name is shorter
+paged_attention_decode_workspace_size = workspace_size
+paged_attention_decode_shared_prefix_workspace_size = shared_prefix_workspace_size
+paged_attention_decode_shared_prefix_plan = shared_prefix_plan
+paged_attention_decode_grouped_prefix_workspace_size = grouped_prefix_workspace_size
+paged_attention_decode_grouped_prefix_plan = grouped_prefix_plan
+paged_attention_prefill_workspace_size = prefill_workspace_size
+paged_attention_prefill_plan = prefill_plan
+
+
+def version() -> int:
+    """The library's ABI version (``pa_version``)."""
+    from . import capi
+    return int(capi.lib().pa_version())
 
 BLOCK_SIZE = 16

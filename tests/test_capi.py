@@ -46,8 +46,26 @@ def test_binding_declares_exactly_the_header(lib):
     assert set(capi.SIGNATURES) == declared_symbols()
 
 
+def test_python_binding_carries_every_entry_point_name():
+    """Each declared call has a Python function of the same name (without
+    ``pa_``; pool calls as ``BlockPool`` methods).  Pool creation and
+    destruction are the ``BlockPool`` constructor and finaliser; the error
+    string travels inside ``PagedAttnError``."""
+    import pagedattention_decode_attention_gb300 as pa
+    missing = []
+    for n in sorted(declared_symbols() - {"pa_pool_create", "pa_pool_destroy", "pa_last_error"}):
+        if n.startswith("pa_pool_"):
+            found = callable(getattr(pa.BlockPool, n[len("pa_pool_"):], None))
+        else:
+            found = callable(getattr(pa, n[len("pa_"):], None))
+        if not found:
+            missing.append(n)
+    assert not missing, missing
+
+
 def test_version(lib):
-    assert lib.pa_version() >= 100
+    import pagedattention_decode_attention_gb300 as pa
+    assert lib.pa_version() >= 100 and pa.version() == lib.pa_version()
 
 
 def test_workspace_size_is_host_only(lib):
