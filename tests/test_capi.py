@@ -159,3 +159,24 @@ def test_fused_cascade_runs_reject_on_host(lib):
     assert lib.pa_paged_attention_decode_shared_prefix_append_run(
         ptr, ptr, ptr, ptr, ptr, ptr, ptr, ptr, 9, 4, 32, 8, 128, 8, 64, 0.125, 2, ptr, ptr,
         1 << 30, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch):
+    """With the shared library absent every call raises: the pool, the
+    version query and the attention entry point.  Nothing falls back to a
+    host computation."""
+    import torch
+
+    import pagedattention_decode_attention_gb300 as pa
+    from pagedattention_decode_attention_gb300 import capi
+    monkeypatch.setattr(capi, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libpagedattn.so"))
+    monkeypatch.setattr(capi, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pa.BlockPool(4)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        pa.version()
+    q = torch.zeros(1, 4, 64)
+    kc = torch.zeros(2, 4, 16, 64)
+    with pytest.raises(Exception):
+        pa.paged_attention_decode(q, kc, kc.clone(), torch.zeros(1, 1, dtype=torch.int32),
+                                  torch.ones(1, dtype=torch.int32), 0.125)
