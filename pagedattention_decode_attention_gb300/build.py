@@ -40,7 +40,10 @@ def _flags(src: str) -> list[str]:
     common = ["-O3", "-std=c++17", "-I", INCLUDE, "-I", CSRC,
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
     if src.endswith(".cu"):
-        return common + ARCH + ["-lineinfo", "--expt-relaxed-constexpr", "-Xptxas", "-v"]
+        # PA_NVCC_EXTRA adds flags for a diagnostic build, e.g. -DPA_PROFILE_TIMES
+        # for the per-role wait counters (rebuild with --force to apply)
+        extra = os.environ.get("PA_NVCC_EXTRA", "").split()
+        return common + ARCH + ["-lineinfo", "--expt-relaxed-constexpr", "-Xptxas", "-v"] + extra
     return common + ["-x", "c++"]
 
 
