@@ -38,6 +38,10 @@ def replay(pool, ops, is_native):
             elif kind == "append":
                 slot, cow = pool.append_slot(op[1])
                 out.append(("append", slot, None if cow is None else tuple(int(x) for x in cow)))
+            elif kind == "tokens":
+                slots, pairs, done = pool.append_tokens(op[1], op[2])
+                out.append(("tokens", [int(x) for x in slots],
+                            [tuple(int(v) for v in p) for p in pairs], done))
             elif kind == "fork":
                 out.append(("fork", pool.fork(op[1])))
             elif kind == "share":
@@ -91,12 +95,19 @@ def random_script(gen, n_ops, model, swaps=False):
                 ops.append(("swapout", s))
                 model.swap_out(s)
             continue
-        if r < 14:
+        if r < 12:
             ops.append(("append", s))
             try:
                 model.append_slot(s)
             except NoBlocks:
                 pass
+        elif r < 14:                                  # a batch over resident sequences
+            resident = [x for x in live if not model.is_swapped(x)]
+            k = int(gen.integers(1, 7))
+            seqs = [resident[int(i)] for i in gen.integers(len(resident), size=k)]
+            toks = [int(t) for t in gen.integers(0, 50_000, size=k)]
+            ops.append(("tokens", seqs, toks))
+            model.append_tokens(seqs, toks)
         elif r < 16:
             ops.append(("fork", s))
             live.append(model.fork(s))
