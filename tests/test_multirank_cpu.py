@@ -90,3 +90,22 @@ def test_reference_arm_prints_one_complete_line(workload):
         assert key in line, key
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"]["workload"].startswith(workload.split("_")[0])
+
+
+def test_pool_churn_arms_drive_the_same_stream():
+    """``bench.py --workload pool_churn`` runs on the host alone; the native
+    pool and the oracle's model of it take the same steps on the same request
+    stream and end with the same prefix hits and evictions (CPU only)."""
+    lines = []
+    for extra in ([], ["--impl", "reference"]):
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "pool_churn",
+               "--steps", "1", "--warmup", "3"] + extra
+        out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+        assert out.returncode == 0, out.stderr[-2000:]
+        lines.append(json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1]))
+    nat, ref = lines
+    assert "impl" not in nat and ref["impl"] == "reference"
+    assert nat["steps"] == ref["steps"] > 0
+    for key in ("prefix_hit_tokens", "evictions"):
+        assert nat["config"][key] == ref["config"][key], key
+    assert nat["config"]["prefix_hit_tokens"] > 0
