@@ -652,7 +652,9 @@ PA_API int pa_pool_new_seq_with_prompt(pa_pool* pool, const int32_t* tokens, int
                                        int* hit_tokens);
 PA_API int pa_pool_append_token(pa_pool* pool, int seq, int32_t token, int64_t* slot,
                                 int64_t* cow_src, int64_t* cow_dst);
-/* Batched form of pa_pool_append_token: token tokens[i] appended to sequence
+/* Batched form of pa_pool_append_token, for a serving loop that adds one
+ * token to every running sequence each step ("留书阁 / knowledge-20" page,
+ * section on continuous batching): token tokens[i] appended to sequence
  * seqs[i] for i = 0, 1, ... in order (a sequence may repeat: a prompt's
  * tokens), slots to slots[], copy pairs appended to pairs[] (int64
  * [*num_pairs][2], capacity pair_cap; NULL only when pair_cap == 0).  Stops
