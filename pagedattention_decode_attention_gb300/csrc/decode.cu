@@ -1282,6 +1282,8 @@ int check_decode_shapes(int num_seqs, int num_q_heads, int num_kv_heads, int hea
                 num_q_heads / num_kv_heads, kMaxGroup);
   if (double(max_blocks_per_seq) * kBlockSize >= 2147483647.0)
     return fail(PA_ERR_INVALID_ARG, "%s: max_blocks_per_seq too large", who);
+  if (layout_too_large(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq))
+    return fail(PA_ERR_INVALID_ARG, "%s: these shapes need an impossibly large workspace", who);
   return PA_OK;
 }
 
@@ -1382,6 +1384,23 @@ int plan_impl(const int32_t* context_lens, int num_seqs, int num_q_heads, int nu
   return PA_OK;
 }
 
+// Host-side checks of the attention launch's own arguments.  Every one-shot
+// entry point runs them before its plan, so a call that is rejected leaves
+// the workspace untouched.
+int check_run_args(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, const int32_t* context_lens, const void* out,
+                   int num_kv_heads, int num_blocks, const char* who) {
+  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "%s: num_blocks must be positive", who);
+  if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
+    return fail(PA_ERR_INVALID_ARG, "%s: cache has too many rows", who);
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
+  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
+    return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
+  return PA_OK;
+}
+
 // The new tokens a fused call appends (all null: plain attention).
 struct AppendArgs {
   const void* k_new = nullptr;
@@ -1408,17 +1427,12 @@ int run_impl(const void* q, const void* k_cache, const void* v_cache, const int3
              void* out, void* workspace, size_t workspace_bytes, cudaStream_t stream,
              const char* who, const AppendArgs& app = AppendArgs(),
              const SuffixArgs& sfx = SuffixArgs()) {
-  if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "%s: num_blocks must be positive", who);
-  if (double(num_blocks) * num_kv_heads * kBlockSize >= 2147483647.0)
-    return fail(PA_ERR_INVALID_ARG, "%s: cache has too many rows", who);
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
-  auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) != 0; };
-  if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
-    return fail(PA_ERR_INVALID_ARG, "%s: tensors must be 16-byte aligned", who);
+  int rc = check_run_args(q, k_cache, v_cache, block_tables, context_lens, out, num_kv_heads,
+                          num_blocks, who);
+  if (rc != PA_OK) return rc;
   const Layout lay =
       workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
-  int rc = check_workspace(workspace, workspace_bytes, lay, who);
+  rc = check_workspace(workspace, workspace_bytes, lay, who);
   if (rc != PA_OK) return rc;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
@@ -1509,6 +1523,8 @@ PA_API int pa_paged_attention_decode_workspace_size(int num_seqs, int num_q_head
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG, "workspace_size: sizes must be positive");
+  if (layout_too_large(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq))
+    return fail(PA_ERR_INVALID_ARG, "workspace_size: these shapes need an impossibly large workspace");
   *bytes = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
   return PA_OK;
 }
@@ -1610,6 +1626,9 @@ PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_blocks_per_seq <= 0 || num_q_heads % num_kv_heads != 0)
     return fail(PA_ERR_INVALID_ARG, "shared_prefix_workspace_size: bad sizes");
+  if (layout_too_large(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq))
+    return fail(PA_ERR_INVALID_ARG,
+                "shared_prefix_workspace_size: these shapes need an impossibly large workspace");
   *bytes = shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
   return PA_OK;
 }
@@ -1643,6 +1662,11 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
   if (!context_lens) return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (runs) {
+    rc = check_run_args(q, k_cache, v_cache, block_tables, context_lens, out, num_kv_heads,
+                        num_blocks, who);
+    if (rc != PA_OK) return rc;
+  }
   if (prefix_blocks == 0 || dtype == PA_F32) {
     // nothing shared to exploit (or the fp32 path): a plain decode is exact
     if (plans && dtype != PA_F32) {
@@ -1755,8 +1779,6 @@ int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, con
   const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
   if (plans && (!context_lens || !block_tables))
     return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
-  if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
-    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1767,6 +1789,13 @@ int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, con
   int32_t* sfx_tables = reinterpret_cast<int32_t*>(ws + gl.sfx_tables);
   int32_t* sfx_ctx = reinterpret_cast<int32_t*>(ws + gl.sfx_ctx);
   int32_t* seq_blocks = reinterpret_cast<int32_t*>(ws + gl.seq_blocks);
+  if (runs) {
+    // the suffix decode reads the suffix lengths the plan writes (a run-only
+    // caller passes no context_lens)
+    rc = check_run_args(q, k_cache, v_cache, block_tables, sfx_ctx, out, num_kv_heads, num_blocks,
+                        who);
+    if (rc != PA_OK) return rc;
+  }
   SuffixArgs sfx;  // no offsets: the suffix decode reads the suffix tables
   sfx.cas_o = so;
   sfx.cas_lse = slse;
@@ -1967,6 +1996,14 @@ PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const v
                                dtype, who);
   if (rc != PA_OK || num_seqs == 0) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = check_run_args(q, k_cache, v_cache, block_tables, context_lens, out, num_kv_heads,
+                      num_blocks, who);
+  if (rc != PA_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes,
+                       workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                        max_blocks_per_seq),
+                       who);
+  if (rc != PA_OK) return rc;
   if (dtype != PA_F32) {
     rc = plan_impl(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                    workspace, workspace_bytes, s, who);
@@ -2034,6 +2071,11 @@ PA_API int pa_paged_attention_decode_noalloc(const void* q, const void* k_cache,
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG, "paged_attention_decode_noalloc: sizes must be positive");
+  if (layout_too_large(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq))
+    return fail(PA_ERR_INVALID_ARG,
+                "paged_attention_decode_noalloc: these shapes need far more than the library's "
+                "built-in scratch of %zu bytes",
+                kStaticScratchBytes);
   const size_t need =
       workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
   if (need > kStaticScratchBytes)

@@ -43,7 +43,7 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
                                int max_blocks_per_seq) {
   Layout l;
   // sized for the smallest split the plan may choose
-  l.max_splits = (max_blocks_per_seq + kMinSplitBlocks - 1) / kMinSplitBlocks;
+  l.max_splits = int((int64_t(max_blocks_per_seq) + kMinSplitBlocks - 1) / kMinSplitBlocks);
   if (l.max_splits < 1) l.max_splits = 1;
   const size_t units = size_t(num_seqs) * l.max_splits;
   l.header = 0;
@@ -54,6 +54,23 @@ inline Layout workspace_layout(int num_seqs, int num_q_heads, int num_kv_heads, 
   l.part_o = align256(l.part_lse + units * num_q_heads * 4);
   l.total = align256(l.part_o + units * num_q_heads * size_t(head_dim) * 4);
   return l;
+}
+
+// True when the workspace of these shapes (with the shared-prefix and
+// grouped additions on top) would come near the range of size_t.  The
+// layouts multiply the sizes in size_t, so such shapes are rejected before
+// any layout is computed; a real device holds far less than the 2^50 bytes
+// allowed here.
+inline bool layout_too_large(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int max_blocks_per_seq) {
+  const double splits = (double(max_blocks_per_seq) + kMinSplitBlocks - 1) / kMinSplitBlocks;
+  const double units = double(num_seqs) * (splits < 1.0 ? 1.0 : splits);
+  const double rows = double(num_seqs) * num_q_heads;
+  const double bytes = units * (16.0 + num_q_heads * (head_dim + 1.0) * 4.0) +
+                       double(num_seqs) * (num_kv_heads + 2.0) * 4.0 +
+                       double(num_seqs) * max_blocks_per_seq * 4.0 +
+                       16.0 * rows * (head_dim + 1.0) * 4.0 + 65536.0;
+  return bytes > double(uint64_t(1) << 50);
 }
 
 // Identifies the shapes a plan was made for, so a run can refuse a workspace

@@ -96,6 +96,44 @@ def test_decode_rejects_on_host(lib, kwargs, status):
     assert lib.pa_last_error()
 
 
+def test_workspace_sizes_refuse_overflowing_shapes(lib):
+    """Shapes whose workspace would wrap size_t arithmetic are refused, not
+    reported as a small size."""
+    out = C.c_size_t(0)
+    big = (1 << 31) - 1
+    assert lib.pa_paged_attention_decode_workspace_size(big, big, 1, 128, big, C.byref(out)) == 1
+    assert b"workspace" in lib.pa_last_error()
+    assert lib.pa_paged_attention_decode_shared_prefix_workspace_size(
+        big, 1024, 1, 128, 1 << 20, C.byref(out)) == 1
+    assert lib.pa_paged_attention_decode_grouped_prefix_workspace_size(
+        big, 64, 8, 128, 1 << 20, C.byref(out)) == 1
+    # the attention entry point refuses the same shapes before touching any pointer
+    assert lib.pa_paged_attention_decode(256, 256, 256, 256, 256, big, 64, 8, 128, 1 << 20, 64,
+                                         0.1, 2, 256, 256, 1 << 62, None) == 1
+
+
+def test_one_shot_decode_checks_every_pointer_before_its_plan(lib):
+    """A NULL query is refused on the host before the plan would be launched
+    (on a machine without a GPU a launch attempt reports PA_ERR_CUDA
+    instead), so a rejected call leaves the workspace untouched."""
+    rc = lib.pa_paged_attention_decode(None, 256, 256, 256, 256, 2, 4, 4, 64, 4, 8, 0.125, 2,
+                                       256, 256, 1 << 20, None)
+    assert rc == 1 and b"NULL" in lib.pa_last_error()
+    rc = lib.pa_paged_attention_decode(256, 256, 256 + 8, 256, 256, 2, 4, 4, 64, 4, 8, 0.125, 2,
+                                       256, 256, 1 << 20, None)
+    assert rc == 1 and b"aligned" in lib.pa_last_error()
+
+
+def test_noalloc_refuses_shapes_beyond_its_scratch_on_host(lib):
+    rc = lib.pa_paged_attention_decode_noalloc(None, None, None, None, None, 4096, 32, 8, 128,
+                                               4096, 100000, C.c_float(0.1), 2, None, None)
+    assert rc == 1 and b"built into the library" in lib.pa_last_error()
+    big = (1 << 31) - 1
+    rc = lib.pa_paged_attention_decode_noalloc(None, None, None, None, None, big, big, 8, 128,
+                                               big, 100000, C.c_float(0.1), 2, None, None)
+    assert rc == 1 and b"built-in scratch" in lib.pa_last_error()
+
+
 def test_empty_batches_are_noops(lib):
     assert lib.pa_kv_append(None, None, None, None, None, 0, 8, 128, 16, 2, None) == 0
     assert lib.pa_block_copy(None, None, 1, None, 0, 8, 128, 16, 2, None) == 0
