@@ -11,10 +11,12 @@ sharing a system prompt hit the prefix cache.
 This driver exercises the pool the way a serving loop does -- admissions with
 prefix-cache hits, one token per running sequence per step, retirements,
 preemption by swapping out, resumption by swapping in -- and reports what the
-device kernels would need each step (slots, copy-on-write pairs, swap pairs).
-A prompt's appends, and a step's appends for all running sequences, each go
-to the pool in one ``append_tokens`` call.  It only calls pool methods, so the native pool and a model pool with the same
-methods can be driven by the same script and compared step by step.
+device kernels would need each step (slots, copy-on-write pairs, swap pairs),
+also as one ordered list of device operations.  A prompt's appends, and a
+step's appends for all running sequences, each go to the pool in one
+``append_tokens`` call.  It only calls pool methods, so the native pool and a
+model pool with the same methods can be driven by the same script and
+compared step by step.
 
 Policy (ours; the pages leave it to the product): first-come first-served
 admission while the pool can hold the prompt's uncached blocks plus one; when
@@ -50,6 +52,16 @@ class StepReport:
     swap_in: list = field(default_factory=list)      # (seq, [(host, device), ...])
     retired: list = field(default_factory=list)      # request ids
     requeued: list = field(default_factory=list)     # request ids freed for recomputation
+    aborted: list = field(default_factory=list)      # (request id, seq): prompt did not fit
+    # The same work as an ordered list of device operations, in the order the
+    # device must apply them:
+    #   ("swap_in", seq, [(host, device), ...])
+    #   ("append", [(src, dst), ...], [(seq, slot, token, position), ...]):
+    #       the block copies first, then every token's K/V into its slot
+    #   ("swap_out", seq, [(device, host), ...])
+    # Order matters: a block freed by a swap-out can be handed to a later
+    # append of the same step.
+    ops: list = field(default_factory=list)
 
 
 class ContinuousBatcher:
@@ -88,7 +100,9 @@ class ContinuousBatcher:
             except Exception:  # noqa: BLE001  (shared or pinned blocks cannot leave)
                 pairs = None
             if pairs is not None:
-                rep.swap_out.append((victim.seq, [tuple(int(x) for x in p) for p in pairs]))
+                moved = [tuple(int(x) for x in p) for p in pairs]
+                rep.swap_out.append((victim.seq, moved))
+                rep.ops.append(("swap_out", victim.seq, moved))
                 self.swapped.append(victim)
                 return True
         self.pool.free_seq(victim.seq)
@@ -107,8 +121,9 @@ class ContinuousBatcher:
             table, _ = self.pool.block_table(req.seq)
             if self._free_blocks() < len(table) + 1:
                 break
-            pairs = self.pool.swap_in(req.seq)
-            rep.swap_in.append((req.seq, [tuple(int(x) for x in p) for p in pairs]))
+            pairs = [tuple(int(x) for x in p) for p in self.pool.swap_in(req.seq)]
+            rep.swap_in.append((req.seq, pairs))
+            rep.ops.append(("swap_in", req.seq, pairs))
             self.running.append(self.swapped.popleft())
         # admit waiting requests while their uncached blocks fit
         while self.waiting and len(self.running) < self.max_running and not self.swapped:
@@ -120,9 +135,16 @@ class ContinuousBatcher:
             req.seq, req.hit_tokens = seq, hit
             rest = req.prompt[hit:]
             slots, pairs, done = self.pool.append_tokens([seq] * len(rest), rest)
+            # Reported even when the prompt does not fit after all: every block
+            # the partial append filled was keyed into the prefix cache and
+            # stays there after the sequence is freed, so its K/V must be
+            # written for a later request that hits it.
             rep.slots.extend((seq, int(s)) for s in slots)
             rep.cow_pairs.extend((int(a), int(b)) for a, b in pairs)
+            rep.ops.append(("append", [(int(a), int(b)) for a, b in pairs],
+                            [(seq, int(s), rest[j], hit + j) for j, s in enumerate(slots)]))
             if done < len(rest):                         # cached blocks were evicted meanwhile
+                rep.aborted.append((req.rid, seq))
                 self.pool.free_seq(seq)
                 req.seq = -1
                 break
@@ -134,12 +156,15 @@ class ContinuousBatcher:
         i = 0
         while i < len(self.running):
             batch = self.running[i:]
-            slots, pairs, done = self.pool.append_tokens([r.seq for r in batch],
-                                                         [next_token(r) for r in batch])
-            for r, s in zip(batch[:done], slots):
+            tokens = [next_token(r) for r in batch]
+            slots, pairs, done = self.pool.append_tokens([r.seq for r in batch], tokens)
+            entries = []
+            for r, s, t in zip(batch[:done], slots, tokens):
+                entries.append((r.seq, int(s), t, len(r.prompt) + r.generated))
                 r.generated += 1
                 rep.slots.append((r.seq, int(s)))
             rep.cow_pairs.extend((int(a), int(b)) for a, b in pairs)
+            rep.ops.append(("append", [(int(a), int(b)) for a, b in pairs], entries))
             i += done
             if i < len(self.running):
                 req = self.running[i]
