@@ -35,7 +35,6 @@ import argparse  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
 import math  # noqa: E402
-import re  # noqa: E402
 import statistics  # noqa: E402
 import subprocess  # noqa: E402
 import sys  # noqa: E402
@@ -72,6 +71,8 @@ def parse_args():
                     help="override the workload's layer count (profiling at a small footprint)")
     ap.add_argument("--warmup-seconds", type=float, default=1.0,
                     help="keep warming up until this much wall time has passed")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload only: skip the other configurations' lines")
     ap.add_argument("--cascade", action="store_true",
                     help="prefix_8b / sampling_8b: time the (grouped) shared-prefix decode "
                          "against the plain one")
@@ -339,33 +340,32 @@ def copy_kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def _recorded_traffic(key: str, source_hash: str):
+    """DRAM bytes per launch (``dram__bytes_read.sum + dram__bytes_write.sum``)
+    of one kernel on one workload from the committed ncu record, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_RECORD):
+        return None
+    with open(TRAFFIC_RECORD) as f:
+        rec = json.load(f).get(key)
+    if not rec or rec.get("kernel_source_sha256_16") != source_hash:
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
 def profiled_copy_traffic():
     """Steady-state DRAM bytes per block_copy launch of the block_copy_8b
-    workload from the committed ncu summary, if it was taken on the current
-    kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", "block_copy_cow_divergence_8b.md")
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not val or src.group(1) != copy_kernel_source_hash():
-        return None
-    return float(val.group(1))
+    workload (current kernel source only)."""
+    return _recorded_traffic("block_copy_8b", copy_kernel_source_hash())
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_attention_{workload}.md")
-    if not os.path.exists(path):
-        return None
-    text = open(path).read()
-    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not src or not val or src.group(1) != kernel_source_hash():
-        return None
-    return float(val.group(1))
+    """DRAM bytes per attention launch of a decode workload (current kernel
+    source only)."""
+    return _recorded_traffic(f"decode_{workload}", kernel_source_hash())
 
 
 class ClockSampler:
@@ -750,27 +750,43 @@ def cpu_oracle_all_cores(batch: wl.DecodeBatch, inp: OracleInputs, seconds: floa
     return units / batch.num_layers / el, units, el, cores
 
 
-def run_ours(args):
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", init_method="env://")
-    device = torch.device("cuda", local if world > 1 else 0)
-    torch.cuda.set_device(device)
-    batch = make_batch(args.workload, rank)
-    if args.layers > 0:
-        batch.num_layers = args.layers
-    rep = Replica(batch, device)
-    # Warm-up: at least max(W, 3) steps and at least 1 s, so clocks have ramped.
+def decode_config(batch: wl.DecodeBatch, world: int) -> dict:
+    """The ``config`` of a decode line; the reference arm prints the same."""
+    ab = algorithmic_bytes(batch)
+    return {
+        "workload": batch.name, "num_seqs": batch.num_seqs,
+        "num_q_heads": batch.num_q_heads, "num_kv_heads": batch.num_kv_heads,
+        "head_dim": batch.head_dim, "block_size": 16, "layers": batch.num_layers,
+        "context_tokens": ab["tokens"], "num_blocks_per_layer": batch.num_blocks,
+        "l2": (f"inputs larger than L2: {ab['kv'] * batch.num_layers / 1e9:.2f} GB of KV "
+               f"read per step across {batch.num_layers} separate layer caches"),
+        "step": ("plan the work list once from the context lengths, then per layer one "
+                 "launch: kv_append of the new K/V rows fused with paged decode "
+                 "attention"),
+        "parallelism": f"replicas x{world} (independent batches, no collective)",
+    }
+
+
+def warm_up(step, requested: int, seconds: float, sync_every: int = 8) -> int:
+    """At least max(requested, 3) steps and at least ``seconds`` of wall time,
+    so the clocks have ramped; returns the steps run."""
     warm, t0 = 0, time.perf_counter()
-    while warm < max(args.warmup, 3) or time.perf_counter() - t0 < args.warmup_seconds:
-        rep.step()
+    while warm < max(requested, 3) or time.perf_counter() - t0 < seconds:
+        step()
         warm += 1
-        if warm % 8 == 0:
+        if warm % sync_every == 0:
             torch.cuda.synchronize()
-    rep.pa.check_status()
     torch.cuda.synchronize()
+    return warm
+
+
+def measure_decode(args, batch: wl.DecodeBatch, device, world: int, rank: int,
+                   cpu_seconds: float, all_cores: bool) -> dict:
+    """One decode workload measured the bench's way; returns its JSON line
+    (rank 0) or None."""
+    rep = Replica(batch, device)
+    warm = warm_up(rep.step, args.warmup, args.warmup_seconds)
+    rep.pa.check_status()
 
     clocks = ClockSampler(device)
     clocks.start()
@@ -799,7 +815,8 @@ def run_ours(args):
     events_ms = statistics.mean(per_launch)
     achieved = ab["total"] / (avg_ms / 1e3) / 1e9
     peak, peak_kind = load_peaks()
-    traffic = profiled_traffic(args.workload)
+    workload = next((k for k in ("mha_7b", "gqa_8b") if batch.name.startswith(k)), batch.name)
+    traffic = profiled_traffic(workload)
 
     e2e = None
     if not args.no_e2e:
@@ -815,40 +832,35 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inp = OracleInputs(batch, rep)
-        v1, units1, el1 = cpu_oracle_sample(batch, inp, args.cpu_seconds)
-        one = {"value": v1, "unit": "tokens/s", "cores": 1,
+        v1, units1, el1 = cpu_oracle_sample(batch, inp, cpu_seconds)
+        one = {"value": v1, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": (f"{units1} (sequence, layer) attention units of layer 0, all "
                           f"{batch.num_q_heads} query heads each, float64 numpy on 1 host "
                           f"thread in {el1:.1f} s; {batch.num_layers} units = 1 token")}
-        try:
-            vn, unitsn, eln, cores = cpu_oracle_all_cores(batch, inp, args.cpu_seconds)
-            cpu = {"value": vn, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                   "sample": (f"{unitsn} (sequence, layer) attention units of layer 0 on "
-                              f"{cores} single-threaded processes (one per host core) in "
-                              f"{eln:.1f} s; {batch.num_layers} units = 1 token"),
-                   "one_thread": one}
-        except Exception as exc:  # noqa: BLE001  (no room for the inputs, a worker died, timeout)
-            cpu = dict(one, kind="oracle", all_cores_unavailable=str(exc)[:200])
+        cpu = one
+        if all_cores:
+            try:
+                vn, unitsn, eln, cores = cpu_oracle_all_cores(batch, inp, cpu_seconds)
+                cpu = {"value": vn, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                       "sample": (f"{unitsn} (sequence, layer) attention units of layer 0 on "
+                                  f"{cores} single-threaded processes (one per host core) in "
+                                  f"{eln:.1f} s; {batch.num_layers} units = 1 token"),
+                       "one_thread": one}
+            except Exception as exc:  # noqa: BLE001  (no room for the inputs, a worker died, timeout)
+                cpu = dict(one, all_cores_unavailable=str(exc)[:200])
+        del inp
 
+    line = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": warm,
+            "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": warm,
+            "warmup_rule": (f"at least max(--warmup, 3) steps and at least "
+                            f"{args.warmup_seconds:g} s of wall time (clock ramp)"),
             "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
             "data": "synthetic (seeded N(0,1) K/V/Q, seeded lengths and placements)",
-            "config": {
-                "workload": batch.name, "num_seqs": batch.num_seqs,
-                "num_q_heads": batch.num_q_heads, "num_kv_heads": batch.num_kv_heads,
-                "head_dim": batch.head_dim, "block_size": 16, "layers": batch.num_layers,
-                "context_tokens": ab["tokens"], "num_blocks_per_layer": batch.num_blocks,
-                "l2": (f"inputs larger than L2: {ab['kv'] * batch.num_layers / 1e9:.2f} GB of KV "
-                       f"read per step across {batch.num_layers} separate layer caches"),
-                "step": ("plan the work list once from the context lengths, then per layer one "
-                         "launch: kv_append of the new K/V rows fused with paged decode "
-                         "attention"),
-                "parallelism": f"replicas x{world} (independent batches, no collective)",
-            },
+            "config": decode_config(batch, world),
             "kv_read_gbs": ab["kv"] / (avg_ms / 1e3) / 1e9,
             "kv_read_gbs_unique": unique_kv_bytes(batch) / (avg_ms / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -876,6 +888,34 @@ def run_ours(args):
             "host_ms_per_step": host_secs / args.steps * 1e3,
             "clocks": clk,
         }
+    del rep
+    torch.cuda.empty_cache()
+    return line
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    batch = make_batch(args.workload, rank)
+    if args.layers > 0:
+        batch.num_layers = args.layers
+    line = measure_decode(args, batch, device, world, rank, args.cpu_seconds, all_cores=True)
+    if (line is not None and world == 1 and args.workload == "mha_7b" and args.layers == 0
+            and not args.no_secondary):
+        # the other configurations, each timed the same way in the same run
+        sec_cpu = min(args.cpu_seconds, 3.0)
+        line["secondary"] = {
+            "gqa_8b": measure_decode(args, make_batch("gqa_8b", 0), device, 1, 0, sec_cpu,
+                                     all_cores=False),
+            "sampling_8b_grouped_cascade": measure_cascade(args, "sampling_8b", device, sec_cpu),
+            "prefix_8b_cascade": measure_cascade(args, "prefix_8b", device, sec_cpu),
+        }
+    if line is not None:
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -883,7 +923,25 @@ def run_ours(args):
 
 
 # ---------------------------------------------------------------- reference
+def cascade_config(batch: wl.DecodeBatch) -> dict:
+    """The ``config`` of a cascade line; the reference arm prints the same."""
+    grouped = "group_start" in batch.extra
+    return {"workload": batch.name, "num_seqs": batch.num_seqs, "layers": batch.num_layers,
+            "prefix_blocks": (int(batch.extra["group_blocks"].min()) if grouped
+                              else batch.extra["prefix_blocks"]),
+            "context_tokens": int(batch.context_lens.sum()),
+            "groups": len(batch.extra["group_start"]) - 1 if grouped else 1,
+            "step": "one plan, then per layer: append the new tokens' K/V and attend"}
+
+
 def run_cascade_bench(args):
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    print(json.dumps(measure_cascade(args, args.workload, device, args.cpu_seconds / 2,
+                                     layers=args.layers)))
+
+
+def measure_cascade(args, workload: str, device, cpu_seconds: float, layers: int = 0) -> dict:
     """Shared-prefix (cascade) decode beside the plain decode of the same
     batch: the prefix-mix batch (one prefix for the whole batch) or the
     parallel-sampling batch (grouped: each prompt's branches share their
@@ -892,11 +950,9 @@ def run_cascade_bench(args):
     path in one launch; the cascade path as its prefix phase, the suffix
     decode that also stores the new rows, and the combine)."""
     import pagedattention_decode_attention_gb300 as pa
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
-    batch = make_batch(args.workload, 0)
-    if args.layers > 0:
-        batch.num_layers = args.layers
+    batch = make_batch(workload, 0)
+    if layers > 0:
+        batch.num_layers = layers
     rep = Replica(batch, device)
     grouped = "group_start" in batch.extra
     L = batch.num_layers
@@ -926,10 +982,10 @@ def run_cascade_bench(args):
                     rep.q[i], rep.k_new[i], rep.v_new[i], rep.slots, rep.k_cache[i],
                     rep.v_cache[i], rep.tables, rep.lens, P, batch.scale, ws, out=rep.out[i])
 
+    warm = []
+
     def timed(step):
-        for _ in range(max(args.warmup, 3)):
-            step()
-        torch.cuda.synchronize()
+        warm.append(warm_up(step, args.warmup, args.warmup_seconds))
         pa.check_status()
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         start.record()
@@ -955,13 +1011,11 @@ def run_cascade_bench(args):
         "metric": ("decode tokens/s, grouped shared-prefix (cascade) path, 1 GPU" if grouped
                    else "decode tokens/s, shared-prefix (cascade) path, 1 GPU"),
         "value": batch.num_seqs / cascade_s, "unit": "tokens/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": cascade_s * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "warmup_steps_run": warm[-1],
+        "ms_per_step": cascade_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": batch.dtype,
         "data": "synthetic (seeded N(0,1) Q/K/V; seeded lengths and pool tables)",
-        "config": {"workload": batch.name, "num_seqs": batch.num_seqs, "layers": L,
-                   "prefix_blocks": P, "context_tokens": int(batch.context_lens.sum()),
-                   "groups": len(batch.extra["group_start"]) - 1 if grouped else 1,
-                   "step": "one plan, then per layer: append the new tokens' K/V and attend"},
+        "config": cascade_config(batch),
         "roofline": {"bound": "hbm", "achieved": uniq / (cascade_s / L) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": uniq / (cascade_s / L) / 1e9 / peak,
                      "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
@@ -977,11 +1031,13 @@ def run_cascade_bench(args):
     }
     if not args.no_cpu_baseline:
         # the oracle computes the same attention (the cascade is exact)
-        v, units, _ = cpu_oracle_sample(batch, OracleInputs(batch, rep), args.cpu_seconds / 2)
+        v, units, _ = cpu_oracle_sample(batch, OracleInputs(batch, rep), cpu_seconds)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": (f"{units} (sequence, layer) units of layer 0, float64 "
                                            f"numpy, 1 thread; {L} units = 1 token")}
-    print(json.dumps(line))
+    del rep, ws
+    torch.cuda.empty_cache()
+    return line
 
 
 def run_swap_bench(args):
@@ -1496,19 +1552,19 @@ def run_reference(args):
     value = units / batch.num_layers / secs
     # with --cascade the measured arm reports the cascade metric; the oracle
     # computes the same attention either way (the cascade is exact)
-    metric = METRIC
+    metric, config = METRIC, decode_config(batch, world)
     if args.cascade and args.workload in ("prefix_8b", "sampling_8b"):
         metric = ("decode tokens/s, grouped shared-prefix (cascade) path, 1 GPU"
                   if "group_start" in batch.extra
                   else "decode tokens/s, shared-prefix (cascade) path, 1 GPU")
+        config = cascade_config(batch)
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": "tokens/s",
-        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "warmup_steps_run": max(args.warmup, 3),
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": batch.name, "num_seqs": batch.num_seqs,
-                   "num_q_heads": batch.num_q_heads, "num_kv_heads": batch.num_kv_heads,
-                   "head_dim": batch.head_dim, "block_size": 16, "layers": batch.num_layers},
+        "config": config,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": (f"each step: {per_step_units} (sequence, layer) units "
                                     "(one token) of the workload, float64 numpy, 1 thread")},

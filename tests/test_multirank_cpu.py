@@ -109,3 +109,23 @@ def test_pool_churn_arms_drive_the_same_stream():
     for key in ("prefix_hit_tokens", "evictions"):
         assert nat["config"][key] == ref["config"][key], key
     assert nat["config"]["prefix_hit_tokens"] > 0
+
+
+@pytest.mark.parametrize("workload,cascade", [("mha_7b", False), ("gqa_8b", False),
+                                              ("sampling_8b", True)])
+def test_reference_arm_config_and_warmup_match_the_measured_arm(workload, cascade):
+    """The reference arm prints the measured arm's ``config`` (built by the
+    same function from the same batch) and the requested warm-up count."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           workload, "--steps", "1", "--warmup", "4"] + (["--cascade"] if cascade else [])
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][-1])
+    batch = bench.make_batch(workload, 0, model_pool=True)
+    want = bench.cascade_config(batch) if cascade else bench.decode_config(batch, 1)
+    assert line["config"] == json.loads(json.dumps(want))
+    assert line["warmup"] == 4 and line["steps"] == 1
