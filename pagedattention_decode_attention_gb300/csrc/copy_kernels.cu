@@ -19,6 +19,7 @@
 #include <mutex>
 
 #include "device_common.cuh"
+#include "trace.h"
 #include "pagedattn.h"
 #include "status.h"
 
@@ -171,6 +172,7 @@ extern "C" {
 PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cache,
                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
                         int head_dim, int num_blocks, int dtype, void* stream) {
+  PA_TRACE("pa_kv_append");
   int rc = check_common(dtype, head_dim, num_kv_heads, num_blocks, "kv_append");
   if (rc != PA_OK) return rc;
   if (num_tokens < 0) return fail(PA_ERR_INVALID_ARG, "kv_append: num_tokens < 0");
@@ -207,6 +209,7 @@ PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cac
 PA_API int pa_block_copy(void* const* k_caches, void* const* v_caches, int num_layers,
                          const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads,
                          int head_dim, int num_blocks, int dtype, void* stream) {
+  PA_TRACE("pa_block_copy");
   int rc = check_common(dtype, head_dim, num_kv_heads, num_blocks, "block_copy");
   if (rc != PA_OK) return rc;
   if (num_pairs < 0 || num_layers < 0 || num_layers > kMaxLayers)
@@ -245,6 +248,7 @@ PA_API int pa_block_swap(void* const* dev_k_caches, void* const* dev_v_caches,
                          const int64_t* pairs, int num_pairs, int direction, int num_kv_heads,
                          int head_dim, int num_dev_blocks, int num_host_blocks, int dtype,
                          void* stream) {
+  PA_TRACE("pa_block_swap");
   int rc = check_common(dtype, head_dim, num_kv_heads, num_dev_blocks, "block_swap");
   if (rc != PA_OK) return rc;
   if (num_host_blocks <= 0 || num_pairs < 0 || num_layers < 0 || num_layers > kMaxLayers ||

@@ -41,6 +41,7 @@
 #include <type_traits>
 
 #include "device_common.cuh"
+#include "trace.h"
 #include "pagedattn.h"
 #include "prefill.h"
 #include "tc05.cuh"
@@ -1804,6 +1805,7 @@ PA_API int pa_paged_attention_prefill(const void* q, const void* k_cache, const 
                                       int max_blocks_per_seq, int num_blocks, float scale,
                                       int dtype, void* out, void* workspace,
                                       size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_prefill");
   return pa::prefill::prefill_entry(pa::prefill::Mode::kPlanAndRun, q, k_cache, v_cache,
                                     block_tables, context_lens, query_start, num_seqs, total_q,
                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
@@ -1817,6 +1819,7 @@ PA_API int pa_paged_attention_prefill_plan(const int32_t* context_lens,
                                            int head_dim, int max_blocks_per_seq, float scale,
                                            int dtype, void* workspace, size_t workspace_bytes,
                                            void* stream) {
+  PA_TRACE("pa_paged_attention_prefill_plan");
   return pa::prefill::prefill_entry(pa::prefill::Mode::kPlanOnly, nullptr, nullptr, nullptr,
                                     nullptr, context_lens, query_start, num_seqs, total_q,
                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0,
@@ -1831,6 +1834,7 @@ PA_API int pa_paged_attention_prefill_run(const void* q, const void* k_cache, co
                                           int max_blocks_per_seq, int num_blocks, float scale,
                                           int dtype, void* out, void* workspace,
                                           size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_prefill_run");
   return pa::prefill::prefill_entry(pa::prefill::Mode::kRunOnly, q, k_cache, v_cache,
                                     block_tables, context_lens, query_start, num_seqs, total_q,
                                     num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
