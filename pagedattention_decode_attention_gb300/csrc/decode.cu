@@ -58,6 +58,7 @@
 #include <type_traits>
 
 #include "decode.cuh"
+#include "trace.h"
 #include "device_common.cuh"
 #include "pagedattn.h"
 #include "prefill.h"
@@ -105,8 +106,11 @@ struct Smem {
   static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, head) tile
   static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
   // one warp's staging buffer: its item's query rows, then the new token's
-  // K row and V row when the item carries the append
-  static constexpr int kQBytes = kMaxGroup * D * 2 + 2 * D * 2;
+  // K row and V row when the item carries the append.  Query rows are kQRow
+  // elements apart (16 bytes of padding), so the lanes that read the same
+  // head_dim columns of different rows hit different banks.
+  static constexpr int kQRow = D + 8;
+  static constexpr int kQBytes = kMaxGroup * kQRow * 2 + 2 * D * 2;
   // layout: rings [W][stages][stage] | query buffers [W] | barriers [W][stages + 1]
   static constexpr size_t kFixedBytes =
       1024 /* alignment slack */ + size_t(W) * kQBytes + size_t(W) * (kWarpStages + 1) * 8;
@@ -619,21 +623,21 @@ __global__ void __launch_bounds__(W * 32)
       // the G query rows of (b, g) (and the new K/V row) go to this warp's
       // staging buffer, which the current item no longer reads: its rows are
       // in registers
-      if (lane == 0) {
-        const uint32_t qbytes = uint32_t(G) * D * 2;
-        const uint32_t rbytes = nxt.slot >= 0 ? 2u * D * 2 : 0u;
-        dev::mbar_arrive_expect_tx(my_q, qbytes + rbytes);
-        dev::bulk_load(qbuf,
+      const uint32_t rbytes = nxt.slot >= 0 ? 2u * D * 2 : 0u;
+      if (lane == 0) dev::mbar_arrive_expect_tx(my_q, uint32_t(G) * D * 2 + rbytes);
+      __syncwarp();
+      // lane h copies query row h into its padded row of the buffer
+      if (lane < G)
+        dev::bulk_load(qbuf + lane * S::kQRow,
                        static_cast<const uint8_t*>(p.q) +
-                           (size_t(nxt.b) * Hq + size_t(nxt.g) * G) * D * 2,
-                       qbytes, my_q);
-        if (rbytes) {
-          const size_t row = (size_t(nxt.b) * Hkv + nxt.g) * D * 2;
-          dev::bulk_load(qbuf + kMaxGroup * D, static_cast<const uint8_t*>(p.k_new) + row, D * 2,
-                         my_q);
-          dev::bulk_load(qbuf + kMaxGroup * D + D, static_cast<const uint8_t*>(p.v_new) + row,
-                         D * 2, my_q);
-        }
+                           (size_t(nxt.b) * Hq + size_t(nxt.g) * G + lane) * D * 2,
+                       D * 2, my_q);
+      if (rbytes && lane == 0) {
+        const size_t row = (size_t(nxt.b) * Hkv + nxt.g) * D * 2;
+        dev::bulk_load(qbuf + kMaxGroup * S::kQRow, static_cast<const uint8_t*>(p.k_new) + row,
+                       D * 2, my_q);
+        dev::bulk_load(qbuf + kMaxGroup * S::kQRow + D,
+                       static_cast<const uint8_t*>(p.v_new) + row, D * 2, my_q);
       }
       ++q_issued;
       cstage = 4;
@@ -713,7 +717,7 @@ __global__ void __launch_bounds__(W * 32)
     {
       const int hq = lane >> 2;
       const int n0 = 2 * (lane & 3);
-      const uint16_t* qrow = qbuf + hq * D + n0;
+      const uint16_t* qrow = qbuf + hq * S::kQRow + n0;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
         qb0[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk) : 0u;
@@ -724,7 +728,7 @@ __global__ void __launch_bounds__(W * 32)
     // or V row; they go to the cache slot now and into the tile at the last block
     uint4 nkv = make_uint4(0, 0, 0, 0);
     if (cur.slot >= 0 && lane < D / 4) {
-      nkv = *reinterpret_cast<const uint4*>(qbuf + kMaxGroup * D + lane * 8);
+      nkv = *reinterpret_cast<const uint4*>(qbuf + kMaxGroup * S::kQRow + lane * 8);
       const bool isv = lane >= D / 8;
       const int c = isv ? lane - D / 8 : lane;
       const size_t dst = ((size_t(cur.slot / kBlockSize) * Hkv + g) * kBlockSize +
@@ -1533,6 +1537,7 @@ PA_API int pa_paged_attention_decode_plan(const int32_t* context_lens, int num_s
                                           int num_q_heads, int num_kv_heads, int head_dim,
                                           int max_blocks_per_seq, void* workspace,
                                           size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_plan");
   const char* who = "paged_attention_decode_plan";
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                PA_BF16, who);
@@ -1547,6 +1552,7 @@ PA_API int pa_paged_attention_decode_run(const void* q, const void* k_cache, con
                                          int head_dim, int max_blocks_per_seq, int num_blocks,
                                          float scale, int dtype, void* out, void* workspace,
                                          size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_run");
   const char* who = "paged_attention_decode_run";
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
@@ -1562,6 +1568,7 @@ PA_API int pa_paged_attention_decode_append_run(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,
     int num_blocks, float scale, int dtype, void* out, void* workspace, size_t workspace_bytes,
     void* stream) {
+  PA_TRACE("pa_paged_attention_decode_append_run");
   const char* who = "paged_attention_decode_append_run";
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
@@ -1876,6 +1883,7 @@ PA_API int pa_paged_attention_decode_shared_prefix(
     const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_shared_prefix");
   return shared_prefix_impl(SharedMode::kPlanAndRun, q, k_cache, v_cache, block_tables,
                             context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
@@ -1887,6 +1895,7 @@ PA_API int pa_paged_attention_decode_shared_prefix_plan(
     const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
     void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_shared_prefix_plan");
   return shared_prefix_impl(SharedMode::kPlanOnly, nullptr, nullptr, nullptr, nullptr,
                             context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, max_blocks_per_seq, 0, scale, dtype, nullptr, workspace,
@@ -1898,6 +1907,7 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
     const int32_t* context_lens, int prefix_blocks, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_shared_prefix_run");
   return shared_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables,
                             context_lens, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
                             head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
@@ -1922,6 +1932,7 @@ PA_API int pa_paged_attention_decode_grouped_prefix(
     int num_groups, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
     size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_grouped_prefix");
   return grouped_prefix_impl(SharedMode::kPlanAndRun, q, k_cache, v_cache, block_tables,
                              context_lens, group_start, group_prefix_blocks, num_groups, num_seqs,
                              num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, num_blocks,
@@ -1934,6 +1945,7 @@ PA_API int pa_paged_attention_decode_grouped_prefix_plan(
     const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int max_blocks_per_seq, float scale, int dtype,
     void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_grouped_prefix_plan");
   return grouped_prefix_impl(SharedMode::kPlanOnly, nullptr, nullptr, nullptr, block_tables,
                              context_lens, group_start, group_prefix_blocks, num_groups, num_seqs,
                              num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq, 0, scale,
@@ -1946,6 +1958,7 @@ PA_API int pa_paged_attention_decode_grouped_prefix_run(
     const int32_t* group_start, const int32_t* group_prefix_blocks, int num_groups, int num_seqs,
     int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks,
     float scale, int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_grouped_prefix_run");
   return grouped_prefix_impl(SharedMode::kRunOnly, q, k_cache, v_cache, block_tables, nullptr,
                              group_start, group_prefix_blocks, num_groups, num_seqs, num_q_heads,
                              num_kv_heads, head_dim, max_blocks_per_seq, num_blocks, scale, dtype,
@@ -1959,6 +1972,7 @@ PA_API int pa_paged_attention_decode_shared_prefix_append_run(
     int prefix_blocks, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* out, void* workspace,
     size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_shared_prefix_append_run");
   const char* who = "paged_attention_decode_shared_prefix_append_run";
   AppendArgs app;
   int rc = append_args(k_new, v_new, slot_mapping, app, who);
@@ -1975,6 +1989,7 @@ PA_API int pa_paged_attention_decode_grouped_prefix_append_run(
     const int32_t* group_prefix_blocks, int num_groups, int num_seqs, int num_q_heads,
     int num_kv_heads, int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
     int dtype, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_grouped_prefix_append_run");
   const char* who = "paged_attention_decode_grouped_prefix_append_run";
   AppendArgs app;
   int rc = append_args(k_new, v_new, slot_mapping, app, who);
@@ -1991,6 +2006,7 @@ PA_API int pa_paged_attention_decode(const void* q, const void* k_cache, const v
                                      int max_blocks_per_seq, int num_blocks, float scale, int dtype,
                                      void* out, void* workspace, size_t workspace_bytes,
                                      void* stream) {
+  PA_TRACE("pa_paged_attention_decode");
   const char* who = "paged_attention_decode";
   int rc = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
                                dtype, who);
@@ -2068,6 +2084,7 @@ PA_API int pa_paged_attention_decode_noalloc(const void* q, const void* k_cache,
                                              int num_q_heads, int num_kv_heads, int head_dim,
                                              int max_blocks_per_seq, int num_blocks, float scale,
                                              int dtype, void* out, void* stream) {
+  PA_TRACE("pa_paged_attention_decode_noalloc");
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
       max_blocks_per_seq <= 0)
     return fail(PA_ERR_INVALID_ARG, "paged_attention_decode_noalloc: sizes must be positive");
