@@ -227,7 +227,10 @@ PA_API int pa_paged_attention_decode_append_run(
  * * 16 (a violation sets PA_ERR_DEVICE_BOUNDS; that sequence's output is then
  * unspecified).  Three phases on `stream`: the prefix (all queries against
  * the shared blocks, a CTA-shared K/V ring, tensor cores), each sequence's
- * own blocks (the decode kernel), and a log-sum-exp merge.  Workspace:
+ * own blocks (the decode kernel), and a log-sum-exp merge.  (With the
+ * environment variable PA_CASCADE=grouped, read once per process, it runs
+ * as the one-group case of pa_paged_attention_decode_grouped_prefix
+ * instead.)  Workspace:
  * pa_paged_attention_decode_shared_prefix_workspace_size bytes.
  * prefix_blocks == 0 or F32 runs a plain decode.
  * ---------------------------------------------------------------------- */
@@ -306,15 +309,21 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
  * aligned).
  *
  * _plan (block_tables, context_lens and the group arrays; once per decode
- * step) writes each sequence's table past its group's prefix and the plans
- * of the prefix phase and the suffix decode into the workspace; _run (per
- * layer, same sizes and arrays, same workspace, stream order) launches the
- * prefix phase, the suffix decode and the combine.  In a run whose
- * workspace holds no plan for its sizes the attention kernels do nothing
- * and set the status word (PA_ERR_INVALID_ARG), and out is unspecified;
- * tables or lengths changed after the plan are not detected and give
- * unspecified output.  The one-shot entry is _plan then
- * _run.
+ * step) checks the groups and writes the work list into the workspace; _run
+ * (per layer, same sizes and arrays, same workspace, stream order) launches
+ * the attention and then the merge of each sequence's splits.  The work list
+ * has units of two kinds: a split of a group's shared blocks for up to 16
+ * query rows of its members (16 / (num_q_heads / num_kv_heads) members,
+ * every shared block read once for them), and a split of one sequence's
+ * blocks past the shared ones; a chunk of at most 4 members with at most 16
+ * blocks of its own in all takes those into its last shared split instead.
+ * (With the environment variable PA_CASCADE=phases, read once per process,
+ * the entry points use the three launches of the single-prefix form
+ * instead: prefix phase, suffix decode, combine.)  In a run whose workspace
+ * holds no plan for its sizes the attention kernel does nothing and sets
+ * the status word (PA_ERR_INVALID_ARG), and out is unspecified; tables or
+ * lengths changed after the plan are not detected and give unspecified
+ * output.  The one-shot entry is _plan then _run.
  * ---------------------------------------------------------------------- */
 PA_API int pa_paged_attention_decode_grouped_prefix_workspace_size(
     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq,

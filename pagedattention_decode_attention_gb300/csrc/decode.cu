@@ -54,6 +54,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -101,16 +102,18 @@ __device__ unsigned long long g_item_trace[2048 * 16 * 16 * 4];
 #define ITEM_TRACE(n, start, blocks, splits, merge_ns, qwait_ns)
 #endif
 
-template <int D, int W>
+template <int D, int W, int NT>
 struct Smem {
   static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, head) tile
   static constexpr int kStageBytes = 2 * kTileBytes;     // K tile + V tile
-  // one warp's staging buffer: its item's query rows, then the new token's
-  // K row and V row when the item carries the append.  Query rows are kQRow
-  // elements apart (16 bytes of padding), so the lanes that read the same
-  // head_dim columns of different rows hit different banks.
-  static constexpr int kQRow = D + 8;
-  static constexpr int kQBytes = kMaxGroup * kQRow * 2 + 2 * D * 2;
+  // one warp's staging buffer: its item's query rows (up to 8 NT), and the
+  // new token's K row and V row when the item carries the append (after row
+  // 7: an item with an append has at most 8 query rows).  With one row tile
+  // the rows are kQRow elements apart (16 bytes of padding), so the lanes
+  // that read the same head_dim columns of different rows hit different
+  // banks; with two the padding would cost the third ring stage.
+  static constexpr int kQRow = NT == 1 ? D + 8 : D;
+  static constexpr int kQBytes = NT == 1 ? (8 * kQRow + 2 * D) * 2 : 16 * kQRow * 2;
   // layout: rings [W][stages][stage] | query buffers [W] | barriers [W][stages + 1]
   static constexpr size_t kFixedBytes =
       1024 /* alignment slack */ + size_t(W) * kQBytes + size_t(W) * (kWarpStages + 1) * 8;
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
   __syncthreads();
 
   // pass 3: place every unit of a sequence, in block order, into its size's
-  // bucket: (b, first block, split index << 8 | blocks, context length)
+  // bucket: (b, first block, split index << 16 | blocks, context length)
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx = p.context_lens[b] - p.ctx_offset;
     ctx = ctx < 0 ? 0 : (ctx > cap ? cap : ctx);
@@ -258,10 +261,397 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
       for (int j = 0; j < np; ++j) {
         const int sz = j < pr ? pb + 1 : pb;
         const int pos = j < pr ? at[k][0]++ : at[k][1]++;
-        units[pos] = make_int4(b, first, (si << 8) | sz, ctx);
+        units[pos] = make_int4(b, first, (si << 16) | sz, ctx);
         first += sz;
         ++si;
       }
+    }
+  }
+}
+
+// ------------------------------------------------------------ grouped plan
+// A grouped decode's batch is made of groups of consecutive sequences whose
+// tables start with the same blocks (the branches of a forked prompt, the
+// requests on one system prompt: "vLLM: treating the KV cache as virtual
+// memory", section 碎片从哪里来, and the OS-lab appendix, section 4.3, where
+// forked tables point at the same blocks).  The plan makes two kinds of
+// unit: a shared unit covers a split of a group's shared blocks for up to
+// `chunk` members at once (their m * G query rows read every block once),
+// and an own unit a split of one sequence's blocks past the shared ones.  A
+// sequence's splits are its group's shared splits (indices 0 ..) followed by
+// its own; the warp that completes the last of them merges them, as in the
+// plain decode, so the whole cascade is one attention launch.
+struct GroupArgs {
+  const int32_t* group_start;   // [num_groups + 1], or null: one group of every sequence
+  const int32_t* group_blocks;  // [num_groups] shared blocks, or null: single_blocks
+  int num_groups;
+  int single_blocks;
+  int chunk;                    // most members of one shared unit
+  int nwarps;                   // math warps of the attention launch
+  int32_t* gp;                  // workspace [num_groups]: shared blocks that passed the checks
+  int32_t* seq_prefix;          // workspace [num_seqs]: each sequence's shared blocks
+  int32_t* seq_ctx;             // workspace [num_seqs]: context lengths, clamped
+  int32_t* seq_group;           // workspace [num_seqs]: each sequence's group
+  int2* seq_chunk;              // workspace [num_seqs]: its chunk's first member, members
+  int4* chunk_plan;             // workspace [num_seqs]: at a chunk's first member, its cut
+                                //   (absorbs, own blocks absorbed, shared splits, last shared)
+};
+
+__device__ __forceinline__ int group_of(const GroupArgs& ga, int b) {
+  if (!ga.group_start) return 0;
+  int lo = 0, hi = ga.num_groups - 1;  // the last g with group_start[g] <= b
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ga.group_start[mid] <= b) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// A chunk of at most kAbsorbMembers members whose blocks past the shared
+// ones add up to at most kAbsorbBlocks takes them into its last shared unit:
+// one unit then covers the chunk's last shared blocks (every row) and each
+// member's own blocks (its rows only), so the members need no units of their
+// own, all of them have the same splits, and the chunk's splits are counted
+// and merged together.
+constexpr int kAbsorbMembers = 4;
+constexpr int kAbsorbBlocks = 16;
+// flags in the blocks byte of a unit (blocks <= 32 use bits 0-5)
+constexpr int kUnitChunk = 0x40;  // the chunk's splits are counted and merged together
+constexpr int kUnitOwn = 0x80;    // the unit also covers the members' own blocks
+constexpr int kUnitBlocks = 0x3f;
+
+struct ChunkPlan {
+  bool absorb;
+  int own;          // absorbed: the members' own blocks in all
+  int ns;           // shared splits (absorbed: the last one carries the own blocks)
+  int last_shared;  // absorbed: shared blocks of the last split
+};
+
+// Parts that `total` blocks are cut into for units of about sp (>= 16)
+// blocks: rounded down, so that the units are no more than the math warps
+// (one wave), and no part above 32 blocks.
+__device__ __forceinline__ int shared_parts(int total, int sp) {
+  int n = total / sp;
+  const int at_most_32 = (total + kSplitBlocks - 1) / kSplitBlocks;
+  if (n < at_most_32) n = at_most_32;
+  return n < 1 ? 1 : n;
+}
+
+// Balanced parts: n parts of `total` blocks, the first `big` one larger.
+__device__ __forceinline__ void parts_shape(int total, int n, int& base, int& big) {
+  base = n ? total / n : 0;
+  big = n ? total - base * n : 0;
+}
+
+// How the chunk of m members from b0, sharing P blocks, is cut (shared
+// splits of about sp blocks).
+__device__ __forceinline__ ChunkPlan plan_chunk(const GroupArgs& ga, int b0, int m, int P,
+                                                int sp) {
+  ChunkPlan c;
+  c.absorb = false;
+  c.own = 0;
+  c.last_shared = 0;
+  if (P > 0 && m <= kAbsorbMembers) {
+    int own = 0;
+    for (int i = 0; i < m; ++i) own += (ga.seq_ctx[b0 + i] + kBlockSize - 1) / kBlockSize - P;
+    if (own <= kAbsorbBlocks) {
+      const int total = P + own;
+      int ns = shared_parts(total, sp);
+      if (ns > P) ns = P;
+      int last = P;
+      if (ns <= 1) {
+        ns = 1;
+      } else {
+        const int size = (total + ns - 1) / ns;
+        last = size - own < 1 ? 1 : size - own;
+        if (P - last < ns - 1) last = P - (ns - 1);
+      }
+      if (last + own <= kSplitBlocks) {
+        c.absorb = true;
+        c.own = own;
+        c.ns = ns;
+        c.last_shared = last;
+      }
+    }
+  }
+  if (!c.absorb) c.ns = shared_parts(P, sp);
+  return c;
+}
+
+constexpr int kGroupedPlanThreads = 512;
+
+__global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const Params p,
+                                                                           const GroupArgs ga) {
+  constexpr int NT = kGroupedPlanThreads;
+  __shared__ int hist[kSplitBlocks + 2];
+  __shared__ int bucket[kSplitBlocks + 2];
+  __shared__ int cut_s, bad_s, sp_s;
+  __shared__ unsigned long long work_s;
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();  // the previous kernel may still read the workspace
+  const int tid = threadIdx.x;
+  const int ng = ga.group_start ? ga.num_groups : 1;
+  const int cap = p.max_blocks * kBlockSize;
+  const int mb = p.max_blocks;
+  int4* units = reinterpret_cast<int4*>(p.ws.units);
+  if (tid < kSplitBlocks + 2) hist[tid] = 0;
+  if (tid == 0) {
+    bad_s = ga.group_start && (ga.group_start[0] != 0 || ga.group_start[ng] != p.num_seqs);
+    work_s = 0;
+  }
+  __syncthreads();
+  // group starts must not decrease (every thread checks its share)
+  if (ga.group_start) {
+    bool down = false;
+    for (int g = tid; g < ng; g += NT) down |= ga.group_start[g] > ga.group_start[g + 1];
+    if (down) bad_s = 1;
+  }
+  __syncthreads();
+  // With unusable group arrays every sequence decodes on its own.
+  const bool bad = bad_s;
+  if (bad && tid == 0) dev::flag_status(p.status, kStatusBounds);
+  for (int g = tid; g < ng; g += NT) {
+    int nb = bad ? 0 : (ga.group_blocks ? ga.group_blocks[g] : ga.single_blocks);
+    if (nb < 0 || nb > mb) {
+      dev::flag_status(p.status, kStatusBounds);
+      nb = 0;
+    }
+    ga.gp[g] = nb;
+  }
+  // every sequence's group and clamped context
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    ga.seq_group[b] = bad ? 0 : group_of(ga, b);
+    int ctx = p.context_lens[b];
+    if (ctx < 0 || ctx > cap) {
+      dev::flag_status(p.status, kStatusBounds);
+      ctx = ctx < 0 ? 0 : cap;
+    }
+    ga.seq_ctx[b] = ctx;
+    for (int h = 0; h < p.num_kv_heads; ++h) p.ws.arrivals[size_t(b) * p.num_kv_heads + h] = 0;
+  }
+  __syncthreads();
+  // Every member's context must cover the shared blocks and its table must
+  // start with the first member's entries; a group with a member that does
+  // not keeps no shared blocks (its members then decode on their own, which
+  // gives the same attention).  One thread per sequence, its entries' loads
+  // all in flight at once; a plan of one shared prefix gets no tables (the
+  // run checks them).
+  for (int b = tid; b < p.num_seqs && !bad; b += NT) {
+    const int g = ga.seq_group[b];
+    const int nb = ga.gp[g];
+    if (nb == 0) continue;
+    const int ctx = p.context_lens[b];
+    bool differ = ctx < nb * kBlockSize || ctx > cap;
+    const int first = ga.group_start ? ga.group_start[g] : 0;
+    if (p.block_tables && b != first) {
+      const int32_t* row = p.block_tables + size_t(b) * mb;
+      const int32_t* lead = p.block_tables + size_t(first) * mb;
+#pragma unroll 8
+      for (int j = 0; j < nb; ++j) differ |= __ldg(row + j) != __ldg(lead + j);
+    }
+    if (differ) {
+      atomicExch(&ga.gp[g], 0);
+      dev::flag_status(p.status, kStatusBounds);
+    }
+  }
+  __syncthreads();
+  // per sequence: its shared blocks and chunk (first member, members); the
+  // work (blocks per KV head) of the own blocks and of every chunk's shared
+  // blocks, which sizes the shared splits
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    const int g = ga.seq_group[b];
+    const int nb = bad ? 0 : ga.gp[g];
+    const int first = ga.group_start && !bad ? ga.group_start[g] : 0;
+    const int end = ga.group_start && !bad ? ga.group_start[g + 1] : p.num_seqs;
+    const int b0 = first + (b - first) / ga.chunk * ga.chunk;
+    const int m = end - b0 < ga.chunk ? end - b0 : ga.chunk;
+    ga.seq_prefix[b] = nb;
+    ga.seq_chunk[b] = make_int2(b0, m);
+    unsigned long long w = (ga.seq_ctx[b] + kBlockSize - 1) / kBlockSize - nb;
+    if (b == b0) w += nb;  // the chunk's shared blocks, read once
+    atomicAdd(&work_s, w);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // shared splits of about the work one math warp gets, 16 to 32 blocks
+    // (the workspace holds a sequence's splits for sizes of 16 and more)
+    const unsigned long long per_warp =
+        (work_s * p.num_kv_heads + ga.nwarps - 1) / (unsigned long long)ga.nwarps;
+    sp_s = per_warp < kMinSplitBlocks ? kMinSplitBlocks
+                                      : (per_warp > kSplitBlocks ? kSplitBlocks : int(per_warp));
+  }
+  __syncthreads();
+  const int sp = sp_s;
+  // every chunk's cut, once (by the thread of its first member)
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    const int2 cm = ga.seq_chunk[b];
+    const int P = ga.seq_prefix[b];
+    if (b != cm.x || P == 0) continue;
+    const ChunkPlan c = plan_chunk(ga, b, cm.y, P, sp);
+    ga.chunk_plan[b] = make_int4(c.absorb, c.own, c.ns, c.last_shared);
+  }
+  __syncthreads();
+  // a sequence's own blocks that become units of its own (none when its
+  // chunk absorbs them), and its chunk's shared splits
+  auto own_and_shared = [&](int b, int& own, int& pn) {
+    const int P = ga.seq_prefix[b];
+    pn = 0;
+    own = (ga.seq_ctx[b] + kBlockSize - 1) / kBlockSize - P;
+    if (P > 0) {
+      const int4 c = ga.chunk_plan[ga.seq_chunk[b].x];
+      pn = c.z;
+      if (c.x) own = 0;
+    }
+  };
+  // shared units of the chunk whose first member is b: sizes into counts
+  auto chunk_units = [&](int b, int* counts) {
+    const int4 c = ga.chunk_plan[b];
+    const int P = ga.seq_prefix[b];
+    if (c.x) {
+      // the shared blocks before the last split, in ns - 1 balanced parts
+      const int k = c.z - 1, X = P - c.w;
+      if (k > 0) {
+        const int base = X / k, big = X % k;
+        if (big) atomicAdd(&counts[base + 1], big);
+        if (k - big) atomicAdd(&counts[base], k - big);
+      }
+      atomicAdd(&counts[c.w + c.y], 1);
+    } else {
+      int base, big;
+      parts_shape(P, c.z, base, big);
+      if (big) atomicAdd(&counts[base + 1], big);
+      if (c.z - big) atomicAdd(&counts[base], c.z - big);
+    }
+  };
+
+  // pass 1: unit sizes before any cut
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    int own, pn;
+    own_and_shared(b, own, pn);
+    int nsplit, base, big;
+    split_shape(own, p.split_blocks, nsplit, base, big);
+    if (big) atomicAdd(&hist[base + 1], big);
+    if (nsplit - big) atomicAdd(&hist[base], nsplit - big);
+    if (b == ga.seq_chunk[b].x && ga.seq_prefix[b] > 0) chunk_units(b, hist);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    // largest size `cut` such that all units of at most `cut` blocks hold no
+    // more than the tail's share of the work (only own units are cut)
+    const long long budget = p.tail_blocks / p.num_kv_heads;
+    long long acc = 0;
+    int cut = 0;
+    while (cut < kSplitBlocks && acc + (long long)hist[cut + 1] * (cut + 1) <= budget) {
+      ++cut;
+      acc += (long long)hist[cut] * cut;
+    }
+    cut_s = cut;
+  }
+  __syncthreads();
+  const int cut_all = cut_s;
+  if (tid < kSplitBlocks + 2) hist[tid] = 0;
+  __syncthreads();
+
+  // pass 2: sizes of the final units, and every sequence's split count
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    int own, pn;
+    own_and_shared(b, own, pn);
+    int nsplit, base, big;
+    split_shape(own, p.split_blocks, nsplit, base, big);
+    int cut = cut_all;
+    if (pn + big * pieces_of(base + 1, cut, p.piece_blocks) +
+            (nsplit - big) * pieces_of(base, cut, p.piece_blocks) > p.max_splits)
+      cut = 0;
+    int count = 0;
+    for (int k = 0; k < 2; ++k) {  // the two split sizes
+      const int n = base + 1 - k, mm = k ? nsplit - big : big;
+      if (mm == 0 || n == 0) continue;
+      const int np = pieces_of(n, cut, p.piece_blocks);
+      count += mm * np;
+      const int pb = n / np, pr = n - pb * np;
+      if (pr) atomicAdd(&hist[pb + 1], mm * pr);
+      if (np - pr) atomicAdd(&hist[pb], mm * (np - pr));
+    }
+    p.ws.nsplits[b] = pn + count;
+    if (b == ga.seq_chunk[b].x && ga.seq_prefix[b] > 0) chunk_units(b, hist);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int pos = 0;
+    for (int r = kSplitBlocks; r >= 1; --r) {
+      bucket[r] = pos;
+      pos += hist[r];
+    }
+    p.ws.header[kHdrTotal] = pos * p.num_kv_heads;
+    p.ws.header[kHdrNext] = 0;
+    p.ws.header[kHdrDone] = 0;
+    p.ws.header[kHdrSignature] = p.signature;
+  }
+  __syncthreads();
+
+  // pass 3: place the units.  Own units: (b, first block, split index << 16
+  // | blocks, context), split indices after the chunk's shared ones.
+  // Shared units: (first member, first block, split index << 16 | members
+  // << 8 | flags | blocks, shared tokens).
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    int own, pn;
+    own_and_shared(b, own, pn);
+    const int P = ga.seq_prefix[b], ctx = ga.seq_ctx[b];
+    int nsplit, base, big;
+    split_shape(own, p.split_blocks, nsplit, base, big);
+    int cut = cut_all;
+    if (pn + big * pieces_of(base + 1, cut, p.piece_blocks) +
+            (nsplit - big) * pieces_of(base, cut, p.piece_blocks) > p.max_splits)
+      cut = 0;
+    int at[2][2];
+    for (int k = 0; k < 2; ++k) {
+      const int n = base + 1 - k, mm = k ? nsplit - big : big;
+      at[k][0] = at[k][1] = 0;
+      if (mm == 0 || n == 0) continue;
+      const int np = pieces_of(n, cut, p.piece_blocks);
+      const int pb = n / np, pr = n - pb * np;
+      if (pr) at[k][0] = atomicAdd(&bucket[pb + 1], mm * pr);
+      if (np - pr) at[k][1] = atomicAdd(&bucket[pb], mm * (np - pr));
+    }
+    int first = P, si = pn;
+    for (int s = 0; s < nsplit; ++s) {
+      const int k = s < big ? 0 : 1;
+      const int n = base + 1 - k;
+      const int np = pieces_of(n, cut, p.piece_blocks);
+      const int pb = n / np, pr = n - pb * np;
+      for (int j = 0; j < np; ++j) {
+        const int sz = j < pr ? pb + 1 : pb;
+        const int pos = j < pr ? at[k][0]++ : at[k][1]++;
+        units[pos] = make_int4(b, first, (si << 16) | sz, ctx);
+        first += sz;
+        ++si;
+      }
+    }
+    const int2 cm = ga.seq_chunk[b];
+    if (b != cm.x || P == 0) continue;
+    // this thread places its chunk's shared units
+    const int4 c = ga.chunk_plan[b];
+    const int flags = c.x ? kUnitChunk : 0;
+    int sn, sbase, sbig;
+    if (c.x) {
+      sn = c.z - 1;  // the parts before the last split
+      parts_shape(P - c.w, sn, sbase, sbig);
+    } else {
+      sn = c.z;
+      parts_shape(P, sn, sbase, sbig);
+    }
+    int off = 0;
+    for (int s = 0; s < sn; ++s) {
+      const int sz = s < sbig ? sbase + 1 : sbase;
+      const int pos = atomicAdd(&bucket[sz], 1);
+      units[pos] = make_int4(b, off, (s << 16) | (cm.y << 8) | flags | sz, P * kBlockSize);
+      off += sz;
+    }
+    if (c.x) {
+      const int pos = atomicAdd(&bucket[c.w + c.y], 1);
+      units[pos] = make_int4(b, off, ((c.z - 1) << 16) | (cm.y << 8) | kUnitChunk | kUnitOwn | c.w,
+                             P * kBlockSize);
     }
   }
 }
@@ -275,24 +665,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
 // round, then lane l owns the float4 columns c = l + 32 k (k < NK) of the
 // group's G x D outputs and issues the loads of U splits at once.
 // Where the partial results of one (b, g) live and where its merge goes.
+// A merge covers `rows` (<= 8) query rows from row0 of a group of members:
+// row r belongs to member r / G (consecutive sequences from b) and query
+// head g G + r % G; one member's rows are the plain case (row0 0, rows G).
 struct MergeArgs {
   const float* lse;   // part_lse at (b, split 0, head g G); split stride Hq
   const float4* po;   // part_o at the same row, as float4
   void* out;          // out row of head g G of sequence b
-  float* cas_o;       // suffix mode: fp32 o rows of head g G (else null)
+  float* cas_o;       // suffix mode: fp32 o rows of head g G (else null; one member only)
   float* cas_lse;     // suffix mode: base-2 log-sum-exp of head g G
   int G, Hq, nsplit;
+  int rows, row0;
+  size_t mrow;        // part rows (lse entries) between consecutive members: max_splits Hq
+  size_t mout;        // out elements between consecutive members: Hq D
 };
 
 template <typename T, int D, int NK>
 __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
   using M = dev::Mma<T>;
   constexpr int U = NK >= 6 ? 2 : 16 / NK;
-  const int G = a.G, Hq = a.Hq, nsplit = a.nsplit;
-  const int C = G * D / 4;  // float4 columns of the group's outputs
+  const int G = a.G, Hq = a.Hq, nsplit = a.nsplit, rows = a.rows;
+  const int C = rows * D / 4;  // float4 columns of the merged rows
   const float* lse = a.lse;
   const float4* po = a.po;
-  const size_t split4 = size_t(Hq) * D / 4;  // float4s between two splits
+  // part row (lse index) of merged row r at split 0: its member's, its head's
+  auto prow = [&](int r) -> size_t {
+    if (a.mrow == 0) return size_t(r);  // one member's rows
+    const int R = a.row0 + r;
+    return size_t(R / G) * a.mrow + size_t(R % G);
+  };
 
   // ---- per head: the largest lse and the sum of 2^(lse - largest)
   float hm[kMaxGroup], hl[kMaxGroup];
@@ -305,10 +706,10 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
     float x[kMaxGroup];
 #pragma unroll
     for (int hh = 0; hh < kMaxGroup; ++hh)
-      x[hh] = hh < G ? __ldcg(lse + size_t(sp) * Hq + hh) : -INFINITY;
+      x[hh] = hh < rows ? __ldcg(lse + prow(hh) + size_t(sp) * Hq) : -INFINITY;
 #pragma unroll
     for (int hh = 0; hh < kMaxGroup; ++hh) {
-      if (hh < G) {
+      if (hh < rows) {
         const float mn = fmaxf(hm[hh], x[hh]);
         hl[hh] = hl[hh] * dev::fast_exp2(hm[hh] - mn) + dev::fast_exp2(x[hh] - mn);
         hm[hh] = mn;
@@ -317,7 +718,7 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
   }
 #pragma unroll
   for (int hh = 0; hh < kMaxGroup; ++hh) {
-    if (hh < G) {
+    if (hh < rows) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, hm[hh], off);
@@ -355,8 +756,10 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
       for (int k = 0; k < NK; ++k) {
         const int sp = sp0 + u, c = lane + 32 * k;
         const bool on = sp < nsplit && c < C;
-        v[u][k] = on ? __ldcg(po + size_t(sp) * split4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        w[u][k] = on ? __ldcg(lse + size_t(sp) * Hq + (4 * c) / D) : -INFINITY;
+        const size_t pr = on ? prow((4 * c) / D) : 0;  // merged row of column c
+        v[u][k] = on ? __ldcg(po + (pr + size_t(sp) * Hq) * (D / 4) + c % (D / 4))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[u][k] = on ? __ldcg(lse + pr + size_t(sp) * Hq) : -INFINITY;
       }
     }
 #pragma unroll
@@ -381,14 +784,16 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
         *reinterpret_cast<float4*>(a.cas_o + 4 * c) =
             make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
       } else {
+        const int R = a.row0 + (4 * c) / D;  // its member's out row, its head's columns
         uint2 pk;
         pk.x = M::pack(acc[k].x * inv, acc[k].y * inv);
         pk.y = M::pack(acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<uint2*>(orow + 4 * c) = pk;
+        *reinterpret_cast<uint2*>(orow + size_t(R / G) * a.mout + size_t(R % G) * D +
+                                  4 * (c % (D / 4))) = pk;
       }
     }
   }
-  if (a.cas_lse && lane < G) {
+  if (a.cas_lse && lane < rows) {
     // lse of head `lane` = its largest lse plus log2 of its weight sum
     float mh = hm[0], lh = hl[0];
 #pragma unroll
@@ -403,7 +808,7 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
 
 template <typename T, int D>
 __device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
-  const int nk = (a.G * D / 4 + 31) / 32;
+  const int nk = (a.rows * D / 4 + 31) / 32;
   switch (nk) {
     case 1: merge_splits<T, D, 1>(a, lane); break;
     case 2: merge_splits<T, D, 2>(a, lane); break;
@@ -423,19 +828,33 @@ __device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
 
 // A work item as a math warp holds it: registers only.  Lane j keeps the
 // physical block of the item's logical block j (an item has at most 32).
+// An item of a grouped decode may cover a block range that several
+// consecutive sequences share (the m members b .. b + m - 1 of a group,
+// m * G query rows); otherwise it is one sequence's (m = 1, G rows).
 struct Item {
-  int b;  // sequence, or -1 once the work list is exhausted
+  int b;  // sequence (first member), or -1 once the work list is exhausted
   int g, s, nblk, first, ctx, nsplit;
+  int m, rows;  // members and query rows
+  int flags;    // kUnitChunk, kUnitOwn of the unit
   int phys;
+  // kUnitOwn items, lane j for block j: the member the block belongs to (-1:
+  // shared by all rows), its tokens in context, and the row of the member's
+  // new token in it (-1: none); lane i < m: member i's new-token slot
+  int bmem, bvalid, bpatch;
+  long long mslot;
+  unsigned okmask;  // members whose new token is stored and attended
   int slot;  // fused append: the new token's slot, or -1 (none / not this item)
   bool patch;  // the new token is this item's last attended token
 };
 
-template <typename T, int D, int W>
+// NT: query-row tiles of 8 per item (1: up to 8 rows, one sequence's query
+// group; 2: up to 16, the rows of the members of a group sharing the item's
+// blocks).
+template <typename T, int D, int W, int NT>
 __global__ void __launch_bounds__(W * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmap_k,
                   const __grid_constant__ CUtensorMap tmap_v, const Params p) {
-  using S = Smem<D, W>;
+  using S = Smem<D, W, NT>;
   using M = dev::Mma<T>;
   constexpr int KT = D / 16;      // 16-wide steps along head_dim
   constexpr int HALVES = D / 64;  // 128-byte TMA boxes per tile row
@@ -480,7 +899,7 @@ __global__ void __launch_bounds__(W * 32)
     const int total0 = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]);
     if (x0 < total0 && x0 < cap) {
       const int4 u = reinterpret_cast<const int4*>(p.ws.units)[x0 / p.num_kv_heads];
-      const int hg = x0 % p.num_kv_heads, n = u.z & 0xff;
+      const int hg = x0 % p.num_kv_heads, n = u.z & kUnitBlocks;
       constexpr int kWarmBlocks = 4;
       if (u.x >= 0 && u.x < p.num_seqs && u.y >= 0 && n >= 1 && n <= kSplitBlocks &&
           p.table_offset + u.y + n <= p.max_blocks) {
@@ -515,6 +934,15 @@ __global__ void __launch_bounds__(W * 32)
 
   const bool fused = p.slot_mapping != nullptr;
   const long long num_slots = (long long)p.num_blocks * kBlockSize;
+  if (planned && warp == W - 1 && p.verify_prefix) {
+    // one shared prefix: every table must start with sequence 0's entries
+    const long long pairs = (long long)p.num_seqs * p.max_blocks;
+    for (long long i = blockIdx.x * 32 + lane; i < pairs; i += gridDim.x * 32) {
+      const int b = int(i / p.max_blocks), j = int(i % p.max_blocks);
+      if (j < p.seq_prefix[b] && p.block_tables[i] != p.block_tables[j])
+        dev::flag_status(p.status, kStatusBounds);
+    }
+  }
   if (planned && warp == W - 1) {
     // rows of empty sequences are zero; a new token of such a sequence is
     // still stored (it attends nothing)
@@ -526,6 +954,11 @@ __global__ void __launch_bounds__(W * 32)
         for (int i = 0; i < Hq * D; ++i) p.cas_o[size_t(b) * Hq * D + i] = 0.f;
         for (int h = 0; h < Hq; ++h) p.cas_lse[size_t(b) * Hq + h] = -INFINITY;
         if (fused && p.slot_mapping[b] >= 0) dev::flag_status(p.status, kStatusBounds);
+      } else if (p.seq_prefix && fused && p.context_lens[b] > 0 &&
+                 p.context_lens[b] <= p.seq_prefix[b] * kBlockSize && p.slot_mapping[b] >= 0) {
+        // grouped mode: the new token would sit inside the shared blocks,
+        // which a sequence never writes; it is neither stored nor attended
+        dev::flag_status(p.status, kStatusBounds);
       } else if (!p.cas_o && p.context_lens[b] <= 0) {
         uint4* row = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + size_t(b) * Hq * D);
         for (int i = 0; i < Hq * D * 2 / 16; ++i) row[i] = make_uint4(0, 0, 0, 0);
@@ -555,6 +988,15 @@ __global__ void __launch_bounds__(W * 32)
   cur.b = nxt.b = -1;
   cur.g = cur.s = cur.nblk = cur.first = cur.ctx = cur.nsplit = cur.phys = 0;
   nxt.g = nxt.s = nxt.nblk = nxt.first = nxt.ctx = nxt.nsplit = nxt.phys = 0;
+  cur.m = nxt.m = 1;
+  cur.rows = nxt.rows = G;
+  cur.flags = nxt.flags = 0;
+  cur.bmem = nxt.bmem = -1;
+  cur.bvalid = nxt.bvalid = 0;
+  cur.bpatch = nxt.bpatch = -1;
+  cur.mslot = nxt.mslot = -1;
+  cur.okmask = nxt.okmask = 0u;
+  int octx = 0;  // kUnitOwn claim: lane i < m holds member i's context
   cur.slot = nxt.slot = -1;
   cur.patch = nxt.patch = false;
   long long cslot = -1;  // slot_mapping[b] of the item being claimed
@@ -589,20 +1031,99 @@ __global__ void __launch_bounds__(W * 32)
     } else if (cstage == 2) {
       nxt.b = cu.x;
       nxt.first = cu.y;
-      nxt.s = cu.z >> 8;
-      nxt.nblk = cu.z & 0xff;
+      nxt.s = cu.z >> 16;
+      nxt.m = (cu.z >> 8) & 0xff;
+      nxt.nblk = cu.z & kUnitBlocks;
+      nxt.flags = cu.z & (kUnitChunk | kUnitOwn);
       nxt.ctx = cu.w;
+      // a unit shared by several members (grouped plans only)
+      if (nxt.m < 1 || NT == 1 || nxt.m * G > 8 * NT || nxt.b + nxt.m > p.num_seqs) {
+        if (nxt.m != 0 || nxt.flags) dev::flag_status(p.status, kStatusBounds);
+        nxt.m = 1;
+        nxt.flags = 0;
+      }
+      if ((nxt.flags & kUnitOwn) && nxt.m > kAbsorbMembers) {
+        dev::flag_status(p.status, kStatusBounds);
+        nxt.flags &= ~kUnitOwn;
+      }
+      nxt.rows = nxt.m * G;
       nxt.nsplit = __ldg(&p.ws.nsplits[nxt.b]);
-      cslot = fused ? __ldg(&p.slot_mapping[nxt.b]) : -1;
+      // only an item of one sequence carries its new token
+      cslot = fused && (cu.z & 0xff00) == 0 ? __ldg(&p.slot_mapping[nxt.b]) : -1;
       nxt.phys = lane < nxt.nblk
                      ? __ldg(&p.block_tables[size_t(nxt.b) * p.max_blocks + p.table_offset +
                                              nxt.first + lane])
                      : 0;
+      nxt.bmem = -1;
+      nxt.bvalid = nxt.ctx - (nxt.first + lane) * kBlockSize;
+      nxt.bpatch = -1;
+      nxt.okmask = 0u;
+      nxt.mslot = -1;
+      if (nxt.flags & kUnitOwn) {
+        // the members' contexts and new-token slots, for the next step
+        octx = lane < nxt.m ? __ldg(&p.context_lens[nxt.b + lane]) : 0;
+        nxt.mslot = fused && lane < nxt.m ? __ldg(&p.slot_mapping[nxt.b + lane]) : -1;
+        cstage = 5;
+      } else {
+        cstage = 3;
+      }
+    } else if (cstage == 5) {
+      // kUnitOwn: after the shared blocks (they end at the group's shared
+      // count P), member i's own blocks P .. ceil(ctx_i / 16) - 1, member
+      // after member; lane j takes block j of that list
+      const int P = nxt.first + nxt.nblk;
+      const int own = lane < nxt.m ? max(0, (octx + kBlockSize - 1) / kBlockSize - P) : 0;
+      int off = own;  // inclusive sum over lanes 0 .. lane
+#pragma unroll
+      for (int d = 1; d < kAbsorbMembers; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, off, d);
+        if (lane >= d) off += v;
+      }
+      const int total = __shfl_sync(0xffffffffu, off, kAbsorbMembers - 1);
+      off -= own;  // exclusive
+      const int n0 = nxt.nblk;
+      const int jj = lane - n0;
+      int mem = -1, mctx = 0, moff = 0;
+#pragma unroll
+      for (int i = 0; i < kAbsorbMembers; ++i) {
+        const int oi = __shfl_sync(0xffffffffu, off, i), ni = __shfl_sync(0xffffffffu, own, i);
+        const int ci = __shfl_sync(0xffffffffu, octx, i);
+        if (i < nxt.m && jj >= oi && jj < oi + ni) {
+          mem = i;
+          mctx = ci;
+          moff = oi;
+        }
+      }
+      if (n0 + total > kSplitBlocks) {  // the plan keeps every item within 32 blocks
+        dev::flag_status(p.status, kStatusBounds);
+        mem = -1;
+      } else {
+        nxt.nblk = n0 + total;
+      }
+      if (mem >= 0) {
+        const int local = P + jj - moff;
+        nxt.phys = __ldg(&p.block_tables[size_t(nxt.b + mem) * p.max_blocks + local]);
+        nxt.bmem = mem;
+        nxt.bvalid = mctx - local * kBlockSize;
+        nxt.bpatch = local == (mctx + kBlockSize - 1) / kBlockSize - 1 ? (mctx - 1) % kBlockSize : -1;
+      }
       cstage = 3;
     } else if (cstage == 3) {
       if (lane < nxt.nblk && (nxt.phys < 0 || nxt.phys >= p.num_blocks)) {
         dev::flag_status(p.status, kStatusBounds);
         nxt.phys = 0;
+      }
+      if (nxt.flags & kUnitOwn) {
+        // the lane of a member's last block checks that member's new-token
+        // slot against the position of its last token
+        const long long ms = __shfl_sync(0xffffffffu, nxt.mslot, nxt.bmem < 0 ? 0 : nxt.bmem);
+        bool ok = false;
+        if (lane < nxt.nblk && nxt.bpatch >= 0 && ms >= 0) {
+          ok = ms < num_slots && (long long)nxt.phys * kBlockSize + nxt.bpatch == ms;
+          if (!ok) dev::flag_status(p.status, kStatusBounds);
+        }
+        if (!ok) nxt.bpatch = -1;
+        nxt.okmask = __reduce_or_sync(0xffffffffu, ok ? 1u << nxt.bmem : 0u);
       }
       // Fused append: the item holding the sequence's last block stores the
       // new token's K/V row of its KV head and uses it as its last token.
@@ -624,20 +1145,22 @@ __global__ void __launch_bounds__(W * 32)
       // staging buffer, which the current item no longer reads: its rows are
       // in registers
       const uint32_t rbytes = nxt.slot >= 0 ? 2u * D * 2 : 0u;
-      if (lane == 0) dev::mbar_arrive_expect_tx(my_q, uint32_t(G) * D * 2 + rbytes);
+      if (lane == 0) dev::mbar_arrive_expect_tx(my_q, uint32_t(nxt.rows) * D * 2 + rbytes);
       __syncwarp();
-      // lane h copies query row h into its padded row of the buffer
-      if (lane < G)
+      // lane r copies query row r (member r / G, head r % G of the group)
+      // into row r of the buffer
+      if (lane < nxt.rows)
         dev::bulk_load(qbuf + lane * S::kQRow,
                        static_cast<const uint8_t*>(p.q) +
-                           (size_t(nxt.b) * Hq + size_t(nxt.g) * G + lane) * D * 2,
+                           ((size_t(nxt.b) + lane / G) * Hq + size_t(nxt.g) * G + lane % G) *
+                               D * 2,
                        D * 2, my_q);
       if (rbytes && lane == 0) {
         const size_t row = (size_t(nxt.b) * Hkv + nxt.g) * D * 2;
-        dev::bulk_load(qbuf + kMaxGroup * S::kQRow, static_cast<const uint8_t*>(p.k_new) + row,
-                       D * 2, my_q);
-        dev::bulk_load(qbuf + kMaxGroup * S::kQRow + D,
-                       static_cast<const uint8_t*>(p.v_new) + row, D * 2, my_q);
+        dev::bulk_load(qbuf + 8 * S::kQRow, static_cast<const uint8_t*>(p.k_new) + row, D * 2,
+                       my_q);
+        dev::bulk_load(qbuf + 8 * S::kQRow + D, static_cast<const uint8_t*>(p.v_new) + row, D * 2,
+                       my_q);
       }
       ++q_issued;
       cstage = 4;
@@ -702,7 +1225,9 @@ __global__ void __launch_bounds__(W * 32)
     const unsigned long long item_t0 = dev::global_timer_ns();
 #endif
     const int b = cur.b, g = cur.g, s = cur.s, ctx = cur.ctx, nblk = cur.nblk, first = cur.first;
-    const int nsplit = cur.nsplit;
+    const int nsplit = cur.nsplit, rows = cur.rows;
+    // the second row tile holds rows (warp-uniform)
+    const bool two = NT == 2 && rows > 8;
     // B fragments of Q^T (k = head_dim, n = query head of the group)
     if (!mbar_wait_bounded(my_q, q_taken & 1, tmo, p.status)) {
       drain();
@@ -713,27 +1238,43 @@ __global__ void __launch_bounds__(W * 32)
     const unsigned long long qwait_ns = dev::global_timer_ns() - item_t0;
     unsigned long long merge_ns = 0;
 #endif
-    uint32_t qb0[KT], qb1[KT];
-    {
-      const int hq = lane >> 2;
+    uint32_t qb0[NT][KT], qb1[NT][KT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int hq = 8 * t + (lane >> 2);
       const int n0 = 2 * (lane & 3);
       const uint16_t* qrow = qbuf + hq * S::kQRow + n0;
 #pragma unroll
       for (int kk = 0; kk < KT; ++kk) {
-        qb0[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk) : 0u;
-        qb1[kk] = hq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
+        qb0[t][kk] = hq < rows ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk) : 0u;
+        qb1[t][kk] = hq < rows ? *reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8) : 0u;
       }
     }
     // fused append: lane l < D/4 holds 16 bytes of the new K row (l < D/8)
     // or V row; they go to the cache slot now and into the tile at the last block
     uint4 nkv = make_uint4(0, 0, 0, 0);
     if (cur.slot >= 0 && lane < D / 4) {
-      nkv = *reinterpret_cast<const uint4*>(qbuf + kMaxGroup * S::kQRow + lane * 8);
+      nkv = *reinterpret_cast<const uint4*>(qbuf + 8 * S::kQRow + lane * 8);
       const bool isv = lane >= D / 8;
       const int c = isv ? lane - D / 8 : lane;
       const size_t dst = ((size_t(cur.slot / kBlockSize) * Hkv + g) * kBlockSize +
                           size_t(cur.slot % kBlockSize)) * (D / 8) + c;
       static_cast<uint4*>(const_cast<void*>(isv ? p.v_cache : p.k_cache))[dst] = nkv;
+    }
+    // kUnitOwn: lane l < D/4 loads 16 bytes of member i's new K row (l < D/8)
+    // or V row, used when the member's last block is patched and stored to
+    // its slot after the item (its own blocks are at the item's end, so the
+    // loads have the shared blocks' time to land)
+    uint4 mkv[NT == 2 ? kAbsorbMembers : 1];
+#pragma unroll
+    for (int i = 0; i < (NT == 2 ? kAbsorbMembers : 1); ++i) {
+      mkv[i] = make_uint4(0, 0, 0, 0);
+      if (NT == 2 && ((cur.okmask >> i) & 1u) && lane < D / 4) {
+        const bool isv = lane >= D / 8;
+        const int c = isv ? lane - D / 8 : lane;
+        mkv[i] = __ldg(static_cast<const uint4*>(isv ? p.v_new : p.k_new) +
+                       (size_t(b + i) * Hkv + g) * (D / 8) + c);
+      }
     }
     // qbuf is read: order those reads before the copy that refills it
     dev::fence_proxy_async_smem();
@@ -741,10 +1282,17 @@ __global__ void __launch_bounds__(W * 32)
     if (nblk - cur_issued <= kLead) request();
     top_up(kc);
 
-    float o[KT][4];
+    // per row tile t: O^T accumulators, and the running max / sum of its
+    // two query columns (n0, n0 + 1) held by this lane
+    float o[NT][KT][4];
+    float m0[NT], m1[NT], l0[NT], l1[NT];
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    for (int t = 0; t < NT; ++t) {
+#pragma unroll
+      for (int mt = 0; mt < KT; ++mt) o[t][mt][0] = o[t][mt][1] = o[t][mt][2] = o[t][mt][3] = 0.f;
+      m0[t] = m1[t] = -INFINITY;
+      l0[t] = l1[t] = 0.f;
+    }
     const float sl2 = p.scale_log2;
 
     for (int j = 0; j < nblk; ++j) {
@@ -755,6 +1303,32 @@ __global__ void __launch_bounds__(W * 32)
       }
       const uint32_t kt = dev::smem_u32(ring + size_t(st) * S::kStageBytes);
       const uint32_t vt = kt + S::kTileBytes;
+      // the block's member (-1: every row), tokens in context, patch row
+      int bmem = -1, bval = ctx - (first + j) * kBlockSize;
+      if constexpr (NT == 2) {
+        if (cur.flags & kUnitOwn) {
+          bmem = __shfl_sync(0xffffffffu, cur.bmem, j);
+          bval = __shfl_sync(0xffffffffu, cur.bvalid, j);
+          const int bpr = __shfl_sync(0xffffffffu, cur.bpatch, j);
+          if (bpr >= 0) {
+            // member bmem's new token replaces whatever its slot held
+            uint4 v = mkv[0];
+#pragma unroll
+            for (int i = 1; i < kAbsorbMembers; ++i)
+              if (bmem == i) v = mkv[i];
+            if (lane < D / 4) {
+              const bool isv = lane >= D / 8;
+              const int c = isv ? lane - D / 8 : lane;
+              const uint32_t addr =
+                  (isv ? vt : kt) + (c >> 3) * 2048 + bpr * 128 + (((c & 7) ^ (bpr & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                           "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
+            __syncwarp();
+          }
+        }
+      }
       if (cur.patch && j == nblk - 1) {
         // the new token's row replaces whatever the cache held at its slot
         const int r = (ctx - 1) % kBlockSize;
@@ -769,8 +1343,11 @@ __global__ void __launch_bounds__(W * 32)
         }
         __syncwarp();
       }
-      // ---- S^T (16 tokens x 8 heads) = K (16 x D) . Q^T (D x 8)
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T (16 tokens x 8 rows) = K (16 x D) . Q^T (D x 8), per row tile
+      float sa[NT][4], sb[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+        sa[t][0] = sa[t][1] = sa[t][2] = sa[t][3] = sb[t][0] = sb[t][1] = sb[t][2] = sb[t][3] = 0.f;
       {
         const int row = lane & 15;
 #pragma unroll
@@ -780,47 +1357,66 @@ __global__ void __launch_bounds__(W * 32)
               kt + (gc >> 3) * 2048 + row * 128 + ((((gc & 7) ^ (row & 7))) << 4);
           uint32_t a0, a1, a2, a3;
           dev::ldmatrix_x4(addr, a0, a1, a2, a3);
-          if (kk & 1)
-            M::run(sb, a0, a1, a2, a3, qb0[kk], qb1[kk]);
-          else
-            M::run(sa, a0, a1, a2, a3, qb0[kk], qb1[kk]);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t == 1 && !two) continue;
+            if (kk & 1)
+              M::run(sb[t], a0, a1, a2, a3, qb0[t][kk], qb1[t][kk]);
+            else
+              M::run(sa[t], a0, a1, a2, a3, qb0[t][kk], qb1[t][kk]);
+          }
         }
       }
-      // ---- mask, scale to base 2, online softmax per head column
-      const int valid = ctx - (first + j) * kBlockSize;  // tokens of the block in context
+      // ---- mask, scale to base 2, online softmax per query column
+      const int valid = bval;  // tokens of the block in context
       const int r0 = lane >> 2;
       const bool v0 = r0 < valid, v1 = r0 + 8 < valid;
-      const float x0 = v0 ? (sa[0] + sb[0]) * sl2 : -INFINITY;
-      const float x1 = v0 ? (sa[1] + sb[1]) * sl2 : -INFINITY;
-      const float x2 = v1 ? (sa[2] + sb[2]) * sl2 : -INFINITY;
-      const float x3 = v1 ? (sa[3] + sb[3]) * sl2 : -INFINITY;
-      float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+      uint32_t pb0[NT], pb1[NT];
 #pragma unroll
-      for (int o_ = 4; o_ < 32; o_ <<= 1) {
-        bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o_));
-        bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o_));
-      }
-      const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-      const float al0 = dev::fast_exp2(m0 - mn0), al1 = dev::fast_exp2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      const uint32_t p01 = M::pack(dev::fast_exp2(x0 - mn0), dev::fast_exp2(x1 - mn1));
-      const uint32_t p23 = M::pack(dev::fast_exp2(x2 - mn0), dev::fast_exp2(x3 - mn1));
-      {
-        const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
-        l0 = l0 * al0 + f01.x + f23.x;
-        l1 = l1 * al1 + f01.y + f23.y;
-      }
+      for (int t = 0; t < NT; ++t) {
+        if (t == 1 && !two) {
+          pb0[t] = pb1[t] = 0u;
+          continue;
+        }
+        // a member's own block counts for that member's rows only
+        const int qr = 8 * t + 2 * (lane & 3);
+        const bool c0 = bmem < 0 || qr / G == bmem, c1 = bmem < 0 || (qr + 1) / G == bmem;
+        const float x0 = v0 && c0 ? (sa[t][0] + sb[t][0]) * sl2 : -INFINITY;
+        const float x1 = v0 && c1 ? (sa[t][1] + sb[t][1]) * sl2 : -INFINITY;
+        const float x2 = v1 && c0 ? (sa[t][2] + sb[t][2]) * sl2 : -INFINITY;
+        const float x3 = v1 && c1 ? (sa[t][3] + sb[t][3]) * sl2 : -INFINITY;
+        float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        o[mt][0] *= al0;
-        o[mt][1] *= al1;
-        o[mt][2] *= al0;
-        o[mt][3] *= al1;
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+          bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, o_));
+          bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, o_));
+        }
+        const float mn0 = fmaxf(m0[t], bm0), mn1 = fmaxf(m1[t], bm1);
+        const float al0 = dev::fast_exp2(m0[t] - mn0), al1 = dev::fast_exp2(m1[t] - mn1);
+        m0[t] = mn0;
+        m1[t] = mn1;
+        const uint32_t p01 = M::pack(dev::fast_exp2(x0 - mn0), dev::fast_exp2(x1 - mn1));
+        const uint32_t p23 = M::pack(dev::fast_exp2(x2 - mn0), dev::fast_exp2(x3 - mn1));
+        {
+          const float2 f01 = M::unpack(p01), f23 = M::unpack(p23);
+          l0[t] = l0[t] * al0 + f01.x + f23.x;
+          l1[t] = l1[t] * al1 + f01.y + f23.y;
+        }
+        // rescale O only when some column's running max grew (x 1 is exact;
+        // with two row tiles the multiplies are a good share of the block)
+        if (NT == 1 || __any_sync(0xffffffffu, al0 < 1.f || al1 < 1.f)) {
+#pragma unroll
+          for (int mt = 0; mt < KT; ++mt) {
+            o[t][mt][0] *= al0;
+            o[t][mt][1] *= al1;
+            o[t][mt][2] *= al0;
+            o[t][mt][3] *= al1;
+          }
+        }
+        // ---- P^T as the B operand: transpose the two 8x8 halves in registers
+        pb0[t] = dev::movmatrix_trans(p01);
+        pb1[t] = dev::movmatrix_trans(p23);
       }
-      // ---- P^T as the B operand: transpose the two 8x8 halves in registers
-      const uint32_t pb0 = dev::movmatrix_trans(p01);
-      const uint32_t pb1 = dev::movmatrix_trans(p23);
       // V^T fragments hold tokens 2(lane%4)+{0,1} (a0, a1) and +8 (a2, a3):
       // zero the ones past the context so their bits never meet P = 0.
       uint32_t vm_lo = 0xffffffffu, vm_hi = 0xffffffffu;
@@ -829,7 +1425,7 @@ __global__ void __launch_bounds__(W * 32)
         vm_lo = (t < valid ? 0x0000ffffu : 0u) | (t + 1 < valid ? 0xffff0000u : 0u);
         vm_hi = (t + 8 < valid ? 0x0000ffffu : 0u) | (t + 9 < valid ? 0xffff0000u : 0u);
       }
-      // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8)
+      // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8), per row tile
       {
         const int tok = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
@@ -839,7 +1435,11 @@ __global__ void __launch_bounds__(W * 32)
               vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
           uint32_t a0, a1, a2, a3;
           dev::ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-          M::run(o[mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0, pb1);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t == 1 && !two) continue;
+            M::run(o[t][mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0[t], pb1[t]);
+          }
         }
       }
       // the stage is read; order those reads before the copy that reuses it
@@ -852,78 +1452,231 @@ __global__ void __launch_bounds__(W * 32)
     }
 
     // ---- end of the item: this warp holds the whole (m, l, O) of its split
+    if constexpr (NT == 1) {
 #pragma unroll
-    for (int o_ = 4; o_ < 32; o_ <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o_);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o_);
-    }
-    const int n0 = 2 * (lane & 3), n1 = n0 + 1;
-    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-    const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-    if (nsplit == 1 && p.cas_o) {
-      float* crow = p.cas_o + head0 * D;
-#pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        const int d0 = 16 * mt + (lane >> 2);
-        if (n0 < G) {
-          crow[n0 * D + d0] = o[mt][0] * inv0;
-          crow[n0 * D + d0 + 8] = o[mt][2] * inv0;
-        }
-        if (n1 < G) {
-          crow[n1 * D + d0] = o[mt][1] * inv1;
-          crow[n1 * D + d0 + 8] = o[mt][3] * inv1;
-        }
+      for (int o_ = 4; o_ < 32; o_ <<= 1) {
+        l0[0] += __shfl_xor_sync(0xffffffffu, l0[0], o_);
+        l1[0] += __shfl_xor_sync(0xffffffffu, l1[0], o_);
       }
-      if (lane < 4) {
-        if (n0 < G) p.cas_lse[head0 + n0] = m0 + log2f(l0);
-        if (n1 < G) p.cas_lse[head0 + n1] = m1 + log2f(l1);
-      }
-    } else if (nsplit == 1) {
-      T* orow = static_cast<T*>(p.out) + head0 * D;
+      const int n0 = 2 * (lane & 3), n1 = n0 + 1;
+      const float inv0 = 1.f / l0[0], inv1 = 1.f / l1[0];
+      const size_t head0 = size_t(b) * Hq + size_t(g) * G;
+      if (nsplit == 1 && p.cas_o) {
+        float* crow = p.cas_o + head0 * D;
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        const int d0 = 16 * mt + (lane >> 2);
-        if (n0 < G) {
-          orow[n0 * D + d0] = M::from_float(o[mt][0] * inv0);
-          orow[n0 * D + d0 + 8] = M::from_float(o[mt][2] * inv0);
+        for (int mt = 0; mt < KT; ++mt) {
+          const int d0 = 16 * mt + (lane >> 2);
+          if (n0 < G) {
+            crow[n0 * D + d0] = o[0][mt][0] * inv0;
+            crow[n0 * D + d0 + 8] = o[0][mt][2] * inv0;
+          }
+          if (n1 < G) {
+            crow[n1 * D + d0] = o[0][mt][1] * inv1;
+            crow[n1 * D + d0 + 8] = o[0][mt][3] * inv1;
+          }
         }
-        if (n1 < G) {
-          orow[n1 * D + d0] = M::from_float(o[mt][1] * inv1);
-          orow[n1 * D + d0 + 8] = M::from_float(o[mt][3] * inv1);
+        if (lane < 4) {
+          if (n0 < G) p.cas_lse[head0 + n0] = m0[0] + log2f(l0[0]);
+          if (n1 < G) p.cas_lse[head0 + n1] = m1[0] + log2f(l1[0]);
+        }
+      } else if (nsplit == 1) {
+        T* orow = static_cast<T*>(p.out) + head0 * D;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          const int d0 = 16 * mt + (lane >> 2);
+          if (n0 < G) {
+            orow[n0 * D + d0] = M::from_float(o[0][mt][0] * inv0);
+            orow[n0 * D + d0 + 8] = M::from_float(o[0][mt][2] * inv0);
+          }
+          if (n1 < G) {
+            orow[n1 * D + d0] = M::from_float(o[0][mt][1] * inv1);
+            orow[n1 * D + d0 + 8] = M::from_float(o[0][mt][3] * inv1);
+          }
+        }
+      } else {
+        const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
+        float* prow = p.ws.part_o + part0 * D;
+#pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          const int d0 = 16 * mt + (lane >> 2);
+          if (n0 < G) {
+            prow[n0 * D + d0] = o[0][mt][0] * inv0;
+            prow[n0 * D + d0 + 8] = o[0][mt][2] * inv0;
+          }
+          if (n1 < G) {
+            prow[n1 * D + d0] = o[0][mt][1] * inv1;
+            prow[n1 * D + d0 + 8] = o[0][mt][3] * inv1;
+          }
+        }
+        if (lane < 4) {
+          if (n0 < G) p.ws.part_lse[part0 + n0] = m0[0] + log2f(l0[0]);
+          if (n1 < G) p.ws.part_lse[part0 + n1] = m1[0] + log2f(l1[0]);
+        }
+        // Publish this split and count it (release); the warp that completes
+        // (b, g) sees every other split's results (acquire) and merges them.
+        __syncwarp();
+        int last = 0;
+        if (lane == 0)
+          last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+#ifdef PA_PROFILE_TIMES
+          const unsigned long long merge_t0 = dev::global_timer_ns();
+#endif
+          __syncwarp();
+          const size_t row0 = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+          MergeArgs ma;
+          ma.lse = p.ws.part_lse + row0;
+          ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
+          ma.out = static_cast<T*>(p.out) + head0 * D;
+          ma.cas_o = p.cas_o ? p.cas_o + head0 * D : nullptr;
+          ma.cas_lse = p.cas_lse ? p.cas_lse + head0 : nullptr;
+          ma.G = G;
+          ma.Hq = Hq;
+          ma.nsplit = nsplit;
+          ma.rows = G;
+          ma.row0 = 0;
+          ma.mrow = 0;
+          ma.mout = 0;
+          merge_dispatch<T, D>(ma, lane);
+          if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+#ifdef PA_PROFILE_TIMES
+          merge_ns = dev::global_timer_ns() - merge_t0;
+#endif
         }
       }
     } else {
-      const size_t part0 = (size_t(b) * p.max_splits + s) * Hq + size_t(g) * G;
-      float* prow = p.ws.part_o + part0 * D;
+      // Rows of several members: row r belongs to sequence b + r / G, query
+      // head g G + r % G, and each member has its own split count.
 #pragma unroll
-      for (int mt = 0; mt < KT; ++mt) {
-        const int d0 = 16 * mt + (lane >> 2);
-        if (n0 < G) {
-          prow[n0 * D + d0] = o[mt][0] * inv0;
-          prow[n0 * D + d0 + 8] = o[mt][2] * inv0;
-        }
-        if (n1 < G) {
-          prow[n1 * D + d0] = o[mt][1] * inv1;
-          prow[n1 * D + d0 + 8] = o[mt][3] * inv1;
+      for (int t = 0; t < NT; ++t) {
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+          l0[t] += __shfl_xor_sync(0xffffffffu, l0[t], o_);
+          l1[t] += __shfl_xor_sync(0xffffffffu, l1[t], o_);
         }
       }
-      if (lane < 4) {
-        if (n0 < G) p.ws.part_lse[part0 + n0] = m0 + log2f(l0);
-        if (n1 < G) p.ws.part_lse[part0 + n1] = m1 + log2f(l1);
+      const int n0 = 2 * (lane & 3);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (t == 1 && !two) continue;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int r = 8 * t + n0 + c;
+          if (r >= rows) continue;
+          const int bi = b + r / G, head = g * G + r % G;
+          const int nsi = r < G ? nsplit : __ldg(&p.ws.nsplits[bi]);
+          const float lsum = c ? l1[t] : l0[t];
+          const float inv = 1.f / lsum;
+          const float lse = (c ? m1[t] : m0[t]) + log2f(lsum);
+          const size_t hrow = size_t(bi) * Hq + head;
+          if (nsi == 1 && p.cas_o) {
+            float* crow = p.cas_o + hrow * D;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+              const int d0 = 16 * mt + (lane >> 2);
+              crow[d0] = o[t][mt][c] * inv;
+              crow[d0 + 8] = o[t][mt][2 + c] * inv;
+            }
+            if (lane < 4) p.cas_lse[hrow] = lse;
+          } else if (nsi == 1) {
+            T* orow = static_cast<T*>(p.out) + hrow * D;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+              const int d0 = 16 * mt + (lane >> 2);
+              orow[d0] = M::from_float(o[t][mt][c] * inv);
+              orow[d0 + 8] = M::from_float(o[t][mt][2 + c] * inv);
+            }
+          } else if (s >= p.max_splits) {
+            dev::flag_status(p.status, kStatusBounds);  // (the plan never makes so many)
+          } else {
+            const size_t part = (size_t(bi) * p.max_splits + s) * Hq + head;
+            float* prow = p.ws.part_o + part * D;
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+              const int d0 = 16 * mt + (lane >> 2);
+              prow[d0] = o[t][mt][c] * inv;
+              prow[d0 + 8] = o[t][mt][2 + c] * inv;
+            }
+            if (lane < 4) p.ws.part_lse[part] = lse;
+          }
+        }
       }
-      // Publish this split and count it (release); the warp that completes
-      // (b, g) sees every other split's results (acquire) and merges them.
+      // the members' new tokens go to their slots (kUnitOwn; attended above)
+#pragma unroll
+      for (int i = 0; i < kAbsorbMembers; ++i) {
+        const long long ms = __shfl_sync(0xffffffffu, cur.mslot, i);
+        if (((cur.okmask >> i) & 1u) && lane < D / 4) {
+          const bool isv = lane >= D / 8;
+          const int c = isv ? lane - D / 8 : lane;
+          const size_t dst = ((size_t(ms / kBlockSize) * Hkv + g) * kBlockSize +
+                              size_t(ms % kBlockSize)) * (D / 8) + c;
+          static_cast<uint4*>(const_cast<void*>(isv ? p.v_cache : p.k_cache))[dst] = mkv[i];
+        }
+      }
+      if (p.defer_merge) {
+        // the merge launch after this one merges every split set
+      } else if (cur.flags & kUnitChunk) {
+        // Every member of the chunk has the chunk's splits: they are counted
+        // on the first member's counter (release), and the warp that
+        // completes the set merges all the chunk's rows, eight at a time.
+        __syncwarp();
+        int last = 0;
+        if (lane == 0 && nsplit > 1)
+          last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+#ifdef PA_PROFILE_TIMES
+          const unsigned long long merge_t0 = dev::global_timer_ns();
+#endif
+          __syncwarp();
+          const size_t head0 = size_t(b) * Hq + size_t(g) * G;
+          const size_t row0 = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+          for (int r0 = 0; r0 < rows; r0 += 8) {
+            MergeArgs ma;
+            ma.lse = p.ws.part_lse + row0;
+            ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
+            ma.out = static_cast<T*>(p.out) + head0 * D;
+            ma.cas_o = nullptr;
+            ma.cas_lse = nullptr;
+            ma.G = G;
+            ma.Hq = Hq;
+            ma.nsplit = nsplit;
+            ma.rows = rows - r0 < 8 ? rows - r0 : 8;
+            ma.row0 = r0;
+            ma.mrow = size_t(p.max_splits) * Hq;
+            ma.mout = size_t(Hq) * D;
+            merge_dispatch<T, D>(ma, lane);
+          }
+          if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+#ifdef PA_PROFILE_TIMES
+          merge_ns += dev::global_timer_ns() - merge_t0;
+#endif
+        }
+      } else {
+      // Publish and count: lane i counts this split for member i (release);
+      // the warp that completes a member's (sequence, g) merges it.
+      const int members = cur.m;
       __syncwarp();
-      int last = 0;
-      if (lane == 0)
-        last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
+      int last = 0, nsl = 0;
+      if (lane < members) {
+        nsl = lane == 0 ? nsplit : __ldg(&p.ws.nsplits[b + lane]);
+        if (nsl > 1)
+          last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b + lane) * Hkv + g], 1) ==
+                 nsl - 1;
+      }
+      unsigned lastmask = __ballot_sync(0xffffffffu, last);
+      while (lastmask) {
+        const int i = __ffs(lastmask) - 1;
+        lastmask &= lastmask - 1;
+        const int bi = b + i;
+        const int nsi = __shfl_sync(0xffffffffu, nsl, i);
 #ifdef PA_PROFILE_TIMES
         const unsigned long long merge_t0 = dev::global_timer_ns();
 #endif
         __syncwarp();
-        const size_t row0 = size_t(b) * p.max_splits * Hq + size_t(g) * G;
+        const size_t head0 = size_t(bi) * Hq + size_t(g) * G;
+        const size_t row0 = size_t(bi) * p.max_splits * Hq + size_t(g) * G;
         MergeArgs ma;
         ma.lse = p.ws.part_lse + row0;
         ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
@@ -932,12 +1685,17 @@ __global__ void __launch_bounds__(W * 32)
         ma.cas_lse = p.cas_lse ? p.cas_lse + head0 : nullptr;
         ma.G = G;
         ma.Hq = Hq;
-        ma.nsplit = nsplit;
+        ma.nsplit = nsi;
+        ma.rows = G;
+        ma.row0 = 0;
+        ma.mrow = 0;
+        ma.mout = 0;
         merge_dispatch<T, D>(ma, lane);
-        if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
+        if (lane == 0) p.ws.arrivals[size_t(bi) * Hkv + g] = 0;  // ready for the next run
 #ifdef PA_PROFILE_TIMES
-        merge_ns = dev::global_timer_ns() - merge_t0;
+        merge_ns += dev::global_timer_ns() - merge_t0;
 #endif
+      }
       }
     }
 #ifdef PA_PROFILE_TIMES
@@ -1010,6 +1768,45 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const Params p) {
 
 namespace pa {
 namespace decode {
+
+// The merges of a grouped decode, as a launch of their own: one warp per
+// (sequence, KV head) with more than one split merges that sequence's split
+// results of the head's query group (log-sum-exp weights, splits in order).
+// Run after the attention launch, so the merges are spread over the whole
+// GPU instead of queueing in the warps that finish a chunk's splits last.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) merge_kernel(const Params p) {
+  dev::grid_launch_dependents();
+  dev::grid_dependency_wait();  // the attention launch has written every split
+  const int lane = threadIdx.x & 31;
+  const long long pairs = (long long)p.num_seqs * p.num_kv_heads;
+  for (long long x = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; x < pairs;
+       x += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int b = int(x / p.num_kv_heads), g = int(x % p.num_kv_heads);
+    const int nsplit = p.ws.nsplits[b];
+    if (nsplit <= 1) continue;  // written by its only split (or an empty row)
+    if (nsplit > p.max_splits) {
+      if (lane == 0) dev::flag_status(p.status, kStatusBounds);
+      continue;
+    }
+    const size_t head0 = size_t(b) * p.num_q_heads + size_t(g) * p.group;
+    const size_t row0 = size_t(b) * p.max_splits * p.num_q_heads + size_t(g) * p.group;
+    MergeArgs ma;
+    ma.lse = p.ws.part_lse + row0;
+    ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
+    ma.out = static_cast<T*>(p.out) + head0 * D;
+    ma.cas_o = nullptr;
+    ma.cas_lse = nullptr;
+    ma.G = p.group;
+    ma.Hq = p.num_q_heads;
+    ma.nsplit = nsplit;
+    ma.rows = p.group;
+    ma.row0 = 0;
+    ma.mrow = 0;
+    ma.mout = 0;
+    merge_dispatch<T, D>(ma, lane);
+  }
+}
 
 // Last step of a shared-prefix decode: each (sequence, head) merges the
 // shared prefix's (o, lse) with its own suffix's by log-sum-exp weights
@@ -1191,25 +1988,26 @@ struct DeviceState {
   int error = 0;  // PA_OK or the status the set-up failed with
   int sms = 0;
   Tuning tuning;
-  KernelConfig cfg[2][2];  // [bf16?][head_dim 128?]
+  KernelConfig cfg[2][2];   // [bf16?][head_dim 128?]
+  KernelConfig cfg2[2][2];  // the same for two query-row tiles (grouped decode, 8 warps)
 };
 DeviceState g_dev[kMaxDevices];
 
 
-template <typename T, int D, int W>
+template <typename T, int D, int W, int NT = 1>
 cudaError_t configure_kernel(KernelConfig* cfg, const Tuning& t, size_t optin, size_t per_sm) {
   // shared memory per CTA when `ctas_per_sm` CTAs share an SM (1 KiB reserved each)
   size_t budget = per_sm / t.ctas_per_sm - 1024;
   if (budget > optin) budget = optin;
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, W>,
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, W, NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(budget));
   if (e != cudaSuccess) return e;
-  int stages = Smem<D, W>::stages_for(budget);  // per math warp
+  int stages = Smem<D, W, NT>::stages_for(budget);  // per math warp
   if (stages > t.max_stages) stages = t.max_stages;
   cfg->stages = stages;
-  cfg->smem = Smem<D, W>::bytes(stages);
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg->ctas_per_sm, decode_kernel<T, D, W>,
-                                                    W * 32, cfg->smem);
+  cfg->smem = Smem<D, W, NT>::bytes(stages);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cfg->ctas_per_sm,
+                                                    decode_kernel<T, D, W, NT>, W * 32, cfg->smem);
   if (cfg->ctas_per_sm > t.ctas_per_sm) cfg->ctas_per_sm = t.ctas_per_sm;
   return e;
 }
@@ -1220,6 +2018,13 @@ cudaError_t configure_all(DeviceState& st, size_t optin, size_t per_sm) {
   if (e == cudaSuccess) e = configure_kernel<__nv_bfloat16, 64, W>(&st.cfg[1][0], st.tuning, optin, per_sm);
   if (e == cudaSuccess) e = configure_kernel<__half, 128, W>(&st.cfg[0][1], st.tuning, optin, per_sm);
   if (e == cudaSuccess) e = configure_kernel<__half, 64, W>(&st.cfg[0][0], st.tuning, optin, per_sm);
+  // the grouped decode always runs 8 math warps per CTA
+  if (e == cudaSuccess)
+    e = configure_kernel<__nv_bfloat16, 128, 8, 2>(&st.cfg2[1][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess)
+    e = configure_kernel<__nv_bfloat16, 64, 8, 2>(&st.cfg2[1][0], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 128, 8, 2>(&st.cfg2[0][1], st.tuning, optin, per_sm);
+  if (e == cudaSuccess) e = configure_kernel<__half, 64, 8, 2>(&st.cfg2[0][0], st.tuning, optin, per_sm);
   return e;
 }
 
@@ -1241,13 +2046,15 @@ int device_setup(int device) {
     st.error = e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     for (int a = 0; a < 2 && st.error == PA_OK; ++a)
       for (int d = 0; d < 2; ++d)
-        if (st.cfg[a][d].stages < 1 || st.cfg[a][d].ctas_per_sm < 1) st.error = PA_ERR_UNSUPPORTED;
+        if (st.cfg[a][d].stages < 1 || st.cfg[a][d].ctas_per_sm < 1 ||
+            st.cfg2[a][d].stages < 1 || st.cfg2[a][d].ctas_per_sm < 1)
+          st.error = PA_ERR_UNSUPPORTED;
   });
   if (st.error != PA_OK) return fail(st.error, "decode: per-device set-up failed on device %d", device);
   return PA_OK;
 }
 
-template <typename T, int D, int W>
+template <typename T, int D, int W, int NT = 1>
 int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) {
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   alignas(64) CUtensorMap mk, mv;
@@ -1265,7 +2072,7 @@ int launch_tc(Params prm, const KernelConfig& kc, int sms, cudaStream_t stream) 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<T, D, W>, mk, mv, prm);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<T, D, W, NT>, mk, mv, prm);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "decode: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
 }
@@ -1612,6 +2419,29 @@ struct GroupedLayout {
   SharedLayout sh;
   size_t sfx_tables, sfx_ctx, seq_blocks, total;
 };
+// Workspace of the one-launch cascade (a grouped decode): the decode
+// workspace with one more split per sequence (a sequence's shared splits and
+// own splits can round up once each), then each group's checked shared
+// blocks, each sequence's shared blocks and its clamped context.
+struct FusedLayout {
+  Layout dec;
+  size_t gp, seq_prefix, seq_ctx, seq_group, seq_chunk, chunk_plan, total;
+};
+FusedLayout fused_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int max_blocks_per_seq) {
+  FusedLayout l;
+  l.dec = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                           max_blocks_per_seq + kMinSplitBlocks);
+  l.gp = l.dec.total;
+  l.seq_prefix = align256(l.gp + size_t(num_seqs) * 4 + 4);
+  l.seq_ctx = align256(l.seq_prefix + size_t(num_seqs) * 4);
+  l.seq_group = align256(l.seq_ctx + size_t(num_seqs) * 4);
+  l.seq_chunk = align256(l.seq_group + size_t(num_seqs) * 4);
+  l.chunk_plan = align256(l.seq_chunk + size_t(num_seqs) * 8);
+  l.total = align256(l.chunk_plan + size_t(num_seqs) * 16);
+  return l;
+}
+
 GroupedLayout grouped_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                              int max_blocks_per_seq) {
   GroupedLayout l;
@@ -1636,7 +2466,9 @@ PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
   if (layout_too_large(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq))
     return fail(PA_ERR_INVALID_ARG,
                 "shared_prefix_workspace_size: these shapes need an impossibly large workspace");
-  *bytes = shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
+  *bytes = std::max(
+      shared_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total,
+      fused_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total);
   return PA_OK;
 }
 
@@ -1645,6 +2477,155 @@ PA_API int pa_paged_attention_decode_shared_prefix_workspace_size(
 namespace {
 
 enum class SharedMode { kPlanAndRun, kPlanOnly, kRunOnly };
+
+// Which cascade implementation an entry point uses: the three phases (the
+// prefix phase on the chunked-prefill kernels, the suffix decode, the
+// combine) or the grouped decode (one attention launch over shared and own
+// units, then one merge launch).  Measured on GB300 (8B-shaped GQA): 128
+// forked branches in groups of 4 sharing 64 blocks take 50 us per layer
+// grouped against 52 in phases; 100 requests on one 64-block prefix take 76
+// in phases against 91 grouped (the phases read the prefix once for all 400
+// query rows; the grouped decode once per 16).  So the grouped entry points
+// use the grouped decode and the single-prefix ones the phases;
+// PA_CASCADE=phases or =grouped makes every entry point use one of them.
+// Read once per process.
+enum class CascadeImpl { kDefault, kPhases, kGrouped };
+CascadeImpl cascade_impl() {
+  static const CascadeImpl impl = [] {
+    const char* v = std::getenv("PA_CASCADE");
+    if (v && std::strcmp(v, "phases") == 0) return CascadeImpl::kPhases;
+    if (v && std::strcmp(v, "grouped") == 0) return CascadeImpl::kGrouped;
+    return CascadeImpl::kDefault;
+  }();
+  return impl;
+}
+
+// The one-launch cascade.  group_start == null: one group of every sequence
+// sharing `single_blocks` leading blocks.  kPlanOnly reads the lengths, the
+// tables and the group arrays (q, the caches and out may be NULL); kRunOnly
+// reads the lengths the plan copied into the workspace.
+int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens,
+                       const int32_t* group_start, const int32_t* group_blocks, int num_groups,
+                       int single_blocks, int num_seqs, int num_q_heads, int num_kv_heads,
+                       int head_dim, int max_blocks_per_seq, int num_blocks, float scale,
+                       int dtype, void* out, void* workspace, size_t workspace_bytes,
+                       cudaStream_t s, const char* who, const AppendArgs& app) {
+  const FusedLayout fl =
+      fused_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < fl.total)
+    return fail(PA_ERR_INVALID_ARG, "%s: workspace NULL, unaligned or < %zu bytes", who, fl.total);
+  const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* seq_ctx = reinterpret_cast<int32_t*>(ws + fl.seq_ctx);
+  int rc = PA_OK;
+  // the grouped plan checks the members' tables; one shared prefix is
+  // checked by the run (its plan gets no tables)
+  if (plans && (!context_lens || (group_start && !block_tables)))
+    return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (runs) {
+    rc = check_run_args(q, k_cache, v_cache, block_tables, seq_ctx, out, num_kv_heads, num_blocks,
+                        who);
+    if (rc != PA_OK) return rc;
+  }
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kMaxDevices)
+    return fail(PA_ERR_CUDA, "%s: no current CUDA device", who);
+  rc = device_setup(device);
+  if (rc != PA_OK) return rc;
+  unsigned* status = device_status_word();
+  if (!status) return PA_ERR_CUDA;
+  const DeviceState& st = g_dev[device];
+  const int signature = plan_signature(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                       max_blocks_per_seq,
+                                       st.tuning.split_blocks ? st.tuning.split_blocks
+                                                              : kSplitBlocks,
+                                       0, 1);
+  const KernelConfig& kc2 = st.cfg2[dtype == PA_BF16][head_dim == 128];
+  if (plans) {
+    Params prm = make_params(context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                             max_blocks_per_seq, workspace, fl.dec, status);
+    prm.block_tables = group_start ? block_tables : nullptr;
+    prm.signature = signature;
+    const int nwarps = st.sms * kc2.ctas_per_sm * 8;
+    prm.piece_blocks = st.tuning.piece_blocks;
+    prm.tail_blocks = st.tuning.tail_waves * nwarps * prm.piece_blocks;
+    GroupArgs ga;
+    ga.group_start = group_start;
+    ga.group_blocks = group_blocks;
+    ga.num_groups = group_start ? num_groups : 1;
+    ga.single_blocks = single_blocks;
+    ga.chunk = 16 / (num_q_heads / num_kv_heads);
+    ga.nwarps = nwarps;
+    ga.gp = reinterpret_cast<int32_t*>(ws + fl.gp);
+    ga.seq_prefix = reinterpret_cast<int32_t*>(ws + fl.seq_prefix);
+    ga.seq_ctx = seq_ctx;
+    ga.seq_group = reinterpret_cast<int32_t*>(ws + fl.seq_group);
+    ga.seq_chunk = reinterpret_cast<int2*>(ws + fl.seq_chunk);
+    ga.chunk_plan = reinterpret_cast<int4*>(ws + fl.chunk_plan);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(kGroupedPlanThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_plan_kernel, prm, ga);
+    if (e != cudaSuccess)
+      return fail(PA_ERR_CUDA, "%s: plan launch failed: %s", who, cudaGetErrorString(e));
+  }
+  if (!runs) return PA_OK;
+  Params prm = make_params(seq_ctx, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                           max_blocks_per_seq, workspace, fl.dec, status);
+  prm.seq_prefix = reinterpret_cast<const int32_t*>(ws + fl.seq_prefix);
+  prm.verify_prefix = group_start == nullptr;
+  prm.defer_merge = 1;
+  prm.signature = signature;
+  prm.q = q;
+  prm.k_cache = k_cache;
+  prm.v_cache = v_cache;
+  prm.out = out;
+  prm.block_tables = block_tables;
+  prm.num_blocks = num_blocks;
+  prm.scale = scale;
+  prm.scale_log2 = scale * 1.4426950408889634f;
+  if (app.slot_mapping) {
+    prm.k_new = app.k_new;
+    prm.v_new = app.v_new;
+    prm.slot_mapping = app.slot_mapping;
+  }
+  if (dtype == PA_BF16)
+    rc = head_dim == 128 ? launch_tc<__nv_bfloat16, 128, 8, 2>(prm, kc2, st.sms, s)
+                         : launch_tc<__nv_bfloat16, 64, 8, 2>(prm, kc2, st.sms, s);
+  else
+    rc = head_dim == 128 ? launch_tc<__half, 128, 8, 2>(prm, kc2, st.sms, s)
+                         : launch_tc<__half, 64, 8, 2>(prm, kc2, st.sms, s);
+  if (rc != PA_OK) return rc;
+  // the merges, one warp per (sequence, KV head)
+  const long long pairs = (long long)num_seqs * num_kv_heads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(std::min<long long>((pairs + 7) / 8, (long long)st.sms * 8)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  if (dtype == PA_BF16)
+    e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 128>, prm)
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 64>, prm);
+  else
+    e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<__half, 128>, prm)
+                        : cudaLaunchKernelEx(&cfg, merge_kernel<__half, 64>, prm);
+  if (e != cudaSuccess)
+    return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
+  return PA_OK;
+}
 
 // The cascade decode: the prefix phase, each sequence's own blocks, the
 // combine.  kPlanOnly launches the two plans (they read only the lengths and
@@ -1688,6 +2669,11 @@ int shared_prefix_impl(SharedMode mode, const void* q, const void* k_cache, cons
   }
   if (runs && (!q || !k_cache || !v_cache || !block_tables || !out))
     return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (cascade_impl() == CascadeImpl::kGrouped)
+    return fused_cascade_impl(mode, q, k_cache, v_cache, block_tables, context_lens, nullptr,
+                              nullptr, 1, prefix_blocks, num_seqs, num_q_heads, num_kv_heads,
+                              head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                              workspace, workspace_bytes, s, who, app);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* po = reinterpret_cast<float*>(ws + sl.po);
   float* plse = reinterpret_cast<float*>(ws + sl.plse);
@@ -1786,6 +2772,11 @@ int grouped_prefix_impl(SharedMode mode, const void* q, const void* k_cache, con
   const bool plans = mode != SharedMode::kRunOnly, runs = mode != SharedMode::kPlanOnly;
   if (plans && (!context_lens || !block_tables))
     return fail(PA_ERR_INVALID_ARG, "%s: NULL pointer", who);
+  if (cascade_impl() != CascadeImpl::kPhases)
+    return fused_cascade_impl(mode, q, k_cache, v_cache, block_tables, context_lens, group_start,
+                              group_blocks, num_groups, 0, num_seqs, num_q_heads, num_kv_heads,
+                              head_dim, max_blocks_per_seq, num_blocks, scale, dtype, out,
+                              workspace, workspace_bytes, s, who, app);
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -1922,7 +2913,9 @@ PA_API int pa_paged_attention_decode_grouped_prefix_workspace_size(
                                PA_BF16, "paged_attention_decode_grouped_prefix_workspace_size");
   if (rc != PA_OK) return rc;
   if (!bytes) return fail(PA_ERR_INVALID_ARG, "grouped_prefix_workspace_size: bytes is NULL");
-  *bytes = grouped_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total;
+  *bytes = std::max(
+      grouped_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total,
+      fused_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq).total);
   return PA_OK;
 }
 

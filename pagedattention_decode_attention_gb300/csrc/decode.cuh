@@ -25,7 +25,10 @@ constexpr int kHdrSignature = 3;  // shape signature written by the plan
 // Views into the caller's workspace (all offsets 256-byte aligned).
 struct Workspace {
   int* header;       // see kHdr*
-  int* units;        // int4 per unit: b, first block, split index << 8 | blocks, ctx
+  // int4 per unit: (b, first block, split index << 16 | members << 8 | blocks,
+  // ctx); members is 0 for a unit of one sequence, else the number of
+  // consecutive sequences from b that share the unit's blocks (grouped plan)
+  int* units;
   int* arrivals;     // [num_seqs * num_kv_heads] finished splits per (b, kv head)
   int* nsplits;      // [num_seqs] splits the plan made of each sequence
   float* part_lse;   // [num_seqs][max_splits][num_q_heads]  (log2 domain)
@@ -76,10 +79,11 @@ inline bool layout_too_large(int num_seqs, int num_q_heads, int num_kv_heads, in
 // Identifies the shapes a plan was made for, so a run can refuse a workspace
 // planned for something else.
 inline int plan_signature(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                          int max_blocks_per_seq, int split_blocks, int table_offset = 0) {
+                          int max_blocks_per_seq, int split_blocks, int table_offset = 0,
+                          int grouped = 0) {
   uint32_t h = 2166136261u;
-  const int v[7] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
-                    split_blocks, table_offset};
+  const int v[8] = {num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                    split_blocks, table_offset, grouped};
   for (int x : v) {
     h ^= uint32_t(x);
     h *= 16777619u;
@@ -94,6 +98,15 @@ struct Params {
   void* out;
   const int32_t* block_tables;
   const int32_t* context_lens;
+  // Grouped mode (non-null): per sequence, the leading blocks it shares with
+  // its group (written by the grouped plan).  verify_prefix: the run checks
+  // that every table starts with sequence 0's seq_prefix[b] entries (the
+  // plan of a single shared prefix does not see the tables).
+  const int32_t* seq_prefix;
+  int verify_prefix;
+  // Grouped mode: the splits' results are only written; a separate merge
+  // launch merges them.
+  int defer_merge;
   // Fused append (all three null: none).  Row b of k_new / v_new
   // ([num_seqs][num_kv_heads][head_dim]) is sequence b's new token, stored at
   // slot_mapping[b] and attended as its token context_lens[b] - 1.

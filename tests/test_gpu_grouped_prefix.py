@@ -30,7 +30,8 @@ GROUPS = [("share", 1024, [0, 5, 300]),
           ("fork", 100, [1, 1, 20, 3]),
           ("share", 48, [1]),
           ("share", 160, [16, 17, 900, 2]),
-          ("fork", 512, [1, 16])]
+          ("fork", 512, [1, 16]),
+          ("share", 64, [3, 1, 2, 50, 7, 9])]   # more members than one shared unit holds
 
 
 def grouped_batch(groups, hq, hkv, d, dtype, seed, dev):

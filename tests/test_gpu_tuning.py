@@ -38,3 +38,19 @@ def test_prefill_parity_per_kernel(gpu, tc):
     r = subprocess.run([sys.executable, "-m", "tests.prefill_child"], cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+@pytest.mark.parametrize("impl", ["phases", "grouped"])
+def test_cascade_implementations(gpu, impl):
+    """The shared- and grouped-prefix entry points each on one cascade
+    implementation (PA_CASCADE, read once per process): the three phases
+    (prefix phase on the chunked-prefill kernels, suffix decode, combine) or
+    the grouped decode (one attention launch over shared and own units, one
+    merge launch).  By default the grouped entry points use the grouped
+    decode and the single-prefix ones the phases; both pass the same tests."""
+    env = dict(os.environ, PA_CASCADE=impl)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p",
+                        "no:cacheprovider", "tests/test_gpu_shared_prefix.py",
+                        "tests/test_gpu_grouped_prefix.py"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=1200)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]

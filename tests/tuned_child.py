@@ -33,6 +33,21 @@ def main() -> int:
         for o in outs:
             assert_attention_close(o, ref, TORCH_DTYPES[dt])
         assert torch.equal(outs[0], outs[1])
+    # the grouped decode's plan under the same split, tail and piece settings
+    import numpy as np
+
+    import oracle.attention as oa
+    from tests.gpu_helpers import to_f32_numpy
+    from tests.test_gpu_grouped_prefix import GROUPS, grouped_batch
+    for hq, hkv, d, dt in ((32, 8, 128, "bf16"), (16, 2, 64, "f16")):
+        q, kc, vc, tables, lens, gs, gb = grouped_batch(GROUPS, hq, hkv, d, dt, seed=77, dev=dev)
+        bt, cl, gs_d, gb_d = (torch.from_numpy(a).to(dev) for a in (tables, lens, gs, gb))
+        scale = 1.0 / np.sqrt(d)
+        out = pa.paged_attention_decode_grouped_prefix(q, kc, vc, bt, cl, gs_d, gb_d, scale)
+        pa.check_status()
+        ref = oa.paged_attention_decode(to_f32_numpy(q), to_f32_numpy(kc), to_f32_numpy(vc),
+                                        tables, lens, scale)
+        assert_attention_close(out, ref, TORCH_DTYPES[dt])
     return 0
 
 
