@@ -329,11 +329,27 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   __syncthreads();
   // pass 3: place the units, claim partial slots and arrival counters for
   // the split ones.  Unit = {b, qb, first block, blocks} {split << 16 | nsplit,
-  // first partial slot, arrival group, ctx}.
+  // first partial slot, arrival group, ctx}.  A sequence's units of one size
+  // bucket take consecutive places, query block after query block, so the
+  // query blocks of a (sequence, KV head) run at about the same time on
+  // different SMs and read its K/V tiles while they are in L2.
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
     int ctx, qlen;
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + ROWS - 1) / ROWS;
+    int at[kSizeBuckets];
+#pragma unroll
+    for (int r = 0; r < kSizeBuckets; ++r) at[r] = 0;
+    for (int qb = 0; qb < nq; ++qb) {
+      const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
+      const int ns = nsplits_of(nb, split);
+      const int base = nb / ns, big = nb - base * ns;
+      if (big) at[size_bucket(base + 1)] += big;
+      if (ns - big) at[size_bucket(base)] += ns - big;
+    }
+#pragma unroll
+    for (int r = 0; r < kSizeBuckets; ++r)
+      if (at[r]) at[r] = atomicAdd(&bucket[r], at[r]);
     for (int qb = 0; qb < nq; ++qb) {
       const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
       const int ns = nsplits_of(nb, split);
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       int first = 0;
       for (int s = 0; s < ns; ++s) {
         const int n = s < big ? base + 1 : base;
-        const int pos = atomicAdd(&bucket[size_bucket(n)], 1);
+        const int pos = at[size_bucket(n)]++;
         p.units[2 * pos] = make_int4(b, qb, first, n);
         p.units[2 * pos + 1] = make_int4((s << 16) | ns, slot, grp, ctx);
         first += n;
