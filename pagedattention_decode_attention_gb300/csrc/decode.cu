@@ -43,6 +43,14 @@
 //    every run.
 //  * Every wait is an mbarrier wait with a time limit; running out sets the
 //    timeout bit of the device status word and the warp returns.
+//  * Grouped decode (sequences in groups that share leading blocks): the same
+//    kernel with two row tiles per item (up to 16 query rows: G heads of up
+//    to 16 / G members of a group), planned by grouped_plan_kernel.  A shared
+//    unit reads a split of the group's shared blocks once for its members'
+//    rows; an own unit covers one sequence's blocks past them; a small chunk
+//    takes its members' own blocks into its last shared unit, each block's
+//    scores masked to its member's rows.  The splits are merged by a merge
+//    launch after the attention.
 //
 // An fp32 path (CUDA cores, one warp per (sequence, head), online softmax in
 // natural base) serves float32 caches; it is exact to fp32 rounding and is not
