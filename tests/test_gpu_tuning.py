@@ -51,6 +51,7 @@ def test_cascade_implementations(gpu, impl):
     env = dict(os.environ, PA_CASCADE=impl)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p",
                         "no:cacheprovider", "tests/test_gpu_shared_prefix.py",
-                        "tests/test_gpu_grouped_prefix.py"], cwd=ROOT, env=env,
+                        "tests/test_gpu_grouped_prefix.py", "tests/test_gpu_grouped_random.py"],
+                       cwd=ROOT, env=env,
                        capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
