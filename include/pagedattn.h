@@ -31,6 +31,12 @@
  *   PA_ERR_DEVICE_TIMEOUT in the same word instead of hanging.
  * - Element types: PA_F32, PA_F16, PA_BF16.  Caches, queries, new K/V and the
  *   output all share one dtype per call.  head_dim is 64 or 128.
+ * - Shapes whose workspace would come near the range of size_t are refused
+ *   (PA_ERR_INVALID_ARG) by every entry point and workspace-size query.
+ * - Every compute entry point opens an NVTX range named after itself in the
+ *   "pagedattn" domain, so an NVTX-aware profiler attributes each call and
+ *   the kernels it launched; without a profiler attached this costs a test
+ *   of an unset function pointer.
  *
  * Layouts (row-major, contiguous)
  * -------------------------------
