@@ -58,6 +58,7 @@ def test_random_grouped_batches_with_append(gpu, seed):
     pos = lens.astype(np.int64) - 1
     slots = tables[np.arange(b), pos // 16].astype(np.int64) * 16 + pos % 16
     slots[pos < first_private] = -1
+    slots[gen.random(b) < 0.15] = -1           # padding rows: nothing stored for them
     k_new = wl.normal((b, hkv, d), dt, 7200 + seed, gpu)
     v_new = wl.normal((b, hkv, d), dt, 7300 + seed, gpu)
     host_k, host_v = to_f32_numpy(kc), to_f32_numpy(vc)
