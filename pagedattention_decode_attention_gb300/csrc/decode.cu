@@ -287,8 +287,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
 // `chunk` members at once (their m * G query rows read every block once),
 // and an own unit a split of one sequence's blocks past the shared ones.  A
 // sequence's splits are its group's shared splits (indices 0 ..) followed by
-// its own; the warp that completes the last of them merges them, as in the
-// plain decode, so the whole cascade is one attention launch.
+// its own; a merge launch after the attention merges them.
 struct GroupArgs {
   const int32_t* group_start;   // [num_groups + 1], or null: one group of every sequence
   const int32_t* group_blocks;  // [num_groups] shared blocks, or null: single_blocks
@@ -320,12 +319,10 @@ __device__ __forceinline__ int group_of(const GroupArgs& ga, int b) {
 // ones add up to at most kAbsorbBlocks takes them into its last shared unit:
 // one unit then covers the chunk's last shared blocks (every row) and each
 // member's own blocks (its rows only), so the members need no units of their
-// own, all of them have the same splits, and the chunk's splits are counted
-// and merged together.
+// own and all of them have the same splits.
 constexpr int kAbsorbMembers = 4;
 constexpr int kAbsorbBlocks = 16;
-// flags in the blocks byte of a unit (blocks <= 32 use bits 0-5)
-constexpr int kUnitChunk = 0x40;  // the chunk's splits are counted and merged together
+// flag in the blocks byte of a unit (blocks <= 32 use bits 0-5)
 constexpr int kUnitOwn = 0x80;    // the unit also covers the members' own blocks
 constexpr int kUnitBlocks = 0x3f;
 
@@ -601,7 +598,7 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   // pass 3: place the units.  Own units: (b, first block, split index << 16
   // | blocks, context), split indices after the chunk's shared ones.
   // Shared units: (first member, first block, split index << 16 | members
-  // << 8 | flags | blocks, shared tokens).
+  // << 8 | kUnitOwn for a last split that absorbs | blocks, shared tokens).
   for (int b = tid; b < p.num_seqs; b += NT) {
     int own, pn;
     own_and_shared(b, own, pn);
@@ -640,7 +637,6 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
     if (b != cm.x || P == 0) continue;
     // this thread places its chunk's shared units
     const int4 c = ga.chunk_plan[b];
-    const int flags = c.x ? kUnitChunk : 0;
     int sn, sbase, sbig;
     if (c.x) {
       sn = c.z - 1;  // the parts before the last split
@@ -653,12 +649,12 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
     for (int s = 0; s < sn; ++s) {
       const int sz = s < sbig ? sbase + 1 : sbase;
       const int pos = atomicAdd(&bucket[sz], 1);
-      units[pos] = make_int4(b, off, (s << 16) | (cm.y << 8) | flags | sz, P * kBlockSize);
+      units[pos] = make_int4(b, off, (s << 16) | (cm.y << 8) | sz, P * kBlockSize);
       off += sz;
     }
     if (c.x) {
       const int pos = atomicAdd(&bucket[c.w + c.y], 1);
-      units[pos] = make_int4(b, off, ((c.z - 1) << 16) | (cm.y << 8) | kUnitChunk | kUnitOwn | c.w,
+      units[pos] = make_int4(b, off, ((c.z - 1) << 16) | (cm.y << 8) | kUnitOwn | c.w,
                              P * kBlockSize);
     }
   }
@@ -673,35 +669,24 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
 // round, then lane l owns the float4 columns c = l + 32 k (k < NK) of the
 // group's G x D outputs and issues the loads of U splits at once.
 // Where the partial results of one (b, g) live and where its merge goes.
-// A merge covers `rows` (<= 8) query rows from row0 of a group of members:
-// row r belongs to member r / G (consecutive sequences from b) and query
-// head g G + r % G; one member's rows are the plain case (row0 0, rows G).
 struct MergeArgs {
   const float* lse;   // part_lse at (b, split 0, head g G); split stride Hq
   const float4* po;   // part_o at the same row, as float4
   void* out;          // out row of head g G of sequence b
-  float* cas_o;       // suffix mode: fp32 o rows of head g G (else null; one member only)
+  float* cas_o;       // suffix mode: fp32 o rows of head g G (else null)
   float* cas_lse;     // suffix mode: base-2 log-sum-exp of head g G
   int G, Hq, nsplit;
-  int rows, row0;
-  size_t mrow;        // part rows (lse entries) between consecutive members: max_splits Hq
-  size_t mout;        // out elements between consecutive members: Hq D
 };
 
 template <typename T, int D, int NK>
 __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
   using M = dev::Mma<T>;
   constexpr int U = NK >= 6 ? 2 : 16 / NK;
-  const int G = a.G, Hq = a.Hq, nsplit = a.nsplit, rows = a.rows;
-  const int C = rows * D / 4;  // float4 columns of the merged rows
+  const int G = a.G, Hq = a.Hq, nsplit = a.nsplit;
+  const int C = G * D / 4;  // float4 columns of the group's outputs
   const float* lse = a.lse;
   const float4* po = a.po;
-  // part row (lse index) of merged row r at split 0: its member's, its head's
-  auto prow = [&](int r) -> size_t {
-    if (a.mrow == 0) return size_t(r);  // one member's rows
-    const int R = a.row0 + r;
-    return size_t(R / G) * a.mrow + size_t(R % G);
-  };
+  const size_t split4 = size_t(Hq) * D / 4;  // float4s between two splits
 
   // ---- per head: the largest lse and the sum of 2^(lse - largest)
   float hm[kMaxGroup], hl[kMaxGroup];
@@ -714,10 +699,10 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
     float x[kMaxGroup];
 #pragma unroll
     for (int hh = 0; hh < kMaxGroup; ++hh)
-      x[hh] = hh < rows ? __ldcg(lse + prow(hh) + size_t(sp) * Hq) : -INFINITY;
+      x[hh] = hh < G ? __ldcg(lse + size_t(sp) * Hq + hh) : -INFINITY;
 #pragma unroll
     for (int hh = 0; hh < kMaxGroup; ++hh) {
-      if (hh < rows) {
+      if (hh < G) {
         const float mn = fmaxf(hm[hh], x[hh]);
         hl[hh] = hl[hh] * dev::fast_exp2(hm[hh] - mn) + dev::fast_exp2(x[hh] - mn);
         hm[hh] = mn;
@@ -726,7 +711,7 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
   }
 #pragma unroll
   for (int hh = 0; hh < kMaxGroup; ++hh) {
-    if (hh < rows) {
+    if (hh < G) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, hm[hh], off);
@@ -764,10 +749,8 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
       for (int k = 0; k < NK; ++k) {
         const int sp = sp0 + u, c = lane + 32 * k;
         const bool on = sp < nsplit && c < C;
-        const size_t pr = on ? prow((4 * c) / D) : 0;  // merged row of column c
-        v[u][k] = on ? __ldcg(po + (pr + size_t(sp) * Hq) * (D / 4) + c % (D / 4))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-        w[u][k] = on ? __ldcg(lse + pr + size_t(sp) * Hq) : -INFINITY;
+        v[u][k] = on ? __ldcg(po + size_t(sp) * split4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[u][k] = on ? __ldcg(lse + size_t(sp) * Hq + (4 * c) / D) : -INFINITY;
       }
     }
 #pragma unroll
@@ -792,16 +775,14 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
         *reinterpret_cast<float4*>(a.cas_o + 4 * c) =
             make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv);
       } else {
-        const int R = a.row0 + (4 * c) / D;  // its member's out row, its head's columns
         uint2 pk;
         pk.x = M::pack(acc[k].x * inv, acc[k].y * inv);
         pk.y = M::pack(acc[k].z * inv, acc[k].w * inv);
-        *reinterpret_cast<uint2*>(orow + size_t(R / G) * a.mout + size_t(R % G) * D +
-                                  4 * (c % (D / 4))) = pk;
+        *reinterpret_cast<uint2*>(orow + 4 * c) = pk;
       }
     }
   }
-  if (a.cas_lse && lane < rows) {
+  if (a.cas_lse && lane < G) {
     // lse of head `lane` = its largest lse plus log2 of its weight sum
     float mh = hm[0], lh = hl[0];
 #pragma unroll
@@ -816,7 +797,7 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
 
 template <typename T, int D>
 __device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
-  const int nk = (a.rows * D / 4 + 31) / 32;
+  const int nk = (a.G * D / 4 + 31) / 32;
   switch (nk) {
     case 1: merge_splits<T, D, 1>(a, lane); break;
     case 2: merge_splits<T, D, 2>(a, lane); break;
@@ -843,7 +824,7 @@ struct Item {
   int b;  // sequence (first member), or -1 once the work list is exhausted
   int g, s, nblk, first, ctx, nsplit;
   int m, rows;  // members and query rows
-  int flags;    // kUnitChunk, kUnitOwn of the unit
+  int flags;    // kUnitOwn of the unit
   int phys;
   // kUnitOwn items, lane j for block j: the member the block belongs to (-1:
   // shared by all rows), its tokens in context, and the row of the member's
@@ -1042,7 +1023,7 @@ __global__ void __launch_bounds__(W * 32)
       nxt.s = cu.z >> 16;
       nxt.m = (cu.z >> 8) & 0xff;
       nxt.nblk = cu.z & kUnitBlocks;
-      nxt.flags = cu.z & (kUnitChunk | kUnitOwn);
+      nxt.flags = cu.z & kUnitOwn;
       nxt.ctx = cu.w;
       // a unit shared by several members (grouped plans only)
       if (nxt.m < 1 || NT == 1 || nxt.m * G > 8 * NT || nxt.b + nxt.m > p.num_seqs) {
@@ -1542,10 +1523,6 @@ __global__ void __launch_bounds__(W * 32)
           ma.G = G;
           ma.Hq = Hq;
           ma.nsplit = nsplit;
-          ma.rows = G;
-          ma.row0 = 0;
-          ma.mrow = 0;
-          ma.mout = 0;
           merge_dispatch<T, D>(ma, lane);
           if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
 #ifdef PA_PROFILE_TIMES
@@ -1555,7 +1532,9 @@ __global__ void __launch_bounds__(W * 32)
       }
     } else {
       // Rows of several members: row r belongs to sequence b + r / G, query
-      // head g G + r % G, and each member has its own split count.
+      // head g G + r % G, and each member has its own split count.  A
+      // member's only split writes its output; otherwise the split's result
+      // goes to the member's split slot for the merge launch.
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -1622,89 +1601,7 @@ __global__ void __launch_bounds__(W * 32)
           static_cast<uint4*>(const_cast<void*>(isv ? p.v_cache : p.k_cache))[dst] = mkv[i];
         }
       }
-      if (p.defer_merge) {
-        // the merge launch after this one merges every split set
-      } else if (cur.flags & kUnitChunk) {
-        // Every member of the chunk has the chunk's splits: they are counted
-        // on the first member's counter (release), and the warp that
-        // completes the set merges all the chunk's rows, eight at a time.
-        __syncwarp();
-        int last = 0;
-        if (lane == 0 && nsplit > 1)
-          last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b) * Hkv + g], 1) == nsplit - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-#ifdef PA_PROFILE_TIMES
-          const unsigned long long merge_t0 = dev::global_timer_ns();
-#endif
-          __syncwarp();
-          const size_t head0 = size_t(b) * Hq + size_t(g) * G;
-          const size_t row0 = size_t(b) * p.max_splits * Hq + size_t(g) * G;
-          for (int r0 = 0; r0 < rows; r0 += 8) {
-            MergeArgs ma;
-            ma.lse = p.ws.part_lse + row0;
-            ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
-            ma.out = static_cast<T*>(p.out) + head0 * D;
-            ma.cas_o = nullptr;
-            ma.cas_lse = nullptr;
-            ma.G = G;
-            ma.Hq = Hq;
-            ma.nsplit = nsplit;
-            ma.rows = rows - r0 < 8 ? rows - r0 : 8;
-            ma.row0 = r0;
-            ma.mrow = size_t(p.max_splits) * Hq;
-            ma.mout = size_t(Hq) * D;
-            merge_dispatch<T, D>(ma, lane);
-          }
-          if (lane == 0) p.ws.arrivals[size_t(b) * Hkv + g] = 0;  // ready for the next run
-#ifdef PA_PROFILE_TIMES
-          merge_ns += dev::global_timer_ns() - merge_t0;
-#endif
-        }
-      } else {
-      // Publish and count: lane i counts this split for member i (release);
-      // the warp that completes a member's (sequence, g) merges it.
-      const int members = cur.m;
-      __syncwarp();
-      int last = 0, nsl = 0;
-      if (lane < members) {
-        nsl = lane == 0 ? nsplit : __ldg(&p.ws.nsplits[b + lane]);
-        if (nsl > 1)
-          last = dev::atom_add_acq_rel_gpu(&p.ws.arrivals[size_t(b + lane) * Hkv + g], 1) ==
-                 nsl - 1;
-      }
-      unsigned lastmask = __ballot_sync(0xffffffffu, last);
-      while (lastmask) {
-        const int i = __ffs(lastmask) - 1;
-        lastmask &= lastmask - 1;
-        const int bi = b + i;
-        const int nsi = __shfl_sync(0xffffffffu, nsl, i);
-#ifdef PA_PROFILE_TIMES
-        const unsigned long long merge_t0 = dev::global_timer_ns();
-#endif
-        __syncwarp();
-        const size_t head0 = size_t(bi) * Hq + size_t(g) * G;
-        const size_t row0 = size_t(bi) * p.max_splits * Hq + size_t(g) * G;
-        MergeArgs ma;
-        ma.lse = p.ws.part_lse + row0;
-        ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
-        ma.out = static_cast<T*>(p.out) + head0 * D;
-        ma.cas_o = p.cas_o ? p.cas_o + head0 * D : nullptr;
-        ma.cas_lse = p.cas_lse ? p.cas_lse + head0 : nullptr;
-        ma.G = G;
-        ma.Hq = Hq;
-        ma.nsplit = nsi;
-        ma.rows = G;
-        ma.row0 = 0;
-        ma.mrow = 0;
-        ma.mout = 0;
-        merge_dispatch<T, D>(ma, lane);
-        if (lane == 0) p.ws.arrivals[size_t(bi) * Hkv + g] = 0;  // ready for the next run
-#ifdef PA_PROFILE_TIMES
-        merge_ns += dev::global_timer_ns() - merge_t0;
-#endif
-      }
-      }
+      // (the merge launch after this one merges every sequence's splits)
     }
 #ifdef PA_PROFILE_TIMES
     ITEM_TRACE(n_items, item_t0, nblk, nsplit, merge_ns, qwait_ns);
@@ -1808,10 +1705,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const Params p) {
     ma.G = p.group;
     ma.Hq = p.num_q_heads;
     ma.nsplit = nsplit;
-    ma.rows = p.group;
-    ma.row0 = 0;
-    ma.mrow = 0;
-    ma.mout = 0;
     merge_dispatch<T, D>(ma, lane);
   }
 }
@@ -2590,7 +2483,6 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
                            max_blocks_per_seq, workspace, fl.dec, status);
   prm.seq_prefix = reinterpret_cast<const int32_t*>(ws + fl.seq_prefix);
   prm.verify_prefix = group_start == nullptr;
-  prm.defer_merge = 1;
   prm.signature = signature;
   prm.q = q;
   prm.k_cache = k_cache;

@@ -104,9 +104,6 @@ struct Params {
   // plan of a single shared prefix does not see the tables).
   const int32_t* seq_prefix;
   int verify_prefix;
-  // Grouped mode: the splits' results are only written; a separate merge
-  // launch merges them.
-  int defer_merge;
   // Fused append (all three null: none).  Row b of k_new / v_new
   // ([num_seqs][num_kv_heads][head_dim]) is sequence b's new token, stored at
   // slot_mapping[b] and attended as its token context_lens[b] - 1.
