@@ -299,18 +299,28 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
   __syncthreads();
   const int split = s_split < 0 ? -s_split : 0;  // 0: no splitting
 
-  // pass 2: sizes of the units (a query block's splits are balanced)
-  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+  // pass 2: the work list is ordered by size, largest first, at the grain
+  // of sequences: all of a sequence's units go into the size bucket of its
+  // largest one, next to each other, so the query blocks of a (sequence, KV
+  // head) run at about the same time on different SMs and read its K/V
+  // tiles while they are in L2.  (A query block's splits are balanced.)
+  auto units_of = [&](int b, int& count, int& largest) {
     int ctx, qlen;
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + ROWS - 1) / ROWS;
+    count = 0;
+    largest = 0;
     for (int qb = 0; qb < nq; ++qb) {
       const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
       const int ns = nsplits_of(nb, split);
-      const int base = nb / ns, big = nb - base * ns;
-      if (big) atomicAdd(&hist[size_bucket(base + 1)], big);
-      if (ns - big) atomicAdd(&hist[size_bucket(base)], ns - big);
+      count += ns;
+      largest = max(largest, (nb + ns - 1) / ns);
     }
+  };
+  for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    int count, largest;
+    units_of(b, count, largest);
+    if (count) atomicAdd(&hist[size_bucket(largest)], count);
   }
   __syncthreads();
   if (tid == 0) {
@@ -327,30 +337,19 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
     p.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
-  // pass 3: place the units, claim partial slots and arrival counters for
-  // the split ones.  Unit = {b, qb, first block, blocks} {split << 16 | nsplit,
-  // first partial slot, arrival group, ctx}.  A sequence's units of one size
-  // bucket take consecutive places, query block after query block, so the
-  // query blocks of a (sequence, KV head) run at about the same time on
-  // different SMs and read its K/V tiles while they are in L2.
+  // pass 3: place the units (the last query block, the largest, first),
+  // claim partial slots and arrival counters for the split ones.  Unit =
+  // {b, qb, first block, blocks} {split << 16 | nsplit, first partial slot,
+  // arrival group, ctx}.
   for (int b = tid; b < p.num_seqs; b += kPlanThreads) {
+    int count, largest;
+    units_of(b, count, largest);
+    if (count == 0) continue;
+    int pos = atomicAdd(&bucket[size_bucket(largest)], count);
     int ctx, qlen;
     chunk(b, ctx, qlen);
     const int nq = (qlen * G + ROWS - 1) / ROWS;
-    int at[kSizeBuckets];
-#pragma unroll
-    for (int r = 0; r < kSizeBuckets; ++r) at[r] = 0;
-    for (int qb = 0; qb < nq; ++qb) {
-      const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
-      const int ns = nsplits_of(nb, split);
-      const int base = nb / ns, big = nb - base * ns;
-      if (big) at[size_bucket(base + 1)] += big;
-      if (ns - big) at[size_bucket(base)] += ns - big;
-    }
-#pragma unroll
-    for (int r = 0; r < kSizeBuckets; ++r)
-      if (at[r]) at[r] = atomicAdd(&bucket[r], at[r]);
-    for (int qb = 0; qb < nq; ++qb) {
+    for (int qb = nq - 1; qb >= 0; --qb) {
       const int nb = qblock_blocks<ROWS>(ctx, qlen, G, qb, shared);
       const int ns = nsplits_of(nb, split);
       const int base = nb / ns, big = nb - base * ns;
@@ -363,9 +362,9 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const Params
       int first = 0;
       for (int s = 0; s < ns; ++s) {
         const int n = s < big ? base + 1 : base;
-        const int pos = at[size_bucket(n)]++;
         p.units[2 * pos] = make_int4(b, qb, first, n);
         p.units[2 * pos + 1] = make_int4((s << 16) | ns, slot, grp, ctx);
+        ++pos;
         first += n;
       }
     }
@@ -965,7 +964,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp >= 8) dev::setmaxnreg_dec<kTcRegsProducer>();
   if (warp == 8) {
     // ====================================================== producer warp
-    const uint64_t policy = dev::l2_policy_evict_first();
+    // every query block of a (sequence, KV head) reads its K/V tiles: keep
+    // them in L2 for the query blocks that run beside this one
+    const uint64_t policy = dev::l2_policy_evict_last();
     PF_DECL;
     int kt = 0;  // K / V tiles loaded so far
     int qn = 0;  // query-tile loads so far
