@@ -17,24 +17,25 @@
 //    of a decode step.
 //  * persistent attention kernel, one CTA of W math warps per SM.  Each warp
 //    works alone: it claims whole work items from a global counter (its first
-//    item is dealt statically), and streams every block of them through its
-//    own small ring, issuing the 2-D tensor copies (128-byte swizzled, L2
-//    evict-first) of a block's K and V tiles a few blocks before it needs
-//    them.  The claim of the next item is pipelined over the last blocks of
-//    the current one (counter reply, work unit, block-table entries with one
-//    entry per lane, then a bulk copy of the G query rows), so a warp commits
-//    to an item only shortly before it starts it and the work left in the
-//    list goes to whichever warp frees up first.  Many independent issuers
-//    keep HBM busy; a single issuing thread per CTA could not (each copy
-//    instruction costs it hundreds of cycles), and no CTA-wide barrier is
-//    needed.  Per 16-token block: S^T = K . Q^T on the tensor cores
-//    (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of the group,
-//    K = head_dim), online softmax in base 2 with per-head running max / sum,
-//    P rounded to the input type and transposed in registers (movmatrix),
-//    O^T += V^T . P^T (M = head_dim rows of V^T via ldmatrix.trans).  Each K/V
-//    tile is read from HBM once for the whole query group.  Slots past the
-//    context in the last block are zeroed in registers, so whatever bits they
-//    hold cannot reach the output.
+//    item is dealt statically: W consecutive items per CTA, or round robin over
+//    the SMs when the list is shorter than the warps, so that it still spreads
+//    over every SM), and streams every block of them through its own small ring,
+//    issuing the 2-D tensor copies (128-byte swizzled, L2 evict-first) of a
+//    block's K and V tiles a few blocks before it needs them.  The claim of the
+//    next item is pipelined over the last blocks of the current one (counter
+//    reply, work unit, block-table entries with one entry per lane, then a bulk
+//    copy of the G query rows), so a warp commits to an item only shortly before
+//    it starts it and the work left in the list goes to whichever warp frees up
+//    first.  Many independent issuers keep HBM busy; a single issuing thread per
+//    CTA could not (each copy instruction costs it hundreds of cycles), and no
+//    CTA-wide barrier is needed.  Per 16-token block: S^T = K . Q^T on the
+//    tensor cores (m16n8k16, M = the 16 tokens, N = the G <= 8 query heads of
+//    the group, K = head_dim), online softmax in base 2 with per-head running
+//    max / sum, P rounded to the input type and transposed in registers
+//    (movmatrix), O^T += V^T . P^T (M = head_dim rows of V^T via
+//    ldmatrix.trans).  Each K/V tile is read from HBM once for the whole query
+//    group.  Slots past the context in the last block are zeroed in registers,
+//    so whatever bits they hold cannot reach the output.
 //    A sequence with one split is written to `out` straight from the
 //    warp's registers; otherwise the warp writes (o, lse) to the workspace,
 //    publishes it (fence) and counts it (atomic), and the warp that completes
@@ -837,6 +838,16 @@ __global__ void __launch_bounds__(W * 32)
   // The next kernel of the stream may start launching; it waits for this
   // one's completion before it touches memory.
   dev::grid_launch_dependents();
+  // This warp's first item, dealt statically.  W consecutive items (the
+  // heads of one unit, reading neighbouring tiles) per CTA measured best
+  // when every warp gets one (MHA 7B decode 0.868 of the measured copy
+  // bandwidth dealt round robin, 0.883 so); a shorter list (a grouped decode
+  // has at most one unit per warp) goes round robin over the SMs, or the
+  // last SMs would idle (grouped decode 0.5-0.7 us faster per layer).
+  auto first_item = [&](int items) {
+    return items < int(gridDim.x) * W ? warp * int(gridDim.x) + int(blockIdx.x)
+                                      : int(blockIdx.x) * W + warp;
+  };
   // While the kernel before this one finishes: warm L2 with the first blocks
   // of this warp's statically dealt first item.  The work list and tables may
   // still be changing (the previous kernel may be the plan), so this is only
@@ -846,9 +857,9 @@ __global__ void __launch_bounds__(W * 32)
   // launches, whose start weighs most; 0.872 -> 0.882 of the measured copy
   // bandwidth per layer step on GB300), else 4 (GQA got 0.6 % slower with 8).
   {
-    const int x0 = blockIdx.x * W + warp;
     const long long cap = (long long)p.num_seqs * p.max_splits * p.num_kv_heads;
     const int total0 = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]);
+    const int x0 = first_item(total0);
     if (x0 < total0 && x0 < cap) {
       const int4 u = reinterpret_cast<const int4*>(p.ws.units)[x0 / p.num_kv_heads];
       const int hg = x0 % p.num_kv_heads, n = u.z & kUnitBlocks;
@@ -953,7 +964,7 @@ __global__ void __launch_bounds__(W * 32)
   cur.patch = nxt.patch = false;
   long long cslot = -1;  // slot_mapping[b] of the item being claimed
   int cstage = 1;
-  int cx = blockIdx.x * W + warp;  // first item of every warp: dealt statically
+  int cx = first_item(total);  // first item of every warp: dealt statically
   int4 cu = make_int4(0, 0, 0, 0);
   int q_issued = 0, q_taken = 0;  // query copies issued into / read from qbuf
   auto finished = [&]() {
@@ -1383,7 +1394,8 @@ __global__ void __launch_bounds__(W * 32)
         vm_hi = (t + 8 < valid ? 0x0000ffffu : 0u) | (t + 9 < valid ? 0xffff0000u : 0u);
       }
       // ---- O^T (D x 8) += V^T (D x 16 tokens) . P^T (16 tokens x 8), per row tile
-      {
+      // (a block full of context, all but a sequence's last, takes no masks)
+      auto pv = [&](auto masked) {
         const int tok = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
@@ -1392,13 +1404,23 @@ __global__ void __launch_bounds__(W * 32)
               vt + (gc >> 3) * 2048 + tok * 128 + ((((gc & 7) ^ (tok & 7))) << 4);
           uint32_t a0, a1, a2, a3;
           dev::ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+          if constexpr (decltype(masked)::value) {
+            a0 &= vm_lo;
+            a1 &= vm_lo;
+            a2 &= vm_hi;
+            a3 &= vm_hi;
+          }
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (t == 1 && !two) continue;
-            M::run(o[t][mt], a0 & vm_lo, a1 & vm_lo, a2 & vm_hi, a3 & vm_hi, pb0[t], pb1[t]);
+            M::run(o[t][mt], a0, a1, a2, a3, pb0[t], pb1[t]);
           }
         }
-      }
+      };
+      if (valid < kBlockSize)
+        pv(std::true_type{});
+      else
+        pv(std::false_type{});
       // the stage is read; order those reads before the copy that reuses it
       dev::fence_proxy_async_smem();
       __syncwarp();
