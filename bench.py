@@ -941,14 +941,28 @@ def run_cascade_bench(args):
                                      layers=args.layers)))
 
 
+def cascade_launches_per_step(grouped: bool, layers: int) -> int:
+    """Kernel launches of one cascade step: the grouped decode (the default
+    for groups, or PA_CASCADE=grouped) is one plan, then one attention launch
+    per layer; the three phases are two or three plans (the suffix tables of
+    groups, the prefix phase's plan, the suffix decode's plan), then per
+    layer the prefix phase, the suffix decode and the combine."""
+    impl = os.environ.get("PA_CASCADE", "")
+    if impl == "grouped" or (grouped and impl != "phases"):
+        return 1 + layers
+    return (3 if grouped else 2) + 3 * layers
+
+
 def measure_cascade(args, workload: str, device, cpu_seconds: float, layers: int = 0) -> dict:
     """Shared-prefix (cascade) decode beside the plain decode of the same
     batch: the prefix-mix batch (one prefix for the whole batch) or the
     parallel-sampling batch (grouped: each prompt's branches share their
     prompt).  Both run as a model step would: one plan, then per layer the
     new tokens' K/V appended and attention over the whole context (the plain
-    path in one launch; the cascade path as its prefix phase, the suffix
-    decode that also stores the new rows, and the combine)."""
+    path in one launch; the grouped cascade in one launch too, over units
+    that read a group's shared blocks once for its members; the single-prefix
+    cascade as its prefix phase, the suffix decode that also stores the new
+    rows, and the combine)."""
     import pagedattention_decode_attention_gb300 as pa
     batch = make_batch(workload, 0)
     if layers > 0:
@@ -1026,7 +1040,7 @@ def measure_cascade(args, workload: str, device, cpu_seconds: float, layers: int
         "plain_us_per_layer": plain_s / L * 1e6,
         "plain_value": batch.num_seqs / plain_s,
         "max_abs_diff_vs_plain": diff,
-        "gpu_launches": args.steps * ((3 if grouped else 2) + 3 * L),
+        "gpu_launches": args.steps * cascade_launches_per_step(grouped, L),
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

@@ -317,7 +317,7 @@ PA_API int pa_paged_attention_decode_shared_prefix_run(
  * _plan (block_tables, context_lens and the group arrays; once per decode
  * step) checks the groups and writes the work list into the workspace; _run
  * (per layer, same sizes and arrays, same workspace, stream order) launches
- * the attention and then the merge of each sequence's splits.  The work list
+ * the attention, which also merges each sequence's splits.  The work list
  * has units of two kinds: a split of a group's shared blocks for up to 16
  * query rows of its members (16 / (num_q_heads / num_kv_heads) members,
  * every shared block read once for them), and a split of one sequence's

@@ -50,8 +50,9 @@
 //    unit reads a split of the group's shared blocks once for its members'
 //    rows; an own unit covers one sequence's blocks past them; a small chunk
 //    takes its members' own blocks into its last shared unit, each block's
-//    scores masked to its member's rows.  The splits are merged by a merge
-//    launch after the attention.
+//    scores masked to its member's rows.  A member's last split to finish
+//    queues the member's merge; warps that have run out of items take the
+//    queued merges, in the same launch.
 //
 // An fp32 path (CUDA cores, one warp per (sequence, head), online softmax in
 // natural base) serves float32 caches; it is exact to fp32 rounding and is not
@@ -124,8 +125,10 @@ struct Smem {
   static constexpr int kQRow = NT == 1 ? D + 8 : D;
   static constexpr int kQBytes = NT == 1 ? (8 * kQRow + 2 * D) * 2 : 16 * kQRow * 2;
   // layout: rings [W][stages][stage] | query buffers [W] | barriers [W][stages + 1]
-  static constexpr size_t kFixedBytes =
-      1024 /* alignment slack */ + size_t(W) * kQBytes + size_t(W) * (kWarpStages + 1) * 8;
+  // | team barriers [W / kTeamWarps]
+  static constexpr size_t kFixedBytes = 1024 /* alignment slack */ + size_t(W) * kQBytes +
+                                        size_t(W) * (kWarpStages + 1) * 8 +
+                                        size_t(W / kTeamWarps + 1) * 8;
   static size_t bytes(int stages) { return kFixedBytes + size_t(W) * stages * kStageBytes; }
   // deepest ring (stages per warp) that fits in `budget` bytes
   static int stages_for(size_t budget) {
@@ -288,7 +291,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const Params p) {
 // `chunk` members at once (their m * G query rows read every block once),
 // and an own unit a split of one sequence's blocks past the shared ones.  A
 // sequence's splits are its group's shared splits (indices 0 ..) followed by
-// its own; a merge launch after the attention merges them.
+// its own; the attention launch merges them (a queue of ready merges that
+// warps out of items take).
 struct GroupArgs {
   const int32_t* group_start;   // [num_groups + 1], or null: one group of every sequence
   const int32_t* group_blocks;  // [num_groups] shared blocks, or null: single_blocks
@@ -296,6 +300,7 @@ struct GroupArgs {
   int single_blocks;
   int chunk;                    // most members of one shared unit
   int nwarps;                   // math warps of the attention launch
+  int teams;                    // the attention launch can merge in teams (rings of >= 2 stages)
   int32_t* gp;                  // workspace [num_groups]: shared blocks that passed the checks
   int32_t* seq_prefix;          // workspace [num_seqs]: each sequence's shared blocks
   int32_t* seq_ctx;             // workspace [num_seqs]: context lengths, clamped
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   constexpr int NT = kGroupedPlanThreads;
   __shared__ int hist[kSplitBlocks + 2];
   __shared__ int bucket[kSplitBlocks + 2];
-  __shared__ int cut_s, bad_s, sp_s;
+  __shared__ int cut_s, bad_s, sp_s, merges_s, team_s, chunks_s, chunk_ctr;
   __shared__ unsigned long long work_s;
   dev::grid_launch_dependents();
   dev::grid_dependency_wait();  // the previous kernel may still read the workspace
@@ -405,6 +410,10 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   if (tid == 0) {
     bad_s = ga.group_start && (ga.group_start[0] != 0 || ga.group_start[ng] != p.num_seqs);
     work_s = 0;
+    merges_s = 0;
+    team_s = 1;
+    chunks_s = 0;
+    chunk_ctr = 0;
   }
   __syncthreads();
   // group starts must not decrease (every thread checks its share)
@@ -434,7 +443,10 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
       ctx = ctx < 0 ? 0 : cap;
     }
     ga.seq_ctx[b] = ctx;
-    for (int h = 0; h < p.num_kv_heads; ++h) p.ws.arrivals[size_t(b) * p.num_kv_heads + h] = 0;
+    for (int h = 0; h < p.num_kv_heads; ++h) {
+      p.ws.arrivals[size_t(b) * p.num_kv_heads + h] = 0;
+      p.ws.mqueue[size_t(b) * p.num_kv_heads + h] = 0;
+    }
   }
   __syncthreads();
   // Every member's context must cover the shared blocks and its table must
@@ -498,6 +510,26 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
     ga.chunk_plan[b] = make_int4(c.absorb, c.own, c.ns, c.last_shared);
   }
   __syncthreads();
+  // Teams: when every sequence shares blocks with its chunk, every chunk
+  // takes its members' own blocks into its last shared split (so no unit
+  // covers one sequence alone) with at most kTeamWarps splits, and the
+  // (chunk, KV head) pairs fit the launch's teams of kTeamWarps warps, the
+  // splits of each pair go to one team of one CTA and are merged there, in
+  // shared memory.
+  for (int b = tid; b < p.num_seqs; b += NT) {
+    const int2 cm = ga.seq_chunk[b];
+    if (ga.seq_prefix[b] == 0) {
+      team_s = 0;
+      continue;
+    }
+    const int4 c = ga.chunk_plan[cm.x];
+    if (!c.x || c.z > kTeamWarps) team_s = 0;
+    if (b == cm.x) atomicAdd(&chunks_s, 1);
+  }
+  __syncthreads();
+  const bool team = ga.teams && team_s && p.num_seqs > 0 &&
+                    (long long)chunks_s * p.num_kv_heads * kTeamWarps <= ga.nwarps &&
+                    (long long)chunks_s * kTeamWarps <= (long long)p.num_seqs * p.max_splits;
   // a sequence's own blocks that become units of its own (none when its
   // chunk absorbs them), and its chunk's shared splits
   auto own_and_shared = [&](int b, int& own, int& pn) {
@@ -580,6 +612,7 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
       if (np - pr) atomicAdd(&hist[pb], mm * (np - pr));
     }
     p.ws.nsplits[b] = pn + count;
+    if (pn + count > 1) atomicAdd(&merges_s, 1);
     if (b == ga.seq_chunk[b].x && ga.seq_prefix[b] > 0) chunk_units(b, hist);
   }
   __syncthreads();
@@ -589,9 +622,14 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
       bucket[r] = pos;
       pos += hist[r];
     }
-    p.ws.header[kHdrTotal] = pos * p.num_kv_heads;
+    p.ws.header[kHdrTotal] = team ? chunks_s * p.num_kv_heads * kTeamWarps : pos * p.num_kv_heads;
     p.ws.header[kHdrNext] = 0;
     p.ws.header[kHdrDone] = 0;
+    p.ws.header[kHdrQHead] = 0;
+    p.ws.header[kHdrQTail] = 0;
+    p.ws.header[kHdrQDone] = 0;
+    p.ws.header[kHdrMerges] = team ? 0 : merges_s * p.num_kv_heads;
+    p.ws.header[kHdrTeam] = team ? kTeamWarps : 0;
     p.ws.header[kHdrSignature] = p.signature;
   }
   __syncthreads();
@@ -600,6 +638,8 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   // | blocks, context), split indices after the chunk's shared ones.
   // Shared units: (first member, first block, split index << 16 | members
   // << 8 | kUnitOwn for a last split that absorbs | blocks, shared tokens).
+  // With teams, chunk i's splits take places kTeamWarps i .. (the run reads
+  // them once per KV head), unused places hold b = -1.
   for (int b = tid; b < p.num_seqs; b += NT) {
     int own, pn;
     own_and_shared(b, own, pn);
@@ -646,18 +686,21 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
       sn = c.z;
       parts_shape(P, sn, sbase, sbig);
     }
+    const int place = team ? atomicAdd(&chunk_ctr, 1) * kTeamWarps : 0;
     int off = 0;
     for (int s = 0; s < sn; ++s) {
       const int sz = s < sbig ? sbase + 1 : sbase;
-      const int pos = atomicAdd(&bucket[sz], 1);
+      const int pos = team ? place + s : atomicAdd(&bucket[sz], 1);
       units[pos] = make_int4(b, off, (s << 16) | (cm.y << 8) | sz, P * kBlockSize);
       off += sz;
     }
     if (c.x) {
-      const int pos = atomicAdd(&bucket[c.w + c.y], 1);
+      const int pos = team ? place + c.z - 1 : atomicAdd(&bucket[c.w + c.y], 1);
       units[pos] = make_int4(b, off, ((c.z - 1) << 16) | (cm.y << 8) | kUnitOwn | c.w,
                              P * kBlockSize);
     }
+    if (team)
+      for (int s = c.z; s < kTeamWarps; ++s) units[place + s] = make_int4(-1, 0, 0, 0);
   }
 }
 
@@ -753,9 +796,8 @@ __device__ __forceinline__ void merge_splits(const MergeArgs a, int lane) {
   }
 }
 
-// L: float4 loads in flight per lane.  Measured on GB300: 24 inside the
-// attention kernel (MHA and GQA decode 1 % faster than with 16), 16 in the
-// merge launch of the grouped decode (1 us per layer faster than with 24).
+// L: float4 loads in flight per lane (24 measured 1 % faster than 16 for the
+// MHA and GQA decode on GB300).
 template <typename T, int D, int L>
 __device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
   const int nk = (a.G * D / 4 + 31) / 32;
@@ -773,6 +815,55 @@ __device__ __forceinline__ void merge_dispatch(const MergeArgs a, int lane) {
           default: merge_splits<T, D, 8, L>(a, lane); break;
         }
       }
+  }
+}
+
+// Floats between two rows of a split's results in a team warp's ring (16
+// bytes of padding, so the four rows a store instruction writes fall in
+// different banks); the 16 rows' base-2 lse follow the rows.
+template <int D>
+constexpr int team_row() { return D + 4; }
+
+// A team's merge: member rows r0 .. r0 + G - 1 of the ns splits whose results
+// (o normalised, fp32, then the rows' lse) sit in the rings of the team's
+// warps, ring_bytes apart from ring0, merged with log-sum-exp weights into
+// out (the member's G x D outputs).  Lane l owns the float4 columns l + 32 k.
+template <typename T, int D>
+__device__ __forceinline__ void team_merge(const uint8_t* ring0, size_t ring_bytes, int ns,
+                                           int r0, int G, T* out, int lane) {
+  using M = dev::Mma<T>;
+  constexpr int RS = team_row<D>();
+  const int C = G * D / 4;
+  for (int c = lane; c < C; c += 32) {
+    const int r = r0 + (4 * c) / D, d = (4 * c) % D;
+    float l[kTeamWarps];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kTeamWarps; ++s) {
+      l[s] = s < ns ? reinterpret_cast<const float*>(ring0 + s * ring_bytes)[16 * RS + r]
+                    : -INFINITY;
+      mx = fmaxf(mx, l[s]);
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float sum = 0.f;
+#pragma unroll
+    for (int s = 0; s < kTeamWarps; ++s) {
+      if (s < ns) {
+        const float w = dev::fast_exp2(l[s] - mx);
+        const float4 v = *reinterpret_cast<const float4*>(
+            reinterpret_cast<const float*>(ring0 + s * ring_bytes) + r * RS + d);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+        sum += w;
+      }
+    }
+    const float inv = 1.f / sum;
+    uint2 pk;
+    pk.x = M::pack(acc.x * inv, acc.y * inv);
+    pk.y = M::pack(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(out + 4 * c) = pk;
   }
 }
 
@@ -807,6 +898,10 @@ __global__ void __launch_bounds__(W * 32)
   using S = Smem<D, W, NT>;
   using M = dev::Mma<T>;
   constexpr int KT = D / 16;      // 16-wide steps along head_dim
+  constexpr int kTeamRow = team_row<D>();
+  static_assert(NT == 1 || (W % kTeamWarps == 0 &&
+                            (16 * kTeamRow + 16) * 4 <= 2 * S::kStageBytes),
+                "a team warp's results fit the first two stages of its ring");
   constexpr int HALVES = D / 64;  // 128-byte TMA boxes per tile row
   // The next item is claimed when this many blocks of the current one are
   // still to be issued: its claim takes one pipeline step per block (counter,
@@ -816,6 +911,16 @@ __global__ void __launch_bounds__(W * 32)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int G = p.group;
+  // the member of each of this lane's two query columns, per row tile
+  // (computed once: the divisions in the block loop cost the grouped decode
+  // 1.6 us per layer)
+  int mc0[NT], mc1[NT];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int qr = 8 * t + 2 * ((threadIdx.x & 31) & 3);
+    mc0[t] = qr / G;
+    mc1[t] = (qr + 1) / G;
+  }
   const int NS = p.stages;  // ring stages of each warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + size_t(warp) * NS * S::kStageBytes;
@@ -825,6 +930,10 @@ __global__ void __launch_bounds__(W * 32)
                                                   size_t(W) * S::kQBytes) +
                       warp * (kWarpStages + 1);
   uint64_t* my_q = my_full + kWarpStages;
+  // grouped decode in teams: one barrier per team of kTeamWarps warps
+  uint64_t* team_bars = reinterpret_cast<uint64_t*>(smem + size_t(W) * NS * S::kStageBytes +
+                                                    size_t(W) * S::kQBytes) +
+                        W * (kWarpStages + 1);
 
   // Every warp owns its barriers, so no CTA-wide synchronisation is needed.
   if (lane == 0) {
@@ -835,6 +944,14 @@ __global__ void __launch_bounds__(W * 32)
     dev::prefetch_tensormap(&tmap_v);
   }
   __syncwarp();
+  if constexpr (NT == 2) {
+    // the team barriers are the CTA's: initialised before any warp goes on
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < W / kTeamWarps; ++i) dev::mbar_init(&team_bars[i], kTeamWarps);
+      dev::mbar_fence_init();
+    }
+    __syncthreads();
+  }
   // The next kernel of the stream may start launching; it waits for this
   // one's completion before it touches memory.
   dev::grid_launch_dependents();
@@ -844,9 +961,30 @@ __global__ void __launch_bounds__(W * 32)
   // bandwidth dealt round robin, 0.883 so); a shorter list (a grouped decode
   // has at most one unit per warp) goes round robin over the SMs, or the
   // last SMs would idle (grouped decode 0.5-0.7 us faster per layer).
-  auto first_item = [&](int items) {
+  // With teams (tm: a grouped plan that placed each (chunk, KV head)'s
+  // splits as kTeamWarps consecutive items), team t goes to CTA t % (CTAs),
+  // whose warps w with w / kTeamWarps == t / (CTAs) take its items.
+  auto first_item = [&](int items, bool tm) {
+    if constexpr (NT == 2) {
+      if (tm)
+        return ((warp / kTeamWarps) * int(gridDim.x) + int(blockIdx.x)) * kTeamWarps +
+               warp % kTeamWarps;
+    }
     return items < int(gridDim.x) * W ? warp * int(gridDim.x) + int(blockIdx.x)
                                       : int(blockIdx.x) * W + warp;
+  };
+  // item x -> its unit and KV head: the heads of a unit are consecutive
+  // items, or (teams) the splits of a (chunk, head) are
+  auto unit_of = [&](int x, bool tm, int& hg) {
+    if constexpr (NT == 2) {
+      if (tm) {
+        const int t = x / kTeamWarps;
+        hg = t % p.num_kv_heads;
+        return (t / p.num_kv_heads) * kTeamWarps + x % kTeamWarps;
+      }
+    }
+    hg = x % p.num_kv_heads;
+    return x / p.num_kv_heads;
   };
   // While the kernel before this one finishes: warm L2 with the first blocks
   // of this warp's statically dealt first item.  The work list and tables may
@@ -857,12 +995,17 @@ __global__ void __launch_bounds__(W * 32)
   // launches, whose start weighs most; 0.872 -> 0.882 of the measured copy
   // bandwidth per layer step on GB300), else 4 (GQA got 0.6 % slower with 8).
   {
-    const long long cap = (long long)p.num_seqs * p.max_splits * p.num_kv_heads;
+    const long long cap = (long long)p.num_seqs * p.max_splits * p.num_kv_heads;  // items
     const int total0 = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]);
-    const int x0 = first_item(total0);
-    if (x0 < total0 && x0 < cap) {
-      const int4 u = reinterpret_cast<const int4*>(p.ws.units)[x0 / p.num_kv_heads];
-      const int hg = x0 % p.num_kv_heads, n = u.z & kUnitBlocks;
+    bool team0 = false;
+    if constexpr (NT == 2)
+      team0 = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTeam]) == kTeamWarps;
+    const int x0 = first_item(total0, team0);
+    int hg = 0;
+    const int u0 = unit_of(x0, team0, hg);
+    if (x0 < total0 && x0 < cap && u0 < (long long)p.num_seqs * p.max_splits) {
+      const int4 u = reinterpret_cast<const int4*>(p.ws.units)[u0];
+      const int n = u.z & kUnitBlocks;
       const int kWarmBlocks = p.group == 1 ? 8 : 4;
       if (u.x >= 0 && u.x < p.num_seqs && u.y >= 0 && n >= 1 && n <= kSplitBlocks &&
           p.table_offset + u.y + n <= p.max_blocks) {
@@ -888,12 +1031,23 @@ __global__ void __launch_bounds__(W * 32)
 
   const unsigned long long tmo = p.timeout_ns;
   const int Hkv = p.num_kv_heads, Hq = p.num_q_heads;
-  const bool planned =
+  const int nwarps = int(gridDim.x) * W;
+  const bool signed_ok =
       *reinterpret_cast<volatile int*>(&p.ws.header[kHdrSignature]) == p.signature;
-  if (!planned && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+  if (!signed_ok && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusPlan);
+  // a grouped decode placed in teams: the plan made sure that the teams fit
+  // the launch and that the rings hold a split's results
+  bool team = false, team_bad = false;
+  if constexpr (NT == 2) {
+    team = signed_ok &&
+           *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTeam]) == kTeamWarps;
+    team_bad = team && (*reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]) > nwarps ||
+                        size_t(NS) * S::kStageBytes < size_t(16 * kTeamRow + 16) * 4);
+    if (team_bad && blockIdx.x == 0 && threadIdx.x == 0) dev::flag_status(p.status, kStatusBounds);
+  }
+  const bool planned = signed_ok && !team_bad;
   const int total = planned ? *reinterpret_cast<volatile int*>(&p.ws.header[kHdrTotal]) : 0;
   const int4* units = reinterpret_cast<const int4*>(p.ws.units);
-  const int nwarps = int(gridDim.x) * W;
 
   const bool fused = p.slot_mapping != nullptr;
   const long long num_slots = (long long)p.num_blocks * kBlockSize;
@@ -964,7 +1118,7 @@ __global__ void __launch_bounds__(W * 32)
   cur.patch = nxt.patch = false;
   long long cslot = -1;  // slot_mapping[b] of the item being claimed
   int cstage = 1;
-  int cx = first_item(total);  // first item of every warp: dealt statically
+  int cx = first_item(total, team);  // first item of every warp: dealt statically
   int4 cu = make_int4(0, 0, 0, 0);
   int q_issued = 0, q_taken = 0;  // query copies issued into / read from qbuf
   auto finished = [&]() {
@@ -987,11 +1141,25 @@ __global__ void __launch_bounds__(W * 32)
         cstage = 4;
         finished();
       } else {
-        cu = __ldg(&units[x / Hkv]);
-        nxt.g = x % Hkv;
+        if constexpr (NT == 2) {
+          int hg;
+          cu = __ldg(&units[unit_of(x, team, hg)]);
+          nxt.g = hg;
+        } else {
+          cu = __ldg(&units[x / Hkv]);
+          nxt.g = x % Hkv;
+        }
         cstage = 2;
       }
     } else if (cstage == 2) {
+      if (NT == 2 && team && cu.x < 0) {
+        // an unused place of a team: this warp takes no item
+        nxt.b = -1;
+        nxt.nblk = 0;
+        cstage = 4;
+        finished();
+        return;
+      }
       nxt.b = cu.x;
       nxt.first = cu.y;
       nxt.s = cu.z >> 16;
@@ -1347,8 +1515,7 @@ __global__ void __launch_bounds__(W * 32)
           continue;
         }
         // a member's own block counts for that member's rows only
-        const int qr = 8 * t + 2 * (lane & 3);
-        const bool c0 = bmem < 0 || qr / G == bmem, c1 = bmem < 0 || (qr + 1) / G == bmem;
+        const bool c0 = bmem < 0 || mc0[t] == bmem, c1 = bmem < 0 || mc1[t] == bmem;
         const float x0 = v0 && c0 ? (sa[t][0] + sb[t][0]) * sl2 : -INFINITY;
         const float x1 = v0 && c1 ? (sa[t][1] + sb[t][1]) * sl2 : -INFINITY;
         const float x2 = v1 && c0 ? (sa[t][2] + sb[t][2]) * sl2 : -INFINITY;
@@ -1532,7 +1699,7 @@ __global__ void __launch_bounds__(W * 32)
       // Rows of several members: row r belongs to sequence b + r / G, query
       // head g G + r % G, and each member has its own split count.  A
       // member's only split writes its output; otherwise the split's result
-      // goes to the member's split slot for the merge launch.
+      // goes to the member's split slot for the member's merge.
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -1572,6 +1739,16 @@ __global__ void __launch_bounds__(W * 32)
               orow[d0] = M::from_float(o[t][mt][c] * inv);
               orow[d0 + 8] = M::from_float(o[t][mt][2 + c] * inv);
             }
+          } else if (team) {
+            // the team merges from shared memory: rows kTeamRow floats apart
+            float* area = reinterpret_cast<float*>(ring);
+#pragma unroll
+            for (int mt = 0; mt < KT; ++mt) {
+              const int d0 = 16 * mt + (lane >> 2);
+              area[r * kTeamRow + d0] = o[t][mt][c] * inv;
+              area[r * kTeamRow + d0 + 8] = o[t][mt][2 + c] * inv;
+            }
+            if (lane < 4) area[16 * kTeamRow + r] = lse;
           } else if (s >= p.max_splits) {
             dev::flag_status(p.status, kStatusBounds);  // (the plan never makes so many)
           } else {
@@ -1599,7 +1776,26 @@ __global__ void __launch_bounds__(W * 32)
           static_cast<uint4*>(const_cast<void*>(isv ? p.v_cache : p.k_cache))[dst] = mkv[i];
         }
       }
-      // (the merge launch after this one merges every sequence's splits)
+      // Count this split in for each of its members with several; the
+      // member's last split queues the member's merge, which a warp that
+      // has run out of items takes (after the item loop).  (Teams merge
+      // after the item loop, from shared memory.)
+      __syncwarp();
+      if (!team && lane < cur.m) {
+        const int bi = b + lane;
+        const int nsi = lane == 0 ? nsplit : __ldg(&p.ws.nsplits[bi]);
+        if (nsi > 1) {
+          const int pair = bi * Hkv + g;
+          if (dev::atom_add_acq_rel_gpu(&p.ws.arrivals[pair], 1) == nsi - 1) {
+            p.ws.arrivals[pair] = 0;  // ready for the next run
+            const int at = atomicAdd(&p.ws.header[kHdrQTail], 1);
+            if (at < p.num_seqs * Hkv)
+              dev::st_release_gpu(&p.ws.mqueue[at], pair + 1);
+            else
+              dev::flag_status(p.status, kStatusBounds);
+          }
+        }
+      }
     }
 #ifdef PA_PROFILE_TIMES
     ITEM_TRACE(n_items, item_t0, nblk, nsplit, merge_ns, qwait_ns);
@@ -1608,6 +1804,80 @@ __global__ void __launch_bounds__(W * 32)
     // the next item must be complete before it becomes the current one
     if (cstage == 0) request();
     while (cstage != 4) advance();
+  }
+  if constexpr (NT == 2) {
+    if (team && planned) {
+      // Every warp of the team is here (an item of its own done, or none):
+      // member j of the team's (chunk, KV head) is merged by the team's
+      // warp j from the splits' rows in the team's rings.
+      uint64_t* tbar = &team_bars[warp / kTeamWarps];
+      if (lane == 0) dev::mbar_arrive(tbar);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(tbar, 0, tmo, p.status);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int t = (warp / kTeamWarps) * int(gridDim.x) + int(blockIdx.x);
+      const int j = warp % kTeamWarps;
+      if (ok && t * kTeamWarps < total) {
+        const int gg = t % Hkv;
+        const int4 u0 = __ldg(&units[(t / Hkv) * kTeamWarps]);
+        const int b0 = u0.x, m = (u0.z >> 8) & 0xff;
+        if (b0 >= 0 && j < m && b0 + j < p.num_seqs) {
+          const int ns = __ldg(&p.ws.nsplits[b0 + j]);
+          if (ns > 1 && ns <= kTeamWarps)
+            team_merge<T, D>(smem + size_t(warp - j) * NS * S::kStageBytes,
+                             size_t(NS) * S::kStageBytes, ns, j * G, G,
+                             static_cast<T*>(p.out) + (size_t(b0 + j) * Hq + size_t(gg) * G) * D,
+                             lane);
+          else if (ns > kTeamWarps && lane == 0)
+            dev::flag_status(p.status, kStatusBounds);
+        }
+      }
+    } else if (planned) {
+      // The queued merges: every warp out of items takes entries in turn,
+      // waits for each to be filled and merges that (sequence, KV head).
+      // All items are claimed by then, so each awaited entry is filled by a
+      // warp still at work on one (none waits on a warp that waits).
+      const int merges = *reinterpret_cast<volatile int*>(&p.ws.header[kHdrMerges]);
+      const int cap = p.num_seqs * Hkv;
+      for (;;) {
+        int at = 0;
+        if (lane == 0) at = atomicAdd(&p.ws.header[kHdrQHead], 1);
+        at = __shfl_sync(0xffffffffu, at, 0);
+        if (at >= merges || at >= cap) break;
+        int v = 0;
+        if (lane == 0) v = dev::wait_nonzero_bounded(&p.ws.mqueue[at], tmo, p.status);
+        v = __shfl_sync(0xffffffffu, v, 0);
+        if (v <= 0 || v > cap) {
+          if (v > cap && lane == 0) dev::flag_status(p.status, kStatusBounds);
+          break;  // (v == 0: the wait ran out and set the status)
+        }
+        __syncwarp();
+        const int bb = (v - 1) / Hkv, gg = (v - 1) % Hkv;
+        const int nsi = __ldg(&p.ws.nsplits[bb]);
+        if (nsi > 1 && nsi <= p.max_splits) {
+          const size_t row0 = size_t(bb) * p.max_splits * Hq + size_t(gg) * G;
+          MergeArgs ma;
+          ma.lse = p.ws.part_lse + row0;
+          ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
+          ma.out = static_cast<T*>(p.out) + (size_t(bb) * Hq + size_t(gg) * G) * D;
+          ma.cas_o = nullptr;
+          ma.cas_lse = nullptr;
+          ma.G = G;
+          ma.Hq = Hq;
+          ma.nsplit = nsi;
+          merge_dispatch<T, D, 24>(ma, lane);
+        } else if (lane == 0) {
+          dev::flag_status(p.status, kStatusBounds);
+        }
+        if (lane == 0) p.ws.mqueue[at] = 0;  // ready for the next run
+      }
+      // the last warp done with the queue leaves it ready for the next run
+      if (lane == 0 && atomicAdd(&p.ws.header[kHdrQDone], 1) == nwarps - 1) {
+        p.ws.header[kHdrQHead] = 0;
+        p.ws.header[kHdrQTail] = 0;
+        p.ws.header[kHdrQDone] = 0;
+      }
+    }
   }
   TIME_MARK(1, dev::global_timer_ns());
   TIME_MARK(2, static_cast<unsigned long long>(kc));
@@ -1671,41 +1941,6 @@ __global__ void __launch_bounds__(128) decode_f32_kernel(const Params p) {
 
 namespace pa {
 namespace decode {
-
-// The merges of a grouped decode, as a launch of their own: one warp per
-// (sequence, KV head) with more than one split merges that sequence's split
-// results of the head's query group (log-sum-exp weights, splits in order).
-// Run after the attention launch, so the merges are spread over the whole
-// GPU instead of queueing in the warps that finish a chunk's splits last.
-template <typename T, int D>
-__global__ void __launch_bounds__(256) merge_kernel(const Params p) {
-  dev::grid_launch_dependents();
-  dev::grid_dependency_wait();  // the attention launch has written every split
-  const int lane = threadIdx.x & 31;
-  const long long pairs = (long long)p.num_seqs * p.num_kv_heads;
-  for (long long x = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; x < pairs;
-       x += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const int b = int(x / p.num_kv_heads), g = int(x % p.num_kv_heads);
-    const int nsplit = p.ws.nsplits[b];
-    if (nsplit <= 1) continue;  // written by its only split (or an empty row)
-    if (nsplit > p.max_splits) {
-      if (lane == 0) dev::flag_status(p.status, kStatusBounds);
-      continue;
-    }
-    const size_t head0 = size_t(b) * p.num_q_heads + size_t(g) * p.group;
-    const size_t row0 = size_t(b) * p.max_splits * p.num_q_heads + size_t(g) * p.group;
-    MergeArgs ma;
-    ma.lse = p.ws.part_lse + row0;
-    ma.po = reinterpret_cast<const float4*>(p.ws.part_o + row0 * D);
-    ma.out = static_cast<T*>(p.out) + head0 * D;
-    ma.cas_o = nullptr;
-    ma.cas_lse = nullptr;
-    ma.G = p.group;
-    ma.Hq = p.num_q_heads;
-    ma.nsplit = nsplit;
-    merge_dispatch<T, D, 16>(ma, lane);
-  }
-}
 
 // Last step of a shared-prefix decode: each (sequence, head) merges the
 // shared prefix's (o, lse) with its own suffix's by log-sum-exp weights
@@ -2324,7 +2559,7 @@ struct GroupedLayout {
 // blocks, each sequence's shared blocks and its clamped context.
 struct FusedLayout {
   Layout dec;
-  size_t gp, seq_prefix, seq_ctx, seq_group, seq_chunk, chunk_plan, total;
+  size_t gp, seq_prefix, seq_ctx, seq_group, seq_chunk, chunk_plan, mqueue, total;
 };
 FusedLayout fused_layout(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                          int max_blocks_per_seq) {
@@ -2337,7 +2572,8 @@ FusedLayout fused_layout(int num_seqs, int num_q_heads, int num_kv_heads, int he
   l.seq_group = align256(l.seq_ctx + size_t(num_seqs) * 4);
   l.seq_chunk = align256(l.seq_group + size_t(num_seqs) * 4);
   l.chunk_plan = align256(l.seq_chunk + size_t(num_seqs) * 8);
-  l.total = align256(l.chunk_plan + size_t(num_seqs) * 16);
+  l.mqueue = align256(l.chunk_plan + size_t(num_seqs) * 16);
+  l.total = align256(l.mqueue + size_t(num_seqs) * num_kv_heads * 4);
   return l;
 }
 
@@ -2380,9 +2616,9 @@ enum class SharedMode { kPlanAndRun, kPlanOnly, kRunOnly };
 // Which cascade implementation an entry point uses: the three phases (the
 // prefix phase on the chunked-prefill kernels, the suffix decode, the
 // combine) or the grouped decode (one attention launch over shared and own
-// units, then one merge launch).  Measured on GB300 (8B-shaped GQA): 128
-// forked branches in groups of 4 sharing 64 blocks take 50 us per layer
-// grouped against 52 in phases; 100 requests on one 64-block prefix take 76
+// units, which also merges each sequence's splits).  Measured on GB300
+// (8B-shaped GQA): 128 forked branches in groups of 4 sharing 64 blocks took
+// 50 us per layer grouped against 52 in phases; 100 requests on one 64-block prefix take 76
 // in phases against 91 grouped (the phases read the prefix once for all 400
 // query rows; the grouped decode once per 16).  So the grouped entry points
 // use the grouped decode and the single-prefix ones the phases;
@@ -2447,6 +2683,7 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
                              max_blocks_per_seq, workspace, fl.dec, status);
     prm.block_tables = group_start ? block_tables : nullptr;
     prm.signature = signature;
+    prm.ws.mqueue = reinterpret_cast<int*>(ws + fl.mqueue);
     const int nwarps = st.sms * kc2.ctas_per_sm * 8;
     prm.piece_blocks = st.tuning.piece_blocks;
     prm.tail_blocks = st.tuning.tail_waves * nwarps * prm.piece_blocks;
@@ -2457,6 +2694,7 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
     ga.single_blocks = single_blocks;
     ga.chunk = 16 / (num_q_heads / num_kv_heads);
     ga.nwarps = nwarps;
+    ga.teams = kc2.stages >= 2;  // a split's results fill most of two stages
     ga.gp = reinterpret_cast<int32_t*>(ws + fl.gp);
     ga.seq_prefix = reinterpret_cast<int32_t*>(ws + fl.seq_prefix);
     ga.seq_ctx = seq_ctx;
@@ -2480,6 +2718,7 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
   Params prm = make_params(seq_ctx, num_seqs, num_q_heads, num_kv_heads, head_dim,
                            max_blocks_per_seq, workspace, fl.dec, status);
   prm.seq_prefix = reinterpret_cast<const int32_t*>(ws + fl.seq_prefix);
+  prm.ws.mqueue = reinterpret_cast<int*>(ws + fl.mqueue);
   prm.verify_prefix = group_start == nullptr;
   prm.signature = signature;
   prm.q = q;
@@ -2502,26 +2741,6 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
     rc = head_dim == 128 ? launch_tc<__half, 128, 8, 2>(prm, kc2, st.sms, s)
                          : launch_tc<__half, 64, 8, 2>(prm, kc2, st.sms, s);
   if (rc != PA_OK) return rc;
-  // the merges, one warp per (sequence, KV head)
-  const long long pairs = (long long)num_seqs * num_kv_heads;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(std::min<long long>((pairs + 7) / 8, (long long)st.sms * 8)));
-  cfg.blockDim = dim3(256);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (dtype == PA_BF16)
-    e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 128>, prm)
-                        : cudaLaunchKernelEx(&cfg, merge_kernel<__nv_bfloat16, 64>, prm);
-  else
-    e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<__half, 128>, prm)
-                        : cudaLaunchKernelEx(&cfg, merge_kernel<__half, 64>, prm);
-  if (e != cudaSuccess)
-    return fail(PA_ERR_CUDA, "%s: merge launch failed: %s", who, cudaGetErrorString(e));
   return PA_OK;
 }
 

@@ -21,6 +21,16 @@ constexpr int kHdrNext = 0;       // next work item (self-resetting)
 constexpr int kHdrTotal = 1;      // number of work items (written by the plan)
 constexpr int kHdrDone = 2;       // warps that have taken their last item (self-resetting)
 constexpr int kHdrSignature = 3;  // shape signature written by the plan
+// grouped decode: its merges go through a queue in the attention launch
+constexpr int kHdrQHead = 4;      // next queue entry to take (self-resetting)
+constexpr int kHdrQTail = 5;      // next queue entry to fill (self-resetting)
+constexpr int kHdrQDone = 6;      // warps done with the queue (self-resetting)
+constexpr int kHdrMerges = 7;     // merges the run will queue (written by the plan)
+// grouped decode: kTeamWarps when the plan placed its units in teams (the
+// splits of one (chunk, KV head) on kTeamWarps warps of one CTA, merged in
+// shared memory), else 0 (merges through the queue)
+constexpr int kHdrTeam = 8;
+constexpr int kTeamWarps = 4;
 
 // Views into the caller's workspace (all offsets 256-byte aligned).
 struct Workspace {
@@ -33,6 +43,9 @@ struct Workspace {
   int* nsplits;      // [num_seqs] splits the plan made of each sequence
   float* part_lse;   // [num_seqs][max_splits][num_q_heads]  (log2 domain)
   float* part_o;     // [num_seqs][max_splits][num_q_heads][head_dim]
+  // grouped decode only (else null): [num_seqs * num_kv_heads] queue of
+  // merges, entry i = 1 + (b * num_kv_heads + g) once (b, g) is ready, 0 before
+  int* mqueue;
 };
 
 struct Layout {
@@ -70,7 +83,7 @@ inline bool layout_too_large(int num_seqs, int num_q_heads, int num_kv_heads, in
   const double units = double(num_seqs) * (splits < 1.0 ? 1.0 : splits);
   const double rows = double(num_seqs) * num_q_heads;
   const double bytes = units * (16.0 + num_q_heads * (head_dim + 1.0) * 4.0) +
-                       double(num_seqs) * (num_kv_heads + 2.0) * 4.0 +
+                       double(num_seqs) * (2.0 * num_kv_heads + 2.0) * 4.0 +
                        double(num_seqs) * max_blocks_per_seq * 4.0 +
                        16.0 * rows * (head_dim + 1.0) * 4.0 + 65536.0;
   return bytes > double(uint64_t(1) << 50);

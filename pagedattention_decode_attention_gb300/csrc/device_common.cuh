@@ -51,6 +51,38 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// Store with release semantics at GPU scope: whoever acquires the value also
+// sees the caller's earlier writes (and those it acquired).
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Waits until *p is nonzero (acquire) and returns it.  Gives up after
+// `limit_ns` nanoseconds, sets the timeout bit of the status word and returns
+// 0.  It sleeps between polls, so a waiting warp takes few issue slots from
+// the warps of its SM that still work.
+__device__ __forceinline__ int wait_nonzero_bounded(const int* p, uint64_t limit_ns,
+                                                    unsigned* status) {
+  int v = ld_acquire_gpu(p);
+  if (v != 0) return v;
+  const uint64_t start = global_timer_ns();
+  for (;;) {
+    __nanosleep(128);
+    v = ld_acquire_gpu(p);
+    if (v != 0) return v;
+    if (global_timer_ns() - start > limit_ns) {
+      flag_status(status, kStatusTimeout);
+      return 0;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
