@@ -1304,7 +1304,8 @@ __global__ void __launch_bounds__(W * 32)
 
   // ---- issue cursor: blocks of `cur`, then of `nxt` once it is complete
   int cur_issued = 0, nxt_issued = 0;
-  int ik = 0;  // blocks issued into the ring so far
+  int ik = 0;   // blocks issued into the ring so far
+  int ist = 0;  // ik % NS (kept as a count: NS is a launch value)
   const uint64_t policy = dev::l2_policy_evict_first();
   auto top_up = [&](int kc) {
     while (ik < kc + NS) {
@@ -1313,7 +1314,8 @@ __global__ void __launch_bounds__(W * 32)
       const int j = from_cur ? cur_issued++ : nxt_issued++;
       const int phys = __shfl_sync(0xffffffffu, from_cur ? cur.phys : nxt.phys, j);
       const int gg = from_cur ? cur.g : nxt.g;
-      const int st = ik % NS;
+      const int st = ist;
+      if (++ist == NS) ist = 0;
       if (lane == 0) dev::mbar_arrive_expect_tx(&my_full[st], S::kStageBytes);
       __syncwarp();
       // lanes 0..HALVES-1 each issue one 128-byte-wide box of the K tile,
@@ -1327,7 +1329,8 @@ __global__ void __launch_bounds__(W * 32)
       ++ik;
     }
   };
-  int kc = 0;  // blocks consumed so far
+  int kc = 0;            // blocks consumed so far
+  int cst = 0, cph = 0;  // kc % NS and (kc / NS) & 1: the stage and phase to wait for
   // On a timeout: let this warp's copies in flight land, then give up.
   auto drain = [&]() {
     if (lane == 0) {
@@ -1430,10 +1433,10 @@ __global__ void __launch_bounds__(W * 32)
     int seen = -1;
 
     for (int j = 0; j < nblk; ++j) {
-      const int st = kc % NS;
+      const int st = cst;
       if (NT == 1 && j == nblk - 1 && nsplit > 1 && lane == 0)
         seen = dev::ld_relaxed_gpu(&p.ws.arrivals[size_t(b) * Hkv + g]);
-      if (!mbar_wait_bounded(&my_full[st], (kc / NS) & 1, tmo, p.status)) {
+      if (!mbar_wait_bounded(&my_full[st], cph, tmo, p.status)) {
         drain();
         return;
       }
@@ -1592,6 +1595,10 @@ __global__ void __launch_bounds__(W * 32)
       dev::fence_proxy_async_smem();
       __syncwarp();
       ++kc;
+      if (++cst == NS) {
+        cst = 0;
+        cph ^= 1;
+      }
       advance();
       if (cstage == 0 && nblk - cur_issued <= kLead) request();
       top_up(kc);
