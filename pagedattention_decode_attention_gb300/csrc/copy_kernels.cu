@@ -38,31 +38,38 @@ struct StatusSlot {
 };
 StatusSlot g_slots[kMaxDevices];
 
+// Token t's rows (heads_vecs 16-byte chunks: head h, chunk c of a row of
+// 1 << row_shift) go to slot_mapping[t].  Threads (x, y) of a CTA: y picks a
+// token, x walks its row, so no thread divides a flat index (the division
+// by the row length, 64-bit, used to cost as much issue time as the copy).
 __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                                  uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                 const int64_t* __restrict__ slots, int64_t total_vecs,
-                                 int heads_vecs, int row_vecs, int64_t num_slots,
+                                 const int64_t* __restrict__ slots, int num_tokens,
+                                 int heads_vecs, int row_shift, int64_t num_slots,
                                  unsigned* status) {
   // Let the next kernel of the stream start its prologue now; touch memory only
   // once the kernel before this one has finished.
   dev::grid_launch_dependents();
   dev::grid_dependency_wait();
-  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t t = i / heads_vecs;
-    const int rem = int(i - t * heads_vecs);
-    const int h = rem / row_vecs, c = rem - h * row_vecs;
+  const int row_mask = (1 << row_shift) - 1;
+  const int64_t num_heads = heads_vecs >> row_shift;
+  for (int t = blockIdx.x * blockDim.y + threadIdx.y; t < num_tokens;
+       t += gridDim.x * blockDim.y) {
     const int64_t slot = slots[t];
     if (slot < 0) continue;  // padding token
     if (slot >= num_slots) {
-      dev::flag_status(status, kStatusBounds);
+      if (threadIdx.x == 0) dev::flag_status(status, kStatusBounds);
       continue;
     }
     const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-    const int64_t num_heads = heads_vecs / row_vecs;
-    const int64_t dst = ((blk * num_heads + h) * kBlockSize + off) * row_vecs + c;
-    k_cache[dst] = k[i];
-    v_cache[dst] = v[i];
+    const uint4* kr = k + int64_t(t) * heads_vecs;
+    const uint4* vr = v + int64_t(t) * heads_vecs;
+    for (int j = threadIdx.x; j < heads_vecs; j += blockDim.x) {
+      const int h = j >> row_shift, c = j & row_mask;
+      const int64_t dst = (((blk * num_heads + h) * kBlockSize + off) << row_shift) + c;
+      k_cache[dst] = kr[j];
+      v_cache[dst] = vr[j];
+    }
   }
 }
 
@@ -183,15 +190,16 @@ PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cac
     return fail(PA_ERR_INVALID_ARG, "kv_append: tensors must be 16-byte aligned");
   unsigned* status = device_status_word();
   if (!status) return PA_ERR_CUDA;
-  const int row_vecs = head_dim * elem_bytes(dtype) / 16;
+  const int row_vecs = head_dim * elem_bytes(dtype) / 16;  // 8, 16 or 32
+  const int row_shift = row_vecs == 8 ? 3 : (row_vecs == 16 ? 4 : 5);
   const int heads_vecs = num_kv_heads * row_vecs;
-  const int64_t total = int64_t(num_tokens) * heads_vecs;
-  const int threads = 256;
-  const int64_t want = (total + threads - 1) / threads;
+  // 256 threads: x over a token's row, y over tokens
+  const int tx = heads_vecs < 256 ? heads_vecs : 256, ty = 256 / tx;
+  const int64_t want = (int64_t(num_tokens) + ty - 1) / ty;
   const int blocks = int(want < 65535 * 16 ? want : 65535 * 16);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(threads);
+  cfg.blockDim = dim3(tx, ty);
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -200,8 +208,9 @@ PA_API int pa_kv_append(const void* k, const void* v, void* k_cache, void* v_cac
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<const uint4*>(k),
                                      static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
-                                     static_cast<uint4*>(v_cache), slot_mapping, total, heads_vecs,
-                                     row_vecs, int64_t(num_blocks) * kBlockSize, status);
+                                     static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
+                                     heads_vecs, row_shift, int64_t(num_blocks) * kBlockSize,
+                                     status);
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, "kv_append: launch failed: %s", cudaGetErrorString(e));
   return PA_OK;
 }

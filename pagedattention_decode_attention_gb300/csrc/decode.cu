@@ -301,6 +301,8 @@ struct GroupArgs {
   int chunk;                    // most members of one shared unit
   int nwarps;                   // math warps of the attention launch
   int teams;                    // the attention launch can merge in teams (rings of >= 2 stages)
+  int small;                    // the per-sequence and per-group arrays fit the plan's
+                                //   shared memory (kGroupedPlanSmallSeqs; see grouped_plan_smem)
   int32_t* gp;                  // workspace [num_groups]: shared blocks that passed the checks
   int32_t* seq_prefix;          // workspace [num_seqs]: each sequence's shared blocks
   int32_t* seq_ctx;             // workspace [num_seqs]: context lengths, clamped
@@ -391,17 +393,45 @@ __device__ __forceinline__ ChunkPlan plan_chunk(const GroupArgs& ga, int b0, int
 }
 
 constexpr int kGroupedPlanThreads = 512;
+// A batch of at most this many sequences and groups keeps the plan's
+// per-sequence and per-group arrays in shared memory: every pass of the plan
+// reads what the last one wrote, and from L2 those reads made the plan a
+// chain of round trips (20 us per step on the 128-branch sampling batch).
+constexpr int kGroupedPlanSmallSeqs = 1024;
+inline size_t grouped_plan_smem(int num_seqs, int num_groups) {
+  return size_t(num_seqs) * (16 + 8 + 3 * 4) + size_t(2 * num_groups + 1) * 4;
+}
 
 __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const Params p,
-                                                                           const GroupArgs ga) {
+                                                                           const GroupArgs gin) {
   constexpr int NT = kGroupedPlanThreads;
   __shared__ int hist[kSplitBlocks + 2];
   __shared__ int bucket[kSplitBlocks + 2];
   __shared__ int cut_s, bad_s, sp_s, merges_s, team_s, chunks_s, chunk_ctr;
   __shared__ unsigned long long work_s;
+  extern __shared__ __align__(16) unsigned char plan_arrays[];
   dev::grid_launch_dependents();
   dev::grid_dependency_wait();  // the previous kernel may still read the workspace
   const int tid = threadIdx.x;
+  // the arrays the passes share: in shared memory for a small batch (the
+  // run's seq_ctx and seq_prefix are copied out at the end), else in the
+  // workspace
+  GroupArgs ga = gin;
+  if (gin.small) {
+    const int B = p.num_seqs, G = gin.group_start ? gin.num_groups : 1;
+    ga.chunk_plan = reinterpret_cast<int4*>(plan_arrays);
+    ga.seq_chunk = reinterpret_cast<int2*>(ga.chunk_plan + B);
+    ga.seq_ctx = reinterpret_cast<int32_t*>(ga.seq_chunk + B);
+    ga.seq_group = ga.seq_ctx + B;
+    ga.seq_prefix = ga.seq_group + B;
+    ga.gp = ga.seq_prefix + B;
+    if (gin.group_start) {
+      int32_t* starts = ga.gp + G;
+      for (int g = tid; g <= G; g += NT) starts[g] = gin.group_start[g];
+      ga.group_start = starts;
+    }
+    __syncthreads();
+  }
   const int ng = ga.group_start ? ga.num_groups : 1;
   const int cap = p.max_blocks * kBlockSize;
   const int mb = p.max_blocks;
@@ -452,25 +482,38 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   // Every member's context must cover the shared blocks and its table must
   // start with the first member's entries; a group with a member that does
   // not keeps no shared blocks (its members then decode on their own, which
-  // gives the same attention).  One thread per sequence, its entries' loads
-  // all in flight at once; a plan of one shared prefix gets no tables (the
-  // run checks them).
+  // gives the same attention).  The contexts one thread per sequence; the
+  // tables eight entries per thread over all (member, entry) pairs, so that
+  // every load is in flight at once.  A plan of one shared prefix gets no
+  // tables (the run checks them).
   for (int b = tid; b < p.num_seqs && !bad; b += NT) {
     const int g = ga.seq_group[b];
     const int nb = ga.gp[g];
-    if (nb == 0) continue;
     const int ctx = p.context_lens[b];
-    bool differ = ctx < nb * kBlockSize || ctx > cap;
-    const int first = ga.group_start ? ga.group_start[g] : 0;
-    if (p.block_tables && b != first) {
-      const int32_t* row = p.block_tables + size_t(b) * mb;
-      const int32_t* lead = p.block_tables + size_t(first) * mb;
-#pragma unroll 8
-      for (int j = 0; j < nb; ++j) differ |= __ldg(row + j) != __ldg(lead + j);
-    }
-    if (differ) {
+    if (nb > 0 && (ctx < nb * kBlockSize || ctx > cap)) {
       atomicExch(&ga.gp[g], 0);
       dev::flag_status(p.status, kStatusBounds);
+    }
+  }
+  if (!bad && p.block_tables) {
+    const int per_seq = (mb + 7) / 8;
+    const long long items = (long long)p.num_seqs * per_seq;
+    for (long long i = tid; i < items; i += NT) {
+      const int b = int(i / per_seq), j0 = int(i - (long long)b * per_seq) * 8;
+      const int g = ga.seq_group[b];
+      const int nb = ga.gp[g];
+      const int first = ga.group_start ? ga.group_start[g] : 0;
+      if (j0 >= nb || b == first) continue;
+      const int32_t* row = p.block_tables + size_t(b) * mb;
+      const int32_t* lead = p.block_tables + size_t(first) * mb;
+      bool differ = false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (j0 + k < nb) differ |= __ldg(row + j0 + k) != __ldg(lead + j0 + k);
+      if (differ) {
+        atomicExch(&ga.gp[g], 0);
+        dev::flag_status(p.status, kStatusBounds);
+      }
     }
   }
   __syncthreads();
@@ -701,6 +744,13 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
     }
     if (team)
       for (int s = c.z; s < kTeamWarps; ++s) units[place + s] = make_int4(-1, 0, 0, 0);
+  }
+  if (gin.small) {
+    // what the run reads: the clamped contexts and every sequence's shared blocks
+    for (int b = tid; b < p.num_seqs; b += NT) {
+      gin.seq_ctx[b] = ga.seq_ctx[b];
+      gin.seq_prefix[b] = ga.seq_prefix[b];
+    }
   }
 }
 
@@ -2702,6 +2752,7 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
     ga.chunk = 16 / (num_q_heads / num_kv_heads);
     ga.nwarps = nwarps;
     ga.teams = kc2.stages >= 2;  // a split's results fill most of two stages
+    ga.small = num_seqs <= kGroupedPlanSmallSeqs && ga.num_groups <= kGroupedPlanSmallSeqs;
     ga.gp = reinterpret_cast<int32_t*>(ws + fl.gp);
     ga.seq_prefix = reinterpret_cast<int32_t*>(ws + fl.seq_prefix);
     ga.seq_ctx = seq_ctx;
@@ -2711,6 +2762,7 @@ int fused_cascade_impl(SharedMode mode, const void* q, const void* k_cache, cons
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
     cfg.blockDim = dim3(kGroupedPlanThreads);
+    cfg.dynamicSmemBytes = ga.small ? grouped_plan_smem(num_seqs, ga.num_groups) : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
