@@ -519,7 +519,9 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
   __syncthreads();
   // per sequence: its shared blocks and chunk (first member, members); the
   // work (blocks per KV head) of the own blocks and of every chunk's shared
-  // blocks, which sizes the shared splits
+  // blocks, which sizes the shared splits (summed per thread, then per warp:
+  // one 64-bit shared atomic per sequence, all on one word, took 6 us)
+  unsigned long long work = 0;
   for (int b = tid; b < p.num_seqs; b += NT) {
     const int g = ga.seq_group[b];
     const int nb = bad ? 0 : ga.gp[g];
@@ -531,8 +533,11 @@ __global__ void __launch_bounds__(kGroupedPlanThreads) grouped_plan_kernel(const
     ga.seq_chunk[b] = make_int2(b0, m);
     unsigned long long w = (ga.seq_ctx[b] + kBlockSize - 1) / kBlockSize - nb;
     if (b == b0) w += nb;  // the chunk's shared blocks, read once
-    atomicAdd(&work_s, w);
+    work += w;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) work += __shfl_down_sync(0xffffffffu, work, o);
+  if ((tid & 31) == 0 && work) atomicAdd(&work_s, work);
   __syncthreads();
   if (tid == 0) {
     // shared splits of about the work one math warp gets, 16 to 32 blocks
