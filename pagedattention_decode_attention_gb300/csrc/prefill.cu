@@ -37,6 +37,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <type_traits>
 
@@ -109,6 +110,9 @@ struct Params {
   int defer_merge;
   float* cas_o;      // [total_q * num_q_heads][head_dim]
   float* cas_lse;    // [total_q * num_q_heads]
+  // tcgen05 kernel: whole warps of output rows go out through the tensor
+  // map of out (tensor-copy stores from shared memory), else thread by thread
+  int out_tma;
   float scale, scale_log2;
   int* header;
   int4* units;       // 2 x int4 per unit (see plan)
@@ -845,20 +849,57 @@ constexpr int kTcRegsSoftmax = 224, kTcRegsProducer = 56;
 constexpr uint32_t kTcCols = 512;  // TMEM columns: S_0, S_1, O_0, O_1
 constexpr float kTcRescale = 8.f;  // log2 of the growth that forces an O rescale
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// Tensor-copy store of one box from shared memory (x: element column, a
+// multiple of 8 here; y: head; z: token), completed through bulk groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int x, int y,
+                                             int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The shared memory of every committed store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 struct TcSmem {  // head_dim 128, 16-bit: every chunk is [128 rows][128 bytes]
   static constexpr int kChunk = kTcRows * 128;  // 16 KB
   static constexpr int kQ = 0;                  // [2 tiles][2 chunks (d 0-63, 64-127)]
   static constexpr int kK = 4 * kChunk;         // [2 stages][2 chunks]
   static constexpr int kV = kK + 4 * kChunk;    // [2 stages][2 chunks]
   static constexpr int kBars = kV + 4 * kChunk; // mbarriers, item slots
-  static constexpr int kBytes = kBars + 256 + 1024;  // + alignment slack
+  // per softmax warp: 32 output rows x 64 elements staged for a store
+  static constexpr int kOutWarp = 32 * 128;
+  static constexpr int kOut = kBars + 1024;
+  static constexpr int kBytes = kOut + 8 * kOutWarp + 1024;  // + alignment slack
 };
+static_assert(TcSmem::kBytes <= 227 * 1024, "tcgen05 prefill shared memory");
 
 template <typename T>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmap_q,
                       const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+                      const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ CUtensorMap tmap_o, const Params p) {
   constexpr int D = 128;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   using M = dev::Mma<T>;
@@ -913,6 +954,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     dev::mbar_init(&sb_full[1], 1);
     dev::mbar_fence_init();
     dev::prefetch_tensormap(&tmap_q);
+    if (p.out_tma) dev::prefetch_tensormap(&tmap_o);
     dev::prefetch_tensormap(&tmap_k);
     dev::prefetch_tensormap(&tmap_v);
   }
@@ -1484,6 +1526,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             dev::st_global_v8(crow + 32 * c + 8 * i, f);
           }
         p.cas_lse[size_t(it.s) * rows + hrow] = l > 0.f ? mref + log2f(l) : -INFINITY;
+      } else if (p.out_tma && __all_sync(0xffffffffu, valid)) {
+        // The warp's 32 rows are 32 / G tokens x the G heads of the group:
+        // one box of the output's tensor map per 64 columns.  Each row goes
+        // to shared memory in the box's 128-byte-swizzled layout (so the 32
+        // rows' 16-byte stores spread over every bank), then one lane stores
+        // the box; the staging buffer is reused once the previous store has
+        // read it.
+        const uint32_t stage = sbase + TcSmem::kOut + warp * TcSmem::kOutWarp;
+        const int tok0 = it.q_first + (gr - lane) / G;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t* x = &ov[2 * h + (k >> 2)][8 * (k & 3)];
+            st_shared_v4(stage + lane * 128 + ((k ^ (lane & 7)) << 4),
+                         M::pack(__uint_as_float(x[0]) * inv, __uint_as_float(x[1]) * inv),
+                         M::pack(__uint_as_float(x[2]) * inv, __uint_as_float(x[3]) * inv),
+                         M::pack(__uint_as_float(x[4]) * inv, __uint_as_float(x[5]) * inv),
+                         M::pack(__uint_as_float(x[6]) * inv, __uint_as_float(x[7]) * inv));
+          }
+          dev::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmap_o, stage, h * 64, it.g * G, tok0);
+            bulk_commit_group();
+          }
+        }
       } else if (valid) {
         T* orow = static_cast<T*>(p.out) +
                   (size_t(it.q_first + gr / G) * Hq + it.g * G + gr % G) * D;
@@ -1511,6 +1582,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       dev::tc_fence_before_sync();
       PF_ADD(4, pf_epi);
     }
+    if (p.out_tma && lane == 0) bulk_wait_all();  // the output stores have landed
     PF_STORE(8 + 8 * w, r == 0);
   }
   PF_STAMP(2);
@@ -1919,10 +1991,11 @@ int launch_plan(const Params& prm, bool use_tc, cudaStream_t s, const char* who)
 }
 
 // The attention kernel over a planned workspace.
-int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, const char* who) {
+int launch_attention(const Params& prm_in, bool use_tc, int dtype, cudaStream_t s, const char* who) {
   const bool bf16 = dtype == PA_BF16;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  alignas(64) CUtensorMap mq, mk, mv;
+  alignas(64) CUtensorMap mq, mk, mv, mo;
+  Params prm = prm_in;
   int rc = cache_tensor_map(&mk, prm.k_cache, bf16, prm.num_blocks, prm.num_kv_heads, prm.head_dim);
   if (rc == PA_OK)
     rc = cache_tensor_map(&mv, prm.v_cache, bf16, prm.num_blocks, prm.num_kv_heads, prm.head_dim);
@@ -1932,6 +2005,16 @@ int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, 
     rc = query_tensor_map(&mq, prm.q, bf16, prm.total_q, prm.num_q_heads, prm.head_dim,
                           prm.num_q_heads / prm.num_kv_heads, kTcRows);
     if (rc != PA_OK) return rc;
+    // rows to out by tensor-copy stores: a warp's 32 rows at a time (the
+    // shared-prefix modes write fp32 parts instead)
+    std::memset(&mo, 0, sizeof(mo));
+    prm.out_tma = prm.out && prm.shared_ctx == 0 && !prm.shared_blocks &&
+                  (reinterpret_cast<uintptr_t>(prm.out) & 15) == 0;
+    if (prm.out_tma) {
+      rc = output_tensor_map(&mo, prm.out, bf16, prm.total_q, prm.num_q_heads, prm.head_dim,
+                             prm.num_q_heads / prm.num_kv_heads, 32);
+      if (rc != PA_OK) return rc;
+    }
     cudaLaunchConfig_t tc = {};
     tc.gridDim = dim3(prm.ncta);
     tc.blockDim = dim3(kTcThreads);
@@ -1939,8 +2022,8 @@ int launch_attention(const Params& prm, bool use_tc, int dtype, cudaStream_t s, 
     tc.stream = s;
     tc.attrs = attr;
     tc.numAttrs = 1;
-    e = bf16 ? cudaLaunchKernelEx(&tc, prefill_tc_kernel<__nv_bfloat16>, mq, mk, mv, prm)
-             : cudaLaunchKernelEx(&tc, prefill_tc_kernel<__half>, mq, mk, mv, prm);
+    e = bf16 ? cudaLaunchKernelEx(&tc, prefill_tc_kernel<__nv_bfloat16>, mq, mk, mv, mo, prm)
+             : cudaLaunchKernelEx(&tc, prefill_tc_kernel<__half>, mq, mk, mv, mo, prm);
   } else {
     cudaLaunchConfig_t kc = {};
     kc.gridDim = dim3(prm.ncta);

@@ -102,4 +102,21 @@ int query_tensor_map(CUtensorMap* out, const void* q, bool bf16, int total_q, in
   return PA_OK;
 }
 
+int output_tensor_map(CUtensorMap* out, void* o, bool bf16, int total_q, int num_q_heads,
+                      int head_dim, int group, int rows) {
+  int rc = get_encoder();
+  if (rc != PA_OK) return rc;
+  const cuuint64_t dims[3] = {cuuint64_t(head_dim), cuuint64_t(num_q_heads), cuuint64_t(total_q)};
+  const cuuint64_t strides[2] = {cuuint64_t(head_dim) * 2, cuuint64_t(num_q_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(rows / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = g_encode(out, dt, 3, o, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (%d)", int(r));
+  return PA_OK;
+}
+
 }  // namespace pa

@@ -24,4 +24,13 @@ int cache_tensor_map(CUtensorMap* out, const void* cache, bool bf16, int num_blo
 int query_tensor_map(CUtensorMap* out, const void* q, bool bf16, int total_q, int num_q_heads,
                      int head_dim, int group, int rows);
 
+// Encodes the 3-D tensor map of an output tensor `[total_q][num_q_heads]
+// [head_dim]` (16-bit) for stores whose box is 64 elements x `group` heads x
+// (rows / group) tokens with 128-byte swizzle: in shared memory the box's
+// `rows` rows of 128 bytes sit one after another (row = token * group + head
+// within the group), the 16-byte chunk c of row r at chunk c ^ (r % 8).
+// Returns a pa_status.
+int output_tensor_map(CUtensorMap* out, void* o, bool bf16, int total_q, int num_q_heads,
+                      int head_dim, int group, int rows);
+
 }  // namespace pa
