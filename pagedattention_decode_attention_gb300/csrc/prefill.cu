@@ -1398,10 +1398,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           // blocks are zeroed, so whatever bits they hold meet only p = 0
           if (!dev::mbar_wait_bounded(&v_full[kt & 1], (kt >> 1) & 1, tmo, p.status)) ok = false;
           if (ok && t0 + r >= bound) {
+            // (each row's 16-byte chunks in an order rotated by the row, so
+            // the warp's 32 rows, 128 bytes apart, do not all hit one bank)
             uint8_t* vrow = smem + TcSmem::kV + (kt & 1) * 2 * TcSmem::kChunk + r * 128;
+#pragma unroll
             for (int h = 0; h < 2; ++h)
+#pragma unroll
               for (int q16 = 0; q16 < 8; ++q16)
-                *reinterpret_cast<uint4*>(vrow + h * TcSmem::kChunk + q16 * 16) =
+                *reinterpret_cast<uint4*>(vrow + h * TcSmem::kChunk + ((q16 + r) & 7) * 16) =
                     make_uint4(0, 0, 0, 0);
           }
           dev::fence_proxy_async_smem();
