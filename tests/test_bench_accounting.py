@@ -44,3 +44,17 @@ def test_prefill_flops_by_hand():
     # a whole prompt (chunk = context) attends 1 + 2 + ... + n tokens
     b = batch([4], [[1]], hq=1, d=64, extra={"query_lens": np.array([4])})
     assert bench.prefill_flops(b) == (1 + 2 + 3 + 4) * 4 * 64
+
+
+def test_cascade_launch_counts(monkeypatch):
+    """The cascade lines' `gpu_launches`: the grouped decode is one plan and
+    one attention launch per layer (its merges run inside that launch); the
+    three phases are their plans and three launches per layer."""
+    import bench
+    monkeypatch.delenv("PA_CASCADE", raising=False)
+    assert bench.cascade_launches_per_step(True, 8) == 1 + 8        # groups: grouped decode
+    assert bench.cascade_launches_per_step(False, 32) == 2 + 3 * 32  # one prefix: phases
+    monkeypatch.setenv("PA_CASCADE", "phases")
+    assert bench.cascade_launches_per_step(True, 8) == 3 + 3 * 8
+    monkeypatch.setenv("PA_CASCADE", "grouped")
+    assert bench.cascade_launches_per_step(False, 32) == 1 + 32
