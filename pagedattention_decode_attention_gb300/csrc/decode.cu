@@ -1173,6 +1173,10 @@ __global__ void __launch_bounds__(W * 32)
   cur.patch = nxt.patch = false;
   long long cslot = -1;  // slot_mapping[b] of the item being claimed
   int cstage = 1;
+  // blocks of `nxt` whose physical block is known before its claim is
+  // complete (a shared unit's shared blocks, from its stage 5 on), so that
+  // their copies may start early
+  int nxt_known = 0;
   int cx = first_item(total, team);  // first item of every warp: dealt statically
   int4 cu = make_int4(0, 0, 0, 0);
   int q_issued = 0, q_taken = 0;  // query copies issued into / read from qbuf
@@ -1257,6 +1261,7 @@ __global__ void __launch_bounds__(W * 32)
       // kUnitOwn: after the shared blocks (they end at the group's shared
       // count P), member i's own blocks P .. ceil(ctx_i / 16) - 1, member
       // after member; lane j takes block j of that list
+      nxt_known = nxt.nblk;  // the shared blocks' entries came with the unit
       const int P = nxt.first + nxt.nblk;
       const int own = lane < nxt.m ? max(0, (octx + kBlockSize - 1) / kBlockSize - P) : 0;
       int off = own;  // inclusive sum over lanes 0 .. lane
@@ -1355,6 +1360,7 @@ __global__ void __launch_bounds__(W * 32)
   auto request = [&]() {  // starts the claim of the next item
     if (lane == 0) cx = nwarps + atomicAdd(&p.ws.header[kHdrNext], 1);
     cstage = 1;
+    nxt_known = 0;
   };
 
   // ---- issue cursor: blocks of `cur`, then of `nxt` once it is complete
@@ -1365,7 +1371,7 @@ __global__ void __launch_bounds__(W * 32)
   auto top_up = [&](int kc) {
     while (ik < kc + NS) {
       bool from_cur = cur_issued < cur.nblk;
-      if (!from_cur && !(cstage == 4 && nxt_issued < nxt.nblk)) break;
+      if (!from_cur && !(nxt_issued < (cstage == 4 ? nxt.nblk : nxt_known))) break;
       const int j = from_cur ? cur_issued++ : nxt_issued++;
       const int phys = __shfl_sync(0xffffffffu, from_cur ? cur.phys : nxt.phys, j);
       const int gg = from_cur ? cur.g : nxt.g;
@@ -1396,8 +1402,12 @@ __global__ void __launch_bounds__(W * 32)
     __syncwarp();
   };
 
-  // the first item, claimed in full before anything else
-  while (cstage != 4) advance();
+  // the first item, claimed in full before anything else (its blocks'
+  // copies start as soon as their entries are known)
+  while (cstage != 4) {
+    advance();
+    top_up(kc);
+  }
 #ifdef PA_PROFILE_TIMES
   int n_items = 0;
 #endif
@@ -1410,6 +1420,7 @@ __global__ void __launch_bounds__(W * 32)
     nxt.nblk = 0;
     cstage = 0;
     if (cur.b < 0) break;
+    nxt_known = 0;
 #ifdef PA_PROFILE_TIMES
     const unsigned long long item_t0 = dev::global_timer_ns();
 #endif
