@@ -1059,7 +1059,9 @@ __global__ void __launch_bounds__(W * 32)
     int hg = 0;
     const int u0 = unit_of(x0, team0, hg);
     if (x0 < total0 && x0 < cap && u0 < (long long)p.num_seqs * p.max_splits) {
-      const int4 u = reinterpret_cast<const int4*>(p.ws.units)[u0];
+      // (read through L2 only: a line left in L1 now could be stale for the
+      // claim's read of the same unit after the wait)
+      const int4 u = __ldcg(reinterpret_cast<const int4*>(p.ws.units) + u0);
       const int n = u.z & kUnitBlocks;
       const int kWarmBlocks = p.group == 1 ? 8 : 4;
       if (u.x >= 0 && u.x < p.num_seqs && u.y >= 0 && n >= 1 && n <= kSplitBlocks &&
@@ -1067,7 +1069,8 @@ __global__ void __launch_bounds__(W * 32)
         const int nb = n < kWarmBlocks ? n : kWarmBlocks;
         int phys = -1;
         if (lane < nb)
-          phys = p.block_tables[size_t(u.x) * p.max_blocks + p.table_offset + u.y + lane];
+          phys = __ldcg(p.block_tables + size_t(u.x) * p.max_blocks + p.table_offset + u.y +
+                        lane);
         for (int j = 0; j < nb; ++j) {
           const int pj = __shfl_sync(0xffffffffu, phys, j);
           if (pj < 0 || pj >= p.num_blocks) continue;
