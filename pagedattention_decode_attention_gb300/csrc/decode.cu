@@ -1891,6 +1891,7 @@ __global__ void __launch_bounds__(W * 32)
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(tbar, 0, tmo, p.status);
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      __syncwarp();  // every lane reads the team's rings after lane 0's acquire
       const int t = (warp / kTeamWarps) * int(gridDim.x) + int(blockIdx.x);
       const int j = warp % kTeamWarps;
       if (ok && t * kTeamWarps < total) {
