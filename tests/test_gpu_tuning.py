@@ -45,8 +45,8 @@ def test_cascade_implementations(gpu, impl):
     """The shared- and grouped-prefix entry points each on one cascade
     implementation (PA_CASCADE, read once per process): the three phases
     (prefix phase on the chunked-prefill kernels, suffix decode, combine) or
-    the grouped decode (one attention launch over shared and own units, one
-    merge launch).  By default the grouped entry points use the grouped
+    the grouped decode (one attention launch over shared and own units, which
+    also merges each sequence's splits).  By default the grouped entry points use the grouped
     decode and the single-prefix ones the phases; both pass the same tests."""
     env = dict(os.environ, PA_CASCADE=impl)
     r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", "-p",
