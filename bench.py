@@ -368,6 +368,15 @@ def profiled_traffic(workload: str):
     return _recorded_traffic(f"decode_{workload}", kernel_source_hash())
 
 
+def profiled_cascade_traffic(workload: str, grouped: bool):
+    """DRAM bytes per layer's attention launch of the grouped decode on a
+    cascade workload (current kernel source only; None for the three-phase
+    path, whose layer is three launches)."""
+    if not grouped or os.environ.get("PA_CASCADE", "") == "phases":
+        return None
+    return _recorded_traffic(f"grouped_decode_{workload}", kernel_source_hash())
+
+
 class ClockSampler:
     """SM clock and clock-event (throttle) reasons sampled during the timed
     region, read through NVML (ctypes on libnvidia-ml; reading only).  Falls
@@ -1032,7 +1041,8 @@ def measure_cascade(args, workload: str, device, cpu_seconds: float, layers: int
         "config": cascade_config(batch),
         "roofline": {"bound": "hbm", "achieved": uniq / (cascade_s / L) / 1e9, "peak": peak,
                      "unit": "GB/s", "frac": uniq / (cascade_s / L) / 1e9 / peak,
-                     "traffic": None, "peak_source": f"{peak_src} hbm_gbs",
+                     "traffic": profiled_cascade_traffic(workload, grouped),
+                     "peak_source": f"{peak_src} hbm_gbs",
                      "bytes_per_layer": uniq,
                      "bytes": "unique K/V (each physical block once: the prefix once, "
                               "every suffix once), q, out"},
